@@ -1,0 +1,183 @@
+/*
+ * flint_moe.h — C ABI of the Flint small-batch decode MoE layer for GB300 (sm_103a).
+ *
+ * The layer: hidden 2048, 256 routed experts scored by a sigmoid and selected
+ * top-6, plus one always-on shared expert; every expert is a SwiGLU FFN
+ * (gate/up projection, SiLU-and-mul, down projection).
+ *   - "256 routed experts with top-6 sigmoid routing plus one shared expert",
+ *     "Qwen3-MoE-style decoder": [Flint on Intel Arc Pro B70, "Setup"].
+ *   - "hidden size of 2048", "256 experts, sigmoid top-6 selection plus a
+ *     shared expert": [vLLM Day-0 Support for Recursive's Flint,
+ *     "Flint Model Architecture"].
+ *   - "router and expert GEMVs ... read only the selected experts' weights":
+ *     [vLLM Day-0 Support for Recursive's Flint, "Optimization Strategies",
+ *     "Small-batch MoE Kernels"].
+ *   - SiLU written as g / (1 + exp(-g)): [Flint on Intel Arc Pro B70,
+ *     "norm.py: Triton kernels that assumed CUDA"].
+ *   - NVFP4 weights run weight-only (W4A16) with BF16 activations:
+ *     [vLLM Day-0 Support for Recursive's Flint, "Flint Model Overview and
+ *     Capabilities"]; [RecursiveSI/flint — vLLM serving recipe, "Guide",
+ *     "Overview"].
+ * The intermediate (expert FFN) size is not given by the pages; this library
+ * is specialised to 512.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer, owned by the caller, and must be
+ *    16-byte aligned.  Tensors are dense and row-major in the shapes written
+ *    beside each argument.  bf16 tensors are passed as `const void*` holding
+ *    IEEE bfloat16 bit patterns.
+ *  - The library allocates no device or host memory and keeps no state between
+ *    calls.  Scratch lives in a caller-provided workspace (see
+ *    flint_moe_workspace_bytes / flint_moe_workspace_init).  Two calls may run
+ *    concurrently only with distinct workspaces.
+ *  - Calls validate their arguments on the host and return an error status
+ *    BEFORE any launch if anything is wrong; nothing is then written.  On
+ *    FLINT_OK, the work has been enqueued on `stream` and nothing has been
+ *    synchronised: results are visible after the caller's next sync on that
+ *    stream.  Launch failures reported by the runtime map to FLINT_ERR_CUDA.
+ *  - Every wait inside a kernel is bounded by a time limit stored in the
+ *    workspace.  A kernel that runs out of time records
+ *    FLINT_ERR_DEVICE_TIMEOUT in the workspace's error word, waits (bounded)
+ *    for its own asynchronous copies and returns; read the word with
+ *    flint_moe_get_device_status.  The outputs of such a call are undefined,
+ *    and the workspace must be re-initialised before the next call.
+ *  - Routing: logits are computed in fp32 from bf16 inputs.  Experts are
+ *    ranked by (logit descending, expert index ascending), the first top_k are
+ *    kept, and each kept expert's weight is sigmoid(logit) divided by the sum
+ *    of the kept sigmoids (so the weights sum to 1).  topk_idx rows list the
+ *    experts in that rank order.
+ */
+#ifndef FLINT_MOE_H_
+#define FLINT_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLINT_OK = 0,
+  FLINT_ERR_INVALID_ARG = 1,    /* NULL / misaligned pointer, bad batch, aliasing */
+  FLINT_ERR_UNSUPPORTED = 2,    /* dims other than the specialised shape */
+  FLINT_ERR_WORKSPACE = 3,      /* workspace NULL or smaller than required */
+  FLINT_ERR_CUDA = 4,           /* the CUDA runtime reported an error */
+  FLINT_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait ran out */
+} flint_status;
+
+/* Layer shape.  Supported: hidden 2048, n_experts 256, top_k 6, inter 512,
+ * n_shared 1.  Any other value returns FLINT_ERR_UNSUPPORTED. */
+typedef struct {
+  int32_t hidden;     /* H */
+  int32_t n_experts;  /* E, routed experts */
+  int32_t top_k;      /* k, experts selected per token */
+  int32_t inter;      /* I, expert intermediate size */
+  int32_t n_shared;   /* S, always-on shared experts (added with weight 1) */
+} flint_moe_dims;
+
+/* Largest batch (tokens per call) any entry point accepts. */
+#define FLINT_MOE_MAX_BATCH 256
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* flint_status_string(flint_status status);
+
+/* Bytes of workspace a call with `max_batch` tokens needs (0 if the dims are
+ * unsupported or max_batch is outside [1, FLINT_MOE_MAX_BATCH]).  One
+ * workspace sized for max_batch serves every call with batch <= max_batch. */
+size_t flint_moe_workspace_bytes(const flint_moe_dims* dims, int32_t max_batch);
+
+/* Prepares a workspace for use: zero-fills it (cudaMemsetAsync on `stream`)
+ * and stores the device-side wait limit.  wait_limit_ns = 0 selects the
+ * default limit of one second.  Must be called once before the first call
+ * that uses the workspace, and again after any call whose device status was
+ * not FLINT_OK.  Every successful call leaves the workspace ready for the
+ * next one. */
+flint_status flint_moe_workspace_init(void* workspace, size_t ws_bytes,
+                                      uint64_t wait_limit_ns, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and returns the workspace's device error
+ * word (FLINT_OK or FLINT_ERR_DEVICE_TIMEOUT). */
+flint_status flint_moe_get_device_status(const void* workspace, cudaStream_t stream);
+
+/* Router only: logits, sigmoid top-k, renormalised weights.
+ *   x_bf16        [batch, H]   token activations (already normalised)
+ *   w_router_bf16 [E, H]       router matrix
+ *   logit_bias    [E] fp32 or NULL; added to every logit before ranking and
+ *                 before the sigmoid (so it moves both selection and weights)
+ *   topk_idx      [batch, k]   int32 out, expert ids in rank order
+ *   topk_w        [batch, k]   fp32 out, renormalised weights
+ * Router matrix and logits follow "sigmoid top-6" routing:
+ * [vLLM Day-0 Support for Recursive's Flint, "Flint Model Architecture"]. */
+flint_status flint_moe_route(const flint_moe_dims* dims, int32_t batch,
+                             const void* x_bf16, const void* w_router_bf16,
+                             const float* logit_bias,
+                             int32_t* topk_idx, float* topk_w,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* The whole BF16 decode MoE layer:
+ *   out[t] = residual[t] + sum_s FFN_shared_s(x[t])
+ *                        + sum_{j<k} topk_w[t,j] * FFN_{topk_idx[t,j]}(x[t])
+ *   FFN_e(v) = Wd_e ( silu(Wg_e v) * (Wu_e v) ),  silu(g) = g / (1 + exp(-g))
+ * Only the selected experts' weights, the shared expert and the router are
+ * read ("read only the selected experts' weights":
+ * [vLLM Day-0 Support for Recursive's Flint, "Optimization Strategies"]).
+ *   x_bf16, residual_bf16 [batch, H]
+ *   w_router_bf16 [E, H]; logit_bias [E] fp32 or NULL (as flint_moe_route)
+ *   w13_bf16  [E, 2I, H]   rows 0..I-1 are Wg, rows I..2I-1 are Wu
+ *   w2_bf16   [E, H, I]    Wd
+ *   ws13_bf16 [S, 2I, H], ws2_bf16 [S, H, I]  shared expert(s), same layout
+ *   out_bf16  [batch, H]   out; may alias residual_bf16 exactly (in-place
+ *                          residual add); no other overlap is allowed
+ *   topk_idx_out [batch, k] int32, topk_w_out [batch, k] fp32: optional
+ *                          copies of the routing (NULL to skip)
+ * Accumulation is fp32; the SiLU-and-mul output is kept in fp32; `out` is
+ * rounded to bf16 once. */
+flint_status flint_moe_decode_bf16(const flint_moe_dims* dims, int32_t batch,
+                                   const void* x_bf16, const void* residual_bf16,
+                                   const void* w_router_bf16, const float* logit_bias,
+                                   const void* w13_bf16, const void* w2_bf16,
+                                   const void* ws13_bf16, const void* ws2_bf16,
+                                   void* out_bf16,
+                                   int32_t* topk_idx_out, float* topk_w_out,
+                                   void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* NVFP4 weight-only (W4A16) variant of flint_moe_decode_bf16.  The router,
+ * activations and output stay bf16.  Each expert projection is stored as
+ *   q   uint8 [rows, K/2]   e2m1 codes; byte j holds k = 2j in its low nibble
+ *                           and k = 2j+1 in its high nibble
+ *   sf  uint8 [rows, K/16]  OCP E4M3FN scale of each block of 16 consecutive k
+ *   ts  fp32                one tensor scale per (expert, projection)
+ * and dequantises to W[r,k] = e2m1(q) * e4m3(sf[r, k/16]) * ts.
+ *   w13_q [E, 2I, H/2], w13_sf [E, 2I, H/16], w13_ts [E, 2] (gate, up)
+ *   w2_q  [E, H, I/2],  w2_sf  [E, H, I/16],  w2_ts  [E]
+ *   ws13_q/ws13_sf/ws13_ts and ws2_q/ws2_sf/ws2_ts: the shared expert(s),
+ *   same layouts with S in place of E.
+ * NVFP4 with BF16 activations: [vLLM Day-0 Support for Recursive's Flint,
+ * "Flint Model Overview and Capabilities"]. */
+flint_status flint_moe_decode_nvfp4_w4a16(
+    const flint_moe_dims* dims, int32_t batch,
+    const void* x_bf16, const void* residual_bf16,
+    const void* w_router_bf16, const float* logit_bias,
+    const uint8_t* w13_q, const uint8_t* w13_sf, const float* w13_ts,
+    const uint8_t* w2_q, const uint8_t* w2_sf, const float* w2_ts,
+    const uint8_t* ws13_q, const uint8_t* ws13_sf, const float* ws13_ts,
+    const uint8_t* ws2_q, const uint8_t* ws2_sf, const float* ws2_ts,
+    void* out_bf16, int32_t* topk_idx_out, float* topk_w_out,
+    void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Pre-norm between stacked layers: out[t] = bf16( in[t] / sqrt(mean(in[t]^2) + eps) )
+ * (unit gain).  in_bf16 and out_bf16 are [batch, H] and must not overlap.
+ * Pre-norm decoder: [vLLM Day-0 Support for Recursive's Flint, "Flint Model
+ * Architecture"]. */
+flint_status flint_moe_rmsnorm_bf16(const flint_moe_dims* dims, int32_t batch,
+                                    const void* in_bf16, void* out_bf16, float eps,
+                                    cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLINT_MOE_H_ */
