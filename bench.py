@@ -1,0 +1,482 @@
+#!/usr/bin/env python
+"""Benchmark of the Flint decode MoE layer on one GB300 (or N replicas).
+
+Headline: one BF16 MoE decode layer (hidden 2048, 256 routed experts, sigmoid
+top-6 + 1 shared, intermediate 512) at batch 8 with i.i.d. unit-RMS tokens,
+timed as CUDA-graph replay with CUDA events, the L2 flushed (512 MiB write)
+between timed steps.  Metric: HBM GB/s over the bytes the layer needs --
+(U+1) experts x 6 MiB + the 1 MiB router, U = distinct selected experts -- and
+the layer latency in microseconds.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on the host instead (the comparison arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import flint_synth as fs  # noqa: E402
+
+METRIC = "MoE decode-layer µs and HBM GB/s (selected-expert bytes) at batch 1/8/32/128"
+EXPERT_BYTES_BF16 = 3 * 512 * 2048 * 2          # 6,291,456
+ROUTER_BYTES = 256 * 2048 * 2                   # 1,048,576
+EXPERT_BYTES_NVFP4 = 3 * 512 * 2048 // 2 + 3 * 512 * 2048 // 16   # 1,769,472 (+12 B of scales)
+GATEUP_BYTES_BF16 = 2 * 512 * 2048 * 2          # 4,194,304
+DOWN_BYTES_BF16 = 512 * 2048 * 2                # 2,097,152
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+LAYER_SEED, TOKEN_SEED, OFFSET_SEED = 1001, 2000, 1003
+
+
+def needed_bytes_bf16(U: int) -> int:
+    return (U + 1) * EXPERT_BYTES_BF16 + ROUTER_BYTES
+
+
+def needed_bytes_nvfp4(U: int) -> int:
+    return (U + 1) * (EXPERT_BYTES_NVFP4 + 12) + ROUTER_BYTES
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        sel = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = None
+        if sel is None:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            sel = vis.split(",")[device_index] if vis else str(device_index)
+        self.sel = sel
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.sel, "--query-gpu=" + self.FIELDS, "--format=csv",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.strip().split(",")]
+                if len(parts) < 9 or not parts[1].split()[0].isdigit():
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        sm = [int(r[1].split()[0]) for r in rows]
+        mx = [int(r[2].split()[0]) for r in rows if r[2].split()[0].isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(self.REASONS, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def stats_us(ms_list):
+    us = sorted(1000.0 * t for t in ms_list)
+    n = len(us)
+    return {"mean": sum(us) / n, "p10": us[int(0.1 * (n - 1))], "p50": us[int(0.5 * (n - 1))],
+            "p90": us[int(0.9 * (n - 1))]}
+
+
+class Flusher:
+    """Writes a buffer larger than L2 (cold-L2 timing between steps)."""
+
+    def __init__(self, device):
+        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.v = 0
+
+    def __call__(self):
+        self.v = (self.v + 1) & 0xFF
+        self.buf.fill_(self.v)
+
+
+def timed_steps(fn, steps, warmup, flush, stream, barrier=None, sampler=None):
+    """warmup untimed, then `steps` timed calls, each bracketed by CUDA events on
+    `stream`, L2 flushed before each call (outside the events)."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush()
+            fn()
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        t0 = time.perf_counter()
+        for s, e in ev:
+            flush()
+            s.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        clocks = sampler.stop() if sampler else None
+        if barrier:
+            barrier()
+    return [s.elapsed_time(e) for s, e in ev], wall, clocks
+
+
+class BF16Layer:
+    def __init__(self, m, W, B, bias_on, device, seed):
+        self.m, self.W, self.B = m, W, B
+        self.x, self.res = fs.tokens(seed, B, device=device)
+        self.bias = fs.logit_offsets(OFFSET_SEED, device=device) if bias_on else None
+        self.out = torch.empty_like(self.res)
+        self.idx = torch.empty((B, 6), dtype=torch.int32, device=device)
+        self.w = torch.empty((B, 6), dtype=torch.float32, device=device)
+        self.ws = m.new_workspace(B, device=device)
+        self.graph = None
+
+    def call(self, stream=None):
+        W = self.W
+        self.m.flint_moe_decode_bf16(self.x, self.res, W["wr"], self.bias, W["w13"], W["w2"],
+                                     W["ws13"], W["ws2"], self.out, self.ws, self.idx, self.w,
+                                     stream=stream)
+
+    def unique_experts(self) -> int:
+        self.call()
+        torch.cuda.synchronize()
+        st = self.m.flint_moe_get_device_status(self.ws)
+        if st != self.m.FLINT_OK:
+            raise RuntimeError("device status " + self.m.status_string(st))
+        return int(torch.unique(self.idx).numel())
+
+    def capture(self, stream):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            self.call(stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                self.call(stream)
+        self.graph = g
+        return g
+
+
+def measure_bf16(m, W, B, bias_on, seed, steps, warmup, flush, stream, barrier=None,
+                 sampler=None):
+    L = BF16Layer(m, W, B, bias_on, W["wr"].device, seed)
+    U = L.unique_experts()
+    g = L.capture(stream)
+    times, wall, clocks = timed_steps(g.replay, steps, warmup, flush, stream, barrier, sampler)
+    st = stats_us(times)
+    nb = needed_bytes_bf16(U)
+    return L, U, nb, times, st, wall, clocks
+
+
+def stage_times(m, L, steps, warmup, flush, stream):
+    """Per-kernel CUDA-event durations of the three kernels, each launched alone."""
+    W = L.W
+    idx = torch.empty_like(L.idx)
+    w = torch.empty_like(L.w)
+    out = torch.empty_like(L.res)
+    route = lambda: m.flint_moe_route(L.x, W["wr"], L.bias, idx, w, L.ws, stream=stream)  # noqa
+    gate = lambda: m.flint_moe_gateup_bf16(L.x, W["w13"], W["ws13"], L.ws, stream=stream)  # noqa
+    down = lambda: m.flint_moe_down_bf16(L.res, W["w2"], W["ws2"], out, L.ws, stream=stream)  # noqa
+    res = {}
+    for name, fn in (("router", route), ("gateup", gate), ("down", down)):
+        with torch.cuda.stream(stream):
+            route()
+            gate()
+        times, _, _ = timed_steps(fn, steps, warmup, flush, stream)
+        res[name] = stats_us(times)
+    torch.cuda.synchronize()
+    return res
+
+
+def e2e_measure(m, L, steps, warmup, flush, stream):
+    """Same layer through the public call with host buffers: pinned H2D of x and
+    residual, the decode call, D2H of out -- all inside the events."""
+    xh = L.x.cpu().pin_memory()
+    rh = L.res.cpu().pin_memory()
+    oh = torch.empty_like(L.out, device="cpu").pin_memory()
+
+    def step():
+        L.x.copy_(xh, non_blocking=True)
+        L.res.copy_(rh, non_blocking=True)
+        L.call(stream)
+        oh.copy_(L.out, non_blocking=True)
+
+    times, _, _ = timed_steps(step, steps, warmup, flush, stream)
+    return times, xh.numel() * 2 + rh.numel() * 2, oh.numel() * 2
+
+
+def cpu_baseline(L, W_host, budget_s=10.0):
+    import oracle
+    x = L.x.cpu()
+    res = L.res.cpu()
+    bias = None if L.bias is None else L.bias.cpu()
+    threads = oracle.max_threads()
+    reps, t_tot = 0, 0.0
+    while t_tot < budget_s and reps < 200:
+        t0 = time.perf_counter()
+        out, idx, _ = oracle.moe_bf16(fs.FULL, x, res, W_host["wr"], bias, W_host["w13"],
+                                      W_host["w2"], W_host["ws13"], W_host["ws2"], nthreads=threads)
+        t_tot += time.perf_counter() - t0
+        reps += 1
+    U = len(set(idx.reshape(-1).tolist()))
+    per = t_tot / reps
+    return {"value": needed_bytes_bf16(U) / per / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "us_per_layer": per * 1e6,
+            "sample": "fp64 C oracle (selected experts only) on the full batch-%d layer, %d "
+                      "repetitions, OpenMP over tokens" % (L.B, reps)}
+
+
+# ---------------------------------------------------------------- arms
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        barrier = dist.barrier
+    return world, rank, local, barrier
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, world, rank, local, barrier):
+    from moe_decode_sigmoid_gb300 import build
+    build.build()
+    import moe_decode_sigmoid_gb300 as m
+    m.lib()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    flush = Flusher(device)
+    peak, peak_kind = peaks()
+    B = args.batch
+    W = fs.layer_weights(LAYER_SEED, fs.FULL, device=device)
+    sampler = ClockSampler(local)
+    L, U, nb, times, st, wall, clocks = measure_bf16(
+        m, W, B, False, TOKEN_SEED + B, args.steps, args.warmup, flush, stream, barrier, sampler)
+    mean_ms = st["mean"] / 1000.0
+    t_max = max_over_ranks(mean_ms, world)
+    value = world * nb / (t_max / 1e3) / 1e9
+
+    roof_steps = min(args.steps, 400)
+    kern = stage_times(m, L, roof_steps, max(3, args.warmup // 4), flush, stream)
+    gate_bytes = (U + 1) * GATEUP_BYTES_BF16 + B * 2048 * 2 + 7 * B * 512 * 4
+    achieved = gate_bytes / (kern["gateup"]["mean"] * 1e-6) / 1e9
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "gateup_bf16_traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            with open(tr_path) as f:
+                tr = json.load(f)
+            if tr.get("batch") == B and tr.get("kernel_sha") == kernel_sha():
+                traffic = tr.get("traffic_bytes")
+        except Exception:
+            traffic = None
+
+    e2e_times, h2d, d2h = e2e_measure(m, L, min(args.steps, 1000), max(3, args.warmup // 4),
+                                      flush, stream)
+    e2e_mean = stats_us(e2e_times)["mean"]
+    e2e_t = max_over_ranks(e2e_mean, world)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "one BF16 Flint MoE decode layer, batch %d: hidden 2048, 256 routed "
+                        "experts sigmoid top-6 + 1 shared, intermediate 512, N(0,0.02) weights, "
+                        "unit-RMS N(0,1) tokens" % B,
+            "batch": B, "unique_experts": U, "needed_bytes": nb,
+            "l2": "flushed between timed steps (512 MiB write, outside the events)",
+            "timing": "CUDA-graph replay of the 3-kernel layer, CUDA events per step",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "us_per_layer": round(st["mean"], 3),
+        "us_p10_p50_p90": [round(st["p10"], 3), round(st["p50"], 3), round(st["p90"], 3)],
+        "frac_of_peak": round(nb / (st["mean"] * 1e-6) / 1e9 / peak, 4),
+        "peak_gbs": peak, "peak_kind": peak_kind,
+        "kernels_us": {k: round(v["mean"], 3) for k, v in kern.items()},
+        "roofline": {"bound": "hbm", "kernel": "gateup_bf16_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": gate_bytes,
+                     "note": "peak = %s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind},
+        "e2e": {"value": round(world * nb / (e2e_t * 1e-6) / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(e2e_t, 3), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 4),
+    }
+    if args.extras and rank == 0:
+        line["per_config"] = extras(m, W, flush, stream, args)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        W_host = {k: v.cpu() for k, v in W.items()}
+        line["cpu_baseline"] = cpu_baseline(L, W_host)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def extras(m, W, flush, stream, args):
+    """Secondary configurations (reported, not the headline)."""
+    out = {}
+    steps = max(50, min(args.steps, 500))
+    for B, bias_on in ((1, False), (8, False), (32, True), (128, True)):
+        L, U, nb, times, st, _, _ = measure_bf16(m, W, B, bias_on, TOKEN_SEED + B, steps,
+                                                 args.warmup, flush, stream)
+        out["bf16_b%d%s" % (B, "_skew" if bias_on else "")] = {
+            "us": round(st["mean"], 3), "p50_us": round(st["p50"], 3), "unique_experts": U,
+            "needed_bytes": nb, "gbs": round(nb / (st["mean"] * 1e-6) / 1e9, 1)}
+        del L
+    return out
+
+
+def kernel_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("gateup.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "moe_decode_sigmoid_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def run_reference(args, world, rank):
+    """The comparison arm: the fp64 CPU oracle on the host cores, same workload.
+    Each step is a bounded sample: one token of the batch-B layer (its six
+    routed experts, the shared expert and the router)."""
+    if rank != 0:
+        return
+    import oracle
+    B = args.batch
+    W = fs.layer_weights(LAYER_SEED, fs.FULL, device="cpu")
+    x, res = fs.tokens(TOKEN_SEED + B, B, device="cpu")
+    threads = oracle.max_threads()
+
+    def step(i):
+        t = i % B
+        out, idx, _ = oracle.moe_bf16(fs.FULL, x[t:t + 1], res[t:t + 1], W["wr"], None, W["w13"],
+                                      W["w2"], W["ws13"], W["ws2"], nthreads=1)
+        return idx
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    wall = time.perf_counter() - t0
+    per = wall / args.steps
+    nb = needed_bytes_bf16(6)   # one token: its 6 routed experts + shared + router
+    value = nb / per / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "one BF16 Flint MoE decode layer, batch %d (one token per step)"
+                               % B, "batch": B},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "one token of the batch-%d layer per step (fp64 C oracle, "
+                                   "selected experts only, single thread; host has %d threads)"
+                                   % (B, threads)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--batch", type=int, default=8)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--extras", action="store_true", default=True)
+    ap.add_argument("--no-extras", dest="extras", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local, barrier = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local, barrier)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -25,7 +25,7 @@ import torch
 
 __all__ = [
     "Dims", "FULL", "TINY", "layer_weights", "tokens", "logit_offsets",
-    "pack_nvfp4", "E2M1_VALUES",
+    "pack_nvfp4", "nvfp4_layer", "E2M1_VALUES",
 ]
 
 
@@ -158,3 +158,16 @@ def pack_nvfp4(w: torch.Tensor, row_split: int | None = None):
         q_codes[..., r0:r1, :] = _e2m1_codes(scaled).reshape(blk.shape)
     q = q_codes[..., 0::2] | (q_codes[..., 1::2] << 4)
     return q.contiguous(), sf.contiguous(), ts.contiguous()
+
+
+def nvfp4_layer(W: dict, dims: Dims = FULL) -> dict:
+    """The twelve packed NVFP4 tensors of a layer, from its bf16 weights:
+    w13_q/w13_sf/w13_ts (gate and up scaled separately), w2_q/w2_sf/w2_ts, and
+    the same for the shared expert(s) (ws13_*, ws2_*)."""
+    nv = {}
+    for pre, w13, w2 in (("w", W["w13"], W["w2"]), ("ws", W["ws13"], W["ws2"])):
+        q, sf, ts = pack_nvfp4(w13, row_split=dims.inter)
+        nv[pre + "13_q"], nv[pre + "13_sf"], nv[pre + "13_ts"] = q, sf, ts
+        q, sf, ts = pack_nvfp4(w2)
+        nv[pre + "2_q"], nv[pre + "2_sf"], nv[pre + "2_ts"] = q, sf, ts[..., 0].contiguous()
+    return nv

@@ -99,7 +99,8 @@ flint_status flint_moe_workspace_init(void* workspace, size_t ws_bytes,
                                       uint64_t wait_limit_ns, cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and returns the workspace's device error
- * word (FLINT_OK or FLINT_ERR_DEVICE_TIMEOUT). */
+ * word: FLINT_OK, FLINT_ERR_DEVICE_TIMEOUT, or FLINT_ERR_INVALID_ARG when
+ * flint_moe_bucket was given a routing row that is not k distinct experts. */
 flint_status flint_moe_get_device_status(const void* workspace, cudaStream_t stream);
 
 /* Router only: logits, sigmoid top-k, renormalised weights.
@@ -109,6 +110,8 @@ flint_status flint_moe_get_device_status(const void* workspace, cudaStream_t str
  *                 before the sigmoid (so it moves both selection and weights)
  *   topk_idx      [batch, k]   int32 out, expert ids in rank order
  *   topk_w        [batch, k]   fp32 out, renormalised weights
+ * Also leaves the token-to-expert buckets in the workspace for the stage
+ * calls below (flint_moe_gateup_bf16 / flint_moe_down_bf16).
  * Router matrix and logits follow "sigmoid top-6" routing:
  * [vLLM Day-0 Support for Recursive's Flint, "Flint Model Architecture"]. */
 flint_status flint_moe_route(const flint_moe_dims* dims, int32_t batch,
@@ -116,6 +119,25 @@ flint_status flint_moe_route(const flint_moe_dims* dims, int32_t batch,
                              const float* logit_bias,
                              int32_t* topk_idx, float* topk_w,
                              void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Token-to-expert bucketing alone: the dedup pass the decode calls run after
+ * routing, so that each selected expert's weights are read once per batch
+ * ("router and expert GEMVs ... read only the selected experts' weights":
+ * [vLLM Day-0 Support for Recursive's Flint, "Optimization Strategies"]).
+ *   topk_idx [batch, k] int32   device routing; every row must hold k distinct
+ *                               experts in [0, E) (otherwise the device error
+ *                               word becomes FLINT_ERR_INVALID_ARG and the
+ *                               outputs are undefined)
+ *   uniq     [E]   int32 out    distinct experts, ascending (first n_uniq valid)
+ *   offsets  [E+1] int32 out    first pair of each distinct expert; entry n_uniq
+ *                               holds batch*k
+ *   pairs    [batch*k] int32 out  token*8 + slot, ordered by (expert, token)
+ *   n_uniq   [1]   int32 out
+ * Uses (and leaves ready) the workspace like the other calls. */
+flint_status flint_moe_bucket(const flint_moe_dims* dims, int32_t batch,
+                              const int32_t* topk_idx, int32_t* uniq, int32_t* offsets,
+                              int32_t* pairs, int32_t* n_uniq,
+                              void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* The whole BF16 decode MoE layer:
  *   out[t] = residual[t] + sum_s FFN_shared_s(x[t])
@@ -143,6 +165,28 @@ flint_status flint_moe_decode_bf16(const flint_moe_dims* dims, int32_t batch,
                                    void* out_bf16,
                                    int32_t* topk_idx_out, float* topk_w_out,
                                    void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* The two expert stages of flint_moe_decode_bf16, callable on their own.
+ * They use the routing and buckets that the last flint_moe_route or decode
+ * call left in `workspace` (same batch, earlier on the same stream), so
+ *   flint_moe_route; flint_moe_gateup_bf16; flint_moe_down_bf16
+ * computes exactly what flint_moe_decode_bf16 computes (with the routing
+ * copies written by flint_moe_route).
+ * flint_moe_gateup_bf16: for every selected (token, expert) pair and for the
+ *   shared expert(s), h = silu(Wg x) * (Wu x), kept in the workspace (fp32).
+ * flint_moe_down_bf16: out = residual + sum of the routing-weighted
+ *   Wd h terms + the shared expert's Wd h ("expert combine" fused into the
+ *   down GEMV: [vLLM Day-0 Support for Recursive's Flint, "Optimization
+ *   Strategies", "Low-Latency Decode Path"]).  out may alias residual exactly.
+ * Arguments as in flint_moe_decode_bf16. */
+flint_status flint_moe_gateup_bf16(const flint_moe_dims* dims, int32_t batch,
+                                   const void* x_bf16, const void* w13_bf16,
+                                   const void* ws13_bf16,
+                                   void* workspace, size_t ws_bytes, cudaStream_t stream);
+flint_status flint_moe_down_bf16(const flint_moe_dims* dims, int32_t batch,
+                                 const void* residual_bf16, const void* w2_bf16,
+                                 const void* ws2_bf16, void* out_bf16,
+                                 void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* NVFP4 weight-only (W4A16) variant of flint_moe_decode_bf16.  The router,
  * activations and output stay bf16.  Each expert projection is stored as
@@ -175,6 +219,14 @@ flint_status flint_moe_decode_nvfp4_w4a16(
 flint_status flint_moe_rmsnorm_bf16(const flint_moe_dims* dims, int32_t batch,
                                     const void* in_bf16, void* out_bf16, float eps,
                                     cudaStream_t stream);
+
+/* Fault-injection hook for tests: arms a one-shot device-side wait, in the
+ * next routing launch on this workspace, on a workspace flag that nothing ever
+ * sets.  That wait runs out after the workspace's wait limit and records
+ * FLINT_ERR_DEVICE_TIMEOUT, exactly as a stuck pipeline wait would; the
+ * kernels then finish without hanging the GPU.  Re-initialise the workspace
+ * afterwards. */
+flint_status flint_moe_debug_arm_stall(void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

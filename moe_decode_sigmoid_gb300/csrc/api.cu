@@ -1,0 +1,297 @@
+// api.cu — the C ABI (include/flint_moe.h): argument validation, workspace
+// views and launch sequencing.  Every check runs on the host before the first
+// launch; the kernels of one call are chained on the caller's stream with
+// programmatic dependent launch, so each kernel's prologue overlaps the
+// previous kernel's tail.  Nothing here allocates memory or synchronises,
+// except flint_moe_get_device_status.
+#include <cstdint>
+#include <cstring>
+
+#include "flint_moe.h"
+#include "kernels.h"
+
+using namespace flint;
+
+namespace {
+
+constexpr uint64_t DEFAULT_WAIT_NS = 1000000000ull;  // 1 s
+
+bool dims_supported(const flint_moe_dims* d) {
+  return d->hidden == H && d->n_experts == E && d->top_k == TOPK && d->inter == I &&
+         d->n_shared == S;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Required pointer: non-null and 16-byte aligned.
+bool req(const void* p) { return p != nullptr && aligned16(p); }
+// Optional pointer: null, or 16-byte aligned.
+bool opt(const void* p) { return p == nullptr || aligned16(p); }
+
+bool overlap(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+flint_status check_common(const flint_moe_dims* dims, int32_t batch, void* ws, size_t ws_bytes) {
+  if (dims == nullptr) return FLINT_ERR_INVALID_ARG;
+  if (!dims_supported(dims)) return FLINT_ERR_UNSUPPORTED;
+  if (batch < 1 || batch > MAX_B) return FLINT_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned16(ws) || ws_bytes < WsLayout::total(batch))
+    return FLINT_ERR_WORKSPACE;
+  return FLINT_OK;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+flint_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FLINT_OK;
+  (void)cudaGetLastError();  // clear a non-sticky launch error
+  return FLINT_ERR_CUDA;
+}
+
+// Output / input aliasing rule of the decode calls.
+bool aliasing_ok(int32_t batch, const void* x, const void* residual, const void* out,
+                 const void* ws, size_t ws_bytes) {
+  const size_t act = (size_t)batch * H * 2;
+  if (overlap(out, act, x, act)) return false;
+  if (out != residual && overlap(out, act, residual, act)) return false;
+  if (overlap(out, act, ws, ws_bytes)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* flint_status_string(flint_status status) {
+  switch (status) {
+    case FLINT_OK: return "FLINT_OK";
+    case FLINT_ERR_INVALID_ARG: return "FLINT_ERR_INVALID_ARG";
+    case FLINT_ERR_UNSUPPORTED: return "FLINT_ERR_UNSUPPORTED";
+    case FLINT_ERR_WORKSPACE: return "FLINT_ERR_WORKSPACE";
+    case FLINT_ERR_CUDA: return "FLINT_ERR_CUDA";
+    case FLINT_ERR_DEVICE_TIMEOUT: return "FLINT_ERR_DEVICE_TIMEOUT";
+  }
+  return "FLINT_ERR_UNKNOWN";
+}
+
+size_t flint_moe_workspace_bytes(const flint_moe_dims* dims, int32_t max_batch) {
+  if (dims == nullptr || !dims_supported(dims)) return 0;
+  if (max_batch < 1 || max_batch > MAX_B) return 0;
+  return WsLayout::total(max_batch);
+}
+
+flint_status flint_moe_workspace_init(void* workspace, size_t ws_bytes, uint64_t wait_limit_ns,
+                                      cudaStream_t stream) {
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < WsLayout::total(1))
+    return FLINT_ERR_WORKSPACE;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  Ws w = ws_view(workspace);
+  return cuda_status(launch_ws_init(w.hdr, wait_limit_ns ? wait_limit_ns : DEFAULT_WAIT_NS, stream));
+}
+
+flint_status flint_moe_get_device_status(const void* workspace, cudaStream_t stream) {
+  if (workspace == nullptr || !aligned16(workspace)) return FLINT_ERR_WORKSPACE;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  switch (word) {
+    case DEV_OK: return FLINT_OK;
+    case DEV_BAD_ROUTING: return FLINT_ERR_INVALID_ARG;
+    case DEV_TIMEOUT: return FLINT_ERR_DEVICE_TIMEOUT;
+    default: return FLINT_ERR_CUDA;
+  }
+}
+
+flint_status flint_moe_debug_arm_stall(void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < WsLayout::total(1))
+    return FLINT_ERR_WORKSPACE;
+  WsHeader* hdr = ws_view(workspace).hdr;
+  return cuda_status(cudaMemsetAsync(&hdr->stall_armed, 1, sizeof(uint32_t), stream));
+}
+
+flint_status flint_moe_route(const flint_moe_dims* dims, int32_t batch, const void* x_bf16,
+                             const void* w_router_bf16, const float* logit_bias, int32_t* topk_idx,
+                             float* topk_w, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  flint_status st = check_common(dims, batch, workspace, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(x_bf16) || !req(w_router_bf16) || !opt(logit_bias) || !req(topk_idx) || !req(topk_w))
+    return FLINT_ERR_INVALID_ARG;
+  RouterArgs a = {};
+  a.x = static_cast<const uint16_t*>(x_bf16);
+  a.wr = static_cast<const uint16_t*>(w_router_bf16);
+  a.bias = logit_bias;
+  a.B = batch;
+  a.ws = ws_view(workspace);
+  a.user_idx = topk_idx;
+  a.user_w = topk_w;
+  a.do_bucket = 1;
+  a.stall_check = 1;
+  return cuda_status(launch_router(a, stream, true));
+}
+
+flint_status flint_moe_bucket(const flint_moe_dims* dims, int32_t batch, const int32_t* topk_idx,
+                              int32_t* uniq, int32_t* offsets, int32_t* pairs, int32_t* n_uniq,
+                              void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  flint_status st = check_common(dims, batch, workspace, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(topk_idx) || !req(uniq) || !req(offsets) || !req(pairs) || !req(n_uniq))
+    return FLINT_ERR_INVALID_ARG;
+  Ws w = ws_view(workspace);
+  cudaError_t e = cudaMemcpyAsync(w.topk_idx, topk_idx, sizeof(int32_t) * (size_t)batch * TOPK,
+                                  cudaMemcpyDeviceToDevice, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  BucketOut bo = {uniq, offsets, pairs, n_uniq};
+  return cuda_status(launch_bucket(w, batch, bo, stream));
+}
+
+static flint_status decode_checks(const flint_moe_dims* dims, int32_t batch, const void* x,
+                                  const void* residual, const void* wr, const float* bias,
+                                  void* out, int32_t* idx_out, float* w_out, void* ws,
+                                  size_t ws_bytes) {
+  flint_status st = check_common(dims, batch, ws, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(x) || !req(residual) || !req(wr) || !opt(bias) || !req(out) || !opt(idx_out) ||
+      !opt(w_out))
+    return FLINT_ERR_INVALID_ARG;
+  if (!aliasing_ok(batch, x, residual, out, ws, ws_bytes)) return FLINT_ERR_INVALID_ARG;
+  return FLINT_OK;
+}
+
+static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const void* residual,
+                              const void* wr, const float* bias, const ExpertW& w, void* out,
+                              int32_t* idx_out, float* w_out, void* workspace,
+                              cudaStream_t stream) {
+  const int sms = num_sms();
+  if (sms <= 0) return FLINT_ERR_CUDA;
+  RouterArgs r = {};
+  r.x = static_cast<const uint16_t*>(x);
+  r.wr = static_cast<const uint16_t*>(wr);
+  r.bias = bias;
+  r.B = batch;
+  r.ws = ws_view(workspace);
+  r.user_idx = idx_out;
+  r.user_w = w_out;
+  r.do_bucket = 1;
+  r.stall_check = 1;
+  cudaError_t e = launch_router(r, stream, true);
+  if (e != cudaSuccess) return cuda_status(e);
+  ExpertArgs a = {};
+  a.x = r.x;
+  a.residual = static_cast<const uint16_t*>(residual);
+  a.out = static_cast<uint16_t*>(out);
+  a.w = w;
+  a.B = batch;
+  a.ws = r.ws;
+  e = nvfp4 ? launch_gateup_nvfp4(a, stream, sms) : launch_gateup_bf16(a, stream, sms);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = nvfp4 ? launch_down_nvfp4(a, stream) : launch_down_bf16(a, stream);
+  return cuda_status(e);
+}
+
+flint_status flint_moe_decode_bf16(const flint_moe_dims* dims, int32_t batch, const void* x_bf16,
+                                   const void* residual_bf16, const void* w_router_bf16,
+                                   const float* logit_bias, const void* w13_bf16,
+                                   const void* w2_bf16, const void* ws13_bf16,
+                                   const void* ws2_bf16, void* out_bf16, int32_t* topk_idx_out,
+                                   float* topk_w_out, void* workspace, size_t ws_bytes,
+                                   cudaStream_t stream) {
+  flint_status st = decode_checks(dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias,
+                                  out_bf16, topk_idx_out, topk_w_out, workspace, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(w13_bf16) || !req(w2_bf16) || !req(ws13_bf16) || !req(ws2_bf16))
+    return FLINT_ERR_INVALID_ARG;
+  ExpertW w = {};
+  w.w13 = static_cast<const uint16_t*>(w13_bf16);
+  w.w2 = static_cast<const uint16_t*>(w2_bf16);
+  w.ws13 = static_cast<const uint16_t*>(ws13_bf16);
+  w.ws2 = static_cast<const uint16_t*>(ws2_bf16);
+  return run_layer(false, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias, w, out_bf16,
+                   topk_idx_out, topk_w_out, workspace, stream);
+}
+
+flint_status flint_moe_gateup_bf16(const flint_moe_dims* dims, int32_t batch, const void* x_bf16,
+                                   const void* w13_bf16, const void* ws13_bf16, void* workspace,
+                                   size_t ws_bytes, cudaStream_t stream) {
+  flint_status st = check_common(dims, batch, workspace, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(x_bf16) || !req(w13_bf16) || !req(ws13_bf16)) return FLINT_ERR_INVALID_ARG;
+  const int sms = num_sms();
+  if (sms <= 0) return FLINT_ERR_CUDA;
+  ExpertArgs a = {};
+  a.x = static_cast<const uint16_t*>(x_bf16);
+  a.w.w13 = static_cast<const uint16_t*>(w13_bf16);
+  a.w.ws13 = static_cast<const uint16_t*>(ws13_bf16);
+  a.B = batch;
+  a.ws = ws_view(workspace);
+  return cuda_status(launch_gateup_bf16(a, stream, sms));
+}
+
+flint_status flint_moe_down_bf16(const flint_moe_dims* dims, int32_t batch,
+                                 const void* residual_bf16, const void* w2_bf16,
+                                 const void* ws2_bf16, void* out_bf16, void* workspace,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  flint_status st = check_common(dims, batch, workspace, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(residual_bf16) || !req(w2_bf16) || !req(ws2_bf16) || !req(out_bf16))
+    return FLINT_ERR_INVALID_ARG;
+  const size_t act = (size_t)batch * H * 2;
+  if (out_bf16 != residual_bf16 && overlap(out_bf16, act, residual_bf16, act))
+    return FLINT_ERR_INVALID_ARG;
+  if (overlap(out_bf16, act, workspace, ws_bytes)) return FLINT_ERR_INVALID_ARG;
+  ExpertArgs a = {};
+  a.residual = static_cast<const uint16_t*>(residual_bf16);
+  a.out = static_cast<uint16_t*>(out_bf16);
+  a.w.w2 = static_cast<const uint16_t*>(w2_bf16);
+  a.w.ws2 = static_cast<const uint16_t*>(ws2_bf16);
+  a.B = batch;
+  a.ws = ws_view(workspace);
+  return cuda_status(launch_down_bf16(a, stream));
+}
+
+flint_status flint_moe_decode_nvfp4_w4a16(
+    const flint_moe_dims* dims, int32_t batch, const void* x_bf16, const void* residual_bf16,
+    const void* w_router_bf16, const float* logit_bias, const uint8_t* w13_q,
+    const uint8_t* w13_sf, const float* w13_ts, const uint8_t* w2_q, const uint8_t* w2_sf,
+    const float* w2_ts, const uint8_t* ws13_q, const uint8_t* ws13_sf, const float* ws13_ts,
+    const uint8_t* ws2_q, const uint8_t* ws2_sf, const float* ws2_ts, void* out_bf16,
+    int32_t* topk_idx_out, float* topk_w_out, void* workspace, size_t ws_bytes,
+    cudaStream_t stream) {
+  flint_status st = decode_checks(dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias,
+                                  out_bf16, topk_idx_out, topk_w_out, workspace, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(w13_q) || !req(w13_sf) || !req(w13_ts) || !req(w2_q) || !req(w2_sf) || !req(w2_ts) ||
+      !req(ws13_q) || !req(ws13_sf) || !req(ws13_ts) || !req(ws2_q) || !req(ws2_sf) ||
+      !req(ws2_ts))
+    return FLINT_ERR_INVALID_ARG;
+  ExpertW w = {};
+  w.w13_q = w13_q; w.w13_sf = w13_sf; w.w13_ts = w13_ts;
+  w.w2_q = w2_q; w.w2_sf = w2_sf; w.w2_ts = w2_ts;
+  w.ws13_q = ws13_q; w.ws13_sf = ws13_sf; w.ws13_ts = ws13_ts;
+  w.ws2_q = ws2_q; w.ws2_sf = ws2_sf; w.ws2_ts = ws2_ts;
+  return run_layer(true, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias, w, out_bf16,
+                   topk_idx_out, topk_w_out, workspace, stream);
+}
+
+flint_status flint_moe_rmsnorm_bf16(const flint_moe_dims* dims, int32_t batch, const void* in_bf16,
+                                    void* out_bf16, float eps, cudaStream_t stream) {
+  if (dims == nullptr) return FLINT_ERR_INVALID_ARG;
+  if (dims->hidden != H) return FLINT_ERR_UNSUPPORTED;
+  if (batch < 1 || batch > MAX_B || !req(in_bf16) || !req(out_bf16) || !(eps >= 0.0f))
+    return FLINT_ERR_INVALID_ARG;
+  const size_t act = (size_t)batch * H * 2;
+  if (overlap(in_bf16, act, out_bf16, act)) return FLINT_ERR_INVALID_ARG;
+  return cuda_status(launch_rmsnorm(static_cast<const uint16_t*>(in_bf16),
+                                    static_cast<uint16_t*>(out_bf16), batch, eps, stream));
+}
+
+}  // extern "C"

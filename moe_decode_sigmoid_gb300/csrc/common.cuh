@@ -1,0 +1,199 @@
+// common.cuh — shapes, workspace layout and sm_103a PTX helpers shared by the
+// Flint decode-MoE kernels.  Device code only uses what is defined here and in
+// the CUDA runtime headers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace flint {
+
+// ---- the specialised layer shape ------------------------------------------
+constexpr int H = 2048;   // hidden
+constexpr int E = 256;    // routed experts
+constexpr int TOPK = 6;   // experts per token
+constexpr int I = 512;    // expert intermediate size
+constexpr int S = 1;      // shared experts
+constexpr int MAX_B = 256;
+constexpr int SLOTS = TOPK + S;          // h rows per token
+constexpr int GROUP_MAX = 24;            // tokens per (expert, token-range) group
+// Groups: each distinct expert contributes ceil(cnt/G) <= cnt/G + 1 groups,
+// so routed groups <= TOPK*B/G + min(E, TOPK*B); plus S*ceil(B/G) shared.
+constexpr int MAX_GROUPS = TOPK * MAX_B / GROUP_MAX + E + S * (MAX_B / GROUP_MAX + 1);
+
+// Device error codes written to the workspace error word.
+constexpr uint32_t DEV_OK = 0;
+constexpr uint32_t DEV_BAD_ROUTING = 1;  // bucketing got an index outside [0,E) or a repeat
+constexpr uint32_t DEV_TIMEOUT = 5;
+
+// ---- workspace layout ------------------------------------------------------
+// [ header | logits fp32 [MAX_B,E] | topk_idx i32 [MAX_B,K] | topk_w f32 [MAX_B,K] |
+//   pair_tok i32 [MAX_B*SLOTS] | pair_w f32 [MAX_B*SLOTS] | groups int4 [MAX_GROUPS] |
+//   h fp32 [max_batch*SLOTS, I] ]
+// Every array but the last is sized for MAX_B, so the offsets do not depend on
+// the batch a workspace was sized for; only h grows with max_batch.
+struct WsHeader {
+  uint32_t error;            // DEV_OK or an error code (first writer wins)
+  uint32_t tiles_done;       // router: token tiles whose top-k is final
+  uint32_t n_groups;         // number of (expert, token range) groups
+  uint32_t n_uniq;           // distinct routed experts
+  uint64_t wait_limit_ns;    // bound of every device-side wait
+  uint32_t stall_armed;      // test hook: one-shot wait on stall_release
+  uint32_t stall_release;    // never written by the library
+  uint32_t tile_ctas_done[MAX_B / 8];  // router: finished CTAs per token tile
+  uint32_t pad[24];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+__host__ __device__ constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct WsLayout {
+  static constexpr size_t logits = sizeof(WsHeader);
+  static constexpr size_t topk_idx = align256(logits + sizeof(float) * (size_t)MAX_B * E);
+  static constexpr size_t topk_w = align256(topk_idx + sizeof(int) * (size_t)MAX_B * TOPK);
+  static constexpr size_t pair_tok = align256(topk_w + sizeof(float) * (size_t)MAX_B * TOPK);
+  static constexpr size_t pair_w = align256(pair_tok + sizeof(int) * (size_t)MAX_B * SLOTS);
+  static constexpr size_t groups = align256(pair_w + sizeof(float) * (size_t)MAX_B * SLOTS);
+  static constexpr size_t h = align256(groups + 16 * (size_t)MAX_GROUPS);
+  static constexpr size_t total(int max_b) {
+    return align256(h + sizeof(float) * (size_t)max_b * SLOTS * I);
+  }
+};
+
+// Pointers into one workspace (built on the host, passed by value).
+struct Ws {
+  WsHeader* hdr;
+  float* logits;
+  int* topk_idx;
+  float* topk_w;
+  int* pair_tok;
+  float* pair_w;
+  int4* groups;   // {expert (E.. for shared), first pair, pair count, 0}
+  float* h;
+};
+
+inline Ws ws_view(void* base) {
+  char* b = static_cast<char*>(base);
+  Ws w;
+  w.hdr = reinterpret_cast<WsHeader*>(b);
+  w.logits = reinterpret_cast<float*>(b + WsLayout::logits);
+  w.topk_idx = reinterpret_cast<int*>(b + WsLayout::topk_idx);
+  w.topk_w = reinterpret_cast<float*>(b + WsLayout::topk_w);
+  w.pair_tok = reinterpret_cast<int*>(b + WsLayout::pair_tok);
+  w.pair_w = reinterpret_cast<float*>(b + WsLayout::pair_w);
+  w.groups = reinterpret_cast<int4*>(b + WsLayout::groups);
+  w.h = reinterpret_cast<float*>(b + WsLayout::h);
+  return w;
+}
+
+// ---- small device helpers ---------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Programmatic dependent launch: wait for the preceding grid's completion and
+// memory flush / allow the next grid to start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Bounded wait for the phase with the given parity; false if the deadline passed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline) {
+  if (mbar_try_wait(bar, parity)) return true;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() > deadline) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared (TMA engine); completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Named barrier over the first `nthreads` threads (multiple of 32).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// bf16 pair (one 32-bit word, low half first) -> two fp32.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// fp32 -> bf16 bits, round to nearest even.
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+// Two fp32 -> packed bf16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Record a device error (first writer wins).
+__device__ __forceinline__ void set_error(WsHeader* hdr, uint32_t code) {
+  atomicCAS(&hdr->error, DEV_OK, code);
+}
+
+__device__ __forceinline__ uint64_t wait_deadline(const WsHeader* hdr) {
+  uint64_t lim = *reinterpret_cast<const volatile uint64_t*>(&hdr->wait_limit_ns);
+  return globaltimer_ns() + lim;
+}
+
+// silu(g) * u with silu(g) = g / (1 + exp(-g))
+// ("SiLU-and-mul": Flint on Intel Arc Pro B70, "norm.py: Triton kernels that assumed CUDA").
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+}  // namespace flint

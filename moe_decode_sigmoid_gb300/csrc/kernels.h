@@ -1,0 +1,67 @@
+// kernels.h — argument blocks and host launch wrappers of the Flint decode-MoE
+// kernels (one translation unit per kernel family; the C ABI in api.cu calls
+// these wrappers).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace flint {
+
+// Optional plain description of the buckets (flint_moe_bucket).
+struct BucketOut {
+  int* uniq;     // [E]   distinct experts, ascending (first n_uniq valid)
+  int* offsets;  // [E+1] first pair of each, then B*TOPK
+  int* pairs;    // [B*TOPK] token*8 + slot, ordered by (expert, token)
+  int* n_uniq;   // [1]
+};
+
+struct RouterArgs {
+  const uint16_t* x;   // [B,H] bf16
+  const uint16_t* wr;  // [E,H] bf16
+  const float* bias;   // [E] or null
+  int B;
+  Ws ws;
+  int* user_idx;       // [B,TOPK] or null
+  float* user_w;       // [B,TOPK] or null
+  int do_bucket;       // build pairs/groups for the expert kernels
+  int stall_check;     // honour the workspace's one-shot stall hook
+  BucketOut bucket;    // optional plain bucket outputs (all null to skip)
+};
+
+// Expert weights of one layer in one of the two storage formats.
+struct ExpertW {
+  // bf16
+  const uint16_t* w13;   // [E,2I,H]
+  const uint16_t* w2;    // [E,H,I]
+  const uint16_t* ws13;  // [S,2I,H]
+  const uint16_t* ws2;   // [S,H,I]
+  // nvfp4
+  const uint8_t *w13_q, *w13_sf, *w2_q, *w2_sf;
+  const float *w13_ts, *w2_ts;
+  const uint8_t *ws13_q, *ws13_sf, *ws2_q, *ws2_sf;
+  const float *ws13_ts, *ws2_ts;
+};
+
+struct ExpertArgs {
+  const uint16_t* x;         // [B,H] bf16
+  const uint16_t* residual;  // [B,H] bf16 (down kernel)
+  uint16_t* out;             // [B,H] bf16 (down kernel)
+  ExpertW w;
+  int B;
+  Ws ws;
+};
+
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl);
+cudaError_t launch_bucket(const Ws& ws, int B, const BucketOut& user, cudaStream_t stream);
+cudaError_t launch_gateup_bf16(const ExpertArgs& a, cudaStream_t stream, int num_sms);
+cudaError_t launch_down_bf16(const ExpertArgs& a, cudaStream_t stream);
+cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
+cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream);
+cudaError_t launch_rmsnorm(const uint16_t* in, uint16_t* out, int B, float eps,
+                           cudaStream_t stream);
+cudaError_t launch_ws_init(WsHeader* hdr, uint64_t wait_limit_ns, cudaStream_t stream);
+
+}  // namespace flint

@@ -1,0 +1,515 @@
+// nvfp4.cu — NVFP4 weight-only (W4A16) expert kernels: gate/up + SiLU-and-mul
+// and down + combine + shared + residual, with the weights dequantised in
+// registers.  "run weight-only (W4A16) while maintaining BF16 activations":
+// vLLM Day-0 Support for Recursive's Flint, "Flint Model Overview and
+// Capabilities".
+//
+// Storage (per projection, rows x K): q = e2m1 codes, two per byte (low nibble
+// = even k); sf = one OCP E4M3 scale per 16 consecutive k; ts = fp32 tensor
+// scale.  W = e2m1(q) * e4m3(sf) * ts.
+//
+// The product e2m1 * e4m3 has at most 6 significant bits and lies in
+// [2^-10, 2688], so it is EXACT in f16: each thread converts its fragment's
+// codes with cvt.rn.f16x2.e2m1x2, multiplies by the block scale (f16x2, exact)
+// and feeds mma.sync m16n8k16 f16 x f16 -> fp32.  Activations (bf16 x, fp32 h)
+// are rounded to f16 for the MMA operand; the tensor scale is applied to the
+// fp32 sums.  Dequantisation costs about one instruction per weight, which is
+// why this path uses the tensor cores for every group, including single-token
+// ones: the FMAs then cost nothing on the CUDA cores that do the unpacking.
+//
+// The work decomposition and the TMA/mbarrier pipeline are the same as the
+// BF16 kernels (gateup.cu, down.cu): gate/up units are (group, 8 gate + 8 up
+// rows) ranges split evenly over one CTA per SM; the down kernel is
+// row-slice-major (16 output rows per CTA, all groups, deterministic combine).
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace flint {
+namespace f4 {
+constexpr int CWARPS = 8;
+constexpr int THREADS = CWARPS * 32 + 32;
+constexpr uint64_t DRAIN_NS = 2000000000ull;
+// gate/up
+constexpr int GU_QROW = H / 2;                       // 1024 code bytes per row
+constexpr int GU_QSTRIDE = GU_QROW + 16;             // 4-bank shift per row
+constexpr int GU_SFROW = H / 16;                     // 128 scale bytes per row
+constexpr int GU_STAGE = 16 * GU_QSTRIDE + 16 * GU_SFROW;  // 18,688
+constexpr int GU_NSTAGE = 10;
+constexpr int GU_RED = CWARPS * 16 * GROUP_MAX;
+constexpr size_t GU_SMEM = (size_t)GU_NSTAGE * GU_STAGE + GU_RED * 4 + 2 * GU_NSTAGE * 8;
+constexpr int UNITS = I / 8;
+// down
+constexpr int RS = 16;
+constexpr int DN_QROW = I / 2;                       // 256
+constexpr int DN_QSTRIDE = DN_QROW + 16;             // 272
+constexpr int DN_SFROW = I / 16;                     // 32
+constexpr int DN_WBYTES = RS * DN_QSTRIDE + RS * DN_SFROW;  // 4,864
+constexpr int HROW = I * 4;
+constexpr int HSTRIDE = HROW + 64;
+constexpr int DN_RED = CWARPS * RS * GROUP_MAX;
+constexpr int DN_MAX_STAGES = 8;
+constexpr int SMEM_CAP = 232448 - 1024;
+__host__ __device__ inline int dn_nmax(int B) { return B < GROUP_MAX ? B : GROUP_MAX; }
+__host__ __device__ inline int dn_stage(int B) { return DN_WBYTES + dn_nmax(B) * HSTRIDE; }
+__host__ __device__ inline int dn_fixed(int B) { return DN_RED * 4 + B * RS * 4 + 2 * DN_MAX_STAGES * 8; }
+__host__ __device__ inline int dn_nstages(int B) {
+  int n = (SMEM_CAP - dn_fixed(B)) / dn_stage(B);
+  return n > DN_MAX_STAGES ? DN_MAX_STAGES : n;
+}
+__host__ __device__ inline int dn_smem(int B) { return dn_nstages(B) * dn_stage(B) + dn_fixed(B); }
+}  // namespace f4
+
+namespace {
+
+// Eight e2m1 codes (one 32-bit word, code k in bits 4k..4k+3) -> four f16x2,
+// each holding codes (2i, 2i+1) in its (low, high) halves.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& p0, uint32_t& p1,
+                                                uint32_t& p2, uint32_t& p3) {
+  asm("{ .reg .b8 b0, b1, b2, b3;\n"
+      "  mov.b32 {b0, b1, b2, b3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      "  cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      "  cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      "  cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(p0), "=r"(p1), "=r"(p2), "=r"(p3)
+      : "r"(w));
+}
+
+// One E4M3 byte -> f16x2 with the scale in both halves.
+__device__ __forceinline__ uint32_t e4m3_bcast_f16x2(uint32_t byte) {
+  const uint16_t two = (uint16_t)(byte | (byte << 8));
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// bf16 x 8 (uint4) -> f16 x 8 (uint4), same element order.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& v) {
+  uint4 r;
+  r.x = f16x2_of(bf_lo(v.x), bf_hi(v.x));
+  r.y = f16x2_of(bf_lo(v.y), bf_hi(v.y));
+  r.z = f16x2_of(bf_lo(v.z), bf_hi(v.z));
+  r.w = f16x2_of(bf_lo(v.w), bf_hi(v.w));
+  return r;
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+struct Pipe {
+  uint8_t* stages;
+  uint32_t stages_addr;
+  int stage_bytes, nstage;
+  uint32_t full0, empty0;
+  uint64_t deadline;
+  WsHeader* hdr;
+  volatile int* abort_flag;
+};
+
+__device__ __forceinline__ uint32_t full_bar(const Pipe& p, int s) { return p.full0 + 8u * s; }
+__device__ __forceinline__ uint32_t empty_bar(const Pipe& p, int s) { return p.empty0 + 8u * s; }
+
+__device__ __forceinline__ bool wait_full(const Pipe& p, int slot, uint32_t parity) {
+  if (*p.abort_flag) return false;
+  if (mbar_wait(full_bar(p, slot), parity, p.deadline)) return true;
+  *p.abort_flag = 1;
+  set_error(p.hdr, DEV_TIMEOUT);
+  return false;
+}
+
+// Producer-side acquire of a free stage; false means stop issuing.
+__device__ __forceinline__ bool acquire_stage(const Pipe& p, int it) {
+  const int slot = it % p.nstage;
+  bool got = true;
+  if (it >= p.nstage)
+    got = mbar_wait(empty_bar(p, slot), (uint32_t)((it / p.nstage) - 1) & 1u, p.deadline);
+  if (!got || *p.abort_flag) {
+    *p.abort_flag = 1;
+    if (!got) set_error(p.hdr, DEV_TIMEOUT);
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void drain(const Pipe& p, int it) {
+  const uint64_t dl = globaltimer_ns() + f4::DRAIN_NS;
+  for (int j = it - p.nstage < 0 ? 0 : it - p.nstage; j < it; ++j)
+    mbar_wait(full_bar(p, j % p.nstage), (uint32_t)(j / p.nstage) & 1u, dl);
+}
+
+__device__ __forceinline__ void init_pipe(Pipe& p, uint8_t* smem, int stage_bytes, int nstage,
+                                          uint64_t* bars, int max_stages, volatile int* abort_flag,
+                                          WsHeader* hdr) {
+  p.stages = smem;
+  p.stages_addr = smem_addr(smem);
+  p.stage_bytes = stage_bytes;
+  p.nstage = nstage;
+  p.full0 = smem_addr(bars);
+  p.empty0 = smem_addr(bars + max_stages);
+  p.abort_flag = abort_flag;
+  p.hdr = hdr;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(full_bar(p, s), 1);
+      mbar_init(empty_bar(p, s), f4::CWARPS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+}
+
+// ---------------------------------------------------------------- gate/up
+
+template <int NT>
+__device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, float* red, int u0,
+                                           int u1, int expert, int pair0, int n, int& it,
+                                           bool& ok) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  named_sync(1, f4::CWARPS * 32);  // the previous segment is done with `red`
+  // B fragments: this warp's 256-column K slice of each token, as f16.
+  uint4 bfr[NT][8];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int slot = nt * 8 + g;
+    if (slot < n) {
+      const int tok = __ldcg(a.ws.pair_tok + pair0 + slot);
+      const uint16_t* row = a.x + (size_t)tok * H + warp * 256 + q * 8;
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb)
+        bfr[nt][kb] = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(row + kb * 32)));
+    } else {
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) bfr[nt][kb] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  const float* ts = expert < E ? a.w.w13_ts + 2 * expert : a.w.ws13_ts + 2 * (expert - E);
+  const float ts_g = __ldg(ts), ts_u = __ldg(ts + 1);
+  for (int u = u0; u < u1; ++u) {
+    const int blk = u & (f4::UNITS - 1);
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const int slot = it % p.nstage;
+    if (ok) ok = wait_full(p, slot, (uint32_t)(it / p.nstage) & 1u);
+    if (ok) {
+      const uint8_t* st = p.stages + slot * p.stage_bytes;
+      const uint8_t* qlo = st + g * f4::GU_QSTRIDE + warp * 128 + q * 4;
+      const uint8_t* qhi = qlo + 8 * f4::GU_QSTRIDE;
+      const uint8_t* sfb = st + 16 * f4::GU_QSTRIDE;
+      const uint4 slo = *reinterpret_cast<const uint4*>(sfb + g * f4::GU_SFROW + warp * 16);
+      const uint4 shi = *reinterpret_cast<const uint4*>(sfb + (g + 8) * f4::GU_SFROW + warp * 16);
+      const uint32_t sl[4] = {slo.x, slo.y, slo.z, slo.w};
+      const uint32_t sh[4] = {shi.x, shi.y, shi.z, shi.w};
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) {
+        const int sh_bits = 8 * (2 * (kb & 1) + (q >> 1));
+        const uint32_t scl = e4m3_bcast_f16x2((sl[kb >> 1] >> sh_bits) & 0xffu);
+        const uint32_t sch = e4m3_bcast_f16x2((sh[kb >> 1] >> sh_bits) & 0xffu);
+        uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(qlo + kb * 16), l0, l1, l2, l3);
+        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(qhi + kb * 16), h0, h1, h2, h3);
+        l0 = hmul2(l0, scl); l1 = hmul2(l1, scl); l2 = hmul2(l2, scl); l3 = hmul2(l3, scl);
+        h0 = hmul2(h0, sch); h1 = hmul2(h1, sch); h2 = hmul2(h2, sch); h3 = hmul2(h3, sch);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint4 b = bfr[nt][kb];
+          mma_f16(acc[nt], l0, h0, l1, h1, b.x, b.y);
+          mma_f16(acc[nt], l2, h2, l3, h3, b.z, b.w);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(p, slot));
+    ++it;
+    float* rw = red + warp * 16 * GROUP_MAX;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = nt * 8 + 2 * q;
+      rw[g * GROUP_MAX + col] = acc[nt][0];
+      rw[g * GROUP_MAX + col + 1] = acc[nt][1];
+      rw[(g + 8) * GROUP_MAX + col] = acc[nt][2];
+      rw[(g + 8) * GROUP_MAX + col + 1] = acc[nt][3];
+    }
+    named_sync(1, f4::CWARPS * 32);
+    {
+      const int r = threadIdx.x >> 5;
+      const int j = threadIdx.x & 31;
+      if (j < n && ok) {
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int w = 0; w < f4::CWARPS; ++w) {
+          gs += red[(w * 16 + r) * GROUP_MAX + j];
+          us += red[(w * 16 + r + 8) * GROUP_MAX + j];
+        }
+        a.ws.h[(size_t)(pair0 + j) * I + blk * 8 + r] = silu_mul(gs * ts_g, us * ts_u);
+      }
+    }
+    named_sync(1, f4::CWARPS * 32);
+  }
+}
+
+__device__ __forceinline__ void gu_produce(const Pipe& p, const ExpertArgs& a, int u_begin,
+                                           int u_end) {
+  int it = 0;
+  for (int u = u_begin; u < u_end; ++u) {
+    const int4 grp = __ldcg(a.ws.groups + (u / f4::UNITS));
+    const int blk = u & (f4::UNITS - 1);
+    const bool routed = grp.x < E;
+    const int e = routed ? grp.x : grp.x - E;
+    const uint8_t* qb = (routed ? a.w.w13_q : a.w.ws13_q) + (size_t)e * (2 * I) * f4::GU_QROW;
+    const uint8_t* sb = (routed ? a.w.w13_sf : a.w.ws13_sf) + (size_t)e * (2 * I) * f4::GU_SFROW;
+    if (!acquire_stage(p, it)) break;
+    const int slot = it % p.nstage;
+    mbar_expect_tx(full_bar(p, slot), 16 * f4::GU_QROW + 16 * f4::GU_SFROW);
+    const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
+#pragma unroll 1
+    for (int r = 0; r < 16; ++r) {
+      const int row = (r < 8 ? 0 : I) + blk * 8 + (r & 7);
+      bulk_g2s(dst + r * f4::GU_QSTRIDE, qb + (size_t)row * f4::GU_QROW, f4::GU_QROW,
+               full_bar(p, slot));
+    }
+    bulk_g2s(dst + 16 * f4::GU_QSTRIDE, sb + (size_t)(blk * 8) * f4::GU_SFROW, 8 * f4::GU_SFROW,
+             full_bar(p, slot));
+    bulk_g2s(dst + 16 * f4::GU_QSTRIDE + 8 * f4::GU_SFROW, sb + (size_t)(I + blk * 8) * f4::GU_SFROW,
+             8 * f4::GU_SFROW, full_bar(p, slot));
+    ++it;
+  }
+  drain(p, it);
+}
+
+// ---------------------------------------------------------------- down
+
+template <int NT>
+__device__ __forceinline__ void dn_group(const ExpertArgs& a, const uint8_t* st, float* red,
+                                         float* acc_s, int expert, int pair0, int n) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  const uint8_t* qlo = st + g * f4::DN_QSTRIDE + warp * 32 + q * 4;
+  const uint8_t* qhi = qlo + 8 * f4::DN_QSTRIDE;
+  const uint8_t* sfb = st + f4::RS * f4::DN_QSTRIDE;
+  const uint32_t slo = *reinterpret_cast<const uint32_t*>(sfb + g * f4::DN_SFROW + warp * 4);
+  const uint32_t shi = *reinterpret_cast<const uint32_t*>(sfb + (g + 8) * f4::DN_SFROW + warp * 4);
+  const uint8_t* hs = st + f4::DN_WBYTES + (warp * 64 + q * 8) * 4;
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb) {
+    const int sh_bits = 8 * (2 * kb + (q >> 1));
+    const uint32_t scl = e4m3_bcast_f16x2((slo >> sh_bits) & 0xffu);
+    const uint32_t sch = e4m3_bcast_f16x2((shi >> sh_bits) & 0xffu);
+    uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+    e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(qlo + kb * 16), l0, l1, l2, l3);
+    e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(qhi + kb * 16), h0, h1, h2, h3);
+    l0 = hmul2(l0, scl); l1 = hmul2(l1, scl); l2 = hmul2(l2, scl); l3 = hmul2(l3, scl);
+    h0 = hmul2(h0, sch); h1 = hmul2(h1, sch); h2 = hmul2(h2, sch); h3 = hmul2(h3, sch);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int slot = nt * 8 + g;
+      uint32_t b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+      if (slot < n) {
+        const float4 v0 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + kb * 128);
+        const float4 v1 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + kb * 128 + 16);
+        b0 = f16x2_of(v0.x, v0.y);
+        b1 = f16x2_of(v0.z, v0.w);
+        b2 = f16x2_of(v1.x, v1.y);
+        b3 = f16x2_of(v1.z, v1.w);
+      }
+      mma_f16(acc[nt], l0, h0, l1, h1, b0, b1);
+      mma_f16(acc[nt], l2, h2, l3, h3, b2, b3);
+    }
+  }
+  float* rw = red + warp * f4::RS * GROUP_MAX;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int col = nt * 8 + 2 * q;
+    rw[g * GROUP_MAX + col] = acc[nt][0];
+    rw[g * GROUP_MAX + col + 1] = acc[nt][1];
+    rw[(g + 8) * GROUP_MAX + col] = acc[nt][2];
+    rw[(g + 8) * GROUP_MAX + col + 1] = acc[nt][3];
+  }
+  named_sync(1, f4::CWARPS * 32);
+  const float ts = expert < E ? __ldg(a.w.w2_ts + expert) : __ldg(a.w.ws2_ts + (expert - E));
+  for (int i = threadIdx.x; i < f4::RS * n; i += f4::CWARPS * 32) {
+    const int r = i & (f4::RS - 1), j = i >> 4;
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < f4::CWARPS; ++w) s += red[(w * f4::RS + r) * GROUP_MAX + j];
+    const int t = __ldcg(a.ws.pair_tok + pair0 + j);
+    const float wt = __ldcg(a.ws.pair_w + pair0 + j);
+    acc_s[t * f4::RS + r] += wt * (s * ts);
+  }
+  named_sync(1, f4::CWARPS * 32);
+}
+
+__device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, int n_groups,
+                                           int r0) {
+  int it = 0;
+  for (int gi = 0; gi < n_groups; ++gi) {
+    const int4 grp = __ldcg(a.ws.groups + gi);
+    if (!acquire_stage(p, it)) break;
+    const int slot = it % p.nstage;
+    const int n = grp.z;
+    const bool routed = grp.x < E;
+    const int e = routed ? grp.x : grp.x - E;
+    const uint8_t* qb = (routed ? a.w.w2_q : a.w.ws2_q) + ((size_t)e * H + r0) * f4::DN_QROW;
+    const uint8_t* sb = (routed ? a.w.w2_sf : a.w.ws2_sf) + ((size_t)e * H + r0) * f4::DN_SFROW;
+    mbar_expect_tx(full_bar(p, slot), f4::RS * (f4::DN_QROW + f4::DN_SFROW) + n * f4::HROW);
+    const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
+#pragma unroll 1
+    for (int r = 0; r < f4::RS; ++r)
+      bulk_g2s(dst + r * f4::DN_QSTRIDE, qb + (size_t)r * f4::DN_QROW, f4::DN_QROW, full_bar(p, slot));
+    bulk_g2s(dst + f4::RS * f4::DN_QSTRIDE, sb, f4::RS * f4::DN_SFROW, full_bar(p, slot));
+#pragma unroll 1
+    for (int i = 0; i < n; ++i)
+      bulk_g2s(dst + f4::DN_WBYTES + i * f4::HSTRIDE, a.ws.h + (size_t)(grp.y + i) * I, f4::HROW,
+               full_bar(p, slot));
+    ++it;
+  }
+  drain(p, it);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(f4::THREADS, 1) gateup_nvfp4_kernel(ExpertArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_abort;
+  float* red = reinterpret_cast<float*>(smem + f4::GU_NSTAGE * f4::GU_STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red + f4::GU_RED);
+  Pipe p;
+  init_pipe(p, smem, f4::GU_STAGE, f4::GU_NSTAGE, bars, f4::GU_NSTAGE, &s_abort, a.ws.hdr);
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int n_units = (int)__ldcg(&a.ws.hdr->n_groups) * f4::UNITS;
+  const int u_begin = (int)((long long)blockIdx.x * n_units / gridDim.x);
+  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
+  p.deadline = wait_deadline(a.ws.hdr);
+  if ((threadIdx.x >> 5) == f4::CWARPS) {
+    if ((threadIdx.x & 31) == 0) gu_produce(p, a, u_begin, u_end);
+    return;
+  }
+  int it = 0;
+  bool ok = true;
+  int u = u_begin;
+  while (u < u_end) {
+    const int gi = u / f4::UNITS;
+    const int4 grp = __ldcg(a.ws.groups + gi);
+    const int u1 = min(u_end, (gi + 1) * f4::UNITS);
+    switch ((grp.z + 7) >> 3) {
+      case 1: gu_segment<1>(p, a, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+      case 2: gu_segment<2>(p, a, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+      default: gu_segment<3>(p, a, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+    }
+    u = u1;
+  }
+}
+
+__global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_abort;
+  const int B = a.B;
+  const int nstage = f4::dn_nstages(B), stage = f4::dn_stage(B);
+  float* red = reinterpret_cast<float*>(smem + nstage * stage);
+  float* acc = red + f4::DN_RED;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(acc + B * f4::RS);
+  Pipe p;
+  init_pipe(p, smem, stage, nstage, bars, f4::DN_MAX_STAGES, &s_abort, a.ws.hdr);
+  for (int i = threadIdx.x; i < B * f4::RS; i += blockDim.x) acc[i] = 0.f;
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int n_groups = (int)__ldcg(&a.ws.hdr->n_groups);
+  const int r0 = blockIdx.x * f4::RS;
+  p.deadline = wait_deadline(a.ws.hdr);
+  if ((threadIdx.x >> 5) == f4::CWARPS) {
+    if ((threadIdx.x & 31) == 0) dn_produce(p, a, n_groups, r0);
+    return;
+  }
+  bool ok = true;
+  for (int gi = 0; gi < n_groups; ++gi) {
+    const int4 grp = __ldcg(a.ws.groups + gi);
+    const int slot = gi % nstage;
+    if (ok) ok = wait_full(p, slot, (uint32_t)(gi / nstage) & 1u);
+    const uint8_t* st = p.stages + slot * stage;
+    const int n = ok ? grp.z : 0;
+    switch ((grp.z + 7) >> 3) {  // uniform across the consumer warps
+      case 1: dn_group<1>(a, st, red, acc, grp.x, grp.y, n); break;
+      case 2: dn_group<2>(a, st, red, acc, grp.x, grp.y, n); break;
+      default: dn_group<3>(a, st, red, acc, grp.x, grp.y, n); break;
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar(p, slot));
+  }
+  named_sync(1, f4::CWARPS * 32);
+  if (!ok) return;
+  for (int i = threadIdx.x; i < B * f4::RS; i += f4::CWARPS * 32) {
+    const int t = i / f4::RS, r = i % f4::RS;
+    const size_t o = (size_t)t * H + r0 + r;
+    a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + acc[i]);
+  }
+}
+
+cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gateup_nvfp4_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f4::GU_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms, 1, 1);
+  cfg.blockDim = dim3(f4::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = f4::GU_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gateup_nvfp4_kernel, a);
+}
+
+cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(down_nvfp4_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, f4::SMEM_CAP);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(H / f4::RS, 1, 1);
+  cfg.blockDim = dim3(f4::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = f4::dn_smem(a.B);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, down_nvfp4_kernel, a);
+}
+
+}  // namespace flint

@@ -1,0 +1,110 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, sizes workspaces, and rejects bad arguments on the host
+before any CUDA call."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_decode_sigmoid_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from moe_decode_sigmoid_gb300 import build
+    build.build()
+    return m.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "flint_moe.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const char\*|size_t|flint_status)\s+(flint_\w+)\s*\(",
+                                 src, re.M)))
+
+
+def test_header_declarations_match_binding_list():
+    assert sorted(m.EXPORTS) == _declared()
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code, name in [(0, "FLINT_OK"), (1, "FLINT_ERR_INVALID_ARG"), (2, "FLINT_ERR_UNSUPPORTED"),
+                       (3, "FLINT_ERR_WORKSPACE"), (4, "FLINT_ERR_CUDA"),
+                       (5, "FLINT_ERR_DEVICE_TIMEOUT")]:
+        assert m.status_string(code) == name
+    assert m.status_string(99) == "FLINT_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(L):
+    a = m.flint_moe_workspace_bytes(1)
+    b = m.flint_moe_workspace_bytes(128)
+    c = m.flint_moe_workspace_bytes(256)
+    assert 0 < a < b < c
+    assert (b - a) == 127 * 7 * 512 * 4   # only the fp32 h rows grow with the batch
+    assert a % 256 == 0 and b % 256 == 0
+    assert m.flint_moe_workspace_bytes(0) == 0
+    assert m.flint_moe_workspace_bytes(257) == 0
+    bad = m.Dims(2048, 256, 6, 256, 1)
+    assert m.flint_moe_workspace_bytes(8, bad) == 0
+
+
+# Fake device addresses: validation fails before anything is dereferenced.
+A = 0x100000
+WS = 0x7000000
+
+
+def _decode(L, dims=None, batch=1, x=A, res=A + 0x10000, wr=A, bias=None, w13=A, w2=A, ws13=A,
+            ws2=A, out=A + 0x20000, idx=None, w=None, ws=WS, wsb=None):
+    if wsb is None:
+        wsb = m.flint_moe_workspace_bytes(max(1, min(batch, 256)))
+    d = ctypes.byref(dims if dims is not None else m.FULL_DIMS)
+    return L.flint_moe_decode_bf16(d, batch, x, res, wr, bias, w13, w2, ws13, ws2, out, idx, w,
+                                   ws, wsb, None)
+
+
+def test_decode_rejects_bad_arguments_before_launch(L):
+    assert _decode(L, dims=m.Dims(2048, 128, 6, 512, 1)) == m.FLINT_ERR_UNSUPPORTED
+    assert _decode(L, dims=m.Dims(4096, 256, 6, 512, 1)) == m.FLINT_ERR_UNSUPPORTED
+    assert _decode(L, dims=m.Dims(2048, 256, 8, 512, 1)) == m.FLINT_ERR_UNSUPPORTED
+    assert _decode(L, batch=0) == m.FLINT_ERR_INVALID_ARG
+    assert _decode(L, batch=257, wsb=1 << 30) == m.FLINT_ERR_INVALID_ARG
+    assert _decode(L, x=None) == m.FLINT_ERR_INVALID_ARG
+    assert _decode(L, x=A + 2) == m.FLINT_ERR_INVALID_ARG            # misaligned
+    assert _decode(L, w13=None) == m.FLINT_ERR_INVALID_ARG
+    assert _decode(L, bias=A + 4) == m.FLINT_ERR_INVALID_ARG         # misaligned optional
+    assert _decode(L, idx=A + 8) == m.FLINT_ERR_INVALID_ARG
+    assert _decode(L, ws=None) == m.FLINT_ERR_WORKSPACE
+    assert _decode(L, ws=WS + 8) == m.FLINT_ERR_WORKSPACE
+    assert _decode(L, batch=8, wsb=m.flint_moe_workspace_bytes(4)) == m.FLINT_ERR_WORKSPACE
+    # out overlapping x, or partially overlapping residual, or the workspace
+    assert _decode(L, out=A + 0x100) == m.FLINT_ERR_INVALID_ARG
+    assert _decode(L, res=A + 0x20000 + 0x10) == m.FLINT_ERR_INVALID_ARG
+    assert _decode(L, out=WS + 0x100) == m.FLINT_ERR_INVALID_ARG
+    d = ctypes.byref(m.FULL_DIMS)
+    assert L.flint_moe_decode_bf16(None, 1, A, A, A, None, A, A, A, A, A, None, None, WS,
+                                   1 << 30, None) == m.FLINT_ERR_INVALID_ARG
+    assert L.flint_moe_decode_nvfp4_w4a16(d, 1, A, A + 0x10000, A, None, *([A] * 11), None,
+                                          A + 0x20000, None, None, WS, 1 << 30,
+                                          None) == m.FLINT_ERR_INVALID_ARG
+
+
+def test_route_bucket_rmsnorm_reject_bad_arguments(L):
+    d = ctypes.byref(m.FULL_DIMS)
+    wsb = m.flint_moe_workspace_bytes(4)
+    assert L.flint_moe_route(d, 4, None, A, None, A, A, WS, wsb, None) == m.FLINT_ERR_INVALID_ARG
+    assert L.flint_moe_route(d, 4, A, A, None, A, A, WS, 16, None) == m.FLINT_ERR_WORKSPACE
+    assert L.flint_moe_bucket(d, 4, A, A, A, None, A, WS, wsb, None) == m.FLINT_ERR_INVALID_ARG
+    assert L.flint_moe_rmsnorm_bf16(d, 4, A, A + 0x100, 1e-6, None) == m.FLINT_ERR_INVALID_ARG
+    assert L.flint_moe_rmsnorm_bf16(d, 4, A, A + 0x10000, -1.0, None) == m.FLINT_ERR_INVALID_ARG
+    assert L.flint_moe_workspace_init(None, wsb, 0, None) == m.FLINT_ERR_WORKSPACE
+    assert L.flint_moe_workspace_init(WS, 64, 0, None) == m.FLINT_ERR_WORKSPACE
+    assert L.flint_moe_debug_arm_stall(None, wsb, None) == m.FLINT_ERR_WORKSPACE

@@ -1,0 +1,324 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Bar (applied to every case):
+  - expert indices bit-exact on every token whose fp64 gap between the 6th and
+    7th logit is >= TAU; on the rare near-tie token the GPU's set must be a
+    valid top-6 within TAU of the boundary;
+  - routing weights within 1e-5 relative of the oracle's for the GPU's set;
+  - out and the MoE delta (out - residual) within REL_TOL under the error rule
+    of tests/_util.py, against the oracle evaluated on the GPU's expert set.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import flint_synth as fs
+import oracle
+from tests._util import REL_TOL, TAU, bf16_bits_to_f64, rel_err, topk_margin
+
+pytestmark = pytest.mark.gpu
+
+D = fs.FULL
+K = D.top_k
+
+
+@pytest.fixture(scope="module")
+def m():
+    from moe_decode_sigmoid_gb300 import build
+    build.build()
+    import moe_decode_sigmoid_gb300 as mod
+    mod.lib()
+    return mod
+
+
+@pytest.fixture(scope="module")
+def layer():
+    dev = torch.device("cuda:0")
+    W = fs.layer_weights(1001, D, device=dev)
+    host = {k: v.cpu() for k, v in W.items()}
+    return W, host
+
+
+@pytest.fixture(scope="module")
+def ws(m):
+    return m.new_workspace(256)
+
+
+def run_decode(m, W, x, res, bias, ws, out=None):
+    B = x.shape[0]
+    out = torch.empty_like(res) if out is None else out
+    idx = torch.full((B, K), -1, dtype=torch.int32, device=x.device)
+    w = torch.zeros((B, K), dtype=torch.float32, device=x.device)
+    m.flint_moe_decode_bf16(x, res, W["wr"], bias, W["w13"], W["w2"], W["ws13"], W["ws2"], out,
+                            ws, idx, w)
+    torch.cuda.synchronize()
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_OK
+    return out, idx, w
+
+
+def check_routing(host, x, bias, idx, w):
+    """Returns the oracle weights for the GPU's expert set (f64 [B,k])."""
+    ref_idx, _, logits = oracle.route(D, x.cpu(), host["wr"], None if bias is None else bias.cpu())
+    gi = idx.cpu().numpy().astype(np.int64)
+    margin = topk_margin(logits, K)
+    clear = margin >= TAU
+    np.testing.assert_array_equal(gi[clear], ref_idx[clear])
+    for t in np.nonzero(~clear)[0]:   # near-tie tokens: a valid top-k within TAU
+        s = -np.sort(-logits[t])
+        sel = logits[t, gi[t]]
+        assert len(set(gi[t].tolist())) == K
+        assert sel.min() >= s[K - 1] - TAU
+        assert np.all(np.diff(sel) <= TAU)
+    L = np.take_along_axis(logits, gi, axis=1)
+    s = 1.0 / (1.0 + np.exp(-L))
+    w_ref = s / s.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=1e-5, atol=0)
+    return gi.astype(np.int32), w_ref
+
+
+def check_layer(host, x, res, bias, out, idx, w):
+    gi, w_ref = check_routing(host, x, bias, idx, w)
+    ref = oracle.moe_bf16_given_routing(D, x.cpu(), res.cpu(), gi, w_ref, host["w13"], host["w2"],
+                                        host["ws13"], host["ws2"])
+    got = bf16_bits_to_f64(out)
+    r = bf16_bits_to_f64(res)
+    e_out = rel_err(got, ref)
+    e_delta = rel_err(got - r, ref - r)
+    assert e_out <= REL_TOL and e_delta <= REL_TOL, (e_out, e_delta)
+    return e_delta
+
+
+ROUTE_CASES = [(1, False), (5, False), (8, False), (64, True), (128, True), (256, False)]
+
+
+@pytest.mark.parametrize("B,with_bias", ROUTE_CASES)
+def test_route_matches_oracle(m, layer, ws, B, with_bias):
+    W, host = layer
+    x, _ = fs.tokens(3000 + B, B, device="cuda")
+    bias = fs.logit_offsets(1003, device="cuda") if with_bias else None
+    idx = torch.full((B, K), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((B, K), dtype=torch.float32, device="cuda")
+    m.flint_moe_route(x, W["wr"], bias, idx, w, ws)
+    torch.cuda.synchronize()
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_OK
+    check_routing(host, x, bias, idx, w)
+
+
+@pytest.mark.parametrize("B", [1, 8, 37, 128, 256])
+def test_bucket_matches_oracle(m, layer, ws, B):
+    W, host = layer
+    x, _ = fs.tokens(3100 + B, B, device="cuda")
+    bias = fs.logit_offsets(1003, device="cuda")
+    ref_idx, _, _ = oracle.route(D, x.cpu(), host["wr"], bias.cpu())
+    u_ref, off_ref, pairs_ref = oracle.bucket(ref_idx, D.n_experts)
+    dev_idx = torch.from_numpy(ref_idx).cuda()
+    uniq = torch.full((256,), -7, dtype=torch.int32, device="cuda")
+    offsets = torch.full((257,), -7, dtype=torch.int32, device="cuda")
+    pairs = torch.full((B * K,), -7, dtype=torch.int32, device="cuda")
+    n = torch.zeros((4,), dtype=torch.int32, device="cuda")
+    m.flint_moe_bucket(dev_idx, uniq, offsets, pairs, n, ws)
+    torch.cuda.synchronize()
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_OK
+    U = int(n[0])
+    assert U == len(u_ref)
+    np.testing.assert_array_equal(uniq[:U].cpu().numpy(), u_ref)
+    np.testing.assert_array_equal(offsets[:U + 1].cpu().numpy(), off_ref)
+    np.testing.assert_array_equal(pairs.cpu().numpy(), pairs_ref)
+
+
+DECODE_CASES = [(1, False), (2, False), (3, False), (5, False), (8, False), (13, False),
+                (31, True), (32, True), (77, True), (128, True), (128, False)]
+
+
+@pytest.mark.parametrize("B,with_bias", DECODE_CASES)
+def test_decode_bf16_matches_oracle(m, layer, ws, B, with_bias):
+    W, host = layer
+    x, res = fs.tokens(2000 + B, B, device="cuda")
+    bias = fs.logit_offsets(1003, device="cuda") if with_bias else None
+    out, idx, w = run_decode(m, W, x, res, bias, ws)
+    check_layer(host, x, res, bias, out, idx, w)
+
+
+def test_zero_input_gives_lowest_experts_and_residual_bitwise(m, layer, ws):
+    W, _ = layer
+    B = 4
+    _, res = fs.tokens(11, B, device="cuda")
+    x = torch.zeros_like(res)
+    out, idx, w = run_decode(m, W, x, res, None, ws)
+    assert torch.equal(idx.cpu(), torch.arange(K, dtype=torch.int32).repeat(B, 1))
+    assert torch.all(w.cpu() == 1.0 / K)
+    assert torch.equal(out.view(torch.int16), res.view(torch.int16))
+
+
+def test_planted_router_ties_pick_lower_index(m, layer, ws):
+    """x = sqrt(H) e_0 (45.25, exact in bf16) and a router whose column 0 holds
+    planted duplicates at the 6/7 boundary: logits are single exact products, so
+    both sides see exact ties and the lower index must win."""
+    W, host = layer
+    H, E = D.hidden, D.n_experts
+    col = torch.zeros(E)
+    col[[200, 13, 77, 5]] = torch.tensor([4.0, 3.0, 2.5, 2.0])
+    col[[250, 9, 130, 64]] = 1.5      # four-way tie for the last two slots
+    wr = torch.zeros((E, H))
+    wr[:, 0] = col
+    wr = wr.to(torch.bfloat16)
+    x = torch.zeros((2, H))
+    x[:, 0] = 45.25
+    x = x.to(torch.bfloat16)
+    _, res = fs.tokens(12, 2)
+    Wt = dict(W)
+    Wt["wr"] = wr.cuda()
+    out, idx, w = run_decode(m, Wt, x.cuda(), res.cuda(), None, ws)
+    expect = [200, 13, 77, 5, 9, 64]
+    assert idx.cpu().tolist() == [expect, expect]
+    ref_idx, _, _ = oracle.route(D, x, wr, None)
+    assert ref_idx.tolist() == [expect, expect]
+    hostt = dict(host)
+    hostt["wr"] = wr
+    check_layer(hostt, x.cuda(), res.cuda(), None, out, idx, w)
+
+
+def test_token_permutation_permutes_outputs_bitwise(m, layer, ws):
+    W, _ = layer
+    B = 24
+    x, res = fs.tokens(13, B, device="cuda")
+    perm = torch.randperm(B, generator=torch.Generator().manual_seed(0)).cuda()
+    out, idx, _ = run_decode(m, W, x, res, None, ws)
+    out_p, idx_p, _ = run_decode(m, W, x[perm].contiguous(), res[perm].contiguous(), None, ws)
+    assert torch.equal(idx_p, idx[perm])
+    assert torch.equal(out_p.view(torch.int16), out[perm].view(torch.int16))
+
+
+def test_batch_invariance(m, layer, ws):
+    W, host = layer
+    B = 16
+    x, res = fs.tokens(14, B, device="cuda")
+    out, idx, _ = run_decode(m, W, x, res, None, ws)
+    for t in (0, 7, 15):
+        o1, i1, _ = run_decode(m, W, x[t:t + 1].contiguous(), res[t:t + 1].contiguous(), None, ws)
+        assert torch.equal(i1[0], idx[t])
+        ref = bf16_bits_to_f64(out[t:t + 1])
+        assert rel_err(bf16_bits_to_f64(o1), ref) <= REL_TOL
+
+
+def test_in_place_residual_and_repeat_determinism(m, layer, ws):
+    W, _ = layer
+    B = 8
+    x, res = fs.tokens(15, B, device="cuda")
+    out1, _, _ = run_decode(m, W, x, res, None, ws)
+    out2, _, _ = run_decode(m, W, x, res, None, ws)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    buf = res.clone()
+    run_decode(m, W, x, buf, None, ws, out=buf)   # out aliases residual exactly
+    assert torch.equal(buf.view(torch.int16), out1.view(torch.int16))
+
+
+def test_cuda_graph_replay_matches_eager(m, layer):
+    W, _ = layer
+    B = 8
+    ws = m.new_workspace(B)
+    x, res = fs.tokens(16, B, device="cuda")
+    out_e, _, _ = run_decode(m, W, x, res, None, ws)
+    out = torch.empty_like(res)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        m.flint_moe_decode_bf16(x, res, W["wr"], None, W["w13"], W["w2"], W["ws13"], W["ws2"],
+                                out, ws, stream=s)   # warm-up outside capture
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            m.flint_moe_decode_bf16(x, res, W["wr"], None, W["w13"], W["w2"], W["ws13"], W["ws2"],
+                                    out, ws, stream=s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_OK
+    assert torch.equal(out.view(torch.int16), out_e.view(torch.int16))
+
+
+def test_stuck_wait_reports_timeout_and_workspace_recovers(m, layer):
+    """The stall hook makes one device wait on a flag nothing sets; the wait
+    runs out after the (short) limit, the call reports a timeout instead of
+    hanging, and after re-initialisation the next call is correct."""
+    W, host = layer
+    B = 2
+    ws = m.new_workspace(B, wait_limit_ns=20_000_000)   # 20 ms
+    x, res = fs.tokens(17, B, device="cuda")
+    m.flint_moe_debug_arm_stall(ws)
+    out = torch.empty_like(res)
+    m.flint_moe_decode_bf16(x, res, W["wr"], None, W["w13"], W["w2"], W["ws13"], W["ws2"], out, ws)
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_ERR_DEVICE_TIMEOUT
+    m.flint_moe_workspace_init(ws)
+    out, idx, w = run_decode(m, W, x, res, None, ws)
+    check_layer(host, x, res, None, out, idx, w)
+
+
+def test_bucket_reports_bad_routing(m, ws):
+    B = 2
+    bad = torch.tensor([[0, 1, 2, 3, 4, 4], [0, 1, 2, 3, 4, 300]], dtype=torch.int32).cuda()
+    z = lambda n: torch.zeros((n,), dtype=torch.int32, device="cuda")  # noqa: E731
+    m.flint_moe_bucket(bad, z(256), z(257), z(B * K), z(4), ws)
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_ERR_INVALID_ARG
+    m.flint_moe_workspace_init(ws)
+
+
+def test_rmsnorm_matches_oracle(m):
+    B = 37
+    x, _ = fs.tokens(18, B, device="cuda")
+    y = (x.float() * 3.0).to(torch.bfloat16)
+    out = torch.empty_like(y)
+    m.flint_moe_rmsnorm_bf16(y, out, 1e-6)
+    torch.cuda.synchronize()
+    ref = oracle.rmsnorm(y.cpu(), 1e-6)
+    got = bf16_bits_to_f64(out)
+    assert np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1e-3)) <= 2 ** -8
+
+
+# ---------------------------------------------------------------- NVFP4 (W4A16)
+
+@pytest.fixture(scope="module")
+def nv_layer(layer):
+    W, _ = layer
+    nv = fs.nvfp4_layer(W)
+    torch.cuda.synchronize()
+    return nv, {k: v.cpu() for k, v in nv.items()}
+
+
+def run_nvfp4(m, W, nv, x, res, bias, ws):
+    B = x.shape[0]
+    out = torch.empty_like(res)
+    idx = torch.full((B, K), -1, dtype=torch.int32, device=x.device)
+    w = torch.zeros((B, K), dtype=torch.float32, device=x.device)
+    m.flint_moe_decode_nvfp4_w4a16(x, res, W["wr"], bias, nv, out, ws, idx, w)
+    torch.cuda.synchronize()
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_OK
+    return out, idx, w
+
+
+@pytest.mark.parametrize("B,with_bias", [(1, False), (3, False), (8, False), (13, False),
+                                          (32, True), (128, True)])
+def test_decode_nvfp4_matches_oracle(m, layer, nv_layer, ws, B, with_bias):
+    W, host = layer
+    nv, nv_host = nv_layer
+    x, res = fs.tokens(4000 + B, B, device="cuda")
+    bias = fs.logit_offsets(1003, device="cuda") if with_bias else None
+    out, idx, w = run_nvfp4(m, W, nv, x, res, bias, ws)
+    gi, w_ref = check_routing(host, x, bias, idx, w)
+    ref = oracle.moe_nvfp4_given_routing(D, x.cpu(), res.cpu(), gi, w_ref, nv_host)
+    got = bf16_bits_to_f64(out)
+    r = bf16_bits_to_f64(res)
+    e_out, e_delta = rel_err(got, ref), rel_err(got - r, ref - r)
+    assert e_out <= REL_TOL and e_delta <= REL_TOL, (e_out, e_delta)
+
+
+def test_nvfp4_zero_input_residual_bitwise(m, layer, nv_layer, ws):
+    W, _ = layer
+    nv, _ = nv_layer
+    _, res = fs.tokens(19, 3, device="cuda")
+    out, idx, _ = run_nvfp4(m, W, nv, torch.zeros_like(res), res, None, ws)
+    assert torch.equal(idx.cpu(), torch.arange(K, dtype=torch.int32).repeat(3, 1))
+    assert torch.equal(out.view(torch.int16), res.view(torch.int16))
