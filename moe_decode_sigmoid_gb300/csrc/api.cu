@@ -192,6 +192,10 @@ static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const vo
   a.w = w;
   a.B = batch;
   a.ws = r.ws;
+  // The router starts only after everything before it on the stream is done,
+  // and lets the gate/up kernel launch early: the shared expert, which does not
+  // depend on routing, is then computed while the router runs.
+  a.early_shared = 1;
   e = nvfp4 ? launch_gateup_nvfp4(a, stream, sms) : launch_gateup_bf16(a, stream, sms);
   if (e != cudaSuccess) return cuda_status(e);
   e = nvfp4 ? launch_down_nvfp4(a, stream) : launch_down_bf16(a, stream);

@@ -15,8 +15,9 @@
 // of Wd (16 KiB) plus the group's h rows (fp32) through a shared-memory ring
 // with cp.async.bulk; per-token accumulators live in shared memory.
 //   <= 4 tokens: CUDA cores, warp w owns rows 2w and 2w+1.
-//   5..24 tokens: mma.sync m16n8k16 with Wd rows as M and tokens as N (h is
-//      rounded to bf16 for the MMA operand), warp w owns a 64-column K-slice.
+//   5..24 tokens: mma.sync m16n8k16 with Wd rows as M and tokens as N; the
+//      fp32 h is split into two bf16 parts (hi + lo, two MMAs) so the operand
+//      keeps ~16 significant bits; warp w owns a 64-column K-slice.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -137,17 +138,20 @@ __device__ __forceinline__ void group_mma(const DnCtx& c, const uint8_t* st, int
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int slot = nt * 8 + g;
-      uint32_t b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+      // h (fp32) = hi + lo with both parts bf16: two MMAs keep ~16 bits of h.
+      uint32_t b[4] = {0u, 0u, 0u, 0u}, l[4] = {0u, 0u, 0u, 0u};
       if (slot < n) {
         const float4 h0 = *reinterpret_cast<const float4*>(hs + slot * dn::HSTRIDE + kb * 128);
         const float4 h1 = *reinterpret_cast<const float4*>(hs + slot * dn::HSTRIDE + kb * 128 + 16);
-        b0 = pack_bf2(h0.x, h0.y);
-        b1 = pack_bf2(h0.z, h0.w);
-        b2 = pack_bf2(h1.x, h1.y);
-        b3 = pack_bf2(h1.z, h1.w);
+        split_bf2(h0.x, h0.y, b[0], l[0]);
+        split_bf2(h0.z, h0.w, b[1], l[1]);
+        split_bf2(h1.x, h1.y, b[2], l[2]);
+        split_bf2(h1.z, h1.w, b[3], l[3]);
       }
-      mma_bf16(acc[nt], alo.x, ahi.x, alo.y, ahi.y, b0, b1);
-      mma_bf16(acc[nt], alo.z, ahi.z, alo.w, ahi.w, b2, b3);
+      mma_bf16(acc[nt], alo.x, ahi.x, alo.y, ahi.y, b[0], b[1]);
+      mma_bf16(acc[nt], alo.z, ahi.z, alo.w, ahi.w, b[2], b[3]);
+      mma_bf16(acc[nt], alo.x, ahi.x, alo.y, ahi.y, l[0], l[1]);
+      mma_bf16(acc[nt], alo.z, ahi.z, alo.w, ahi.w, l[2], l[3]);
     }
   }
   float* red = c.red + warp * dn::RS * GROUP_MAX;

@@ -94,13 +94,14 @@ __device__ __forceinline__ void dot8x2(const uint4& wg, const uint4& wu, const u
 // group's activations are staged once in shared memory (xs, which aliases the
 // tensor-core reduction buffer; segments are separated by consumer barriers).
 template <int NTOK>
-__device__ __forceinline__ void seg_cc(const GuCtx& c, int u0, int u1, int pair0, int& it, bool& ok) {
+__device__ __forceinline__ void seg_cc(const GuCtx& c, int u0, int u1, int pair0, int tok_base,
+                                       int& it, bool& ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint4* xs = reinterpret_cast<uint4*>(c.red);
   named_sync(1, gu::CWARPS * 32);  // previous segment is done with xs
 #pragma unroll
   for (int i = 0; i < NTOK; ++i) {
-    const int tok = __ldcg(c.pair_tok + pair0 + i);
+    const int tok = tok_base >= 0 ? tok_base + i : __ldcg(c.pair_tok + pair0 + i);
     const uint4* row = reinterpret_cast<const uint4*>(c.x + (size_t)tok * H);
     xs[i * (H / 8) + threadIdx.x] = __ldg(row + threadIdx.x);  // 256 threads x 16 B = one row
   }
@@ -142,7 +143,8 @@ __device__ __forceinline__ void seg_cc(const GuCtx& c, int u0, int u1, int pair0
 
 // Tensor-core segment: units [u0, u1) of one group with n tokens, NT = ceil(n/8).
 template <int NT>
-__device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair0, int n, int& it, bool& ok) {
+__device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair0, int n,
+                                        int tok_base, int& it, bool& ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   named_sync(1, gu::CWARPS * 32);  // a preceding CUDA-core segment is done with xs
@@ -151,7 +153,7 @@ __device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair
   for (int nt = 0; nt < NT; ++nt) {
     const int slot = nt * 8 + g;
     if (slot < n) {
-      const int tok = __ldcg(c.pair_tok + pair0 + slot);
+      const int tok = tok_base >= 0 ? tok_base + slot : __ldcg(c.pair_tok + pair0 + slot);
       const uint16_t* row = c.x + (size_t)tok * H + warp * 128 + q * 8;
 #pragma unroll
       for (int kh = 0; kh < 2; ++kh)
@@ -221,44 +223,139 @@ __device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair
   }
 }
 
-__device__ __forceinline__ void produce(const GuCtx& c, const int4* groups, const uint16_t* w13,
-                        const uint16_t* ws13, int u_begin, int u_end) {
-  int it = 0;
-  for (int u = u_begin; u < u_end; ++u) {
-    const int4 grp = __ldcg(groups + (u / gu::UNITS));
-    const int blk = u & (gu::UNITS - 1);
-    const uint16_t* base = grp.x < E ? w13 + (size_t)grp.x * (2 * I) * H
-                                     : ws13 + (size_t)(grp.x - E) * (2 * I) * H;
-    bool stop = false;
+// Issues the two stages of one unit (8 gate + 8 up rows of expert `e`, block
+// `blk`); false if the ring could not be acquired (abort).
+__device__ __forceinline__ bool issue_unit(const GuCtx& c, const uint16_t* base, int blk, int& it) {
 #pragma unroll 1
-    for (int kh = 0; kh < 2; ++kh) {
-      const int slot = it % gu::NSTAGE;
-      bool got = true;
-      if (it >= gu::NSTAGE)
-        got = mbar_wait(empty_bar(c, slot), (uint32_t)((it / gu::NSTAGE) - 1) & 1u, c.deadline);
-      // A consumer that gave up sets the flag before releasing its stage.
-      if (!got || *c.abort_flag) {
-        *c.abort_flag = 1;
-        if (!got) set_error(c.hdr, DEV_TIMEOUT);
-        stop = true;
-        break;
-      }
-      mbar_expect_tx(full_bar(c, slot), gu::ROWS * gu::ROW_BYTES);
-      const uint32_t dst = c.stages_addr + slot * gu::STAGE_BYTES;
-#pragma unroll 1
-      for (int r = 0; r < gu::ROWS; ++r) {
-        const int row = (r < 8 ? 0 : I) + blk * 8 + (r & 7);
-        bulk_g2s(dst + r * gu::ROW_STRIDE, base + (size_t)row * H + kh * gu::KS, gu::ROW_BYTES,
-                 full_bar(c, slot));
-      }
-      ++it;
+  for (int kh = 0; kh < 2; ++kh) {
+    const int slot = it % gu::NSTAGE;
+    bool got = true;
+    if (it >= gu::NSTAGE)
+      got = mbar_wait(empty_bar(c, slot), (uint32_t)((it / gu::NSTAGE) - 1) & 1u, c.deadline);
+    // A consumer that gave up sets the flag before releasing its stage.
+    if (!got || *c.abort_flag) {
+      *c.abort_flag = 1;
+      if (!got) set_error(c.hdr, DEV_TIMEOUT);
+      return false;
     }
-    if (stop) break;
+    mbar_expect_tx(full_bar(c, slot), gu::ROWS * gu::ROW_BYTES);
+    const uint32_t dst = c.stages_addr + slot * gu::STAGE_BYTES;
+#pragma unroll 1
+    for (int r = 0; r < gu::ROWS; ++r) {
+      const int row = (r < 8 ? 0 : I) + blk * 8 + (r & 7);
+      bulk_g2s(dst + r * gu::ROW_STRIDE, base + (size_t)row * H + kh * gu::KS, gu::ROW_BYTES,
+               full_bar(c, slot));
+    }
+    ++it;
   }
-  // Never leave the CTA with copies still landing in its shared memory.
+  return true;
+}
+
+// Never leave the CTA with copies still landing in its shared memory.
+__device__ __forceinline__ void drain(const GuCtx& c, int it) {
   const uint64_t drain = globaltimer_ns() + gu::DRAIN_NS;
   for (int j = it - gu::NSTAGE < 0 ? 0 : it - gu::NSTAGE; j < it; ++j)
     mbar_wait(full_bar(c, j % gu::NSTAGE), (uint32_t)(j / gu::NSTAGE) & 1u, drain);
+}
+
+// Which units a CTA runs.  Shared-expert groups do not depend on routing; in
+// the decode chain ("early") they are dealt round-robin over the CTAs and
+// started before the wait for the router, and the routed units are then split
+// so that every CTA ends up with the same total.  Otherwise every group,
+// shared ones included, is split evenly after the wait.
+struct Plan {
+  int nsg;        // shared groups per shared expert
+  int nsu;        // shared units handled before the wait (early only)
+  int r_begin, r_end;
+};
+
+__device__ __forceinline__ int shared_units_below(int c, int nsu, int G) {
+  return c * (nsu / G) + min(c, nsu % G);
+}
+
+__device__ __forceinline__ Plan plan_pre(int B, bool early) {
+  Plan p;
+  p.nsg = (B + GROUP_MAX - 1) / GROUP_MAX;
+  p.nsu = early ? S * p.nsg * gu::UNITS : 0;
+  p.r_begin = p.r_end = 0;
+  return p;
+}
+
+__device__ __forceinline__ void plan_post(Plan& p, int n_groups, bool early) {
+  const int G = gridDim.x, c = blockIdx.x;
+  if (!early) {
+    const int n = n_groups * gu::UNITS;
+    p.r_begin = (int)((long long)c * n / G);
+    p.r_end = (int)((long long)(c + 1) * n / G);
+    return;
+  }
+  const int nru = (n_groups - S * p.nsg) * gu::UNITS;
+  const long long T = (long long)p.nsu + nru;
+  auto R = [&](int cc) {
+    long long r = cc * T / G - shared_units_below(cc, p.nsu, G);
+    return (int)(r < 0 ? 0 : (r > nru ? nru : r));
+  };
+  p.r_begin = R(c);
+  p.r_end = max(p.r_begin, R(c + 1));
+}
+
+// Shared unit j -> (shared expert, group, block) and its pairs / tokens.
+struct SharedUnit {
+  int s, gi, blk, pair0, n, tok0;
+};
+__device__ __forceinline__ SharedUnit shared_unit(int j, int B, int nsg) {
+  SharedUnit u;
+  const int sg = j / gu::UNITS;
+  u.blk = j % gu::UNITS;
+  u.s = sg / nsg;
+  u.gi = sg % nsg;
+  u.tok0 = u.gi * GROUP_MAX;
+  u.n = min(GROUP_MAX, B - u.tok0);
+  u.pair0 = B * TOPK + u.s * B + u.tok0;
+  return u;
+}
+
+__device__ __forceinline__ void produce(const GuCtx& c, const ExpertArgs& a, Plan& pl, bool early) {
+  int it = 0;
+  bool ok = true;
+  for (int j = blockIdx.x; ok && j < pl.nsu; j += gridDim.x) {
+    const SharedUnit su = shared_unit(j, a.B, pl.nsg);
+    ok = issue_unit(c, a.w.ws13 + (size_t)su.s * (2 * I) * H, su.blk, it);
+  }
+  pdl_wait();     // routing and buckets come from the router kernel
+  plan_post(pl, (int)__ldcg(&a.ws.hdr->n_groups), early);
+  for (int u = pl.r_begin; ok && u < pl.r_end; ++u) {
+    const int4 grp = __ldcg(a.ws.groups + (u / gu::UNITS));
+    const uint16_t* base = grp.x < E ? a.w.w13 + (size_t)grp.x * (2 * I) * H
+                                     : a.w.ws13 + (size_t)(grp.x - E) * (2 * I) * H;
+    ok = issue_unit(c, base, u & (gu::UNITS - 1), it);
+  }
+  drain(c, it);
+}
+
+template <bool CC>
+__device__ __forceinline__ void run_segment(const GuCtx& c, int u0, int u1, int pair0, int n,
+                                            int tok_base, int& it, bool& ok) {
+  if (CC) {
+    switch (n) {
+      case 1: seg_cc<1>(c, u0, u1, pair0, tok_base, it, ok); break;
+      case 2: seg_cc<2>(c, u0, u1, pair0, tok_base, it, ok); break;
+      case 3: seg_cc<3>(c, u0, u1, pair0, tok_base, it, ok); break;
+      default: seg_cc<4>(c, u0, u1, pair0, tok_base, it, ok); break;
+    }
+  } else {
+    switch ((n + 7) >> 3) {
+      case 1: seg_mma<1>(c, u0, u1, pair0, n, tok_base, it, ok); break;
+      case 2: seg_mma<2>(c, u0, u1, pair0, n, tok_base, it, ok); break;
+      default: seg_mma<3>(c, u0, u1, pair0, n, tok_base, it, ok); break;
+    }
+  }
+}
+
+__device__ __forceinline__ void segment(const GuCtx& c, int u0, int u1, int pair0, int n,
+                                        int tok_base, int& it, bool& ok) {
+  if (n <= gu::CC_MAX) run_segment<true>(c, u0, u1, pair0, n, tok_base, it, ok);
+  else run_segment<false>(c, u0, u1, pair0, n, tok_base, it, ok);
 }
 
 }  // namespace
@@ -287,39 +384,30 @@ __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs 
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();     // routing and buckets come from the router kernel
-  pdl_trigger();  // the down kernel may start its prologue
-  const int n_units = (int)__ldcg(&a.ws.hdr->n_groups) * gu::UNITS;
-  const int u_begin = (int)((long long)blockIdx.x * n_units / gridDim.x);
-  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
+  const bool early = a.early_shared != 0;
+  Plan pl = plan_pre(a.B, early);
   c.deadline = wait_deadline(a.ws.hdr);
-  const int warp = threadIdx.x >> 5;
-  if (warp == gu::CWARPS) {
-    if ((threadIdx.x & 31) == 0) produce(c, a.ws.groups, a.w.w13, a.w.ws13, u_begin, u_end);
+  if ((threadIdx.x >> 5) == gu::CWARPS) {
+    if ((threadIdx.x & 31) == 0) produce(c, a, pl, early);
+    pdl_trigger();
     return;
   }
   int it = 0;
   bool ok = true;
-  int u = u_begin;
-  while (u < u_end) {
+  for (int j = blockIdx.x; j < pl.nsu; j += gridDim.x) {
+    const SharedUnit su = shared_unit(j, a.B, pl.nsg);
+    // unit numbers inside a segment only serve as block indices (u & 63)
+    segment(c, su.blk, su.blk + 1, su.pair0, su.n, su.tok0, it, ok);
+  }
+  pdl_wait();     // routing and buckets come from the router kernel
+  pdl_trigger();  // the down kernel may start its prologue
+  plan_post(pl, (int)__ldcg(&a.ws.hdr->n_groups), early);
+  int u = pl.r_begin;
+  while (u < pl.r_end) {
     const int gi = u / gu::UNITS;
     const int4 grp = __ldcg(a.ws.groups + gi);
-    const int u1 = min(u_end, (gi + 1) * gu::UNITS);
-    const int n = grp.z, pair0 = grp.y;
-    if (n <= gu::CC_MAX) {
-      switch (n) {
-        case 1: seg_cc<1>(c, u, u1, pair0, it, ok); break;
-        case 2: seg_cc<2>(c, u, u1, pair0, it, ok); break;
-        case 3: seg_cc<3>(c, u, u1, pair0, it, ok); break;
-        default: seg_cc<4>(c, u, u1, pair0, it, ok); break;
-      }
-    } else {
-      switch ((n + 7) >> 3) {
-        case 1: seg_mma<1>(c, u, u1, pair0, n, it, ok); break;
-        case 2: seg_mma<2>(c, u, u1, pair0, n, it, ok); break;
-        default: seg_mma<3>(c, u, u1, pair0, n, it, ok); break;
-      }
-    }
+    const int u1 = min(pl.r_end, (gi + 1) * gu::UNITS);
+    segment(c, u, u1, grp.y, grp.z, -1, it, ok);
     u = u1;
   }
 }

@@ -52,6 +52,7 @@ struct ExpertArgs {
   ExpertW w;
   int B;
   Ws ws;
+  int early_shared;  // gate/up: start the shared expert before the router finishes
 };
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl);

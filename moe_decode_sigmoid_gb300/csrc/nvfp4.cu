@@ -11,9 +11,10 @@
 // The product e2m1 * e4m3 has at most 6 significant bits and lies in
 // [2^-10, 2688], so it is EXACT in f16: each thread converts its fragment's
 // codes with cvt.rn.f16x2.e2m1x2, multiplies by the block scale (f16x2, exact)
-// and feeds mma.sync m16n8k16 f16 x f16 -> fp32.  Activations (bf16 x, fp32 h)
-// are rounded to f16 for the MMA operand; the tensor scale is applied to the
-// fp32 sums.  Dequantisation costs about one instruction per weight, which is
+// and feeds mma.sync m16n8k16 f16 x f16 -> fp32.  bf16 activations convert to
+// f16 exactly (8 significant bits; |x| inside f16's normal range); the fp32 h
+// is split into two f16 parts (hi + lo, two MMAs); the tensor scale is
+// applied to the fp32 sums.  Dequantisation costs about one instruction per weight, which is
 // why this path uses the tensor cores for every group, including single-token
 // ones: the FMAs then cost nothing on the CUDA cores that do the unpacking.
 //
@@ -94,6 +95,14 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// (a, b) = hi + lo, both f16x2.
+__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  const float2 back = __half22float2(h);
+  lo = f16x2_of(a - back.x, b - back.y);
 }
 
 // bf16 x 8 (uint4) -> f16 x 8 (uint4), same element order.
@@ -326,17 +335,20 @@ __device__ __forceinline__ void dn_group(const ExpertArgs& a, const uint8_t* st,
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int slot = nt * 8 + g;
-      uint32_t b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+      // h (fp32) = hi + lo with both parts f16: two MMAs keep ~22 bits of h.
+      uint32_t b[4] = {0u, 0u, 0u, 0u}, r[4] = {0u, 0u, 0u, 0u};
       if (slot < n) {
         const float4 v0 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + kb * 128);
         const float4 v1 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + kb * 128 + 16);
-        b0 = f16x2_of(v0.x, v0.y);
-        b1 = f16x2_of(v0.z, v0.w);
-        b2 = f16x2_of(v1.x, v1.y);
-        b3 = f16x2_of(v1.z, v1.w);
+        split_f16x2(v0.x, v0.y, b[0], r[0]);
+        split_f16x2(v0.z, v0.w, b[1], r[1]);
+        split_f16x2(v1.x, v1.y, b[2], r[2]);
+        split_f16x2(v1.z, v1.w, b[3], r[3]);
       }
-      mma_f16(acc[nt], l0, h0, l1, h1, b0, b1);
-      mma_f16(acc[nt], l2, h2, l3, h3, b2, b3);
+      mma_f16(acc[nt], l0, h0, l1, h1, b[0], b[1]);
+      mma_f16(acc[nt], l2, h2, l3, h3, b[2], b[3]);
+      mma_f16(acc[nt], l0, h0, l1, h1, r[0], r[1]);
+      mma_f16(acc[nt], l2, h2, l3, h3, r[2], r[3]);
     }
   }
   float* rw = red + warp * f4::RS * GROUP_MAX;

@@ -16,7 +16,7 @@ import torch
 
 import flint_synth as fs
 import oracle
-from tests._util import REL_TOL, TAU, bf16_bits_to_f64, rel_err, topk_margin
+from tests._util import REL_TOL, TAU, bf16_bits_to_f64, rel_err, rel_err_delta, topk_margin
 
 pytestmark = pytest.mark.gpu
 
@@ -85,9 +85,9 @@ def check_layer(host, x, res, bias, out, idx, w):
     got = bf16_bits_to_f64(out)
     r = bf16_bits_to_f64(res)
     e_out = rel_err(got, ref)
-    e_delta = rel_err(got - r, ref - r)
+    e_delta = rel_err_delta(got, ref, r)
     assert e_out <= REL_TOL and e_delta <= REL_TOL, (e_out, e_delta)
-    return e_delta
+    return e_out, e_delta
 
 
 ROUTE_CASES = [(1, False), (5, False), (8, False), (64, True), (128, True), (256, False)]
@@ -139,6 +139,21 @@ def test_decode_bf16_matches_oracle(m, layer, ws, B, with_bias):
     bias = fs.logit_offsets(1003, device="cuda") if with_bias else None
     out, idx, w = run_decode(m, W, x, res, bias, ws)
     check_layer(host, x, res, bias, out, idx, w)
+
+
+@pytest.mark.parametrize("B,with_bias", [(1, False), (4, False), (8, False), (24, False),
+                                          (64, True)])
+def test_decode_bf16_zero_residual_pins_expert_path(m, layer, ws, B, with_bias):
+    """residual = 0: out = bf16(MoE delta), so the expert path's own error is
+    visible without the residual's rounding (CUDA-core groups at B <= 4, the
+    tensor-core path for the shared expert from B = 5, both above)."""
+    W, host = layer
+    x, _ = fs.tokens(2100 + B, B, device="cuda")
+    res = torch.zeros_like(x)
+    bias = fs.logit_offsets(1003, device="cuda") if with_bias else None
+    out, idx, w = run_decode(m, W, x, res, bias, ws)
+    e_out, _ = check_layer(host, x, res, bias, out, idx, w)
+    assert e_out <= 8e-3, e_out    # bf16 output rounding is <= 2^-8 relative
 
 
 def test_zero_input_gives_lowest_experts_and_residual_bitwise(m, layer, ws):
@@ -311,7 +326,7 @@ def test_decode_nvfp4_matches_oracle(m, layer, nv_layer, ws, B, with_bias):
     ref = oracle.moe_nvfp4_given_routing(D, x.cpu(), res.cpu(), gi, w_ref, nv_host)
     got = bf16_bits_to_f64(out)
     r = bf16_bits_to_f64(res)
-    e_out, e_delta = rel_err(got, ref), rel_err(got - r, ref - r)
+    e_out, e_delta = rel_err(got, ref), rel_err_delta(got, ref, r)
     assert e_out <= REL_TOL and e_delta <= REL_TOL, (e_out, e_delta)
 
 
