@@ -3,8 +3,9 @@
 
 Headline: one BF16 MoE decode layer (hidden 2048, 256 routed experts, sigmoid
 top-6 + 1 shared, intermediate 512) at batch 8 with i.i.d. unit-RMS tokens,
-timed as CUDA-graph replay with CUDA events, the L2 flushed (512 MiB write)
-between timed steps.  Metric: HBM GB/s over the bytes the layer needs --
+timed as CUDA-graph replay with CUDA events, with a cold L2 for every step
+(default: 8 distinct copies of the layer rotated per step; --l2 flush writes a
+512 MiB buffer between steps instead).  Metric: HBM GB/s over the bytes the layer needs --
 (U+1) experts x 6 MiB + the 1 MiB router, U = distinct selected experts -- and
 the layer latency in microseconds.
 
@@ -37,6 +38,7 @@ EXPERT_BYTES_NVFP4 = 3 * 512 * 2048 // 2 + 3 * 512 * 2048 // 16   # 1,769,472 (+
 GATEUP_BYTES_BF16 = 2 * 512 * 2048 * 2          # 4,194,304
 DOWN_BYTES_BF16 = 512 * 2048 * 2                # 2,097,152
 L2_FLUSH_BYTES = 512 << 20
+SPACER_CYCLES = 100_000
 FALLBACK_HBM_GBS = 6800.0
 LAYER_SEED, TOKEN_SEED, OFFSET_SEED = 1001, 2000, 1003
 
@@ -131,25 +133,54 @@ def stats_us(ms_list):
             "p90": us[int(0.9 * (n - 1))]}
 
 
-class Flusher:
-    """Writes a buffer larger than L2 (cold-L2 timing between steps)."""
+class Cold:
+    """Keeps the L2 cold for every timed step.
 
-    def __init__(self, device):
-        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    rotate (default): R distinct copies of the layer's weights (R x 1.6 GB,
+      inputs far larger than L2); step i uses copy i mod R, so the weights a
+      step reads were last touched R-1 steps (>= 7 x 45 MB > L2) earlier.
+    flush: one copy; before each step a 512 MiB buffer is written (outside the
+      events).  The write leaves ~L2-sized dirty data whose write-back then
+      overlaps the timed step, so this mode over-states the layer's time.
+    """
+
+    def __init__(self, mode, W, device, copies=8):
+        self.mode = mode
+        if mode == "rotate":
+            self.Ws = [W] + [{k: v.clone() for k, v in W.items()} for _ in range(copies - 1)]
+            self.buf = None
+        else:
+            self.Ws = [W]
+            self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
         self.v = 0
 
-    def __call__(self):
-        self.v = (self.v + 1) & 0xFF
-        self.buf.fill_(self.v)
+    def weights(self, i):
+        return self.Ws[i % len(self.Ws)]
+
+    def before(self, i):
+        if self.buf is not None:
+            self.v = (self.v + 1) & 0xFF
+            self.buf.fill_(self.v)
+        else:
+            # A ~50 us spin kernel (no memory traffic) between steps keeps the
+            # GPU busy while the host enqueues the next step, so host launch
+            # latency never lands inside the timed events.
+            torch.cuda._sleep(SPACER_CYCLES)
+
+    def describe(self):
+        if self.mode == "rotate":
+            return ("inputs larger than L2: %d distinct copies of the layer weights (%.1f GB), "
+                    "rotated per step" % (len(self.Ws), len(self.Ws) * 1.618))
+        return "flushed between timed steps (512 MiB write, outside the events)"
 
 
-def timed_steps(fn, steps, warmup, flush, stream, barrier=None, sampler=None):
-    """warmup untimed, then `steps` timed calls, each bracketed by CUDA events on
-    `stream`, L2 flushed before each call (outside the events)."""
+def timed_steps(fn, steps, warmup, cold, stream, barrier=None, sampler=None):
+    """warmup untimed calls, then `steps` timed calls fn(i), each bracketed by
+    CUDA events on `stream`; cold.before(i) runs outside the events."""
     with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            flush()
-            fn()
+        for i in range(warmup):
+            cold.before(i)
+            fn(i)
         torch.cuda.synchronize()
         if barrier:
             barrier()
@@ -159,10 +190,10 @@ def timed_steps(fn, steps, warmup, flush, stream, barrier=None, sampler=None):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
         t0 = time.perf_counter()
-        for s, e in ev:
-            flush()
+        for i, (s, e) in enumerate(ev):
+            cold.before(warmup + i)
             s.record(stream)
-            fn()
+            fn(warmup + i)
             e.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
@@ -173,18 +204,18 @@ def timed_steps(fn, steps, warmup, flush, stream, barrier=None, sampler=None):
 
 
 class BF16Layer:
-    def __init__(self, m, W, B, bias_on, device, seed):
-        self.m, self.W, self.B = m, W, B
+    def __init__(self, m, cold, B, bias_on, device, seed):
+        self.m, self.cold, self.B = m, cold, B
         self.x, self.res = fs.tokens(seed, B, device=device)
         self.bias = fs.logit_offsets(OFFSET_SEED, device=device) if bias_on else None
         self.out = torch.empty_like(self.res)
         self.idx = torch.empty((B, 6), dtype=torch.int32, device=device)
         self.w = torch.empty((B, 6), dtype=torch.float32, device=device)
         self.ws = m.new_workspace(B, device=device)
-        self.graph = None
+        self.graphs = []
 
-    def call(self, stream=None):
-        W = self.W
+    def call(self, i=0, stream=None):
+        W = self.cold.weights(i)
         self.m.flint_moe_decode_bf16(self.x, self.res, W["wr"], self.bias, W["w13"], W["w2"],
                                      W["ws13"], W["ws2"], self.out, self.ws, self.idx, self.w,
                                      stream=stream)
@@ -198,61 +229,76 @@ class BF16Layer:
         return int(torch.unique(self.idx).numel())
 
     def capture(self, stream):
-        g = torch.cuda.CUDAGraph()
+        """One CUDA graph per weight copy."""
+        self.graphs = []
         with torch.cuda.stream(stream):
-            self.call(stream)
-            stream.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                self.call(stream)
-        self.graph = g
-        return g
+            for i in range(len(self.cold.Ws)):
+                self.call(i, stream)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    self.call(i, stream)
+                self.graphs.append(g)
+
+    def replay(self, i):
+        self.graphs[i % len(self.graphs)].replay()
 
 
-def measure_bf16(m, W, B, bias_on, seed, steps, warmup, flush, stream, barrier=None,
-                 sampler=None):
-    L = BF16Layer(m, W, B, bias_on, W["wr"].device, seed)
+def measure_bf16(m, cold, B, bias_on, seed, steps, warmup, stream, barrier=None, sampler=None):
+    L = BF16Layer(m, cold, B, bias_on, cold.Ws[0]["wr"].device, seed)
     U = L.unique_experts()
-    g = L.capture(stream)
-    times, wall, clocks = timed_steps(g.replay, steps, warmup, flush, stream, barrier, sampler)
+    L.capture(stream)
+    times, wall, clocks = timed_steps(L.replay, steps, warmup, cold, stream, barrier, sampler)
     st = stats_us(times)
     nb = needed_bytes_bf16(U)
     return L, U, nb, times, st, wall, clocks
 
 
-def stage_times(m, L, steps, warmup, flush, stream):
-    """Per-kernel CUDA-event durations of the three kernels, each launched alone."""
-    W = L.W
+def stage_times(m, L, steps, warmup, stream):
+    """Per-kernel CUDA-event durations of the three kernels, each launched alone
+    on `stream` (route -> gate/up -> down on a routed workspace)."""
+    cold = L.cold
     idx = torch.empty_like(L.idx)
     w = torch.empty_like(L.w)
     out = torch.empty_like(L.res)
-    route = lambda: m.flint_moe_route(L.x, W["wr"], L.bias, idx, w, L.ws, stream=stream)  # noqa
-    gate = lambda: m.flint_moe_gateup_bf16(L.x, W["w13"], W["ws13"], L.ws, stream=stream)  # noqa
-    down = lambda: m.flint_moe_down_bf16(L.res, W["w2"], W["ws2"], out, L.ws, stream=stream)  # noqa
+
+    def route(i):
+        W = cold.weights(i)
+        m.flint_moe_route(L.x, W["wr"], L.bias, idx, w, L.ws, stream=stream)
+
+    def gate(i):
+        W = cold.weights(i)
+        m.flint_moe_gateup_bf16(L.x, W["w13"], W["ws13"], L.ws, stream=stream)
+
+    def down(i):
+        W = cold.weights(i)
+        m.flint_moe_down_bf16(L.res, W["w2"], W["ws2"], out, L.ws, stream=stream)
+
     res = {}
     for name, fn in (("router", route), ("gateup", gate), ("down", down)):
         with torch.cuda.stream(stream):
-            route()
-            gate()
-        times, _, _ = timed_steps(fn, steps, warmup, flush, stream)
+            route(0)
+            gate(0)
+        times, _, _ = timed_steps(fn, steps, warmup, cold, stream)
         res[name] = stats_us(times)
     torch.cuda.synchronize()
     return res
 
 
-def e2e_measure(m, L, steps, warmup, flush, stream):
+def e2e_measure(m, L, steps, warmup, stream):
     """Same layer through the public call with host buffers: pinned H2D of x and
     residual, the decode call, D2H of out -- all inside the events."""
     xh = L.x.cpu().pin_memory()
     rh = L.res.cpu().pin_memory()
     oh = torch.empty_like(L.out, device="cpu").pin_memory()
 
-    def step():
+    def step(i):
         L.x.copy_(xh, non_blocking=True)
         L.res.copy_(rh, non_blocking=True)
-        L.call(stream)
+        L.call(i, stream)
         oh.copy_(L.out, non_blocking=True)
 
-    times, _, _ = timed_steps(step, steps, warmup, flush, stream)
+    times, _, _ = timed_steps(step, steps, warmup, L.cold, stream)
     return times, xh.numel() * 2 + rh.numel() * 2, oh.numel() * 2
 
 
@@ -311,19 +357,19 @@ def run_ours(args, world, rank, local, barrier):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
-    flush = Flusher(device)
     peak, peak_kind = peaks()
     B = args.batch
     W = fs.layer_weights(LAYER_SEED, fs.FULL, device=device)
+    cold = Cold(args.l2, W, device)
     sampler = ClockSampler(local)
     L, U, nb, times, st, wall, clocks = measure_bf16(
-        m, W, B, False, TOKEN_SEED + B, args.steps, args.warmup, flush, stream, barrier, sampler)
+        m, cold, B, False, TOKEN_SEED + B, args.steps, args.warmup, stream, barrier, sampler)
     mean_ms = st["mean"] / 1000.0
     t_max = max_over_ranks(mean_ms, world)
     value = world * nb / (t_max / 1e3) / 1e9
 
     roof_steps = min(args.steps, 400)
-    kern = stage_times(m, L, roof_steps, max(3, args.warmup // 4), flush, stream)
+    kern = stage_times(m, L, roof_steps, max(3, args.warmup // 4), stream)
     gate_bytes = (U + 1) * GATEUP_BYTES_BF16 + B * 2048 * 2 + 7 * B * 512 * 4
     achieved = gate_bytes / (kern["gateup"]["mean"] * 1e-6) / 1e9
     traffic = None
@@ -338,7 +384,7 @@ def run_ours(args, world, rank, local, barrier):
             traffic = None
 
     e2e_times, h2d, d2h = e2e_measure(m, L, min(args.steps, 1000), max(3, args.warmup // 4),
-                                      flush, stream)
+                                      stream)
     e2e_mean = stats_us(e2e_times)["mean"]
     e2e_t = max_over_ranks(e2e_mean, world)
     line = {
@@ -359,7 +405,7 @@ def run_ours(args, world, rank, local, barrier):
                         "experts sigmoid top-6 + 1 shared, intermediate 512, N(0,0.02) weights, "
                         "unit-RMS N(0,1) tokens" % B,
             "batch": B, "unique_experts": U, "needed_bytes": nb,
-            "l2": "flushed between timed steps (512 MiB write, outside the events)",
+            "l2": cold.describe(),
             "timing": "CUDA-graph replay of the 3-kernel layer, CUDA events per step",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
@@ -380,7 +426,7 @@ def run_ours(args, world, rank, local, barrier):
         "wall_s_timed": round(wall, 4),
     }
     if args.extras and rank == 0:
-        line["per_config"] = extras(m, W, flush, stream, args)
+        line["per_config"] = extras(m, cold, stream, args)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         W_host = {k: v.cpu() for k, v in W.items()}
         line["cpu_baseline"] = cpu_baseline(L, W_host)
@@ -388,13 +434,13 @@ def run_ours(args, world, rank, local, barrier):
         print(json.dumps(line), flush=True)
 
 
-def extras(m, W, flush, stream, args):
+def extras(m, cold, stream, args):
     """Secondary configurations (reported, not the headline)."""
     out = {}
     steps = max(50, min(args.steps, 500))
     for B, bias_on in ((1, False), (8, False), (32, True), (128, True)):
-        L, U, nb, times, st, _, _ = measure_bf16(m, W, B, bias_on, TOKEN_SEED + B, steps,
-                                                 args.warmup, flush, stream)
+        L, U, nb, times, st, _, _ = measure_bf16(m, cold, B, bias_on, TOKEN_SEED + B, steps,
+                                                 args.warmup, stream)
         out["bf16_b%d%s" % (B, "_skew" if bias_on else "")] = {
             "us": round(st["mean"], 3), "p50_us": round(st["p50"], 3), "unique_experts": U,
             "needed_bytes": nb, "gbs": round(nb / (st["mean"] * 1e-6) / 1e9, 1)}
@@ -465,6 +511,8 @@ def main():
     ap.add_argument("--extras", action="store_true", default=True)
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2", choices=("rotate", "flush"), default="rotate",
+                    help="cold-L2 method between timed steps")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

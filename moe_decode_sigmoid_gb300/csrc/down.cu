@@ -12,8 +12,9 @@
 // walks all groups in order, so each weight byte is read by exactly one CTA,
 // the combine needs no atomics, and the summation order is fixed (results are
 // bitwise reproducible).  The producer streams, per group, the CTA's 16 rows
-// of Wd (16 KiB) plus the group's h rows (fp32) through a shared-memory ring
-// with cp.async.bulk; per-token accumulators live in shared memory.
+// of Wd (one contiguous 16 KiB copy) plus the group's h rows (fp32, one
+// contiguous copy) through a shared-memory ring with cp.async.bulk; per-token
+// accumulators live in shared memory.
 //   <= 4 tokens: CUDA cores, warp w owns rows 2w and 2w+1.
 //   5..24 tokens: mma.sync m16n8k16 with Wd rows as M and tokens as N; the
 //      fp32 h is split into two bf16 parts (hi + lo, two MMAs) so the operand
@@ -25,10 +26,10 @@ namespace flint {
 namespace dn {
 constexpr int RS = 16;                    // output rows per CTA
 constexpr int WROW = I * 2;               // bytes of one Wd row
-constexpr int WSTRIDE = WROW + 64;        // 64 mod 128
-constexpr int WBYTES = RS * WSTRIDE;
+constexpr int WSTRIDE = WROW;             // the 16 rows are one contiguous copy
+constexpr int WBYTES = RS * WSTRIDE;      // 16 KiB
 constexpr int HROW = I * 4;               // bytes of one fp32 h row
-constexpr int HSTRIDE = HROW + 64;
+constexpr int HSTRIDE = HROW;             // the group's h rows are one contiguous copy
 constexpr int CWARPS = 8;
 constexpr int THREADS = CWARPS * 32 + 32;
 constexpr int RED_FLOATS = CWARPS * RS * GROUP_MAX;
@@ -197,13 +198,8 @@ __device__ void produce(const DnCtx& c, const int4* groups, int n_groups, const 
     const uint32_t dst = c.stages_addr + slot * c.stage_bytes;
     const uint16_t* wb = (grp.x < E ? w2 + (size_t)grp.x * H * I : ws2 + (size_t)(grp.x - E) * H * I) +
                          (size_t)r0 * I;
-#pragma unroll 1
-    for (int r = 0; r < dn::RS; ++r)
-      bulk_g2s(dst + r * dn::WSTRIDE, wb + (size_t)r * I, dn::WROW, full_bar(c, slot));
-#pragma unroll 1
-    for (int i = 0; i < n; ++i)
-      bulk_g2s(dst + dn::WBYTES + i * dn::HSTRIDE, h + (size_t)(grp.y + i) * I, dn::HROW,
-               full_bar(c, slot));
+    bulk_g2s(dst, wb, dn::WBYTES, full_bar(c, slot));
+    bulk_g2s(dst + dn::WBYTES, h + (size_t)grp.y * I, n * dn::HROW, full_bar(c, slot));
     ++it;
   }
   const uint64_t drain = globaltimer_ns() + dn::DRAIN_NS;

@@ -8,24 +8,23 @@
 // for Recursive's Flint, "Optimization Strategies").
 //
 // Work unit: one group x one block of 8 intermediate rows = the 8 gate rows
-// plus the 8 matching up rows (64 KiB of weights).  Units are numbered
-// group-major and each CTA takes one contiguous range of them, so every SM
-// streams the same number of weight bytes.
+// plus the 8 matching up rows: two contiguous 32 KiB runs of w13.  Each CTA
+// (one per SM) takes an equal share of the units.
 //
 // Per CTA: 8 consumer warps + 1 producer warp.  The producer's elected lane
-// streams each unit as two 32 KiB stages (16 rows x 1024 columns) through a
-// 6-stage shared-memory ring with cp.async.bulk (TMA) and mbarriers, so up to
-// ~200 KiB per SM is in flight at once.  Rows land at a 2112-byte stride
-// (= 64 mod 128) so the tensor-core fragment loads are bank-conflict free.
-// Consumers, per group:
+// streams each unit as one 64 KiB stage -- two cp.async.bulk copies -- through
+// a 3-stage shared-memory ring with full/empty mbarriers, so 192 KiB per SM is
+// in flight.  Consumers, per group:
 //   <= 4 tokens (the batch-1/8 case): CUDA cores.  Warp w owns gate row w and
-//      up row w of the stage; each lane keeps its slice of the group's
-//      activations in registers for the whole group and accumulates fp32.
+//      up row w; the group's activations are staged once as fp32 in shared
+//      memory; each lane keeps one independent fp32 partial sum per 16-byte
+//      chunk so the FMA chains overlap.
 //   5..24 tokens: mma.sync m16n8k16 (bf16 in, fp32 acc) with the 16 weight
-//      rows as M and the tokens as N; warp w owns a 128-column K-slice; the
-//      8 partial tiles are summed through shared memory.  Because each
-//      fragment's K order is the same permutation for weights and
-//      activations, both are loaded as plain 16-byte row chunks.
+//      rows as M (8 gate + 8 up: the same thread then holds g and u) and the
+//      tokens as N; warp w owns a 256-column K-slice; the 8 partial tiles are
+//      summed through shared memory.  Because each fragment's K order is the
+//      same permutation for weights and activations, both are loaded as plain
+//      16-byte row chunks.
 // Every wait is bounded by the workspace's limit.
 #include "common.cuh"
 #include "kernels.h"
@@ -33,19 +32,19 @@
 namespace flint {
 namespace gu {
 constexpr int ROWS = 16;                        // 8 gate + 8 up rows
-constexpr int KS = 1024;                        // columns per stage
-constexpr int ROW_BYTES = KS * 2;               // bf16
-constexpr int ROW_STRIDE = ROW_BYTES + 64;      // 64 mod 128
-constexpr int STAGE_BYTES = ROWS * ROW_STRIDE;  // 33,792
-constexpr int NSTAGE = 6;
+constexpr int ROW_BYTES = H * 2;                // 4 KiB (bf16)
+constexpr int STAGE_BYTES = ROWS * ROW_BYTES;   // 64 KiB
+constexpr int NSTAGE = 3;
 constexpr int UNITS = I / 8;                    // units per group
 constexpr int CWARPS = 8;
 constexpr int THREADS = CWARPS * 32 + 32;
 constexpr int CC_MAX = 4;
-// Shared buffer: tensor-core partial tiles, or the CUDA-core path's activations.
-constexpr int RED_FLOATS = (CWARPS * ROWS * GROUP_MAX > CC_MAX * H / 2) ? CWARPS * ROWS * GROUP_MAX
-                                                                        : CC_MAX * H / 2;
-constexpr size_t SMEM = (size_t)NSTAGE * STAGE_BYTES + RED_FLOATS * 4 + 2 * NSTAGE * 8;
+// Shared buffer: tensor-core partial tiles, or the CUDA-core path's fp32
+// activations (CC_MAX x H floats).
+constexpr int RED_FLOATS = CWARPS * ROWS * GROUP_MAX;
+constexpr int XS_FLOATS = CC_MAX * H;
+constexpr int BUF_FLOATS = RED_FLOATS > XS_FLOATS ? RED_FLOATS : XS_FLOATS;
+constexpr size_t SMEM = (size_t)NSTAGE * STAGE_BYTES + BUF_FLOATS * 4 + 2 * NSTAGE * 8;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
 }  // namespace gu
 
@@ -53,7 +52,7 @@ namespace {
 
 struct GuCtx {
   uint8_t* stages;
-  float* red;
+  float* buf;
   uint32_t stages_addr;
   uint32_t full0, empty0;
   uint64_t deadline;
@@ -76,67 +75,81 @@ __device__ __forceinline__ bool wait_full(const GuCtx& c, int slot, uint32_t par
   return false;
 }
 
-__device__ __forceinline__ void dot8x2(const uint4& wg, const uint4& wu, const uint4& x, float& ag,
-                                       float& au) {
-  const float x0 = bf_lo(x.x), x1 = bf_hi(x.x), x2 = bf_lo(x.y), x3 = bf_hi(x.y);
-  const float x4 = bf_lo(x.z), x5 = bf_hi(x.z), x6 = bf_lo(x.w), x7 = bf_hi(x.w);
-  ag = fmaf(bf_lo(wg.x), x0, ag); au = fmaf(bf_lo(wu.x), x0, au);
-  ag = fmaf(bf_hi(wg.x), x1, ag); au = fmaf(bf_hi(wu.x), x1, au);
-  ag = fmaf(bf_lo(wg.y), x2, ag); au = fmaf(bf_lo(wu.y), x2, au);
-  ag = fmaf(bf_hi(wg.y), x3, ag); au = fmaf(bf_hi(wu.y), x3, au);
-  ag = fmaf(bf_lo(wg.z), x4, ag); au = fmaf(bf_lo(wu.z), x4, au);
-  ag = fmaf(bf_hi(wg.z), x5, ag); au = fmaf(bf_hi(wu.z), x5, au);
-  ag = fmaf(bf_lo(wg.w), x6, ag); au = fmaf(bf_lo(wu.w), x6, au);
-  ag = fmaf(bf_hi(wg.w), x7, ag); au = fmaf(bf_hi(wu.w), x7, au);
+// 8 bf16 weights . 8 fp32 activations, as one short independent chain.
+__device__ __forceinline__ float dot8(const uint4& w, const float4& a, const float4& b) {
+  float s = bf_lo(w.x) * a.x;
+  s = fmaf(bf_hi(w.x), a.y, s);
+  s = fmaf(bf_lo(w.y), a.z, s);
+  s = fmaf(bf_hi(w.y), a.w, s);
+  s = fmaf(bf_lo(w.z), b.x, s);
+  s = fmaf(bf_hi(w.z), b.y, s);
+  s = fmaf(bf_lo(w.w), b.z, s);
+  s = fmaf(bf_hi(w.w), b.w, s);
+  return s;
 }
 
 // CUDA-core segment: units [u0, u1) of one group with NTOK tokens.  The
-// group's activations are staged once in shared memory (xs, which aliases the
-// tensor-core reduction buffer; segments are separated by consumer barriers).
+// group's activations are staged once as fp32 in shared memory (the buffer is
+// shared with the tensor-core reduction; segments are separated by consumer
+// barriers).
 template <int NTOK>
 __device__ __forceinline__ void seg_cc(const GuCtx& c, int u0, int u1, int pair0, int tok_base,
                                        int& it, bool& ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint4* xs = reinterpret_cast<uint4*>(c.red);
-  named_sync(1, gu::CWARPS * 32);  // previous segment is done with xs
+  float4* xs = reinterpret_cast<float4*>(c.buf);  // [NTOK][H/4]
+  named_sync(1, gu::CWARPS * 32);                  // previous segment is done with buf
 #pragma unroll
   for (int i = 0; i < NTOK; ++i) {
     const int tok = tok_base >= 0 ? tok_base + i : __ldcg(c.pair_tok + pair0 + i);
-    const uint4* row = reinterpret_cast<const uint4*>(c.x + (size_t)tok * H);
-    xs[i * (H / 8) + threadIdx.x] = __ldg(row + threadIdx.x);  // 256 threads x 16 B = one row
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)tok * H) + threadIdx.x);
+    xs[i * (H / 4) + 2 * threadIdx.x] = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
+    xs[i * (H / 4) + 2 * threadIdx.x + 1] =
+        make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
   }
   named_sync(1, gu::CWARPS * 32);
   for (int u = u0; u < u1; ++u) {
     const int blk = u & (gu::UNITS - 1);
-    float ag[NTOK], au[NTOK];
+    const int slot = it % gu::NSTAGE;
+    float g[NTOK], v[NTOK];
 #pragma unroll
-    for (int i = 0; i < NTOK; ++i) ag[i] = au[i] = 0.f;
+    for (int i = 0; i < NTOK; ++i) g[i] = v[i] = 0.f;
+    if (ok) ok = wait_full(c, slot, (uint32_t)(it / gu::NSTAGE) & 1u);
+    if (ok) {
+      const uint8_t* st = c.stages + slot * gu::STAGE_BYTES;
+      const uint4* gr = reinterpret_cast<const uint4*>(st + warp * gu::ROW_BYTES);
+      const uint4* ur = reinterpret_cast<const uint4*>(st + (8 + warp) * gu::ROW_BYTES);
 #pragma unroll
-    for (int kh = 0; kh < 2; ++kh) {
-      const int slot = it % gu::NSTAGE;
-      if (ok) ok = wait_full(c, slot, (uint32_t)(it / gu::NSTAGE) & 1u);
-      if (ok) {
-        const uint8_t* st = c.stages + slot * gu::STAGE_BYTES;
-        const uint4* gr = reinterpret_cast<const uint4*>(st + warp * gu::ROW_STRIDE);
-        const uint4* ur = reinterpret_cast<const uint4*>(st + (8 + warp) * gu::ROW_STRIDE);
-        const uint4* xk = xs + kh * (gu::KS / 8) + lane;
+      for (int half = 0; half < 2; ++half) {
+        uint4 wg[4], wu[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint4 wg = gr[lane + 32 * j];
-          const uint4 wu = ur[lane + 32 * j];
+          wg[j] = gr[lane + 32 * (4 * half + j)];
+          wu[j] = ur[lane + 32 * (4 * half + j)];
+        }
 #pragma unroll
-          for (int i = 0; i < NTOK; ++i) dot8x2(wg, wu, xk[i * (H / 8) + 32 * j], ag[i], au[i]);
+        for (int i = 0; i < NTOK; ++i) {
+          float pg[4], pu[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int ch = lane + 32 * (4 * half + j);
+            const float4 a = xs[i * (H / 4) + 2 * ch];
+            const float4 b = xs[i * (H / 4) + 2 * ch + 1];
+            pg[j] = dot8(wg[j], a, b);
+            pu[j] = dot8(wu[j], a, b);
+          }
+          g[i] += (pg[0] + pg[1]) + (pg[2] + pg[3]);
+          v[i] += (pu[0] + pu[1]) + (pu[2] + pu[3]);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(c, slot));
-      ++it;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(c, slot));
+    ++it;
 #pragma unroll
     for (int i = 0; i < NTOK; ++i) {
-      const float g = warp_sum(ag[i]);
-      const float v = warp_sum(au[i]);
-      if (lane == 0 && ok) c.h[(size_t)(pair0 + i) * I + blk * 8 + warp] = silu_mul(g, v);
+      const float gs = warp_sum(g[i]);
+      const float vs = warp_sum(v[i]);
+      if (lane == 0 && ok) c.h[(size_t)(pair0 + i) * I + blk * 8 + warp] = silu_mul(gs, vs);
     }
   }
 }
@@ -147,24 +160,20 @@ __device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair
                                         int tok_base, int& it, bool& ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
-  named_sync(1, gu::CWARPS * 32);  // a preceding CUDA-core segment is done with xs
-  uint4 bfr[NT][2][4];
+  named_sync(1, gu::CWARPS * 32);  // a preceding CUDA-core segment is done with buf
+  uint4 bfr[NT][8];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int slot = nt * 8 + g;
     if (slot < n) {
       const int tok = tok_base >= 0 ? tok_base + slot : __ldcg(c.pair_tok + pair0 + slot);
-      const uint16_t* row = c.x + (size_t)tok * H + warp * 128 + q * 8;
+      const uint16_t* row = c.x + (size_t)tok * H + warp * 256 + q * 8;
 #pragma unroll
-      for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb)
-          bfr[nt][kh][kb] = __ldg(reinterpret_cast<const uint4*>(row + kh * gu::KS + kb * 32));
+      for (int kb = 0; kb < 8; ++kb)
+        bfr[nt][kb] = __ldg(reinterpret_cast<const uint4*>(row + kb * 32));
     } else {
 #pragma unroll
-      for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb) bfr[nt][kh][kb] = make_uint4(0u, 0u, 0u, 0u);
+      for (int kb = 0; kb < 8; ++kb) bfr[nt][kb] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   for (int u = u0; u < u1; ++u) {
@@ -172,31 +181,28 @@ __device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const int slot = it % gu::NSTAGE;
+    if (ok) ok = wait_full(c, slot, (uint32_t)(it / gu::NSTAGE) & 1u);
+    if (ok) {
+      const uint8_t* rlo =
+          c.stages + slot * gu::STAGE_BYTES + g * gu::ROW_BYTES + (warp * 256 + q * 8) * 2;
+      const uint8_t* rhi = rlo + 8 * gu::ROW_BYTES;
 #pragma unroll
-    for (int kh = 0; kh < 2; ++kh) {
-      const int slot = it % gu::NSTAGE;
-      if (ok) ok = wait_full(c, slot, (uint32_t)(it / gu::NSTAGE) & 1u);
-      if (ok) {
-        const uint8_t* rlo =
-            c.stages + slot * gu::STAGE_BYTES + g * gu::ROW_STRIDE + (warp * 128 + q * 8) * 2;
-        const uint8_t* rhi = rlo + 8 * gu::ROW_STRIDE;
+      for (int kb = 0; kb < 8; ++kb) {
+        const uint4 alo = *reinterpret_cast<const uint4*>(rlo + kb * 64);
+        const uint4 ahi = *reinterpret_cast<const uint4*>(rhi + kb * 64);
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-          const uint4 alo = *reinterpret_cast<const uint4*>(rlo + kb * 64);
-          const uint4 ahi = *reinterpret_cast<const uint4*>(rhi + kb * 64);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint4 b = bfr[nt][kh][kb];
-            mma_bf16(acc[nt], alo.x, ahi.x, alo.y, ahi.y, b.x, b.y);
-            mma_bf16(acc[nt], alo.z, ahi.z, alo.w, ahi.w, b.z, b.w);
-          }
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint4 b = bfr[nt][kb];
+          mma_bf16(acc[nt], alo.x, ahi.x, alo.y, ahi.y, b.x, b.y);
+          mma_bf16(acc[nt], alo.z, ahi.z, alo.w, ahi.w, b.z, b.w);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(c, slot));
-      ++it;
     }
-    float* red = c.red + warp * gu::ROWS * GROUP_MAX;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(c, slot));
+    ++it;
+    float* red = c.buf + warp * gu::ROWS * GROUP_MAX;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int col = nt * 8 + 2 * q;
@@ -213,8 +219,8 @@ __device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair
         float gs = 0.f, us = 0.f;
 #pragma unroll
         for (int w = 0; w < gu::CWARPS; ++w) {
-          gs += c.red[(w * gu::ROWS + r) * GROUP_MAX + j];
-          us += c.red[(w * gu::ROWS + r + 8) * GROUP_MAX + j];
+          gs += c.buf[(w * gu::ROWS + r) * GROUP_MAX + j];
+          us += c.buf[(w * gu::ROWS + r + 8) * GROUP_MAX + j];
         }
         c.h[(size_t)(pair0 + j) * I + blk * 8 + r] = silu_mul(gs, us);
       }
@@ -223,31 +229,25 @@ __device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair
   }
 }
 
-// Issues the two stages of one unit (8 gate + 8 up rows of expert `e`, block
-// `blk`); false if the ring could not be acquired (abort).
+// Issues the stage of one unit (8 gate + 8 up rows of the expert at `base`,
+// block `blk`); false if the ring could not be acquired (abort).
 __device__ __forceinline__ bool issue_unit(const GuCtx& c, const uint16_t* base, int blk, int& it) {
-#pragma unroll 1
-  for (int kh = 0; kh < 2; ++kh) {
-    const int slot = it % gu::NSTAGE;
-    bool got = true;
-    if (it >= gu::NSTAGE)
-      got = mbar_wait(empty_bar(c, slot), (uint32_t)((it / gu::NSTAGE) - 1) & 1u, c.deadline);
-    // A consumer that gave up sets the flag before releasing its stage.
-    if (!got || *c.abort_flag) {
-      *c.abort_flag = 1;
-      if (!got) set_error(c.hdr, DEV_TIMEOUT);
-      return false;
-    }
-    mbar_expect_tx(full_bar(c, slot), gu::ROWS * gu::ROW_BYTES);
-    const uint32_t dst = c.stages_addr + slot * gu::STAGE_BYTES;
-#pragma unroll 1
-    for (int r = 0; r < gu::ROWS; ++r) {
-      const int row = (r < 8 ? 0 : I) + blk * 8 + (r & 7);
-      bulk_g2s(dst + r * gu::ROW_STRIDE, base + (size_t)row * H + kh * gu::KS, gu::ROW_BYTES,
-               full_bar(c, slot));
-    }
-    ++it;
+  const int slot = it % gu::NSTAGE;
+  bool got = true;
+  if (it >= gu::NSTAGE)
+    got = mbar_wait(empty_bar(c, slot), (uint32_t)((it / gu::NSTAGE) - 1) & 1u, c.deadline);
+  // A consumer that gave up sets the flag before releasing its stage.
+  if (!got || *c.abort_flag) {
+    *c.abort_flag = 1;
+    if (!got) set_error(c.hdr, DEV_TIMEOUT);
+    return false;
   }
+  mbar_expect_tx(full_bar(c, slot), gu::STAGE_BYTES);
+  const uint32_t dst = c.stages_addr + slot * gu::STAGE_BYTES;
+  bulk_g2s(dst, base + (size_t)(blk * 8) * H, 8 * gu::ROW_BYTES, full_bar(c, slot));
+  bulk_g2s(dst + 8 * gu::ROW_BYTES, base + (size_t)(I + blk * 8) * H, 8 * gu::ROW_BYTES,
+           full_bar(c, slot));
+  ++it;
   return true;
 }
 
@@ -324,19 +324,24 @@ __device__ __forceinline__ void produce(const GuCtx& c, const ExpertArgs& a, Pla
   }
   pdl_wait();     // routing and buckets come from the router kernel
   plan_post(pl, (int)__ldcg(&a.ws.hdr->n_groups), early);
+  int gi_cached = -1;
+  const uint16_t* base = nullptr;
   for (int u = pl.r_begin; ok && u < pl.r_end; ++u) {
-    const int4 grp = __ldcg(a.ws.groups + (u / gu::UNITS));
-    const uint16_t* base = grp.x < E ? a.w.w13 + (size_t)grp.x * (2 * I) * H
-                                     : a.w.ws13 + (size_t)(grp.x - E) * (2 * I) * H;
+    const int gi = u / gu::UNITS;
+    if (gi != gi_cached) {
+      const int4 grp = __ldcg(a.ws.groups + gi);
+      base = grp.x < E ? a.w.w13 + (size_t)grp.x * (2 * I) * H
+                       : a.w.ws13 + (size_t)(grp.x - E) * (2 * I) * H;
+      gi_cached = gi;
+    }
     ok = issue_unit(c, base, u & (gu::UNITS - 1), it);
   }
   drain(c, it);
 }
 
-template <bool CC>
-__device__ __forceinline__ void run_segment(const GuCtx& c, int u0, int u1, int pair0, int n,
-                                            int tok_base, int& it, bool& ok) {
-  if (CC) {
+__device__ __forceinline__ void segment(const GuCtx& c, int u0, int u1, int pair0, int n,
+                                        int tok_base, int& it, bool& ok) {
+  if (n <= gu::CC_MAX) {
     switch (n) {
       case 1: seg_cc<1>(c, u0, u1, pair0, tok_base, it, ok); break;
       case 2: seg_cc<2>(c, u0, u1, pair0, tok_base, it, ok); break;
@@ -352,12 +357,6 @@ __device__ __forceinline__ void run_segment(const GuCtx& c, int u0, int u1, int 
   }
 }
 
-__device__ __forceinline__ void segment(const GuCtx& c, int u0, int u1, int pair0, int n,
-                                        int tok_base, int& it, bool& ok) {
-  if (n <= gu::CC_MAX) run_segment<true>(c, u0, u1, pair0, n, tok_base, it, ok);
-  else run_segment<false>(c, u0, u1, pair0, n, tok_base, it, ok);
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs a) {
@@ -365,8 +364,8 @@ __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs 
   __shared__ int s_abort;
   GuCtx c;
   c.stages = smem;
-  c.red = reinterpret_cast<float*>(smem + gu::NSTAGE * gu::STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(c.red + gu::RED_FLOATS);
+  c.buf = reinterpret_cast<float*>(smem + gu::NSTAGE * gu::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(c.buf + gu::BUF_FLOATS);
   c.stages_addr = smem_addr(smem);
   c.full0 = smem_addr(bars);
   c.empty0 = smem_addr(bars + gu::NSTAGE);

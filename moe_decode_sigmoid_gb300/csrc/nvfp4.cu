@@ -34,9 +34,9 @@ constexpr int THREADS = CWARPS * 32 + 32;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
 // gate/up
 constexpr int GU_QROW = H / 2;                       // 1024 code bytes per row
-constexpr int GU_QSTRIDE = GU_QROW + 16;             // 4-bank shift per row
+constexpr int GU_QSTRIDE = GU_QROW;                  // 8 rows = one contiguous copy
 constexpr int GU_SFROW = H / 16;                     // 128 scale bytes per row
-constexpr int GU_STAGE = 16 * GU_QSTRIDE + 16 * GU_SFROW;  // 18,688
+constexpr int GU_STAGE = 16 * GU_QSTRIDE + 16 * GU_SFROW;  // 18,432
 constexpr int GU_NSTAGE = 10;
 constexpr int GU_RED = CWARPS * 16 * GROUP_MAX;
 constexpr size_t GU_SMEM = (size_t)GU_NSTAGE * GU_STAGE + GU_RED * 4 + 2 * GU_NSTAGE * 8;
@@ -44,11 +44,11 @@ constexpr int UNITS = I / 8;
 // down
 constexpr int RS = 16;
 constexpr int DN_QROW = I / 2;                       // 256
-constexpr int DN_QSTRIDE = DN_QROW + 16;             // 272
+constexpr int DN_QSTRIDE = DN_QROW;                  // 16 rows = one contiguous copy
 constexpr int DN_SFROW = I / 16;                     // 32
-constexpr int DN_WBYTES = RS * DN_QSTRIDE + RS * DN_SFROW;  // 4,864
+constexpr int DN_WBYTES = RS * DN_QSTRIDE + RS * DN_SFROW;  // 4,608
 constexpr int HROW = I * 4;
-constexpr int HSTRIDE = HROW + 64;
+constexpr int HSTRIDE = HROW;
 constexpr int DN_RED = CWARPS * RS * GROUP_MAX;
 constexpr int DN_MAX_STAGES = 8;
 constexpr int SMEM_CAP = 232448 - 1024;
@@ -195,20 +195,26 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, f
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   named_sync(1, f4::CWARPS * 32);  // the previous segment is done with `red`
-  // B fragments: this warp's 256-column K slice of each token, as f16.
-  uint4 bfr[NT][8];
+  // K order inside this warp's 256-column slice: thread q of a quad owns the
+  // 32 consecutive columns [32q + 128m, +32) for m = 0, 1 (16 contiguous code
+  // bytes per row); step (m, i) covers columns 32q + 128m + 8i .. +8.  The
+  // activations follow the same order, so the MMA sums match.
+  uint4 bfr[NT][2][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int slot = nt * 8 + g;
     if (slot < n) {
       const int tok = __ldcg(a.ws.pair_tok + pair0 + slot);
-      const uint16_t* row = a.x + (size_t)tok * H + warp * 256 + q * 8;
+      const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)tok * H + warp * 256 + q * 32);
 #pragma unroll
-      for (int kb = 0; kb < 8; ++kb)
-        bfr[nt][kb] = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(row + kb * 32)));
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bfr[nt][m][i] = bf16x8_to_f16x8(__ldg(row + m * 16 + i));
     } else {
 #pragma unroll
-      for (int kb = 0; kb < 8; ++kb) bfr[nt][kb] = make_uint4(0u, 0u, 0u, 0u);
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bfr[nt][m][i] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   const float* ts = expert < E ? a.w.w13_ts + 2 * expert : a.w.ws13_ts + 2 * (expert - E);
@@ -222,28 +228,38 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, f
     if (ok) ok = wait_full(p, slot, (uint32_t)(it / p.nstage) & 1u);
     if (ok) {
       const uint8_t* st = p.stages + slot * p.stage_bytes;
-      const uint8_t* qlo = st + g * f4::GU_QSTRIDE + warp * 128 + q * 4;
+      const uint8_t* qlo = st + g * f4::GU_QSTRIDE + warp * 128 + q * 16;
       const uint8_t* qhi = qlo + 8 * f4::GU_QSTRIDE;
       const uint8_t* sfb = st + 16 * f4::GU_QSTRIDE;
       const uint4 slo = *reinterpret_cast<const uint4*>(sfb + g * f4::GU_SFROW + warp * 16);
       const uint4 shi = *reinterpret_cast<const uint4*>(sfb + (g + 8) * f4::GU_SFROW + warp * 16);
-      const uint32_t sl[4] = {slo.x, slo.y, slo.z, slo.w};
-      const uint32_t sh[4] = {shi.x, shi.y, shi.z, shi.w};
+      const bool qh = (q >> 1) != 0;
 #pragma unroll
-      for (int kb = 0; kb < 8; ++kb) {
-        const int sh_bits = 8 * (2 * (kb & 1) + (q >> 1));
-        const uint32_t scl = e4m3_bcast_f16x2((sl[kb >> 1] >> sh_bits) & 0xffu);
-        const uint32_t sch = e4m3_bcast_f16x2((sh[kb >> 1] >> sh_bits) & 0xffu);
-        uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
-        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(qlo + kb * 16), l0, l1, l2, l3);
-        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(qhi + kb * 16), h0, h1, h2, h3);
-        l0 = hmul2(l0, scl); l1 = hmul2(l1, scl); l2 = hmul2(l2, scl); l3 = hmul2(l3, scl);
-        h0 = hmul2(h0, sch); h1 = hmul2(h1, sch); h2 = hmul2(h2, sch); h3 = hmul2(h3, sch);
+      for (int m = 0; m < 2; ++m) {
+        const uint4 clo = *reinterpret_cast<const uint4*>(qlo + m * 64);
+        const uint4 chi = *reinterpret_cast<const uint4*>(qhi + m * 64);
+        const uint32_t cl[4] = {clo.x, clo.y, clo.z, clo.w};
+        const uint32_t ch[4] = {chi.x, chi.y, chi.z, chi.w};
+        // block of step (m, i) = 8m + 2q + i/2 within the warp's 16 blocks:
+        // scale word 2m + q/2
+        const uint32_t wl = m ? (qh ? slo.w : slo.z) : (qh ? slo.y : slo.x);
+        const uint32_t wh = m ? (qh ? shi.w : shi.z) : (qh ? shi.y : shi.x);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint4 b = bfr[nt][kb];
-          mma_f16(acc[nt], l0, h0, l1, h1, b.x, b.y);
-          mma_f16(acc[nt], l2, h2, l3, h3, b.z, b.w);
+        for (int i = 0; i < 4; ++i) {
+          const int sh_bits = 8 * (2 * (q & 1) + (i >> 1));
+          const uint32_t scl = e4m3_bcast_f16x2((wl >> sh_bits) & 0xffu);
+          const uint32_t sch = e4m3_bcast_f16x2((wh >> sh_bits) & 0xffu);
+          uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+          e2m1x8_to_f16x2(cl[i], l0, l1, l2, l3);
+          e2m1x8_to_f16x2(ch[i], h0, h1, h2, h3);
+          l0 = hmul2(l0, scl); l1 = hmul2(l1, scl); l2 = hmul2(l2, scl); l3 = hmul2(l3, scl);
+          h0 = hmul2(h0, sch); h1 = hmul2(h1, sch); h2 = hmul2(h2, sch); h3 = hmul2(h3, sch);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint4 b = bfr[nt][m][i];
+            mma_f16(acc[nt], l0, h0, l1, h1, b.x, b.y);
+            mma_f16(acc[nt], l2, h2, l3, h3, b.z, b.w);
+          }
         }
       }
     }
@@ -291,12 +307,9 @@ __device__ __forceinline__ void gu_produce(const Pipe& p, const ExpertArgs& a, i
     const int slot = it % p.nstage;
     mbar_expect_tx(full_bar(p, slot), 16 * f4::GU_QROW + 16 * f4::GU_SFROW);
     const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
-#pragma unroll 1
-    for (int r = 0; r < 16; ++r) {
-      const int row = (r < 8 ? 0 : I) + blk * 8 + (r & 7);
-      bulk_g2s(dst + r * f4::GU_QSTRIDE, qb + (size_t)row * f4::GU_QROW, f4::GU_QROW,
-               full_bar(p, slot));
-    }
+    bulk_g2s(dst, qb + (size_t)(blk * 8) * f4::GU_QROW, 8 * f4::GU_QROW, full_bar(p, slot));
+    bulk_g2s(dst + 8 * f4::GU_QSTRIDE, qb + (size_t)(I + blk * 8) * f4::GU_QROW, 8 * f4::GU_QROW,
+             full_bar(p, slot));
     bulk_g2s(dst + 16 * f4::GU_QSTRIDE, sb + (size_t)(blk * 8) * f4::GU_SFROW, 8 * f4::GU_SFROW,
              full_bar(p, slot));
     bulk_g2s(dst + 16 * f4::GU_QSTRIDE + 8 * f4::GU_SFROW, sb + (size_t)(I + blk * 8) * f4::GU_SFROW,
@@ -316,20 +329,24 @@ __device__ __forceinline__ void dn_group(const ExpertArgs& a, const uint8_t* st,
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-  const uint8_t* qlo = st + g * f4::DN_QSTRIDE + warp * 32 + q * 4;
+  // K order inside this warp's 64-column slice: thread q owns columns
+  // [16q, 16q + 16) (8 contiguous code bytes per row, one scale block); step i
+  // covers 16q + 8i .. +8; h follows the same order.
+  const uint8_t* qlo = st + g * f4::DN_QSTRIDE + warp * 32 + q * 8;
   const uint8_t* qhi = qlo + 8 * f4::DN_QSTRIDE;
   const uint8_t* sfb = st + f4::RS * f4::DN_QSTRIDE;
   const uint32_t slo = *reinterpret_cast<const uint32_t*>(sfb + g * f4::DN_SFROW + warp * 4);
   const uint32_t shi = *reinterpret_cast<const uint32_t*>(sfb + (g + 8) * f4::DN_SFROW + warp * 4);
-  const uint8_t* hs = st + f4::DN_WBYTES + (warp * 64 + q * 8) * 4;
+  const uint32_t scl = e4m3_bcast_f16x2((slo >> (8 * q)) & 0xffu);
+  const uint32_t sch = e4m3_bcast_f16x2((shi >> (8 * q)) & 0xffu);
+  const uint2 clo = *reinterpret_cast<const uint2*>(qlo);
+  const uint2 chi = *reinterpret_cast<const uint2*>(qhi);
+  const uint8_t* hs = st + f4::DN_WBYTES + (warp * 64 + q * 16) * 4;
 #pragma unroll
-  for (int kb = 0; kb < 2; ++kb) {
-    const int sh_bits = 8 * (2 * kb + (q >> 1));
-    const uint32_t scl = e4m3_bcast_f16x2((slo >> sh_bits) & 0xffu);
-    const uint32_t sch = e4m3_bcast_f16x2((shi >> sh_bits) & 0xffu);
+  for (int i = 0; i < 2; ++i) {
     uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
-    e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(qlo + kb * 16), l0, l1, l2, l3);
-    e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(qhi + kb * 16), h0, h1, h2, h3);
+    e2m1x8_to_f16x2(i ? clo.y : clo.x, l0, l1, l2, l3);
+    e2m1x8_to_f16x2(i ? chi.y : chi.x, h0, h1, h2, h3);
     l0 = hmul2(l0, scl); l1 = hmul2(l1, scl); l2 = hmul2(l2, scl); l3 = hmul2(l3, scl);
     h0 = hmul2(h0, sch); h1 = hmul2(h1, sch); h2 = hmul2(h2, sch); h3 = hmul2(h3, sch);
 #pragma unroll
@@ -338,8 +355,8 @@ __device__ __forceinline__ void dn_group(const ExpertArgs& a, const uint8_t* st,
       // h (fp32) = hi + lo with both parts f16: two MMAs keep ~22 bits of h.
       uint32_t b[4] = {0u, 0u, 0u, 0u}, r[4] = {0u, 0u, 0u, 0u};
       if (slot < n) {
-        const float4 v0 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + kb * 128);
-        const float4 v1 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + kb * 128 + 16);
+        const float4 v0 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + i * 32);
+        const float4 v1 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + i * 32 + 16);
         split_f16x2(v0.x, v0.y, b[0], r[0]);
         split_f16x2(v0.z, v0.w, b[1], r[1]);
         split_f16x2(v1.x, v1.y, b[2], r[2]);
@@ -388,14 +405,9 @@ __device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, i
     const uint8_t* sb = (routed ? a.w.w2_sf : a.w.ws2_sf) + ((size_t)e * H + r0) * f4::DN_SFROW;
     mbar_expect_tx(full_bar(p, slot), f4::RS * (f4::DN_QROW + f4::DN_SFROW) + n * f4::HROW);
     const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
-#pragma unroll 1
-    for (int r = 0; r < f4::RS; ++r)
-      bulk_g2s(dst + r * f4::DN_QSTRIDE, qb + (size_t)r * f4::DN_QROW, f4::DN_QROW, full_bar(p, slot));
+    bulk_g2s(dst, qb, f4::RS * f4::DN_QROW, full_bar(p, slot));
     bulk_g2s(dst + f4::RS * f4::DN_QSTRIDE, sb, f4::RS * f4::DN_SFROW, full_bar(p, slot));
-#pragma unroll 1
-    for (int i = 0; i < n; ++i)
-      bulk_g2s(dst + f4::DN_WBYTES + i * f4::HSTRIDE, a.ws.h + (size_t)(grp.y + i) * I, f4::HROW,
-               full_bar(p, slot));
+    bulk_g2s(dst + f4::DN_WBYTES, a.ws.h + (size_t)grp.y * I, n * f4::HROW, full_bar(p, slot));
     ++it;
   }
   drain(p, it);

@@ -8,13 +8,13 @@
 // Kernels", same page, "Optimization Strategies").
 //
 // One launch does all three steps without any device-side wait:
-//   grid (E/8, ceil(B/8)), 256 threads.  Warp w of CTA (bx, by) owns expert
-//   8*bx + w: its 4 KiB router row stays in registers while the warp dots it
-//   with the 8 tokens of tile `by` (fp32 accumulation, warp-shuffle sum).
+//   grid (E/2, ceil(B/8)), 256 threads: each CTA dots two router rows with an
+//   8-token tile (fp32 accumulation, warp-shuffle and shared-memory sums).
 //   The last CTA to finish a token tile (atomic ticket after a fence) ranks
-//   that tile's 8 tokens, one warp per token; the last tile to finish then
-//   buckets the whole batch.  Tickets are reset by their last user, so the
-//   workspace is ready for the next call.
+//   that tile's tokens, one warp per token; with a single tile it buckets the
+//   batch right away from shared memory, otherwise the last tile to finish
+//   buckets it.  Tickets are reset by their last user, so the workspace is
+//   ready for the next call.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -57,7 +57,7 @@ __device__ __forceinline__ float key2f(uint32_t k) {
 // across lanes by the minimum index).  Weights: sigmoid of the selected
 // logits divided by their sum.
 __device__ void topk_token(const float* logits_row, int* idx_out, float* w_out,
-                           int* user_idx, float* user_w) {
+                           int* user_idx, float* user_w, int* s_idx, float* s_w) {
   const int lane = threadIdx.x & 31;
   float v[E / 32];
 #pragma unroll
@@ -100,6 +100,8 @@ __device__ void topk_token(const float* logits_row, int* idx_out, float* w_out,
     w_out[lane] = wl;
     if (user_idx) user_idx[lane] = el;
     if (user_w) user_w[lane] = wl;
+    s_idx[lane] = el;
+    s_w[lane] = wl;
   }
 }
 
@@ -137,7 +139,14 @@ __device__ int block_excl_scan(int v, int* s_warp, int* total) {
 //   n_groups, n_uniq in the header.
 // Optionally also the plain bucket description (distinct experts ascending,
 // their first pair, and the pairs encoded token*8 + slot).
-__device__ void bucket_batch(const Ws& ws, int B, BucketOut user) {
+template <bool SMEM_SRC>
+__device__ __forceinline__ int ld_idx(const int* p) { return SMEM_SRC ? *p : __ldcg(p); }
+template <bool SMEM_SRC>
+__device__ __forceinline__ float ld_w(const float* p) { return SMEM_SRC ? *p : __ldcg(p); }
+
+template <bool SMEM_SRC>
+__device__ void bucket_batch(const Ws& ws, int B, BucketOut user, const int* src_idx,
+                             const float* src_w) {
   constexpr int MW = MAX_B / 32;
   __shared__ uint32_t s_mask[E][MW];  // token bitmask per expert
   __shared__ int s_off[E];            // first pair of each expert
@@ -147,7 +156,7 @@ __device__ void bucket_batch(const Ws& ws, int B, BucketOut user) {
   __syncthreads();
   const int npairs = B * TOPK;
   for (int p = tid; p < npairs; p += 256) {
-    const int e = __ldcg(ws.topk_idx + p);
+    const int e = ld_idx<SMEM_SRC>(src_idx + p);
     const int t = p / TOPK;
     if (e < 0 || e >= E) {
       set_error(ws.hdr, DEV_BAD_ROUTING);
@@ -179,7 +188,7 @@ __device__ void bucket_batch(const Ws& ws, int B, BucketOut user) {
   // Each pair goes to its expert's first slot plus its rank among the expert's
   // tokens (the set bits of the expert's mask below the token).
   for (int p = tid; p < npairs; p += 256) {
-    const int ex = __ldcg(ws.topk_idx + p);
+    const int ex = ld_idx<SMEM_SRC>(src_idx + p);
     const int t = p / TOPK;
     if (ex < 0 || ex >= E) continue;
     const int wd = t >> 5;
@@ -187,7 +196,7 @@ __device__ void bucket_batch(const Ws& ws, int B, BucketOut user) {
     for (int w = 0; w < wd; ++w) rank += __popc(s_mask[ex][w]);
     const int pos = s_off[ex] + rank;
     ws.pair_tok[pos] = t;
-    ws.pair_w[pos] = __ldcg(ws.topk_w + p);
+    ws.pair_w[pos] = ld_w<SMEM_SRC>(src_w + p);
     if (user.pairs) user.pairs[pos] = t * 8 + (p - t * TOPK);
   }
   // Shared experts: every token, weight 1, after the routed pairs.
@@ -209,11 +218,17 @@ __device__ void bucket_batch(const Ws& ws, int B, BucketOut user) {
   }
 }
 
+// grid (E/2, ceil(B/8)), 256 threads.  Warp w of CTA (bx, by) owns expert
+// 2*bx + w/4 and the K-quarter w%4; each lane holds two 16-byte chunks of the
+// router row and issues all 16 activation loads of the 8-token tile at once,
+// so the whole tile costs one memory round trip.  The four quarter sums are
+// combined in shared memory.
 __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
   pdl_wait();     // x may come from the preceding kernel in the stream
   pdl_trigger();  // the expert kernels may start their prologue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + warp;
+  const int el = warp >> 2, qk = warp & 3;
+  const int e = blockIdx.x * 2 + el;
   const int t0 = blockIdx.y * 8;
   const int nt = min(8, a.B - t0);
   WsHeader* hdr = a.ws.hdr;
@@ -232,21 +247,45 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
     hdr->stall_armed = 0;
   }
 
+  const int c0 = qk * 64 + lane, c1 = c0 + 32;  // 16-byte chunks of the 4 KiB row
   const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * H);
-  uint4 w[H / 256];
+  const uint4 w0 = ldg_stream(wrow + c0), w1 = ldg_stream(wrow + c1);
+  uint4 xv[8][2];
 #pragma unroll
-  for (int j = 0; j < H / 256; ++j) w[j] = ldg_stream(wrow + lane + 32 * j);
-  const float bias = a.bias ? __ldg(a.bias + e) : 0.0f;
-  for (int t = 0; t < nt; ++t) {
-    const uint4* xrow = reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + t) * H);
-    float acc = 0.f;
+  for (int t = 0; t < 8; ++t) {
+    if (t < nt) {
+      const uint4* xrow = reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + t) * H);
+      xv[t][0] = __ldg(xrow + c0);
+      xv[t][1] = __ldg(xrow + c1);
+    } else {
+      xv[t][0] = xv[t][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  float acc[8];
 #pragma unroll
-    for (int j = 0; j < H / 256; ++j) acc = dot8(w[j], __ldg(xrow + lane + 32 * j), acc);
-    acc = warp_sum(acc);
-    if (lane == 0) a.ws.logits[(size_t)(t0 + t) * E + e] = acc + bias;
+  for (int t = 0; t < 8; ++t) acc[t] = dot8(w1, xv[t][1], dot8(w0, xv[t][0], 0.f));
+#pragma unroll
+  for (int t = 0; t < 8; ++t) acc[t] = warp_sum(acc[t]);
+  __shared__ float s_part[2][4][8];
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) s_part[el][qk][t] = acc[t];
+  }
+  __syncthreads();
+  if (threadIdx.x < 16) {
+    const int le = threadIdx.x >> 3, t = threadIdx.x & 7;
+    if (t < nt) {
+      const int ee = blockIdx.x * 2 + le;
+      const float v = (s_part[le][0][t] + s_part[le][1][t]) + (s_part[le][2][t] + s_part[le][3][t]) +
+                      (a.bias ? __ldg(a.bias + ee) : 0.0f);
+      a.ws.logits[(size_t)(t0 + t) * E + ee] = v;
+    }
   }
 
+  // The last CTA to finish this token tile ranks its tokens.
   __shared__ uint32_t s_ticket;
+  __shared__ int s_idx[8 * TOPK];
+  __shared__ float s_w[8 * TOPK];
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -261,10 +300,15 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
     topk_token(a.ws.logits + (size_t)t * E, a.ws.topk_idx + (size_t)t * TOPK,
                a.ws.topk_w + (size_t)t * TOPK,
                a.user_idx ? a.user_idx + (size_t)t * TOPK : nullptr,
-               a.user_w ? a.user_w + (size_t)t * TOPK : nullptr);
+               a.user_w ? a.user_w + (size_t)t * TOPK : nullptr, s_idx + warp * TOPK,
+               s_w + warp * TOPK);
   }
   if (!a.do_bucket) return;
   __syncthreads();
+  if (gridDim.y == 1) {  // one token tile: the routing is already in shared memory
+    bucket_batch<true>(a.ws, a.B, a.bucket, s_idx, s_w);
+    return;
+  }
   if (threadIdx.x == 0) {
     __threadfence();
     s_ticket = atomicAdd(&hdr->tiles_done, 1u);
@@ -273,18 +317,18 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
   if (s_ticket != gridDim.y - 1) return;
   __threadfence();
   if (threadIdx.x == 0) hdr->tiles_done = 0u;
-  bucket_batch(a.ws, a.B, a.bucket);
+  bucket_batch<false>(a.ws, a.B, a.bucket, a.ws.topk_idx, a.ws.topk_w);
 }
 
 __global__ void __launch_bounds__(256) bucket_kernel(Ws ws, int B, BucketOut user) {
   pdl_wait();
   pdl_trigger();
-  bucket_batch(ws, B, user);
+  bucket_batch<false>(ws, B, user, ws.topk_idx, ws.topk_w);
 }
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(E / 8, (a.B + 7) / 8, 1);
+  cfg.gridDim = dim3(E / 2, (a.B + 7) / 8, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
