@@ -445,6 +445,102 @@ def extras(m, cold, stream, args):
             "us": round(st["mean"], 3), "p50_us": round(st["p50"], 3), "unique_experts": U,
             "needed_bytes": nb, "gbs": round(nb / (st["mean"] * 1e-6) / 1e9, 1)}
         del L
+    out.update(nvfp4_configs(m, cold, stream, steps, args.warmup))
+    if args.stack:
+        out.update(stack_configs(m, stream, args.warmup))
+    return out
+
+
+def nvfp4_configs(m, cold, stream, steps, warmup):
+    """NVFP4 W4A16 layer at batch 1 and 8 (weights packed from each bf16 copy)."""
+    nvs = [fs.nvfp4_layer(W) for W in cold.Ws]
+    torch.cuda.synchronize()
+    out = {}
+    for B in (1, 8):
+        x, res = fs.tokens(TOKEN_SEED + B, B, device=x_device(cold))
+        o = torch.empty_like(res)
+        idx = torch.empty((B, 6), dtype=torch.int32, device=x.device)
+        ws = m.new_workspace(B, device=x.device)
+        graphs = []
+        with torch.cuda.stream(stream):
+            for i, (W, nv) in enumerate(zip(cold.Ws, nvs)):
+                call = (lambda W=W, nv=nv: m.flint_moe_decode_nvfp4_w4a16(
+                    x, res, W["wr"], None, nv, o, ws, idx, None, stream=stream))
+                call()
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    call()
+                graphs.append(g)
+        torch.cuda.synchronize()
+        U = int(torch.unique(idx).numel())
+        times, _, _ = timed_steps(lambda i: graphs[i % len(graphs)].replay(), steps, warmup, cold,
+                                  stream)
+        st = stats_us(times)
+        nb = needed_bytes_nvfp4(U)
+        out["nvfp4_b%d" % B] = {"us": round(st["mean"], 3), "p50_us": round(st["p50"], 3),
+                                "unique_experts": U, "needed_bytes": nb,
+                                "gbs": round(nb / (st["mean"] * 1e-6) / 1e9, 1)}
+    del nvs
+    return out
+
+
+def x_device(cold):
+    return cold.Ws[0]["wr"].device
+
+
+STACK_LAYERS = 47
+
+
+def stack_configs(m, stream, warmup, steps=20):
+    """47 distinct BF16 MoE layers resident (~76 GB) applied in sequence with
+    RMSNorm between them: one decode step's MoE work, naturally cold in L2."""
+    device = torch.device("cuda", torch.cuda.current_device())
+    free, _ = torch.cuda.mem_get_info(device)
+    need = STACK_LAYERS * 1.62e9 + 8e9
+    if free < need:
+        return {"stack47": {"skipped": "needs %.0f GB free, %.0f GB available"
+                            % (need / 1e9, free / 1e9)}}
+    layers = [fs.layer_weights(5000 + l, fs.FULL, device=device) for l in range(STACK_LAYERS)]
+    torch.cuda.synchronize()
+    out = {}
+    for B in (1, 8, 32):
+        x0, r0 = fs.tokens(6000 + B, B, device=device)
+        xs = [x0] + [torch.empty_like(x0) for _ in range(STACK_LAYERS)]
+        outs = [torch.empty_like(r0) for _ in range(STACK_LAYERS)]
+        idx = torch.empty((STACK_LAYERS, B, 6), dtype=torch.int32, device=device)
+        ws = m.new_workspace(B, device=device)
+
+        def step_once():
+            res = r0
+            for l, W in enumerate(layers):
+                m.flint_moe_decode_bf16(xs[l], res, W["wr"], None, W["w13"], W["w2"], W["ws13"],
+                                        W["ws2"], outs[l], ws, idx[l], None, stream=stream)
+                m.flint_moe_rmsnorm_bf16(outs[l], xs[l + 1], 1e-6, stream=stream)
+                res = outs[l]
+
+        with torch.cuda.stream(stream):
+            step_once()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step_once()
+        torch.cuda.synchronize()
+        nb = sum(needed_bytes_bf16(int(torch.unique(idx[l]).numel())) for l in range(STACK_LAYERS))
+
+        class _Spacer:
+            def before(self, i):
+                torch.cuda._sleep(SPACER_CYCLES)
+
+        times, _, _ = timed_steps(lambda i: g.replay(), steps, warmup, _Spacer(), stream)
+        st = stats_us(times)
+        out["stack47_b%d" % B] = {"us_per_step": round(st["mean"], 2), "p50_us": round(st["p50"], 2),
+                                  "needed_bytes": nb, "gbs": round(nb / (st["mean"] * 1e-6) / 1e9, 1),
+                                  "us_per_layer": round(st["mean"] / STACK_LAYERS, 3),
+                                  "gpu_launches_per_step": 4 * STACK_LAYERS}
+        del g
+    del layers
+    torch.cuda.empty_cache()
     return out
 
 
@@ -511,6 +607,9 @@ def main():
     ap.add_argument("--extras", action="store_true", default=True)
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stack", action="store_true", default=True,
+                    help="also time the 47-layer stack (needs ~85 GB free)")
+    ap.add_argument("--no-stack", dest="stack", action="store_false")
     ap.add_argument("--l2", choices=("rotate", "flush"), default="rotate",
                     help="cold-L2 method between timed steps")
     args = ap.parse_args()
