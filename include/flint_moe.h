@@ -23,10 +23,12 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Every tensor pointer is a DEVICE pointer, owned by the caller, and must be
- *    16-byte aligned.  Tensors are dense and row-major in the shapes written
- *    beside each argument.  bf16 tensors are passed as `const void*` holding
- *    IEEE bfloat16 bit patterns.
+ *  - Every tensor pointer is a DEVICE pointer, owned by the caller.  Weight,
+ *    activation and workspace pointers must be 16-byte aligned; the small
+ *    fp32 / int32 vectors (logit offsets, tensor scales, routing outputs,
+ *    bucket outputs) need only 4-byte alignment.  Tensors are dense and
+ *    row-major in the shapes written beside each argument.  bf16 tensors are
+ *    passed as `const void*` holding IEEE bfloat16 bit patterns.
  *  - The library allocates no device or host memory and keeps no state between
  *    calls.  Scratch lives in a caller-provided workspace (see
  *    flint_moe_workspace_bytes / flint_moe_workspace_init).  Two calls may run

@@ -27,6 +27,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool req(const void* p) { return p != nullptr && aligned16(p); }
 // Optional pointer: null, or 16-byte aligned.
 bool opt(const void* p) { return p == nullptr || aligned16(p); }
+// Small fp32 / int32 vectors (offsets, routing outputs): 4-byte alignment.
+bool req4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool opt4(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool overlap(const void* a, size_t an, const void* b, size_t bn) {
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
@@ -124,7 +127,7 @@ flint_status flint_moe_route(const flint_moe_dims* dims, int32_t batch, const vo
                              float* topk_w, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   flint_status st = check_common(dims, batch, workspace, ws_bytes);
   if (st != FLINT_OK) return st;
-  if (!req(x_bf16) || !req(w_router_bf16) || !opt(logit_bias) || !req(topk_idx) || !req(topk_w))
+  if (!req(x_bf16) || !req(w_router_bf16) || !opt4(logit_bias) || !req4(topk_idx) || !req4(topk_w))
     return FLINT_ERR_INVALID_ARG;
   RouterArgs a = {};
   a.x = static_cast<const uint16_t*>(x_bf16);
@@ -144,7 +147,7 @@ flint_status flint_moe_bucket(const flint_moe_dims* dims, int32_t batch, const i
                               void* workspace, size_t ws_bytes, cudaStream_t stream) {
   flint_status st = check_common(dims, batch, workspace, ws_bytes);
   if (st != FLINT_OK) return st;
-  if (!req(topk_idx) || !req(uniq) || !req(offsets) || !req(pairs) || !req(n_uniq))
+  if (!req4(topk_idx) || !req4(uniq) || !req4(offsets) || !req4(pairs) || !req4(n_uniq))
     return FLINT_ERR_INVALID_ARG;
   Ws w = ws_view(workspace);
   cudaError_t e = cudaMemcpyAsync(w.topk_idx, topk_idx, sizeof(int32_t) * (size_t)batch * TOPK,
@@ -160,8 +163,8 @@ static flint_status decode_checks(const flint_moe_dims* dims, int32_t batch, con
                                   size_t ws_bytes) {
   flint_status st = check_common(dims, batch, ws, ws_bytes);
   if (st != FLINT_OK) return st;
-  if (!req(x) || !req(residual) || !req(wr) || !opt(bias) || !req(out) || !opt(idx_out) ||
-      !opt(w_out))
+  if (!req(x) || !req(residual) || !req(wr) || !opt4(bias) || !req(out) || !opt4(idx_out) ||
+      !opt4(w_out))
     return FLINT_ERR_INVALID_ARG;
   if (!aliasing_ok(batch, x, residual, out, ws, ws_bytes)) return FLINT_ERR_INVALID_ARG;
   return FLINT_OK;
@@ -183,6 +186,10 @@ static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const vo
   r.user_w = w_out;
   r.do_bucket = 1;
   r.stall_check = 1;
+  // Small batches: the router only writes logits and every gate/up CTA ranks
+  // and buckets the tokens itself, which takes the router's serial tail off
+  // the critical path.
+  r.logits_only = batch <= LOCAL_SELECT_MAX_B ? 1 : 0;
   cudaError_t e = launch_router(r, stream, true);
   if (e != cudaSuccess) return cuda_status(e);
   ExpertArgs a = {};
@@ -196,6 +203,9 @@ static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const vo
   // and lets the gate/up kernel launch early: the shared expert, which does not
   // depend on routing, is then computed while the router runs.
   a.early_shared = 1;
+  a.local_select = r.logits_only;
+  a.user_idx = idx_out;
+  a.user_w = w_out;
   e = nvfp4 ? launch_gateup_nvfp4(a, stream, sms) : launch_gateup_bf16(a, stream, sms);
   if (e != cudaSuccess) return cuda_status(e);
   e = nvfp4 ? launch_down_nvfp4(a, stream) : launch_down_bf16(a, stream);
@@ -273,9 +283,9 @@ flint_status flint_moe_decode_nvfp4_w4a16(
   flint_status st = decode_checks(dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias,
                                   out_bf16, topk_idx_out, topk_w_out, workspace, ws_bytes);
   if (st != FLINT_OK) return st;
-  if (!req(w13_q) || !req(w13_sf) || !req(w13_ts) || !req(w2_q) || !req(w2_sf) || !req(w2_ts) ||
-      !req(ws13_q) || !req(ws13_sf) || !req(ws13_ts) || !req(ws2_q) || !req(ws2_sf) ||
-      !req(ws2_ts))
+  if (!req(w13_q) || !req(w13_sf) || !req4(w13_ts) || !req(w2_q) || !req(w2_sf) || !req4(w2_ts) ||
+      !req(ws13_q) || !req(ws13_sf) || !req4(ws13_ts) || !req(ws2_q) || !req(ws2_sf) ||
+      !req4(ws2_ts))
     return FLINT_ERR_INVALID_ARG;
   ExpertW w = {};
   w.w13_q = w13_q; w.w13_sf = w13_sf; w.w13_ts = w13_ts;

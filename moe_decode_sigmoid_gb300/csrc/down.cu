@@ -20,6 +20,7 @@
 //      fp32 h is split into two bf16 parts (hi + lo, two MMAs) so the operand
 //      keeps ~16 significant bits; warp w owns a 64-column K-slice.
 #include "common.cuh"
+#include "expert_common.cuh"
 #include "kernels.h"
 
 namespace flint {
@@ -41,7 +42,8 @@ constexpr uint64_t DRAIN_NS = 2000000000ull;
 __host__ __device__ inline int nmax_for(int B) { return B < GROUP_MAX ? B : GROUP_MAX; }
 __host__ __device__ inline int stage_bytes(int B) { return WBYTES + nmax_for(B) * HSTRIDE; }
 __host__ __device__ inline int fixed_bytes(int B) {
-  return RED_FLOATS * 4 + B * RS * 4 + 2 * MAX_STAGES * 8;
+  return RED_FLOATS * 4 + B * RS * 4 + (int)sizeof(MetaSmem) + MAX_B * SLOTS * 4 +
+         2 * MAX_STAGES * 8;
 }
 __host__ __device__ inline int nstages(int B) {
   int n = (SMEM_CAP - fixed_bytes(B)) / stage_bytes(B);
@@ -64,8 +66,8 @@ struct DnCtx {
   uint64_t deadline;
   WsHeader* hdr;
   volatile int* abort_flag;
-  const int* pair_tok;
-  const float* pair_w;
+  const int* pair_tok;  // shared memory
+  const float* pair_w;  // shared memory
 };
 
 __device__ __forceinline__ uint32_t full_bar(const DnCtx& c, int s) { return c.full0 + 8u * s; }
@@ -114,8 +116,8 @@ __device__ __forceinline__ void group_cc(const DnCtx& c, const uint8_t* st, int 
     s0 = warp_sum(s0);
     s1 = warp_sum(s1);
     if (lane == 0) {
-      const int t = __ldcg(c.pair_tok + pair0 + i);
-      const float wt = __ldcg(c.pair_w + pair0 + i);
+      const int t = c.pair_tok[pair0 + i];
+      const float wt = c.pair_w[pair0 + i];
       c.acc[t * dn::RS + 2 * warp] += wt * s0;
       c.acc[t * dn::RS + 2 * warp + 1] += wt * s1;
     }
@@ -170,18 +172,19 @@ __device__ __forceinline__ void group_mma(const DnCtx& c, const uint8_t* st, int
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < dn::CWARPS; ++w) s += c.red[(w * dn::RS + r) * GROUP_MAX + j];
-    const int t = __ldcg(c.pair_tok + pair0 + j);
-    const float wt = __ldcg(c.pair_w + pair0 + j);
+    const int t = c.pair_tok[pair0 + j];
+    const float wt = c.pair_w[pair0 + j];
     c.acc[t * dn::RS + r] += wt * s;
   }
   named_sync(1, dn::CWARPS * 32);
 }
 
-__device__ void produce(const DnCtx& c, const int4* groups, int n_groups, const uint16_t* w2,
-                        const uint16_t* ws2, const float* h, int r0) {
+__device__ __forceinline__ void produce(const DnCtx& c, const int4* groups, int n_groups,
+                                        const uint16_t* w2, const uint16_t* ws2, const float* h,
+                                        int r0) {
   int it = 0;
   for (int gi = 0; gi < n_groups; ++gi) {
-    const int4 grp = __ldcg(groups + gi);
+    const int4 grp = groups[gi];
     const int slot = it % c.nstage;
     if (it >= c.nstage) {
       const bool got = mbar_wait(empty_bar(c, slot), (uint32_t)((it / c.nstage) - 1) & 1u, c.deadline);
@@ -220,13 +223,15 @@ __global__ void __launch_bounds__(dn::THREADS, 1) down_bf16_kernel(ExpertArgs a)
   c.stages_addr = smem_addr(smem);
   c.red = reinterpret_cast<float*>(smem + c.nstage * c.stage_bytes);
   c.acc = c.red + dn::RED_FLOATS;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(c.acc + B * dn::RS);
+  MetaSmem& meta = *reinterpret_cast<MetaSmem*>(c.acc + B * dn::RS);
+  float* pair_w_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pair_w_s + MAX_B * SLOTS);
   c.full0 = smem_addr(bars);
   c.empty0 = smem_addr(bars + dn::MAX_STAGES);
   c.hdr = a.ws.hdr;
   c.abort_flag = &s_abort;
-  c.pair_tok = a.ws.pair_tok;
-  c.pair_w = a.ws.pair_w;
+  c.pair_tok = meta.pair_tok;
+  c.pair_w = pair_w_s;
   if (threadIdx.x == 0) {
     for (int s = 0; s < c.nstage; ++s) {
       mbar_init(full_bar(c, s), 1);
@@ -237,19 +242,22 @@ __global__ void __launch_bounds__(dn::THREADS, 1) down_bf16_kernel(ExpertArgs a)
   }
   for (int i = threadIdx.x; i < B * dn::RS; i += blockDim.x) c.acc[i] = 0.f;
   __syncthreads();
-  pdl_wait();     // h comes from the gate/up kernel
-  pdl_trigger();
-  const int n_groups = (int)__ldcg(&a.ws.hdr->n_groups);
   const int r0 = blockIdx.x * dn::RS;
   c.deadline = wait_deadline(a.ws.hdr);
+  pdl_wait();     // h, the group table and the pairs come from the preceding kernels
   const int warp = threadIdx.x >> 5;
   if (warp == dn::CWARPS) {
-    if ((threadIdx.x & 31) == 0) produce(c, a.ws.groups, n_groups, a.w.w2, a.w.ws2, a.ws.h, r0);
+    named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
+    if ((threadIdx.x & 31) == 0) produce(c, meta.groups, meta.n_groups, a.w.w2, a.w.ws2, a.ws.h, r0);
     return;
   }
+  fill_meta(a, false, meta, pair_w_s, nullptr, nullptr);
+  pdl_trigger();
+  named_sync(2, ALL_THREADS);
+  const int n_groups = meta.n_groups;
   bool ok = true;
   for (int gi = 0; gi < n_groups; ++gi) {
-    const int4 grp = __ldcg(a.ws.groups + gi);
+    const int4 grp = meta.groups[gi];
     const int slot = gi % c.nstage;
     if (ok) ok = wait_full(c, slot, (uint32_t)(gi / c.nstage) & 1u);
     const uint8_t* st = c.stages + slot * c.stage_bytes;

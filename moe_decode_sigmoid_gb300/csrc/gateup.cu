@@ -1,7 +1,7 @@
 // gateup.cu — gathered gate/up GEMV with fused SiLU-and-mul, BF16 weights.
 //
-// For every (expert, token-range) group built by the router and every token t
-// in it:  h[pair(t), i] = silu(Wg[i] . x_t) * (Wu[i] . x_t),  i < 512, with
+// For every (expert, token-range) group of the routing and every token t in
+// it:  h[pair(t), i] = silu(Wg[i] . x_t) * (Wu[i] . x_t),  i < 512, with
 // silu(g) = g / (1 + exp(-g)) ("SiLU-and-mul": Flint on Intel Arc Pro B70,
 // "norm.py: Triton kernels that assumed CUDA").  Only the selected experts'
 // rows are read ("read only the selected experts' weights": vLLM Day-0 Support
@@ -14,10 +14,13 @@
 // Per CTA: 8 consumer warps + 1 producer warp.  The producer's elected lane
 // streams each unit as one 64 KiB stage -- two cp.async.bulk copies -- through
 // a 3-stage shared-memory ring with full/empty mbarriers, so 192 KiB per SM is
-// in flight.  Consumers, per group:
+// in flight.  The shared expert's units, which do not depend on routing, start
+// before the router has finished (programmatic dependent launch).  Consumers,
+// per group:
 //   <= 4 tokens (the batch-1/8 case): CUDA cores.  Warp w owns gate row w and
-//      up row w; the group's activations are staged once as fp32 in shared
-//      memory; each lane keeps one independent fp32 partial sum per 16-byte
+//      up row w; the group's bf16 activations are staged once in shared
+//      memory; products are formed by fma.rn.f32.bf16 (bf16 x bf16 is exact in
+//      fp32, accumulation in fp32), one independent partial sum per 16-byte
 //      chunk so the FMA chains overlap.
 //   5..24 tokens: mma.sync m16n8k16 (bf16 in, fp32 acc) with the 16 weight
 //      rows as M (8 gate + 8 up: the same thread then holds g and u) and the
@@ -27,6 +30,7 @@
 //      16-byte row chunks.
 // Every wait is bounded by the workspace's limit.
 #include "common.cuh"
+#include "expert_common.cuh"
 #include "kernels.h"
 
 namespace flint {
@@ -39,12 +43,14 @@ constexpr int UNITS = I / 8;                    // units per group
 constexpr int CWARPS = 8;
 constexpr int THREADS = CWARPS * 32 + 32;
 constexpr int CC_MAX = 4;
-// Shared buffer: tensor-core partial tiles, or the CUDA-core path's fp32
-// activations (CC_MAX x H floats).
-constexpr int RED_FLOATS = CWARPS * ROWS * GROUP_MAX;
-constexpr int XS_FLOATS = CC_MAX * H;
-constexpr int BUF_FLOATS = RED_FLOATS > XS_FLOATS ? RED_FLOATS : XS_FLOATS;
-constexpr size_t SMEM = (size_t)NSTAGE * STAGE_BYTES + BUF_FLOATS * 4 + 2 * NSTAGE * 8;
+// Shared buffer: tensor-core partial tiles, the CUDA-core path's bf16
+// activations, or the logits during local selection.
+constexpr int RED_BYTES = CWARPS * ROWS * GROUP_MAX * 4;
+constexpr int XS_BYTES = CC_MAX * H * 2;
+constexpr int LOGIT_BYTES = LOCAL_SELECT_MAX_B * E * 4;
+constexpr int BUF_BYTES = RED_BYTES > XS_BYTES ? (RED_BYTES > LOGIT_BYTES ? RED_BYTES : LOGIT_BYTES)
+                                               : (XS_BYTES > LOGIT_BYTES ? XS_BYTES : LOGIT_BYTES);
+constexpr size_t SMEM = (size_t)NSTAGE * STAGE_BYTES + BUF_BYTES + sizeof(MetaSmem) + 2 * NSTAGE * 8;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
 }  // namespace gu
 
@@ -57,7 +63,7 @@ struct GuCtx {
   uint32_t full0, empty0;
   uint64_t deadline;
   const uint16_t* x;
-  const int* pair_tok;
+  const int* pair_tok;  // shared memory
   float* h;
   WsHeader* hdr;
   volatile int* abort_flag;
@@ -75,36 +81,39 @@ __device__ __forceinline__ bool wait_full(const GuCtx& c, int slot, uint32_t par
   return false;
 }
 
-// 8 bf16 weights . 8 fp32 activations, as one short independent chain.
-__device__ __forceinline__ float dot8(const uint4& w, const float4& a, const float4& b) {
-  float s = bf_lo(w.x) * a.x;
-  s = fmaf(bf_hi(w.x), a.y, s);
-  s = fmaf(bf_lo(w.y), a.z, s);
-  s = fmaf(bf_hi(w.y), a.w, s);
-  s = fmaf(bf_lo(w.z), b.x, s);
-  s = fmaf(bf_hi(w.z), b.y, s);
-  s = fmaf(bf_lo(w.w), b.z, s);
-  s = fmaf(bf_hi(w.w), b.w, s);
+// sum of 8 bf16 products w[k] * x[k], one short chain of mixed-precision FMAs
+// (each product is exact in fp32; the sum is rounded in fp32).
+__device__ __forceinline__ float dot8_bf16(const uint4& w, const uint4& x) {
+  float s = 0.f;
+  asm("{ .reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n"
+      "  mov.b32 {a0, a1}, %1;\n  mov.b32 {a2, a3}, %2;\n"
+      "  mov.b32 {a4, a5}, %3;\n  mov.b32 {a6, a7}, %4;\n"
+      "  mov.b32 {b0, b1}, %5;\n  mov.b32 {b2, b3}, %6;\n"
+      "  mov.b32 {b4, b5}, %7;\n  mov.b32 {b6, b7}, %8;\n"
+      "  fma.rn.f32.bf16 %0, a0, b0, %0;\n  fma.rn.f32.bf16 %0, a1, b1, %0;\n"
+      "  fma.rn.f32.bf16 %0, a2, b2, %0;\n  fma.rn.f32.bf16 %0, a3, b3, %0;\n"
+      "  fma.rn.f32.bf16 %0, a4, b4, %0;\n  fma.rn.f32.bf16 %0, a5, b5, %0;\n"
+      "  fma.rn.f32.bf16 %0, a6, b6, %0;\n  fma.rn.f32.bf16 %0, a7, b7, %0; }"
+      : "+f"(s)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w));
   return s;
 }
 
 // CUDA-core segment: units [u0, u1) of one group with NTOK tokens.  The
-// group's activations are staged once as fp32 in shared memory (the buffer is
-// shared with the tensor-core reduction; segments are separated by consumer
-// barriers).
+// group's bf16 activations are staged once in shared memory (the buffer is
+// shared with the tensor-core reduction and the local selection; segments are
+// separated by consumer barriers).
 template <int NTOK>
 __device__ __forceinline__ void seg_cc(const GuCtx& c, int u0, int u1, int pair0, int tok_base,
                                        int& it, bool& ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float4* xs = reinterpret_cast<float4*>(c.buf);  // [NTOK][H/4]
-  named_sync(1, gu::CWARPS * 32);                  // previous segment is done with buf
+  uint4* xs = reinterpret_cast<uint4*>(c.buf);  // [NTOK][H/8]
+  named_sync(1, gu::CWARPS * 32);                // previous user of buf is done
 #pragma unroll
   for (int i = 0; i < NTOK; ++i) {
-    const int tok = tok_base >= 0 ? tok_base + i : __ldcg(c.pair_tok + pair0 + i);
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)tok * H) + threadIdx.x);
-    xs[i * (H / 4) + 2 * threadIdx.x] = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
-    xs[i * (H / 4) + 2 * threadIdx.x + 1] =
-        make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
+    const int tok = tok_base >= 0 ? tok_base + i : c.pair_tok[pair0 + i];
+    xs[i * (H / 8) + threadIdx.x] =
+        __ldg(reinterpret_cast<const uint4*>(c.x + (size_t)tok * H) + threadIdx.x);
   }
   named_sync(1, gu::CWARPS * 32);
   for (int u = u0; u < u1; ++u) {
@@ -131,11 +140,9 @@ __device__ __forceinline__ void seg_cc(const GuCtx& c, int u0, int u1, int pair0
           float pg[4], pu[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int ch = lane + 32 * (4 * half + j);
-            const float4 a = xs[i * (H / 4) + 2 * ch];
-            const float4 b = xs[i * (H / 4) + 2 * ch + 1];
-            pg[j] = dot8(wg[j], a, b);
-            pu[j] = dot8(wu[j], a, b);
+            const uint4 xv = xs[i * (H / 8) + lane + 32 * (4 * half + j)];
+            pg[j] = dot8_bf16(wg[j], xv);
+            pu[j] = dot8_bf16(wu[j], xv);
           }
           g[i] += (pg[0] + pg[1]) + (pg[2] + pg[3]);
           v[i] += (pu[0] + pu[1]) + (pu[2] + pu[3]);
@@ -160,13 +167,13 @@ __device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair
                                         int tok_base, int& it, bool& ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
-  named_sync(1, gu::CWARPS * 32);  // a preceding CUDA-core segment is done with buf
+  named_sync(1, gu::CWARPS * 32);  // the previous user of buf is done
   uint4 bfr[NT][8];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int slot = nt * 8 + g;
     if (slot < n) {
-      const int tok = tok_base >= 0 ? tok_base + slot : __ldcg(c.pair_tok + pair0 + slot);
+      const int tok = tok_base >= 0 ? tok_base + slot : c.pair_tok[pair0 + slot];
       const uint16_t* row = c.x + (size_t)tok * H + warp * 256 + q * 8;
 #pragma unroll
       for (int kb = 0; kb < 8; ++kb)
@@ -315,30 +322,6 @@ __device__ __forceinline__ SharedUnit shared_unit(int j, int B, int nsg) {
   return u;
 }
 
-__device__ __forceinline__ void produce(const GuCtx& c, const ExpertArgs& a, Plan& pl, bool early) {
-  int it = 0;
-  bool ok = true;
-  for (int j = blockIdx.x; ok && j < pl.nsu; j += gridDim.x) {
-    const SharedUnit su = shared_unit(j, a.B, pl.nsg);
-    ok = issue_unit(c, a.w.ws13 + (size_t)su.s * (2 * I) * H, su.blk, it);
-  }
-  pdl_wait();     // routing and buckets come from the router kernel
-  plan_post(pl, (int)__ldcg(&a.ws.hdr->n_groups), early);
-  int gi_cached = -1;
-  const uint16_t* base = nullptr;
-  for (int u = pl.r_begin; ok && u < pl.r_end; ++u) {
-    const int gi = u / gu::UNITS;
-    if (gi != gi_cached) {
-      const int4 grp = __ldcg(a.ws.groups + gi);
-      base = grp.x < E ? a.w.w13 + (size_t)grp.x * (2 * I) * H
-                       : a.w.ws13 + (size_t)(grp.x - E) * (2 * I) * H;
-      gi_cached = gi;
-    }
-    ok = issue_unit(c, base, u & (gu::UNITS - 1), it);
-  }
-  drain(c, it);
-}
-
 __device__ __forceinline__ void segment(const GuCtx& c, int u0, int u1, int pair0, int n,
                                         int tok_base, int& it, bool& ok) {
   if (n <= gu::CC_MAX) {
@@ -362,15 +345,17 @@ __device__ __forceinline__ void segment(const GuCtx& c, int u0, int u1, int pair
 __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
+  __shared__ LocalSelectSmem s_sel;
   GuCtx c;
   c.stages = smem;
   c.buf = reinterpret_cast<float*>(smem + gu::NSTAGE * gu::STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(c.buf + gu::BUF_FLOATS);
+  MetaSmem& meta = *reinterpret_cast<MetaSmem*>(smem + gu::NSTAGE * gu::STAGE_BYTES + gu::BUF_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
   c.stages_addr = smem_addr(smem);
   c.full0 = smem_addr(bars);
   c.empty0 = smem_addr(bars + gu::NSTAGE);
   c.x = a.x;
-  c.pair_tok = a.ws.pair_tok;
+  c.pair_tok = meta.pair_tok;
   c.h = a.ws.h;
   c.hdr = a.ws.hdr;
   c.abort_flag = &s_abort;
@@ -386,9 +371,33 @@ __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs 
   const bool early = a.early_shared != 0;
   Plan pl = plan_pre(a.B, early);
   c.deadline = wait_deadline(a.ws.hdr);
-  if ((threadIdx.x >> 5) == gu::CWARPS) {
-    if ((threadIdx.x & 31) == 0) produce(c, a, pl, early);
-    pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x >> 5) == gu::CWARPS) {  // producer warp (lane 0 issues)
+    int it = 0;
+    bool ok = true;
+    if (lane == 0)
+      for (int j = blockIdx.x; ok && j < pl.nsu; j += gridDim.x) {
+        const SharedUnit su = shared_unit(j, a.B, pl.nsg);
+        ok = issue_unit(c, a.w.ws13 + (size_t)su.s * (2 * I) * H, su.blk, it);
+      }
+    __syncwarp();
+    named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
+    if (lane == 0) {
+      plan_post(pl, meta.n_groups, early);
+      int gi_cached = -1;
+      const uint16_t* base = nullptr;
+      for (int u = pl.r_begin; ok && u < pl.r_end; ++u) {
+        const int gi = u / gu::UNITS;
+        if (gi != gi_cached) {
+          const int4 grp = meta.groups[gi];
+          base = grp.x < E ? a.w.w13 + (size_t)grp.x * (2 * I) * H
+                           : a.w.ws13 + (size_t)(grp.x - E) * (2 * I) * H;
+          gi_cached = gi;
+        }
+        ok = issue_unit(c, base, u & (gu::UNITS - 1), it);
+      }
+      drain(c, it);
+    }
     return;
   }
   int it = 0;
@@ -398,13 +407,16 @@ __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs 
     // unit numbers inside a segment only serve as block indices (u & 63)
     segment(c, su.blk, su.blk + 1, su.pair0, su.n, su.tok0, it, ok);
   }
-  pdl_wait();     // routing and buckets come from the router kernel
+  pdl_wait();     // the router's logits / routing
+  named_sync(1, gu::CWARPS * 32);  // the last segment is done with buf
+  fill_meta(a, a.local_select != 0, meta, nullptr, c.buf, &s_sel);
   pdl_trigger();  // the down kernel may start its prologue
-  plan_post(pl, (int)__ldcg(&a.ws.hdr->n_groups), early);
+  named_sync(2, ALL_THREADS);
+  plan_post(pl, meta.n_groups, early);
   int u = pl.r_begin;
   while (u < pl.r_end) {
     const int gi = u / gu::UNITS;
-    const int4 grp = __ldcg(a.ws.groups + gi);
+    const int4 grp = meta.groups[gi];
     const int u1 = min(pl.r_end, (gi + 1) * gu::UNITS);
     segment(c, u, u1, grp.y, grp.z, -1, it, ok);
     u = u1;

@@ -7,16 +7,9 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "select.cuh"
 
 namespace flint {
-
-// Optional plain description of the buckets (flint_moe_bucket).
-struct BucketOut {
-  int* uniq;     // [E]   distinct experts, ascending (first n_uniq valid)
-  int* offsets;  // [E+1] first pair of each, then B*TOPK
-  int* pairs;    // [B*TOPK] token*8 + slot, ordered by (expert, token)
-  int* n_uniq;   // [1]
-};
 
 struct RouterArgs {
   const uint16_t* x;   // [B,H] bf16
@@ -27,6 +20,7 @@ struct RouterArgs {
   int* user_idx;       // [B,TOPK] or null
   float* user_w;       // [B,TOPK] or null
   int do_bucket;       // build pairs/groups for the expert kernels
+  int logits_only;     // write logits only: the expert kernels select (batch <= 8)
   int stall_check;     // honour the workspace's one-shot stall hook
   BucketOut bucket;    // optional plain bucket outputs (all null to skip)
 };
@@ -53,7 +47,13 @@ struct ExpertArgs {
   int B;
   Ws ws;
   int early_shared;  // gate/up: start the shared expert before the router finishes
+  int local_select;  // gate/up: rank and bucket the batch in every CTA (batch <= 8)
+  int* user_idx;     // gate/up with local_select: optional routing copies
+  float* user_w;
 };
+
+// Largest batch whose routing the expert kernels compute themselves.
+constexpr int LOCAL_SELECT_MAX_B = 8;
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_bucket(const Ws& ws, int B, const BucketOut& user, cudaStream_t stream);

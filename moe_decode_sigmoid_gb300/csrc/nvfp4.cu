@@ -25,6 +25,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "expert_common.cuh"
 #include "kernels.h"
 
 namespace flint {
@@ -39,7 +40,10 @@ constexpr int GU_SFROW = H / 16;                     // 128 scale bytes per row
 constexpr int GU_STAGE = 16 * GU_QSTRIDE + 16 * GU_SFROW;  // 18,432
 constexpr int GU_NSTAGE = 10;
 constexpr int GU_RED = CWARPS * 16 * GROUP_MAX;
-constexpr size_t GU_SMEM = (size_t)GU_NSTAGE * GU_STAGE + GU_RED * 4 + 2 * GU_NSTAGE * 8;
+// The reduction buffer doubles as the logits buffer of the local selection.
+constexpr int GU_BUF = GU_RED * 4 > LOCAL_SELECT_MAX_B * E * 4 ? GU_RED * 4 : LOCAL_SELECT_MAX_B * E * 4;
+constexpr size_t GU_SMEM =
+    (size_t)GU_NSTAGE * GU_STAGE + GU_BUF + sizeof(MetaSmem) + 2 * GU_NSTAGE * 8;
 constexpr int UNITS = I / 8;
 // down
 constexpr int RS = 16;
@@ -54,7 +58,9 @@ constexpr int DN_MAX_STAGES = 8;
 constexpr int SMEM_CAP = 232448 - 1024;
 __host__ __device__ inline int dn_nmax(int B) { return B < GROUP_MAX ? B : GROUP_MAX; }
 __host__ __device__ inline int dn_stage(int B) { return DN_WBYTES + dn_nmax(B) * HSTRIDE; }
-__host__ __device__ inline int dn_fixed(int B) { return DN_RED * 4 + B * RS * 4 + 2 * DN_MAX_STAGES * 8; }
+__host__ __device__ inline int dn_fixed(int B) {
+  return DN_RED * 4 + B * RS * 4 + (int)sizeof(MetaSmem) + MAX_B * SLOTS * 4 + 2 * DN_MAX_STAGES * 8;
+}
 __host__ __device__ inline int dn_nstages(int B) {
   int n = (SMEM_CAP - dn_fixed(B)) / dn_stage(B);
   return n > DN_MAX_STAGES ? DN_MAX_STAGES : n;
@@ -189,7 +195,8 @@ __device__ __forceinline__ void init_pipe(Pipe& p, uint8_t* smem, int stage_byte
 // ---------------------------------------------------------------- gate/up
 
 template <int NT>
-__device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, float* red, int u0,
+__device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, const int* pair_tok,
+                                           float* red, int u0,
                                            int u1, int expert, int pair0, int n, int& it,
                                            bool& ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -204,7 +211,7 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, f
   for (int nt = 0; nt < NT; ++nt) {
     const int slot = nt * 8 + g;
     if (slot < n) {
-      const int tok = __ldcg(a.ws.pair_tok + pair0 + slot);
+      const int tok = pair_tok[pair0 + slot];
       const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)tok * H + warp * 256 + q * 32);
 #pragma unroll
       for (int m = 0; m < 2; ++m)
@@ -293,11 +300,12 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, f
   }
 }
 
-__device__ __forceinline__ void gu_produce(const Pipe& p, const ExpertArgs& a, int u_begin,
+__device__ __forceinline__ void gu_produce(const Pipe& p, const ExpertArgs& a, const int4* groups,
+                                           int u_begin,
                                            int u_end) {
   int it = 0;
   for (int u = u_begin; u < u_end; ++u) {
-    const int4 grp = __ldcg(a.ws.groups + (u / f4::UNITS));
+    const int4 grp = groups[u / f4::UNITS];
     const int blk = u & (f4::UNITS - 1);
     const bool routed = grp.x < E;
     const int e = routed ? grp.x : grp.x - E;
@@ -322,7 +330,8 @@ __device__ __forceinline__ void gu_produce(const Pipe& p, const ExpertArgs& a, i
 // ---------------------------------------------------------------- down
 
 template <int NT>
-__device__ __forceinline__ void dn_group(const ExpertArgs& a, const uint8_t* st, float* red,
+__device__ __forceinline__ void dn_group(const ExpertArgs& a, const int* pair_tok,
+                                         const float* pair_w, const uint8_t* st, float* red,
                                          float* acc_s, int expert, int pair0, int n) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
@@ -384,18 +393,19 @@ __device__ __forceinline__ void dn_group(const ExpertArgs& a, const uint8_t* st,
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < f4::CWARPS; ++w) s += red[(w * f4::RS + r) * GROUP_MAX + j];
-    const int t = __ldcg(a.ws.pair_tok + pair0 + j);
-    const float wt = __ldcg(a.ws.pair_w + pair0 + j);
+    const int t = pair_tok[pair0 + j];
+    const float wt = pair_w[pair0 + j];
     acc_s[t * f4::RS + r] += wt * (s * ts);
   }
   named_sync(1, f4::CWARPS * 32);
 }
 
-__device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, int n_groups,
+__device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, const int4* groups,
+                                           int n_groups,
                                            int r0) {
   int it = 0;
   for (int gi = 0; gi < n_groups; ++gi) {
-    const int4 grp = __ldcg(a.ws.groups + gi);
+    const int4 grp = groups[gi];
     if (!acquire_stage(p, it)) break;
     const int slot = it % p.nstage;
     const int n = grp.z;
@@ -418,32 +428,41 @@ __device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, i
 __global__ void __launch_bounds__(f4::THREADS, 1) gateup_nvfp4_kernel(ExpertArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
+  __shared__ LocalSelectSmem s_sel;
   float* red = reinterpret_cast<float*>(smem + f4::GU_NSTAGE * f4::GU_STAGE);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red + f4::GU_RED);
+  MetaSmem& meta = *reinterpret_cast<MetaSmem*>(reinterpret_cast<uint8_t*>(red) + f4::GU_BUF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
   Pipe p;
   init_pipe(p, smem, f4::GU_STAGE, f4::GU_NSTAGE, bars, f4::GU_NSTAGE, &s_abort, a.ws.hdr);
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();
-  const int n_units = (int)__ldcg(&a.ws.hdr->n_groups) * f4::UNITS;
-  const int u_begin = (int)((long long)blockIdx.x * n_units / gridDim.x);
-  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
   p.deadline = wait_deadline(a.ws.hdr);
+  pdl_wait();     // the router's logits / routing
   if ((threadIdx.x >> 5) == f4::CWARPS) {
-    if ((threadIdx.x & 31) == 0) gu_produce(p, a, u_begin, u_end);
+    named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
+    if ((threadIdx.x & 31) == 0) {
+      const int n_units = meta.n_groups * f4::UNITS;
+      gu_produce(p, a, meta.groups, (int)((long long)blockIdx.x * n_units / gridDim.x),
+                 (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x));
+    }
     return;
   }
+  fill_meta(a, a.local_select != 0, meta, nullptr, red, &s_sel);
+  pdl_trigger();
+  named_sync(2, ALL_THREADS);
+  const int n_units = meta.n_groups * f4::UNITS;
+  const int u_begin = (int)((long long)blockIdx.x * n_units / gridDim.x);
+  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
   int it = 0;
   bool ok = true;
   int u = u_begin;
   while (u < u_end) {
     const int gi = u / f4::UNITS;
-    const int4 grp = __ldcg(a.ws.groups + gi);
+    const int4 grp = meta.groups[gi];
     const int u1 = min(u_end, (gi + 1) * f4::UNITS);
     switch ((grp.z + 7) >> 3) {
-      case 1: gu_segment<1>(p, a, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
-      case 2: gu_segment<2>(p, a, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
-      default: gu_segment<3>(p, a, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+      case 1: gu_segment<1>(p, a, meta.pair_tok, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+      case 2: gu_segment<2>(p, a, meta.pair_tok, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+      default: gu_segment<3>(p, a, meta.pair_tok, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
     }
     u = u1;
   }
@@ -456,31 +475,36 @@ __global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a
   const int nstage = f4::dn_nstages(B), stage = f4::dn_stage(B);
   float* red = reinterpret_cast<float*>(smem + nstage * stage);
   float* acc = red + f4::DN_RED;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(acc + B * f4::RS);
+  MetaSmem& meta = *reinterpret_cast<MetaSmem*>(acc + B * f4::RS);
+  float* pair_w_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pair_w_s + MAX_B * SLOTS);
   Pipe p;
   init_pipe(p, smem, stage, nstage, bars, f4::DN_MAX_STAGES, &s_abort, a.ws.hdr);
   for (int i = threadIdx.x; i < B * f4::RS; i += blockDim.x) acc[i] = 0.f;
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();
-  const int n_groups = (int)__ldcg(&a.ws.hdr->n_groups);
   const int r0 = blockIdx.x * f4::RS;
   p.deadline = wait_deadline(a.ws.hdr);
+  pdl_wait();     // h, the group table and the pairs come from the preceding kernels
   if ((threadIdx.x >> 5) == f4::CWARPS) {
-    if ((threadIdx.x & 31) == 0) dn_produce(p, a, n_groups, r0);
+    named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
+    if ((threadIdx.x & 31) == 0) dn_produce(p, a, meta.groups, meta.n_groups, r0);
     return;
   }
+  fill_meta(a, false, meta, pair_w_s, nullptr, nullptr);
+  pdl_trigger();
+  named_sync(2, ALL_THREADS);
+  const int n_groups = meta.n_groups;
   bool ok = true;
   for (int gi = 0; gi < n_groups; ++gi) {
-    const int4 grp = __ldcg(a.ws.groups + gi);
+    const int4 grp = meta.groups[gi];
     const int slot = gi % nstage;
     if (ok) ok = wait_full(p, slot, (uint32_t)(gi / nstage) & 1u);
     const uint8_t* st = p.stages + slot * stage;
     const int n = ok ? grp.z : 0;
     switch ((grp.z + 7) >> 3) {  // uniform across the consumer warps
-      case 1: dn_group<1>(a, st, red, acc, grp.x, grp.y, n); break;
-      case 2: dn_group<2>(a, st, red, acc, grp.x, grp.y, n); break;
-      default: dn_group<3>(a, st, red, acc, grp.x, grp.y, n); break;
+      case 1: dn_group<1>(a, meta.pair_tok, pair_w_s, st, red, acc, grp.x, grp.y, n); break;
+      case 2: dn_group<2>(a, meta.pair_tok, pair_w_s, st, red, acc, grp.x, grp.y, n); break;
+      default: dn_group<3>(a, meta.pair_tok, pair_w_s, st, red, acc, grp.x, grp.y, n); break;
     }
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar(p, slot));

@@ -1,0 +1,195 @@
+// select.cuh — sigmoid top-k selection and token-to-expert bucketing, used by
+// the router kernel and, for small batches, inside the expert kernels.
+//
+// "256 experts, employing a sigmoid top-6 selection mechanism plus a shared
+// expert" (vLLM Day-0 Support for Recursive's Flint, "Flint Model
+// Architecture").  Experts are ranked by (logit descending, index ascending);
+// the weights are the selected sigmoids divided by their sum.
+#pragma once
+
+#include "common.cuh"
+
+namespace flint {
+
+// Order-preserving map of fp32 onto uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t f2key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-k of one token's E logits by one warp.  Lane l holds experts l + 32 j.
+// Each round takes the largest remaining logit; among equal logits the lowest
+// expert index wins (first within a lane by ascending j, then across lanes by
+// the minimum index).  Lanes 0..k-1 return slot `lane`'s expert and weight.
+template <bool GLOBAL_SRC>
+__device__ __forceinline__ void topk_warp(const float* logits_row, int& idx_out, float& w_out) {
+  const int lane = threadIdx.x & 31;
+  float v[E / 32];
+#pragma unroll
+  for (int j = 0; j < E / 32; ++j)
+    v[j] = GLOBAL_SRC ? __ldcg(logits_row + lane + 32 * j) : logits_row[lane + 32 * j];
+  uint32_t taken = 0;
+  int sel_e[TOPK];
+  float sel_v[TOPK];
+#pragma unroll
+  for (int r = 0; r < TOPK; ++r) {
+    uint32_t best_key = 0;
+    uint32_t best_e = 0xffffffffu;
+#pragma unroll
+    for (int j = 0; j < E / 32; ++j) {
+      const uint32_t k = f2key(v[j]);
+      const bool free_j = !((taken >> j) & 1u);
+      if (free_j && (best_e == 0xffffffffu || k > best_key)) {
+        best_key = k;
+        best_e = (uint32_t)(lane + 32 * j);
+      }
+    }
+    const uint32_t top = __reduce_max_sync(0xffffffffu, best_key);
+    const uint32_t win = __reduce_min_sync(0xffffffffu, best_key == top ? best_e : 0xffffffffu);
+    if ((int)(win & 31u) == lane) taken |= 1u << (win >> 5);
+    sel_e[r] = (int)win;
+    sel_v[r] = key2f(top);
+  }
+  float s[TOPK], ssum = 0.f;
+#pragma unroll
+  for (int r = 0; r < TOPK; ++r) {
+    s[r] = 1.0f / (1.0f + expf(-sel_v[r]));
+    ssum += s[r];
+  }
+  idx_out = 0;
+  w_out = 0.f;
+#pragma unroll
+  for (int r = 0; r < TOPK; ++r)
+    if (r == lane) {
+      idx_out = sel_e[r];
+      w_out = s[r] / ssum;
+    }
+}
+
+// Optional plain description of the buckets (flint_moe_bucket).
+struct BucketOut {
+  int* uniq;     // [E]   distinct experts, ascending (first n_uniq valid)
+  int* offsets;  // [E+1] first pair of each, then B*TOPK
+  int* pairs;    // [B*TOPK] token*8 + slot, ordered by (expert, token)
+  int* n_uniq;   // [1]
+};
+
+// Where the buckets go: pairs (routed ones ordered by (expert, token), then
+// the shared experts' pairs in token order with weight 1) and the group table
+// (expert, first pair, count <= GROUP_MAX), routed groups first.
+struct BucketDst {
+  int* pair_tok;
+  float* pair_w;   // may be null
+  int4* groups;
+  int* n_groups;   // [1]
+  int* n_uniq;     // [1] or null
+};
+
+// Scratch for bucket_cta, MW = 32-bit words of token mask per expert.
+template <int MW>
+struct BucketScratch {
+  uint32_t mask[E][MW];
+  int off[E];
+  int warp_tot[8];
+};
+
+// Exclusive scan of one int per thread over 256 threads; `sync` is the
+// barrier all 256 threads take.
+template <typename Sync>
+__device__ __forceinline__ int scan256(int v, int* warp_tot, int* total, Sync sync) {
+  const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) & 7;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  sync();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int c = warp_tot[w];
+    if (w < warp) base += c;
+    tot += c;
+  }
+  sync();
+  *total = tot;
+  return base + incl - v;
+}
+
+// Buckets a batch's (token, slot) pairs by expert, by 256 threads (thread e
+// owns expert e).  The routing is read from src_idx / src_w ([B, TOPK], shared
+// or global memory).  Each pair's position is its expert's offset plus the
+// number of the expert's tokens below it (popcount of the token mask), so the
+// order is deterministic.  Indices outside [0, E) or repeated within a token
+// are reported through `bad` and skipped.
+template <int MW, bool GLOBAL_SRC, typename Sync>
+__device__ void bucket_cta(int B, const int* src_idx, const float* src_w, BucketDst dst,
+                           BucketOut user, BucketScratch<MW>& sc, bool& bad, Sync sync) {
+  const int tid = threadIdx.x & 255;
+  for (int i = tid; i < E * MW; i += 256) (&sc.mask[0][0])[i] = 0u;
+  sync();
+  const int npairs = B * TOPK;
+  for (int p = tid; p < npairs; p += 256) {
+    const int e = GLOBAL_SRC ? __ldcg(src_idx + p) : src_idx[p];
+    const int t = p / TOPK;
+    if (e < 0 || e >= E) {
+      bad = true;
+      continue;
+    }
+    const uint32_t bit = 1u << (t & 31);
+    if (atomicOr(&sc.mask[e][t >> 5], bit) & bit) bad = true;
+  }
+  sync();
+  const int e = tid;
+  int cnt = 0;
+#pragma unroll
+  for (int w = 0; w < MW; ++w) cnt += __popc(sc.mask[e][w]);
+  const int ng = (cnt + GROUP_MAX - 1) / GROUP_MAX;
+  int tot_pairs, tot_groups, n_uniq;
+  const int off = scan256(cnt, sc.warp_tot, &tot_pairs, sync);
+  const int goff = scan256(ng, sc.warp_tot, &tot_groups, sync);
+  const int urank = scan256(cnt > 0 ? 1 : 0, sc.warp_tot, &n_uniq, sync);
+  sc.off[e] = off;
+  for (int gi = 0; gi < ng; ++gi)
+    dst.groups[goff + gi] = make_int4(e, off + gi * GROUP_MAX, min(GROUP_MAX, cnt - gi * GROUP_MAX), 0);
+  if (user.uniq && cnt > 0) {
+    user.uniq[urank] = e;
+    user.offsets[urank] = off;
+  }
+  sync();
+  for (int p = tid; p < npairs; p += 256) {
+    const int ex = GLOBAL_SRC ? __ldcg(src_idx + p) : src_idx[p];
+    if (ex < 0 || ex >= E) continue;
+    const int t = p / TOPK;
+    const int wd = t >> 5;
+    int rank = __popc(sc.mask[ex][wd] & ((1u << (t & 31)) - 1u));
+    for (int w = 0; w < wd; ++w) rank += __popc(sc.mask[ex][w]);
+    const int pos = sc.off[ex] + rank;
+    dst.pair_tok[pos] = t;
+    if (dst.pair_w) dst.pair_w[pos] = GLOBAL_SRC ? __ldcg(src_w + p) : src_w[p];
+    if (user.pairs) user.pairs[pos] = t * 8 + (p - t * TOPK);
+  }
+  const int nsg = (B + GROUP_MAX - 1) / GROUP_MAX;
+  for (int i = tid; i < S * B; i += 256) {
+    dst.pair_tok[npairs + i] = i % B;
+    if (dst.pair_w) dst.pair_w[npairs + i] = 1.0f;
+  }
+  for (int i = tid; i < S * nsg; i += 256) {
+    const int s = i / nsg, gi = i % nsg;
+    dst.groups[tot_groups + i] =
+        make_int4(E + s, npairs + s * B + gi * GROUP_MAX, min(GROUP_MAX, B - gi * GROUP_MAX), 0);
+  }
+  if (tid == 0) {
+    *dst.n_groups = tot_groups + S * nsg;
+    if (dst.n_uniq) *dst.n_uniq = n_uniq;
+    if (user.offsets) user.offsets[n_uniq] = npairs;
+    if (user.n_uniq) *user.n_uniq = n_uniq;
+  }
+}
+
+}  // namespace flint

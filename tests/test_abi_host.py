@@ -80,8 +80,8 @@ def test_decode_rejects_bad_arguments_before_launch(L):
     assert _decode(L, x=None) == m.FLINT_ERR_INVALID_ARG
     assert _decode(L, x=A + 2) == m.FLINT_ERR_INVALID_ARG            # misaligned
     assert _decode(L, w13=None) == m.FLINT_ERR_INVALID_ARG
-    assert _decode(L, bias=A + 4) == m.FLINT_ERR_INVALID_ARG         # misaligned optional
-    assert _decode(L, idx=A + 8) == m.FLINT_ERR_INVALID_ARG
+    assert _decode(L, bias=A + 2) == m.FLINT_ERR_INVALID_ARG         # misaligned optional
+    assert _decode(L, idx=A + 6) == m.FLINT_ERR_INVALID_ARG
     assert _decode(L, ws=None) == m.FLINT_ERR_WORKSPACE
     assert _decode(L, ws=WS + 8) == m.FLINT_ERR_WORKSPACE
     assert _decode(L, batch=8, wsb=m.flint_moe_workspace_bytes(4)) == m.FLINT_ERR_WORKSPACE
