@@ -25,8 +25,6 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Required pointer: non-null and 16-byte aligned.
 bool req(const void* p) { return p != nullptr && aligned16(p); }
-// Optional pointer: null, or 16-byte aligned.
-bool opt(const void* p) { return p == nullptr || aligned16(p); }
 // Small fp32 / int32 vectors (offsets, routing outputs): 4-byte alignment.
 bool req4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool opt4(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -190,8 +188,6 @@ static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const vo
   // and buckets the tokens itself, which takes the router's serial tail off
   // the critical path.
   r.logits_only = batch <= LOCAL_SELECT_MAX_B ? 1 : 0;
-  cudaError_t e = launch_router(r, stream, true);
-  if (e != cudaSuccess) return cuda_status(e);
   ExpertArgs a = {};
   a.x = r.x;
   a.residual = static_cast<const uint16_t*>(residual);
@@ -206,6 +202,10 @@ static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const vo
   a.local_select = r.logits_only;
   a.user_idx = idx_out;
   a.user_w = w_out;
+  if (!nvfp4 && batch <= LOCAL_SELECT_MAX_B)  // one persistent kernel for the whole layer
+    return cuda_status(launch_small_bf16(a, r, stream, sms));
+  cudaError_t e = launch_router(r, stream, true);
+  if (e != cudaSuccess) return cuda_status(e);
   e = nvfp4 ? launch_gateup_nvfp4(a, stream, sms) : launch_gateup_bf16(a, stream, sms);
   if (e != cudaSuccess) return cuda_status(e);
   e = nvfp4 ? launch_down_nvfp4(a, stream) : launch_down_bf16(a, stream);

@@ -43,7 +43,8 @@ struct WsHeader {
   uint32_t stall_armed;      // test hook: one-shot wait on stall_release
   uint32_t stall_release;    // never written by the library
   uint32_t tile_ctas_done[MAX_B / 8];  // router: finished CTAs per token tile
-  uint32_t pad[24];
+  uint32_t grid_bar[3];      // fused kernel: two grid barriers and an exit count
+  uint32_t pad[21];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
