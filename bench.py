@@ -41,6 +41,7 @@ L2_FLUSH_BYTES = 512 << 20
 SPACER_CYCLES = 100_000
 FALLBACK_HBM_GBS = 6800.0
 LAYER_SEED, TOKEN_SEED, OFFSET_SEED = 1001, 2000, 1003
+SMALL_BATCH_MAX = 8      # batches the library runs as one persistent kernel
 
 
 def needed_bytes_bf16(U: int) -> int:
@@ -370,18 +371,18 @@ def run_ours(args, world, rank, local, barrier):
 
     roof_steps = min(args.steps, 400)
     kern = stage_times(m, L, roof_steps, max(3, args.warmup // 4), stream)
-    gate_bytes = (U + 1) * GATEUP_BYTES_BF16 + B * 2048 * 2 + 7 * B * 512 * 4
-    achieved = gate_bytes / (kern["gateup"]["mean"] * 1e-6) / 1e9
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "gateup_bf16_traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            with open(tr_path) as f:
-                tr = json.load(f)
-            if tr.get("batch") == B and tr.get("kernel_sha") == kernel_sha():
-                traffic = tr.get("traffic_bytes")
-        except Exception:
-            traffic = None
+    if B <= SMALL_BATCH_MAX:
+        # The whole layer is one launch of the persistent kernel: the per-step
+        # events time exactly that kernel on its stream.
+        roof_kernel = "moe_small_bf16_kernel"
+        alg_bytes = nb + 3 * B * 2048 * 2          # weights + x, residual, out
+        dur_us = st["mean"]
+    else:
+        roof_kernel = "gateup_bf16_kernel"
+        alg_bytes = (U + 1) * GATEUP_BYTES_BF16 + B * 2048 * 2 + 7 * B * 512 * 4
+        dur_us = kern["gateup"]["mean"]
+    achieved = alg_bytes / (dur_us * 1e-6) / 1e9
+    traffic = recorded_traffic(roof_kernel, B)
 
     e2e_times, h2d, d2h = e2e_measure(m, L, min(args.steps, 1000), max(3, args.warmup // 4),
                                       stream)
@@ -406,7 +407,8 @@ def run_ours(args, world, rank, local, barrier):
                         "unit-RMS N(0,1) tokens" % B,
             "batch": B, "unique_experts": U, "needed_bytes": nb,
             "l2": cold.describe(),
-            "timing": "CUDA-graph replay of the 3-kernel layer, CUDA events per step",
+            "timing": "CUDA-graph replay of the layer (%s), CUDA events per step"
+                      % ("one persistent kernel" if B <= SMALL_BATCH_MAX else "3 kernels"),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "us_per_layer": round(st["mean"], 3),
@@ -414,14 +416,15 @@ def run_ours(args, world, rank, local, barrier):
         "frac_of_peak": round(nb / (st["mean"] * 1e-6) / 1e9 / peak, 4),
         "peak_gbs": peak, "peak_kind": peak_kind,
         "kernels_us": {k: round(v["mean"], 3) for k, v in kern.items()},
-        "roofline": {"bound": "hbm", "kernel": "gateup_bf16_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": roof_kernel, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes": gate_bytes,
+                     "traffic": traffic, "algorithmic_bytes": alg_bytes,
+                     "launch_us": round(dur_us, 3),
                      "note": "peak = %s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind},
         "e2e": {"value": round(world * nb / (e2e_t * 1e-6) / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(e2e_t, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (1 if B <= SMALL_BATCH_MAX else 3) * args.steps,
         "clocks": clocks,
         "wall_s_timed": round(wall, 4),
     }
@@ -544,13 +547,30 @@ def stack_configs(m, stream, warmup, steps=20):
     return out
 
 
-def kernel_sha() -> str:
+def sources_sha() -> str:
+    """Hash of the CUDA sources: recorded ncu traffic only counts while it matches."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("gateup.cu", "common.cuh"):
-        with open(os.path.join(ROOT, "moe_decode_sigmoid_gb300", "csrc", name), "rb") as f:
+    csrc = os.path.join(ROOT, "moe_decode_sigmoid_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, batch: int):
+    """dram bytes (read + write) per launch from profiles/traffic.json, or None
+    when no capture matches this kernel, batch and source revision."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get("%s_b%d" % (kernel, batch))
+        if rec and rec.get("sources_sha") == sources_sha():
+            return rec.get("traffic_bytes")
+    except Exception:
+        pass
+    return None
 
 
 def run_reference(args, world, rank):

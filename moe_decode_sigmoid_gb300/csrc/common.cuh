@@ -43,10 +43,12 @@ struct WsHeader {
   uint32_t stall_armed;      // test hook: one-shot wait on stall_release
   uint32_t stall_release;    // never written by the library
   uint32_t tile_ctas_done[MAX_B / 8];  // router: finished CTAs per token tile
-  uint32_t grid_bar[3];      // fused kernel: two grid barriers and an exit count
-  uint32_t pad[21];
+  uint32_t grid_bar[3];      // fused kernel: logits barrier, (unused), exit count
+  uint32_t unit_next;        // fused kernel: next unclaimed gate/up unit
+  uint32_t pad[20];
+  uint32_t group_done[64];   // fused kernel: finished (unit, warp) parts per group
 };
-static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+static_assert(sizeof(WsHeader) == 512, "header is 512 bytes");
 
 __host__ __device__ constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 

@@ -46,7 +46,14 @@ __device__ __forceinline__ void fill_meta(const ExpertArgs& a, bool local, MetaS
   const int tid = threadIdx.x;
   const int B = a.B;
   if (local) {
-    for (int i = tid; i < B * E; i += CONSUMER_THREADS) logits_buf[i] = __ldcg(a.ws.logits + i);
+    // thread e loads expert e's logit of every token (all loads in flight at once)
+    float lv[LOCAL_SELECT_MAX_B];
+#pragma unroll
+    for (int t = 0; t < LOCAL_SELECT_MAX_B; ++t)
+      lv[t] = t < B ? __ldcg(a.ws.logits + (size_t)t * E + tid) : 0.f;
+#pragma unroll
+    for (int t = 0; t < LOCAL_SELECT_MAX_B; ++t)
+      if (t < B) logits_buf[t * E + tid] = lv[t];
     named_sync(1, CONSUMER_THREADS);
     const int warp = tid >> 5, lane = tid & 31;
     if (warp < B) {
@@ -88,11 +95,38 @@ __device__ __forceinline__ void fill_meta(const ExpertArgs& a, bool local, MetaS
       if (tid == 0) a.ws.hdr->n_groups = (uint32_t)n;
     }
   } else {
+    // Loads first, stores after, so the round trips overlap (the loop bounds
+    // are at most MAX_GROUPS and MAX_B * SLOTS).
     const int n = (int)__ldcg(&a.ws.hdr->n_groups);
-    for (int i = tid; i < n; i += CONSUMER_THREADS) m.groups[i] = __ldcg(a.ws.groups + i);
-    for (int i = tid; i < B * SLOTS; i += CONSUMER_THREADS) {
-      m.pair_tok[i] = __ldcg(a.ws.pair_tok + i);
-      if (pair_w) pair_w[i] = __ldcg(a.ws.pair_w + i);
+    constexpr int GR = (MAX_GROUPS + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
+    constexpr int PR = (MAX_B * SLOTS + CONSUMER_THREADS - 1) / CONSUMER_THREADS;
+    int4 gv[GR];
+    int tv[PR];
+    float wv[PR];
+#pragma unroll
+    for (int k = 0; k < GR; ++k) {
+      const int i = tid + k * CONSUMER_THREADS;
+      gv[k] = i < n ? __ldcg(a.ws.groups + i) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < PR; ++k) {
+      const int i = tid + k * CONSUMER_THREADS;
+      const bool in = i < B * SLOTS;
+      tv[k] = in ? __ldcg(a.ws.pair_tok + i) : 0;
+      wv[k] = in && pair_w ? __ldcg(a.ws.pair_w + i) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < GR; ++k) {
+      const int i = tid + k * CONSUMER_THREADS;
+      if (i < n) m.groups[i] = gv[k];
+    }
+#pragma unroll
+    for (int k = 0; k < PR; ++k) {
+      const int i = tid + k * CONSUMER_THREADS;
+      if (i < B * SLOTS) {
+        m.pair_tok[i] = tv[k];
+        if (pair_w) pair_w[i] = wv[k];
+      }
     }
     if (tid == 0) m.n_groups = n;
   }

@@ -4,22 +4,38 @@
 // the neighbouring GEMVs ("Low-Latency Decode Path": vLLM Day-0 Support for
 // Recursive's Flint, "Optimization Strategies").
 //
-// One CTA per SM (cooperative launch, so all CTAs are co-resident), 8 consumer
-// warps + 1 producer warp, the gate/up kernel's shared-memory layout:
-//   1. router: each CTA dots its 1-2 router rows with the batch and writes the
-//      logits; meanwhile the producer streams the shared expert's gate/up
-//      units, which do not depend on routing, and the consumers compute them.
-//   2. grid barrier 1 (logits complete); every CTA ranks and buckets the
-//      batch itself in shared memory (identical results in every CTA).
-//   3. gate/up of the routed units, split evenly over the CTAs; while these
-//      stream, the producer also prefetches into L2 the down-projection rows
-//      its CTA will need (cp.async.bulk.prefetch.L2).
-//   4. grid barrier 2 (all h written).  CTAs 0..127 then run the row-slice-major
-//      down projection + combine + shared expert + residual over their 16
-//      output rows: the Wd slices are copied into the (now free) ring right
-//      after the CTA's last gate/up unit, the h rows only after the barrier.
-// The grid barriers are arrive/wait pairs on workspace counters with bounded
-// spins; the last CTA to finish resets them.
+// One CTA per SM (its shared memory admits no second CTA, so the #SMs CTAs are
+// all resident), 8 consumer warps + 1 producer warp.  The producer's lane 0
+// feeds a ring of 32 KiB shared-memory slots with cp.async.bulk copies and
+// tags each slot with what it holds; the consumers take the slots in order.
+//
+//   1. Router: the consumers dot the CTA's 1-2 router rows with the batch and
+//      write the logits; one grid-wide arrive.  Meanwhile the producer streams
+//      shared-expert gate/up units, which do not depend on routing.
+//   2. Work queue: gate/up units (8 gate + 8 up rows of one group, two slots)
+//      are claimed one at a time from a workspace counter -- the shared
+//      expert's 64 units first, then the routed groups' in group order -- so
+//      CTAs that stream faster take more units and groups finish roughly in
+//      order.  The first claim past the shared units makes the producer post a
+//      SELECT slot: the consumers wait for every CTA's logits, rank and bucket
+//      the batch in shared memory (identical in every CTA) and hand the group
+//      table to the producer.
+//   3. Completion counters: after storing its h values of a unit, each
+//      consumer warp adds 1 to its group's counter (release); the add is
+//      deferred until the warp's next unit is computed or the warp runs idle,
+//      so the fence finds the stores already done.  64 units x 8 warps = 512
+//      marks a group's h complete.
+//   4. Down: CTA b < 128 owns output rows [16b, 16b+16) of every token.  As
+//      soon as a group is complete (acquire), its producer posts a DOWN slot:
+//      the 16 rows of the expert's Wd (16 KiB) and the group's h rows, and the
+//      consumers accumulate w(t, g) * (Wd h) per token.  Down slots take
+//      priority over gate/up units, so the down projection streams while
+//      gate/up is still running instead of after a grid barrier.  The shared
+//      expert is accumulated separately and added last, so every token's sum
+//      runs in the group table's order (routed groups by expert, shared last)
+//      exactly as in the three-kernel path.
+// Every wait is bounded by the workspace's limit; the last CTA out resets the
+// workspace counters for the next call.
 #include "common.cuh"
 #include "down_impl.cuh"
 #include "expert_common.cuh"
@@ -28,33 +44,78 @@
 
 namespace flint {
 namespace fz {
-constexpr int THREADS = gu::THREADS;
-constexpr int DN_NSTAGE = 6;
-constexpr int DN_STAGE = dn::WBYTES + LOCAL_SELECT_MAX_B * dn::HROW;  // 32 KiB
-static_assert(DN_NSTAGE * DN_STAGE <= gu::NSTAGE * gu::STAGE_BYTES, "down stages overlay the ring");
-static_assert(dn::RED_FLOATS * 4 <= gu::BUF_BYTES, "down reduction fits in the shared buffer");
-constexpr int DOWN_CTAS = H / dn::RS;
-constexpr size_t SMEM = gu::SMEM;
+constexpr int CW = 8;                          // consumer warps
+constexpr int THREADS = (CW + 2) * 32;         // + producer warp + signalling warp
+constexpr int CT = CW * 32;                    // consumer threads
+constexpr int SLOT = 32 * 1024;                // ring slot bytes
+constexpr int NS = 5;                          // ring slots
+constexpr int ROWB = H * 2;                    // one gate/up row (bf16), 4 KiB
+constexpr int UNITS = I / 8;                   // gate/up units per group
+constexpr int MAXB = LOCAL_SELECT_MAX_B;
+constexpr int MAXG = MAXB * TOPK + S;          // groups at these batches (one shared group)
+constexpr int NPAIR = MAXB * SLOTS;
+constexpr int DONE_SHARED = 63;                // counter slot of the shared group
+constexpr uint32_t DONE_TARGET = UNITS;        // finished units per group
+constexpr int SIGQ = 8;                        // finished units in flight to the signalling warp
+constexpr int DOWN_CTAS = H / dn::RS;          // 128 row-slice owners
+constexpr int XS_BYTES = MAXB * H * 2;         // bf16 activations of the batch, 32 KiB
+constexpr int RED_BYTES = CW * 16 * GROUP_MAX * 4;
+constexpr int LOGIT_BYTES = MAXB * E * 4;
+constexpr int BUF_BYTES = RED_BYTES > LOGIT_BYTES ? RED_BYTES : LOGIT_BYTES;
+constexpr size_t SMEM = (size_t)NS * SLOT + XS_BYTES + BUF_BYTES;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
+enum : int { IT_GATE = 0, IT_UP = 1, IT_DOWN = 2, IT_SELECT = 3, IT_END = 4 };
+static_assert(S == 1 && MAXB <= GROUP_MAX, "one shared group at these batches");
+static_assert(MAXG <= DONE_SHARED, "routed groups and the shared group have distinct counters");
+static_assert(dn::WBYTES + MAXB * dn::HROW <= SLOT, "a down item fits one slot");
+static_assert(8 * ROWB == SLOT, "8 gate (or up) rows fill one slot");
+static_assert(dn::RED_FLOATS * 4 <= BUF_BYTES, "down partial tiles fit the buffer");
 }  // namespace fz
 
 namespace {
+
+// What a ring slot holds (written by the producer before it arms the slot).
+struct Item {
+  int kind;
+  int blk;       // gate/up: block of 8 intermediate rows
+  int pair0;     // first h row (pair) of the group
+  int n;         // tokens in the group
+  int tok0;      // gate/up of the shared group: first token (tokens are consecutive), else -1
+  int done_idx;  // completion counter of the group
+  int shared;    // down: the shared expert (accumulated separately)
+  int pad;
+};
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-
-// Grid-wide barrier halves; all CTAs are co-resident (cooperative launch).
-__device__ __forceinline__ void grid_arrive(uint32_t* ctr) {
-  __threadfence();
-  atomicAdd(ctr, 1u);
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void red_add_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ bool grid_wait(const uint32_t* ctr, uint32_t target, uint64_t deadline) {
   while (ld_acquire(ctr) < target)
     if (globaltimer_ns() > deadline) return false;
-  __threadfence();
   return true;
 }
 
@@ -94,13 +155,15 @@ __device__ __forceinline__ void router_slice(const RouterArgs& r, int e_begin, i
       const int c0 = qk * 64 + lane, c1 = c0 + 32;
       const uint4* wrow = reinterpret_cast<const uint4*>(r.wr + (size_t)e * H);
       const uint4 w0 = ldg_stream(wrow + c0), w1 = ldg_stream(wrow + c1);
+      uint4 xv[8][2];  // every load of the tile in flight before any FMA
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        if (t < B) {
-          const uint4* xrow = reinterpret_cast<const uint4*>(r.x + (size_t)t * H);
-          acc[t] = dot8(w1, __ldg(xrow + c1), dot8(w0, __ldg(xrow + c0), 0.f));
-        }
+        const uint4* xrow = reinterpret_cast<const uint4*>(r.x + (size_t)t * H);
+        xv[t][0] = t < B ? __ldg(xrow + c0) : make_uint4(0u, 0u, 0u, 0u);
+        xv[t][1] = t < B ? __ldg(xrow + c1) : make_uint4(0u, 0u, 0u, 0u);
       }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) acc[t] = dot8(w1, xv[t][1], dot8(w0, xv[t][0], 0.f));
 #pragma unroll
       for (int t = 0; t < 8; ++t) acc[t] = warp_sum(acc[t]);
     }
@@ -108,7 +171,7 @@ __device__ __forceinline__ void router_slice(const RouterArgs& r, int e_begin, i
 #pragma unroll
       for (int t = 0; t < 8; ++t) s_part[el][qk][t] = acc[t];
     }
-    named_sync(1, CONSUMER_THREADS);
+    named_sync(1, fz::CT);
     if (tid < 16) {
       const int le = tid >> 3, t = tid & 7, ee = base + le;
       if (ee < e_end && t < B)
@@ -116,165 +179,451 @@ __device__ __forceinline__ void router_slice(const RouterArgs& r, int e_begin, i
             (s_part[le][0][t] + s_part[le][1][t]) + (s_part[le][2][t] + s_part[le][3][t]) +
             (r.bias ? __ldg(r.bias + ee) : 0.0f);
     }
-    named_sync(1, CONSUMER_THREADS);
+    named_sync(1, fz::CT);
   }
 }
+
+// ---- consumer side -----------------------------------------------------------
+
+__device__ __forceinline__ void release_slot(uint32_t empty_bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar);
+}
+
+// Finished gate/up units go to the signalling warp through a small ring of
+// mbarriers (8 consumer-warp arrivals each, after the warps' h stores); it
+// publishes them to the group counters, so no consumer warp waits on a
+// GPU-scope fence.
+struct Sig {
+  uint32_t full0, free0;
+  int* grp;
+  uint64_t limit;
+};
+// gidx: the unit's group counter, -2 for a unit skipped after an abort, -1 at the end.
+__device__ __forceinline__ void signal_unit(const Sig& s, int seq, int gidx) {
+  const int j = seq & (fz::SIGQ - 1);
+  if (seq >= fz::SIGQ && (threadIdx.x & 31) == 0)
+    mbar_wait(s.free0 + 8u * j, (uint32_t)((seq / fz::SIGQ) - 1) & 1u, s.limit);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (threadIdx.x == 0) s.grp[j] = gidx;
+    mbar_arrive(s.full0 + 8u * j);
+  }
+}
+
+// Gate/up unit on CUDA cores (<= 2 tokens): warp w owns gate row w and up row
+// w; the same arithmetic, in the same order, as the standalone gate/up kernel,
+// done in two passes so the gate slot is released before the up rows are
+// read.
+template <int NTOK>
+__device__ __forceinline__ void rows_cc(const uint8_t* st, const uint4* xs, const int (&tok)[2],
+                                        float (&acc)[NTOK]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint4* wr = reinterpret_cast<const uint4*>(st + warp * fz::ROWB);
+#pragma unroll
+  for (int i = 0; i < NTOK; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint4 w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = wr[lane + 32 * (4 * half + j)];
+#pragma unroll
+    for (int i = 0; i < NTOK; ++i) {
+      float p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        p[j] = gu_impl::dot8_bf16(w[j], xs[tok[i] * (H / 8) + lane + 32 * (4 * half + j)]);
+      acc[i] += (p[0] + p[1]) + (p[2] + p[3]);
+    }
+  }
+}
+
+template <int NTOK>
+__device__ __forceinline__ void unit_cc(const uint8_t* gs, const uint8_t* us, const uint4* xs,
+                                        const int (&tok)[2], float* h, const Item& d, bool ok,
+                                        uint32_t emA, uint32_t emB) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float g[NTOK], v[NTOK];
+  if (ok) rows_cc<NTOK>(gs, xs, tok, g);
+  release_slot(emA);
+  if (ok) rows_cc<NTOK>(us, xs, tok, v);
+  release_slot(emB);
+  if (!ok) return;
+#pragma unroll
+  for (int i = 0; i < NTOK; ++i) {
+    const float gsum = warp_sum(g[i]);
+    const float vsum = warp_sum(v[i]);
+    if (lane == 0) h[(size_t)(d.pair0 + i) * I + d.blk * 8 + warp] = silu_mul(gsum, vsum);
+  }
+}
+
+// Gate/up unit on tensor cores (3..8 tokens): m16n8k16 with the 8 gate + 8 up
+// rows as M and the tokens as N, warp w owns a 256-column K-slice; the same
+// arithmetic as the standalone gate/up kernel.
+__device__ __forceinline__ void unit_mma(const uint8_t* gs, const uint8_t* us, const uint16_t* xs,
+                                         const int* pair_tok, float* buf, float* h, const Item& d,
+                                         bool ok, uint32_t emA, uint32_t emB) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int n = d.n;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (ok) {
+    uint4 bfr[8];
+    if (g < n) {
+      const int tok = d.tok0 >= 0 ? d.tok0 + g : pair_tok[d.pair0 + g];
+      const uint16_t* row = xs + (size_t)tok * H + warp * 256 + q * 8;
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) bfr[kb] = *reinterpret_cast<const uint4*>(row + kb * 32);
+    } else {
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) bfr[kb] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const uint8_t* rlo = gs + g * fz::ROWB + (warp * 256 + q * 8) * 2;
+    const uint8_t* rhi = us + g * fz::ROWB + (warp * 256 + q * 8) * 2;
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      const uint4 alo = *reinterpret_cast<const uint4*>(rlo + kb * 64);
+      const uint4 ahi = *reinterpret_cast<const uint4*>(rhi + kb * 64);
+      mma_bf16(acc, alo.x, ahi.x, alo.y, ahi.y, bfr[kb].x, bfr[kb].y);
+      mma_bf16(acc, alo.z, ahi.z, alo.w, ahi.w, bfr[kb].z, bfr[kb].w);
+    }
+  }
+  release_slot(emA);
+  release_slot(emB);
+  float* red = buf + warp * gu::ROWS * GROUP_MAX;
+  const int col = 2 * q;
+  red[g * GROUP_MAX + col] = acc[0];
+  red[g * GROUP_MAX + col + 1] = acc[1];
+  red[(g + 8) * GROUP_MAX + col] = acc[2];
+  red[(g + 8) * GROUP_MAX + col + 1] = acc[3];
+  named_sync(1, fz::CT);
+  {
+    const int r = warp, j = lane;  // row r of the block, token slot j
+    if (j < n && ok) {
+      float gsum = 0.f, usum = 0.f;
+#pragma unroll
+      for (int w = 0; w < fz::CW; ++w) {
+        gsum += buf[(w * gu::ROWS + r) * GROUP_MAX + j];
+        usum += buf[(w * gu::ROWS + r + 8) * GROUP_MAX + j];
+      }
+      h[(size_t)(d.pair0 + j) * I + d.blk * 8 + r] = silu_mul(gsum, usum);
+    }
+  }
+  named_sync(1, fz::CT);  // buf is free again
+}
+
+// ---- producer side (lane 0 of the producer warp) -----------------------------
+
+struct Prod {
+  uint32_t full0, empty0, stages_addr;
+  Item* desc;
+  int it;
+  uint64_t deadline;
+  WsHeader* hdr;
+  volatile int* abort_flag;
+};
+
+__device__ __forceinline__ bool take_slot(Prod& p, int& slot) {
+  slot = p.it % fz::NS;
+  if (p.it >= fz::NS &&
+      !mbar_wait(p.empty0 + 8u * slot, (uint32_t)((p.it / fz::NS) - 1) & 1u, p.deadline)) {
+    *p.abort_flag = 1;
+    set_error(p.hdr, DEV_TIMEOUT);
+    return false;
+  }
+  if (*p.abort_flag) return false;
+  ++p.it;
+  return true;
+}
+
+// A slot with no payload (SELECT / END): armed by a plain arrive.
+__device__ __forceinline__ void post_marker(Prod& p, int kind) {
+  const int slot = p.it % fz::NS;
+  if (p.it >= fz::NS)  // END is posted even after an abort; wait out the drain bound
+    mbar_wait(p.empty0 + 8u * slot, (uint32_t)((p.it / fz::NS) - 1) & 1u,
+              p.deadline + fz::DRAIN_NS);
+  ++p.it;
+  Item d = {};
+  d.kind = kind;
+  p.desc[slot] = d;
+  mbar_arrive(p.full0 + 8u * slot);
+}
+
+__device__ __forceinline__ bool post_gateup(Prod& p, const uint16_t* base, const Item& d) {
+  int sa, sb;
+  if (!take_slot(p, sa)) return false;
+  p.desc[sa] = d;
+  mbar_expect_tx(p.full0 + 8u * sa, fz::SLOT);
+  bulk_g2s(p.stages_addr + sa * fz::SLOT, base + (size_t)(d.blk * 8) * H, fz::SLOT, p.full0 + 8u * sa);
+  if (!take_slot(p, sb)) return false;  // the END posted next takes the up half's place
+  Item du = d;
+  du.kind = fz::IT_UP;
+  p.desc[sb] = du;
+  mbar_expect_tx(p.full0 + 8u * sb, fz::SLOT);
+  bulk_g2s(p.stages_addr + sb * fz::SLOT, base + (size_t)(I + d.blk * 8) * H, fz::SLOT,
+           p.full0 + 8u * sb);
+  return true;
+}
+
 
 }  // namespace
 
 __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertArgs a, RouterArgs r) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
+  __shared__ int s_ngroups;
+  __shared__ Item s_desc[fz::NS];
+  __shared__ int4 s_groups[fz::MAXG];
+  __shared__ int s_pair_tok[fz::NPAIR];
+  __shared__ float s_pair_w[fz::NPAIR];
+  __shared__ float s_acc[fz::MAXB * dn::RS];     // routed groups
+  __shared__ float s_acc_sh[fz::MAXB * dn::RS];  // shared expert
   __shared__ LocalSelectSmem s_sel;
   __shared__ float s_part[2][4][8];
-  __shared__ float s_pair_w[LOCAL_SELECT_MAX_B * SLOTS];
-  __shared__ float s_acc[LOCAL_SELECT_MAX_B * dn::RS];
-  __shared__ __align__(8) uint64_t s_dn_bars[2 * fz::DN_NSTAGE];
+  __shared__ int s_hgrp[fz::SIGQ];
+  // ring full / empty, SELECT done, finished-unit full / free, signalling done
+  __shared__ __align__(8) uint64_t s_bars[2 * fz::NS + 1 + 2 * fz::SIGQ + 1];
   WsHeader* hdr = a.ws.hdr;
+  uint32_t* done = hdr->group_done;
   const int G = gridDim.x, cta = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
   const int B = a.B;
-
-  gu_impl::GuCtx c;
-  c.stages = smem;
-  c.buf = reinterpret_cast<float*>(smem + gu::NSTAGE * gu::STAGE_BYTES);
-  MetaSmem& meta = *reinterpret_cast<MetaSmem*>(smem + gu::NSTAGE * gu::STAGE_BYTES + gu::BUF_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
-  c.stages_addr = smem_addr(smem);
-  c.full0 = smem_addr(bars);
-  c.empty0 = smem_addr(bars + gu::NSTAGE);
-  c.x = a.x;
-  c.pair_tok = meta.pair_tok;
-  c.h = a.ws.h;
-  c.hdr = hdr;
-  c.abort_flag = &s_abort;
-
-  dn_impl::DnCtx d;
-  d.stages = smem;
-  d.stages_addr = c.stages_addr;
-  d.stage_bytes = fz::DN_STAGE;
-  d.nstage = fz::DN_NSTAGE;
-  d.red = c.buf;
-  d.acc = s_acc;
-  d.full0 = smem_addr(s_dn_bars);
-  d.empty0 = smem_addr(s_dn_bars + fz::DN_NSTAGE);
-  d.hdr = hdr;
-  d.abort_flag = &s_abort;
-  d.pair_tok = meta.pair_tok;
-  d.pair_w = s_pair_w;
+  uint8_t* ring = smem;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + fz::NS * fz::SLOT);
+  float* buf = reinterpret_cast<float*>(smem + fz::NS * fz::SLOT + fz::XS_BYTES);
+  const uint32_t full0 = smem_addr(s_bars), empty0 = smem_addr(s_bars + fz::NS);
+  const uint32_t sel_bar = smem_addr(s_bars + 2 * fz::NS);
+  const uint32_t hfull0 = smem_addr(s_bars + 2 * fz::NS + 1);
+  const uint32_t hfree0 = hfull0 + 8u * fz::SIGQ;
+  const uint32_t sig_done = hfree0 + 8u * fz::SIGQ;
 
   if (tid == 0) {
-    for (int s = 0; s < gu::NSTAGE; ++s) {
-      mbar_init(gu_impl::full_bar(c, s), 1);
-      mbar_init(gu_impl::empty_bar(c, s), gu::CWARPS);
+    for (int s = 0; s < fz::NS; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, fz::CW);
     }
-    for (int s = 0; s < fz::DN_NSTAGE; ++s) {
-      mbar_init(dn_impl::full_bar(d, s), 1);
-      mbar_init(dn_impl::empty_bar(d, s), dn::CWARPS);
+    mbar_init(sel_bar, 1);
+    for (int j = 0; j < fz::SIGQ; ++j) {
+      mbar_init(hfull0 + 8u * j, fz::CW);
+      mbar_init(hfree0 + 8u * j, 1);
     }
+    mbar_init(sig_done, 1);
     s_abort = 0;
+    s_ngroups = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < LOCAL_SELECT_MAX_B * dn::RS; i += blockDim.x) s_acc[i] = 0.f;
+  for (int i = tid; i < fz::MAXB * dn::RS; i += blockDim.x) s_acc[i] = s_acc_sh[i] = 0.f;
   __syncthreads();
-  c.deadline = wait_deadline(hdr);
-  d.deadline = c.deadline;
-  gu_impl::Plan pl = gu_impl::plan_pre(B, true);
-  const bool down_cta = cta < fz::DOWN_CTAS;
+  // Launched with programmatic serialization: the set-up above overlaps the
+  // preceding kernel; x, the weights and the workspace are read only after it.
+  pdl_wait();
+  const uint64_t deadline = wait_deadline(hdr);
+  const bool owner = cta < fz::DOWN_CTAS;
   const int r0 = cta * dn::RS;
+  const int npairs = B * TOPK;
 
-  if ((tid >> 5) == gu::CWARPS) {  // ---------------- producer warp (lane 0 issues)
-    int it = 0;
-    bool ok = true;
-    if (lane == 0)
-      for (int j = cta; ok && j < pl.nsu; j += G) {
-        const gu_impl::SharedUnit su = gu_impl::shared_unit(j, B, pl.nsg);
-        ok = gu_impl::issue_unit(c, a.w.ws13 + (size_t)su.s * (2 * I) * H, su.blk, it);
-      }
-    __syncwarp();
-    named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
+  if ((tid >> 5) == fz::CW) {  // ---------------- producer warp (lane 0 issues)
     if (lane != 0) return;
-    gu_impl::plan_post(pl, meta.n_groups, true);
-    const int ng = meta.n_groups;
-    const int nu = pl.r_end - pl.r_begin;
-    int pf = 0;  // down-row prefetches issued (one per group)
-    int gi_cached = -1;
-    const uint16_t* base = nullptr;
-    for (int u = pl.r_begin; ok && u < pl.r_end; ++u) {
-      const int gi = u / gu::UNITS;
-      if (gi != gi_cached) {
-        const int4 grp = meta.groups[gi];
-        base = grp.x < E ? a.w.w13 + (size_t)grp.x * (2 * I) * H
-                         : a.w.ws13 + (size_t)(grp.x - E) * (2 * I) * H;
-        gi_cached = gi;
+    Prod p;
+    p.full0 = full0;
+    p.empty0 = empty0;
+    p.stages_addr = smem_addr(ring);
+    p.desc = s_desc;
+    p.it = 0;
+    p.deadline = deadline;
+    p.hdr = hdr;
+    p.abort_flag = &s_abort;
+    int u = (int)atomicAdd(&hdr->unit_next, 1u);    // unit being issued
+    int nxt = (int)atomicAdd(&hdr->unit_next, 1u);  // claimed ahead
+    bool meta = false, claims_open = true;
+    int total = 0x7fffffff, ng = 0, ndn = 0;
+    // Down items: the shared group first (its h is ready first), then the
+    // routed groups in table order.  kw: items whose Wd copy is issued, kh:
+    // items whose h copy is issued (kh <= kw; items in between were posted
+    // ahead with only their Wd slice, once this CTA had no gate/up left).
+    int kw = 0, kh = 0;
+    int dslot[fz::NS];
+    auto dn_group = [&](int kk) { return kk == 0 ? ng - 1 : kk - 1; };
+    auto dn_done = [&](int kk) { return kk == 0 ? fz::DONE_SHARED : kk - 1; };
+    auto dn_item = [&](int kk, const uint16_t*& wd, const float*& hr) {
+      const int4 grp = s_groups[dn_group(kk)];
+      Item d = {};
+      d.kind = fz::IT_DOWN;
+      d.pair0 = grp.y;
+      d.n = grp.z;
+      d.shared = kk == 0;
+      wd = (grp.x < E ? a.w.w2 + (size_t)grp.x * H * I : a.w.ws2 + (size_t)(grp.x - E) * H * I) +
+           (size_t)r0 * I;
+      hr = a.ws.h + (size_t)grp.y * I;
+      return d;
+    };
+    // Completion counters of the next PW down items, all loads in flight at once.
+    constexpr int PW = 8;
+    // Their values are read only once the loads have surely returned (or when
+    // there is nothing else to do), so polling never stalls the issue of
+    // gate/up copies.
+    constexpr uint64_t POLL_NS = 1500;
+    uint32_t pw[PW];
+    bool polled = false;
+    uint64_t poll_t = 0;
+    auto poll = [&]() {
+#pragma unroll
+      for (int j = 0; j < PW; ++j) pw[j] = kh + j < ndn ? ld_relaxed(done + dn_done(kh + j)) : 0u;
+      polled = true;
+      poll_t = globaltimer_ns();
+    };
+    bool ok = true;
+    while (ok && !s_abort) {
+      if (polled && kh < ndn && (!claims_open || globaltimer_ns() - poll_t > POLL_NS)) {
+        int rdy = 0;
+        bool run = true;
+#pragma unroll
+        for (int j = 0; j < PW; ++j) {
+          run = run && kh + j < ndn && pw[j] >= fz::DONE_TARGET;
+          rdy += run ? 1 : 0;
+        }
+        polled = false;
+        if (rdy > 0) {
+          // h of these groups was written by other CTAs (generic proxy, seen
+          // complete through the counters); order it before the bulk reads.
+          fence_acq_rel_gpu();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          for (int j = 0; ok && j < rdy; ++j, ++kh) {
+            const uint16_t* wd;
+            const float* hr;
+            const Item d = dn_item(kh, wd, hr);
+            if (kh < kw) {  // Wd already on its way: add the h rows
+              const int sl = dslot[kh % fz::NS];
+              bulk_g2s(p.stages_addr + sl * fz::SLOT + dn::WBYTES, hr, d.n * dn::HROW,
+                       p.full0 + 8u * sl);
+            } else {
+              int sl;
+              if (!(ok = take_slot(p, sl))) break;
+              p.desc[sl] = d;
+              mbar_expect_tx(p.full0 + 8u * sl, dn::WBYTES + d.n * dn::HROW);
+              bulk_g2s(p.stages_addr + sl * fz::SLOT, wd, dn::WBYTES, p.full0 + 8u * sl);
+              bulk_g2s(p.stages_addr + sl * fz::SLOT + dn::WBYTES, hr, d.n * dn::HROW,
+                       p.full0 + 8u * sl);
+              kw = kh + 1;
+            }
+          }
+          poll();
+          continue;
+        }
       }
-      ok = gu_impl::issue_unit(c, base, u & (gu::UNITS - 1), it);
-      // Interleave the L2 prefetches of this CTA's down rows with the units.
-      const int upto = down_cta ? (nu > 0 ? (int)(((long long)(u - pl.r_begin + 1) * ng + nu - 1) / nu) : ng) : 0;
-      for (; pf < upto && pf < ng; ++pf) {
-        const int4 g2 = meta.groups[pf];
-        const uint16_t* wb = (g2.x < E ? a.w.w2 + (size_t)g2.x * H * I
-                                       : a.w.ws2 + (size_t)(g2.x - E) * H * I) + (size_t)r0 * I;
-        prefetch_l2_bulk(wb, dn::WBYTES);
-      }
-    }
-    if (down_cta)
-      for (; pf < ng; ++pf) {
-        const int4 g2 = meta.groups[pf];
-        const uint16_t* wb = (g2.x < E ? a.w.w2 + (size_t)g2.x * H * I
-                                       : a.w.ws2 + (size_t)(g2.x - E) * H * I) + (size_t)r0 * I;
-        prefetch_l2_bulk(wb, dn::WBYTES);
-      }
-    // The ring is free once the consumers have released every gate/up stage.
-    const uint64_t drain = globaltimer_ns() + fz::DRAIN_NS;
-    for (int j = it - gu::NSTAGE < 0 ? 0 : it - gu::NSTAGE; j < it; ++j)
-      if (!mbar_wait(gu_impl::empty_bar(c, j % gu::NSTAGE), (uint32_t)(j / gu::NSTAGE) & 1u, drain))
-        ok = false;
-    if (!ok || !down_cta) {
-      if (!ok) {
-        *c.abort_flag = 1;
-        set_error(hdr, DEV_TIMEOUT);
-      }
-      return;
-    }
-    // Down: Wd slices first (from L2), h rows once every CTA has written h.
-    int k = 0;
-    bool h_ready = false;
-    const int early = ng < fz::DN_NSTAGE ? ng : fz::DN_NSTAGE;
-    for (int gi = 0; gi < ng; ++gi) {
-      const int4 grp = meta.groups[gi];
-      const int slot = gi % fz::DN_NSTAGE;
-      if (gi >= fz::DN_NSTAGE) {
-        if (!mbar_wait(dn_impl::empty_bar(d, slot), (uint32_t)((gi / fz::DN_NSTAGE) - 1) & 1u,
-                       d.deadline) ||
-            *d.abort_flag) {
-          *d.abort_flag = 1;
+      if (claims_open && u >= fz::UNITS && !meta) {
+        post_marker(p, fz::IT_SELECT);
+        if (!mbar_wait(sel_bar, 0u, deadline)) {
+          s_abort = 1;
           set_error(hdr, DEV_TIMEOUT);
           break;
         }
+        ng = s_ngroups;
+        total = ng * fz::UNITS;  // the shared group's units and the routed ones
+        ndn = owner ? ng : 0;
+        meta = true;
+        poll();
+        continue;
       }
-      mbar_expect_tx(dn_impl::full_bar(d, slot), dn::WBYTES + grp.z * dn::HROW);
-      const uint16_t* wb = (grp.x < E ? a.w.w2 + (size_t)grp.x * H * I
-                                      : a.w.ws2 + (size_t)(grp.x - E) * H * I) + (size_t)r0 * I;
-      bulk_g2s(d.stages_addr + slot * fz::DN_STAGE, wb, dn::WBYTES, dn_impl::full_bar(d, slot));
-      if (!h_ready && gi + 1 < early) continue;
-      if (!h_ready) {  // all early Wd copies are out; now wait for h
-        if (!grid_wait(&hdr->grid_bar[1], (uint32_t)G, d.deadline)) {
-          *d.abort_flag = 1;
-          set_error(hdr, DEV_TIMEOUT);
+      if (claims_open && u < total) {
+        Item d = {};
+        d.kind = fz::IT_GATE;
+        const uint16_t* base;
+        if (u < fz::UNITS) {  // shared expert: tokens 0..B-1, pairs after the routed ones
+          d.blk = u;
+          d.pair0 = npairs;
+          d.n = B;
+          d.tok0 = 0;
+          d.done_idx = fz::DONE_SHARED;
+          base = a.w.ws13;
+        } else {
+          const int ru = u - fz::UNITS;
+          const int gi = ru / fz::UNITS;
+          const int4 grp = s_groups[gi];
+          d.blk = ru % fz::UNITS;
+          d.pair0 = grp.y;
+          d.n = grp.z;
+          d.tok0 = -1;
+          d.done_idx = gi;
+          base = a.w.w13 + (size_t)grp.x * (2 * I) * H;
         }
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        h_ready = true;
+        ok = post_gateup(p, base, d);
+        u = nxt;
+        nxt = (int)atomicAdd(&hdr->unit_next, 1u);
+        if (meta && !polled) poll();
+        continue;
       }
-      for (; k <= gi; ++k) {
-        const int4 gk = meta.groups[k];
-        bulk_g2s(d.stages_addr + (k % fz::DN_NSTAGE) * fz::DN_STAGE + dn::WBYTES,
-                 a.ws.h + (size_t)gk.y * I, gk.z * dn::HROW, dn_impl::full_bar(d, k % fz::DN_NSTAGE));
+      claims_open = false;
+      if (kh < ndn) {  // nothing left to stream but this CTA's down rows
+        if (kw < ndn && kw - kh < fz::NS) {
+          // post the next item's Wd slice now; its h follows once complete
+          const uint16_t* wd;
+          const float* hr;
+          const Item d = dn_item(kw, wd, hr);
+          int sl;
+          if (!(ok = take_slot(p, sl))) break;
+          p.desc[sl] = d;
+          mbar_expect_tx(p.full0 + 8u * sl, dn::WBYTES + d.n * dn::HROW);
+          bulk_g2s(p.stages_addr + sl * fz::SLOT, wd, dn::WBYTES, p.full0 + 8u * sl);
+          dslot[kw % fz::NS] = sl;
+          ++kw;
+          continue;
+        }
+        if (globaltimer_ns() > deadline) {
+          s_abort = 1;
+          set_error(hdr, DEV_TIMEOUT);
+          break;
+        }
+        poll();
+        continue;
       }
+      break;
     }
-    const uint64_t dr = globaltimer_ns() + fz::DRAIN_NS;
-    for (int j = k - fz::DN_NSTAGE < 0 ? 0 : k - fz::DN_NSTAGE; j < k; ++j)
-      mbar_wait(dn_impl::full_bar(d, j % fz::DN_NSTAGE), (uint32_t)(j / fz::DN_NSTAGE) & 1u, dr);
+    // Items posted with their Wd slice only still wait for h: on an abort,
+    // complete them with the h rows as they are, so no copy stays pending.
+    for (; kh < kw; ++kh) {
+      const uint16_t* wd;
+      const float* hr;
+      const Item d = dn_item(kh, wd, hr);
+      const int sl = dslot[kh % fz::NS];
+      bulk_g2s(p.stages_addr + sl * fz::SLOT + dn::WBYTES, hr, d.n * dn::HROW, p.full0 + 8u * sl);
+    }
+    // The claim made ahead must have landed before the CTA counts itself out
+    // (the last CTA out resets the counter): wait for its value.
+    if (nxt < 0) s_abort = 1;
+    post_marker(p, fz::IT_END);
+    return;
+  }
+
+  if ((tid >> 5) == fz::CW + 1) {  // ---------------- signalling warp (lane 0)
+    if (lane != 0) return;
+    // Publishes finished units in order, one release fence per batch of units
+    // found finished (the consumers' h stores were ordered before their
+    // arrivals on the unit's barrier, which this thread has observed).
+    const uint64_t limit = deadline + fz::DRAIN_NS;
+    int q = 0;
+    bool end = false;
+    while (!end) {
+      if (!mbar_wait(hfull0 + 8u * (q & (fz::SIGQ - 1)), (uint32_t)(q / fz::SIGQ) & 1u, limit)) break;
+      int n = 1;
+      while (n < fz::SIGQ &&
+             mbar_test(hfull0 + 8u * ((q + n) & (fz::SIGQ - 1)), (uint32_t)((q + n) / fz::SIGQ) & 1u))
+        ++n;
+      fence_acq_rel_gpu();
+      int k = 0;
+      for (; k < n; ++k) {
+        const int gi = s_hgrp[(q + k) & (fz::SIGQ - 1)];
+        if (gi == -1) {
+          end = true;
+          break;
+        }
+        if (gi >= 0) red_add_relaxed(done + gi, 1u);
+      }
+      for (int j = 0; j < k; ++j) mbar_arrive(hfree0 + 8u * ((q + j) & (fz::SIGQ - 1)));
+      q += k;
+    }
+    __threadfence();  // the adds are performed before the CTA counts itself out
+    mbar_arrive(sig_done);
     return;
   }
 
@@ -283,7 +632,6 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
       *reinterpret_cast<volatile uint32_t*>(&hdr->stall_armed)) {
     // Test hook: wait for a flag that nothing sets; the bounded wait runs out
     // and records the timeout, exactly like a stuck pipeline wait would.
-    const uint64_t deadline = wait_deadline(hdr);
     while (!*reinterpret_cast<volatile uint32_t*>(&hdr->stall_release)) {
       if (globaltimer_ns() > deadline) {
         set_error(hdr, DEV_TIMEOUT);
@@ -292,76 +640,169 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     }
     hdr->stall_armed = 0;
   }
+  {  // the batch's activations, once (all loads in flight together)
+    uint4 v[fz::MAXB];
+#pragma unroll
+    for (int t = 0; t < fz::MAXB; ++t)
+      v[t] = t < B ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H) + tid)
+                   : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int t = 0; t < fz::MAXB; ++t)
+      if (t < B) reinterpret_cast<uint4*>(xs)[t * (H / 8) + tid] = v[t];
+  }
   // 1. router logits for this CTA's experts
   router_slice(r, (int)((long long)cta * E / G), (int)((long long)(cta + 1) * E / G), s_part);
-  if (tid == 0) grid_arrive(&hdr->grid_bar[0]);
-  int it = 0;
-  bool ok = true;
-  for (int j = cta; j < pl.nsu; j += G) {
-    const gu_impl::SharedUnit su = gu_impl::shared_unit(j, B, pl.nsg);
-    gu_impl::segment(c, su.blk, su.blk + 1, su.pair0, su.n, su.tok0, it, ok);
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(&hdr->grid_bar[0], 1u);
   }
-  // 2. every CTA ranks and buckets the batch once all logits are in
-  if (tid == 0 && !grid_wait(&hdr->grid_bar[0], (uint32_t)G, c.deadline)) {
-    *c.abort_flag = 1;
-    set_error(hdr, DEV_TIMEOUT);
-  }
-  named_sync(1, CONSUMER_THREADS);
-  fill_meta(a, true, meta, s_pair_w, c.buf, &s_sel);
-  named_sync(2, ALL_THREADS);
-  // 3. routed gate/up units
-  gu_impl::plan_post(pl, meta.n_groups, true);
-  int u = pl.r_begin;
-  while (u < pl.r_end) {
-    const int gi = u / gu::UNITS;
-    const int4 grp = meta.groups[gi];
-    const int u1 = min(pl.r_end, (gi + 1) * gu::UNITS);
-    gu_impl::segment(c, u, u1, grp.y, grp.z, -1, it, ok);
-    u = u1;
-  }
-  named_sync(1, CONSUMER_THREADS);  // every h store of this CTA is issued
-  if (tid == 0) grid_arrive(&hdr->grid_bar[1]);
-  // 4. down + combine + shared expert + residual over this CTA's 16 rows
-  if (down_cta) {
-    const int ng = meta.n_groups;
-    bool dok = ok;
-    for (int gi = 0; gi < ng; ++gi) {
-      const int4 grp = meta.groups[gi];
-      const int slot = gi % fz::DN_NSTAGE;
-      if (dok) dok = dn_impl::wait_full(d, slot, (uint32_t)(gi / fz::DN_NSTAGE) & 1u);
-      const uint8_t* st = d.stages + slot * fz::DN_STAGE;
-      const int n = grp.z;
-      if (n <= dn::CC_MAX) {
-        if (dok) {
-          switch (n) {
-            case 1: dn_impl::group_cc<1>(d, st, grp.y); break;
-            case 2: dn_impl::group_cc<2>(d, st, grp.y); break;
-            case 3: dn_impl::group_cc<3>(d, st, grp.y); break;
-            default: dn_impl::group_cc<4>(d, st, grp.y); break;
+
+  dn_impl::DnCtx dc;
+  dc.red = buf;
+  dc.pair_tok = s_pair_tok;
+  dc.pair_w = s_pair_w;
+  dc.hdr = hdr;
+  dc.abort_flag = &s_abort;
+
+  int it = 0, useq = 0;
+  const uint64_t drain = deadline + fz::DRAIN_NS;
+  Sig sig;
+  sig.full0 = hfull0;
+  sig.free0 = hfree0;
+  sig.grp = s_hgrp;
+  sig.limit = drain;
+  while (true) {
+    const int slot = it % fz::NS;
+    const uint32_t par = (uint32_t)(it / fz::NS) & 1u;
+    if (!mbar_wait(full0 + 8u * slot, par, deadline)) {
+      s_abort = 1;
+      set_error(hdr, DEV_TIMEOUT);
+      if (!mbar_wait(full0 + 8u * slot, par, drain)) break;
+    }
+    const Item d = s_desc[slot];
+    const bool ok = !s_abort;
+    if (d.kind == fz::IT_END) break;
+    if (d.kind == fz::IT_SELECT) {
+      // 2. every CTA ranks and buckets the batch once all logits are in
+      if (tid == 0 && !grid_wait(&hdr->grid_bar[0], (uint32_t)G, deadline)) {
+        s_abort = 1;
+        set_error(hdr, DEV_TIMEOUT);
+      }
+      named_sync(1, fz::CT);
+      {
+        float lv[fz::MAXB];
+#pragma unroll
+        for (int t = 0; t < fz::MAXB; ++t)
+          lv[t] = t < B ? __ldcg(a.ws.logits + (size_t)t * E + tid) : 0.f;
+#pragma unroll
+        for (int t = 0; t < fz::MAXB; ++t)
+          if (t < B) buf[t * E + tid] = lv[t];
+      }
+      named_sync(1, fz::CT);
+      const int warp = tid >> 5;
+      if (warp < B) {
+        int ix;
+        float wt;
+        topk_warp<false>(buf + warp * E, ix, wt);
+        if (lane < TOPK) {
+          const int pp = warp * TOPK + lane;
+          s_sel.idx[pp] = ix;
+          s_sel.w[pp] = wt;
+          if (cta == 0) {
+            a.ws.topk_idx[pp] = ix;
+            a.ws.topk_w[pp] = wt;
+            if (a.user_idx) a.user_idx[pp] = ix;
+            if (a.user_w) a.user_w[pp] = wt;
+          }
+        }
+      }
+      named_sync(1, fz::CT);
+      BucketDst bd;
+      bd.pair_tok = s_pair_tok;
+      bd.pair_w = s_pair_w;
+      bd.groups = s_groups;
+      bd.n_groups = &s_ngroups;
+      bd.n_uniq = nullptr;
+      BucketOut none = {nullptr, nullptr, nullptr, nullptr};
+      bool bad = false;  // indices come from topk_warp: always valid
+      bucket_cta<1, false>(B, s_sel.idx, s_sel.w, bd, none, s_sel.sc, bad, ConsumerSync());
+      named_sync(1, fz::CT);
+      if (tid == 0) mbar_arrive(sel_bar);
+      release_slot(empty0 + 8u * slot);
+      ++it;
+      continue;
+    }
+    if (d.kind == fz::IT_DOWN) {
+      // 4. this CTA's 16 output rows of the group, weighted into the accumulators
+      const uint8_t* st = ring + slot * fz::SLOT;
+      float* acc = d.shared ? s_acc_sh : s_acc;
+      const uint32_t em = empty0 + 8u * slot;
+      dc.acc = acc;
+      if (d.n <= dn::CC_MAX) {
+        if (ok) {
+          switch (d.n) {
+            case 1: dn_impl::group_cc<1>(dc, st, d.pair0); break;
+            case 2: dn_impl::group_cc<2>(dc, st, d.pair0); break;
+            case 3: dn_impl::group_cc<3>(dc, st, d.pair0); break;
+            default: dn_impl::group_cc<4>(dc, st, d.pair0); break;
           }
         }
       } else {
-        dn_impl::group_mma<1>(d, st, grp.y, dok ? n : 0);  // n <= 8 here
+        dn_impl::group_mma<1>(dc, st, d.pair0, ok ? d.n : 0);  // n <= 8 here
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dn_impl::empty_bar(d, slot));
+      release_slot(em);
+      ++it;
+      continue;
     }
-    named_sync(1, CONSUMER_THREADS);
-    if (dok) {
-      for (int i = tid; i < B * dn::RS; i += CONSUMER_THREADS) {
-        const int t = i / dn::RS, rr = i % dn::RS;
-        const size_t o = (size_t)t * H + r0 + rr;
-        a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + s_acc[i]);
-      }
+    // 3. gate/up unit: gate rows in this slot, up rows in the next
+    const int slot2 = (it + 1) % fz::NS;
+    const uint32_t par2 = (uint32_t)((it + 1) / fz::NS) & 1u;
+    bool ok2 = ok;
+    if (!mbar_wait(full0 + 8u * slot2, par2, deadline)) {
+      s_abort = 1;
+      set_error(hdr, DEV_TIMEOUT);
+      ok2 = false;
+      if (!mbar_wait(full0 + 8u * slot2, par2, drain)) break;
+    }
+    if (s_desc[slot2].kind != fz::IT_UP) break;  // the producer gave up mid-unit (abort)
+    const uint8_t* gs = ring + slot * fz::SLOT;
+    const uint8_t* us = ring + slot2 * fz::SLOT;
+    if (d.n <= gu::CC_MAX) {
+      int tok[2];
+      tok[0] = d.tok0 >= 0 ? d.tok0 : s_pair_tok[d.pair0];
+      tok[1] = d.n > 1 ? (d.tok0 >= 0 ? d.tok0 + 1 : s_pair_tok[d.pair0 + 1]) : tok[0];
+      if (d.n == 1)
+        unit_cc<1>(gs, us, reinterpret_cast<const uint4*>(xs), tok, a.ws.h, d, ok2,
+                   empty0 + 8u * slot, empty0 + 8u * slot2);
+      else
+        unit_cc<2>(gs, us, reinterpret_cast<const uint4*>(xs), tok, a.ws.h, d, ok2,
+                   empty0 + 8u * slot, empty0 + 8u * slot2);
+    } else {
+      unit_mma(gs, us, xs, s_pair_tok, buf, a.ws.h, d, ok2, empty0 + 8u * slot,
+               empty0 + 8u * slot2);
+    }
+    signal_unit(sig, useq++, ok2 ? d.done_idx : -2);
+    it += 2;
+  }
+  signal_unit(sig, useq, -1);
+  named_sync(1, fz::CT);
+  if (owner && !s_abort) {
+    for (int i = tid; i < B * dn::RS; i += fz::CT) {
+      const int t = i / dn::RS, rr = i % dn::RS;
+      const size_t o = (size_t)t * H + r0 + rr;
+      // routed groups in expert order, then the shared expert (added last)
+      a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + (s_acc[i] + s_acc_sh[i]));
     }
   }
-  // The last CTA out resets the barrier counters for the next call (every
-  // CTA has passed both barriers by the time it counts itself out).
+  // The last CTA out resets the counters for the next call (every CTA has
+  // finished its claims, marks and polls by the time it counts itself out).
   if (tid == 0) {
+    mbar_wait(sig_done, 0u, drain);
     __threadfence();
     if (atomicAdd(&hdr->grid_bar[2], 1u) == (uint32_t)G - 1) {
       hdr->grid_bar[0] = 0u;
-      hdr->grid_bar[1] = 0u;
+      hdr->unit_next = 0u;
+      for (int i = 0; i < 64; ++i) done[i] = 0u;
       hdr->grid_bar[2] = 0u;
       __threadfence();
     }
@@ -382,9 +823,12 @@ cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStre
   cfg.blockDim = dim3(fz::THREADS, 1, 1);
   cfg.dynamicSmemBytes = fz::SMEM;
   cfg.stream = stream;
+  // One CTA per SM: the kernel's shared memory (> half an SM's) allows no
+  // second one, so the grid of #SMs CTAs is resident as soon as the SMs are
+  // free; the grid-wide waits are bounded in any case.
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, moe_small_bf16_kernel, a, r);
