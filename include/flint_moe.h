@@ -230,6 +230,48 @@ flint_status flint_moe_rmsnorm_bf16(const flint_moe_dims* dims, int32_t batch,
  * afterwards. */
 flint_status flint_moe_debug_arm_stall(void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* Largest batch flint_moe_decode_bf16_noalloc accepts. */
+#define FLINT_MOE_NOALLOC_MAX_BATCH 8
+
+/* flint_moe_decode_bf16 for callers that cannot allocate device memory.
+ * The pages describe no such entry point: it exists for hosts that own all
+ * device memory themselves -- a serving engine that splits the GPU into fixed
+ * pools and forbids its plugins to call cudaMalloc, a runtime with a memory
+ * budget fixed at build time, a step loop that may never take the allocator's
+ * locks -- and so cannot provide the workspace the other entry points take.
+ *
+ * Instead of a workspace it uses one static device array of this library
+ * (about 400 KiB, sized for FLINT_MOE_NOALLOC_MAX_BATCH tokens), which every
+ * GPU that loads the library holds until the process exits.  It calls no
+ * allocating routine.  Inputs, outputs and their layouts are those of
+ * flint_moe_decode_bf16, and so are the results.
+ *  - batch must be in [1, FLINT_MOE_NOALLOC_MAX_BATCH]; a larger batch returns
+ *    FLINT_ERR_INVALID_ARG before anything is enqueued.
+ *  - device_status_out: optional device pointer (4-byte aligned).  After the
+ *    layer, the call's device-side status is copied there, in stream order, as
+ *    a flint_status code (FLINT_OK, FLINT_ERR_INVALID_ARG for bad routing,
+ *    FLINT_ERR_DEVICE_TIMEOUT); it takes the place of
+ *    flint_moe_get_device_status, which needs a workspace.
+ *  - The first call on a device (the current device) looks up the array's
+ *    address, initialises its header and synchronises `stream` once.  Make
+ *    that first call before any stream capture: during a capture it returns
+ *    FLINT_ERR_CUDA instead.
+ *  - Each call clears the header's error word and counters; the array keeps
+ *    the rest of the previous call's contents, which the layer overwrites
+ *    before reading.
+ *  - All calls on a device share the one array: calls whose GPU work overlaps
+ *    (other streams, other host threads) race and corrupt each other's
+ *    results.  Order them, or use flint_moe_decode_bf16 with one workspace per
+ *    stream. */
+flint_status flint_moe_decode_bf16_noalloc(const flint_moe_dims* dims, int32_t batch,
+                                           const void* x_bf16, const void* residual_bf16,
+                                           const void* w_router_bf16, const float* logit_bias,
+                                           const void* w13_bf16, const void* w2_bf16,
+                                           const void* ws13_bf16, const void* ws2_bf16,
+                                           void* out_bf16,
+                                           int32_t* topk_idx_out, float* topk_w_out,
+                                           int32_t* device_status_out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

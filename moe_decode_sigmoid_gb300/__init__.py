@@ -35,7 +35,9 @@ EXPORTS = (
     "flint_moe_get_device_status", "flint_moe_route", "flint_moe_bucket",
     "flint_moe_decode_bf16", "flint_moe_decode_nvfp4_w4a16", "flint_moe_rmsnorm_bf16",
     "flint_moe_debug_arm_stall", "flint_moe_gateup_bf16", "flint_moe_down_bf16",
+    "flint_moe_decode_bf16_noalloc",
 )
+NOALLOC_MAX_BATCH = 8
 
 
 class FlintError(RuntimeError):
@@ -91,6 +93,8 @@ def lib() -> ctypes.CDLL:
     L.flint_moe_down_bf16.argtypes = [_P, _I32, _P, _P, _P, _P, _P, _SZ, _P]
     L.flint_moe_rmsnorm_bf16.restype = ctypes.c_int
     L.flint_moe_rmsnorm_bf16.argtypes = [_P, _I32, _P, _P, ctypes.c_float, _P]
+    L.flint_moe_decode_bf16_noalloc.restype = ctypes.c_int
+    L.flint_moe_decode_bf16_noalloc.argtypes = [_P, _I32] + [_P] * 13
     _lib = L
     return L
 
@@ -178,6 +182,19 @@ def flint_moe_decode_bf16(x, residual, w_router, logit_bias, w13, w2, ws13, ws2,
                                        _ptr(ws13), _ptr(ws2), _ptr(out), _ptr(topk_idx_out),
                                        _ptr(topk_w_out), wp, wb, _stream(stream)),
            "flint_moe_decode_bf16")
+
+
+def flint_moe_decode_bf16_noalloc(x, residual, w_router, logit_bias, w13, w2, ws13, ws2, out,
+                                  topk_idx_out=None, topk_w_out=None, device_status_out=None,
+                                  stream=None, dims: Dims | None = None):
+    """flint_moe_decode_bf16 without a workspace (the library's static device
+    array instead; batch <= NOALLOC_MAX_BATCH).  For callers that cannot
+    allocate device memory; calls whose GPU work overlaps race."""
+    _check(lib().flint_moe_decode_bf16_noalloc(
+        _dims(dims), x.shape[0], _ptr(x), _ptr(residual), _ptr(w_router), _ptr(logit_bias),
+        _ptr(w13), _ptr(w2), _ptr(ws13), _ptr(ws2), _ptr(out), _ptr(topk_idx_out),
+        _ptr(topk_w_out), _ptr(device_status_out), _stream(stream)),
+        "flint_moe_decode_bf16_noalloc")
 
 
 def flint_moe_gateup_bf16(x, w13, ws13, workspace, stream=None, dims: Dims | None = None):
