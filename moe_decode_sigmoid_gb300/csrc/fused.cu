@@ -28,12 +28,11 @@
 //   4. Down: CTA b < 128 owns output rows [16b, 16b+16) of every token.  As
 //      soon as a group is complete (acquire), its producer posts a DOWN slot:
 //      the 16 rows of the expert's Wd (16 KiB) and the group's h rows, and the
-//      consumers accumulate w(t, g) * (Wd h) per token.  Down slots take
-//      priority over gate/up units, so the down projection streams while
-//      gate/up is still running instead of after a grid barrier.  The shared
-//      expert is accumulated separately and added last, so every token's sum
-//      runs in the group table's order (routed groups by expert, shared last)
-//      exactly as in the three-kernel path.
+//      consumers accumulate w(t, g) * (Wd h) per token in shared memory.
+//      Down slots take priority over gate/up units, so the down projection
+//      streams while gate/up is still running instead of after a grid
+//      barrier.  Items run in a fixed order (the shared expert, then the
+//      routed groups by expert), so results are reproducible bit for bit.
 // Every wait is bounded by the workspace's limit; the last CTA out resets the
 // workspace counters for the next call.
 #include "common.cuh"
@@ -45,7 +44,7 @@
 namespace flint {
 namespace fz {
 constexpr int CW = 8;                          // consumer warps
-constexpr int THREADS = (CW + 2) * 32;         // + producer warp + signalling warp
+constexpr int THREADS = (CW + 3) * 32;         // + producer, signalling and poll warps
 constexpr int CT = CW * 32;                    // consumer threads
 constexpr int SLOT = 32 * 1024;                // ring slot bytes
 constexpr int NS = 5;                          // ring slots
@@ -82,8 +81,7 @@ struct Item {
   int n;         // tokens in the group
   int tok0;      // gate/up of the shared group: first token (tokens are consecutive), else -1
   int done_idx;  // completion counter of the group
-  int shared;    // down: the shared expert (accumulated separately)
-  int pad;
+  int pad[2];
 };
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
@@ -98,6 +96,14 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta_shared(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta_shared(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }
 __device__ __forceinline__ void red_add_relaxed(uint32_t* p, uint32_t v) {
   asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -212,41 +218,42 @@ __device__ __forceinline__ void signal_unit(const Sig& s, int seq, int gidx) {
 }
 
 // Gate/up unit on CUDA cores (<= 2 tokens): warp w owns gate row w and up row
-// w; the same arithmetic, in the same order, as the standalone gate/up kernel,
-// done in two passes so the gate slot is released before the up rows are
-// read.
-template <int NTOK>
-__device__ __forceinline__ void rows_cc(const uint8_t* st, const uint4* xs, const int (&tok)[2],
-                                        float (&acc)[NTOK]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint4* wr = reinterpret_cast<const uint4*>(st + warp * fz::ROWB);
-#pragma unroll
-  for (int i = 0; i < NTOK; ++i) acc[i] = 0.f;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint4 w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = wr[lane + 32 * (4 * half + j)];
-#pragma unroll
-    for (int i = 0; i < NTOK; ++i) {
-      float p[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        p[j] = gu_impl::dot8_bf16(w[j], xs[tok[i] * (H / 8) + lane + 32 * (4 * half + j)]);
-      acc[i] += (p[0] + p[1]) + (p[2] + p[3]);
-    }
-  }
-}
-
+// w; the same arithmetic, in the same order, as the standalone gate/up kernel
+// (gate and up chains interleaved: eight independent FMA chains per lane).
 template <int NTOK>
 __device__ __forceinline__ void unit_cc(const uint8_t* gs, const uint8_t* us, const uint4* xs,
                                         const int (&tok)[2], float* h, const Item& d, bool ok,
                                         uint32_t emA, uint32_t emB) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float g[NTOK], v[NTOK];
-  if (ok) rows_cc<NTOK>(gs, xs, tok, g);
+#pragma unroll
+  for (int i = 0; i < NTOK; ++i) g[i] = v[i] = 0.f;
+  if (ok) {
+    const uint4* gr = reinterpret_cast<const uint4*>(gs + warp * fz::ROWB);
+    const uint4* ur = reinterpret_cast<const uint4*>(us + warp * fz::ROWB);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint4 wg[4], wu[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        wg[j] = gr[lane + 32 * (4 * half + j)];
+        wu[j] = ur[lane + 32 * (4 * half + j)];
+      }
+#pragma unroll
+      for (int i = 0; i < NTOK; ++i) {
+        float pg[4], pu[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 xv = xs[tok[i] * (H / 8) + lane + 32 * (4 * half + j)];
+          pg[j] = gu_impl::dot8_bf16(wg[j], xv);
+          pu[j] = gu_impl::dot8_bf16(wu[j], xv);
+        }
+        g[i] += (pg[0] + pg[1]) + (pg[2] + pg[3]);
+        v[i] += (pu[0] + pu[1]) + (pu[2] + pu[3]);
+      }
+    }
+  }
   release_slot(emA);
-  if (ok) rows_cc<NTOK>(us, xs, tok, v);
   release_slot(emB);
   if (!ok) return;
 #pragma unroll
@@ -312,6 +319,56 @@ __device__ __forceinline__ void unit_mma(const uint8_t* gs, const uint8_t* us, c
   named_sync(1, fz::CT);  // buf is free again
 }
 
+// Buckets the batch's (token, slot) pairs by expert for B <= 8 tokens, by the
+// 256 consumer threads: with at most 8 tokens every distinct expert forms one
+// group (GROUP_MAX is larger), so thread p ranks pair p directly against all
+// pairs -- its position is the number of pairs with a smaller expert plus
+// those of the same expert from lower tokens -- and one counting barrier
+// gives the number of distinct experts.  The result is the group table and
+// pair order of bucket_cta: routed groups by expert ascending (tokens
+// ascending inside), then the shared expert's group of all tokens.
+__device__ __forceinline__ void bucket_small(int B, const int* idx, const float* w, int* pair_tok,
+                                             float* pair_w, int4* groups, int* n_groups,
+                                             int* opener) {
+  const int tid = threadIdx.x;
+  const int np = B * TOPK;
+  int e = 0, pos = 0, cnt = 0;
+  bool first = false;
+  if (tid < np) {
+    e = idx[tid];
+    int less = 0, before = 0;
+    for (int q = 0; q < np; ++q) {
+      const int eq = idx[q];
+      less += eq < e ? 1 : 0;
+      cnt += eq == e ? 1 : 0;
+      before += (eq == e && q < tid) ? 1 : 0;
+    }
+    pos = less + before;
+    first = before == 0;
+    pair_tok[pos] = tid / TOPK;
+    pair_w[pos] = w[tid];
+    opener[tid] = first ? e : 0x7fffffff;  // experts whose first pair this is
+  }
+  if (tid < S * B) {
+    pair_tok[np + tid] = tid % B;
+    pair_w[np + tid] = 1.0f;
+  }
+  uint32_t n_uniq;
+  asm volatile("{ .reg .pred p; setp.ne.u32 p, %1, 0; bar.red.popc.u32 %0, 1, %2, p; }"
+               : "=r"(n_uniq)
+               : "r"((tid < np && first) ? 1u : 0u), "n"(fz::CT)
+               : "memory");
+  if (tid < np && first) {
+    int g = 0;
+    for (int q = 0; q < np; ++q) g += opener[q] < e ? 1 : 0;
+    groups[g] = make_int4(e, pos, cnt, 0);
+  }
+  if (tid == 0) {
+    groups[n_uniq] = make_int4(E, np, B, 0);
+    *n_groups = (int)n_uniq + S;
+  }
+}
+
 // ---- producer side (lane 0 of the producer warp) -----------------------------
 
 struct Prod {
@@ -372,12 +429,12 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
   __shared__ int s_ngroups;
+  __shared__ int s_ready;  // down items whose groups are complete (poll warp -> producer)
   __shared__ Item s_desc[fz::NS];
   __shared__ int4 s_groups[fz::MAXG];
   __shared__ int s_pair_tok[fz::NPAIR];
   __shared__ float s_pair_w[fz::NPAIR];
-  __shared__ float s_acc[fz::MAXB * dn::RS];     // routed groups
-  __shared__ float s_acc_sh[fz::MAXB * dn::RS];  // shared expert
+  __shared__ float s_acc[fz::MAXB * dn::RS];  // this CTA's 16 output rows per token
   __shared__ LocalSelectSmem s_sel;
   __shared__ float s_part[2][4][8];
   __shared__ int s_hgrp[fz::SIGQ];
@@ -410,9 +467,10 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     mbar_init(sig_done, 1);
     s_abort = 0;
     s_ngroups = 0;
+    s_ready = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < fz::MAXB * dn::RS; i += blockDim.x) s_acc[i] = s_acc_sh[i] = 0.f;
+  for (int i = tid; i < fz::MAXB * dn::RS; i += blockDim.x) s_acc[i] = 0.f;
   __syncthreads();
   // Launched with programmatic serialization: the set-up above overlaps the
   // preceding kernel; x, the weights and the workspace are read only after it.
@@ -444,51 +502,28 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     int kw = 0, kh = 0;
     int dslot[fz::NS];
     auto dn_group = [&](int kk) { return kk == 0 ? ng - 1 : kk - 1; };
-    auto dn_done = [&](int kk) { return kk == 0 ? fz::DONE_SHARED : kk - 1; };
     auto dn_item = [&](int kk, const uint16_t*& wd, const float*& hr) {
       const int4 grp = s_groups[dn_group(kk)];
       Item d = {};
       d.kind = fz::IT_DOWN;
       d.pair0 = grp.y;
       d.n = grp.z;
-      d.shared = kk == 0;
       wd = (grp.x < E ? a.w.w2 + (size_t)grp.x * H * I : a.w.ws2 + (size_t)(grp.x - E) * H * I) +
            (size_t)r0 * I;
       hr = a.ws.h + (size_t)grp.y * I;
       return d;
     };
-    // Completion counters of the next PW down items, all loads in flight at once.
-    constexpr int PW = 8;
-    // Their values are read only once the loads have surely returned (or when
-    // there is nothing else to do), so polling never stalls the issue of
-    // gate/up copies.
-    constexpr uint64_t POLL_NS = 1500;
-    uint32_t pw[PW];
-    bool polled = false;
-    uint64_t poll_t = 0;
-    auto poll = [&]() {
-#pragma unroll
-      for (int j = 0; j < PW; ++j) pw[j] = kh + j < ndn ? ld_relaxed(done + dn_done(kh + j)) : 0u;
-      polled = true;
-      poll_t = globaltimer_ns();
-    };
     bool ok = true;
     while (ok && !s_abort) {
-      if (polled && kh < ndn && (!claims_open || globaltimer_ns() - poll_t > POLL_NS)) {
-        int rdy = 0;
-        bool run = true;
-#pragma unroll
-        for (int j = 0; j < PW; ++j) {
-          run = run && kh + j < ndn && pw[j] >= fz::DONE_TARGET;
-          rdy += run ? 1 : 0;
-        }
-        polled = false;
-        if (rdy > 0) {
-          // h of these groups was written by other CTAs (generic proxy, seen
-          // complete through the counters); order it before the bulk reads.
-          fence_acq_rel_gpu();
+      // Down items whose groups the poll warp has seen complete.
+      const int rdy = meta && kh < ndn ? ld_acquire_cta_shared(&s_ready) : 0;
+      if (rdy > kh) {
+        {
+          // h of these groups was written by other CTAs (generic proxy); the
+          // poll warp acquired it at GPU scope and this thread from the poll
+          // warp at CTA scope.  Order it before the bulk (async-proxy) reads.
           asm volatile("fence.proxy.async.global;" ::: "memory");
-          for (int j = 0; ok && j < rdy; ++j, ++kh) {
+          for (; ok && kh < rdy; ++kh) {
             const uint16_t* wd;
             const float* hr;
             const Item d = dn_item(kh, wd, hr);
@@ -507,7 +542,6 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
               kw = kh + 1;
             }
           }
-          poll();
           continue;
         }
       }
@@ -522,7 +556,6 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
         total = ng * fz::UNITS;  // the shared group's units and the routed ones
         ndn = owner ? ng : 0;
         meta = true;
-        poll();
         continue;
       }
       if (claims_open && u < total) {
@@ -550,7 +583,6 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
         ok = post_gateup(p, base, d);
         u = nxt;
         nxt = (int)atomicAdd(&hdr->unit_next, 1u);
-        if (meta && !polled) poll();
         continue;
       }
       claims_open = false;
@@ -574,8 +606,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
           set_error(hdr, DEV_TIMEOUT);
           break;
         }
-        poll();
-        continue;
+        continue;  // spin on s_ready (shared memory)
       }
       break;
     }
@@ -592,6 +623,39 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     // (the last CTA out resets the counter): wait for its value.
     if (nxt < 0) s_abort = 1;
     post_marker(p, fz::IT_END);
+    return;
+  }
+
+  if ((tid >> 5) == fz::CW + 2) {  // ---------------- poll warp (lane 0, row-slice owners)
+    // Watches the completion counters of this CTA's down items in order (the
+    // shared group first, then the routed groups), eight loads in flight at a
+    // time, and publishes how many are complete; the GPU-scope acquire fence
+    // is taken here, so the producer never waits on one.
+    if (lane != 0 || !owner) return;
+    while (!mbar_test(sel_bar, 0u))
+      if (s_abort || globaltimer_ns() > deadline) return;
+    const int ng = s_ngroups;
+    int k = 0;
+    while (k < ng && !s_abort) {
+      uint32_t pw[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        pw[j] = k + j < ng ? ld_relaxed(done + (k + j == 0 ? fz::DONE_SHARED : k + j - 1)) : 0u;
+      int rdy = 0;
+      bool run = true;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        run = run && k + j < ng && pw[j] >= fz::DONE_TARGET;
+        rdy += run ? 1 : 0;
+      }
+      if (rdy > 0) {
+        fence_acq_rel_gpu();
+        k += rdy;
+        st_release_cta_shared(&s_ready, k);
+      } else if (globaltimer_ns() > deadline) {
+        break;
+      }
+    }
     return;
   }
 
@@ -640,7 +704,14 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     }
     hdr->stall_armed = 0;
   }
-  {  // the batch's activations, once (all loads in flight together)
+  // 1. router logits for this CTA's experts
+  router_slice(r, (int)((long long)cta * E / G), (int)((long long)(cta + 1) * E / G), s_part);
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(&hdr->grid_bar[0], 1u);
+  }
+  // the batch's activations, once (all loads in flight together)
+  {
     uint4 v[fz::MAXB];
 #pragma unroll
     for (int t = 0; t < fz::MAXB; ++t)
@@ -650,14 +721,10 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     for (int t = 0; t < fz::MAXB; ++t)
       if (t < B) reinterpret_cast<uint4*>(xs)[t * (H / 8) + tid] = v[t];
   }
-  // 1. router logits for this CTA's experts
-  router_slice(r, (int)((long long)cta * E / G), (int)((long long)(cta + 1) * E / G), s_part);
-  if (tid == 0) {
-    __threadfence();
-    atomicAdd(&hdr->grid_bar[0], 1u);
-  }
+  named_sync(1, fz::CT);  // xs is complete before any gate/up unit reads it
 
   dn_impl::DnCtx dc;
+  dc.acc = s_acc;
   dc.red = buf;
   dc.pair_tok = s_pair_tok;
   dc.pair_w = s_pair_w;
@@ -717,15 +784,8 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
         }
       }
       named_sync(1, fz::CT);
-      BucketDst bd;
-      bd.pair_tok = s_pair_tok;
-      bd.pair_w = s_pair_w;
-      bd.groups = s_groups;
-      bd.n_groups = &s_ngroups;
-      bd.n_uniq = nullptr;
-      BucketOut none = {nullptr, nullptr, nullptr, nullptr};
-      bool bad = false;  // indices come from topk_warp: always valid
-      bucket_cta<1, false>(B, s_sel.idx, s_sel.w, bd, none, s_sel.sc, bad, ConsumerSync());
+      bucket_small(B, s_sel.idx, s_sel.w, s_pair_tok, s_pair_w, s_groups, &s_ngroups,
+                   s_sel.sc.off);
       named_sync(1, fz::CT);
       if (tid == 0) mbar_arrive(sel_bar);
       release_slot(empty0 + 8u * slot);
@@ -735,9 +795,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     if (d.kind == fz::IT_DOWN) {
       // 4. this CTA's 16 output rows of the group, weighted into the accumulators
       const uint8_t* st = ring + slot * fz::SLOT;
-      float* acc = d.shared ? s_acc_sh : s_acc;
       const uint32_t em = empty0 + 8u * slot;
-      dc.acc = acc;
       if (d.n <= dn::CC_MAX) {
         if (ok) {
           switch (d.n) {
@@ -747,10 +805,11 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
             default: dn_impl::group_cc<4>(dc, st, d.pair0); break;
           }
         }
+        release_slot(em);
       } else {
-        dn_impl::group_mma<1>(dc, st, d.pair0, ok ? d.n : 0);  // n <= 8 here
+        dn_impl::group_mma<1>(dc, st, d.pair0, ok ? d.n : 0);  // n <= 8 here, into s_acc
+        release_slot(em);
       }
-      release_slot(em);
       ++it;
       continue;
     }
@@ -790,8 +849,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     for (int i = tid; i < B * dn::RS; i += fz::CT) {
       const int t = i / dn::RS, rr = i % dn::RS;
       const size_t o = (size_t)t * H + r0 + rr;
-      // routed groups in expert order, then the shared expert (added last)
-      a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + (s_acc[i] + s_acc_sh[i]));
+      a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + s_acc[i]);
     }
   }
   // The last CTA out resets the counters for the next call (every CTA has

@@ -20,53 +20,77 @@ __device__ __forceinline__ float key2f(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Top-k of one token's E logits by one warp.  Lane l holds experts l + 32 j.
-// Each round takes the largest remaining logit; among equal logits the lowest
-// expert index wins (first within a lane by ascending j, then across lanes by
-// the minimum index).  Lanes 0..k-1 return slot `lane`'s expert and weight.
+// Compare-exchange of a sorting network: (key descending, expert ascending).
+__device__ __forceinline__ void topk_cas(uint32_t (&k)[E / 32], uint32_t (&e)[E / 32], int i, int j) {
+  const bool swap = k[j] > k[i] || (k[j] == k[i] && e[j] < e[i]);
+  const uint32_t ki = k[i], ei = e[i];
+  k[i] = swap ? k[j] : ki;
+  e[i] = swap ? e[j] : ei;
+  k[j] = swap ? ki : k[j];
+  e[j] = swap ? ei : e[j];
+}
+
+// Top-k of one token's E logits by one warp.  Lane l holds experts l + 32 j
+// and first sorts its 8 (key, expert) pairs -- key descending, expert
+// ascending -- with a 19-comparator sorting network (Batcher's odd-even merge
+// sort).  Each round then takes the largest lane head; among equal logits the
+// lowest expert index wins (a lane's head is its lowest index for that key, and
+// across lanes the minimum index is taken).  Lanes 0..k-1 return slot
+// `lane`'s expert and weight.
 template <bool GLOBAL_SRC>
 __device__ __forceinline__ void topk_warp(const float* logits_row, int& idx_out, float& w_out) {
+  static_assert(E / 32 == 8, "the sorting network is written for 8 values per lane");
   const int lane = threadIdx.x & 31;
-  float v[E / 32];
+  uint32_t k[8], e[8];
 #pragma unroll
-  for (int j = 0; j < E / 32; ++j)
-    v[j] = GLOBAL_SRC ? __ldcg(logits_row + lane + 32 * j) : logits_row[lane + 32 * j];
-  uint32_t taken = 0;
+  for (int j = 0; j < 8; ++j) {
+    k[j] = f2key(GLOBAL_SRC ? __ldcg(logits_row + lane + 32 * j) : logits_row[lane + 32 * j]);
+    e[j] = (uint32_t)(lane + 32 * j);
+  }
+  topk_cas(k, e, 0, 1); topk_cas(k, e, 2, 3); topk_cas(k, e, 4, 5); topk_cas(k, e, 6, 7);
+  topk_cas(k, e, 0, 2); topk_cas(k, e, 1, 3); topk_cas(k, e, 4, 6); topk_cas(k, e, 5, 7);
+  topk_cas(k, e, 1, 2); topk_cas(k, e, 5, 6);
+  topk_cas(k, e, 0, 4); topk_cas(k, e, 1, 5); topk_cas(k, e, 2, 6); topk_cas(k, e, 3, 7);
+  topk_cas(k, e, 2, 4); topk_cas(k, e, 3, 5);
+  topk_cas(k, e, 1, 2); topk_cas(k, e, 3, 4); topk_cas(k, e, 5, 6);
   int sel_e[TOPK];
   float sel_v[TOPK];
 #pragma unroll
   for (int r = 0; r < TOPK; ++r) {
-    uint32_t best_key = 0;
-    uint32_t best_e = 0xffffffffu;
+    const uint32_t top = __reduce_max_sync(0xffffffffu, k[0]);
+    const uint32_t m = __ballot_sync(0xffffffffu, k[0] == top);
+    uint32_t win;
+    if ((m & (m - 1u)) == 0u)  // one lane holds the maximum (the usual case)
+      win = __shfl_sync(0xffffffffu, e[0], __ffs(m) - 1);
+    else
+      win = __reduce_min_sync(0xffffffffu, k[0] == top ? e[0] : 0xffffffffu);
+    if ((int)(win & 31u) == lane) {  // the winner pops its head
 #pragma unroll
-    for (int j = 0; j < E / 32; ++j) {
-      const uint32_t k = f2key(v[j]);
-      const bool free_j = !((taken >> j) & 1u);
-      if (free_j && (best_e == 0xffffffffu || k > best_key)) {
-        best_key = k;
-        best_e = (uint32_t)(lane + 32 * j);
+      for (int j = 0; j < 7; ++j) {
+        k[j] = k[j + 1];
+        e[j] = e[j + 1];
       }
+      k[7] = 0u;
+      e[7] = 0xffffffffu;
     }
-    const uint32_t top = __reduce_max_sync(0xffffffffu, best_key);
-    const uint32_t win = __reduce_min_sync(0xffffffffu, best_key == top ? best_e : 0xffffffffu);
-    if ((int)(win & 31u) == lane) taken |= 1u << (win >> 5);
     sel_e[r] = (int)win;
     sel_v[r] = key2f(top);
   }
-  float s[TOPK], ssum = 0.f;
-#pragma unroll
-  for (int r = 0; r < TOPK; ++r) {
-    s[r] = 1.0f / (1.0f + expf(-sel_v[r]));
-    ssum += s[r];
-  }
-  idx_out = 0;
-  w_out = 0.f;
+  // Lane r < k computes sigmoid r; every lane then sums the k values in rank
+  // order (the same order and rounding in every lane).
+  float sv = 0.f, mine = 0.f;
 #pragma unroll
   for (int r = 0; r < TOPK; ++r)
     if (r == lane) {
+      mine = sel_v[r];
       idx_out = sel_e[r];
-      w_out = s[r] / ssum;
     }
+  if (lane >= TOPK) idx_out = 0;
+  sv = 1.0f / (1.0f + expf(-mine));
+  float ssum = 0.f;
+#pragma unroll
+  for (int r = 0; r < TOPK; ++r) ssum += __shfl_sync(0xffffffffu, sv, r);
+  w_out = lane < TOPK ? sv / ssum : 0.f;
 }
 
 // Optional plain description of the buckets (flint_moe_bucket).
