@@ -28,7 +28,9 @@
 //   4. Down: CTA b < 128 owns output rows [16b, 16b+16) of every token.  As
 //      soon as a group is complete (acquire), its producer posts a DOWN slot:
 //      the 16 rows of the expert's Wd (16 KiB) and the group's h rows, and the
-//      consumers accumulate w(t, g) * (Wd h) per token in shared memory.
+//      consumers accumulate w(t, g) * (Wd h) per token: groups of <= 4 tokens
+//      on CUDA cores into per-lane running sums (reduced once, at the end),
+//      larger ones on tensor cores.
 //      Down slots take priority over gate/up units, so the down projection
 //      streams while gate/up is still running instead of after a grid
 //      barrier.  Items run in a fixed order (the shared expert, then the
@@ -61,7 +63,12 @@ constexpr int XS_BYTES = MAXB * H * 2;         // bf16 activations of the batch,
 constexpr int RED_BYTES = CW * 16 * GROUP_MAX * 4;
 constexpr int LOGIT_BYTES = MAXB * E * 4;
 constexpr int BUF_BYTES = RED_BYTES > LOGIT_BYTES ? RED_BYTES : LOGIT_BYTES;
-constexpr size_t SMEM = (size_t)NS * SLOT + XS_BYTES + BUF_BYTES;
+// Per-lane running sums of the CUDA-core down items: [token * 2 + row][thread],
+// rows padded to 257 floats so that both the updates (one row, consecutive
+// lanes) and the final per-row sums (16 lanes each) are free of bank conflicts.
+constexpr int LACC_STRIDE = CW * 32 + 1;
+constexpr int LACC_BYTES = MAXB * 2 * LACC_STRIDE * 4;
+constexpr size_t SMEM = (size_t)NS * SLOT + XS_BYTES + BUF_BYTES + LACC_BYTES;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
 enum : int { IT_GATE = 0, IT_UP = 1, IT_DOWN = 2, IT_SELECT = 3, IT_END = 4 };
 static_assert(S == 1 && MAXB <= GROUP_MAX, "one shared group at these batches");
@@ -264,6 +271,67 @@ __device__ __forceinline__ void unit_cc(const uint8_t* gs, const uint8_t* us, co
   }
 }
 
+// Down item on CUDA cores (<= 4 tokens): warp w owns Wd rows 2w and 2w+1 of
+// the slice.  The lane's 32 weights are unpacked once and reused by every
+// token; each lane adds w(t, g) times its partial dot product (16 columns) to
+// its own running sum in shared memory -- the sums across lanes are taken
+// once, when the output is written.
+__device__ __forceinline__ void down_cc(const uint8_t* st, int pair0, int n, const int* pair_tok,
+                                        const float* pair_w, float* lacc, bool ok, uint32_t em) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float s0[dn::CC_MAX], s1[dn::CC_MAX];
+#pragma unroll
+  for (int i = 0; i < dn::CC_MAX; ++i) s0[i] = s1[i] = 0.f;
+  if (ok) {
+    const uint8_t* w0 = st + (2 * warp) * dn::WSTRIDE;
+    const uint8_t* w1 = w0 + dn::WSTRIDE;
+    float f0[16], f1[16];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint2 a0 = *reinterpret_cast<const uint2*>(w0 + (4 * lane + 128 * m) * 2);
+      const uint2 a1 = *reinterpret_cast<const uint2*>(w1 + (4 * lane + 128 * m) * 2);
+      f0[4 * m] = bf_lo(a0.x);
+      f0[4 * m + 1] = bf_hi(a0.x);
+      f0[4 * m + 2] = bf_lo(a0.y);
+      f0[4 * m + 3] = bf_hi(a0.y);
+      f1[4 * m] = bf_lo(a1.x);
+      f1[4 * m + 1] = bf_hi(a1.x);
+      f1[4 * m + 2] = bf_lo(a1.y);
+      f1[4 * m + 3] = bf_hi(a1.y);
+    }
+#pragma unroll
+    for (int i = 0; i < dn::CC_MAX; ++i) {
+      if (i < n) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float4 hv = *reinterpret_cast<const float4*>(st + dn::WBYTES + i * dn::HSTRIDE +
+                                                             (4 * lane + 128 * m) * 4);
+          s0[i] = fmaf(f0[4 * m], hv.x, s0[i]);
+          s0[i] = fmaf(f0[4 * m + 1], hv.y, s0[i]);
+          s0[i] = fmaf(f0[4 * m + 2], hv.z, s0[i]);
+          s0[i] = fmaf(f0[4 * m + 3], hv.w, s0[i]);
+          s1[i] = fmaf(f1[4 * m], hv.x, s1[i]);
+          s1[i] = fmaf(f1[4 * m + 1], hv.y, s1[i]);
+          s1[i] = fmaf(f1[4 * m + 2], hv.z, s1[i]);
+          s1[i] = fmaf(f1[4 * m + 3], hv.w, s1[i]);
+        }
+      }
+    }
+  }
+  release_slot(em);
+  if (!ok) return;
+#pragma unroll
+  for (int i = 0; i < dn::CC_MAX; ++i) {
+    if (i < n) {
+      const int t = pair_tok[pair0 + i];
+      const float wt = pair_w[pair0 + i];
+      float* acc = lacc + (2 * t) * fz::LACC_STRIDE + threadIdx.x;
+      acc[0] = fmaf(wt, s0[i], acc[0]);
+      acc[fz::LACC_STRIDE] = fmaf(wt, s1[i], acc[fz::LACC_STRIDE]);
+    }
+  }
+}
+
 // Gate/up unit on tensor cores (3..8 tokens): m16n8k16 with the 8 gate + 8 up
 // rows as M and the tokens as N, warp w owns a 256-column K-slice; the same
 // arithmetic as the standalone gate/up kernel.
@@ -448,6 +516,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
   uint8_t* ring = smem;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + fz::NS * fz::SLOT);
   float* buf = reinterpret_cast<float*>(smem + fz::NS * fz::SLOT + fz::XS_BYTES);
+  float* lacc = reinterpret_cast<float*>(smem + fz::NS * fz::SLOT + fz::XS_BYTES + fz::BUF_BYTES);
   const uint32_t full0 = smem_addr(s_bars), empty0 = smem_addr(s_bars + fz::NS);
   const uint32_t sel_bar = smem_addr(s_bars + 2 * fz::NS);
   const uint32_t hfull0 = smem_addr(s_bars + 2 * fz::NS + 1);
@@ -471,6 +540,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     fence_mbar_init();
   }
   for (int i = tid; i < fz::MAXB * dn::RS; i += blockDim.x) s_acc[i] = 0.f;
+  for (int i = tid; i < fz::LACC_BYTES / 4; i += blockDim.x) lacc[i] = 0.f;
   __syncthreads();
   // Launched with programmatic serialization: the set-up above overlaps the
   // preceding kernel; x, the weights and the workspace are read only after it.
@@ -797,15 +867,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
       const uint8_t* st = ring + slot * fz::SLOT;
       const uint32_t em = empty0 + 8u * slot;
       if (d.n <= dn::CC_MAX) {
-        if (ok) {
-          switch (d.n) {
-            case 1: dn_impl::group_cc<1>(dc, st, d.pair0); break;
-            case 2: dn_impl::group_cc<2>(dc, st, d.pair0); break;
-            case 3: dn_impl::group_cc<3>(dc, st, d.pair0); break;
-            default: dn_impl::group_cc<4>(dc, st, d.pair0); break;
-          }
-        }
-        release_slot(em);
+        down_cc(st, d.pair0, d.n, s_pair_tok, s_pair_w, lacc, ok, em);
       } else {
         dn_impl::group_mma<1>(dc, st, d.pair0, ok ? d.n : 0);  // n <= 8 here, into s_acc
         release_slot(em);
@@ -846,10 +908,20 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
   signal_unit(sig, useq, -1);
   named_sync(1, fz::CT);
   if (owner && !s_abort) {
-    for (int i = tid; i < B * dn::RS; i += fz::CT) {
-      const int t = i / dn::RS, rr = i % dn::RS;
-      const size_t o = (size_t)t * H + r0 + rr;
-      a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + s_acc[i]);
+    // Thread pair (2s, 2s+1) finishes sum s = (warp w, token t, row r): each
+    // adds 16 lanes' running sums, one shuffle joins the halves; the
+    // tensor-core items' share is in s_acc.  Row 2w + r of the CTA's slice.
+    const int sidx = tid >> 1, half = tid & 1;
+    const int w = sidx >> 4, j = sidx & 15, t = j >> 1, rr = j & 1;
+    const float* src = lacc + j * fz::LACC_STRIDE + w * 32 + half * 16;
+    float v = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v += src[k];
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    if (half == 0 && t < B) {
+      const int row = 2 * w + rr;
+      const size_t o = (size_t)t * H + r0 + row;
+      a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + (v + s_acc[t * dn::RS + row]));
     }
   }
   // The last CTA out resets the counters for the next call (every CTA has
