@@ -65,45 +65,64 @@ __device__ __forceinline__ bool wait_full(const DnCtx& c, int slot, uint32_t par
   return false;
 }
 
-// 4 bf16 weights (uint2) . 4 fp32 activations.
-__device__ __forceinline__ float dot4(const uint2& w, const float4& h, float acc) {
-  acc = fmaf(bf_lo(w.x), h.x, acc);
-  acc = fmaf(bf_hi(w.x), h.y, acc);
-  acc = fmaf(bf_lo(w.y), h.z, acc);
-  acc = fmaf(bf_hi(w.y), h.w, acc);
-  return acc;
-}
-
+// CUDA-core group of NTOK <= 4 tokens.  Warp w owns Wd rows 2w and 2w+1; lane
+// l covers K elements [4l + 128m, 4l + 128m + 4), m = 0..3.  The lane's 32
+// weights are unpacked once for all tokens, every token's two partial dots are
+// formed first, then all the warp reductions run interleaved (no branch
+// between them), then lane 0 applies the combine weights.
 template <int NTOK>
 __device__ __forceinline__ void group_cc(const DnCtx& c, const uint8_t* st, int pair0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Lane l covers K elements [4l + 128m, 4l + 128m + 4), m = 0..3.
   const uint8_t* w0 = st + (2 * warp) * dn::WSTRIDE;
   const uint8_t* w1 = w0 + dn::WSTRIDE;
-  uint2 a0[4], a1[4];
+  float f0[16], f1[16];
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    a0[m] = *reinterpret_cast<const uint2*>(w0 + (4 * lane + 128 * m) * 2);
-    a1[m] = *reinterpret_cast<const uint2*>(w1 + (4 * lane + 128 * m) * 2);
+    const uint2 a0 = *reinterpret_cast<const uint2*>(w0 + (4 * lane + 128 * m) * 2);
+    const uint2 a1 = *reinterpret_cast<const uint2*>(w1 + (4 * lane + 128 * m) * 2);
+    f0[4 * m] = bf_lo(a0.x);
+    f0[4 * m + 1] = bf_hi(a0.x);
+    f0[4 * m + 2] = bf_lo(a0.y);
+    f0[4 * m + 3] = bf_hi(a0.y);
+    f1[4 * m] = bf_lo(a1.x);
+    f1[4 * m + 1] = bf_hi(a1.x);
+    f1[4 * m + 2] = bf_lo(a1.y);
+    f1[4 * m + 3] = bf_hi(a1.y);
   }
   const uint8_t* hs = st + dn::WBYTES;
+  float s0[NTOK], s1[NTOK];
 #pragma unroll
   for (int i = 0; i < NTOK; ++i) {
-    float s0 = 0.f, s1 = 0.f;
+    s0[i] = s1[i] = 0.f;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const float4 hv =
           *reinterpret_cast<const float4*>(hs + i * dn::HSTRIDE + (4 * lane + 128 * m) * 4);
-      s0 = dot4(a0[m], hv, s0);
-      s1 = dot4(a1[m], hv, s1);
+      s0[i] = fmaf(f0[4 * m], hv.x, s0[i]);
+      s0[i] = fmaf(f0[4 * m + 1], hv.y, s0[i]);
+      s0[i] = fmaf(f0[4 * m + 2], hv.z, s0[i]);
+      s0[i] = fmaf(f0[4 * m + 3], hv.w, s0[i]);
+      s1[i] = fmaf(f1[4 * m], hv.x, s1[i]);
+      s1[i] = fmaf(f1[4 * m + 1], hv.y, s1[i]);
+      s1[i] = fmaf(f1[4 * m + 2], hv.z, s1[i]);
+      s1[i] = fmaf(f1[4 * m + 3], hv.w, s1[i]);
     }
-    s0 = warp_sum(s0);
-    s1 = warp_sum(s1);
-    if (lane == 0) {
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int i = 0; i < NTOK; ++i) {
+      s0[i] += __shfl_xor_sync(0xffffffffu, s0[i], o);
+      s1[i] += __shfl_xor_sync(0xffffffffu, s1[i], o);
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < NTOK; ++i) {
       const int t = c.pair_tok[pair0 + i];
       const float wt = c.pair_w[pair0 + i];
-      c.acc[t * dn::RS + 2 * warp] += wt * s0;
-      c.acc[t * dn::RS + 2 * warp + 1] += wt * s1;
+      c.acc[t * dn::RS + 2 * warp] += wt * s0[i];
+      c.acc[t * dn::RS + 2 * warp + 1] += wt * s1[i];
     }
   }
 }
