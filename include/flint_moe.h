@@ -175,7 +175,8 @@ flint_status flint_moe_decode_bf16(const flint_moe_dims* dims, int32_t batch,
  * computes exactly what flint_moe_decode_bf16 computes (with the routing
  * copies written by flint_moe_route).
  * flint_moe_gateup_bf16: for every selected (token, expert) pair and for the
- *   shared expert(s), h = silu(Wg x) * (Wu x), kept in the workspace (fp32).
+ *   shared expert(s), h = silu(Wg x) * (Wu x), kept in the workspace (each
+ *   fp32 value as a bf16 pair hi + lo, ~16 significant bits).
  * flint_moe_down_bf16: out = residual + sum of the routing-weighted
  *   Wd h terms + the shared expert's Wd h ("expert combine" fused into the
  *   down GEMV: [vLLM Day-0 Support for Recursive's Flint, "Optimization

@@ -31,7 +31,10 @@ constexpr uint32_t DEV_TIMEOUT = 5;
 // ---- workspace layout ------------------------------------------------------
 // [ header | logits fp32 [MAX_B,E] | topk_idx i32 [MAX_B,K] | topk_w f32 [MAX_B,K] |
 //   pair_tok i32 [MAX_B*SLOTS] | pair_w f32 [MAX_B*SLOTS] | groups int4 [MAX_GROUPS] |
-//   h fp32 [max_batch*SLOTS, I] ]
+//   h [max_batch*SLOTS, I] x 4 bytes ]
+// h holds fp32 for the fused kernel and the NVFP4 kernels; the BF16 gate/up
+// and down kernels of the large-batch path store each element as a bf16
+// hi + lo pair instead (see store_h_split), in the same 4 bytes.
 // Every array but the last is sized for MAX_B, so the offsets do not depend on
 // the batch a workspace was sized for; only h grows with max_batch.
 struct WsHeader {
@@ -174,6 +177,48 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
 __device__ __forceinline__ void split_bf2(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf2(a, b);
   lo = pack_bf2(a - bf_lo(hi), b - bf_hi(hi));
+}
+
+// Split h rows.  Each block of 8 consecutive elements k in [8b, 8b + 8) has a
+// 16-byte chunk of hi = bf16(h) values and a 16-byte chunk of lo =
+// bf16(h - hi) values (hi + lo keeps ~16 significant bits of the fp32 h; the
+// parts are ready-made bf16 MMA operands).  Line b / 4 (128 bytes) of the row
+// holds blocks 4(b/4) .. 4(b/4)+3, chunk 2(b%4) + part, permuted by XOR with
+// the row's pair index mod 8: 8 consecutive rows read at the same columns then
+// fall in distinct shared-memory banks after a plain row-by-row copy.
+__host__ __device__ __forceinline__ int h_chunk(size_t pair, int blk, int part) {
+  return (blk >> 2) * 128 + (((2 * (blk & 3) + part) ^ (int)(pair & 7)) * 16);
+}
+
+// One element.
+__device__ __forceinline__ void store_h_split(float* h, size_t pair, int k, float v) {
+  uint8_t* row = reinterpret_cast<uint8_t*>(h + pair * I);
+  const uint16_t hi = f2bf(v);
+  *reinterpret_cast<uint16_t*>(row + h_chunk(pair, k >> 3, 0) + (k & 7) * 2) = hi;
+  *reinterpret_cast<uint16_t*>(row + h_chunk(pair, k >> 3, 1) + (k & 7) * 2) =
+      f2bf(v - bf_lo((uint32_t)hi));
+}
+
+// A whole block at once: called by all 32 lanes of a warp, lanes 8m..8m+7
+// holding elements 0..7 of one block (v); the first lane of each 8-lane group
+// stores the two chunks when `store` is true (uniform within the group).
+__device__ __forceinline__ void store_h_block8(float* h, size_t pair, int blk, float v,
+                                               bool store) {
+  const uint32_t hi = f2bf(v);
+  const uint32_t lo = f2bf(v - bf_lo(hi));
+  const uint32_t hw = hi | (__shfl_down_sync(0xffffffffu, hi, 1) << 16);
+  const uint32_t lw = lo | (__shfl_down_sync(0xffffffffu, lo, 1) << 16);
+  const uint4 hv = make_uint4(hw, __shfl_down_sync(0xffffffffu, hw, 2),
+                              __shfl_down_sync(0xffffffffu, hw, 4),
+                              __shfl_down_sync(0xffffffffu, hw, 6));
+  const uint4 lv = make_uint4(lw, __shfl_down_sync(0xffffffffu, lw, 2),
+                              __shfl_down_sync(0xffffffffu, lw, 4),
+                              __shfl_down_sync(0xffffffffu, lw, 6));
+  if ((threadIdx.x & 7) == 0 && store) {
+    uint8_t* row = reinterpret_cast<uint8_t*>(h + pair * I);
+    *reinterpret_cast<uint4*>(row + h_chunk(pair, blk, 0)) = hv;
+    *reinterpret_cast<uint4*>(row + h_chunk(pair, blk, 1)) = lv;
+  }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

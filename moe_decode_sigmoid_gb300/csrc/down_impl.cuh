@@ -1,6 +1,13 @@
-// down_impl.cuh — device code of the BF16 down / combine stage (see down.cu
-// for the design); shared by the standalone down kernel and the fused
-// small-batch kernel.
+// down_impl.cuh — the tensor-core down / combine step for a group of 5..8
+// tokens, used by the fused small-batch kernel (its own CUDA-core path takes
+// groups of up to 4 tokens).
+//
+// A CTA owns 16 output rows; the group's 16 Wd rows (16 KiB, contiguous) and
+// fp32 h rows sit in one shared-memory slot.  mma.sync m16n8k16 with the Wd
+// rows as M and the tokens as N; the fp32 h is split into two bf16 parts
+// (hi + lo, two MMAs) so the operand keeps ~16 significant bits; warp w owns a
+// 64-column K-slice; the 8 partial tiles are summed through shared memory and
+// weighted into the CTA's accumulators.
 #pragma once
 
 #include "common.cuh"
@@ -16,116 +23,18 @@ constexpr int WBYTES = RS * WSTRIDE;      // 16 KiB
 constexpr int HROW = I * 4;               // bytes of one fp32 h row
 constexpr int HSTRIDE = HROW;             // the group's h rows are one contiguous copy
 constexpr int CWARPS = 8;
-constexpr int THREADS = CWARPS * 32 + 32;
 constexpr int RED_FLOATS = CWARPS * RS * GROUP_MAX;
-constexpr int MAX_STAGES = 8;
-constexpr int SMEM_CAP = 232448 - 1024;   // opt-in maximum minus static/slack
-constexpr int CC_MAX = 4;
-constexpr uint64_t DRAIN_NS = 2000000000ull;
-
-__host__ __device__ inline int nmax_for(int B) { return B < GROUP_MAX ? B : GROUP_MAX; }
-__host__ __device__ inline int stage_bytes(int B) { return WBYTES + nmax_for(B) * HSTRIDE; }
-__host__ __device__ inline int fixed_bytes(int B) {
-  return RED_FLOATS * 4 + B * RS * 4 + (int)sizeof(MetaSmem) + MAX_B * SLOTS * 4 +
-         2 * MAX_STAGES * 8;
-}
-__host__ __device__ inline int nstages(int B) {
-  int n = (SMEM_CAP - fixed_bytes(B)) / stage_bytes(B);
-  return n > MAX_STAGES ? MAX_STAGES : n;
-}
-__host__ __device__ inline int smem_bytes(int B) {
-  return nstages(B) * stage_bytes(B) + fixed_bytes(B);
-}
+constexpr int CC_MAX = 4;                 // larger groups take the tensor-core step
 }  // namespace dn
 
 namespace dn_impl {
 
 struct DnCtx {
-  uint8_t* stages;
-  uint32_t stages_addr;
-  int stage_bytes, nstage;
-  float* red;
-  float* acc;  // [B][RS]
-  uint32_t full0, empty0;
-  uint64_t deadline;
-  WsHeader* hdr;
-  volatile int* abort_flag;
+  float* red;           // [CWARPS][RS][GROUP_MAX] partial tiles
+  float* acc;           // [B][RS] accumulators
   const int* pair_tok;  // shared memory
   const float* pair_w;  // shared memory
 };
-
-__device__ __forceinline__ uint32_t full_bar(const DnCtx& c, int s) { return c.full0 + 8u * s; }
-__device__ __forceinline__ uint32_t empty_bar(const DnCtx& c, int s) { return c.empty0 + 8u * s; }
-
-__device__ __forceinline__ bool wait_full(const DnCtx& c, int slot, uint32_t parity) {
-  if (*c.abort_flag) return false;
-  if (mbar_wait(full_bar(c, slot), parity, c.deadline)) return true;
-  *c.abort_flag = 1;
-  set_error(c.hdr, DEV_TIMEOUT);
-  return false;
-}
-
-// CUDA-core group of NTOK <= 4 tokens.  Warp w owns Wd rows 2w and 2w+1; lane
-// l covers K elements [4l + 128m, 4l + 128m + 4), m = 0..3.  The lane's 32
-// weights are unpacked once for all tokens, every token's two partial dots are
-// formed first, then all the warp reductions run interleaved (no branch
-// between them), then lane 0 applies the combine weights.
-template <int NTOK>
-__device__ __forceinline__ void group_cc(const DnCtx& c, const uint8_t* st, int pair0) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint8_t* w0 = st + (2 * warp) * dn::WSTRIDE;
-  const uint8_t* w1 = w0 + dn::WSTRIDE;
-  float f0[16], f1[16];
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const uint2 a0 = *reinterpret_cast<const uint2*>(w0 + (4 * lane + 128 * m) * 2);
-    const uint2 a1 = *reinterpret_cast<const uint2*>(w1 + (4 * lane + 128 * m) * 2);
-    f0[4 * m] = bf_lo(a0.x);
-    f0[4 * m + 1] = bf_hi(a0.x);
-    f0[4 * m + 2] = bf_lo(a0.y);
-    f0[4 * m + 3] = bf_hi(a0.y);
-    f1[4 * m] = bf_lo(a1.x);
-    f1[4 * m + 1] = bf_hi(a1.x);
-    f1[4 * m + 2] = bf_lo(a1.y);
-    f1[4 * m + 3] = bf_hi(a1.y);
-  }
-  const uint8_t* hs = st + dn::WBYTES;
-  float s0[NTOK], s1[NTOK];
-#pragma unroll
-  for (int i = 0; i < NTOK; ++i) {
-    s0[i] = s1[i] = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const float4 hv =
-          *reinterpret_cast<const float4*>(hs + i * dn::HSTRIDE + (4 * lane + 128 * m) * 4);
-      s0[i] = fmaf(f0[4 * m], hv.x, s0[i]);
-      s0[i] = fmaf(f0[4 * m + 1], hv.y, s0[i]);
-      s0[i] = fmaf(f0[4 * m + 2], hv.z, s0[i]);
-      s0[i] = fmaf(f0[4 * m + 3], hv.w, s0[i]);
-      s1[i] = fmaf(f1[4 * m], hv.x, s1[i]);
-      s1[i] = fmaf(f1[4 * m + 1], hv.y, s1[i]);
-      s1[i] = fmaf(f1[4 * m + 2], hv.z, s1[i]);
-      s1[i] = fmaf(f1[4 * m + 3], hv.w, s1[i]);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-    for (int i = 0; i < NTOK; ++i) {
-      s0[i] += __shfl_xor_sync(0xffffffffu, s0[i], o);
-      s1[i] += __shfl_xor_sync(0xffffffffu, s1[i], o);
-    }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < NTOK; ++i) {
-      const int t = c.pair_tok[pair0 + i];
-      const float wt = c.pair_w[pair0 + i];
-      c.acc[t * dn::RS + 2 * warp] += wt * s0[i];
-      c.acc[t * dn::RS + 2 * warp + 1] += wt * s1[i];
-    }
-  }
-}
 
 template <int NT>
 __device__ __forceinline__ void group_mma(const DnCtx& c, const uint8_t* st, int pair0, int n) {
@@ -180,37 +89,6 @@ __device__ __forceinline__ void group_mma(const DnCtx& c, const uint8_t* st, int
     c.acc[t * dn::RS + r] += wt * s;
   }
   named_sync(1, dn::CWARPS * 32);
-}
-
-__device__ __forceinline__ void produce(const DnCtx& c, const int4* groups, int n_groups,
-                                        const uint16_t* w2, const uint16_t* ws2, const float* h,
-                                        int r0) {
-  int it = 0;
-  for (int gi = 0; gi < n_groups; ++gi) {
-    const int4 grp = groups[gi];
-    const int slot = it % c.nstage;
-    if (it >= c.nstage) {
-      const bool got = mbar_wait(empty_bar(c, slot), (uint32_t)((it / c.nstage) - 1) & 1u, c.deadline);
-      if (!got || *c.abort_flag) {
-        *c.abort_flag = 1;
-        if (!got) set_error(c.hdr, DEV_TIMEOUT);
-        break;
-      }
-    } else if (*c.abort_flag) {
-      break;
-    }
-    const int n = grp.z;
-    mbar_expect_tx(full_bar(c, slot), dn::RS * dn::WROW + n * dn::HROW);
-    const uint32_t dst = c.stages_addr + slot * c.stage_bytes;
-    const uint16_t* wb = (grp.x < E ? w2 + (size_t)grp.x * H * I : ws2 + (size_t)(grp.x - E) * H * I) +
-                         (size_t)r0 * I;
-    bulk_g2s(dst, wb, dn::WBYTES, full_bar(c, slot));
-    bulk_g2s(dst + dn::WBYTES, h + (size_t)grp.y * I, n * dn::HROW, full_bar(c, slot));
-    ++it;
-  }
-  const uint64_t drain = globaltimer_ns() + dn::DRAIN_NS;
-  for (int j = it - c.nstage < 0 ? 0 : it - c.nstage; j < it; ++j)
-    mbar_wait(full_bar(c, j % c.nstage), (uint32_t)(j / c.nstage) & 1u, drain);
 }
 
 }  // namespace dn_impl

@@ -798,8 +798,6 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
   dc.red = buf;
   dc.pair_tok = s_pair_tok;
   dc.pair_w = s_pair_w;
-  dc.hdr = hdr;
-  dc.abort_flag = &s_abort;
 
   int it = 0, useq = 0;
   const uint64_t drain = deadline + fz::DRAIN_NS;

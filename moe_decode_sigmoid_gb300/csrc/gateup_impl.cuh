@@ -136,7 +136,7 @@ __device__ __forceinline__ void seg_cc(const GuCtx& c, int u0, int u1, int pair0
     for (int i = 0; i < NTOK; ++i) {
       const float gs = warp_sum(g[i]);
       const float vs = warp_sum(v[i]);
-      if (lane == 0 && ok) c.h[(size_t)(pair0 + i) * I + blk * 8 + warp] = silu_mul(gs, vs);
+      if (lane == 0 && ok) store_h_split(c.h, (size_t)(pair0 + i), blk * 8 + warp, silu_mul(gs, vs));
     }
   }
 }
@@ -200,17 +200,19 @@ __device__ __forceinline__ void seg_mma(const GuCtx& c, int u0, int u1, int pair
     }
     named_sync(1, gu::CWARPS * 32);
     {
-      const int r = threadIdx.x >> 5;  // 0..7
-      const int j = threadIdx.x & 31;  // token slot (GROUP_MAX <= 32)
-      if (j < n && ok) {
-        float gs = 0.f, us = 0.f;
+      // thread (token slot j, row r): the 8 rows of a token are 8 adjacent
+      // lanes, which store the token's h block together
+      static_assert(gu::CWARPS * 32 / 8 >= GROUP_MAX, "one 8-lane group per token slot");
+      const int j = threadIdx.x >> 3;
+      const int r = threadIdx.x & 7;
+      const int jr = j < n ? j : 0;
+      float gs = 0.f, us = 0.f;
 #pragma unroll
-        for (int w = 0; w < gu::CWARPS; ++w) {
-          gs += c.buf[(w * gu::ROWS + r) * GROUP_MAX + j];
-          us += c.buf[(w * gu::ROWS + r + 8) * GROUP_MAX + j];
-        }
-        c.h[(size_t)(pair0 + j) * I + blk * 8 + r] = silu_mul(gs, us);
+      for (int w = 0; w < gu::CWARPS; ++w) {
+        gs += c.buf[(w * gu::ROWS + r) * GROUP_MAX + jr];
+        us += c.buf[(w * gu::ROWS + r + 8) * GROUP_MAX + jr];
       }
+      store_h_block8(c.h, (size_t)(pair0 + jr), blk, silu_mul(gs, us), j < n && ok);
     }
     named_sync(1, gu::CWARPS * 32);
   }
