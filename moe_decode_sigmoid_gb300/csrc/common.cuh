@@ -179,15 +179,18 @@ __device__ __forceinline__ void split_bf2(float a, float b, uint32_t& hi, uint32
   lo = pack_bf2(a - bf_lo(hi), b - bf_hi(hi));
 }
 
-// Split h rows.  Each block of 8 consecutive elements k in [8b, 8b + 8) has a
-// 16-byte chunk of hi = bf16(h) values and a 16-byte chunk of lo =
-// bf16(h - hi) values (hi + lo keeps ~16 significant bits of the fp32 h; the
-// parts are ready-made bf16 MMA operands).  Line b / 4 (128 bytes) of the row
-// holds blocks 4(b/4) .. 4(b/4)+3, chunk 2(b%4) + part, permuted by XOR with
-// the row's pair index mod 8: 8 consecutive rows read at the same columns then
-// fall in distinct shared-memory banks after a plain row-by-row copy.
+// Split h rows.  Column k belongs to block b = k / 8; the row is 16 lines of
+// 128 bytes, and block b lives in line kc = 2 (b / 8) + b % 2 at chunk pair
+// q = (b % 8) / 2: its 8 hi = bf16(h) values in 16-byte chunk 2q and its 8
+// lo = bf16(h - hi) values in chunk 2q + 1, both XOR-permuted by the row's
+// pair index mod 8.  hi + lo keeps ~16 significant bits of the fp32 h, the
+// parts are ready-made bf16 MMA operands, and a reader whose lane q takes
+// block 8 (kc / 2) + 2q + kc % 2 at step kc finds the 8 lanes of each
+// 128-bit load phase (two consecutive rows) in distinct banks.
 __host__ __device__ __forceinline__ int h_chunk(size_t pair, int blk, int part) {
-  return (blk >> 2) * 128 + (((2 * (blk & 3) + part) ^ (int)(pair & 7)) * 16);
+  const int line = 2 * (blk >> 3) + (blk & 1);
+  const int q = (blk & 7) >> 1;
+  return line * 128 + (((2 * q + part) ^ (int)(pair & 7)) * 16);
 }
 
 // One element.

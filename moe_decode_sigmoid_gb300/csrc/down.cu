@@ -47,10 +47,8 @@ constexpr int WBYTES = RS * WROW;       // 16 KiB
 constexpr int PAIRS = 4;                // consumer warp pairs; a pair takes one group at a time
 constexpr int CW = 2 * PAIRS;           // consumer warps
 constexpr int PRODUCER = CW;            // warp that fills the ring
-constexpr int PREFETCHER = CW + 1;      // warp that prefetches Wd slices into L2
-constexpr int THREADS = (CW + 2) * 32;
+constexpr int THREADS = (CW + 1) * 32;
 constexpr int NDESC = 16;               // groups in the ring at most (one mbarrier pair each)
-constexpr int PF = 8;                   // groups ahead whose Wd slice is prefetched into L2
 constexpr int SMEM_CAP = 232448 - 1024; // opt-in maximum minus static/slack
 constexpr int ALIGN = 1024;             // 128-byte swizzled tensor copies land on 1 KiB boundaries
 constexpr uint64_t DRAIN_NS = 2000000000ull;
@@ -144,14 +142,18 @@ struct Ring {
 // mbarrier pair are free: the producer waits for the oldest unreleased
 // groups, in issue order, until both hold.
 __device__ void produce(const Ring& R, const DnMeta& meta, const DnMaps& maps, const float* h,
-                        int r0, WsHeader* hdr, volatile int* abort_flag, uint64_t deadline,
-                        uint32_t* gend, volatile int* issued) {
+                        int r0, WsHeader* hdr, volatile int* abort_flag, uint64_t deadline) {
   const int n_groups = meta.n_groups;
   RingPos pos(R.ring);
   uint32_t released = 0;  // ring position up to which every byte is free again
   int rel = 0;            // groups [0, rel) are released
-  // The loop body is one thread's dependent chain: the next descriptor is
-  // loaded one iteration ahead.
+  // Ring ends of the outstanding groups rel, rel + 1, ... in registers (a
+  // shift register: every access is a static index), so that the wait loop's
+  // chain has no shared-memory round trip besides the barrier test.
+  uint32_t ends[NDESC];
+#pragma unroll
+  for (int i = 0; i < NDESC; ++i) ends[i] = 0;
+  // The next descriptor is loaded one iteration ahead.
   int4 grp = n_groups > 0 ? meta.groups[0] : make_int4(0, 0, 0, 0);
   int g = 0;
   for (; g < n_groups; ++g) {
@@ -162,17 +164,22 @@ __device__ void produce(const Ring& R, const DnMeta& meta, const DnMaps& maps, c
     const uint32_t off = pos.place(need, start);
     bool ok = true;
     while (rel < g && (g - rel >= NDESC || start + need - released > R.ring)) {
-      if (!mbar_wait(R.empty(rel), Ring::parity(rel), deadline) || *abort_flag) {
+      if (!mbar_wait(R.empty(rel), Ring::parity(rel), deadline)) {
         if (!*abort_flag) set_error(hdr, DEV_TIMEOUT);
         *abort_flag = 1;
         ok = false;
         break;
       }
-      released = gend[rel % NDESC];
+      released = ends[0];
+#pragma unroll
+      for (int i = 0; i + 1 < NDESC; ++i) ends[i] = ends[i + 1];
       ++rel;
     }
-    if (!ok) break;
-    gend[g % NDESC] = start + need;
+    if (!ok || ((g & 15) == 0 && *abort_flag)) break;
+    const int slot = g - rel;  // < NDESC
+#pragma unroll
+    for (int i = 0; i < NDESC; ++i)
+      if (i == slot) ends[i] = start + need;
     const uint32_t dst = R.base_addr + off;
     mbar_expect_tx(R.full(g), need);
     if (cur.x < E)
@@ -180,31 +187,10 @@ __device__ void produce(const Ring& R, const DnMeta& meta, const DnMaps& maps, c
     else
       tma_load_3d(dst, &maps.ws2, 0, (cur.x - E) * H + r0, 0, R.full(g));
     bulk_g2s(dst + WBYTES, h + (size_t)cur.y * I, cur.z * HROW, R.full(g));
-    *issued = g + 1;
   }
   // No copy may still be landing in shared memory when the CTA exits.
   const uint64_t drain = globaltimer_ns() + DRAIN_NS;
   for (int j = rel; j < g; ++j) mbar_wait(R.full(j), Ring::parity(j), drain);
-}
-
-// One lane of the prefetch warp: keeps the Wd slices of the PF groups after
-// the last issued one on their way into L2, so the ring fills from L2 and
-// each group holds its ring bytes for an L2 round trip instead of an HBM one.
-// A hint only: nothing waits for it.
-__device__ void prefetch_ahead(const DnMeta& meta, const uint16_t* w2, const uint16_t* ws2, int r0,
-                               volatile int* abort_flag, volatile int* issued, uint64_t deadline) {
-  int seen = 0;
-  for (int j = 0; j < meta.n_groups; ++j) {
-    while (j >= seen + PF) {
-      seen = *issued;
-      if (*abort_flag || globaltimer_ns() > deadline) return;
-    }
-    const int4 grp = meta.groups[j];
-    const uint16_t* wb =
-        (grp.x < E ? w2 + (size_t)grp.x * H * I : ws2 + (size_t)(grp.x - E) * H * I) +
-        (size_t)r0 * I;
-    prefetch_l2_bulk(wb, WBYTES);
-  }
 }
 
 // Barrier over one warp pair (64 threads, barrier id) that also ANDs a flag
@@ -221,12 +207,14 @@ __device__ __forceinline__ bool pair_sync_and(uint32_t id, bool v) {
 
 // One warp, half the K columns of one group of n <= 8 * NT tokens:
 // d[nt] = Wd_slice[:, K half] * h[tokens, K half]^T for token tile nt.
-// Lane (gq = lane / 4, q = lane % 4) holds Wd rows gq and gq + 8 and K columns
-// kc * 32 + q * 8 + [0, 8) of chunk kc; the same K relabeling is applied to h,
-// so the products pair up as in the plain dot product.  Both operands sit in
-// shared memory with 16-byte chunks XOR-permuted by row mod 8 (Wd by the
-// tensor copy, h by its writer).  hi and lo, and the two halves of each chunk,
-// go to four independent accumulators so the MMA chains overlap.
+// Lane (gq = lane / 4, q = lane % 4) holds Wd rows gq and gq + 8 and, at step
+// kc, the 8 K columns of block 8 (kc / 2) + 2q + kc % 2; h is read with the
+// same K relabeling, so the products pair up as in the plain dot product.
+// Both operands sit in shared memory with 16-byte chunks XOR-permuted by row
+// mod 8 (Wd by the tensor copy, h by its writer); with this relabeling each
+// 8-lane phase of a 128-bit load touches 8 distinct banks.  hi and lo, and the
+// two halves of each step, go to four independent accumulators so the MMA
+// chains overlap.
 // d element e: (row, token column) = (gq, 2q), (gq, 2q+1), (gq+8, 2q), (gq+8, 2q+1).
 template <int NT>
 __device__ __forceinline__ void group_half(const uint8_t* st, int n, int pair0, int khalf,
@@ -239,6 +227,7 @@ __device__ __forceinline__ void group_half(const uint8_t* st, int n, int pair0, 
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[nt][c][0] = acc[nt][c][1] = acc[nt][c][2] = acc[nt][c][3] = 0.f;
   // Wd (row r, column k) sits at line (k / 64) * 16 + r, chunk ((k / 8) % 8) ^ (r % 8).
+  // h block b of a row sits at line 2 (b / 8) + b % 2, chunks (2 ((b % 8) / 2) + part) ^ x.
   const uint8_t* wrow = st + gq * 128;
   // Token columns past n read token 0's row: their results are never used,
   // and the loads need no branch.
@@ -253,12 +242,12 @@ __device__ __forceinline__ void group_half(const uint8_t* st, int n, int pair0, 
 #pragma unroll
   for (int kk = 0; kk < I / 64; ++kk) {
     const int kc = khalf * (I / 64) + kk;
-    const uint8_t* wl = wrow + (kc >> 1) * (16 * 128) + ((((kc & 1) * 4 + q) ^ gq) * 16);
+    const uint8_t* wl = wrow + (kc >> 1) * (16 * 128) + (((2 * q + (kc & 1)) ^ gq) * 16);
     const uint4 alo = *reinterpret_cast<const uint4*>(wl);
     const uint4 ahi = *reinterpret_cast<const uint4*>(wl + 8 * 128);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      // hi and lo chunks of K columns kc * 32 + q * 8 + [0, 8)
+      // hi and lo chunks of the same block
       const uint8_t* hl = hrow[nt] + kc * 128;
       const uint4 b = *reinterpret_cast<const uint4*>(hl + (((2 * q) ^ hx[nt]) * 16));
       const uint4 l = *reinterpret_cast<const uint4*>(hl + (((2 * q + 1) ^ hx[nt]) * 16));
@@ -323,9 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     down_bf16_kernel(ExpertArgs a, const __grid_constant__ DnMaps maps) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ int s_abort;
-  __shared__ int s_issued;            // groups the producer has issued
   __shared__ int s_ngroups;
-  __shared__ uint32_t s_gend[NDESC];  // producer: monotonic end of the groups in the ring
   volatile int* abort_flag = &s_abort;
   const int B = a.B;
   const uint32_t ring = (uint32_t)ring_bytes(B);
@@ -349,7 +336,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(R.empty0 + 8u * s, 1);
     }
     s_abort = 0;
-    s_issued = 0;
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < PAIRS * B * RS; i += blockDim.x) accw[i] = 0.f;
@@ -362,13 +348,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   meta.groups = groups_s;
   meta.pair_tok = pair_tok_s;
   meta.pair_w = pair_w_s;
-  if (warp >= PRODUCER) {
+  if (warp == PRODUCER) {
     named_sync(2, THREADS);  // routing metadata is in shared memory
     meta.n_groups = s_ngroups;
-    if (lane == 0 && warp == PRODUCER)
-      produce(R, meta, maps, a.ws.h, r0, a.ws.hdr, abort_flag, deadline, s_gend, &s_issued);
-    if (lane == 0 && warp == PREFETCHER)
-      prefetch_ahead(meta, a.w.w2, a.w.ws2, r0, abort_flag, &s_issued, deadline);
+    if (lane == 0) produce(R, meta, maps, a.ws.h, r0, a.ws.hdr, abort_flag, deadline);
     return;
   }
   // Routing metadata into shared memory: all loads first, then the stores,
