@@ -242,7 +242,7 @@ flint_status flint_moe_debug_arm_stall(void* workspace, size_t ws_bytes, cudaStr
  * locks -- and so cannot provide the workspace the other entry points take.
  *
  * Instead of a workspace it uses one static device array of this library
- * (about 400 KiB, sized for FLINT_MOE_NOALLOC_MAX_BATCH tokens), which every
+ * (about 860 KiB, sized for FLINT_MOE_NOALLOC_MAX_BATCH tokens), which every
  * GPU that loads the library holds until the process exits.  It calls no
  * allocating routine.  Inputs, outputs and their layouts are those of
  * flint_moe_decode_bf16, and so are the results.

@@ -208,7 +208,7 @@ static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const vo
   if (e != cudaSuccess) return cuda_status(e);
   e = nvfp4 ? launch_gateup_nvfp4(a, stream, sms) : launch_gateup_bf16(a, stream, sms);
   if (e != cudaSuccess) return cuda_status(e);
-  e = nvfp4 ? launch_down_nvfp4(a, stream) : launch_down_bf16(a, stream);
+  e = nvfp4 ? launch_down_nvfp4(a, stream, sms) : launch_down_bf16(a, stream);
   return cuda_status(e);
 }
 

@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace flint {
@@ -31,12 +32,13 @@ constexpr uint32_t DEV_TIMEOUT = 5;
 // ---- workspace layout ------------------------------------------------------
 // [ header | logits fp32 [MAX_B,E] | topk_idx i32 [MAX_B,K] | topk_w f32 [MAX_B,K] |
 //   pair_tok i32 [MAX_B*SLOTS] | pair_w f32 [MAX_B*SLOTS] | groups int4 [MAX_GROUPS] |
-//   h [max_batch*SLOTS, I] x 4 bytes ]
-// h holds fp32 for the fused kernel and the NVFP4 kernels; the BF16 gate/up
-// and down kernels of the large-batch path store each element as a bf16
-// hi + lo pair instead (see store_h_split), in the same 4 bytes.
-// Every array but the last is sized for MAX_B, so the offsets do not depend on
-// the batch a workspace was sized for; only h grows with max_batch.
+//   h [max_batch*SLOTS, I] x 4 bytes | y fp32 [max_batch*SLOTS, H] ]
+// h holds fp32 for the fused kernel; the BF16 gate/up kernel of the
+// three-kernel path stores each element as a bf16 hi + lo pair instead (same
+// 4 bytes, see h_chunk), the NVFP4 one as one f16 (1 KiB rows, h_off_nv).
+// Every array but the last two is sized for MAX_B, so the offsets do not
+// depend on the batch a workspace was sized for; h and y grow with max_batch,
+// and a call with batch B finds y right after the first B * SLOTS h rows.
 struct WsHeader {
   uint32_t error;            // DEV_OK or an error code (first writer wins)
   uint32_t tiles_done;       // router: token tiles whose top-k is final
@@ -48,7 +50,8 @@ struct WsHeader {
   uint32_t tile_ctas_done[MAX_B / 8];  // router: finished CTAs per token tile
   uint32_t grid_bar[3];      // fused kernel: logits barrier, (unused), exit count
   uint32_t unit_next;        // fused kernel: next unclaimed gate/up unit
-  uint32_t pad[20];
+  uint32_t rb_done[16];      // NVFP4 down: finished units per 128-row block
+  uint32_t pad[4];
   uint32_t group_done[64];   // fused kernel: finished (unit, warp) parts per group
 };
 static_assert(sizeof(WsHeader) == 512, "header is 512 bytes");
@@ -64,7 +67,7 @@ struct WsLayout {
   static constexpr size_t groups = align256(pair_w + sizeof(float) * (size_t)MAX_B * SLOTS);
   static constexpr size_t h = align256(groups + 16 * (size_t)MAX_GROUPS);
   static constexpr size_t total(int max_b) {
-    return align256(h + sizeof(float) * (size_t)max_b * SLOTS * I);
+    return align256(h + sizeof(float) * (size_t)max_b * SLOTS * (I + H));
   }
 };
 
@@ -79,6 +82,9 @@ struct Ws {
   int4* groups;   // {expert (E.. for shared), first pair, pair count, 0}
   float* h;
 };
+// Per-pair partial down projections of the NVFP4 path, [B * SLOTS][H] fp32,
+// for a call with batch B.
+__host__ __device__ inline float* ws_y(const Ws& w, int B) { return w.h + (size_t)B * SLOTS * I; }
 
 inline Ws ws_view(void* base) {
   char* b = static_cast<char*>(base);
@@ -221,6 +227,33 @@ __device__ __forceinline__ void store_h_block8(float* h, size_t pair, int blk, f
     uint8_t* row = reinterpret_cast<uint8_t*>(h + pair * I);
     *reinterpret_cast<uint4*>(row + h_chunk(pair, blk, 0)) = hv;
     *reinterpret_cast<uint4*>(row + h_chunk(pair, blk, 1)) = lv;
+  }
+}
+
+// The NVFP4 path's h: f16 (11 significant bits, far finer than its 4-bit
+// weights), one 1 KiB row per pair (pair p at byte 1024 p of the h region).
+// The 16-byte block b (columns 8b .. 8b + 7) sits in 64-byte line
+// (b % 16) ^ (p % 2) at slot b / 16 -- the order in which the NVFP4 down
+// kernel's lanes take K (lane q: columns 128q .. 128q + 127, blocks 16q ..
+// 16q + 15 in turn); the line swap by pair parity puts two consecutive rows
+// read at the same step in opposite halves of the 128-byte bank window.
+__host__ __device__ __forceinline__ int h_off_nv(size_t pair, int blk) {
+  return ((blk & 15) ^ (int)(pair & 1)) * 64 + (blk >> 4) * 16;
+}
+
+// One block at once: called by all 32 lanes of a warp, lanes 8m..8m+7
+// holding elements 0..7 of one block (v); the first lane of each 8-lane group
+// stores the block when `store` is true (uniform within the group).
+__device__ __forceinline__ void store_h_block8_nv(float* h, size_t pair, int blk, float v,
+                                                  bool store) {
+  const uint32_t hv16 = __half_as_ushort(__float2half_rn(v));
+  const uint32_t w = hv16 | (__shfl_down_sync(0xffffffffu, hv16, 1) << 16);
+  const uint4 hv = make_uint4(w, __shfl_down_sync(0xffffffffu, w, 2),
+                              __shfl_down_sync(0xffffffffu, w, 4),
+                              __shfl_down_sync(0xffffffffu, w, 6));
+  if ((threadIdx.x & 7) == 0 && store) {
+    uint8_t* row = reinterpret_cast<uint8_t*>(h) + pair * (I * 2);
+    *reinterpret_cast<uint4*>(row + h_off_nv(pair, blk)) = hv;
   }
 }
 

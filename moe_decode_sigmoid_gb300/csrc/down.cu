@@ -1,446 +1,56 @@
-// down.cu — down GEMV fused with the routing-weighted combine, the shared-
-// expert add and the residual add, BF16 weights (batches above the fused
-// kernel's limit).
+// down.cu — the BF16 weight format of the large-batch down kernel
+// (down_ring.cuh holds the kernel; the fused kernel covers batches of at most
+// 8 tokens).
 //
-//   out[t] = residual[t] + sum over groups g containing t of
-//            w(t, g) * Wd_{expert(g)} h[pair(t, g)]
-// where shared-expert groups carry weight 1.  The expert combine sits in the
-// same kernel as the down GEMV, as on the pages' low-latency decode path
-// ("fuses ... routing, and expert combine into neighboring GEMV kernels":
-// vLLM Day-0 Support for Recursive's Flint, "Optimization Strategies").
-//
-// Row-slice-major: CTA b owns output rows [16b, 16b+16) of every token and
-// walks all groups in order, so each weight byte is read by exactly one CTA
-// and the combine needs no atomics.  Per group the producer lane copies the
-// CTA's 16 rows of Wd with one 3-D tensor copy (TMA) that swizzles 16-byte
-// chunks by row (128-byte swizzle), and the group's h rows with one bulk copy
-// (the gate/up kernel stores them split into bf16 hi + lo parts and already
-// swizzled by row), into a byte ring in shared memory: each group takes only
-// the bytes it needs (16 KiB + 2 KiB per token), so a ring of ~150-200 KiB
-// keeps ~8 groups of small batches in flight per SM, and the MMA fragment
-// loads from either operand hit distinct banks.
-//
-// Warp pair p (of 4) takes groups p, p + 4, p + 8, ...: mma.sync m16n8k16
-// with the 16 Wd rows as M, the group's tokens as N (8 per tile) and K split
-// between the pair's two warps (256 columns each); the hi and lo parts of h
-// each take one MMA, so the operand keeps ~16 significant bits of the fp32 h.
-// The odd warp hands its partial tiles to the even one through shared memory;
-// the even warp applies the routing weights into the pair's own accumulator
-// rows.  The four pairs work on four groups at once and never wait for each
-// other; the four partial sums are added in a fixed order when the output is
-// written, so results are bitwise reproducible.
-#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched at run time
-
+// A group's 16-row Wd slice (16 KiB) arrives through one 3-D tensor copy
+// (TMA) with a 128-byte swizzle: the map views a Wd stack as (64 columns,
+// row, 8 column blocks) with strides (2 bytes, 1 KiB, 128 bytes), so a
+// (64, 16, 8) box lands as 8 column blocks of 16 rows x 128 bytes with each
+// row's 16-byte chunks XOR-permuted by row mod 8.  Lane q takes, at step kk of
+// K half kh (kc = 8 kh + kk), K block 8 (kc / 2) + 2q + kc % 2: the two rows of
+// every 8-lane phase of a 128-bit load then fall in opposite chunk parities,
+// so the fragment loads are free of bank conflicts.  The gate/up kernel
+// writes h with the same block order (h_chunk).  The odd warp of a pair hands
+// its tiles over in the half of the slice that only it reads.
 #include <mutex>
 
-#include "common.cuh"
-#include "expert_common.cuh"
-#include "kernels.h"
+#include "down_ring.cuh"
 
 namespace flint {
 namespace {
 
-constexpr int RS = 16;                  // output rows per CTA
-constexpr int WROW = I * 2;             // bytes of one Wd row
-constexpr int HROW = I * 4;             // bytes of one split h row
-constexpr int WBYTES = RS * WROW;       // 16 KiB
-constexpr int PAIRS = 4;                // consumer warp pairs; a pair takes one group at a time
-constexpr int CW = 2 * PAIRS;           // consumer warps
-constexpr int PRODUCER = CW;            // warp that fills the ring
-constexpr int THREADS = (CW + 1) * 32;
-constexpr int NDESC = 16;               // groups in the ring at most (one mbarrier pair each)
-constexpr int SMEM_CAP = 232448 - 1024; // opt-in maximum minus static/slack
-constexpr int ALIGN = 1024;             // 128-byte swizzled tensor copies land on 1 KiB boundaries
-constexpr uint64_t DRAIN_NS = 2000000000ull;
-// Pair p consumes groups p, p + PAIRS, ...; with NDESC a multiple of PAIRS the
-// pair that waits on a descriptor's next phase is the one that consumed its last.
-static_assert(NDESC % PAIRS == 0, "descriptor reuse stays within one pair");
-
-// Every group's bytes are a multiple of ALIGN, so every group starts aligned.
-__host__ __device__ constexpr int group_bytes(int n) { return WBYTES + n * HROW; }
-static_assert(WBYTES % ALIGN == 0 && HROW % ALIGN == 0, "groups stay aligned in the ring");
-// Groups the bucketing can form for a batch of B: per routed expert one per
-// GROUP_MAX of its tokens, and the same for the shared expert(s).
-__host__ __device__ inline int group_cap(int B) {
-  const int routed = (TOPK * B + GROUP_MAX - 1) / GROUP_MAX + (TOPK * B < E ? TOPK * B : E);
-  const int cap = routed + S * ((B + GROUP_MAX - 1) / GROUP_MAX);
-  return cap < MAX_GROUPS ? cap : MAX_GROUPS;
-}
-// Shared memory after the ring: accumulators [PAIRS][B][RS] fp32, the group
-// table, the pairs' tokens and weights, the mbarriers.
-__host__ __device__ inline int fixed_bytes(int B) {
-  return PAIRS * B * RS * 4 + group_cap(B) * 16 + 2 * B * SLOTS * 4 + 2 * NDESC * 8;
-}
-__host__ __device__ inline int ring_bytes(int B) {
-  return ((SMEM_CAP - ALIGN - fixed_bytes(B)) / ALIGN) * ALIGN;
-}
-__host__ inline int smem_bytes(int B) { return ALIGN + ring_bytes(B) + fixed_bytes(B); }
-static_assert(MAX_B * RS * 4 * PAIRS + MAX_GROUPS * 16 + 2 * MAX_B * SLOTS * 4 + 2 * NDESC * 8 +
-                      ALIGN + group_bytes(GROUP_MAX) <=
-                  SMEM_CAP,
-              "the ring holds the largest group at the largest batch");
-// The odd warp of a pair hands its tiles over in the half of the group's Wd
-// slice that only it reads (bytes [WBYTES / 2, WBYTES)).
-static_assert(((GROUP_MAX + 7) / 8) * 4 * 32 * 4 <= WBYTES / 2, "hand-over fits the Wd half");
-
-struct DnMeta {
-  const int4* groups;
-  const int* pair_tok;
-  const float* pair_w;
-  int n_groups;
-};
-
-// Tensor maps of the routed and shared Wd stacks, viewed as 3-D
-// (64 columns, row, 8 column blocks) with strides (2 bytes, 1 KiB, 128 bytes):
-// a (64, 16, 8) box is one CTA's 16-row slice, landing as 8 column blocks of
-// 16 rows x 128 bytes, each row's 16-byte chunks XOR-permuted by row mod 8.
-struct DnMaps {
-  CUtensorMap w2;
-  CUtensorMap ws2;
-};
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            int c2, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-
-// Position of each group in the ring, both as a monotonic byte count (for
-// the free-space test) and as the offset in the ring.  A group never
-// straddles the ring's end: if it would, it starts at the next wrap instead.
-struct RingPos {
-  uint32_t mono = 0, off = 0;
-  uint32_t ring;
-  __device__ explicit RingPos(uint32_t r) : ring(r) {}
-  // Returns the group's ring offset; `start` gets its monotonic position.
-  __device__ __forceinline__ uint32_t place(uint32_t need, uint32_t& start) {
-    if (off + need > ring) {
-      mono += ring - off;
-      off = 0;
-    }
-    start = mono;
-    const uint32_t o = off;
-    mono += need;
-    off += need;
-    return o;
-  }
-};
-
-struct Ring {
-  uint8_t* base;
-  uint32_t base_addr, ring;
-  uint32_t full0, empty0;
-  __device__ uint32_t full(int g) const { return full0 + 8u * (uint32_t)(g % NDESC); }
-  __device__ uint32_t empty(int g) const { return empty0 + 8u * (uint32_t)(g % NDESC); }
-  __device__ static uint32_t parity(int g) { return (uint32_t)(g / NDESC) & 1u; }
-};
-
-// One lane of the producer warp.  Group g is issued once its bytes and its
-// mbarrier pair are free: the producer waits for the oldest unreleased
-// groups, in issue order, until both hold.
-__device__ void produce(const Ring& R, const DnMeta& meta, const DnMaps& maps, const float* h,
-                        int r0, WsHeader* hdr, volatile int* abort_flag, uint64_t deadline) {
-  const int n_groups = meta.n_groups;
-  RingPos pos(R.ring);
-  uint32_t released = 0;  // ring position up to which every byte is free again
-  int rel = 0;            // groups [0, rel) are released
-  // Ring ends of the outstanding groups rel, rel + 1, ... in registers (a
-  // shift register: every access is a static index), so that the wait loop's
-  // chain has no shared-memory round trip besides the barrier test.
-  uint32_t ends[NDESC];
-#pragma unroll
-  for (int i = 0; i < NDESC; ++i) ends[i] = 0;
-  // The next descriptor is loaded one iteration ahead.
-  int4 grp = n_groups > 0 ? meta.groups[0] : make_int4(0, 0, 0, 0);
-  int g = 0;
-  for (; g < n_groups; ++g) {
-    const int4 cur = grp;
-    if (g + 1 < n_groups) grp = meta.groups[g + 1];
-    const uint32_t need = (uint32_t)group_bytes(cur.z);
-    uint32_t start;
-    const uint32_t off = pos.place(need, start);
-    bool ok = true;
-    while (rel < g && (g - rel >= NDESC || start + need - released > R.ring)) {
-      if (!mbar_wait(R.empty(rel), Ring::parity(rel), deadline)) {
-        if (!*abort_flag) set_error(hdr, DEV_TIMEOUT);
-        *abort_flag = 1;
-        ok = false;
-        break;
-      }
-      released = ends[0];
-#pragma unroll
-      for (int i = 0; i + 1 < NDESC; ++i) ends[i] = ends[i + 1];
-      ++rel;
-    }
-    if (!ok || ((g & 15) == 0 && *abort_flag)) break;
-    const int slot = g - rel;  // < NDESC
-#pragma unroll
-    for (int i = 0; i < NDESC; ++i)
-      if (i == slot) ends[i] = start + need;
-    const uint32_t dst = R.base_addr + off;
-    mbar_expect_tx(R.full(g), need);
-    if (cur.x < E)
-      tma_load_3d(dst, &maps.w2, 0, cur.x * H + r0, 0, R.full(g));
+struct Bf16Wd {
+  static constexpr int WBYTES = dring::RS * I * 2;  // 16 KiB
+  static constexpr int WCOPY = WBYTES;
+  static constexpr int XCH = WBYTES / 2;
+  static constexpr int NDESC = 16;
+  struct Maps {
+    CUtensorMap w2;
+    CUtensorMap ws2;
+  };
+  struct Frag {};
+  __device__ static void issue(const Maps& maps, const ExpertArgs&, uint32_t dst, int4 grp, int r0,
+                               uint32_t bar) {
+    if (grp.x < E)
+      dring::tma_load_3d(dst, &maps.w2, 0, grp.x * H + r0, 0, bar);
     else
-      tma_load_3d(dst, &maps.ws2, 0, (cur.x - E) * H + r0, 0, R.full(g));
-    bulk_g2s(dst + WBYTES, h + (size_t)cur.y * I, cur.z * HROW, R.full(g));
+      dring::tma_load_3d(dst, &maps.ws2, 0, (grp.x - E) * H + r0, 0, bar);
   }
-  // No copy may still be landing in shared memory when the CTA exits.
-  const uint64_t drain = globaltimer_ns() + DRAIN_NS;
-  for (int j = rel; j < g; ++j) mbar_wait(R.full(j), Ring::parity(j), drain);
-}
-
-// Barrier over one warp pair (64 threads, barrier id) that also ANDs a flag
-// across it: both warps always arrive, so neither can be left waiting.
-__device__ __forceinline__ bool pair_sync_and(uint32_t id, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, %2, 64, p; selp.u32 %0, 1, 0, q; }"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id)
-      : "memory");
-  return r != 0;
-}
-
-// One warp, half the K columns of one group of n <= 8 * NT tokens:
-// d[nt] = Wd_slice[:, K half] * h[tokens, K half]^T for token tile nt.
-// Lane (gq = lane / 4, q = lane % 4) holds Wd rows gq and gq + 8 and, at step
-// kc, the 8 K columns of block 8 (kc / 2) + 2q + kc % 2; h is read with the
-// same K relabeling, so the products pair up as in the plain dot product.
-// Both operands sit in shared memory with 16-byte chunks XOR-permuted by row
-// mod 8 (Wd by the tensor copy, h by its writer); with this relabeling each
-// 8-lane phase of a 128-bit load touches 8 distinct banks.  hi and lo, and the
-// two halves of each step, go to four independent accumulators so the MMA
-// chains overlap.
-// d element e: (row, token column) = (gq, 2q), (gq, 2q+1), (gq+8, 2q), (gq+8, 2q+1).
-template <int NT>
-__device__ __forceinline__ void group_half(const uint8_t* st, int n, int pair0, int khalf,
-                                           float (&d)[NT][4]) {
-  const int lane = threadIdx.x & 31;
-  const int gq = lane >> 2, q = lane & 3;
-  float acc[NT][4][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[nt][c][0] = acc[nt][c][1] = acc[nt][c][2] = acc[nt][c][3] = 0.f;
+  __device__ static void load(const uint8_t*, int, int, int, Frag&) {}
   // Wd (row r, column k) sits at line (k / 64) * 16 + r, chunk ((k / 8) % 8) ^ (r % 8).
-  // h block b of a row sits at line 2 (b / 8) + b % 2, chunks (2 ((b % 8) / 2) + part) ^ x.
-  const uint8_t* wrow = st + gq * 128;
-  // Token columns past n read token 0's row: their results are never used,
-  // and the loads need no branch.
-  const uint8_t* hrow[NT];
-  int hx[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int slot = nt * 8 + gq < n ? nt * 8 + gq : 0;
-    hrow[nt] = st + WBYTES + slot * HROW;
-    hx[nt] = (pair0 + slot) & 7;
-  }
-#pragma unroll
-  for (int kk = 0; kk < I / 64; ++kk) {
+  __device__ static void a(const uint8_t* st, const Frag&, int gq, int q, int khalf, int kk,
+                           uint4& alo, uint4& ahi) {
     const int kc = khalf * (I / 64) + kk;
-    const uint8_t* wl = wrow + (kc >> 1) * (16 * 128) + (((2 * q + (kc & 1)) ^ gq) * 16);
-    const uint4 alo = *reinterpret_cast<const uint4*>(wl);
-    const uint4 ahi = *reinterpret_cast<const uint4*>(wl + 8 * 128);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      // hi and lo chunks of the same block
-      const uint8_t* hl = hrow[nt] + kc * 128;
-      const uint4 b = *reinterpret_cast<const uint4*>(hl + (((2 * q) ^ hx[nt]) * 16));
-      const uint4 l = *reinterpret_cast<const uint4*>(hl + (((2 * q + 1) ^ hx[nt]) * 16));
-      mma_bf16(acc[nt][0], alo.x, ahi.x, alo.y, ahi.y, b.x, b.y);
-      mma_bf16(acc[nt][1], alo.z, ahi.z, alo.w, ahi.w, b.z, b.w);
-      mma_bf16(acc[nt][2], alo.x, ahi.x, alo.y, ahi.y, l.x, l.y);
-      mma_bf16(acc[nt][3], alo.z, ahi.z, alo.w, ahi.w, l.z, l.w);
-    }
+    const uint8_t* wl = st + gq * 128 + (kc >> 1) * (16 * 128) + (((2 * q + (kc & 1)) ^ gq) * 16);
+    alo = *reinterpret_cast<const uint4*>(wl);
+    ahi = *reinterpret_cast<const uint4*>(wl + 8 * 128);
   }
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      d[nt][e] = (acc[nt][0][e] + acc[nt][1][e]) + (acc[nt][2][e] + acc[nt][3][e]);
-}
-
-// One group on one warp pair.  The odd warp hands its K-half tiles to the
-// even warp in the half of the Wd slice that only the odd warp reads; after
-// the pair barrier the even warp adds them and applies the routing weights to
-// the pair's accumulator rows.  Returns false (on both warps) if either
-// warp's data wait failed.
-template <int NT>
-__device__ __forceinline__ bool group_pair(uint8_t* st, bool ok, int n, int pair0, int khalf,
-                                           uint32_t bar_id, float* acc_rows, const int* pair_tok,
-                                           const float* pair_w) {
-  const int lane = threadIdx.x & 31;
-  const int gq = lane >> 2, q = lane & 3;
-  float* xch = reinterpret_cast<float*>(st + WBYTES / 2);
-  float d[NT][4];
-  if (ok) {
-    group_half<NT>(st, n, pair0, khalf, d);
-    if (khalf == 1) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) xch[(nt * 4 + e) * 32 + lane] = d[nt][e];
-    }
+  __device__ static void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                             uint32_t b0, uint32_t b1) {
+    mma_bf16(d, a0, a1, a2, a3, b0, b1);
   }
-  if (!pair_sync_and(bar_id, ok)) return false;
-  if (khalf == 0) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) d[nt][e] += xch[(nt * 4 + e) * 32 + lane];
-      // A group holds each token once, so the lanes' targets are distinct.
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = nt * 8 + 2 * q + e;
-        if (col < n) {
-          const int t = pair_tok[pair0 + col];
-          const float wt = pair_w[pair0 + col];
-          acc_rows[t * RS + gq] += wt * d[nt][e];
-          acc_rows[t * RS + gq + 8] += wt * d[nt][2 + e];
-        }
-      }
-    }
-  }
-  return true;
-}
-
-__global__ void __launch_bounds__(THREADS, 1)
-    down_bf16_kernel(ExpertArgs a, const __grid_constant__ DnMaps maps) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  __shared__ int s_abort;
-  __shared__ int s_ngroups;
-  volatile int* abort_flag = &s_abort;
-  const int B = a.B;
-  const uint32_t ring = (uint32_t)ring_bytes(B);
-  const uint32_t raw_addr = smem_addr(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + ALIGN - 1) & ~uint32_t(ALIGN - 1)) - raw_addr);
-  float* accw = reinterpret_cast<float*>(smem + ring);  // [PAIRS][B][RS]
-  const int gcap = group_cap(B);
-  int4* groups_s = reinterpret_cast<int4*>(accw + PAIRS * B * RS);
-  int* pair_tok_s = reinterpret_cast<int*>(groups_s + gcap);
-  float* pair_w_s = reinterpret_cast<float*>(pair_tok_s + B * SLOTS);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(pair_w_s + B * SLOTS);
-  Ring R;
-  R.base = smem;
-  R.base_addr = smem_addr(smem);
-  R.ring = ring;
-  R.full0 = smem_addr(bars);
-  R.empty0 = smem_addr(bars + NDESC);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NDESC; ++s) {
-      mbar_init(R.full0 + 8u * s, 1);
-      mbar_init(R.empty0 + 8u * s, 1);
-    }
-    s_abort = 0;
-    fence_mbar_init();
-  }
-  for (int i = threadIdx.x; i < PAIRS * B * RS; i += blockDim.x) accw[i] = 0.f;
-  __syncthreads();
-  const int r0 = blockIdx.x * RS;
-  const uint64_t deadline = wait_deadline(a.ws.hdr);
-  pdl_wait();  // h, the group table and the pairs come from the preceding kernels
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  DnMeta meta;
-  meta.groups = groups_s;
-  meta.pair_tok = pair_tok_s;
-  meta.pair_w = pair_w_s;
-  if (warp == PRODUCER) {
-    named_sync(2, THREADS);  // routing metadata is in shared memory
-    meta.n_groups = s_ngroups;
-    if (lane == 0) produce(R, meta, maps, a.ws.h, r0, a.ws.hdr, abort_flag, deadline);
-    return;
-  }
-  // Routing metadata into shared memory: all loads first, then the stores,
-  // so the round trips overlap.
-  {
-    constexpr int CT = CW * 32;
-    constexpr int GR = (MAX_GROUPS + CT - 1) / CT;
-    constexpr int PR = (MAX_B * SLOTS + CT - 1) / CT;
-    int n = (int)__ldcg(&a.ws.hdr->n_groups);
-    if (n > gcap) {  // more groups than the bucketing can form: inconsistent routing
-      if (threadIdx.x == 0) set_error(a.ws.hdr, DEV_BAD_ROUTING);
-      n = 0;
-      *abort_flag = 1;
-    }
-    int4 gv[GR];
-    int tv[PR];
-    float wv[PR];
-#pragma unroll
-    for (int k = 0; k < GR; ++k) {
-      const int i = threadIdx.x + k * CT;
-      gv[k] = i < n ? __ldcg(a.ws.groups + i) : make_int4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int k = 0; k < PR; ++k) {
-      const int i = threadIdx.x + k * CT;
-      const bool in = i < B * SLOTS;
-      tv[k] = in ? __ldcg(a.ws.pair_tok + i) : 0;
-      wv[k] = in ? __ldcg(a.ws.pair_w + i) : 0.f;
-    }
-#pragma unroll
-    for (int k = 0; k < GR; ++k) {
-      const int i = threadIdx.x + k * CT;
-      if (i < n) groups_s[i] = gv[k];
-    }
-#pragma unroll
-    for (int k = 0; k < PR; ++k) {
-      const int i = threadIdx.x + k * CT;
-      if (i < B * SLOTS) {
-        pair_tok_s[i] = tv[k];
-        pair_w_s[i] = wv[k];
-      }
-    }
-    if (threadIdx.x == 0) s_ngroups = n;
-  }
-  pdl_trigger();
-  named_sync(2, THREADS);
-  const int n_groups = s_ngroups;
-  const int pair = warp >> 1, khalf = warp & 1;
-  float* my_acc = accw + pair * B * RS;
-  const uint32_t bar_id = 3 + pair;
-  RingPos pos(ring);
-  int placed = 0;  // groups whose ring position `pos` has passed
-  uint32_t off = 0;
-  for (int g = pair; g < n_groups; g += PAIRS) {
-    uint32_t start;
-    while (placed <= g) off = pos.place((uint32_t)group_bytes(groups_s[placed++].z), start);
-    const int4 grp = groups_s[g];
-    bool ok = !*abort_flag && mbar_wait(R.full(g), Ring::parity(g), deadline);
-    if (!ok && !*abort_flag) {
-      set_error(a.ws.hdr, DEV_TIMEOUT);
-      *abort_flag = 1;
-    }
-    uint8_t* st = smem + off;
-    switch ((grp.z + 7) >> 3) {
-      case 1:
-        ok = group_pair<1>(st, ok, grp.z, grp.y, khalf, bar_id, my_acc, pair_tok_s, pair_w_s);
-        break;
-      case 2:
-        ok = group_pair<2>(st, ok, grp.z, grp.y, khalf, bar_id, my_acc, pair_tok_s, pair_w_s);
-        break;
-      default:
-        ok = group_pair<3>(st, ok, grp.z, grp.y, khalf, bar_id, my_acc, pair_tok_s, pair_w_s);
-        break;
-    }
-    if (!ok) break;
-    // Both warps' ring reads are done (they preceded the pair barrier).
-    if (khalf == 0 && lane == 0) mbar_arrive(R.empty(g));
-  }
-  named_sync(1, CW * 32);
-  if (*abort_flag) return;
-  for (int i = threadIdx.x; i < B * RS; i += CW * 32) {
-    const int t = i / RS, r = i % RS;
-    float v = accw[i];
-#pragma unroll
-    for (int p = 1; p < PAIRS; ++p) v += accw[p * B * RS + i];
-    const size_t o = (size_t)t * H + r0 + r;
-    a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + v);
-  }
-}
+  __device__ static float scale(const ExpertArgs&, int) { return 1.f; }
+};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -466,8 +76,8 @@ cudaError_t encode_wd(CUtensorMap* m, const uint16_t* w, int experts) {
   const EncodeTiledFn enc = encode_tiled();
   if (enc == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {64, (cuuint64_t)experts * H, I / 64};
-  const cuuint64_t strides[2] = {(cuuint64_t)WROW, 128};  // bytes, for dims 1 and 2
-  const cuuint32_t box[3] = {64, RS, I / 64};
+  const cuuint64_t strides[2] = {(cuuint64_t)I * 2, 128};  // bytes, for dims 1 and 2
+  const cuuint32_t box[3] = {64, dring::RS, I / 64};
   const cuuint32_t elem[3] = {1, 1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(w), dims,
                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -479,28 +89,11 @@ cudaError_t encode_wd(CUtensorMap* m, const uint16_t* w, int experts) {
 }  // namespace
 
 cudaError_t launch_down_bf16(const ExpertArgs& a, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(down_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CAP);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  DnMaps maps;
+  Bf16Wd::Maps maps;
   cudaError_t e = encode_wd(&maps.w2, a.w.w2, E);
   if (e == cudaSuccess) e = encode_wd(&maps.ws2, a.w.ws2, S);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(H / RS, 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(a.B);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, down_bf16_kernel, a, maps);
+  return dring::launch_down_ring<Bf16Wd>(a, maps, stream);
 }
 
 }  // namespace flint

@@ -63,7 +63,7 @@ cudaError_t launch_down_bf16(const ExpertArgs& a, cudaStream_t stream);
 cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                               int num_sms);
 cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
-cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream);
+cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
 cudaError_t launch_rmsnorm(const uint16_t* in, uint16_t* out, int B, float eps,
                            cudaStream_t stream);
 cudaError_t launch_ws_init(WsHeader* hdr, uint64_t wait_limit_ns, cudaStream_t stream);

@@ -12,16 +12,17 @@
 // [2^-10, 2688], so it is EXACT in f16: each thread converts its fragment's
 // codes with cvt.rn.f16x2.e2m1x2, multiplies by the block scale (f16x2, exact)
 // and feeds mma.sync m16n8k16 f16 x f16 -> fp32.  bf16 activations convert to
-// f16 exactly (8 significant bits; |x| inside f16's normal range); the fp32 h
-// is split into two f16 parts (hi + lo, two MMAs); the tensor scale is
-// applied to the fp32 sums.  Dequantisation costs about one instruction per weight, which is
+// f16 exactly (8 significant bits; |x| inside f16's normal range); h is
+// stored in f16 (11 significant bits, against 4-bit weights); the tensor scale
+// is applied to the fp32 sums.  Dequantisation costs about one instruction per weight, which is
 // why this path uses the tensor cores for every group, including single-token
 // ones: the FMAs then cost nothing on the CUDA cores that do the unpacking.
 //
-// The work decomposition and the TMA/mbarrier pipeline are the same as the
-// BF16 kernels (gateup.cu, down.cu): gate/up units are (group, 8 gate + 8 up
-// rows) ranges split evenly over one CTA per SM; the down kernel is
-// row-slice-major (16 output rows per CTA, all groups, deterministic combine).
+// The gate/up work decomposition and its TMA/mbarrier pipeline are those of
+// the BF16 gate/up kernel (gate/up units are (group, 8 gate + 8 up rows)
+// ranges split evenly over one CTA per SM); it stores h as f16 for the down
+// kernel, which splits the work into (group, 128-row block) units and
+// combines the partial sums per row block (see below).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -45,27 +46,6 @@ constexpr int GU_BUF = GU_RED * 4 > LOCAL_SELECT_MAX_B * E * 4 ? GU_RED * 4 : LO
 constexpr size_t GU_SMEM =
     (size_t)GU_NSTAGE * GU_STAGE + GU_BUF + sizeof(MetaSmem) + 2 * GU_NSTAGE * 8;
 constexpr int UNITS = I / 8;
-// down
-constexpr int RS = 16;
-constexpr int DN_QROW = I / 2;                       // 256
-constexpr int DN_QSTRIDE = DN_QROW;                  // 16 rows = one contiguous copy
-constexpr int DN_SFROW = I / 16;                     // 32
-constexpr int DN_WBYTES = RS * DN_QSTRIDE + RS * DN_SFROW;  // 4,608
-constexpr int HROW = I * 4;
-constexpr int HSTRIDE = HROW;
-constexpr int DN_RED = CWARPS * RS * GROUP_MAX;
-constexpr int DN_MAX_STAGES = 8;
-constexpr int SMEM_CAP = 232448 - 1024;
-__host__ __device__ inline int dn_nmax(int B) { return B < GROUP_MAX ? B : GROUP_MAX; }
-__host__ __device__ inline int dn_stage(int B) { return DN_WBYTES + dn_nmax(B) * HSTRIDE; }
-__host__ __device__ inline int dn_fixed(int B) {
-  return DN_RED * 4 + B * RS * 4 + (int)sizeof(MetaSmem) + MAX_B * SLOTS * 4 + 2 * DN_MAX_STAGES * 8;
-}
-__host__ __device__ inline int dn_nstages(int B) {
-  int n = (SMEM_CAP - dn_fixed(B)) / dn_stage(B);
-  return n > DN_MAX_STAGES ? DN_MAX_STAGES : n;
-}
-__host__ __device__ inline int dn_smem(int B) { return dn_nstages(B) * dn_stage(B) + dn_fixed(B); }
 }  // namespace f4
 
 namespace {
@@ -101,14 +81,6 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// (a, b) = hi + lo, both f16x2.
-__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  const float2 back = __half22float2(h);
-  lo = f16x2_of(a - back.x, b - back.y);
 }
 
 // bf16 x 8 (uint4) -> f16 x 8 (uint4), same element order.
@@ -284,17 +256,20 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, c
     }
     named_sync(1, f4::CWARPS * 32);
     {
-      const int r = threadIdx.x >> 5;
-      const int j = threadIdx.x & 31;
-      if (j < n && ok) {
-        float gs = 0.f, us = 0.f;
+      // thread (token slot j, row r): a token's 8 rows are 8 adjacent lanes,
+      // which store its split h block together
+      static_assert(f4::CWARPS * 32 / 8 >= GROUP_MAX, "one 8-lane group per token slot");
+      const int j = threadIdx.x >> 3;
+      const int r = threadIdx.x & 7;
+      const int jr = j < n ? j : 0;
+      float gs = 0.f, us = 0.f;
 #pragma unroll
-        for (int w = 0; w < f4::CWARPS; ++w) {
-          gs += red[(w * 16 + r) * GROUP_MAX + j];
-          us += red[(w * 16 + r + 8) * GROUP_MAX + j];
-        }
-        a.ws.h[(size_t)(pair0 + j) * I + blk * 8 + r] = silu_mul(gs * ts_g, us * ts_u);
+      for (int w = 0; w < f4::CWARPS; ++w) {
+        gs += red[(w * 16 + r) * GROUP_MAX + jr];
+        us += red[(w * 16 + r + 8) * GROUP_MAX + jr];
       }
+      store_h_block8_nv(a.ws.h, (size_t)(pair0 + jr), blk, silu_mul(gs * ts_g, us * ts_u),
+                        j < n && ok);
     }
     named_sync(1, f4::CWARPS * 32);
   }
@@ -322,102 +297,6 @@ __device__ __forceinline__ void gu_produce(const Pipe& p, const ExpertArgs& a, c
              full_bar(p, slot));
     bulk_g2s(dst + 16 * f4::GU_QSTRIDE + 8 * f4::GU_SFROW, sb + (size_t)(I + blk * 8) * f4::GU_SFROW,
              8 * f4::GU_SFROW, full_bar(p, slot));
-    ++it;
-  }
-  drain(p, it);
-}
-
-// ---------------------------------------------------------------- down
-
-template <int NT>
-__device__ __forceinline__ void dn_group(const ExpertArgs& a, const int* pair_tok,
-                                         const float* pair_w, const uint8_t* st, float* red,
-                                         float* acc_s, int expert, int pair0, int n) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, q = lane & 3;
-  float acc[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-  // K order inside this warp's 64-column slice: thread q owns columns
-  // [16q, 16q + 16) (8 contiguous code bytes per row, one scale block); step i
-  // covers 16q + 8i .. +8; h follows the same order.
-  const uint8_t* qlo = st + g * f4::DN_QSTRIDE + warp * 32 + q * 8;
-  const uint8_t* qhi = qlo + 8 * f4::DN_QSTRIDE;
-  const uint8_t* sfb = st + f4::RS * f4::DN_QSTRIDE;
-  const uint32_t slo = *reinterpret_cast<const uint32_t*>(sfb + g * f4::DN_SFROW + warp * 4);
-  const uint32_t shi = *reinterpret_cast<const uint32_t*>(sfb + (g + 8) * f4::DN_SFROW + warp * 4);
-  const uint32_t scl = e4m3_bcast_f16x2((slo >> (8 * q)) & 0xffu);
-  const uint32_t sch = e4m3_bcast_f16x2((shi >> (8 * q)) & 0xffu);
-  const uint2 clo = *reinterpret_cast<const uint2*>(qlo);
-  const uint2 chi = *reinterpret_cast<const uint2*>(qhi);
-  const uint8_t* hs = st + f4::DN_WBYTES + (warp * 64 + q * 16) * 4;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
-    e2m1x8_to_f16x2(i ? clo.y : clo.x, l0, l1, l2, l3);
-    e2m1x8_to_f16x2(i ? chi.y : chi.x, h0, h1, h2, h3);
-    l0 = hmul2(l0, scl); l1 = hmul2(l1, scl); l2 = hmul2(l2, scl); l3 = hmul2(l3, scl);
-    h0 = hmul2(h0, sch); h1 = hmul2(h1, sch); h2 = hmul2(h2, sch); h3 = hmul2(h3, sch);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int slot = nt * 8 + g;
-      // h (fp32) = hi + lo with both parts f16: two MMAs keep ~22 bits of h.
-      uint32_t b[4] = {0u, 0u, 0u, 0u}, r[4] = {0u, 0u, 0u, 0u};
-      if (slot < n) {
-        const float4 v0 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + i * 32);
-        const float4 v1 = *reinterpret_cast<const float4*>(hs + slot * f4::HSTRIDE + i * 32 + 16);
-        split_f16x2(v0.x, v0.y, b[0], r[0]);
-        split_f16x2(v0.z, v0.w, b[1], r[1]);
-        split_f16x2(v1.x, v1.y, b[2], r[2]);
-        split_f16x2(v1.z, v1.w, b[3], r[3]);
-      }
-      mma_f16(acc[nt], l0, h0, l1, h1, b[0], b[1]);
-      mma_f16(acc[nt], l2, h2, l3, h3, b[2], b[3]);
-      mma_f16(acc[nt], l0, h0, l1, h1, r[0], r[1]);
-      mma_f16(acc[nt], l2, h2, l3, h3, r[2], r[3]);
-    }
-  }
-  float* rw = red + warp * f4::RS * GROUP_MAX;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int col = nt * 8 + 2 * q;
-    rw[g * GROUP_MAX + col] = acc[nt][0];
-    rw[g * GROUP_MAX + col + 1] = acc[nt][1];
-    rw[(g + 8) * GROUP_MAX + col] = acc[nt][2];
-    rw[(g + 8) * GROUP_MAX + col + 1] = acc[nt][3];
-  }
-  named_sync(1, f4::CWARPS * 32);
-  const float ts = expert < E ? __ldg(a.w.w2_ts + expert) : __ldg(a.w.ws2_ts + (expert - E));
-  for (int i = threadIdx.x; i < f4::RS * n; i += f4::CWARPS * 32) {
-    const int r = i & (f4::RS - 1), j = i >> 4;
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < f4::CWARPS; ++w) s += red[(w * f4::RS + r) * GROUP_MAX + j];
-    const int t = pair_tok[pair0 + j];
-    const float wt = pair_w[pair0 + j];
-    acc_s[t * f4::RS + r] += wt * (s * ts);
-  }
-  named_sync(1, f4::CWARPS * 32);
-}
-
-__device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, const int4* groups,
-                                           int n_groups,
-                                           int r0) {
-  int it = 0;
-  for (int gi = 0; gi < n_groups; ++gi) {
-    const int4 grp = groups[gi];
-    if (!acquire_stage(p, it)) break;
-    const int slot = it % p.nstage;
-    const int n = grp.z;
-    const bool routed = grp.x < E;
-    const int e = routed ? grp.x : grp.x - E;
-    const uint8_t* qb = (routed ? a.w.w2_q : a.w.ws2_q) + ((size_t)e * H + r0) * f4::DN_QROW;
-    const uint8_t* sb = (routed ? a.w.w2_sf : a.w.ws2_sf) + ((size_t)e * H + r0) * f4::DN_SFROW;
-    mbar_expect_tx(full_bar(p, slot), f4::RS * (f4::DN_QROW + f4::DN_SFROW) + n * f4::HROW);
-    const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
-    bulk_g2s(dst, qb, f4::RS * f4::DN_QROW, full_bar(p, slot));
-    bulk_g2s(dst + f4::RS * f4::DN_QSTRIDE, sb, f4::RS * f4::DN_SFROW, full_bar(p, slot));
-    bulk_g2s(dst + f4::DN_WBYTES, a.ws.h + (size_t)grp.y * I, n * f4::HROW, full_bar(p, slot));
     ++it;
   }
   drain(p, it);
@@ -468,56 +347,6 @@ __global__ void __launch_bounds__(f4::THREADS, 1) gateup_nvfp4_kernel(ExpertArgs
   }
 }
 
-__global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_abort;
-  const int B = a.B;
-  const int nstage = f4::dn_nstages(B), stage = f4::dn_stage(B);
-  float* red = reinterpret_cast<float*>(smem + nstage * stage);
-  float* acc = red + f4::DN_RED;
-  MetaSmem& meta = *reinterpret_cast<MetaSmem*>(acc + B * f4::RS);
-  float* pair_w_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(pair_w_s + MAX_B * SLOTS);
-  Pipe p;
-  init_pipe(p, smem, stage, nstage, bars, f4::DN_MAX_STAGES, &s_abort, a.ws.hdr);
-  for (int i = threadIdx.x; i < B * f4::RS; i += blockDim.x) acc[i] = 0.f;
-  __syncthreads();
-  const int r0 = blockIdx.x * f4::RS;
-  p.deadline = wait_deadline(a.ws.hdr);
-  pdl_wait();     // h, the group table and the pairs come from the preceding kernels
-  if ((threadIdx.x >> 5) == f4::CWARPS) {
-    named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
-    if ((threadIdx.x & 31) == 0) dn_produce(p, a, meta.groups, meta.n_groups, r0);
-    return;
-  }
-  fill_meta(a, false, meta, pair_w_s, nullptr, nullptr);
-  pdl_trigger();
-  named_sync(2, ALL_THREADS);
-  const int n_groups = meta.n_groups;
-  bool ok = true;
-  for (int gi = 0; gi < n_groups; ++gi) {
-    const int4 grp = meta.groups[gi];
-    const int slot = gi % nstage;
-    if (ok) ok = wait_full(p, slot, (uint32_t)(gi / nstage) & 1u);
-    const uint8_t* st = p.stages + slot * stage;
-    const int n = ok ? grp.z : 0;
-    switch ((grp.z + 7) >> 3) {  // uniform across the consumer warps
-      case 1: dn_group<1>(a, meta.pair_tok, pair_w_s, st, red, acc, grp.x, grp.y, n); break;
-      case 2: dn_group<2>(a, meta.pair_tok, pair_w_s, st, red, acc, grp.x, grp.y, n); break;
-      default: dn_group<3>(a, meta.pair_tok, pair_w_s, st, red, acc, grp.x, grp.y, n); break;
-    }
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar(p, slot));
-  }
-  named_sync(1, f4::CWARPS * 32);
-  if (!ok) return;
-  for (int i = threadIdx.x; i < B * f4::RS; i += f4::CWARPS * 32) {
-    const int t = i / f4::RS, r = i % f4::RS;
-    const size_t o = (size_t)t * H + r0 + r;
-    a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + acc[i]);
-  }
-}
-
 cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -539,7 +368,267 @@ cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int nu
   return cudaLaunchKernelEx(&cfg, gateup_nvfp4_kernel, a);
 }
 
-cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream) {
+// ---------------------------------------------------------------- down
+//
+// Split-combine: a unit is (group, block of 128 output rows): the block's
+// 128 x 256 code bytes (32 KiB) and 128 x 32 scale bytes (4 KiB), plus the
+// group's f16 h rows, arrive as three bulk copies into one stage; the units
+// are split evenly over one CTA per SM, so each SM streams a few large units
+// instead of walking every group.  Warp w computes rows 16w .. 16w + 15 of the
+// block over all 512 columns: lane (g, q) takes, at MMA step s, columns
+// 128q + 4s .. +3 of rows g and g + 8, so its 64 code bytes and 8 scale bytes
+// per row are loaded once per unit and dequantised from registers; h follows
+// the same order (h_off_nv).  Each warp writes its rows' partial sums,
+// already weighted by the routing weight and the tensor scale, to y[pair][row];
+// the CTA that finishes the last unit of a row block (an atomic ticket after
+// a fence) adds, for each token, its SLOTS rows of y in ascending pair order to
+// the residual -- a fixed order, so the result is bitwise reproducible.
+
+namespace f4 {
+constexpr int DN_RB = 128;                      // output rows per unit
+constexpr int DN_UNITS = H / DN_RB;             // units per group
+constexpr int DN_QROW = I / 2;                  // code bytes per row
+constexpr int DN_SFROW = I / 16;                // scale bytes per row
+constexpr int DN_QB = DN_RB * DN_QROW;          // 32 KiB
+constexpr int DN_SB = DN_RB * DN_SFROW;         // 4 KiB
+constexpr int DN_HROW = I * 2;                  // one f16 h row
+constexpr int DN_MAX_STAGES = 4;
+constexpr int SMEM_CAP = 232448 - 1024;
+static_assert(DN_UNITS <= 16, "one ticket per row block in the header");
+__host__ __device__ inline int dn_stage(int B) {
+  return DN_QB + DN_SB + (B < GROUP_MAX ? B : GROUP_MAX) * DN_HROW;
+}
+__host__ __device__ inline int dn_fixed() {
+  return (int)sizeof(MetaSmem) + MAX_B * SLOTS * 4 + 2 * DN_MAX_STAGES * 8;
+}
+__host__ __device__ inline int dn_nstages(int B) {
+  const int n = (SMEM_CAP - dn_fixed()) / dn_stage(B);
+  return n > DN_MAX_STAGES ? DN_MAX_STAGES : n;
+}
+__host__ __device__ inline int dn_smem(int B) { return dn_nstages(B) * dn_stage(B) + dn_fixed(); }
+static_assert(DN_QB + DN_SB + GROUP_MAX * DN_HROW + (int)sizeof(MetaSmem) + MAX_B * SLOTS * 4 +
+                      2 * DN_MAX_STAGES * 8 <=
+                  SMEM_CAP,
+              "a stage of the largest group fits");
+}  // namespace f4
+
+namespace {
+
+// Barrier over the consumer warps that also ANDs a flag across them (every
+// consumer thread arrives, so the decision is the same in every warp).
+__device__ __forceinline__ bool consumers_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(f4::CWARPS * 32)
+      : "memory");
+  return r != 0;
+}
+
+// One warp, one unit: rows 16w .. 16w + 15 of the block, NT token tiles.
+// Lane (g, q): rows g and g + 8, columns 128q + 4s .. +3 at step s.
+template <int NT>
+__device__ __forceinline__ void dn_unit(const ExpertArgs& a, const uint8_t* st, int expert,
+                                        int pair0, int n, int rb, float* y) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const uint8_t* cr = st + (16 * warp + g) * f4::DN_QROW + 64 * q;
+  uint4 c0[4], c1[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    c0[i] = *reinterpret_cast<const uint4*>(cr + 16 * i);
+    c1[i] = *reinterpret_cast<const uint4*>(cr + 8 * f4::DN_QROW + 16 * i);
+  }
+  const uint8_t* sr = st + f4::DN_QB + (16 * warp + g) * f4::DN_SFROW + 8 * q;
+  const uint2 s0 = *reinterpret_cast<const uint2*>(sr);
+  const uint2 s1 = *reinterpret_cast<const uint2*>(sr + 8 * f4::DN_SFROW);
+  // Token columns past n read token 0's h row: their sums are never used.
+  const uint8_t* hrow[NT];
+  int hx[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int slot = nt * 8 + g < n ? nt * 8 + g : 0;
+    hrow[nt] = st + f4::DN_QB + f4::DN_SB + slot * f4::DN_HROW;
+    hx[nt] = (pair0 + slot) & 1;
+  }
+  float acc[NT][2][4];  // [tile][even, odd step][fragment]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) acc[nt][c][0] = acc[nt][c][1] = acc[nt][c][2] = acc[nt][c][3] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {  // two MMA steps: one code word and one h block per row
+    const uint4 v0 = c0[j >> 2], v1 = c1[j >> 2];
+    const uint32_t w0 = (j & 3) == 0 ? v0.x : (j & 3) == 1 ? v0.y : (j & 3) == 2 ? v0.z : v0.w;
+    const uint32_t w1 = (j & 3) == 0 ? v1.x : (j & 3) == 1 ? v1.y : (j & 3) == 2 ? v1.z : v1.w;
+    // 16 columns per scale: steps 4m .. 4m + 3 share scale m
+    const uint32_t sb0 = (j >> 1) < 4 ? s0.x : s0.y, sb1 = (j >> 1) < 4 ? s1.x : s1.y;
+    const int sh = 8 * ((j >> 1) & 3);
+    const uint32_t sc0 = e4m3_bcast_f16x2((sb0 >> sh) & 0xffu);
+    const uint32_t sc1 = e4m3_bcast_f16x2((sb1 >> sh) & 0xffu);
+    uint32_t l0, l1, l2, l3, u0, u1, u2, u3;
+    e2m1x8_to_f16x2(w0, l0, l1, l2, l3);
+    e2m1x8_to_f16x2(w1, u0, u1, u2, u3);
+    l0 = hmul2(l0, sc0); l1 = hmul2(l1, sc0); l2 = hmul2(l2, sc0); l3 = hmul2(l3, sc0);
+    u0 = hmul2(u0, sc1); u1 = hmul2(u1, sc1); u2 = hmul2(u2, sc1); u3 = hmul2(u3, sc1);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      // block 16q + j of the token's row (h_off_nv)
+      const uint4 hb = *reinterpret_cast<const uint4*>(hrow[nt] + ((j ^ hx[nt]) * 64) + q * 16);
+      mma_f16(acc[nt][0], l0, u0, l1, u1, hb.x, hb.y);
+      mma_f16(acc[nt][1], l2, u2, l3, u3, hb.z, hb.w);
+    }
+  }
+  const float ts = expert < E ? __ldg(a.w.w2_ts + expert) : __ldg(a.w.ws2_ts + (expert - E));
+  const int row = rb * f4::DN_RB + 16 * warp + g;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = nt * 8 + 2 * q + e;
+      if (col < n) {
+        const int pr = pair0 + col;
+        const float wt = __ldg(a.ws.pair_w + pr) * ts;
+        const float d0 = acc[nt][0][e] + acc[nt][1][e];
+        const float d1 = acc[nt][0][2 + e] + acc[nt][1][2 + e];
+        y[(size_t)pr * H + row] = wt * d0;
+        y[(size_t)pr * H + row + 8] = wt * d1;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, const int4* groups,
+                                           int u_begin, int u_end) {
+  int it = 0;
+  for (int u = u_begin; u < u_end; ++u) {
+    const int4 grp = groups[u / f4::DN_UNITS];
+    const int rb = u % f4::DN_UNITS;
+    const bool routed = grp.x < E;
+    const int e = routed ? grp.x : grp.x - E;
+    const size_t row0 = (size_t)e * H + (size_t)rb * f4::DN_RB;
+    const uint8_t* qb = (routed ? a.w.w2_q : a.w.ws2_q) + row0 * f4::DN_QROW;
+    const uint8_t* sb = (routed ? a.w.w2_sf : a.w.ws2_sf) + row0 * f4::DN_SFROW;
+    if (!acquire_stage(p, it)) break;
+    const int slot = it % p.nstage;
+    mbar_expect_tx(full_bar(p, slot), f4::DN_QB + f4::DN_SB + grp.z * f4::DN_HROW);
+    const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
+    bulk_g2s(dst, qb, f4::DN_QB, full_bar(p, slot));
+    bulk_g2s(dst + f4::DN_QB, sb, f4::DN_SB, full_bar(p, slot));
+    bulk_g2s(dst + f4::DN_QB + f4::DN_SB,
+             reinterpret_cast<const uint8_t*>(a.ws.h) + (size_t)grp.y * f4::DN_HROW,
+             grp.z * f4::DN_HROW, full_bar(p, slot));
+    ++it;
+  }
+  drain(p, it);
+}
+
+// out rows of block rb for every token: residual + the token's SLOTS y rows,
+// in ascending pair order.
+__device__ __forceinline__ void dn_combine(const ExpertArgs& a, const float* y, const int* tokp,
+                                           int rb) {
+  const int B = a.B;
+  for (int i = threadIdx.x; i < B * f4::DN_RB; i += f4::CWARPS * 32) {
+    const int t = i / f4::DN_RB;
+    const int r = rb * f4::DN_RB + i % f4::DN_RB;
+    float yv[SLOTS];
+#pragma unroll
+    for (int j = 0; j < SLOTS; ++j) yv[j] = __ldcg(y + (size_t)tokp[t * SLOTS + j] * H + r);
+    float v = 0.f;
+#pragma unroll
+    for (int j = 0; j < SLOTS; ++j) v += yv[j];
+    const size_t o = (size_t)t * H + r;
+    a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + v);
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_abort;
+  __shared__ int s_last;
+  const int B = a.B;
+  const int nstage = f4::dn_nstages(B), stage = f4::dn_stage(B);
+  MetaSmem& meta = *reinterpret_cast<MetaSmem*>(smem + nstage * stage);
+  int* tokp = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tokp + MAX_B * SLOTS);
+  Pipe p;
+  init_pipe(p, smem, stage, nstage, bars, f4::DN_MAX_STAGES, &s_abort, a.ws.hdr);
+  __syncthreads();
+  p.deadline = wait_deadline(a.ws.hdr);
+  pdl_wait();  // h, the group table and the pairs come from the preceding kernels
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == f4::CWARPS) {
+    named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
+    if (lane == 0) {
+      const int n_units = meta.n_groups * f4::DN_UNITS;
+      dn_produce(p, a, meta.groups, (int)((long long)blockIdx.x * n_units / gridDim.x),
+                 (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x));
+    }
+    return;
+  }
+  fill_meta(a, false, meta, nullptr, nullptr, nullptr);
+  // Each token's SLOTS pairs in ascending order (warp per token, ballots).
+  for (int t = warp; t < B; t += f4::CWARPS) {
+    int cnt = 0;
+    for (int base = 0; base < B * SLOTS; base += 32) {
+      const int pr = base + lane;
+      const bool mine = pr < B * SLOTS && meta.pair_tok[pr] == t;
+      const uint32_t m = __ballot_sync(0xffffffffu, mine);
+      const int k = cnt + __popc(m & ((1u << lane) - 1u));
+      if (mine && k < SLOTS) tokp[t * SLOTS + k] = pr;
+      cnt += __popc(m);
+    }
+    if (cnt != SLOTS) {  // every token has SLOTS pairs; without them nothing is combined
+      if (lane == 0) set_error(a.ws.hdr, DEV_BAD_ROUTING);
+      *p.abort_flag = 1;
+    }
+  }
+  pdl_trigger();
+  named_sync(2, ALL_THREADS);
+  float* y = ws_y(a.ws, B);
+  const int n_units = meta.n_groups * f4::DN_UNITS;
+  const int u_begin = (int)((long long)blockIdx.x * n_units / gridDim.x);
+  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
+  bool ok = true;
+  int it = 0;
+  for (int u = u_begin; u < u_end; ++u, ++it) {
+    const int4 grp = meta.groups[u / f4::DN_UNITS];
+    const int rb = u % f4::DN_UNITS;
+    const int slot = it % p.nstage;
+    if (ok) ok = wait_full(p, slot, (uint32_t)(it / p.nstage) & 1u);
+    if (ok) {
+      const uint8_t* st = p.stages + slot * p.stage_bytes;
+      switch ((grp.z + 7) >> 3) {
+        case 1: dn_unit<1>(a, st, grp.x, grp.y, grp.z, rb, y); break;
+        case 2: dn_unit<2>(a, st, grp.x, grp.y, grp.z, rb, y); break;
+        default: dn_unit<3>(a, st, grp.x, grp.y, grp.z, rb, y); break;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(p, slot));
+    // Publish this unit: after the consumers' barrier one thread fences (the
+    // barrier orders every warp's y stores before it) and takes a ticket.
+    ok = consumers_and(ok && !*p.abort_flag);
+    if (!ok) break;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const uint32_t t = atomicAdd(&a.ws.hdr->rb_done[rb], 1u);
+      s_last = t + 1 == (uint32_t)meta.n_groups;
+      if (s_last) a.ws.hdr->rb_done[rb] = 0;  // every unit of the block has counted: reset for the next call
+    }
+    named_sync(1, f4::CWARPS * 32);
+    if (s_last) {
+      __threadfence();
+      dn_combine(a, y, tokp, rb);
+    }
+    named_sync(1, f4::CWARPS * 32);  // s_last is read before it is rewritten
+  }
+}
+
+cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(down_nvfp4_kernel,
@@ -548,7 +637,7 @@ cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream) {
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(H / f4::RS, 1, 1);
+  cfg.gridDim = dim3(num_sms, 1, 1);
   cfg.blockDim = dim3(f4::THREADS, 1, 1);
   cfg.dynamicSmemBytes = f4::dn_smem(a.B);
   cfg.stream = stream;
