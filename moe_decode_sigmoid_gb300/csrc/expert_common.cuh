@@ -38,6 +38,57 @@ struct LocalSelectSmem {
   float pair_w[LOCAL_SELECT_MAX_B * SLOTS];
 };
 
+// Buckets the batch's (token, slot) pairs by expert for B <= 8 tokens, by the
+// first NTHREADS threads (>= TOPK * B and S * B): with at most 8 tokens every distinct expert forms one
+// group (GROUP_MAX is larger), so thread p ranks pair p directly against all
+// pairs -- its position is the number of pairs with a smaller expert plus
+// those of the same expert from lower tokens -- and one counting barrier
+// gives the number of distinct experts.  The result is the group table and
+// pair order of bucket_cta: routed groups by expert ascending (tokens
+// ascending inside), then the shared expert's group of all tokens.
+template <int NTHREADS>
+__device__ __forceinline__ void bucket_small(int B, const int* idx, const float* w, int* pair_tok,
+                                             float* pair_w, int4* groups, int* n_groups,
+                                             int* opener) {
+  const int tid = threadIdx.x;
+  const int np = B * TOPK;
+  int e = 0, pos = 0, cnt = 0;
+  bool first = false;
+  if (tid < np) {
+    e = idx[tid];
+    int less = 0, before = 0;
+    for (int q = 0; q < np; ++q) {
+      const int eq = idx[q];
+      less += eq < e ? 1 : 0;
+      cnt += eq == e ? 1 : 0;
+      before += (eq == e && q < tid) ? 1 : 0;
+    }
+    pos = less + before;
+    first = before == 0;
+    pair_tok[pos] = tid / TOPK;
+    pair_w[pos] = w[tid];
+    opener[tid] = first ? e : 0x7fffffff;  // experts whose first pair this is
+  }
+  if (tid < S * B) {
+    pair_tok[np + tid] = tid % B;
+    pair_w[np + tid] = 1.0f;
+  }
+  uint32_t n_uniq;
+  asm volatile("{ .reg .pred p; setp.ne.u32 p, %1, 0; bar.red.popc.u32 %0, 1, %2, p; }"
+               : "=r"(n_uniq)
+               : "r"((tid < np && first) ? 1u : 0u), "n"(NTHREADS)
+               : "memory");
+  if (tid < np && first) {
+    int g = 0;
+    for (int q = 0; q < np; ++q) g += opener[q] < e ? 1 : 0;
+    groups[g] = make_int4(e, pos, cnt, 0);
+  }
+  if (tid == 0) {
+    groups[n_uniq] = make_int4(E, np, B, 0);
+    *n_groups = (int)n_uniq + S;
+  }
+}
+
 // Run by the 256 consumer threads after the grid dependency is satisfied.
 // logits_buf: >= LOCAL_SELECT_MAX_B * E floats of shared memory, free here.
 // pair_w: shared array for the pairs' weights, or null if not needed.
@@ -73,15 +124,9 @@ __device__ __forceinline__ void fill_meta(const ExpertArgs& a, bool local, MetaS
       }
     }
     named_sync(1, CONSUMER_THREADS);
-    BucketDst d;
-    d.pair_tok = m.pair_tok;
-    d.pair_w = ls->pair_w;
-    d.groups = m.groups;
-    d.n_groups = &m.n_groups;
-    d.n_uniq = nullptr;
-    BucketOut none = {nullptr, nullptr, nullptr, nullptr};
-    bool bad = false;  // indices come from topk_warp: always valid
-    bucket_cta<1, false>(B, ls->idx, ls->w, d, none, ls->sc, bad, ConsumerSync());
+    // indices come from topk_warp: always valid
+    bucket_small<CONSUMER_THREADS>(B, ls->idx, ls->w, m.pair_tok, ls->pair_w, m.groups,
+                                   &m.n_groups, ls->sc.off);
     named_sync(1, CONSUMER_THREADS);
     if (pair_w)
       for (int i = tid; i < B * SLOTS; i += CONSUMER_THREADS) pair_w[i] = ls->pair_w[i];

@@ -387,56 +387,6 @@ __device__ __forceinline__ void unit_mma(const uint8_t* gs, const uint8_t* us, c
   named_sync(1, fz::CT);  // buf is free again
 }
 
-// Buckets the batch's (token, slot) pairs by expert for B <= 8 tokens, by the
-// 256 consumer threads: with at most 8 tokens every distinct expert forms one
-// group (GROUP_MAX is larger), so thread p ranks pair p directly against all
-// pairs -- its position is the number of pairs with a smaller expert plus
-// those of the same expert from lower tokens -- and one counting barrier
-// gives the number of distinct experts.  The result is the group table and
-// pair order of bucket_cta: routed groups by expert ascending (tokens
-// ascending inside), then the shared expert's group of all tokens.
-__device__ __forceinline__ void bucket_small(int B, const int* idx, const float* w, int* pair_tok,
-                                             float* pair_w, int4* groups, int* n_groups,
-                                             int* opener) {
-  const int tid = threadIdx.x;
-  const int np = B * TOPK;
-  int e = 0, pos = 0, cnt = 0;
-  bool first = false;
-  if (tid < np) {
-    e = idx[tid];
-    int less = 0, before = 0;
-    for (int q = 0; q < np; ++q) {
-      const int eq = idx[q];
-      less += eq < e ? 1 : 0;
-      cnt += eq == e ? 1 : 0;
-      before += (eq == e && q < tid) ? 1 : 0;
-    }
-    pos = less + before;
-    first = before == 0;
-    pair_tok[pos] = tid / TOPK;
-    pair_w[pos] = w[tid];
-    opener[tid] = first ? e : 0x7fffffff;  // experts whose first pair this is
-  }
-  if (tid < S * B) {
-    pair_tok[np + tid] = tid % B;
-    pair_w[np + tid] = 1.0f;
-  }
-  uint32_t n_uniq;
-  asm volatile("{ .reg .pred p; setp.ne.u32 p, %1, 0; bar.red.popc.u32 %0, 1, %2, p; }"
-               : "=r"(n_uniq)
-               : "r"((tid < np && first) ? 1u : 0u), "n"(fz::CT)
-               : "memory");
-  if (tid < np && first) {
-    int g = 0;
-    for (int q = 0; q < np; ++q) g += opener[q] < e ? 1 : 0;
-    groups[g] = make_int4(e, pos, cnt, 0);
-  }
-  if (tid == 0) {
-    groups[n_uniq] = make_int4(E, np, B, 0);
-    *n_groups = (int)n_uniq + S;
-  }
-}
-
 // ---- producer side (lane 0 of the producer warp) -----------------------------
 
 struct Prod {
@@ -479,13 +429,14 @@ __device__ __forceinline__ bool post_gateup(Prod& p, const uint16_t* base, const
   if (!take_slot(p, sa)) return false;
   p.desc[sa] = d;
   mbar_expect_tx(p.full0 + 8u * sa, fz::SLOT);
-  bulk_g2s(p.stages_addr + sa * fz::SLOT, base + (size_t)(d.blk * 8) * H, fz::SLOT, p.full0 + 8u * sa);
+  bulk_g2s_stream(p.stages_addr + sa * fz::SLOT, base + (size_t)(d.blk * 8) * H, fz::SLOT,
+                  p.full0 + 8u * sa);
   if (!take_slot(p, sb)) return false;  // the END posted next takes the up half's place
   Item du = d;
   du.kind = fz::IT_UP;
   p.desc[sb] = du;
   mbar_expect_tx(p.full0 + 8u * sb, fz::SLOT);
-  bulk_g2s(p.stages_addr + sb * fz::SLOT, base + (size_t)(I + d.blk * 8) * H, fz::SLOT,
+  bulk_g2s_stream(p.stages_addr + sb * fz::SLOT, base + (size_t)(I + d.blk * 8) * H, fz::SLOT,
            p.full0 + 8u * sb);
   return true;
 }
@@ -606,7 +557,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
               if (!(ok = take_slot(p, sl))) break;
               p.desc[sl] = d;
               mbar_expect_tx(p.full0 + 8u * sl, dn::WBYTES + d.n * dn::HROW);
-              bulk_g2s(p.stages_addr + sl * fz::SLOT, wd, dn::WBYTES, p.full0 + 8u * sl);
+              bulk_g2s_stream(p.stages_addr + sl * fz::SLOT, wd, dn::WBYTES, p.full0 + 8u * sl);
               bulk_g2s(p.stages_addr + sl * fz::SLOT + dn::WBYTES, hr, d.n * dn::HROW,
                        p.full0 + 8u * sl);
               kw = kh + 1;
@@ -666,7 +617,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
           if (!(ok = take_slot(p, sl))) break;
           p.desc[sl] = d;
           mbar_expect_tx(p.full0 + 8u * sl, dn::WBYTES + d.n * dn::HROW);
-          bulk_g2s(p.stages_addr + sl * fz::SLOT, wd, dn::WBYTES, p.full0 + 8u * sl);
+          bulk_g2s_stream(p.stages_addr + sl * fz::SLOT, wd, dn::WBYTES, p.full0 + 8u * sl);
           dslot[kw % fz::NS] = sl;
           ++kw;
           continue;
@@ -852,8 +803,8 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
         }
       }
       named_sync(1, fz::CT);
-      bucket_small(B, s_sel.idx, s_sel.w, s_pair_tok, s_pair_w, s_groups, &s_ngroups,
-                   s_sel.sc.off);
+      bucket_small<fz::CT>(B, s_sel.idx, s_sel.w, s_pair_tok, s_pair_w, s_groups, &s_ngroups,
+                           s_sel.sc.off);
       named_sync(1, fz::CT);
       if (tid == 0) mbar_arrive(sel_bar);
       release_slot(empty0 + 8u * slot);

@@ -233,8 +233,8 @@ __device__ __forceinline__ bool issue_unit(const GuCtx& c, const uint16_t* base,
   }
   mbar_expect_tx(full_bar(c, slot), gu::STAGE_BYTES);
   const uint32_t dst = c.stages_addr + slot * gu::STAGE_BYTES;
-  bulk_g2s(dst, base + (size_t)(blk * 8) * H, 8 * gu::ROW_BYTES, full_bar(c, slot));
-  bulk_g2s(dst + 8 * gu::ROW_BYTES, base + (size_t)(I + blk * 8) * H, 8 * gu::ROW_BYTES,
+  bulk_g2s_stream(dst, base + (size_t)(blk * 8) * H, 8 * gu::ROW_BYTES, full_bar(c, slot));
+  bulk_g2s_stream(dst + 8 * gu::ROW_BYTES, base + (size_t)(I + blk * 8) * H, 8 * gu::ROW_BYTES,
            full_bar(c, slot));
   ++it;
   return true;

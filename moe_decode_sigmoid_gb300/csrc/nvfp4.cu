@@ -40,7 +40,11 @@ constexpr int GU_QSTRIDE = GU_QROW;                  // 8 rows = one contiguous 
 constexpr int GU_SFROW = H / 16;                     // 128 scale bytes per row
 constexpr int GU_STAGE = 16 * GU_QSTRIDE + 16 * GU_SFROW;  // 18,432
 constexpr int GU_NSTAGE = 10;
-constexpr int GU_RED = CWARPS * 16 * GROUP_MAX;
+// A round takes up to GU_UB(NT) units of one group at once; their partial
+// tiles [unit][warp][16 rows][NT * 8 tokens] share one reduction.
+__host__ __device__ constexpr int gu_ub(int nt) { return nt == 1 ? 4 : nt == 2 ? 2 : 1; }
+constexpr int GU_RED = 4 * CWARPS * 16 * 8;  // = 2 * CWARPS * 16 * 16 >= CWARPS * 16 * 24
+static_assert(GU_RED >= 2 * CWARPS * 16 * 16 && GU_RED >= CWARPS * 16 * GROUP_MAX, "rounds fit");
 // The reduction buffer doubles as the logits buffer of the local selection.
 constexpr int GU_BUF = GU_RED * 4 > LOCAL_SELECT_MAX_B * E * 4 ? GU_RED * 4 : LOCAL_SELECT_MAX_B * E * 4;
 constexpr size_t GU_SMEM =
@@ -166,11 +170,17 @@ __device__ __forceinline__ void init_pipe(Pipe& p, uint8_t* smem, int stage_byte
 
 // ---------------------------------------------------------------- gate/up
 
+// Units [u0, u1) of one group with n tokens, NT = ceil(n / 8), taken UB at a
+// time: the warps compute their K-slice of every unit of the round (the
+// units' dequantisation and MMAs interleave), then one reduction round sums
+// the 8 warps' partial tiles of all of them.
 template <int NT>
 __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, const int* pair_tok,
                                            float* red, int u0,
                                            int u1, int expert, int pair0, int n, int& it,
                                            bool& ok) {
+  constexpr int UB = f4::gu_ub(NT);
+  constexpr int NC = NT * 8;  // token columns of a partial tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   named_sync(1, f4::CWARPS * 32);  // the previous segment is done with `red`
@@ -198,78 +208,96 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, c
   }
   const float* ts = expert < E ? a.w.w13_ts + 2 * expert : a.w.ws13_ts + 2 * (expert - E);
   const float ts_g = __ldg(ts), ts_u = __ldg(ts + 1);
-  for (int u = u0; u < u1; ++u) {
-    const int blk = u & (f4::UNITS - 1);
-    float acc[NT][4];
+  for (int u = u0; u < u1; u += UB) {
+    const int ub = u1 - u < UB ? u1 - u : UB;
+    float acc[UB][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    const int slot = it % p.nstage;
-    if (ok) ok = wait_full(p, slot, (uint32_t)(it / p.nstage) & 1u);
+    for (int k = 0; k < UB; ++k)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[k][nt][0] = acc[k][nt][1] = acc[k][nt][2] = acc[k][nt][3] = 0.f;
+    const uint8_t* st[UB];
+#pragma unroll
+    for (int k = 0; k < UB; ++k) {
+      const int slot = (it + k) % p.nstage;
+      if (k < ub && ok) ok = wait_full(p, slot, (uint32_t)((it + k) / p.nstage) & 1u);
+      st[k] = p.stages + slot * p.stage_bytes;
+    }
     if (ok) {
-      const uint8_t* st = p.stages + slot * p.stage_bytes;
-      const uint8_t* qlo = st + g * f4::GU_QSTRIDE + warp * 128 + q * 16;
-      const uint8_t* qhi = qlo + 8 * f4::GU_QSTRIDE;
-      const uint8_t* sfb = st + 16 * f4::GU_QSTRIDE;
-      const uint4 slo = *reinterpret_cast<const uint4*>(sfb + g * f4::GU_SFROW + warp * 16);
-      const uint4 shi = *reinterpret_cast<const uint4*>(sfb + (g + 8) * f4::GU_SFROW + warp * 16);
       const bool qh = (q >> 1) != 0;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        const uint4 clo = *reinterpret_cast<const uint4*>(qlo + m * 64);
-        const uint4 chi = *reinterpret_cast<const uint4*>(qhi + m * 64);
-        const uint32_t cl[4] = {clo.x, clo.y, clo.z, clo.w};
-        const uint32_t ch[4] = {chi.x, chi.y, chi.z, chi.w};
-        // block of step (m, i) = 8m + 2q + i/2 within the warp's 16 blocks:
-        // scale word 2m + q/2
-        const uint32_t wl = m ? (qh ? slo.w : slo.z) : (qh ? slo.y : slo.x);
-        const uint32_t wh = m ? (qh ? shi.w : shi.z) : (qh ? shi.y : shi.x);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int sh_bits = 8 * (2 * (q & 1) + (i >> 1));
-          const uint32_t scl = e4m3_bcast_f16x2((wl >> sh_bits) & 0xffu);
-          const uint32_t sch = e4m3_bcast_f16x2((wh >> sh_bits) & 0xffu);
-          uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
-          e2m1x8_to_f16x2(cl[i], l0, l1, l2, l3);
-          e2m1x8_to_f16x2(ch[i], h0, h1, h2, h3);
-          l0 = hmul2(l0, scl); l1 = hmul2(l1, scl); l2 = hmul2(l2, scl); l3 = hmul2(l3, scl);
-          h0 = hmul2(h0, sch); h1 = hmul2(h1, sch); h2 = hmul2(h2, sch); h3 = hmul2(h3, sch);
+        for (int k = 0; k < UB; ++k) {
+          if (k >= ub) continue;
+          const uint8_t* qlo = st[k] + g * f4::GU_QSTRIDE + warp * 128 + q * 16;
+          const uint8_t* qhi = qlo + 8 * f4::GU_QSTRIDE;
+          const uint8_t* sfb = st[k] + 16 * f4::GU_QSTRIDE;
+          const uint4 slo = *reinterpret_cast<const uint4*>(sfb + g * f4::GU_SFROW + warp * 16);
+          const uint4 shi = *reinterpret_cast<const uint4*>(sfb + (g + 8) * f4::GU_SFROW + warp * 16);
+          const uint4 clo = *reinterpret_cast<const uint4*>(qlo + m * 64);
+          const uint4 chi = *reinterpret_cast<const uint4*>(qhi + m * 64);
+          const uint32_t cl[4] = {clo.x, clo.y, clo.z, clo.w};
+          const uint32_t ch[4] = {chi.x, chi.y, chi.z, chi.w};
+          // block of step (m, i) = 8m + 2q + i/2 within the warp's 16 blocks:
+          // scale word 2m + q/2
+          const uint32_t wl = m ? (qh ? slo.w : slo.z) : (qh ? slo.y : slo.x);
+          const uint32_t wh = m ? (qh ? shi.w : shi.z) : (qh ? shi.y : shi.x);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint4 b = bfr[nt][m][i];
-            mma_f16(acc[nt], l0, h0, l1, h1, b.x, b.y);
-            mma_f16(acc[nt], l2, h2, l3, h3, b.z, b.w);
+          for (int i = 0; i < 4; ++i) {
+            const int sh_bits = 8 * (2 * (q & 1) + (i >> 1));
+            const uint32_t scl = e4m3_bcast_f16x2((wl >> sh_bits) & 0xffu);
+            const uint32_t sch = e4m3_bcast_f16x2((wh >> sh_bits) & 0xffu);
+            uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+            e2m1x8_to_f16x2(cl[i], l0, l1, l2, l3);
+            e2m1x8_to_f16x2(ch[i], h0, h1, h2, h3);
+            l0 = hmul2(l0, scl); l1 = hmul2(l1, scl); l2 = hmul2(l2, scl); l3 = hmul2(l3, scl);
+            h0 = hmul2(h0, sch); h1 = hmul2(h1, sch); h2 = hmul2(h2, sch); h3 = hmul2(h3, sch);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint4 b = bfr[nt][m][i];
+              mma_f16(acc[k][nt], l0, h0, l1, h1, b.x, b.y);
+              mma_f16(acc[k][nt], l2, h2, l3, h3, b.z, b.w);
+            }
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar(p, slot));
-    ++it;
-    float* rw = red + warp * 16 * GROUP_MAX;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int col = nt * 8 + 2 * q;
-      rw[g * GROUP_MAX + col] = acc[nt][0];
-      rw[g * GROUP_MAX + col + 1] = acc[nt][1];
-      rw[(g + 8) * GROUP_MAX + col] = acc[nt][2];
-      rw[(g + 8) * GROUP_MAX + col + 1] = acc[nt][3];
+    for (int k = 0; k < UB; ++k)
+      if (k < ub && lane == 0) mbar_arrive(empty_bar(p, (it + k) % p.nstage));
+    it += ub;
+#pragma unroll
+    for (int k = 0; k < UB; ++k) {
+      float* rw = red + ((k * f4::CWARPS + warp) * 16) * NC;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int col = nt * 8 + 2 * q;
+        rw[g * NC + col] = acc[k][nt][0];
+        rw[g * NC + col + 1] = acc[k][nt][1];
+        rw[(g + 8) * NC + col] = acc[k][nt][2];
+        rw[(g + 8) * NC + col + 1] = acc[k][nt][3];
+      }
     }
     named_sync(1, f4::CWARPS * 32);
     {
-      // thread (token slot j, row r): a token's 8 rows are 8 adjacent lanes,
-      // which store its split h block together
-      static_assert(f4::CWARPS * 32 / 8 >= GROUP_MAX, "one 8-lane group per token slot");
-      const int j = threadIdx.x >> 3;
+      // 8 adjacent lanes = the 8 rows of one (unit k, token j): they store the
+      // token's h block together
+      static_assert(f4::CWARPS * 32 / 8 >= UB * NC, "one 8-lane group per (unit, token)");
+      const int G = threadIdx.x >> 3;
       const int r = threadIdx.x & 7;
-      const int jr = j < n ? j : 0;
+      const int k = G / NC, j = G % NC;
+      const bool valid = k < ub && j < n;
+      const int kr = valid ? k : 0, jr = valid ? j : 0;
       float gs = 0.f, us = 0.f;
 #pragma unroll
       for (int w = 0; w < f4::CWARPS; ++w) {
-        gs += red[(w * 16 + r) * GROUP_MAX + jr];
-        us += red[(w * 16 + r + 8) * GROUP_MAX + jr];
+        gs += red[((kr * f4::CWARPS + w) * 16 + r) * NC + jr];
+        us += red[((kr * f4::CWARPS + w) * 16 + r + 8) * NC + jr];
       }
+      const int blk = (u + kr) & (f4::UNITS - 1);
       store_h_block8_nv(a.ws.h, (size_t)(pair0 + jr), blk, silu_mul(gs * ts_g, us * ts_u),
-                        j < n && ok);
+                        valid && ok);
     }
     named_sync(1, f4::CWARPS * 32);
   }
@@ -290,12 +318,15 @@ __device__ __forceinline__ void gu_produce(const Pipe& p, const ExpertArgs& a, c
     const int slot = it % p.nstage;
     mbar_expect_tx(full_bar(p, slot), 16 * f4::GU_QROW + 16 * f4::GU_SFROW);
     const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
-    bulk_g2s(dst, qb + (size_t)(blk * 8) * f4::GU_QROW, 8 * f4::GU_QROW, full_bar(p, slot));
-    bulk_g2s(dst + 8 * f4::GU_QSTRIDE, qb + (size_t)(I + blk * 8) * f4::GU_QROW, 8 * f4::GU_QROW,
+    bulk_g2s_stream(dst, qb + (size_t)(blk * 8) * f4::GU_QROW, 8 * f4::GU_QROW, full_bar(p, slot));
+    bulk_g2s_stream(dst + 8 * f4::GU_QSTRIDE, qb + (size_t)(I + blk * 8) * f4::GU_QROW,
+                    8 * f4::GU_QROW,
              full_bar(p, slot));
-    bulk_g2s(dst + 16 * f4::GU_QSTRIDE, sb + (size_t)(blk * 8) * f4::GU_SFROW, 8 * f4::GU_SFROW,
+    bulk_g2s_stream(dst + 16 * f4::GU_QSTRIDE, sb + (size_t)(blk * 8) * f4::GU_SFROW,
+                    8 * f4::GU_SFROW,
              full_bar(p, slot));
-    bulk_g2s(dst + 16 * f4::GU_QSTRIDE + 8 * f4::GU_SFROW, sb + (size_t)(I + blk * 8) * f4::GU_SFROW,
+    bulk_g2s_stream(dst + 16 * f4::GU_QSTRIDE + 8 * f4::GU_SFROW,
+                    sb + (size_t)(I + blk * 8) * f4::GU_SFROW,
              8 * f4::GU_SFROW, full_bar(p, slot));
     ++it;
   }
@@ -514,8 +545,8 @@ __device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, c
     const int slot = it % p.nstage;
     mbar_expect_tx(full_bar(p, slot), f4::DN_QB + f4::DN_SB + grp.z * f4::DN_HROW);
     const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
-    bulk_g2s(dst, qb, f4::DN_QB, full_bar(p, slot));
-    bulk_g2s(dst + f4::DN_QB, sb, f4::DN_SB, full_bar(p, slot));
+    bulk_g2s_stream(dst, qb, f4::DN_QB, full_bar(p, slot));
+    bulk_g2s_stream(dst + f4::DN_QB, sb, f4::DN_SB, full_bar(p, slot));
     bulk_g2s(dst + f4::DN_QB + f4::DN_SB,
              reinterpret_cast<const uint8_t*>(a.ws.h) + (size_t)grp.y * f4::DN_HROW,
              grp.z * f4::DN_HROW, full_bar(p, slot));
