@@ -337,3 +337,21 @@ def test_nvfp4_zero_input_residual_bitwise(m, layer, nv_layer, ws):
     out, idx, _ = run_nvfp4(m, W, nv, torch.zeros_like(res), res, None, ws)
     assert torch.equal(idx.cpu(), torch.arange(K, dtype=torch.int32).repeat(3, 1))
     assert torch.equal(out.view(torch.int16), res.view(torch.int16))
+
+
+@pytest.mark.parametrize("B", [8, 40])
+def test_nvfp4_repeat_and_token_permutation_bitwise(m, layer, nv_layer, ws, B):
+    """The NVFP4 down kernel adds each token's partial sums in a fixed order
+    (ascending pair index, i.e. expert order), so a repeat gives the same bits
+    and permuting the tokens permutes the output bits."""
+    W, _ = layer
+    nv, _ = nv_layer
+    x, res = fs.tokens(4200 + B, B, device="cuda")
+    out1, idx1, _ = run_nvfp4(m, W, nv, x, res, None, ws)
+    out2, idx2, _ = run_nvfp4(m, W, nv, x, res, None, ws)
+    assert torch.equal(idx1, idx2)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    perm = torch.randperm(B, generator=torch.Generator().manual_seed(7)).cuda()
+    out_p, idx_p, _ = run_nvfp4(m, W, nv, x[perm].contiguous(), res[perm].contiguous(), None, ws)
+    assert torch.equal(idx_p, idx1[perm])
+    assert torch.equal(out_p.view(torch.int16), out1[perm].view(torch.int16))
