@@ -174,9 +174,6 @@ __device__ __forceinline__ void bulk_g2s_stream(uint32_t dst, const void* src, u
       "l"(src), "r"(bytes), "r"(bar), "l"(l2_evict_first())
       : "memory");
 }
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 // Named barrier over the first `nthreads` threads (multiple of 32).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {

@@ -20,10 +20,6 @@ namespace flint {
 constexpr int CONSUMER_THREADS = 256;
 constexpr int ALL_THREADS = CONSUMER_THREADS + 32;
 
-struct ConsumerSync {
-  __device__ __forceinline__ void operator()() const { named_sync(1, CONSUMER_THREADS); }
-};
-
 struct MetaSmem {
   int4 groups[MAX_GROUPS];
   int pair_tok[MAX_B * SLOTS];
@@ -38,54 +34,108 @@ struct LocalSelectSmem {
   float pair_w[LOCAL_SELECT_MAX_B * SLOTS];
 };
 
-// Buckets the batch's (token, slot) pairs by expert for B <= 8 tokens, by the
-// first NTHREADS threads (>= TOPK * B and S * B): with at most 8 tokens every distinct expert forms one
-// group (GROUP_MAX is larger), so thread p ranks pair p directly against all
-// pairs -- its position is the number of pairs with a smaller expert plus
-// those of the same expert from lower tokens -- and one counting barrier
-// gives the number of distinct experts.  The result is the group table and
+// Buckets the batch's (token, slot) pairs by expert for B <= 8 tokens, by
+// NTHREADS threads (>= LANES * LOCAL_SELECT_MAX_B * TOPK): with at most 8 tokens
+// every distinct expert forms one group (GROUP_MAX is larger), so pair p is
+// ranked directly against all pairs -- its position is the number of pairs
+// with a smaller expert plus those of the same expert from lower tokens --
+// and one counting barrier gives the number of distinct experts.  The result is the group table and
 // pair order of bucket_cta: routed groups by expert ascending (tokens
 // ascending inside), then the shared expert's group of all tokens.
-template <int NTHREADS>
+template <int NTHREADS, int LANES>
 __device__ __forceinline__ void bucket_small(int B, const int* idx, const float* w, int* pair_tok,
                                              float* pair_w, int4* groups, int* n_groups,
                                              int* opener) {
-  const int tid = threadIdx.x;
-  const int np = B * TOPK;
-  int e = 0, pos = 0, cnt = 0;
-  bool first = false;
-  if (tid < np) {
-    e = idx[tid];
-    int less = 0, before = 0;
-    for (int q = 0; q < np; ++q) {
-      const int eq = idx[q];
-      less += eq < e ? 1 : 0;
-      cnt += eq == e ? 1 : 0;
-      before += (eq == e && q < tid) ? 1 : 0;
+  static_assert(LANES == 1 || LANES == 2 || LANES == 4, "lanes per pair divide a warp");
+  static_assert(NTHREADS >= LANES * LOCAL_SELECT_MAX_B * TOPK, "LANES threads per pair");
+  if constexpr (LANES == 1) {
+    const int tid = threadIdx.x;
+    const int np = B * TOPK;
+    int e = 0, pos = 0, cnt = 0;
+    bool first = false;
+    if (tid < np) {
+      e = idx[tid];
+      int less = 0, before = 0;
+      for (int q = 0; q < np; ++q) {
+        const int eq = idx[q];
+        less += eq < e ? 1 : 0;
+        cnt += eq == e ? 1 : 0;
+        before += (eq == e && q < tid) ? 1 : 0;
+      }
+      pos = less + before;
+      first = before == 0;
+      pair_tok[pos] = tid / TOPK;
+      pair_w[pos] = w[tid];
+      opener[tid] = first ? e : 0x7fffffff;  // experts whose first pair this is
     }
-    pos = less + before;
-    first = before == 0;
-    pair_tok[pos] = tid / TOPK;
-    pair_w[pos] = w[tid];
-    opener[tid] = first ? e : 0x7fffffff;  // experts whose first pair this is
-  }
-  if (tid < S * B) {
-    pair_tok[np + tid] = tid % B;
-    pair_w[np + tid] = 1.0f;
-  }
-  uint32_t n_uniq;
-  asm volatile("{ .reg .pred p; setp.ne.u32 p, %1, 0; bar.red.popc.u32 %0, 1, %2, p; }"
-               : "=r"(n_uniq)
-               : "r"((tid < np && first) ? 1u : 0u), "n"(NTHREADS)
-               : "memory");
-  if (tid < np && first) {
+    if (tid < S * B) {
+      pair_tok[np + tid] = tid % B;
+      pair_w[np + tid] = 1.0f;
+    }
+    uint32_t n_uniq;
+    asm volatile("{ .reg .pred p; setp.ne.u32 p, %1, 0; bar.red.popc.u32 %0, 1, %2, p; }"
+                 : "=r"(n_uniq)
+                 : "r"((tid < np && first) ? 1u : 0u), "n"(NTHREADS)
+                 : "memory");
+    if (tid < np && first) {
+      int g = 0;
+      for (int q = 0; q < np; ++q) g += opener[q] < e ? 1 : 0;
+      groups[g] = make_int4(e, pos, cnt, 0);
+    }
+    if (tid == 0) {
+      groups[n_uniq] = make_int4(E, np, B, 0);
+      *n_groups = (int)n_uniq + S;
+    }
+  } else {
+    const int tid = threadIdx.x;
+    const int np = B * TOPK;
+    // LANES adjacent lanes per pair p: each compares against every LANES-th
+    // pair, then shuffles add their counts (fewer serial loads per thread).
+    const int p = tid / LANES, part = tid % LANES;
+    const bool act = p < np;
+    const int e = act ? idx[p] : 0;
+    int less = 0, cnt = 0, before = 0;
+    if (act) {
+      for (int q = part; q < np; q += LANES) {
+        const int eq = idx[q];
+        less += eq < e ? 1 : 0;
+        cnt += eq == e ? 1 : 0;
+        before += (eq == e && q < p) ? 1 : 0;
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < LANES; o <<= 1) {
+      less += __shfl_xor_sync(0xffffffffu, less, o);
+      cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+    }
+    const int pos = less + before;
+    const bool first = act && before == 0;
+    if (act && part == 0) {
+      pair_tok[pos] = p / TOPK;
+      pair_w[pos] = w[p];
+      opener[p] = first ? e : 0x7fffffff;  // experts whose first pair this is
+    }
+    if (tid < S * B) {
+      pair_tok[np + tid] = tid % B;
+      pair_w[np + tid] = 1.0f;
+    }
+    uint32_t n_uniq;
+    asm volatile("{ .reg .pred p; setp.ne.u32 p, %1, 0; bar.red.popc.u32 %0, 1, %2, p; }"
+                 : "=r"(n_uniq)
+                 : "r"((first && part == 0) ? 1u : 0u), "n"(NTHREADS)
+                 : "memory");
     int g = 0;
-    for (int q = 0; q < np; ++q) g += opener[q] < e ? 1 : 0;
-    groups[g] = make_int4(e, pos, cnt, 0);
-  }
-  if (tid == 0) {
-    groups[n_uniq] = make_int4(E, np, B, 0);
-    *n_groups = (int)n_uniq + S;
+    if (first) {
+      for (int q = part; q < np; q += LANES) g += opener[q] < e ? 1 : 0;
+    }
+#pragma unroll
+    for (int o = 1; o < LANES; o <<= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+    if (first && part == 0) groups[g] = make_int4(e, pos, cnt, 0);
+    if (tid == 0) {
+      groups[n_uniq] = make_int4(E, np, B, 0);
+      *n_groups = (int)n_uniq + S;
+    }
   }
 }
 
@@ -125,8 +175,9 @@ __device__ __forceinline__ void fill_meta(const ExpertArgs& a, bool local, MetaS
     }
     named_sync(1, CONSUMER_THREADS);
     // indices come from topk_warp: always valid
-    bucket_small<CONSUMER_THREADS>(B, ls->idx, ls->w, m.pair_tok, ls->pair_w, m.groups,
-                                   &m.n_groups, ls->sc.off);
+    // one lane per pair here: these kernels measured faster with it
+    bucket_small<CONSUMER_THREADS, 1>(B, ls->idx, ls->w, m.pair_tok, ls->pair_w, m.groups,
+                                      &m.n_groups, ls->sc.off);
     named_sync(1, CONSUMER_THREADS);
     if (pair_w)
       for (int i = tid; i < B * SLOTS; i += CONSUMER_THREADS) pair_w[i] = ls->pair_w[i];

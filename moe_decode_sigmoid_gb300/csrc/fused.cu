@@ -803,8 +803,8 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
         }
       }
       named_sync(1, fz::CT);
-      bucket_small<fz::CT>(B, s_sel.idx, s_sel.w, s_pair_tok, s_pair_w, s_groups, &s_ngroups,
-                           s_sel.sc.off);
+      bucket_small<fz::CT, 4>(B, s_sel.idx, s_sel.w, s_pair_tok, s_pair_w, s_groups, &s_ngroups,
+                              s_sel.sc.off);
       named_sync(1, fz::CT);
       if (tid == 0) mbar_arrive(sel_bar);
       release_slot(empty0 + 8u * slot);
