@@ -355,3 +355,24 @@ def test_nvfp4_repeat_and_token_permutation_bitwise(m, layer, nv_layer, ws, B):
     out_p, idx_p, _ = run_nvfp4(m, W, nv, x[perm].contiguous(), res[perm].contiguous(), None, ws)
     assert torch.equal(idx_p, idx1[perm])
     assert torch.equal(out_p.view(torch.int16), out1[perm].view(torch.int16))
+
+
+@pytest.mark.parametrize("B", [1, 3, 8, 13, 32])
+def test_workspace_sized_for_the_batch(m, layer, nv_layer, ws, B):
+    """A workspace sized for exactly B tokens gives the same bits as a larger
+    one on both paths (the offsets of every array but h and the per-pair
+    partials do not depend on the size), and the BF16 output matches the
+    oracle (seed 2001 at batch 3 is the smoke case)."""
+    W, host = layer
+    nv, _ = nv_layer
+    x, res = fs.tokens(2001 if B == 3 else 2300 + B, B, device="cuda")
+    tight = m.new_workspace(B)
+    assert tight.numel() == m.flint_moe_workspace_bytes(B) < ws.numel()
+    out_t, idx_t, w_t = run_decode(m, W, x, res, None, tight)
+    out_l, idx_l, _ = run_decode(m, W, x, res, None, ws)
+    assert torch.equal(idx_t, idx_l)
+    assert torch.equal(out_t.view(torch.int16), out_l.view(torch.int16))
+    check_layer(host, x, res, None, out_t, idx_t, w_t)
+    nv_t, _, _ = run_nvfp4(m, W, nv, x, res, None, tight)
+    nv_l, _, _ = run_nvfp4(m, W, nv, x, res, None, ws)
+    assert torch.equal(nv_t.view(torch.int16), nv_l.view(torch.int16))
