@@ -376,3 +376,26 @@ def test_workspace_sized_for_the_batch(m, layer, nv_layer, ws, B):
     nv_t, _, _ = run_nvfp4(m, W, nv, x, res, None, tight)
     nv_l, _, _ = run_nvfp4(m, W, nv, x, res, None, ws)
     assert torch.equal(nv_t.view(torch.int16), nv_l.view(torch.int16))
+
+
+@pytest.mark.parametrize("B", [3, 8, 32])
+def test_stage_calls_match_oracle(m, layer, ws, B):
+    """route -> gate/up -> down through their own entry points computes the
+    layer (the three-kernel path, also at batches the decode call fuses); above
+    8 tokens the decode call runs the same kernels, so the bits agree."""
+    W, host = layer
+    x, res = fs.tokens(2400 + B, B, device="cuda")
+    bias = fs.logit_offsets(1003, device="cuda") if B > 8 else None
+    idx = torch.full((B, K), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((B, K), dtype=torch.float32, device="cuda")
+    out = torch.empty_like(res)
+    m.flint_moe_route(x, W["wr"], bias, idx, w, ws)
+    m.flint_moe_gateup_bf16(x, W["w13"], W["ws13"], ws)
+    m.flint_moe_down_bf16(res, W["w2"], W["ws2"], out, ws)
+    torch.cuda.synchronize()
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_OK
+    check_layer(host, x, res, bias, out, idx, w)
+    if B > 8:
+        out_d, idx_d, _ = run_decode(m, W, x, res, bias, ws)
+        assert torch.equal(idx_d, idx)
+        assert torch.equal(out_d.view(torch.int16), out.view(torch.int16))
