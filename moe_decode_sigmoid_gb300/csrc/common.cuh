@@ -3,6 +3,7 @@
 // the CUDA runtime headers.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -98,6 +99,22 @@ inline Ws ws_view(void* base) {
   w.groups = reinterpret_cast<int4*>(b + WsLayout::groups);
   w.h = reinterpret_cast<float*>(b + WsLayout::h);
   return w;
+}
+
+// ---- host: launch attributes -------------------------------------------------
+// A kernel's dynamic shared-memory limit belongs to the current device's
+// context, so it is set once per device (bit d of `done` for device d < 64;
+// devices beyond that set it on every call), safely from any host thread.
+template <class Kernel>
+inline cudaError_t set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t{1} << dev) : uint64_t{0};
+  if (bit != 0u && (done.load(std::memory_order_acquire) & bit) != 0u) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 // ---- small device helpers ---------------------------------------------------

@@ -446,13 +446,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 // Launch (PDL-chained after the gate/up kernel); `maps` from F::make_maps.
 template <class F>
 cudaError_t launch_down_ring(const ExpertArgs& a, const typename F::Maps& maps, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(down_ring_kernel<F>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_CAP);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t es = set_smem_limit_once(down_ring_kernel<F>, SMEM_CAP, smem_set);
+  if (es != cudaSuccess) return es;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(H / RS, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);

@@ -890,13 +890,9 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
 
 cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                               int num_sms) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(moe_small_bf16_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fz::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t es = set_smem_limit_once(moe_small_bf16_kernel, (int)fz::SMEM, smem_set);
+  if (es != cudaSuccess) return es;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms, 1, 1);
   cfg.blockDim = dim3(fz::THREADS, 1, 1);

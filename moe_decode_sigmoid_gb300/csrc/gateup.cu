@@ -119,13 +119,9 @@ __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs 
 }
 
 cudaError_t launch_gateup_bf16(const ExpertArgs& a, cudaStream_t stream, int num_sms) {
-  static bool attr_set = false;  // idempotent; racing first calls set the same value
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gateup_bf16_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t es = set_smem_limit_once(gateup_bf16_kernel, (int)gu::SMEM, smem_set);
+  if (es != cudaSuccess) return es;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms, 1, 1);
   cfg.blockDim = dim3(gu::THREADS, 1, 1);

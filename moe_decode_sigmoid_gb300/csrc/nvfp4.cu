@@ -379,13 +379,9 @@ __global__ void __launch_bounds__(f4::THREADS, 1) gateup_nvfp4_kernel(ExpertArgs
 }
 
 cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gateup_nvfp4_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f4::GU_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t es = set_smem_limit_once(gateup_nvfp4_kernel, (int)f4::GU_SMEM, smem_set);
+  if (es != cudaSuccess) return es;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms, 1, 1);
   cfg.blockDim = dim3(f4::THREADS, 1, 1);
@@ -660,13 +656,9 @@ __global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a
 }
 
 cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(down_nvfp4_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, f4::SMEM_CAP);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  const cudaError_t es = set_smem_limit_once(down_nvfp4_kernel, f4::SMEM_CAP, smem_set);
+  if (es != cudaSuccess) return es;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms, 1, 1);
   cfg.blockDim = dim3(f4::THREADS, 1, 1);
