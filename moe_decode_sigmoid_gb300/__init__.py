@@ -6,6 +6,12 @@ lib/libflint_moe.so; every step of the layer runs in that library's CUDA
 kernels.  There is no fallback: if the library is missing or fails to load,
 importing the binding's functions raises.
 
+The C entry points take bare pointers, so the binding checks what they cannot:
+each tensor's dtype, shape (as include/flint_moe.h lays it out), contiguity and
+device (all on the activations' CUDA device), raising FlintError with
+FLINT_ERR_INVALID_ARG before anything is launched.  A plain int is taken as a
+raw device pointer the caller vouches for.
+
 Build the library with `python -m moe_decode_sigmoid_gb300.build` (or
 `__graft_entry__.build()`).
 """
@@ -119,6 +125,55 @@ def _ptr(t):
     return t.data_ptr()
 
 
+_BF16, _F32, _I32T, _U8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+
+
+def _bad(where, name, what, t):
+    got = ("%s %s%s on %s" % (t.dtype, tuple(t.shape), "" if t.is_contiguous() else
+                              " (not contiguous)", t.device)
+           if isinstance(t, torch.Tensor) else type(t).__name__)
+    raise FlintError(FLINT_ERR_INVALID_ARG, "%s: %s must be %s, got %s" % (where, name, what, got))
+
+
+def _arg(where, name, t, dtype, shape, dev, optional=False, min_numel=None):
+    """Device pointer of t after checking it against the layout the C call
+    assumes: dtype, exact shape (or at least min_numel elements), contiguous,
+    on device dev."""
+    if t is None:
+        if optional:
+            return None
+        raise FlintError(FLINT_ERR_INVALID_ARG, "%s: %s is required" % (where, name))
+    if isinstance(t, int):
+        return t
+    if not (isinstance(t, torch.Tensor) and t.dtype == dtype and t.device == dev and
+            (t.shape == shape if shape is not None else t.numel() >= min_numel) and
+            t.is_contiguous()):
+        what = "a contiguous %s tensor %s on %s" % (
+            dtype, shape if shape is not None else "of >= %d elements" % min_numel, dev)
+        _bad(where, name, what, t)
+    return t.data_ptr()
+
+
+def _batch(where, name, t, hidden):
+    """(batch, device) of a [batch, hidden] bf16 activation tensor on a GPU."""
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dim() == 2 and t.shape[1] == hidden):
+        _bad(where, name, "a [batch, %d] tensor on a CUDA device" % hidden, t)
+    return t.shape[0], t.device
+
+
+def _ws_arg(where, workspace, dev):
+    """(pointer, bytes) of a workspace: a contiguous uint8 tensor on dev."""
+    if isinstance(workspace, torch.Tensor):
+        if not (workspace.dtype == _U8 and workspace.dim() == 1 and workspace.device == dev and
+                workspace.is_contiguous()):
+            _bad(where, "workspace", "a contiguous 1-D uint8 tensor on %s" % dev, workspace)
+    return _ws(workspace)
+
+
+def _d(dims):
+    return FULL_DIMS if dims is None else dims
+
+
 def _stream(stream):
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -159,29 +214,56 @@ def _ws(workspace):
 
 def flint_moe_route(x, w_router, logit_bias, topk_idx, topk_w, workspace, stream=None,
                     dims: Dims | None = None):
-    wp, wb = _ws(workspace)
-    _check(lib().flint_moe_route(_dims(dims), x.shape[0], _ptr(x), _ptr(w_router), _ptr(logit_bias),
-                                 _ptr(topk_idx), _ptr(topk_w), wp, wb, _stream(stream)),
-           "flint_moe_route")
+    f, d = "flint_moe_route", _d(dims)
+    B, dev = _batch(f, "x", x, d.hidden)
+    args = (_arg(f, "x", x, _BF16, (B, d.hidden), dev),
+            _arg(f, "w_router", w_router, _BF16, (d.n_experts, d.hidden), dev),
+            _arg(f, "logit_bias", logit_bias, _F32, (d.n_experts,), dev, optional=True),
+            _arg(f, "topk_idx", topk_idx, _I32T, (B, d.top_k), dev),
+            _arg(f, "topk_w", topk_w, _F32, (B, d.top_k), dev))
+    wp, wb = _ws_arg(f, workspace, dev)
+    _check(lib().flint_moe_route(_dims(dims), B, *args, wp, wb, _stream(stream)), f)
 
 
 def flint_moe_bucket(topk_idx, uniq, offsets, pairs, n_uniq, workspace, stream=None,
                      dims: Dims | None = None):
-    wp, wb = _ws(workspace)
-    _check(lib().flint_moe_bucket(_dims(dims), topk_idx.shape[0], _ptr(topk_idx), _ptr(uniq),
-                                  _ptr(offsets), _ptr(pairs), _ptr(n_uniq), wp, wb,
-                                  _stream(stream)), "flint_moe_bucket")
+    f, d = "flint_moe_bucket", _d(dims)
+    B, dev = _batch(f, "topk_idx", topk_idx, d.top_k)
+    args = (_arg(f, "topk_idx", topk_idx, _I32T, (B, d.top_k), dev),
+            _arg(f, "uniq", uniq, _I32T, None, dev, min_numel=d.n_experts),
+            _arg(f, "offsets", offsets, _I32T, None, dev, min_numel=d.n_experts + 1),
+            _arg(f, "pairs", pairs, _I32T, None, dev, min_numel=B * d.top_k),
+            _arg(f, "n_uniq", n_uniq, _I32T, None, dev, min_numel=1))
+    wp, wb = _ws_arg(f, workspace, dev)
+    _check(lib().flint_moe_bucket(_dims(dims), B, *args, wp, wb, _stream(stream)), f)
+
+
+def _layer_args(f, d, B, dev, x, residual, w_router, logit_bias, w13, w2, ws13, ws2, out,
+                topk_idx_out, topk_w_out):
+    """Checked pointers of the BF16 layer's arguments, in the C call's order."""
+    H, E, K, I, S = d.hidden, d.n_experts, d.top_k, d.inter, d.n_shared
+    return (_arg(f, "x", x, _BF16, (B, H), dev),
+            _arg(f, "residual", residual, _BF16, (B, H), dev),
+            _arg(f, "w_router", w_router, _BF16, (E, H), dev),
+            _arg(f, "logit_bias", logit_bias, _F32, (E,), dev, optional=True),
+            _arg(f, "w13", w13, _BF16, (E, 2 * I, H), dev),
+            _arg(f, "w2", w2, _BF16, (E, H, I), dev),
+            _arg(f, "ws13", ws13, _BF16, (S, 2 * I, H), dev),
+            _arg(f, "ws2", ws2, _BF16, (S, H, I), dev),
+            _arg(f, "out", out, _BF16, (B, H), dev),
+            _arg(f, "topk_idx_out", topk_idx_out, _I32T, (B, K), dev, optional=True),
+            _arg(f, "topk_w_out", topk_w_out, _F32, (B, K), dev, optional=True))
 
 
 def flint_moe_decode_bf16(x, residual, w_router, logit_bias, w13, w2, ws13, ws2, out, workspace,
                           topk_idx_out=None, topk_w_out=None, stream=None,
                           dims: Dims | None = None):
-    wp, wb = _ws(workspace)
-    _check(lib().flint_moe_decode_bf16(_dims(dims), x.shape[0], _ptr(x), _ptr(residual),
-                                       _ptr(w_router), _ptr(logit_bias), _ptr(w13), _ptr(w2),
-                                       _ptr(ws13), _ptr(ws2), _ptr(out), _ptr(topk_idx_out),
-                                       _ptr(topk_w_out), wp, wb, _stream(stream)),
-           "flint_moe_decode_bf16")
+    f, d = "flint_moe_decode_bf16", _d(dims)
+    B, dev = _batch(f, "x", x, d.hidden)
+    args = _layer_args(f, d, B, dev, x, residual, w_router, logit_bias, w13, w2, ws13, ws2, out,
+                       topk_idx_out, topk_w_out)
+    wp, wb = _ws_arg(f, workspace, dev)
+    _check(lib().flint_moe_decode_bf16(_dims(dims), B, *args, wp, wb, _stream(stream)), f)
 
 
 def flint_moe_decode_bf16_noalloc(x, residual, w_router, logit_bias, w13, w2, ws13, ws2, out,
@@ -190,24 +272,34 @@ def flint_moe_decode_bf16_noalloc(x, residual, w_router, logit_bias, w13, w2, ws
     """flint_moe_decode_bf16 without a workspace (the library's static device
     array instead; batch <= NOALLOC_MAX_BATCH).  For callers that cannot
     allocate device memory; calls whose GPU work overlaps race."""
-    _check(lib().flint_moe_decode_bf16_noalloc(
-        _dims(dims), x.shape[0], _ptr(x), _ptr(residual), _ptr(w_router), _ptr(logit_bias),
-        _ptr(w13), _ptr(w2), _ptr(ws13), _ptr(ws2), _ptr(out), _ptr(topk_idx_out),
-        _ptr(topk_w_out), _ptr(device_status_out), _stream(stream)),
-        "flint_moe_decode_bf16_noalloc")
+    f, d = "flint_moe_decode_bf16_noalloc", _d(dims)
+    B, dev = _batch(f, "x", x, d.hidden)
+    args = _layer_args(f, d, B, dev, x, residual, w_router, logit_bias, w13, w2, ws13, ws2, out,
+                       topk_idx_out, topk_w_out)
+    st = _arg(f, "device_status_out", device_status_out, _I32T, None, dev, optional=True,
+              min_numel=1)
+    _check(lib().flint_moe_decode_bf16_noalloc(_dims(dims), B, *args, st, _stream(stream)), f)
 
 
 def flint_moe_gateup_bf16(x, w13, ws13, workspace, stream=None, dims: Dims | None = None):
-    wp, wb = _ws(workspace)
-    _check(lib().flint_moe_gateup_bf16(_dims(dims), x.shape[0], _ptr(x), _ptr(w13), _ptr(ws13),
-                                       wp, wb, _stream(stream)), "flint_moe_gateup_bf16")
+    f, d = "flint_moe_gateup_bf16", _d(dims)
+    B, dev = _batch(f, "x", x, d.hidden)
+    args = (_arg(f, "x", x, _BF16, (B, d.hidden), dev),
+            _arg(f, "w13", w13, _BF16, (d.n_experts, 2 * d.inter, d.hidden), dev),
+            _arg(f, "ws13", ws13, _BF16, (d.n_shared, 2 * d.inter, d.hidden), dev))
+    wp, wb = _ws_arg(f, workspace, dev)
+    _check(lib().flint_moe_gateup_bf16(_dims(dims), B, *args, wp, wb, _stream(stream)), f)
 
 
 def flint_moe_down_bf16(residual, w2, ws2, out, workspace, stream=None, dims: Dims | None = None):
-    wp, wb = _ws(workspace)
-    _check(lib().flint_moe_down_bf16(_dims(dims), residual.shape[0], _ptr(residual), _ptr(w2),
-                                     _ptr(ws2), _ptr(out), wp, wb, _stream(stream)),
-           "flint_moe_down_bf16")
+    f, d = "flint_moe_down_bf16", _d(dims)
+    B, dev = _batch(f, "residual", residual, d.hidden)
+    args = (_arg(f, "residual", residual, _BF16, (B, d.hidden), dev),
+            _arg(f, "w2", w2, _BF16, (d.n_experts, d.hidden, d.inter), dev),
+            _arg(f, "ws2", ws2, _BF16, (d.n_shared, d.hidden, d.inter), dev),
+            _arg(f, "out", out, _BF16, (B, d.hidden), dev))
+    wp, wb = _ws_arg(f, workspace, dev)
+    _check(lib().flint_moe_down_bf16(_dims(dims), B, *args, wp, wb, _stream(stream)), f)
 
 
 NVFP4_KEYS = ("w13_q", "w13_sf", "w13_ts", "w2_q", "w2_sf", "w2_ts",
@@ -218,16 +310,36 @@ def flint_moe_decode_nvfp4_w4a16(x, residual, w_router, logit_bias, nv: dict, ou
                                  topk_idx_out=None, topk_w_out=None, stream=None,
                                  dims: Dims | None = None):
     """nv holds the twelve packed tensors named in NVFP4_KEYS."""
-    wp, wb = _ws(workspace)
-    _check(lib().flint_moe_decode_nvfp4_w4a16(
-        _dims(dims), x.shape[0], _ptr(x), _ptr(residual), _ptr(w_router), _ptr(logit_bias),
-        *[_ptr(nv[k]) for k in NVFP4_KEYS], _ptr(out), _ptr(topk_idx_out), _ptr(topk_w_out),
-        wp, wb, _stream(stream)), "flint_moe_decode_nvfp4_w4a16")
+    f, d = "flint_moe_decode_nvfp4_w4a16", _d(dims)
+    H, E, K, I, S = d.hidden, d.n_experts, d.top_k, d.inter, d.n_shared
+    B, dev = _batch(f, "x", x, H)
+    shapes = {}
+    for pre, n in (("w", E), ("ws", S)):
+        shapes[pre + "13_q"] = (_U8, (n, 2 * I, H // 2))
+        shapes[pre + "13_sf"] = (_U8, (n, 2 * I, H // 16))
+        shapes[pre + "13_ts"] = (_F32, (n, 2))
+        shapes[pre + "2_q"] = (_U8, (n, H, I // 2))
+        shapes[pre + "2_sf"] = (_U8, (n, H, I // 16))
+        shapes[pre + "2_ts"] = (_F32, (n,))
+    packed = [_arg(f, k, nv.get(k), shapes[k][0], shapes[k][1], dev) for k in NVFP4_KEYS]
+    args = (_arg(f, "x", x, _BF16, (B, H), dev),
+            _arg(f, "residual", residual, _BF16, (B, H), dev),
+            _arg(f, "w_router", w_router, _BF16, (E, H), dev),
+            _arg(f, "logit_bias", logit_bias, _F32, (E,), dev, optional=True),
+            *packed,
+            _arg(f, "out", out, _BF16, (B, H), dev),
+            _arg(f, "topk_idx_out", topk_idx_out, _I32T, (B, K), dev, optional=True),
+            _arg(f, "topk_w_out", topk_w_out, _F32, (B, K), dev, optional=True))
+    wp, wb = _ws_arg(f, workspace, dev)
+    _check(lib().flint_moe_decode_nvfp4_w4a16(_dims(dims), B, *args, wp, wb, _stream(stream)), f)
 
 
 def flint_moe_rmsnorm_bf16(inp, out, eps: float = 1e-6, stream=None, dims: Dims | None = None):
-    _check(lib().flint_moe_rmsnorm_bf16(_dims(dims), inp.shape[0], _ptr(inp), _ptr(out),
-                                        float(eps), _stream(stream)), "flint_moe_rmsnorm_bf16")
+    f, d = "flint_moe_rmsnorm_bf16", _d(dims)
+    B, dev = _batch(f, "inp", inp, d.hidden)
+    args = (_arg(f, "inp", inp, _BF16, (B, d.hidden), dev),
+            _arg(f, "out", out, _BF16, (B, d.hidden), dev))
+    _check(lib().flint_moe_rmsnorm_bf16(_dims(dims), B, *args, float(eps), _stream(stream)), f)
 
 
 # ---------------------------------------------------------------- conveniences

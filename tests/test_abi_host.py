@@ -108,3 +108,38 @@ def test_route_bucket_rmsnorm_reject_bad_arguments(L):
     assert L.flint_moe_workspace_init(None, wsb, 0, None) == m.FLINT_ERR_WORKSPACE
     assert L.flint_moe_workspace_init(WS, 64, 0, None) == m.FLINT_ERR_WORKSPACE
     assert L.flint_moe_debug_arm_stall(None, wsb, None) == m.FLINT_ERR_WORKSPACE
+
+
+def test_binding_checks_what_the_c_call_cannot():
+    """The C calls take bare pointers: the binding rejects a tensor whose dtype,
+    shape, layout or device differs from the header's layout, naming it, before
+    anything is launched (a plain int passes as a raw device pointer)."""
+    import torch
+    cpu = torch.device("cpu")
+    f = "flint_moe_decode_bf16"
+    x = torch.zeros((4, 2048), dtype=torch.bfloat16)
+    assert m._arg(f, "x", x, torch.bfloat16, (4, 2048), cpu) == x.data_ptr()
+    assert m._arg(f, "bias", None, torch.float32, (256,), cpu, optional=True) is None
+    assert m._arg(f, "w", 0x1000, torch.bfloat16, (1,), cpu) == 0x1000
+    bad = {
+        "dtype": x.float(),
+        "shape": torch.zeros((4, 1024), dtype=torch.bfloat16),
+        "layout": torch.zeros((2048, 4), dtype=torch.bfloat16).t(),
+        "device": x.to("meta"),
+        "type": [0] * 8,
+    }
+    for why, t in bad.items():
+        with pytest.raises(m.FlintError) as e:
+            m._arg(f, "x", t, torch.bfloat16, (4, 2048), cpu)
+        assert e.value.status == m.FLINT_ERR_INVALID_ARG and "x must be" in str(e.value), why
+    with pytest.raises(m.FlintError):
+        m._arg(f, "w13", None, torch.bfloat16, (256, 1024, 2048), cpu)
+    with pytest.raises(m.FlintError) as e:
+        m._arg(f, "pairs", torch.zeros(5, dtype=torch.int32), torch.int32, None, cpu, min_numel=6)
+    assert "pairs" in str(e.value)
+    # activations must live on a GPU: a host tensor is refused before the call
+    with pytest.raises(m.FlintError) as e:
+        m.flint_moe_decode_bf16(x, x, None, None, None, None, None, None, x, None)
+    assert "CUDA" in str(e.value)
+    with pytest.raises(m.FlintError):
+        m.flint_moe_rmsnorm_bf16(torch.zeros((4, 100), dtype=torch.bfloat16), x)
