@@ -1,7 +1,7 @@
 """fp64 CPU oracle of the Flint decode MoE layer -- TEST INFRASTRUCTURE ONLY.
 
-Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may
-import this package.  It wraps the plain C implementation in
+Only tests/, __graft_entry__.smoke() and bench.py's CPU legs (the
+cpu_baseline record and the `--impl reference` arm) may import this package.  It wraps the plain C implementation in
 oracle/flint_moe_ref.c (built by oracle/build.py) and takes host tensors
 (torch CPU tensors or NumPy arrays).  It shares nothing with the CUDA path.
 
