@@ -28,32 +28,37 @@ class _Dims(ctypes.Structure):
                 ("n_shared", ctypes.c_int32)]
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Loads an oracle library build (the tests' mutation check loads builds of
+    altered copies of the source this way)."""
+    L = ctypes.CDLL(path)
+    L.ref_e2m1.restype = ctypes.c_double
+    L.ref_e2m1.argtypes = [ctypes.c_uint8]
+    L.ref_e4m3.restype = ctypes.c_double
+    L.ref_e4m3.argtypes = [ctypes.c_uint8]
+    L.ref_route.restype = _I
+    L.ref_route.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P]
+    L.ref_moe_bf16.restype = _I
+    L.ref_moe_bf16.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P]
+    L.ref_moe_bf16_given_routing.restype = _I
+    L.ref_moe_bf16_given_routing.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]
+    L.ref_moe_nvfp4.restype = _I
+    L.ref_moe_nvfp4.argtypes = [_P, _I, _P, _P, _P, _P] + [_P] * 12 + [_I, _P, _P, _P]
+    L.ref_moe_nvfp4_given_routing.restype = _I
+    L.ref_moe_nvfp4_given_routing.argtypes = [_P, _I, _P, _P, _P, _P] + [_P] * 12 + [_I, _P]
+    L.ref_bucket.restype = _I
+    L.ref_bucket.argtypes = [_I, _I, _I, _P, _P, _P, _P]
+    L.ref_rmsnorm.restype = None
+    L.ref_rmsnorm.argtypes = [_I, _I, _P, ctypes.c_double, _P]
+    L.ref_max_threads.restype = _I
+    L.ref_max_threads.argtypes = []
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
-        L = ctypes.CDLL(path)
-        L.ref_e2m1.restype = ctypes.c_double
-        L.ref_e2m1.argtypes = [ctypes.c_uint8]
-        L.ref_e4m3.restype = ctypes.c_double
-        L.ref_e4m3.argtypes = [ctypes.c_uint8]
-        L.ref_route.restype = _I
-        L.ref_route.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P]
-        L.ref_moe_bf16.restype = _I
-        L.ref_moe_bf16.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P]
-        L.ref_moe_bf16_given_routing.restype = _I
-        L.ref_moe_bf16_given_routing.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]
-        L.ref_moe_nvfp4.restype = _I
-        L.ref_moe_nvfp4.argtypes = [_P, _I, _P, _P, _P, _P] + [_P] * 12 + [_I, _P, _P, _P]
-        L.ref_moe_nvfp4_given_routing.restype = _I
-        L.ref_moe_nvfp4_given_routing.argtypes = [_P, _I, _P, _P, _P, _P] + [_P] * 12 + [_I, _P]
-        L.ref_bucket.restype = _I
-        L.ref_bucket.argtypes = [_I, _I, _I, _P, _P, _P, _P]
-        L.ref_rmsnorm.restype = None
-        L.ref_rmsnorm.argtypes = [_I, _I, _P, ctypes.c_double, _P]
-        L.ref_max_threads.restype = _I
-        L.ref_max_threads.argtypes = []
-        _lib = L
+        _lib = load(_build.build())
     return _lib
 
 
