@@ -192,20 +192,28 @@ def flint_moe_workspace_bytes(max_batch: int, dims: Dims | None = None) -> int:
     return int(lib().flint_moe_workspace_bytes(_dims(dims), int(max_batch)))
 
 
+def _ws_only(where, workspace):
+    """(pointer, bytes) of a workspace passed on its own: a contiguous uint8
+    tensor on a CUDA device."""
+    if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda):
+        _bad(where, "workspace", "a contiguous 1-D uint8 tensor on a CUDA device", workspace)
+    return _ws_arg(where, workspace, workspace.device)
+
+
 def flint_moe_workspace_init(workspace: torch.Tensor, wait_limit_ns: int = 0, stream=None):
-    _check(lib().flint_moe_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
-                                          int(wait_limit_ns), _stream(stream)),
+    wp, wb = _ws_only("flint_moe_workspace_init", workspace)
+    _check(lib().flint_moe_workspace_init(wp, wb, int(wait_limit_ns), _stream(stream)),
            "flint_moe_workspace_init")
 
 
 def flint_moe_get_device_status(workspace: torch.Tensor, stream=None) -> int:
-    return int(lib().flint_moe_get_device_status(_ptr(workspace), _stream(stream)))
+    wp, _ = _ws_only("flint_moe_get_device_status", workspace)
+    return int(lib().flint_moe_get_device_status(wp, _stream(stream)))
 
 
 def flint_moe_debug_arm_stall(workspace: torch.Tensor, stream=None):
-    _check(lib().flint_moe_debug_arm_stall(_ptr(workspace),
-                                           workspace.numel() * workspace.element_size(),
-                                           _stream(stream)), "flint_moe_debug_arm_stall")
+    wp, wb = _ws_only("flint_moe_debug_arm_stall", workspace)
+    _check(lib().flint_moe_debug_arm_stall(wp, wb, _stream(stream)), "flint_moe_debug_arm_stall")
 
 
 def _ws(workspace):

@@ -143,3 +143,13 @@ def test_binding_checks_what_the_c_call_cannot():
     assert "CUDA" in str(e.value)
     with pytest.raises(m.FlintError):
         m.flint_moe_rmsnorm_bf16(torch.zeros((4, 100), dtype=torch.bfloat16), x)
+
+
+def test_binding_refuses_a_host_workspace():
+    import torch
+    ws = torch.zeros(m.flint_moe_workspace_bytes(1), dtype=torch.uint8)
+    for call in (m.flint_moe_workspace_init, m.flint_moe_get_device_status,
+                 m.flint_moe_debug_arm_stall):
+        with pytest.raises(m.FlintError) as e:
+            call(ws)
+        assert "workspace must be" in str(e.value) and "CUDA" in str(e.value)
