@@ -91,3 +91,24 @@ def test_peak_is_measured_or_the_stated_fallback():
     assert kind in ("measured", "fallback") and peak > 0
     if kind == "fallback":
         assert peak == bench.FALLBACK_HBM_GBS
+
+
+def test_profile_summaries_name_safe_commands_over_committed_files():
+    """Every ncu command a profile summary gives leaves the GPU clocks alone and
+    runs a program of this repository (the bench or the tests)."""
+    import glob
+    import re
+    cmds = []
+    for path in glob.glob(os.path.join(bench.ROOT, "profiles", "*")):
+        if path.endswith(".json"):
+            cmds += [(path, r["command"]) for r in json.load(open(path)).values()]
+            continue
+        for line in open(path).read().replace("\\\n", " ").splitlines():
+            if line.strip().startswith("ncu "):
+                cmds.append((path, line.strip()))
+    assert len(cmds) >= 5
+    for path, cmd in cmds:
+        assert "--clock-control none" in cmd, (path, cmd)
+        prog = re.search(r"\bpython(?: -m pytest)? (\S+)", cmd)
+        assert prog, (path, cmd)
+        assert os.path.exists(os.path.join(bench.ROOT, prog.group(1))), (path, cmd)
