@@ -155,10 +155,21 @@ def _arg(where, name, t, dtype, shape, dev, optional=False, min_numel=None):
 
 
 def _batch(where, name, t, hidden):
-    """(batch, device) of a [batch, hidden] bf16 activation tensor on a GPU."""
+    """(batch, device) of a [batch, hidden] activation tensor on the current
+    CUDA device (the library launches on, and sizes its grids for, the
+    current device)."""
     if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dim() == 2 and t.shape[1] == hidden):
         _bad(where, name, "a [batch, %d] tensor on a CUDA device" % hidden, t)
+    _on_current_device(where, name, t)
     return t.shape[0], t.device
+
+
+def _on_current_device(where, name, t):
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise FlintError(FLINT_ERR_INVALID_ARG,
+                         "%s: %s is on %s but the current device is cuda:%d (use "
+                         "torch.cuda.device(...) around the call)" % (where, name, t.device, cur))
 
 
 def _ws_arg(where, workspace, dev):
@@ -194,9 +205,10 @@ def flint_moe_workspace_bytes(max_batch: int, dims: Dims | None = None) -> int:
 
 def _ws_only(where, workspace):
     """(pointer, bytes) of a workspace passed on its own: a contiguous uint8
-    tensor on a CUDA device."""
+    tensor on the current CUDA device."""
     if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda):
         _bad(where, "workspace", "a contiguous 1-D uint8 tensor on a CUDA device", workspace)
+    _on_current_device(where, "workspace", workspace)
     return _ws_arg(where, workspace, workspace.device)
 
 

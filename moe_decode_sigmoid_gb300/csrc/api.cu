@@ -66,7 +66,33 @@ bool aliasing_ok(int32_t batch, const void* x, const void* residual, const void*
   return true;
 }
 
+flint_status decode_checks(const flint_moe_dims* dims, int32_t batch, const void* x,
+                           const void* residual, const void* wr, const float* bias, void* out,
+                           int32_t* idx_out, float* w_out, void* ws, size_t ws_bytes) {
+  flint_status st = check_common(dims, batch, ws, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(x) || !req(residual) || !req(wr) || !opt4(bias) || !req(out) || !opt4(idx_out) ||
+      !opt4(w_out))
+    return FLINT_ERR_INVALID_ARG;
+  if (!aliasing_ok(batch, x, residual, out, ws, ws_bytes)) return FLINT_ERR_INVALID_ARG;
+  return FLINT_OK;
+}
+
 }  // namespace
+
+namespace flint {
+flint_status decode_bf16_checks(const flint_moe_dims* dims, int32_t batch, const void* x,
+                                const void* residual, const void* wr, const float* bias,
+                                const void* w13, const void* w2, const void* ws13,
+                                const void* ws2, void* out, int32_t* idx_out, float* w_out,
+                                void* ws, size_t ws_bytes) {
+  const flint_status st =
+      decode_checks(dims, batch, x, residual, wr, bias, out, idx_out, w_out, ws, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(w13) || !req(w2) || !req(ws13) || !req(ws2)) return FLINT_ERR_INVALID_ARG;
+  return FLINT_OK;
+}
+}  // namespace flint
 
 extern "C" {
 
@@ -155,19 +181,6 @@ flint_status flint_moe_bucket(const flint_moe_dims* dims, int32_t batch, const i
   return cuda_status(launch_bucket(w, batch, bo, stream));
 }
 
-static flint_status decode_checks(const flint_moe_dims* dims, int32_t batch, const void* x,
-                                  const void* residual, const void* wr, const float* bias,
-                                  void* out, int32_t* idx_out, float* w_out, void* ws,
-                                  size_t ws_bytes) {
-  flint_status st = check_common(dims, batch, ws, ws_bytes);
-  if (st != FLINT_OK) return st;
-  if (!req(x) || !req(residual) || !req(wr) || !opt4(bias) || !req(out) || !opt4(idx_out) ||
-      !opt4(w_out))
-    return FLINT_ERR_INVALID_ARG;
-  if (!aliasing_ok(batch, x, residual, out, ws, ws_bytes)) return FLINT_ERR_INVALID_ARG;
-  return FLINT_OK;
-}
-
 static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const void* residual,
                               const void* wr, const float* bias, const ExpertW& w, void* out,
                               int32_t* idx_out, float* w_out, void* workspace,
@@ -202,8 +215,8 @@ static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const vo
   a.local_select = r.logits_only;
   a.user_idx = idx_out;
   a.user_w = w_out;
-  if (!nvfp4 && batch <= LOCAL_SELECT_MAX_B)  // one persistent kernel for the whole layer
-    return cuda_status(launch_small_bf16(a, r, stream, sms));
+  if (!nvfp4 && batch <= LOCAL_SELECT_MAX_B && small_bf16_supported(sms))
+    return cuda_status(launch_small_bf16(a, r, stream, sms));  // one persistent kernel
   cudaError_t e = launch_router(r, stream, true);
   if (e != cudaSuccess) return cuda_status(e);
   e = nvfp4 ? launch_gateup_nvfp4(a, stream, sms) : launch_gateup_bf16(a, stream, sms);
@@ -219,11 +232,11 @@ flint_status flint_moe_decode_bf16(const flint_moe_dims* dims, int32_t batch, co
                                    const void* ws2_bf16, void* out_bf16, int32_t* topk_idx_out,
                                    float* topk_w_out, void* workspace, size_t ws_bytes,
                                    cudaStream_t stream) {
-  flint_status st = decode_checks(dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias,
-                                  out_bf16, topk_idx_out, topk_w_out, workspace, ws_bytes);
+  const flint_status st =
+      flint::decode_bf16_checks(dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias,
+                                w13_bf16, w2_bf16, ws13_bf16, ws2_bf16, out_bf16, topk_idx_out,
+                                topk_w_out, workspace, ws_bytes);
   if (st != FLINT_OK) return st;
-  if (!req(w13_bf16) || !req(w2_bf16) || !req(ws13_bf16) || !req(ws2_bf16))
-    return FLINT_ERR_INVALID_ARG;
   ExpertW w = {};
   w.w13 = static_cast<const uint16_t*>(w13_bf16);
   w.w2 = static_cast<const uint16_t*>(w2_bf16);

@@ -33,29 +33,51 @@ constexpr uint32_t DEV_TIMEOUT = 5;
 // ---- workspace layout ------------------------------------------------------
 // [ header | logits fp32 [MAX_B,E] | topk_idx i32 [MAX_B,K] | topk_w f32 [MAX_B,K] |
 //   pair_tok i32 [MAX_B*SLOTS] | pair_w f32 [MAX_B*SLOTS] | groups int4 [MAX_GROUPS] |
+//   tagged logits u64 [SMALL_B,E] | tagged h u64 [SMALL_B*SLOTS, I] |
 //   h [max_batch*SLOTS, I] x 4 bytes | y fp32 [max_batch*SLOTS, H] ]
-// h holds fp32 for the fused kernel; the BF16 gate/up kernel of the
-// three-kernel path stores each element as a bf16 hi + lo pair instead (same
-// 4 bytes, see h_chunk), the NVFP4 one as one f16 (1 KiB rows, h_off_nv).
-// Every array but the last two is sized for MAX_B, so the offsets do not
-// depend on the batch a workspace was sized for; h and y grow with max_batch,
-// and a call with batch B finds y right after the first B * SLOTS h rows.
+// The tagged regions belong to the persistent small-batch kernels: each 8-byte
+// word holds a 32-bit value and the call's tag (see call_tag), so a reader on
+// another SM knows from the word itself whether it was written in this call.
+// h holds the BF16 gate/up kernel's bf16 hi + lo pairs (see h_chunk) or the
+// NVFP4 one's values (h_off_nv) of the three-kernel paths.
+// Every array but the last two is sized for MAX_B (or the small-batch bound),
+// so the offsets do not depend on the batch a workspace was sized for; h and y
+// grow with max_batch, and a call with batch B finds y right after the first
+// B * SLOTS h rows.
+constexpr int SMALL_B = 8;  // largest batch of the persistent small-batch kernels
+// Counters of the small-batch kernels, one per 128-byte line: polled by many
+// SMs and bumped by many more, they must not share an L2 line (a shared line
+// turns the polling into a hot spot that slows every access mapped there).
+struct alignas(128) SyncLine {
+  uint32_t v;
+  uint32_t pad[31];
+};
+constexpr int SYNC_GROUPS = 64;               // completion counters per call
+constexpr int SYNC_UNIT = SYNC_GROUPS;        // next unclaimed unit
+constexpr int SYNC_ARRIVE = SYNC_GROUPS + 1;  // CTAs whose logits are stored
+constexpr int SYNC_LINES = SYNC_GROUPS + 2;
 struct WsHeader {
   uint32_t error;            // DEV_OK or an error code (first writer wins)
+  uint32_t epoch;            // small-batch kernels: calls completed on this workspace
+  uint64_t wait_limit_ns;    // bound of every device-side wait
+  // ---- everything from here on may be cleared between calls ----
   uint32_t tiles_done;       // router: token tiles whose top-k is final
   uint32_t n_groups;         // number of (expert, token range) groups
   uint32_t n_uniq;           // distinct routed experts
-  uint64_t wait_limit_ns;    // bound of every device-side wait
   uint32_t stall_armed;      // test hook: one-shot wait on stall_release
   uint32_t stall_release;    // never written by the library
+  uint32_t pad0[23];
   uint32_t tile_ctas_done[MAX_B / 8];  // router: finished CTAs per token tile
-  uint32_t grid_bar[3];      // fused kernel: logits barrier, (unused), exit count
-  uint32_t unit_next;        // fused kernel: next unclaimed gate/up unit
   uint32_t rb_done[16];      // NVFP4 down: finished units per 128-row block
-  uint32_t pad[4];
-  uint32_t group_done[64];   // fused kernel: finished (unit, warp) parts per group
+  uint32_t pad1[176];
+  // small-batch kernels, by epoch parity: completion counters of the groups,
+  // the unit queue and the logits arrivals
+  SyncLine sync[2][SYNC_LINES];
 };
-static_assert(sizeof(WsHeader) == 512, "header is 512 bytes");
+static_assert(sizeof(WsHeader) == 1024 + 2 * SYNC_LINES * 128, "header layout");
+constexpr size_t WS_HDR_KEEP = 16;  // error, epoch, wait limit: not cleared between calls
+static_assert(offsetof(WsHeader, tiles_done) == WS_HDR_KEEP, "clearable part starts at 16");
+static_assert(offsetof(WsHeader, sync) == 1024, "counter lines start at 1 KiB");
 
 __host__ __device__ constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -66,7 +88,9 @@ struct WsLayout {
   static constexpr size_t pair_tok = align256(topk_w + sizeof(float) * (size_t)MAX_B * TOPK);
   static constexpr size_t pair_w = align256(pair_tok + sizeof(int) * (size_t)MAX_B * SLOTS);
   static constexpr size_t groups = align256(pair_w + sizeof(float) * (size_t)MAX_B * SLOTS);
-  static constexpr size_t h = align256(groups + 16 * (size_t)MAX_GROUPS);
+  static constexpr size_t tlogits = align256(groups + 16 * (size_t)MAX_GROUPS);
+  static constexpr size_t th = align256(tlogits + 8 * (size_t)SMALL_B * E);
+  static constexpr size_t h = align256(th + 8 * (size_t)SMALL_B * SLOTS * I);
   static constexpr size_t total(int max_b) {
     return align256(h + sizeof(float) * (size_t)max_b * SLOTS * (I + H));
   }
@@ -76,6 +100,8 @@ struct WsLayout {
 struct Ws {
   WsHeader* hdr;
   float* logits;
+  uint64_t* tlogits;  // [SMALL_B][E] tagged
+  uint64_t* th;       // [SMALL_B * SLOTS][I] tagged
   int* topk_idx;
   float* topk_w;
   int* pair_tok;
@@ -92,6 +118,8 @@ inline Ws ws_view(void* base) {
   Ws w;
   w.hdr = reinterpret_cast<WsHeader*>(b);
   w.logits = reinterpret_cast<float*>(b + WsLayout::logits);
+  w.tlogits = reinterpret_cast<uint64_t*>(b + WsLayout::tlogits);
+  w.th = reinterpret_cast<uint64_t*>(b + WsLayout::th);
   w.topk_idx = reinterpret_cast<int*>(b + WsLayout::topk_idx);
   w.topk_w = reinterpret_cast<float*>(b + WsLayout::topk_w);
   w.pair_tok = reinterpret_cast<int*>(b + WsLayout::pair_tok);
@@ -190,6 +218,11 @@ __device__ __forceinline__ void bulk_g2s_stream(uint32_t dst, const void* src, u
       " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(l2_evict_first())
       : "memory");
+}
+
+// Bulk prefetch of global memory into L2 (no shared-memory destination).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Named barrier over the first `nthreads` threads (multiple of 32).
@@ -318,5 +351,45 @@ __device__ __forceinline__ uint64_t wait_deadline(const WsHeader* hdr) {
 // silu(g) * u with silu(g) = g / (1 + exp(-g))
 // ("SiLU-and-mul": Flint on Intel Arc Pro B70, "norm.py: Triton kernels that assumed CUDA").
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// ---- tagged words (cross-CTA publication without fences) ----------------------
+// The persistent small-batch kernels publish values to other SMs as 8-byte
+// words {value bits, tag} written by one 64-bit store: a reader that finds the
+// call's tag in a word has that call's value, with no fence between writer and
+// reader (a GPU-scope fence waits for the SM's outstanding memory traffic and
+// costs microseconds while weight copies stream).  The tag is derived from the
+// workspace's call counter (epoch, taken modulo 2^31) and never equals a
+// zero-filled word.  Counters that announce completion are only hints: the
+// reader confirms every word's tag and re-reads the ones that have not landed.
+__host__ __device__ __forceinline__ uint32_t call_tag(uint32_t epoch) {
+  return 0x80000000u | (epoch & 0x7fffffffu);
+}
+__device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag) {
+  const uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_add_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// A tagged word's value if it carries `tag`; otherwise re-reads it from global
+// memory until it does (bounded by `deadline`; false if the wait ran out).
+__device__ __forceinline__ bool settle_tagged(uint64_t& w, const uint64_t* src, uint32_t tag,
+                                              uint64_t deadline) {
+  while ((uint32_t)(w >> 32) != tag) {
+    if (globaltimer_ns() > deadline) return false;
+    w = ld_tagged(src);
+  }
+  return true;
+}
 
 }  // namespace flint

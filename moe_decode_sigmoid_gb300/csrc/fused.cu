@@ -1,44 +1,50 @@
 // fused.cu — the whole BF16 decode MoE layer in one persistent kernel, for
-// batches of at most LOCAL_SELECT_MAX_B (8) tokens: the pages' low-latency
-// path for up to 8 requests, which fuses routing and the expert combine into
-// the neighbouring GEMVs ("Low-Latency Decode Path": vLLM Day-0 Support for
-// Recursive's Flint, "Optimization Strategies").
+// batches of at most SMALL_B (8) tokens: the pages' low-latency path for up to
+// 8 requests, which fuses routing and the expert combine into the neighbouring
+// GEMVs ("Low-Latency Decode Path": vLLM Day-0 Support for Recursive's Flint,
+// "Optimization Strategies").
 //
-// One CTA per SM (its shared memory admits no second CTA, so the #SMs CTAs are
-// all resident), 8 consumer warps + 1 producer warp.  The producer's lane 0
-// feeds a ring of 32 KiB shared-memory slots with cp.async.bulk copies and
-// tags each slot with what it holds; the consumers take the slots in order.
+// One CTA per SM, all co-resident (cooperative launch), 8 consumer warps + a
+// producer warp + a poll warp.  The producer's lane 0 feeds a ring of 32 KiB
+// shared-memory slots with cp.async.bulk copies and tags each slot with what
+// it holds; the consumers take the slots in order.
 //
-//   1. Router: the consumers dot the CTA's 1-2 router rows with the batch and
-//      write the logits; one grid-wide arrive.  Meanwhile the producer streams
-//      shared-expert gate/up units, which do not depend on routing.
-//   2. Work queue: gate/up units (8 gate + 8 up rows of one group, two slots)
+//   1. Router: the producer copies the CTA's 1-3 router rows into shared
+//      memory as soon as the kernel starts (weights do not depend on the
+//      preceding kernel); the consumers stage the batch's activations, dot
+//      them with the rows and publish the logits as tagged words.  Meanwhile
+//      the producer streams shared-expert gate/up units, which need no routing.
+//   2. Selection: once every CTA has counted its logits in, each CTA reads all
+//      of them, ranks every token (one warp per token) and buckets the pairs --
+//      identical results in every CTA -- and hands the group table to the
+//      producer and the poll warp.
+//   3. Work queue: gate/up units (8 gate + 8 up rows of one group, two slots)
 //      are claimed one at a time from a workspace counter -- the shared
 //      expert's 64 units first, then the routed groups' in group order -- so
 //      CTAs that stream faster take more units and groups finish roughly in
-//      order.  The first claim past the shared units makes the producer post a
-//      SELECT slot: the consumers wait for every CTA's logits, rank and bucket
-//      the batch in shared memory (identical in every CTA) and hand the group
-//      table to the producer.
-//   3. Completion counters: after storing its h values of a unit, each
-//      consumer warp adds 1 to its group's counter (release); the add is
-//      deferred until the warp's next unit is computed or the warp runs idle,
-//      so the fence finds the stores already done.  64 units x 8 warps = 512
+//      order.  The consumer warps store their h values as tagged words; the
+//      last of them to finish a unit adds one to its group's counter, and 64
 //      marks a group's h complete.
-//   4. Down: CTA b < 128 owns output rows [16b, 16b+16) of every token.  As
-//      soon as a group is complete (acquire), its producer posts a DOWN slot:
-//      the 16 rows of the expert's Wd (16 KiB) and the group's h rows, and the
-//      consumers accumulate w(t, g) * (Wd h) per token: groups of <= 4 tokens
-//      on CUDA cores into per-lane running sums (reduced once, at the end),
-//      larger ones on tensor cores.
-//      Down slots take priority over gate/up units, so the down projection
-//      streams while gate/up is still running instead of after a grid
-//      barrier.  Items run in a fixed order (the shared expert, then the
+//   4. Down: CTA b < 128 owns output rows [16b, 16b+16) of every token.  The
+//      poll warp watches the counters of its groups; as soon as one is
+//      complete, the producer posts a DOWN item: the 16 rows of the expert's
+//      Wd (16 KiB) and the group's tagged h rows (4 KiB per token; more than
+//      4 tokens spill into a second slot), and the consumers confirm every h
+//      word's tag and accumulate w(t, g) * (Wd h) per token: groups of <= 4
+//      tokens on CUDA cores into per-lane running sums (reduced once, at the
+//      end), larger ones on tensor cores.  Down items take priority over
+//      gate/up units, so the down projection streams while gate/up is still
+//      running.  Items run in a fixed order (the shared expert, then the
 //      routed groups by expert), so results are reproducible bit for bit.
-// Every wait is bounded by the workspace's limit; the last CTA out resets the
-// workspace counters for the next call.
+//
+// No GPU-scope fence is taken on the data path: a fence waits for the SM's
+// outstanding memory traffic, which while weights stream costs 1-3 us per
+// hand-off.  Logits and h cross SMs as tagged words instead (call_tag), and
+// the counters only say when to look.  The counters come in two sets used by
+// alternate calls: a call clears the set of the next call, and CTA 0 advances
+// the workspace's call counter at its end, so nothing is reset at the exit.
+// Every wait is bounded by the workspace's limit.
 #include "common.cuh"
-#include "down_impl.cuh"
 #include "expert_common.cuh"
 #include "gateup_impl.cuh"
 #include "kernels.h"
@@ -46,23 +52,39 @@
 namespace flint {
 namespace fz {
 constexpr int CW = 8;                          // consumer warps
-constexpr int THREADS = (CW + 3) * 32;         // + producer, signalling and poll warps
+constexpr int PRODUCER = CW;                   // warp index of the producer
+constexpr int POLL = CW + 1;                   // warp index of the poll warp
+constexpr int THREADS = (CW + 2) * 32;
 constexpr int CT = CW * 32;                    // consumer threads
 constexpr int SLOT = 32 * 1024;                // ring slot bytes
 constexpr int NS = 5;                          // ring slots
 constexpr int ROWB = H * 2;                    // one gate/up row (bf16), 4 KiB
 constexpr int UNITS = I / 8;                   // gate/up units per group
-constexpr int MAXB = LOCAL_SELECT_MAX_B;
+constexpr int MAXB = SMALL_B;
 constexpr int MAXG = MAXB * TOPK + S;          // groups at these batches (one shared group)
 constexpr int NPAIR = MAXB * SLOTS;
-constexpr int DONE_SHARED = 63;                // counter slot of the shared group
-constexpr uint32_t DONE_TARGET = UNITS;        // finished units per group
-constexpr int SIGQ = 8;                        // finished units in flight to the signalling warp
-constexpr int DOWN_CTAS = H / dn::RS;          // 128 row-slice owners
+constexpr int DONE_SHARED = SYNC_GROUPS - 1;   // counter of the shared group
+constexpr int UCNT = 8;                        // unit-completion counts in flight
+// Ready down items an owner may post between two of its gate/up units.  A
+// claimed unit must not wait behind a long run of down items: its group would
+// complete late for every owner, and their down items with it.
+constexpr int DN_PER_UNIT = 3;
+constexpr bool PREFETCH_WD = false;            // L2 prefetch of the owner's Wd slices
+constexpr uint32_t DONE_TARGET = UNITS;        // unit marks per complete group
+constexpr int RS = 16;                         // output rows per row-slice owner
+constexpr int DOWN_CTAS = H / RS;              // 128 row-slice owners
+constexpr int WROW = I * 2;                    // one Wd row (bf16)
+constexpr int WBYTES = RS * WROW;              // 16 KiB
+constexpr int THROW = I * 8;                   // one tagged h row, 4 KiB
+constexpr int HROWS_A = (SLOT - WBYTES) / THROW;  // h rows beside the Wd slice: 4
+constexpr int CC_MAX = 4;                      // down items on CUDA cores up to this many tokens
 constexpr int XS_BYTES = MAXB * H * 2;         // bf16 activations of the batch, 32 KiB
 constexpr int RED_BYTES = CW * 16 * GROUP_MAX * 4;
 constexpr int LOGIT_BYTES = MAXB * E * 4;
-constexpr int BUF_BYTES = RED_BYTES > LOGIT_BYTES ? RED_BYTES : LOGIT_BYTES;
+constexpr int RMAX = 3;                        // router rows per CTA (grids of >= 86 CTAs)
+constexpr int RROW_BYTES = RMAX * H * 2;
+constexpr int BUF_BYTES = RED_BYTES > LOGIT_BYTES ? (RED_BYTES > RROW_BYTES ? RED_BYTES : RROW_BYTES)
+                                                  : (LOGIT_BYTES > RROW_BYTES ? LOGIT_BYTES : RROW_BYTES);
 // Per-lane running sums of the CUDA-core down items: [token * 2 + row][thread],
 // rows padded to 257 floats so that both the updates (one row, consecutive
 // lanes) and the final per-row sums (16 lanes each) are free of bank conflicts.
@@ -70,12 +92,14 @@ constexpr int LACC_STRIDE = CW * 32 + 1;
 constexpr int LACC_BYTES = MAXB * 2 * LACC_STRIDE * 4;
 constexpr size_t SMEM = (size_t)NS * SLOT + XS_BYTES + BUF_BYTES + LACC_BYTES;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
-enum : int { IT_GATE = 0, IT_UP = 1, IT_DOWN = 2, IT_SELECT = 3, IT_END = 4 };
+enum : int { IT_GATE = 0, IT_UP = 1, IT_DOWN = 2, IT_DOWN2 = 3, IT_END = 4 };
 static_assert(S == 1 && MAXB <= GROUP_MAX, "one shared group at these batches");
 static_assert(MAXG <= DONE_SHARED, "routed groups and the shared group have distinct counters");
-static_assert(dn::WBYTES + MAXB * dn::HROW <= SLOT, "a down item fits one slot");
+static_assert(SYNC_LINES <= CT, "one thread clears each counter line");
+static_assert(HROWS_A == 4 && MAXB - HROWS_A <= SLOT / THROW, "a down item fits two slots");
 static_assert(8 * ROWB == SLOT, "8 gate (or up) rows fill one slot");
-static_assert(dn::RED_FLOATS * 4 <= BUF_BYTES, "down partial tiles fit the buffer");
+static_assert((E + RMAX - 1) / RMAX <= 86, "grids of 86 CTAs or more keep <= RMAX router rows");
+static_assert(SMEM + 6 * 1024 <= 232448, "fits the opt-in shared memory of one SM");
 }  // namespace fz
 
 namespace {
@@ -91,19 +115,6 @@ struct Item {
   int pad[2];
 };
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
 __device__ __forceinline__ int ld_acquire_cta_shared(const int* p) {
   int v;
   asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
@@ -111,9 +122,6 @@ __device__ __forceinline__ int ld_acquire_cta_shared(const int* p) {
 }
 __device__ __forceinline__ void st_release_cta_shared(int* p, int v) {
   asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_add_relaxed(uint32_t* p, uint32_t v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 // Non-blocking probe of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
@@ -124,20 +132,6 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return done != 0;
-}
-
-__device__ __forceinline__ bool grid_wait(const uint32_t* ctr, uint32_t target, uint64_t deadline) {
-  while (ld_acquire(ctr) < target)
-    if (globaltimer_ns() > deadline) return false;
-  return true;
-}
-
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
 }
 
 __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc) {
@@ -153,12 +147,15 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
 }
 
 // Logits of experts [e_begin, e_end) for the whole batch (B <= 8), by the 8
-// consumer warps: warp w takes expert base + w/4 and the K-quarter w%4.
-__device__ __forceinline__ void router_slice(const RouterArgs& r, int e_begin, int e_end,
-                                             float (*s_part)[4][8]) {
+// consumer warps from shared memory (router rows in `rows`, activations in
+// xs): warp w takes expert base + w/4 and the K-quarter w%4.  Published as
+// tagged words.
+__device__ __forceinline__ void router_slice(int B, const float* bias, uint64_t* tlogits,
+                                             const uint16_t* rows, const uint16_t* xs,
+                                             int e_begin, int e_end, float (*s_part)[4][8],
+                                             uint32_t tag) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int el = warp >> 2, qk = warp & 3;
-  const int B = r.B;
   for (int base = e_begin; base < e_end; base += 2) {
     const int e = base + el;
     float acc[8];
@@ -166,17 +163,15 @@ __device__ __forceinline__ void router_slice(const RouterArgs& r, int e_begin, i
     for (int t = 0; t < 8; ++t) acc[t] = 0.f;
     if (e < e_end) {
       const int c0 = qk * 64 + lane, c1 = c0 + 32;
-      const uint4* wrow = reinterpret_cast<const uint4*>(r.wr + (size_t)e * H);
-      const uint4 w0 = ldg_stream(wrow + c0), w1 = ldg_stream(wrow + c1);
-      uint4 xv[8][2];  // every load of the tile in flight before any FMA
+      const uint4* wrow = reinterpret_cast<const uint4*>(rows + (size_t)(e - e_begin) * H);
+      const uint4 w0 = wrow[c0], w1 = wrow[c1];
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        const uint4* xrow = reinterpret_cast<const uint4*>(r.x + (size_t)t * H);
-        xv[t][0] = t < B ? __ldg(xrow + c0) : make_uint4(0u, 0u, 0u, 0u);
-        xv[t][1] = t < B ? __ldg(xrow + c1) : make_uint4(0u, 0u, 0u, 0u);
+        if (t < B) {
+          const uint4* xrow = reinterpret_cast<const uint4*>(xs + (size_t)t * H);
+          acc[t] = dot8(w1, xrow[c1], dot8(w0, xrow[c0], 0.f));
+        }
       }
-#pragma unroll
-      for (int t = 0; t < 8; ++t) acc[t] = dot8(w1, xv[t][1], dot8(w0, xv[t][0], 0.f));
 #pragma unroll
       for (int t = 0; t < 8; ++t) acc[t] = warp_sum(acc[t]);
     }
@@ -188,9 +183,10 @@ __device__ __forceinline__ void router_slice(const RouterArgs& r, int e_begin, i
     if (tid < 16) {
       const int le = tid >> 3, t = tid & 7, ee = base + le;
       if (ee < e_end && t < B)
-        r.ws.logits[(size_t)t * E + ee] =
-            (s_part[le][0][t] + s_part[le][1][t]) + (s_part[le][2][t] + s_part[le][3][t]) +
-            (r.bias ? __ldg(r.bias + ee) : 0.0f);
+        st_tagged(tlogits + (size_t)t * E + ee,
+                  (s_part[le][0][t] + s_part[le][1][t]) + (s_part[le][2][t] + s_part[le][3][t]) +
+                      (bias ? __ldg(bias + ee) : 0.0f),
+                  tag);
     }
     named_sync(1, fz::CT);
   }
@@ -203,24 +199,16 @@ __device__ __forceinline__ void release_slot(uint32_t empty_bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar);
 }
 
-// Finished gate/up units go to the signalling warp through a small ring of
-// mbarriers (8 consumer-warp arrivals each, after the warps' h stores); it
-// publishes them to the group counters, so no consumer warp waits on a
-// GPU-scope fence.
-struct Sig {
-  uint32_t full0, free0;
-  int* grp;
-  uint64_t limit;
-};
-// gidx: the unit's group counter, -2 for a unit skipped after an abort, -1 at the end.
-__device__ __forceinline__ void signal_unit(const Sig& s, int seq, int gidx) {
-  const int j = seq & (fz::SIGQ - 1);
-  if (seq >= fz::SIGQ && (threadIdx.x & 31) == 0)
-    mbar_wait(s.free0 + 8u * j, (uint32_t)((seq / fz::SIGQ) - 1) & 1u, s.limit);
+// After a warp's h stores of a unit: the last of the 8 consumer warps to get
+// here puts one mark on the group's counter -- a hint; the readers confirm
+// the tags.  The count lives in shared memory, one per unit sequence number
+// modulo UCNT: a warp can be at most a few units ahead of another (the ring
+// refills a slot only once all 8 warps have released it).
+__device__ __forceinline__ void mark_unit(SyncLine* done, int done_idx, int* ucnt) {
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) {
-    if (threadIdx.x == 0) s.grp[j] = gidx;
-    mbar_arrive(s.full0 + 8u * j);
+  if ((threadIdx.x & 31) == 0 && atomicAdd(ucnt, 1) == fz::CW - 1) {
+    *ucnt = 0;
+    red_add_relaxed(&done[done_idx].v, 1u);
   }
 }
 
@@ -229,8 +217,9 @@ __device__ __forceinline__ void signal_unit(const Sig& s, int seq, int gidx) {
 // (gate and up chains interleaved: eight independent FMA chains per lane).
 template <int NTOK>
 __device__ __forceinline__ void unit_cc(const uint8_t* gs, const uint8_t* us, const uint4* xs,
-                                        const int (&tok)[2], float* h, const Item& d, bool ok,
-                                        uint32_t emA, uint32_t emB) {
+                                        const int (&tok)[2], uint64_t* th, const Item& d, bool ok,
+                                        uint32_t emA, uint32_t emB, uint32_t tag, SyncLine* done,
+                                        int* ucnt) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float g[NTOK], v[NTOK];
 #pragma unroll
@@ -267,77 +256,19 @@ __device__ __forceinline__ void unit_cc(const uint8_t* gs, const uint8_t* us, co
   for (int i = 0; i < NTOK; ++i) {
     const float gsum = warp_sum(g[i]);
     const float vsum = warp_sum(v[i]);
-    if (lane == 0) h[(size_t)(d.pair0 + i) * I + d.blk * 8 + warp] = silu_mul(gsum, vsum);
+    if (lane == 0)
+      st_tagged(th + (size_t)(d.pair0 + i) * I + d.blk * 8 + warp, silu_mul(gsum, vsum), tag);
   }
-}
-
-// Down item on CUDA cores (<= 4 tokens): warp w owns Wd rows 2w and 2w+1 of
-// the slice.  The lane's 32 weights are unpacked once and reused by every
-// token; each lane adds w(t, g) times its partial dot product (16 columns) to
-// its own running sum in shared memory -- the sums across lanes are taken
-// once, when the output is written.
-__device__ __forceinline__ void down_cc(const uint8_t* st, int pair0, int n, const int* pair_tok,
-                                        const float* pair_w, float* lacc, bool ok, uint32_t em) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float s0[dn::CC_MAX], s1[dn::CC_MAX];
-#pragma unroll
-  for (int i = 0; i < dn::CC_MAX; ++i) s0[i] = s1[i] = 0.f;
-  if (ok) {
-    const uint8_t* w0 = st + (2 * warp) * dn::WSTRIDE;
-    const uint8_t* w1 = w0 + dn::WSTRIDE;
-    float f0[16], f1[16];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const uint2 a0 = *reinterpret_cast<const uint2*>(w0 + (4 * lane + 128 * m) * 2);
-      const uint2 a1 = *reinterpret_cast<const uint2*>(w1 + (4 * lane + 128 * m) * 2);
-      f0[4 * m] = bf_lo(a0.x);
-      f0[4 * m + 1] = bf_hi(a0.x);
-      f0[4 * m + 2] = bf_lo(a0.y);
-      f0[4 * m + 3] = bf_hi(a0.y);
-      f1[4 * m] = bf_lo(a1.x);
-      f1[4 * m + 1] = bf_hi(a1.x);
-      f1[4 * m + 2] = bf_lo(a1.y);
-      f1[4 * m + 3] = bf_hi(a1.y);
-    }
-#pragma unroll
-    for (int i = 0; i < dn::CC_MAX; ++i) {
-      if (i < n) {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float4 hv = *reinterpret_cast<const float4*>(st + dn::WBYTES + i * dn::HSTRIDE +
-                                                             (4 * lane + 128 * m) * 4);
-          s0[i] = fmaf(f0[4 * m], hv.x, s0[i]);
-          s0[i] = fmaf(f0[4 * m + 1], hv.y, s0[i]);
-          s0[i] = fmaf(f0[4 * m + 2], hv.z, s0[i]);
-          s0[i] = fmaf(f0[4 * m + 3], hv.w, s0[i]);
-          s1[i] = fmaf(f1[4 * m], hv.x, s1[i]);
-          s1[i] = fmaf(f1[4 * m + 1], hv.y, s1[i]);
-          s1[i] = fmaf(f1[4 * m + 2], hv.z, s1[i]);
-          s1[i] = fmaf(f1[4 * m + 3], hv.w, s1[i]);
-        }
-      }
-    }
-  }
-  release_slot(em);
-  if (!ok) return;
-#pragma unroll
-  for (int i = 0; i < dn::CC_MAX; ++i) {
-    if (i < n) {
-      const int t = pair_tok[pair0 + i];
-      const float wt = pair_w[pair0 + i];
-      float* acc = lacc + (2 * t) * fz::LACC_STRIDE + threadIdx.x;
-      acc[0] = fmaf(wt, s0[i], acc[0]);
-      acc[fz::LACC_STRIDE] = fmaf(wt, s1[i], acc[fz::LACC_STRIDE]);
-    }
-  }
+  mark_unit(done, d.done_idx, ucnt);
 }
 
 // Gate/up unit on tensor cores (3..8 tokens): m16n8k16 with the 8 gate + 8 up
 // rows as M and the tokens as N, warp w owns a 256-column K-slice; the same
 // arithmetic as the standalone gate/up kernel.
 __device__ __forceinline__ void unit_mma(const uint8_t* gs, const uint8_t* us, const uint16_t* xs,
-                                         const int* pair_tok, float* buf, float* h, const Item& d,
-                                         bool ok, uint32_t emA, uint32_t emB) {
+                                         const int* pair_tok, float* buf, uint64_t* th,
+                                         const Item& d, bool ok, uint32_t emA, uint32_t emB,
+                                         uint32_t tag, SyncLine* done, int* ucnt) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   const int n = d.n;
@@ -381,10 +312,190 @@ __device__ __forceinline__ void unit_mma(const uint8_t* gs, const uint8_t* us, c
         gsum += buf[(w * gu::ROWS + r) * GROUP_MAX + j];
         usum += buf[(w * gu::ROWS + r + 8) * GROUP_MAX + j];
       }
-      h[(size_t)(d.pair0 + j) * I + d.blk * 8 + r] = silu_mul(gsum, usum);
+      st_tagged(th + (size_t)(d.pair0 + j) * I + d.blk * 8 + r, silu_mul(gsum, usum), tag);
     }
+    if (ok) mark_unit(done, d.done_idx, ucnt);
   }
   named_sync(1, fz::CT);  // buf is free again
+}
+
+// Shared context of the down items.
+struct DnCtx {
+  const int* pair_tok;  // shared memory
+  const float* pair_w;  // shared memory
+  float* lacc;          // CUDA-core running sums
+  float* acc;           // [MAXB][RS] tensor-core accumulators
+  float* red;           // [CW][RS][GROUP_MAX] partial tiles
+  const uint64_t* th;   // tagged h (global), for words whose tag has not landed
+  uint32_t tag;
+  uint64_t deadline;
+  WsHeader* hdr;
+  volatile int* abort_flag;
+};
+
+// h value k of a token's row (copy in shared memory at hrow, the tagged row
+// itself at src), confirmed against the call's tag.
+__device__ __forceinline__ float h_settled(const DnCtx& c, const uint8_t* hrow,
+                                           const uint64_t* src, int k) {
+  uint64_t w = *reinterpret_cast<const uint64_t*>(hrow + (size_t)k * 8);
+  if (!settle_tagged(w, src + k, c.tag, c.deadline)) {
+    *c.abort_flag = 1;
+    set_error(c.hdr, DEV_TIMEOUT);
+  }
+  return __uint_as_float((uint32_t)w);
+}
+
+// Down item on CUDA cores (<= 4 tokens): warp w owns Wd rows 2w and 2w+1 of
+// the slice; lane l takes columns 2l + 64m (+1), m < 8.  The lane's 32 weights
+// are unpacked once and reused by every token; each lane adds w(t, g) times
+// its partial dot product to its own running sum in shared memory -- the sums
+// across lanes are taken once, when the output is written.  A word whose tag
+// has not landed sends the warp through the same arithmetic with every value
+// confirmed from global memory (rare: the counters run behind the stores).
+__device__ __forceinline__ void down_cc(const DnCtx& c, const uint8_t* st, int pair0, int n,
+                                        bool ok, uint32_t em) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float s0[fz::CC_MAX], s1[fz::CC_MAX];
+#pragma unroll
+  for (int i = 0; i < fz::CC_MAX; ++i) s0[i] = s1[i] = 0.f;
+  if (ok) {
+    const uint32_t* w0 = reinterpret_cast<const uint32_t*>(st + (2 * warp) * fz::WROW);
+    const uint32_t* w1 = w0 + fz::WROW / 4;
+    float f0[16], f1[16];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const uint32_t a0 = w0[lane + 32 * m], a1 = w1[lane + 32 * m];
+      f0[2 * m] = bf_lo(a0);
+      f0[2 * m + 1] = bf_hi(a0);
+      f1[2 * m] = bf_lo(a1);
+      f1[2 * m + 1] = bf_hi(a1);
+    }
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < fz::CC_MAX; ++i) {
+      if (i < n) {
+        const uint4* hr = reinterpret_cast<const uint4*>(st + fz::WBYTES + i * fz::THROW);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const uint4 hv = hr[lane + 32 * m];
+          bad |= (hv.y != c.tag) | (hv.w != c.tag);
+          const float h0 = __uint_as_float(hv.x), h1 = __uint_as_float(hv.z);
+          s0[i] = fmaf(f0[2 * m], h0, s0[i]);
+          s0[i] = fmaf(f0[2 * m + 1], h1, s0[i]);
+          s1[i] = fmaf(f1[2 * m], h0, s1[i]);
+          s1[i] = fmaf(f1[2 * m + 1], h1, s1[i]);
+        }
+      }
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+      // Same sums, same order; weights re-read from the slot so that no
+      // register array is indexed at run time.
+#pragma unroll
+      for (int i = 0; i < fz::CC_MAX; ++i) {
+        float a0 = 0.f, a1 = 0.f;
+        if (i < n) {
+          const uint8_t* hrow = st + fz::WBYTES + i * fz::THROW;
+          const uint64_t* src = c.th + (size_t)(pair0 + i) * I;
+#pragma unroll 1
+          for (int m = 0; m < 8; ++m) {
+            const int k = 2 * lane + 64 * m;
+            const uint32_t u0 = w0[lane + 32 * m], u1 = w1[lane + 32 * m];
+            const float h0 = h_settled(c, hrow, src, k);
+            const float h1 = h_settled(c, hrow, src, k + 1);
+            a0 = fmaf(bf_lo(u0), h0, a0);
+            a0 = fmaf(bf_hi(u0), h1, a0);
+            a1 = fmaf(bf_lo(u1), h0, a1);
+            a1 = fmaf(bf_hi(u1), h1, a1);
+          }
+        }
+        s0[i] = a0;
+        s1[i] = a1;
+      }
+    }
+  }
+  release_slot(em);
+  if (!ok) return;
+#pragma unroll
+  for (int i = 0; i < fz::CC_MAX; ++i) {
+    if (i < n) {
+      const int t = c.pair_tok[pair0 + i];
+      const float wt = c.pair_w[pair0 + i];
+      float* acc = c.lacc + (2 * t) * fz::LACC_STRIDE + threadIdx.x;
+      acc[0] = fmaf(wt, s0[i], acc[0]);
+      acc[fz::LACC_STRIDE] = fmaf(wt, s1[i], acc[fz::LACC_STRIDE]);
+    }
+  }
+}
+
+// Down item on tensor cores (5..8 tokens, h rows 0..3 beside the Wd slice in
+// slot A, rows 4.. in slot B): mma.sync m16n8k16 with the 16 Wd rows as M and
+// the tokens as N; the fp32 h is split into two bf16 parts (hi + lo, two
+// MMAs) so the operand keeps ~16 significant bits; warp w owns a 64-column
+// K-slice; the 8 partial tiles are summed through shared memory and weighted
+// into the CTA's accumulators.
+__device__ __forceinline__ void down_mma(const DnCtx& c, const uint8_t* sa, const uint8_t* sb,
+                                         int pair0, int n, bool ok) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint8_t* rlo = sa + g * fz::WROW + (warp * 64 + q * 8) * 2;
+  const uint8_t* rhi = rlo + 8 * fz::WROW;
+  const uint8_t* hrow = g < fz::HROWS_A ? sa + fz::WBYTES + g * fz::THROW
+                                        : sb + (g - fz::HROWS_A) * fz::THROW;
+  if (ok) {
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+      const uint4 alo = *reinterpret_cast<const uint4*>(rlo + kb * 64);
+      const uint4 ahi = *reinterpret_cast<const uint4*>(rhi + kb * 64);
+      // h (fp32) = hi + lo with both parts bf16: two MMAs keep ~16 bits of h.
+      uint32_t b[4] = {0u, 0u, 0u, 0u}, l[4] = {0u, 0u, 0u, 0u};
+      if (g < n) {
+        const int k0 = warp * 64 + kb * 32 + q * 8;
+        float hv[8];
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(hrow + (size_t)(k0 + 2 * j) * 8);
+          bad |= (w.y != c.tag) | (w.w != c.tag);
+          hv[2 * j] = __uint_as_float(w.x);
+          hv[2 * j + 1] = __uint_as_float(w.z);
+        }
+        if (bad) {
+          const uint64_t* src = c.th + (size_t)(pair0 + g) * I;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            hv[j] = h_settled(c, hrow, src, k0 + j);
+        }
+        split_bf2(hv[0], hv[1], b[0], l[0]);
+        split_bf2(hv[2], hv[3], b[1], l[1]);
+        split_bf2(hv[4], hv[5], b[2], l[2]);
+        split_bf2(hv[6], hv[7], b[3], l[3]);
+      }
+      mma_bf16(acc, alo.x, ahi.x, alo.y, ahi.y, b[0], b[1]);
+      mma_bf16(acc, alo.z, ahi.z, alo.w, ahi.w, b[2], b[3]);
+      mma_bf16(acc, alo.x, ahi.x, alo.y, ahi.y, l[0], l[1]);
+      mma_bf16(acc, alo.z, ahi.z, alo.w, ahi.w, l[2], l[3]);
+    }
+  }
+  float* red = c.red + warp * fz::RS * GROUP_MAX;
+  const int col = 2 * q;
+  red[g * GROUP_MAX + col] = acc[0];
+  red[g * GROUP_MAX + col + 1] = acc[1];
+  red[(g + 8) * GROUP_MAX + col] = acc[2];
+  red[(g + 8) * GROUP_MAX + col + 1] = acc[3];
+  named_sync(1, fz::CT);
+  if (ok) {
+    for (int i = threadIdx.x; i < fz::RS * n; i += fz::CT) {
+      const int r = i & (fz::RS - 1), j = i >> 4;
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < fz::CW; ++w) s += c.red[(w * fz::RS + r) * GROUP_MAX + j];
+      const int t = c.pair_tok[pair0 + j];
+      const float wt = c.pair_w[pair0 + j];
+      c.acc[t * fz::RS + r] += wt * s;
+    }
+  }
+  named_sync(1, fz::CT);
 }
 
 // ---- producer side (lane 0 of the producer warp) -----------------------------
@@ -411,15 +522,16 @@ __device__ __forceinline__ bool take_slot(Prod& p, int& slot) {
   return true;
 }
 
-// A slot with no payload (SELECT / END): armed by a plain arrive.
-__device__ __forceinline__ void post_marker(Prod& p, int kind) {
+// The END slot: armed by a plain arrive (posted even after an abort; waits
+// out the drain bound for its slot).
+__device__ __forceinline__ void post_end(Prod& p) {
   const int slot = p.it % fz::NS;
-  if (p.it >= fz::NS)  // END is posted even after an abort; wait out the drain bound
+  if (p.it >= fz::NS)
     mbar_wait(p.empty0 + 8u * slot, (uint32_t)((p.it / fz::NS) - 1) & 1u,
               p.deadline + fz::DRAIN_NS);
   ++p.it;
   Item d = {};
-  d.kind = kind;
+  d.kind = fz::IT_END;
   p.desc[slot] = d;
   mbar_arrive(p.full0 + 8u * slot);
 }
@@ -437,71 +549,108 @@ __device__ __forceinline__ bool post_gateup(Prod& p, const uint16_t* base, const
   p.desc[sb] = du;
   mbar_expect_tx(p.full0 + 8u * sb, fz::SLOT);
   bulk_g2s_stream(p.stages_addr + sb * fz::SLOT, base + (size_t)(I + d.blk * 8) * H, fz::SLOT,
-           p.full0 + 8u * sb);
+                  p.full0 + 8u * sb);
   return true;
 }
 
+// A down item's slots: its Wd slice (issued now) and room for its tagged h
+// rows (counted now, copied once the group is complete).  Returns false on
+// abort; `sl` receives the slots (second -1 for items of <= 4 tokens).
+__device__ __forceinline__ bool post_down_w(Prod& p, const Item& d, const uint16_t* wd,
+                                            int* sl) {
+  sl[1] = -1;
+  if (!take_slot(p, sl[0])) return false;
+  const int na = d.n < fz::HROWS_A ? d.n : fz::HROWS_A;
+  p.desc[sl[0]] = d;
+  mbar_expect_tx(p.full0 + 8u * sl[0], fz::WBYTES + na * fz::THROW);
+  bulk_g2s_stream(p.stages_addr + sl[0] * fz::SLOT, wd, fz::WBYTES, p.full0 + 8u * sl[0]);
+  if (d.n > fz::HROWS_A) {
+    if (!take_slot(p, sl[1])) return false;
+    Item d2 = d;
+    d2.kind = fz::IT_DOWN2;
+    p.desc[sl[1]] = d2;
+    mbar_expect_tx(p.full0 + 8u * sl[1], (d.n - fz::HROWS_A) * fz::THROW);
+  }
+  return true;
+}
+
+__device__ __forceinline__ void post_down_h(Prod& p, const Item& d, const uint64_t* hr,
+                                            const int* sl) {
+  const int na = d.n < fz::HROWS_A ? d.n : fz::HROWS_A;
+  bulk_g2s(p.stages_addr + sl[0] * fz::SLOT + fz::WBYTES, hr, na * fz::THROW, p.full0 + 8u * sl[0]);
+  if (sl[1] >= 0)
+    bulk_g2s(p.stages_addr + sl[1] * fz::SLOT, hr + (size_t)na * I, (d.n - na) * fz::THROW,
+             p.full0 + 8u * sl[1]);
+}
 
 }  // namespace
 
 __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertArgs a, RouterArgs r) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_abort;
+  __shared__ volatile int s_abort;
   __shared__ int s_ngroups;
   __shared__ int s_ready;  // down items whose groups are complete (poll warp -> producer)
   __shared__ Item s_desc[fz::NS];
   __shared__ int4 s_groups[fz::MAXG];
   __shared__ int s_pair_tok[fz::NPAIR];
   __shared__ float s_pair_w[fz::NPAIR];
-  __shared__ float s_acc[fz::MAXB * dn::RS];  // this CTA's 16 output rows per token
+  __shared__ float s_acc[fz::MAXB * fz::RS];  // this CTA's 16 output rows per token
   __shared__ LocalSelectSmem s_sel;
   __shared__ float s_part[2][4][8];
-  __shared__ int s_hgrp[fz::SIGQ];
-  // ring full / empty, SELECT done, finished-unit full / free, signalling done
-  __shared__ __align__(8) uint64_t s_bars[2 * fz::NS + 1 + 2 * fz::SIGQ + 1];
+  __shared__ int s_ucnt[fz::UCNT];  // consumer warps done with recent units
+  __shared__ int s_dslot[fz::NS][2];  // producer: ring slots of its down items in flight
+  // ring full / empty, router rows, selection done
+  __shared__ __align__(8) uint64_t s_bars[2 * fz::NS + 2];
   WsHeader* hdr = a.ws.hdr;
-  uint32_t* done = hdr->group_done;
   const int G = gridDim.x, cta = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = a.B;
   uint8_t* ring = smem;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + fz::NS * fz::SLOT);
   float* buf = reinterpret_cast<float*>(smem + fz::NS * fz::SLOT + fz::XS_BYTES);
   float* lacc = reinterpret_cast<float*>(smem + fz::NS * fz::SLOT + fz::XS_BYTES + fz::BUF_BYTES);
   const uint32_t full0 = smem_addr(s_bars), empty0 = smem_addr(s_bars + fz::NS);
-  const uint32_t sel_bar = smem_addr(s_bars + 2 * fz::NS);
-  const uint32_t hfull0 = smem_addr(s_bars + 2 * fz::NS + 1);
-  const uint32_t hfree0 = hfull0 + 8u * fz::SIGQ;
-  const uint32_t sig_done = hfree0 + 8u * fz::SIGQ;
+  const uint32_t rrow_bar = smem_addr(s_bars + 2 * fz::NS);
+  const uint32_t sel_bar = rrow_bar + 8u;
+  const int e_begin = (int)((long long)cta * E / G), e_end = (int)((long long)(cta + 1) * E / G);
 
-  if (tid == 0) {
+  if (warp == fz::PRODUCER && lane == 0) {
     for (int s = 0; s < fz::NS; ++s) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, fz::CW);
     }
+    mbar_init(rrow_bar, 1);
     mbar_init(sel_bar, 1);
-    for (int j = 0; j < fz::SIGQ; ++j) {
-      mbar_init(hfull0 + 8u * j, fz::CW);
-      mbar_init(hfree0 + 8u * j, 1);
-    }
-    mbar_init(sig_done, 1);
+    fence_mbar_init();
+    // The router rows are weights: nothing the preceding kernel writes.
+    const uint32_t rb = (uint32_t)(e_end - e_begin) * (H * 2);
+    mbar_expect_tx(rrow_bar, rb);
+    bulk_g2s_stream(smem_addr(buf), r.wr + (size_t)e_begin * H, rb, rrow_bar);
+    // So is the shared expert's Wd slice of a row-slice owner (its first down
+    // item, which needs no routing).
+    if (fz::PREFETCH_WD && cta < fz::DOWN_CTAS)
+      bulk_prefetch_l2(a.w.ws2 + (size_t)cta * fz::RS * I, fz::WBYTES);
     s_abort = 0;
     s_ngroups = 0;
     s_ready = 0;
-    fence_mbar_init();
   }
-  for (int i = tid; i < fz::MAXB * dn::RS; i += blockDim.x) s_acc[i] = 0.f;
+  if (tid < fz::UCNT) s_ucnt[tid] = 0;
+  for (int i = tid; i < fz::MAXB * fz::RS; i += blockDim.x) s_acc[i] = 0.f;
   for (int i = tid; i < fz::LACC_BYTES / 4; i += blockDim.x) lacc[i] = 0.f;
   __syncthreads();
   // Launched with programmatic serialization: the set-up above overlaps the
-  // preceding kernel; x, the weights and the workspace are read only after it.
+  // preceding kernel; x and the workspace are read only after it.
   pdl_wait();
   const uint64_t deadline = wait_deadline(hdr);
+  const uint32_t epoch = __ldcg(&hdr->epoch);
+  const uint32_t par = epoch & 1u, tag = call_tag(epoch);
+  SyncLine* sync = hdr->sync[par];
+  SyncLine* done = sync;  // completion counters: lines 0 .. SYNC_GROUPS-1
   const bool owner = cta < fz::DOWN_CTAS;
-  const int r0 = cta * dn::RS;
+  const int r0 = cta * fz::RS;
   const int npairs = B * TOPK;
 
-  if ((tid >> 5) == fz::CW) {  // ---------------- producer warp (lane 0 issues)
+  if (warp == fz::PRODUCER) {  // ---------------- producer warp (lane 0 issues)
     if (lane != 0) return;
     Prod p;
     p.full0 = full0;
@@ -512,8 +661,9 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     p.deadline = deadline;
     p.hdr = hdr;
     p.abort_flag = &s_abort;
-    int u = (int)atomicAdd(&hdr->unit_next, 1u);    // unit being issued
-    int nxt = (int)atomicAdd(&hdr->unit_next, 1u);  // claimed ahead
+    uint32_t* claim = &sync[SYNC_UNIT].v;
+    int u = (int)atomicAdd(claim, 1u);    // unit being issued
+    int nxt = (int)atomicAdd(claim, 1u);  // claimed ahead
     bool meta = false, claims_open = true;
     int total = 0x7fffffff, ng = 0, ndn = 0;
     // Down items: the shared group first (its h is ready first), then the
@@ -521,53 +671,54 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     // items whose h copy is issued (kh <= kw; items in between were posted
     // ahead with only their Wd slice, once this CTA had no gate/up left).
     int kw = 0, kh = 0;
-    int dslot[fz::NS];
-    auto dn_group = [&](int kk) { return kk == 0 ? ng - 1 : kk - 1; };
-    auto dn_item = [&](int kk, const uint16_t*& wd, const float*& hr) {
-      const int4 grp = s_groups[dn_group(kk)];
+    int (*dslot)[2] = s_dslot;  // ring slots of the down items in flight
+    const uint16_t* const w2 = a.w.w2 + (size_t)r0 * I;
+    const uint16_t* const ws2 = a.w.ws2 + (size_t)r0 * I;
+    const uint64_t* const th = a.ws.th;
+    auto dn_item = [&](int kk, const uint16_t*& wd, const uint64_t*& hr) {
+      const int4 grp = s_groups[kk == 0 ? ng - 1 : kk - 1];
       Item d = {};
       d.kind = fz::IT_DOWN;
       d.pair0 = grp.y;
       d.n = grp.z;
-      wd = (grp.x < E ? a.w.w2 + (size_t)grp.x * H * I : a.w.ws2 + (size_t)(grp.x - E) * H * I) +
-           (size_t)r0 * I;
-      hr = a.ws.h + (size_t)grp.y * I;
+      wd = grp.x < E ? w2 + (size_t)grp.x * H * I : ws2 + (size_t)(grp.x - E) * H * I;
+      hr = th + (size_t)grp.y * I;
       return d;
     };
     bool ok = true;
+    int dn_budget = 0;  // ready down items still allowed before the claimed unit
     while (ok && !s_abort) {
       // Down items whose groups the poll warp has seen complete.
       const int rdy = meta && kh < ndn ? ld_acquire_cta_shared(&s_ready) : 0;
-      if (rdy > kh) {
-        {
-          // h of these groups was written by other CTAs (generic proxy); the
-          // poll warp acquired it at GPU scope and this thread from the poll
-          // warp at CTA scope.  Order it before the bulk (async-proxy) reads.
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          for (; ok && kh < rdy; ++kh) {
-            const uint16_t* wd;
-            const float* hr;
-            const Item d = dn_item(kh, wd, hr);
-            if (kh < kw) {  // Wd already on its way: add the h rows
-              const int sl = dslot[kh % fz::NS];
-              bulk_g2s(p.stages_addr + sl * fz::SLOT + dn::WBYTES, hr, d.n * dn::HROW,
-                       p.full0 + 8u * sl);
-            } else {
-              int sl;
-              if (!(ok = take_slot(p, sl))) break;
-              p.desc[sl] = d;
-              mbar_expect_tx(p.full0 + 8u * sl, dn::WBYTES + d.n * dn::HROW);
-              bulk_g2s_stream(p.stages_addr + sl * fz::SLOT, wd, dn::WBYTES, p.full0 + 8u * sl);
-              bulk_g2s(p.stages_addr + sl * fz::SLOT + dn::WBYTES, hr, d.n * dn::HROW,
-                       p.full0 + 8u * sl);
-              kw = kh + 1;
-            }
-          }
-          continue;
+      const bool unit_pending = claims_open && (u < fz::UNITS || (meta && u < total));
+      if (rdy > kh && (!unit_pending || dn_budget > 0)) {
+        const uint16_t* wd;
+        const uint64_t* hr;
+        const Item d = dn_item(kh, wd, hr);
+        if (kh >= kw) {
+          if (!(ok = post_down_w(p, d, wd, dslot[kh % fz::NS]))) break;
+          kw = kh + 1;
         }
+        post_down_h(p, d, hr, dslot[kh % fz::NS]);
+        ++kh;
+        --dn_budget;
+        continue;
       }
-      if (claims_open && u >= fz::UNITS && !meta) {
-        post_marker(p, fz::IT_SELECT);
+      if (claims_open && u < fz::UNITS) {  // shared expert: tokens 0..B-1, pairs after the routed ones
+        Item d = {};
+        d.kind = fz::IT_GATE;
+        d.blk = u;
+        d.pair0 = npairs;
+        d.n = B;
+        d.tok0 = 0;
+        d.done_idx = fz::DONE_SHARED;
+        ok = post_gateup(p, a.w.ws13, d);
+        u = nxt;
+        nxt = (int)atomicAdd(claim, 1u);
+        dn_budget = fz::DN_PER_UNIT;
+        continue;
+      }
+      if (!meta) {
         if (!mbar_wait(sel_bar, 0u, deadline)) {
           s_abort = 1;
           set_error(hdr, DEV_TIMEOUT);
@@ -577,48 +728,45 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
         total = ng * fz::UNITS;  // the shared group's units and the routed ones
         ndn = owner ? ng : 0;
         meta = true;
+        if (fz::PREFETCH_WD) {
+          // This CTA's Wd slices (16 KiB per group) into L2 now: a down item
+          // posted later then waits for L2, not DRAM, and more of them turn
+          // over in the ring while gate/up units stream.  Each byte is still
+          // read from DRAM once.
+          for (int k = 1; k < ndn; ++k) {
+            const uint16_t* wd;
+            const uint64_t* hr;
+            dn_item(k, wd, hr);
+            bulk_prefetch_l2(wd, fz::WBYTES);
+          }
+        }
         continue;
       }
       if (claims_open && u < total) {
+        const int ru = u - fz::UNITS;
+        const int gi = ru / fz::UNITS;
+        const int4 grp = s_groups[gi];
         Item d = {};
         d.kind = fz::IT_GATE;
-        const uint16_t* base;
-        if (u < fz::UNITS) {  // shared expert: tokens 0..B-1, pairs after the routed ones
-          d.blk = u;
-          d.pair0 = npairs;
-          d.n = B;
-          d.tok0 = 0;
-          d.done_idx = fz::DONE_SHARED;
-          base = a.w.ws13;
-        } else {
-          const int ru = u - fz::UNITS;
-          const int gi = ru / fz::UNITS;
-          const int4 grp = s_groups[gi];
-          d.blk = ru % fz::UNITS;
-          d.pair0 = grp.y;
-          d.n = grp.z;
-          d.tok0 = -1;
-          d.done_idx = gi;
-          base = a.w.w13 + (size_t)grp.x * (2 * I) * H;
-        }
-        ok = post_gateup(p, base, d);
+        d.blk = ru % fz::UNITS;
+        d.pair0 = grp.y;
+        d.n = grp.z;
+        d.tok0 = -1;
+        d.done_idx = gi;
+        ok = post_gateup(p, a.w.w13 + (size_t)grp.x * (2 * I) * H, d);
         u = nxt;
-        nxt = (int)atomicAdd(&hdr->unit_next, 1u);
+        nxt = (int)atomicAdd(claim, 1u);
+        dn_budget = fz::DN_PER_UNIT;
         continue;
       }
       claims_open = false;
       if (kh < ndn) {  // nothing left to stream but this CTA's down rows
-        if (kw < ndn && kw - kh < fz::NS) {
+        if (kw < ndn && kw - kh < fz::NS - 1) {
           // post the next item's Wd slice now; its h follows once complete
           const uint16_t* wd;
-          const float* hr;
+          const uint64_t* hr;
           const Item d = dn_item(kw, wd, hr);
-          int sl;
-          if (!(ok = take_slot(p, sl))) break;
-          p.desc[sl] = d;
-          mbar_expect_tx(p.full0 + 8u * sl, dn::WBYTES + d.n * dn::HROW);
-          bulk_g2s_stream(p.stages_addr + sl * fz::SLOT, wd, dn::WBYTES, p.full0 + 8u * sl);
-          dslot[kw % fz::NS] = sl;
+          if (!(ok = post_down_w(p, d, wd, dslot[kw % fz::NS]))) break;
           ++kw;
           continue;
         }
@@ -627,7 +775,8 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
           set_error(hdr, DEV_TIMEOUT);
           break;
         }
-        continue;  // spin on s_ready (shared memory)
+        __nanosleep(64);
+        continue;  // wait for s_ready (shared memory)
       }
       break;
     }
@@ -635,23 +784,18 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     // complete them with the h rows as they are, so no copy stays pending.
     for (; kh < kw; ++kh) {
       const uint16_t* wd;
-      const float* hr;
+      const uint64_t* hr;
       const Item d = dn_item(kh, wd, hr);
-      const int sl = dslot[kh % fz::NS];
-      bulk_g2s(p.stages_addr + sl * fz::SLOT + dn::WBYTES, hr, d.n * dn::HROW, p.full0 + 8u * sl);
+      post_down_h(p, d, hr, dslot[kh % fz::NS]);
     }
-    // The claim made ahead must have landed before the CTA counts itself out
-    // (the last CTA out resets the counter): wait for its value.
-    if (nxt < 0) s_abort = 1;
-    post_marker(p, fz::IT_END);
+    post_end(p);
     return;
   }
 
-  if ((tid >> 5) == fz::CW + 2) {  // ---------------- poll warp (lane 0, row-slice owners)
+  if (warp == fz::POLL) {  // ---------------- poll warp (lane 0, row-slice owners)
     // Watches the completion counters of this CTA's down items in order (the
     // shared group first, then the routed groups), eight loads in flight at a
-    // time, and publishes how many are complete; the GPU-scope acquire fence
-    // is taken here, so the producer never waits on one.
+    // time, and publishes how many are complete.
     if (lane != 0 || !owner) return;
     while (!mbar_test(sel_bar, 0u))
       if (s_abort || globaltimer_ns() > deadline) return;
@@ -661,7 +805,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
       uint32_t pw[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        pw[j] = k + j < ng ? ld_relaxed(done + (k + j == 0 ? fz::DONE_SHARED : k + j - 1)) : 0u;
+        pw[j] = k + j < ng ? ld_relaxed_u32(&done[k + j == 0 ? fz::DONE_SHARED : k + j - 1].v) : 0u;
       int rdy = 0;
       bool run = true;
 #pragma unroll
@@ -670,45 +814,14 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
         rdy += run ? 1 : 0;
       }
       if (rdy > 0) {
-        fence_acq_rel_gpu();
         k += rdy;
         st_release_cta_shared(&s_ready, k);
       } else if (globaltimer_ns() > deadline) {
         break;
+      } else {
+        __nanosleep(128);
       }
     }
-    return;
-  }
-
-  if ((tid >> 5) == fz::CW + 1) {  // ---------------- signalling warp (lane 0)
-    if (lane != 0) return;
-    // Publishes finished units in order, one release fence per batch of units
-    // found finished (the consumers' h stores were ordered before their
-    // arrivals on the unit's barrier, which this thread has observed).
-    const uint64_t limit = deadline + fz::DRAIN_NS;
-    int q = 0;
-    bool end = false;
-    while (!end) {
-      if (!mbar_wait(hfull0 + 8u * (q & (fz::SIGQ - 1)), (uint32_t)(q / fz::SIGQ) & 1u, limit)) break;
-      int n = 1;
-      while (n < fz::SIGQ &&
-             mbar_test(hfull0 + 8u * ((q + n) & (fz::SIGQ - 1)), (uint32_t)((q + n) / fz::SIGQ) & 1u))
-        ++n;
-      fence_acq_rel_gpu();
-      int k = 0;
-      for (; k < n; ++k) {
-        const int gi = s_hgrp[(q + k) & (fz::SIGQ - 1)];
-        if (gi == -1) {
-          end = true;
-          break;
-        }
-        if (gi >= 0) red_add_relaxed(done + gi, 1u);
-      }
-      for (int j = 0; j < k; ++j) mbar_arrive(hfree0 + 8u * ((q + j) & (fz::SIGQ - 1)));
-      q += k;
-    }
-    __threadfence();  // the adds are performed before the CTA counts itself out
-    mbar_arrive(sig_done);
     return;
   }
 
@@ -720,18 +833,19 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     while (!*reinterpret_cast<volatile uint32_t*>(&hdr->stall_release)) {
       if (globaltimer_ns() > deadline) {
         set_error(hdr, DEV_TIMEOUT);
+        s_abort = 1;
         break;
       }
     }
     hdr->stall_armed = 0;
   }
-  // 1. router logits for this CTA's experts
-  router_slice(r, (int)((long long)cta * E / G), (int)((long long)(cta + 1) * E / G), s_part);
-  if (tid == 0) {
-    __threadfence();
-    atomicAdd(&hdr->grid_bar[0], 1u);
+  if (cta == 0 && tid < SYNC_LINES) {
+    // The next call uses the other set of counters: clear it now (the last
+    // call that used it has completed).
+    hdr->sync[par ^ 1u][tid].v = 0u;
   }
-  // the batch's activations, once (all loads in flight together)
+  // 1. the batch's activations (all loads in flight together), then the
+  //    router logits of this CTA's experts
   {
     uint4 v[fz::MAXB];
 #pragma unroll
@@ -742,97 +856,130 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     for (int t = 0; t < fz::MAXB; ++t)
       if (t < B) reinterpret_cast<uint4*>(xs)[t * (H / 8) + tid] = v[t];
   }
-  named_sync(1, fz::CT);  // xs is complete before any gate/up unit reads it
+  named_sync(1, fz::CT);
+  if (!mbar_wait(rrow_bar, 0u, deadline)) {
+    s_abort = 1;
+    set_error(hdr, DEV_TIMEOUT);
+  }
+  router_slice(B, r.bias, a.ws.tlogits, reinterpret_cast<const uint16_t*>(buf), xs, e_begin,
+               e_end, s_part, tag);
+  // 2. every CTA ranks and buckets the batch once all logits are in
+  if (tid == 0) {
+    red_add_relaxed(&sync[SYNC_ARRIVE].v, 1u);
+    while (ld_relaxed_u32(&sync[SYNC_ARRIVE].v) < (uint32_t)G) {
+      if (s_abort || globaltimer_ns() > deadline) {
+        s_abort = 1;
+        set_error(hdr, DEV_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  named_sync(1, fz::CT);
+  {
+    uint64_t lw[fz::MAXB];
+#pragma unroll
+    for (int t = 0; t < fz::MAXB; ++t) lw[t] = t < B ? ld_tagged(a.ws.tlogits + (size_t)t * E + tid) : 0u;
+#pragma unroll
+    for (int t = 0; t < fz::MAXB; ++t) {
+      if (t < B) {
+        if (!s_abort && !settle_tagged(lw[t], a.ws.tlogits + (size_t)t * E + tid, tag, deadline)) {
+          s_abort = 1;
+          set_error(hdr, DEV_TIMEOUT);
+        }
+        buf[t * E + tid] = __uint_as_float((uint32_t)lw[t]);
+      }
+    }
+  }
+  named_sync(1, fz::CT);
+  if (warp < B) {
+    int ix;
+    float wt;
+    topk_warp<false>(buf + warp * E, ix, wt);
+    if (lane < TOPK) {
+      const int pp = warp * TOPK + lane;
+      s_sel.idx[pp] = ix;
+      s_sel.w[pp] = wt;
+      if (cta == 0) {
+        a.ws.topk_idx[pp] = ix;
+        a.ws.topk_w[pp] = wt;
+        if (a.user_idx) a.user_idx[pp] = ix;
+        if (a.user_w) a.user_w[pp] = wt;
+      }
+    }
+  }
+  named_sync(1, fz::CT);
+  bucket_small<fz::CT, 4>(B, s_sel.idx, s_sel.w, s_pair_tok, s_pair_w, s_groups, &s_ngroups,
+                          s_sel.sc.off);
+  named_sync(1, fz::CT);
+  if (tid == 0) mbar_arrive(sel_bar);
+  if (cta == 0) {  // the routing tables, for the stage calls that may follow
+    const int ng = s_ngroups;
+    for (int i = tid; i < ng; i += fz::CT) a.ws.groups[i] = s_groups[i];
+    for (int i = tid; i < B * SLOTS; i += fz::CT) {
+      a.ws.pair_tok[i] = s_pair_tok[i];
+      a.ws.pair_w[i] = s_pair_w[i];
+    }
+    if (tid == 0) hdr->n_groups = (uint32_t)ng;
+  }
 
-  dn_impl::DnCtx dc;
-  dc.acc = s_acc;
-  dc.red = buf;
+  DnCtx dc;
   dc.pair_tok = s_pair_tok;
   dc.pair_w = s_pair_w;
+  dc.lacc = lacc;
+  dc.acc = s_acc;
+  dc.red = buf;
+  dc.th = a.ws.th;
+  dc.tag = tag;
+  dc.deadline = deadline;
+  dc.hdr = hdr;
+  dc.abort_flag = &s_abort;
 
+  // 3./4. the ring: gate/up units and this CTA's down items
   int it = 0, useq = 0;
   const uint64_t drain = deadline + fz::DRAIN_NS;
-  Sig sig;
-  sig.full0 = hfull0;
-  sig.free0 = hfree0;
-  sig.grp = s_hgrp;
-  sig.limit = drain;
   while (true) {
     const int slot = it % fz::NS;
-    const uint32_t par = (uint32_t)(it / fz::NS) & 1u;
-    if (!mbar_wait(full0 + 8u * slot, par, deadline)) {
+    const uint32_t ph = (uint32_t)(it / fz::NS) & 1u;
+    if (!mbar_wait(full0 + 8u * slot, ph, deadline)) {
       s_abort = 1;
       set_error(hdr, DEV_TIMEOUT);
-      if (!mbar_wait(full0 + 8u * slot, par, drain)) break;
+      if (!mbar_wait(full0 + 8u * slot, ph, drain)) break;
     }
     const Item d = s_desc[slot];
     const bool ok = !s_abort;
     if (d.kind == fz::IT_END) break;
-    if (d.kind == fz::IT_SELECT) {
-      // 2. every CTA ranks and buckets the batch once all logits are in
-      if (tid == 0 && !grid_wait(&hdr->grid_bar[0], (uint32_t)G, deadline)) {
+    // both kinds may take a second slot
+    const int slot2 = (it + 1) % fz::NS;
+    const uint32_t ph2 = (uint32_t)((it + 1) / fz::NS) & 1u;
+    if (d.kind == fz::IT_DOWN) {
+      const uint8_t* st = ring + slot * fz::SLOT;
+      if (d.n <= fz::CC_MAX) {
+        down_cc(dc, st, d.pair0, d.n, ok, empty0 + 8u * slot);
+        ++it;
+        continue;
+      }
+      bool ok2 = ok;
+      if (!mbar_wait(full0 + 8u * slot2, ph2, deadline)) {
         s_abort = 1;
         set_error(hdr, DEV_TIMEOUT);
+        ok2 = false;
+        if (!mbar_wait(full0 + 8u * slot2, ph2, drain)) break;
       }
-      named_sync(1, fz::CT);
-      {
-        float lv[fz::MAXB];
-#pragma unroll
-        for (int t = 0; t < fz::MAXB; ++t)
-          lv[t] = t < B ? __ldcg(a.ws.logits + (size_t)t * E + tid) : 0.f;
-#pragma unroll
-        for (int t = 0; t < fz::MAXB; ++t)
-          if (t < B) buf[t * E + tid] = lv[t];
-      }
-      named_sync(1, fz::CT);
-      const int warp = tid >> 5;
-      if (warp < B) {
-        int ix;
-        float wt;
-        topk_warp<false>(buf + warp * E, ix, wt);
-        if (lane < TOPK) {
-          const int pp = warp * TOPK + lane;
-          s_sel.idx[pp] = ix;
-          s_sel.w[pp] = wt;
-          if (cta == 0) {
-            a.ws.topk_idx[pp] = ix;
-            a.ws.topk_w[pp] = wt;
-            if (a.user_idx) a.user_idx[pp] = ix;
-            if (a.user_w) a.user_w[pp] = wt;
-          }
-        }
-      }
-      named_sync(1, fz::CT);
-      bucket_small<fz::CT, 4>(B, s_sel.idx, s_sel.w, s_pair_tok, s_pair_w, s_groups, &s_ngroups,
-                              s_sel.sc.off);
-      named_sync(1, fz::CT);
-      if (tid == 0) mbar_arrive(sel_bar);
+      if (s_desc[slot2].kind != fz::IT_DOWN2) break;  // the producer gave up mid-item (abort)
+      down_mma(dc, st, ring + slot2 * fz::SLOT, d.pair0, d.n, ok2);
       release_slot(empty0 + 8u * slot);
-      ++it;
+      release_slot(empty0 + 8u * slot2);
+      it += 2;
       continue;
     }
-    if (d.kind == fz::IT_DOWN) {
-      // 4. this CTA's 16 output rows of the group, weighted into the accumulators
-      const uint8_t* st = ring + slot * fz::SLOT;
-      const uint32_t em = empty0 + 8u * slot;
-      if (d.n <= dn::CC_MAX) {
-        down_cc(st, d.pair0, d.n, s_pair_tok, s_pair_w, lacc, ok, em);
-      } else {
-        dn_impl::group_mma<1>(dc, st, d.pair0, ok ? d.n : 0);  // n <= 8 here, into s_acc
-        release_slot(em);
-      }
-      ++it;
-      continue;
-    }
-    // 3. gate/up unit: gate rows in this slot, up rows in the next
-    const int slot2 = (it + 1) % fz::NS;
-    const uint32_t par2 = (uint32_t)((it + 1) / fz::NS) & 1u;
+    // gate/up unit: gate rows in this slot, up rows in the next
     bool ok2 = ok;
-    if (!mbar_wait(full0 + 8u * slot2, par2, deadline)) {
+    if (!mbar_wait(full0 + 8u * slot2, ph2, deadline)) {
       s_abort = 1;
       set_error(hdr, DEV_TIMEOUT);
       ok2 = false;
-      if (!mbar_wait(full0 + 8u * slot2, par2, drain)) break;
+      if (!mbar_wait(full0 + 8u * slot2, ph2, drain)) break;
     }
     if (s_desc[slot2].kind != fz::IT_UP) break;  // the producer gave up mid-unit (abort)
     const uint8_t* gs = ring + slot * fz::SLOT;
@@ -842,19 +989,18 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
       tok[0] = d.tok0 >= 0 ? d.tok0 : s_pair_tok[d.pair0];
       tok[1] = d.n > 1 ? (d.tok0 >= 0 ? d.tok0 + 1 : s_pair_tok[d.pair0 + 1]) : tok[0];
       if (d.n == 1)
-        unit_cc<1>(gs, us, reinterpret_cast<const uint4*>(xs), tok, a.ws.h, d, ok2,
-                   empty0 + 8u * slot, empty0 + 8u * slot2);
+        unit_cc<1>(gs, us, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
+                   empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
       else
-        unit_cc<2>(gs, us, reinterpret_cast<const uint4*>(xs), tok, a.ws.h, d, ok2,
-                   empty0 + 8u * slot, empty0 + 8u * slot2);
+        unit_cc<2>(gs, us, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
+                   empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
     } else {
-      unit_mma(gs, us, xs, s_pair_tok, buf, a.ws.h, d, ok2, empty0 + 8u * slot,
-               empty0 + 8u * slot2);
+      unit_mma(gs, us, xs, s_pair_tok, buf, a.ws.th, d, ok2, empty0 + 8u * slot,
+               empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
     }
-    signal_unit(sig, useq++, ok2 ? d.done_idx : -2);
+    useq = (useq + 1) & (fz::UCNT - 1);
     it += 2;
   }
-  signal_unit(sig, useq, -1);
   named_sync(1, fz::CT);
   if (owner && !s_abort) {
     // Thread pair (2s, 2s+1) finishes sum s = (warp w, token t, row r): each
@@ -870,23 +1016,16 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     if (half == 0 && t < B) {
       const int row = 2 * w + rr;
       const size_t o = (size_t)t * H + r0 + row;
-      a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + (v + s_acc[t * dn::RS + row]));
+      a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + (v + s_acc[t * fz::RS + row]));
     }
   }
-  // The last CTA out resets the counters for the next call (every CTA has
-  // finished its claims, marks and polls by the time it counts itself out).
-  if (tid == 0) {
-    mbar_wait(sig_done, 0u, drain);
-    __threadfence();
-    if (atomicAdd(&hdr->grid_bar[2], 1u) == (uint32_t)G - 1) {
-      hdr->grid_bar[0] = 0u;
-      hdr->unit_next = 0u;
-      for (int i = 0; i < 64; ++i) done[i] = 0u;
-      hdr->grid_bar[2] = 0u;
-      __threadfence();
-    }
-  }
+  // CTA 0 counts the call (also after a timeout, so that words a failed call
+  // left behind never carry the next call's tag): every CTA read the counter
+  // before it counted its logits in, and CTA 0 has seen all of them.
+  if (cta == 0 && tid == 0) hdr->epoch = (epoch + 1u) & 0x7fffffffu;
 }
+
+bool small_bf16_supported(int num_sms) { return num_sms >= 86 && num_sms <= 1024; }
 
 cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                               int num_sms) {
@@ -898,14 +1037,17 @@ cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStre
   cfg.blockDim = dim3(fz::THREADS, 1, 1);
   cfg.dynamicSmemBytes = fz::SMEM;
   cfg.stream = stream;
-  // One CTA per SM: the kernel's shared memory (> half an SM's) allows no
-  // second one, so the grid of #SMs CTAs is resident as soon as the SMs are
-  // free; the grid-wide waits are bounded in any case.
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // One CTA per SM, all of them resident at once (the CTAs wait for each
+  // other's logits and h): a cooperative launch, which the runtime refuses
+  // rather than start a grid that cannot be co-resident.  Programmatic
+  // serialization lets the set-up overlap the preceding kernel.
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, moe_small_bf16_kernel, a, r);
 }
 

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "flint_moe.h"
 #include "select.cuh"
 
 namespace flint {
@@ -53,13 +54,15 @@ struct ExpertArgs {
 };
 
 // Largest batch whose routing the expert kernels compute themselves.
-constexpr int LOCAL_SELECT_MAX_B = 8;
+constexpr int LOCAL_SELECT_MAX_B = SMALL_B;
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_bucket(const Ws& ws, int B, const BucketOut& user, cudaStream_t stream);
 cudaError_t launch_gateup_bf16(const ExpertArgs& a, cudaStream_t stream, int num_sms);
 cudaError_t launch_down_bf16(const ExpertArgs& a, cudaStream_t stream);
-// The whole BF16 layer in one persistent cooperative kernel (batch <= 8).
+// The whole BF16 layer in one persistent cooperative kernel (batch <= 8), for
+// grids of num_sms CTAs where small_bf16_supported(num_sms).
+bool small_bf16_supported(int num_sms);
 cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                               int num_sms);
 cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
@@ -67,5 +70,14 @@ cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_
 cudaError_t launch_rmsnorm(const uint16_t* in, uint16_t* out, int B, float eps,
                            cudaStream_t stream);
 cudaError_t launch_ws_init(WsHeader* hdr, uint64_t wait_limit_ns, cudaStream_t stream);
+
+// The host-side argument checks of flint_moe_decode_bf16 (everything but the
+// launch), for entry points that must reject bad arguments before their own
+// set-up.
+flint_status decode_bf16_checks(const flint_moe_dims* dims, int32_t batch, const void* x,
+                                const void* residual, const void* wr, const float* bias,
+                                const void* w13, const void* w2, const void* ws13,
+                                const void* ws2, void* out, int32_t* idx_out, float* w_out,
+                                void* ws, size_t ws_bytes);
 
 }  // namespace flint

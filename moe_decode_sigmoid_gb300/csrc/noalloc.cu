@@ -21,11 +21,17 @@
 
 #include "common.cuh"
 #include "flint_moe.h"
+#include "kernels.h"
 
 namespace {
 
 using flint::WsHeader;
 using flint::WsLayout;
+
+// The device status word is copied out as a flint_status: the codes agree.
+static_assert(flint::DEV_OK == (uint32_t)FLINT_OK, "device and host codes agree");
+static_assert(flint::DEV_BAD_ROUTING == (uint32_t)FLINT_ERR_INVALID_ARG, "device and host codes agree");
+static_assert(flint::DEV_TIMEOUT == (uint32_t)FLINT_ERR_DEVICE_TIMEOUT, "device and host codes agree");
 
 constexpr size_t kScratchBytes = WsLayout::total(FLINT_MOE_NOALLOC_MAX_BATCH);
 
@@ -36,29 +42,39 @@ static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-void* g_scratch_dev[kMaxDevices] = {};  // per device, set once
+void* g_scratch_dev[kMaxDevices] = {};  // per device: the array's address
+bool g_scratch_ready[kMaxDevices] = {};  // per device: header initialised
 
-// Device address of g_scratch on the current device; on the first call for a
-// device, also writes its header (wait limit) and waits for that to finish.
-flint_status scratch_for_current_device(cudaStream_t stream, void** out) {
+// Device address of g_scratch on the current device (a lookup, no GPU work).
+flint_status scratch_address(int* dev_out, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FLINT_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (g_scratch_dev[dev] == nullptr) {
-    // Set-up enqueues work and synchronises `stream`: it must not run while
-    // the stream is being captured.
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return FLINT_ERR_CUDA;
-    if (cs != cudaStreamCaptureStatusNone) return FLINT_ERR_CUDA;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return FLINT_ERR_CUDA;
-    const flint_status st = flint_moe_workspace_init(p, kScratchBytes, 0, stream);
-    if (st != FLINT_OK) return st;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return FLINT_ERR_CUDA;
     g_scratch_dev[dev] = p;
   }
+  *dev_out = dev;
   *out = g_scratch_dev[dev];
+  return FLINT_OK;
+}
+
+// On the first call for a device: zero-fills the array, writes its header
+// (wait limit) and waits for that to finish.
+flint_status scratch_setup(int dev, void* p, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (g_scratch_ready[dev]) return FLINT_OK;
+  // Set-up enqueues work and synchronises `stream`: it must not run while
+  // the stream is being captured.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return FLINT_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return FLINT_ERR_CUDA;
+  const flint_status st = flint_moe_workspace_init(p, kScratchBytes, 0, stream);
+  if (st != FLINT_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FLINT_ERR_CUDA;
+  g_scratch_ready[dev] = true;
   return FLINT_OK;
 }
 
@@ -72,18 +88,27 @@ extern "C" flint_status flint_moe_decode_bf16_noalloc(
   if (batch < 1 || batch > FLINT_MOE_NOALLOC_MAX_BATCH) return FLINT_ERR_INVALID_ARG;
   if (device_status_out != nullptr && (reinterpret_cast<uintptr_t>(device_status_out) & 3u) != 0)
     return FLINT_ERR_INVALID_ARG;
+  int dev = -1;
   void* ws = nullptr;
-  flint_status st = scratch_for_current_device(stream, &ws);
+  flint_status st = scratch_address(&dev, &ws);
+  if (st != FLINT_OK) return st;
+  // Every argument is checked before anything is enqueued.
+  st = flint::decode_bf16_checks(dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias,
+                                 w13_bf16, w2_bf16, ws13_bf16, ws2_bf16, out_bf16, topk_idx_out,
+                                 topk_w_out, ws, kScratchBytes);
+  if (st != FLINT_OK) return st;
+  st = scratch_setup(dev, ws, stream);
   if (st != FLINT_OK) return st;
   // The array keeps whatever the previous call left.  Everything the layer
-  // reads is written earlier in the same call, except the header: its error
-  // word and its counters must start at zero (a call that ran out of time may
-  // have left them set).  Only the wait limit is kept.
+  // reads is written earlier in the same call (the small-batch kernel tells
+  // this call's words from older ones by the header's call counter), except
+  // the header: its error word and counters must start at zero (a call that
+  // ran out of time may have left them set).  The call counter and the wait
+  // limit are kept.
   char* hdr = static_cast<char*>(ws);
-  const size_t lim = offsetof(WsHeader, wait_limit_ns);
-  const size_t after = lim + sizeof(uint64_t);
-  if (cudaMemsetAsync(hdr, 0, lim, stream) != cudaSuccess) return FLINT_ERR_CUDA;
-  if (cudaMemsetAsync(hdr + after, 0, sizeof(WsHeader) - after, stream) != cudaSuccess)
+  if (cudaMemsetAsync(hdr, 0, sizeof(uint32_t), stream) != cudaSuccess) return FLINT_ERR_CUDA;
+  if (cudaMemsetAsync(hdr + flint::WS_HDR_KEEP, 0, sizeof(WsHeader) - flint::WS_HDR_KEEP,
+                      stream) != cudaSuccess)
     return FLINT_ERR_CUDA;
   st = flint_moe_decode_bf16(dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias,
                              w13_bf16, w2_bf16, ws13_bf16, ws2_bf16, out_bf16, topk_idx_out,

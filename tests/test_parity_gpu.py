@@ -129,7 +129,8 @@ def test_bucket_matches_oracle(m, layer, ws, B):
 
 
 DECODE_CASES = [(1, False), (2, False), (3, False), (5, False), (8, False), (13, False),
-                (31, True), (32, True), (77, True), (128, True), (128, False)]
+                (31, True), (32, True), (77, True), (128, True), (128, False), (129, True),
+                (160, True), (200, False), (255, True), (256, True), (256, False)]
 
 
 @pytest.mark.parametrize("B,with_bias", DECODE_CASES)
@@ -314,8 +315,9 @@ def run_nvfp4(m, W, nv, x, res, bias, ws):
     return out, idx, w
 
 
-@pytest.mark.parametrize("B,with_bias", [(1, False), (3, False), (8, False), (13, False),
-                                          (32, True), (128, True)])
+@pytest.mark.parametrize("B,with_bias", [(1, False), (2, False), (3, False), (5, False),
+                                          (8, False), (13, False), (32, True), (128, True),
+                                          (160, True), (200, False), (256, True), (256, False)])
 def test_decode_nvfp4_matches_oracle(m, layer, nv_layer, ws, B, with_bias):
     W, host = layer
     nv, nv_host = nv_layer

@@ -41,7 +41,7 @@ def stack():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("B", [1, 8])
+@pytest.mark.parametrize("B", [1, 8, 32])
 def test_stack_teacher_forced(m, stack, B):
     x0, r0 = fs.tokens(6000 + B, B, device="cuda")
     xs = [x0] + [torch.empty_like(x0) for _ in range(LAYERS)]
