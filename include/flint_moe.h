@@ -29,15 +29,25 @@
  *    bucket outputs) need only 4-byte alignment.  Tensors are dense and
  *    row-major in the shapes written beside each argument.  bf16 tensors are
  *    passed as `const void*` holding IEEE bfloat16 bit patterns.
- *  - The library allocates no device or host memory and keeps no state between
- *    calls.  Scratch lives in a caller-provided workspace (see
- *    flint_moe_workspace_bytes / flint_moe_workspace_init).  Two calls may run
- *    concurrently only with distinct workspaces.
+ *  - The library allocates no device or host memory.  Scratch lives in a
+ *    caller-provided workspace (see flint_moe_workspace_bytes /
+ *    flint_moe_workspace_init), which also keeps a count of the calls made on
+ *    it (the batch <= 8 kernels tell this call's data from older data by it).
+ *    Two calls may run concurrently only with distinct workspaces.  The one
+ *    exception to all of this is flint_moe_decode_bf16_noalloc (below), which
+ *    uses a static device array of the library instead of a workspace.
  *  - Calls validate their arguments on the host and return an error status
  *    BEFORE any launch if anything is wrong; nothing is then written.  On
  *    FLINT_OK, the work has been enqueued on `stream` and nothing has been
- *    synchronised: results are visible after the caller's next sync on that
+ *    synchronised (except in the first flint_moe_decode_bf16_noalloc call on
+ *    a device): results are visible after the caller's next sync on that
  *    stream.  Launch failures reported by the runtime map to FLINT_ERR_CUDA.
+ *  - Batch <= 8 BF16 decode calls run one persistent kernel whose CTAs, one
+ *    per SM, exchange data while they run.  It is launched as a cooperative
+ *    grid, which the runtime starts only when every CTA can be resident at
+ *    once and otherwise refuses (FLINT_ERR_CUDA, e.g. in a context limited to
+ *    fewer SMs).  While it runs it occupies every SM: kernels of other streams
+ *    wait for it, and it waits for them to leave the SMs before it starts.
  *  - Every wait inside a kernel is bounded by a time limit stored in the
  *    workspace.  A kernel that runs out of time records
  *    FLINT_ERR_DEVICE_TIMEOUT in the workspace's error word, waits (bounded)
@@ -63,7 +73,7 @@ extern "C" {
 
 typedef enum {
   FLINT_OK = 0,
-  FLINT_ERR_INVALID_ARG = 1,    /* NULL / misaligned pointer, bad batch, aliasing */
+  FLINT_ERR_INVALID_ARG = 1,    /* NULL / misaligned pointer, bad batch, aliasing, bad input */
   FLINT_ERR_UNSUPPORTED = 2,    /* dims other than the specialised shape */
   FLINT_ERR_WORKSPACE = 3,      /* workspace NULL or smaller than required */
   FLINT_ERR_CUDA = 4,           /* the CUDA runtime reported an error */
@@ -102,7 +112,8 @@ flint_status flint_moe_workspace_init(void* workspace, size_t ws_bytes,
 
 /* Synchronises `stream`, then reads and returns the workspace's device error
  * word: FLINT_OK, FLINT_ERR_DEVICE_TIMEOUT, or FLINT_ERR_INVALID_ARG when
- * flint_moe_bucket was given a routing row that is not k distinct experts. */
+ * flint_moe_bucket was given a routing row that is not k distinct experts or
+ * an NVFP4 call met an activation beyond f16's range. */
 flint_status flint_moe_get_device_status(const void* workspace, cudaStream_t stream);
 
 /* Router only: logits, sigmoid top-k, renormalised weights.
@@ -157,8 +168,9 @@ flint_status flint_moe_bucket(const flint_moe_dims* dims, int32_t batch,
  *                          residual add); no other overlap is allowed
  *   topk_idx_out [batch, k] int32, topk_w_out [batch, k] fp32: optional
  *                          copies of the routing (NULL to skip)
- * Accumulation is fp32; the SiLU-and-mul output is kept in fp32; `out` is
- * rounded to bf16 once. */
+  * Accumulation is fp32 and `out` is rounded to bf16 once.  The SiLU-and-mul
+ * output h is kept in fp32 for batches of <= 8 tokens and as a bf16 pair
+ * hi + lo (about 16 significant bits, the range of fp32) above that. */
 flint_status flint_moe_decode_bf16(const flint_moe_dims* dims, int32_t batch,
                                    const void* x_bf16, const void* residual_bf16,
                                    const void* w_router_bf16, const float* logit_bias,
@@ -198,6 +210,11 @@ flint_status flint_moe_down_bf16(const flint_moe_dims* dims, int32_t batch,
  *   sf  uint8 [rows, K/16]  OCP E4M3FN scale of each block of 16 consecutive k
  *   ts  fp32                one tensor scale per (expert, projection)
  * and dequantises to W[r,k] = e2m1(q) * e4m3(sf[r, k/16]) * ts.
+ * The products e2m1 * e4m3 are exact in f16 and multiply f16 activations on
+ * the tensor cores, so every activation must satisfy |x| < 65504 (an
+ * RMS-normalised x is below sqrt(H) = 45.3): a larger one sets the device
+ * status to FLINT_ERR_INVALID_ARG, and the outputs are undefined.  h is kept
+ * as a bf16 pair hi + lo (the range of fp32). 
  *   w13_q [E, 2I, H/2], w13_sf [E, 2I, H/16], w13_ts [E, 2] (gate, up)
  *   w2_q  [E, H, I/2],  w2_sf  [E, H, I/16],  w2_ts  [E]
  *   ws13_q/ws13_sf/ws13_ts and ws2_q/ws2_sf/ws2_ts: the shared expert(s),

@@ -28,6 +28,7 @@ constexpr int MAX_GROUPS = TOPK * MAX_B / GROUP_MAX + E + S * (MAX_B / GROUP_MAX
 // Device error codes written to the workspace error word.
 constexpr uint32_t DEV_OK = 0;
 constexpr uint32_t DEV_BAD_ROUTING = 1;  // bucketing got an index outside [0,E) or a repeat
+constexpr uint32_t DEV_BAD_INPUT = 1;    // an NVFP4 activation beyond f16's range (|x| >= 65520)
 constexpr uint32_t DEV_TIMEOUT = 5;
 
 // ---- workspace layout ------------------------------------------------------
@@ -38,8 +39,8 @@ constexpr uint32_t DEV_TIMEOUT = 5;
 // The tagged regions belong to the persistent small-batch kernels: each 8-byte
 // word holds a 32-bit value and the call's tag (see call_tag), so a reader on
 // another SM knows from the word itself whether it was written in this call.
-// h holds the BF16 gate/up kernel's bf16 hi + lo pairs (see h_chunk) or the
-// NVFP4 one's values (h_off_nv) of the three-kernel paths.
+// h holds the three-kernel paths' bf16 hi + lo pairs: the BF16 gate/up
+// kernel's (see h_chunk) or the NVFP4 one's (h_off_nv).
 // Every array but the last two is sized for MAX_B (or the small-batch bound),
 // so the offsets do not depend on the batch a workspace was sized for; h and y
 // grow with max_batch, and a call with batch B finds y right after the first
@@ -185,11 +186,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// try_wait that may suspend the thread for up to `ns` nanoseconds; the thread
+// resumes when the phase completes, so a waiting warp leaves its scheduler's
+// issue slots to the warps that compute instead of spinning.
+constexpr uint32_t MBAR_SUSPEND_NS = 0;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return done != 0;
+}
 // Bounded wait for the phase with the given parity; false if the deadline passed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline) {
   if (mbar_try_wait(bar, parity)) return true;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (MBAR_SUSPEND_NS > 0 ? mbar_try_wait_suspend(bar, parity, MBAR_SUSPEND_NS)
+                            : mbar_try_wait(bar, parity))
+      return true;
     if (globaltimer_ns() > deadline) return false;
   }
 }
@@ -295,15 +311,16 @@ __device__ __forceinline__ void store_h_block8(float* h, size_t pair, int blk, f
   }
 }
 
-// The NVFP4 path's h: f16 (11 significant bits, far finer than its 4-bit
-// weights), one 1 KiB row per pair (pair p at byte 1024 p of the h region).
-// The 16-byte block b (columns 8b .. 8b + 7) sits in 64-byte line
-// (b % 16) ^ (p % 2) at slot b / 16 -- the order in which the NVFP4 down
+// The NVFP4 path's h: each value as a bf16 pair hi + lo (as the BF16 path,
+// ~16 significant bits and the range of fp32, so no activation overflows),
+// one 2 KiB row per pair (pair p at byte 2048 p of the h region).  The
+// 32-byte block b (columns 8b .. 8b + 7: 8 hi values, then 8 lo values) sits
+// in 128-byte line b % 16 at slot b / 16 -- the order in which the NVFP4 down
 // kernel's lanes take K (lane q: columns 128q .. 128q + 127, blocks 16q ..
-// 16q + 15 in turn); the line swap by pair parity puts two consecutive rows
-// read at the same step in opposite halves of the 128-byte bank window.
-__host__ __device__ __forceinline__ int h_off_nv(size_t pair, int blk) {
-  return ((blk & 15) ^ (int)(pair & 1)) * 64 + (blk >> 4) * 16;
+// 16q + 15 in turn) -- with the two halves swapped in odd pairs, so that two
+// consecutive rows read at the same step land in opposite 16-byte halves.
+__host__ __device__ __forceinline__ int h_off_nv(size_t pair, int blk, int part) {
+  return (blk & 15) * 128 + (blk >> 4) * 32 + ((part ^ (int)(pair & 1)) * 16);
 }
 
 // One block at once: called by all 32 lanes of a warp, lanes 8m..8m+7
@@ -311,14 +328,20 @@ __host__ __device__ __forceinline__ int h_off_nv(size_t pair, int blk) {
 // stores the block when `store` is true (uniform within the group).
 __device__ __forceinline__ void store_h_block8_nv(float* h, size_t pair, int blk, float v,
                                                   bool store) {
-  const uint32_t hv16 = __half_as_ushort(__float2half_rn(v));
-  const uint32_t w = hv16 | (__shfl_down_sync(0xffffffffu, hv16, 1) << 16);
-  const uint4 hv = make_uint4(w, __shfl_down_sync(0xffffffffu, w, 2),
-                              __shfl_down_sync(0xffffffffu, w, 4),
-                              __shfl_down_sync(0xffffffffu, w, 6));
+  const uint32_t hi = f2bf(v);
+  const uint32_t lo = f2bf(v - bf_lo(hi));
+  const uint32_t hw = hi | (__shfl_down_sync(0xffffffffu, hi, 1) << 16);
+  const uint32_t lw = lo | (__shfl_down_sync(0xffffffffu, lo, 1) << 16);
+  const uint4 hv = make_uint4(hw, __shfl_down_sync(0xffffffffu, hw, 2),
+                              __shfl_down_sync(0xffffffffu, hw, 4),
+                              __shfl_down_sync(0xffffffffu, hw, 6));
+  const uint4 lv = make_uint4(lw, __shfl_down_sync(0xffffffffu, lw, 2),
+                              __shfl_down_sync(0xffffffffu, lw, 4),
+                              __shfl_down_sync(0xffffffffu, lw, 6));
   if ((threadIdx.x & 7) == 0 && store) {
-    uint8_t* row = reinterpret_cast<uint8_t*>(h) + pair * (I * 2);
-    *reinterpret_cast<uint4*>(row + h_off_nv(pair, blk)) = hv;
+    uint8_t* row = reinterpret_cast<uint8_t*>(h) + pair * (I * 4);
+    *reinterpret_cast<uint4*>(row + h_off_nv(pair, blk, 0)) = hv;
+    *reinterpret_cast<uint4*>(row + h_off_nv(pair, blk, 1)) = lv;
   }
 }
 
@@ -359,8 +382,11 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 // reader (a GPU-scope fence waits for the SM's outstanding memory traffic and
 // costs microseconds while weight copies stream).  The tag is derived from the
 // workspace's call counter (epoch, taken modulo 2^31) and never equals a
-// zero-filled word.  Counters that announce completion are only hints: the
-// reader confirms every word's tag and re-reads the ones that have not landed.
+// zero-filled word; every call stamps all words of the tagged regions (the
+// ones it does not use with a dead value), so a stale word always carries the
+// previous call's tag, which differs from the current one.  Counters that
+// announce completion are only hints: the reader confirms every word's tag and
+// re-reads the ones that have not landed.
 __host__ __device__ __forceinline__ uint32_t call_tag(uint32_t epoch) {
   return 0x80000000u | (epoch & 0x7fffffffu);
 }

@@ -76,6 +76,7 @@ constexpr int DOWN_CTAS = H / RS;              // 128 row-slice owners
 constexpr int WROW = I * 2;                    // one Wd row (bf16)
 constexpr int WBYTES = RS * WROW;              // 16 KiB
 constexpr int THROW = I * 8;                   // one tagged h row, 4 KiB
+constexpr int FROW = I * 4;                    // one staged fp32 h row, 2 KiB
 constexpr int HROWS_A = (SLOT - WBYTES) / THROW;  // h rows beside the Wd slice: 4
 constexpr int CC_MAX = 4;                      // down items on CUDA cores up to this many tokens
 constexpr int XS_BYTES = MAXB * H * 2;         // bf16 activations of the batch, 32 KiB
@@ -97,6 +98,7 @@ static_assert(S == 1 && MAXB <= GROUP_MAX, "one shared group at these batches");
 static_assert(MAXG <= DONE_SHARED, "routed groups and the shared group have distinct counters");
 static_assert(SYNC_LINES <= CT, "one thread clears each counter line");
 static_assert(HROWS_A == 4 && MAXB - HROWS_A <= SLOT / THROW, "a down item fits two slots");
+static_assert(WBYTES + MAXB * FROW <= SLOT, "the staged fp32 rows fit the first slot");
 static_assert(8 * ROWB == SLOT, "8 gate (or up) rows fill one slot");
 static_assert((E + RMAX - 1) / RMAX <= 86, "grids of 86 CTAs or more keep <= RMAX router rows");
 static_assert(SMEM + 6 * 1024 <= 232448, "fits the opt-in shared memory of one SM");
@@ -333,25 +335,51 @@ struct DnCtx {
   volatile int* abort_flag;
 };
 
-// h value k of a token's row (copy in shared memory at hrow, the tagged row
-// itself at src), confirmed against the call's tag.
-__device__ __forceinline__ float h_settled(const DnCtx& c, const uint8_t* hrow,
-                                           const uint64_t* src, int k) {
-  uint64_t w = *reinterpret_cast<const uint64_t*>(hrow + (size_t)k * 8);
-  if (!settle_tagged(w, src + k, c.tag, c.deadline)) {
-    *c.abort_flag = 1;
-    set_error(c.hdr, DEV_TIMEOUT);
+// Stages a down item's tagged h rows as plain fp32 rows, row j at
+// sa + WBYTES + j * FROW (rows 0..3 arrived beside the Wd slice in slot sa,
+// rows 4.. in slot sb), confirming every word's tag -- a word that has not
+// landed is re-read from global memory until it has (rare: the counters run
+// behind the stores).  Run by all consumer threads: one 16-byte load per
+// thread and row, then the writes once every thread has read.
+__device__ __forceinline__ void stage_h(const DnCtx& c, uint8_t* sa, const uint8_t* sb, int pair0,
+                                        int n) {
+  const int tid = threadIdx.x;
+  uint4 w[fz::MAXB];
+#pragma unroll
+  for (int j = 0; j < fz::MAXB; ++j) {
+    if (j < n) {
+      const uint8_t* row = j < fz::HROWS_A ? sa + fz::WBYTES + j * fz::THROW
+                                           : sb + (j - fz::HROWS_A) * fz::THROW;
+      w[j] = *reinterpret_cast<const uint4*>(row + 16 * tid);
+    }
   }
-  return __uint_as_float((uint32_t)w);
+  named_sync(1, fz::CT);  // every tagged word is read before the fp32 rows overwrite them
+#pragma unroll
+  for (int j = 0; j < fz::MAXB; ++j) {
+    if (j < n) {
+      uint64_t a = ((uint64_t)w[j].y << 32) | w[j].x;
+      uint64_t b = ((uint64_t)w[j].w << 32) | w[j].z;
+      if ((w[j].y != c.tag) | (w[j].w != c.tag)) {
+        const uint64_t* src = c.th + (size_t)(pair0 + j) * I + 2 * tid;
+        const bool ga = settle_tagged(a, src, c.tag, c.deadline);
+        const bool gb = settle_tagged(b, src + 1, c.tag, c.deadline);
+        if (!(ga && gb)) {
+          *c.abort_flag = 1;
+          set_error(c.hdr, DEV_TIMEOUT);
+        }
+      }
+      *reinterpret_cast<float2*>(sa + fz::WBYTES + j * fz::FROW + 8 * tid) =
+          make_float2(__uint_as_float((uint32_t)a), __uint_as_float((uint32_t)b));
+    }
+  }
+  named_sync(1, fz::CT);
 }
 
 // Down item on CUDA cores (<= 4 tokens): warp w owns Wd rows 2w and 2w+1 of
-// the slice; lane l takes columns 2l + 64m (+1), m < 8.  The lane's 32 weights
-// are unpacked once and reused by every token; each lane adds w(t, g) times
-// its partial dot product to its own running sum in shared memory -- the sums
-// across lanes are taken once, when the output is written.  A word whose tag
-// has not landed sends the warp through the same arithmetic with every value
-// confirmed from global memory (rare: the counters run behind the stores).
+// the slice; lane l takes columns 4l + 128m (.. +3), m < 4.  The lane's 32
+// weights are unpacked once and reused by every token; each lane adds
+// w(t, g) times its partial dot product to its own running sum in shared
+// memory -- the sums across lanes are taken once, when the output is written.
 __device__ __forceinline__ void down_cc(const DnCtx& c, const uint8_t* st, int pair0, int n,
                                         bool ok, uint32_t em) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -359,57 +387,38 @@ __device__ __forceinline__ void down_cc(const DnCtx& c, const uint8_t* st, int p
 #pragma unroll
   for (int i = 0; i < fz::CC_MAX; ++i) s0[i] = s1[i] = 0.f;
   if (ok) {
-    const uint32_t* w0 = reinterpret_cast<const uint32_t*>(st + (2 * warp) * fz::WROW);
-    const uint32_t* w1 = w0 + fz::WROW / 4;
+    const uint8_t* w0 = st + (2 * warp) * fz::WROW;
+    const uint8_t* w1 = w0 + fz::WROW;
     float f0[16], f1[16];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const uint32_t a0 = w0[lane + 32 * m], a1 = w1[lane + 32 * m];
-      f0[2 * m] = bf_lo(a0);
-      f0[2 * m + 1] = bf_hi(a0);
-      f1[2 * m] = bf_lo(a1);
-      f1[2 * m + 1] = bf_hi(a1);
+    for (int m = 0; m < 4; ++m) {
+      const uint2 a0 = *reinterpret_cast<const uint2*>(w0 + (4 * lane + 128 * m) * 2);
+      const uint2 a1 = *reinterpret_cast<const uint2*>(w1 + (4 * lane + 128 * m) * 2);
+      f0[4 * m] = bf_lo(a0.x);
+      f0[4 * m + 1] = bf_hi(a0.x);
+      f0[4 * m + 2] = bf_lo(a0.y);
+      f0[4 * m + 3] = bf_hi(a0.y);
+      f1[4 * m] = bf_lo(a1.x);
+      f1[4 * m + 1] = bf_hi(a1.x);
+      f1[4 * m + 2] = bf_lo(a1.y);
+      f1[4 * m + 3] = bf_hi(a1.y);
     }
-    bool bad = false;
 #pragma unroll
     for (int i = 0; i < fz::CC_MAX; ++i) {
       if (i < n) {
-        const uint4* hr = reinterpret_cast<const uint4*>(st + fz::WBYTES + i * fz::THROW);
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const uint4 hv = hr[lane + 32 * m];
-          bad |= (hv.y != c.tag) | (hv.w != c.tag);
-          const float h0 = __uint_as_float(hv.x), h1 = __uint_as_float(hv.z);
-          s0[i] = fmaf(f0[2 * m], h0, s0[i]);
-          s0[i] = fmaf(f0[2 * m + 1], h1, s0[i]);
-          s1[i] = fmaf(f1[2 * m], h0, s1[i]);
-          s1[i] = fmaf(f1[2 * m + 1], h1, s1[i]);
+        for (int m = 0; m < 4; ++m) {
+          const float4 hv = *reinterpret_cast<const float4*>(st + fz::WBYTES + i * fz::FROW +
+                                                             (4 * lane + 128 * m) * 4);
+          s0[i] = fmaf(f0[4 * m], hv.x, s0[i]);
+          s0[i] = fmaf(f0[4 * m + 1], hv.y, s0[i]);
+          s0[i] = fmaf(f0[4 * m + 2], hv.z, s0[i]);
+          s0[i] = fmaf(f0[4 * m + 3], hv.w, s0[i]);
+          s1[i] = fmaf(f1[4 * m], hv.x, s1[i]);
+          s1[i] = fmaf(f1[4 * m + 1], hv.y, s1[i]);
+          s1[i] = fmaf(f1[4 * m + 2], hv.z, s1[i]);
+          s1[i] = fmaf(f1[4 * m + 3], hv.w, s1[i]);
         }
-      }
-    }
-    if (__any_sync(0xffffffffu, bad)) {
-      // Same sums, same order; weights re-read from the slot so that no
-      // register array is indexed at run time.
-#pragma unroll
-      for (int i = 0; i < fz::CC_MAX; ++i) {
-        float a0 = 0.f, a1 = 0.f;
-        if (i < n) {
-          const uint8_t* hrow = st + fz::WBYTES + i * fz::THROW;
-          const uint64_t* src = c.th + (size_t)(pair0 + i) * I;
-#pragma unroll 1
-          for (int m = 0; m < 8; ++m) {
-            const int k = 2 * lane + 64 * m;
-            const uint32_t u0 = w0[lane + 32 * m], u1 = w1[lane + 32 * m];
-            const float h0 = h_settled(c, hrow, src, k);
-            const float h1 = h_settled(c, hrow, src, k + 1);
-            a0 = fmaf(bf_lo(u0), h0, a0);
-            a0 = fmaf(bf_hi(u0), h1, a0);
-            a1 = fmaf(bf_lo(u1), h0, a1);
-            a1 = fmaf(bf_hi(u1), h1, a1);
-          }
-        }
-        s0[i] = a0;
-        s1[i] = a1;
       }
     }
   }
@@ -427,49 +436,32 @@ __device__ __forceinline__ void down_cc(const DnCtx& c, const uint8_t* st, int p
   }
 }
 
-// Down item on tensor cores (5..8 tokens, h rows 0..3 beside the Wd slice in
-// slot A, rows 4.. in slot B): mma.sync m16n8k16 with the 16 Wd rows as M and
-// the tokens as N; the fp32 h is split into two bf16 parts (hi + lo, two
-// MMAs) so the operand keeps ~16 significant bits; warp w owns a 64-column
-// K-slice; the 8 partial tiles are summed through shared memory and weighted
-// into the CTA's accumulators.
-__device__ __forceinline__ void down_mma(const DnCtx& c, const uint8_t* sa, const uint8_t* sb,
-                                         int pair0, int n, bool ok) {
+// Down item on tensor cores (5..8 tokens, staged h rows in slot sa):
+// mma.sync m16n8k16 with the 16 Wd rows as M and the tokens as N; the fp32 h
+// is split into two bf16 parts (hi + lo, two MMAs) so the operand keeps ~16
+// significant bits; warp w owns a 64-column K-slice; the 8 partial tiles are
+// summed through shared memory and weighted into the CTA's accumulators.
+__device__ __forceinline__ void down_mma(const DnCtx& c, const uint8_t* sa, int pair0, int n,
+                                         bool ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   const uint8_t* rlo = sa + g * fz::WROW + (warp * 64 + q * 8) * 2;
   const uint8_t* rhi = rlo + 8 * fz::WROW;
-  const uint8_t* hrow = g < fz::HROWS_A ? sa + fz::WBYTES + g * fz::THROW
-                                        : sb + (g - fz::HROWS_A) * fz::THROW;
+  const uint8_t* hs = sa + fz::WBYTES + (warp * 64 + q * 8) * 4;
   if (ok) {
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
       const uint4 alo = *reinterpret_cast<const uint4*>(rlo + kb * 64);
       const uint4 ahi = *reinterpret_cast<const uint4*>(rhi + kb * 64);
-      // h (fp32) = hi + lo with both parts bf16: two MMAs keep ~16 bits of h.
       uint32_t b[4] = {0u, 0u, 0u, 0u}, l[4] = {0u, 0u, 0u, 0u};
       if (g < n) {
-        const int k0 = warp * 64 + kb * 32 + q * 8;
-        float hv[8];
-        bool bad = false;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 w = *reinterpret_cast<const uint4*>(hrow + (size_t)(k0 + 2 * j) * 8);
-          bad |= (w.y != c.tag) | (w.w != c.tag);
-          hv[2 * j] = __uint_as_float(w.x);
-          hv[2 * j + 1] = __uint_as_float(w.z);
-        }
-        if (bad) {
-          const uint64_t* src = c.th + (size_t)(pair0 + g) * I;
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            hv[j] = h_settled(c, hrow, src, k0 + j);
-        }
-        split_bf2(hv[0], hv[1], b[0], l[0]);
-        split_bf2(hv[2], hv[3], b[1], l[1]);
-        split_bf2(hv[4], hv[5], b[2], l[2]);
-        split_bf2(hv[6], hv[7], b[3], l[3]);
+        const float4 h0 = *reinterpret_cast<const float4*>(hs + g * fz::FROW + kb * 128);
+        const float4 h1 = *reinterpret_cast<const float4*>(hs + g * fz::FROW + kb * 128 + 16);
+        split_bf2(h0.x, h0.y, b[0], l[0]);
+        split_bf2(h0.z, h0.w, b[1], l[1]);
+        split_bf2(h1.x, h1.y, b[2], l[2]);
+        split_bf2(h1.z, h1.w, b[3], l[3]);
       }
       mma_bf16(acc, alo.x, ahi.x, alo.y, ahi.y, b[0], b[1]);
       mma_bf16(acc, alo.z, ahi.z, alo.w, ahi.w, b[2], b[3]);
@@ -856,6 +848,15 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     for (int t = 0; t < fz::MAXB; ++t)
       if (t < B) reinterpret_cast<uint4*>(xs)[t * (H / 8) + tid] = v[t];
   }
+  // Every word of the tagged regions carries this call's tag or the previous
+  // call's: the rows this call does not use (tokens >= B) are stamped now with
+  // a dead value, so a later call never meets a word older than one call.
+  {
+    const int gid = cta * fz::CT + tid, nthr = G * fz::CT;
+    const int h_used = B * SLOTS * I, h_all = fz::MAXB * SLOTS * I;
+    for (int i = h_used + gid; i < h_all; i += nthr) st_tagged(a.ws.th + i, 0.f, tag);
+    for (int i = B * E + gid; i < fz::MAXB * E; i += nthr) st_tagged(a.ws.tlogits + i, 0.f, tag);
+  }
   named_sync(1, fz::CT);
   if (!mbar_wait(rrow_bar, 0u, deadline)) {
     s_abort = 1;
@@ -953,9 +954,10 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     const int slot2 = (it + 1) % fz::NS;
     const uint32_t ph2 = (uint32_t)((it + 1) / fz::NS) & 1u;
     if (d.kind == fz::IT_DOWN) {
-      const uint8_t* st = ring + slot * fz::SLOT;
-      if (d.n <= fz::CC_MAX) {
-        down_cc(dc, st, d.pair0, d.n, ok, empty0 + 8u * slot);
+      uint8_t* st = ring + slot * fz::SLOT;
+      if (d.n <= fz::HROWS_A) {
+        stage_h(dc, st, st, d.pair0, d.n);
+        down_cc(dc, st, d.pair0, d.n, ok && !s_abort, empty0 + 8u * slot);
         ++it;
         continue;
       }
@@ -967,7 +969,8 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
         if (!mbar_wait(full0 + 8u * slot2, ph2, drain)) break;
       }
       if (s_desc[slot2].kind != fz::IT_DOWN2) break;  // the producer gave up mid-item (abort)
-      down_mma(dc, st, ring + slot2 * fz::SLOT, d.pair0, d.n, ok2);
+      stage_h(dc, st, ring + slot2 * fz::SLOT, d.pair0, d.n);
+      down_mma(dc, st, d.pair0, d.n, ok2 && !s_abort);
       release_slot(empty0 + 8u * slot);
       release_slot(empty0 + 8u * slot2);
       it += 2;

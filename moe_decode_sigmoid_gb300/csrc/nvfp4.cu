@@ -12,9 +12,11 @@
 // [2^-10, 2688], so it is EXACT in f16: each thread converts its fragment's
 // codes with cvt.rn.f16x2.e2m1x2, multiplies by the block scale (f16x2, exact)
 // and feeds mma.sync m16n8k16 f16 x f16 -> fp32.  bf16 activations convert to
-// f16 exactly (8 significant bits; |x| inside f16's normal range); h is
-// stored in f16 (11 significant bits, against 4-bit weights); the tensor scale
-// is applied to the fp32 sums.  Dequantisation costs about one instruction per weight, which is
+// f16 exactly (8 significant bits; |x| inside f16's normal range); the tensor
+// scale is applied to the fp32 sums.  h is stored as a bf16 pair hi + lo (the
+// range of fp32), so the down kernel converts its dequantised weights to bf16
+// -- still exact, the same value in fewer exponent-limited bits -- and runs
+// bf16 MMAs on both halves.  Dequantisation costs about one instruction per weight, which is
 // why this path uses the tensor cores for every group, including single-token
 // ones: the FMAs then cost nothing on the CUDA cores that do the unpacking.
 //
@@ -82,9 +84,29 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   return r;
 }
 
+// f16x2 -> bf16x2, exact for the dequantised weights (<= 6 significant bits,
+// inside bf16's range): each half through fp32.
+__device__ __forceinline__ uint32_t bf2_of_h2(uint32_t h2) {
+  const __half2 v = *reinterpret_cast<const __half2*>(&h2);
+  const float2 f = __half22float2(v);
+  return pack_bf2(f.x, f.y);
+}
+
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// True if one of 8 bf16 values (uint4) is beyond f16's range: |x| >= 2^16
+// (bf16 magnitude bits >= 0x4780), an infinity or a NaN.  The conversion
+// below would make it an f16 infinity.
+__device__ __forceinline__ bool bf16x8_beyond_f16(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  bool out = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    out |= (w[i] & 0x7fffu) >= 0x4780u || ((w[i] >> 16) & 0x7fffu) >= 0x4780u;
+  return out;
 }
 
 // bf16 x 8 (uint4) -> f16 x 8 (uint4), same element order.
@@ -196,9 +218,16 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, c
       const int tok = pair_tok[pair0 + slot];
       const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)tok * H + warp * 256 + q * 32);
 #pragma unroll
+      bool big = false;
+#pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) bfr[nt][m][i] = bf16x8_to_f16x8(__ldg(row + m * 16 + i));
+        for (int i = 0; i < 4; ++i) {
+          const uint4 xv = __ldg(row + m * 16 + i);
+          big |= bf16x8_beyond_f16(xv);
+          bfr[nt][m][i] = bf16x8_to_f16x8(xv);
+        }
+      if (big) set_error(a.ws.hdr, DEV_BAD_INPUT);  // the activations run as f16 here
     } else {
 #pragma unroll
       for (int m = 0; m < 2; ++m)
@@ -418,7 +447,7 @@ constexpr int DN_QROW = I / 2;                  // code bytes per row
 constexpr int DN_SFROW = I / 16;                // scale bytes per row
 constexpr int DN_QB = DN_RB * DN_QROW;          // 32 KiB
 constexpr int DN_SB = DN_RB * DN_SFROW;         // 4 KiB
-constexpr int DN_HROW = I * 2;                  // one f16 h row
+constexpr int DN_HROW = I * 4;                  // one h row (bf16 hi + lo pairs)
 constexpr int DN_MAX_STAGES = 4;
 constexpr int SMEM_CAP = 232448 - 1024;
 static_assert(DN_UNITS <= 16, "one ticket per row block in the header");
@@ -476,8 +505,8 @@ __device__ __forceinline__ void dn_unit(const ExpertArgs& a, const uint8_t* st, 
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int slot = nt * 8 + g < n ? nt * 8 + g : 0;
-    hrow[nt] = st + f4::DN_QB + f4::DN_SB + slot * f4::DN_HROW;
-    hx[nt] = (pair0 + slot) & 1;
+    hrow[nt] = st + f4::DN_QB + f4::DN_SB + slot * f4::DN_HROW + q * 32;
+    hx[nt] = ((pair0 + slot) & 1) * 16;
   }
   float acc[NT][2][4];  // [tile][even, odd step][fragment]
 #pragma unroll
@@ -497,14 +526,20 @@ __device__ __forceinline__ void dn_unit(const ExpertArgs& a, const uint8_t* st, 
     uint32_t l0, l1, l2, l3, u0, u1, u2, u3;
     e2m1x8_to_f16x2(w0, l0, l1, l2, l3);
     e2m1x8_to_f16x2(w1, u0, u1, u2, u3);
-    l0 = hmul2(l0, sc0); l1 = hmul2(l1, sc0); l2 = hmul2(l2, sc0); l3 = hmul2(l3, sc0);
-    u0 = hmul2(u0, sc1); u1 = hmul2(u1, sc1); u2 = hmul2(u2, sc1); u3 = hmul2(u3, sc1);
+    l0 = bf2_of_h2(hmul2(l0, sc0)); l1 = bf2_of_h2(hmul2(l1, sc0));
+    l2 = bf2_of_h2(hmul2(l2, sc0)); l3 = bf2_of_h2(hmul2(l3, sc0));
+    u0 = bf2_of_h2(hmul2(u0, sc1)); u1 = bf2_of_h2(hmul2(u1, sc1));
+    u2 = bf2_of_h2(hmul2(u2, sc1)); u3 = bf2_of_h2(hmul2(u3, sc1));
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      // block 16q + j of the token's row (h_off_nv)
-      const uint4 hb = *reinterpret_cast<const uint4*>(hrow[nt] + ((j ^ hx[nt]) * 64) + q * 16);
-      mma_f16(acc[nt][0], l0, u0, l1, u1, hb.x, hb.y);
-      mma_f16(acc[nt][1], l2, u2, l3, u3, hb.z, hb.w);
+      // block 16q + j of the token's row (h_off_nv): hi and lo halves
+      const uint8_t* hb8 = hrow[nt] + j * 128;
+      const uint4 hh = *reinterpret_cast<const uint4*>(hb8 + hx[nt]);
+      const uint4 hl = *reinterpret_cast<const uint4*>(hb8 + (16 - hx[nt]));
+      mma_bf16(acc[nt][0], l0, u0, l1, u1, hh.x, hh.y);
+      mma_bf16(acc[nt][1], l2, u2, l3, u3, hh.z, hh.w);
+      mma_bf16(acc[nt][0], l0, u0, l1, u1, hl.x, hl.y);
+      mma_bf16(acc[nt][1], l2, u2, l3, u3, hl.z, hl.w);
     }
   }
   const float ts = expert < E ? __ldg(a.w.w2_ts + expert) : __ldg(a.w.ws2_ts + (expert - E));

@@ -401,3 +401,76 @@ def test_stage_calls_match_oracle(m, layer, ws, B):
         out_d, idx_d, _ = run_decode(m, W, x, res, bias, ws)
         assert torch.equal(idx_d, idx)
         assert torch.equal(out_d.view(torch.int16), out.view(torch.int16))
+
+
+@pytest.mark.parametrize("B", [3, 8, 13, 40])
+def test_large_h_beyond_f16_range_matches_oracle(m, layer, nv_layer, ws, B):
+    """Gate and up scaled by 256 (a power of two, so the NVFP4 codes and the
+    bf16 weights stay exact): g and u grow 256x and h ~65536x, far beyond
+    f16's 65504, on both formats, at batches of both the fused and the
+    three-kernel path.  The outputs must still match the oracle."""
+    W, host = layer
+    nv, nv_host = nv_layer
+    x, res = fs.tokens(4600 + B, B, device="cuda")
+    # BF16: w13 x 256 (exact in bf16)
+    Wb = dict(W)
+    Wb["w13"] = (W["w13"].float() * 256.0).to(torch.bfloat16)
+    Wb["ws13"] = (W["ws13"].float() * 256.0).to(torch.bfloat16)
+    out, idx, w = run_decode(m, Wb, x, res, None, ws)
+    hostb = dict(host)
+    hostb["w13"] = Wb["w13"].cpu()
+    hostb["ws13"] = Wb["ws13"].cpu()
+    gi, w_ref = check_routing(host, x, None, idx, w)
+    ref = oracle.moe_bf16_given_routing(D, x.cpu(), res.cpu(), gi, w_ref, hostb["w13"], hostb["w2"],
+                                        hostb["ws13"], hostb["ws2"])
+    assert np.max(np.abs(ref - bf16_bits_to_f64(res))) > 1e3   # the delta really is large
+    got = bf16_bits_to_f64(out)
+    assert rel_err(got, ref) <= REL_TOL
+    assert rel_err_delta(got, ref, bf16_bits_to_f64(res)) <= REL_TOL
+    # NVFP4: tensor scales of gate and up x 256
+    nvb = dict(nv)
+    nvb["w13_ts"] = nv["w13_ts"] * 256.0
+    nvb["ws13_ts"] = nv["ws13_ts"] * 256.0
+    nvh = {k: v.cpu() for k, v in nvb.items()}
+    out4, idx4, w4 = run_nvfp4(m, W, nvb, x, res, None, ws)
+    gi4, w_ref4 = check_routing(host, x, None, idx4, w4)
+    ref4 = oracle.moe_nvfp4_given_routing(D, x.cpu(), res.cpu(), gi4, w_ref4, nvh)
+    got4 = bf16_bits_to_f64(out4)
+    assert rel_err(got4, ref4) <= REL_TOL
+    assert rel_err_delta(got4, ref4, bf16_bits_to_f64(res)) <= REL_TOL
+
+
+def test_nvfp4_reports_activations_beyond_f16(m, layer, nv_layer):
+    """The NVFP4 path multiplies f16 activations: a value beyond f16's range
+    makes the call report FLINT_ERR_INVALID_ARG on the device instead of
+    returning infinities; after re-initialisation the workspace works again."""
+    W, host = layer
+    nv, nv_host = nv_layer
+    B = 13
+    ws = m.new_workspace(B)
+    x, res = fs.tokens(4700, B, device="cuda")
+    xb = x.clone()
+    xb[5, 100] = 70000.0
+    out = torch.empty_like(res)
+    m.flint_moe_decode_nvfp4_w4a16(xb, res, W["wr"], None, nv, out, ws)
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_ERR_INVALID_ARG
+    m.flint_moe_workspace_init(ws)
+    out, idx, w = run_nvfp4(m, W, nv, x, res, None, ws)
+    gi, w_ref = check_routing(host, x, None, idx, w)
+    ref = oracle.moe_nvfp4_given_routing(D, x.cpu(), res.cpu(), gi, w_ref, nv_host)
+    assert rel_err(bf16_bits_to_f64(out), ref) <= REL_TOL
+
+
+def test_calls_of_mixed_batches_on_one_workspace_match_fresh_workspaces(m, layer):
+    """The batch <= 8 kernel tells this call's exchanged data from older data
+    by a call tag; calls of different batches (and of the three-kernel path)
+    on one workspace must give exactly what a fresh workspace gives."""
+    W, _ = layer
+    shared = m.new_workspace(16)
+    for i, B in enumerate([8, 1, 8, 3, 13, 8, 1, 1, 5, 8]):
+        x, res = fs.tokens(4800 + i, B, device="cuda")
+        out_s, idx_s, w_s = run_decode(m, W, x, res, None, shared)
+        out_f, idx_f, w_f = run_decode(m, W, x, res, None, m.new_workspace(B))
+        assert torch.equal(idx_s, idx_f), (i, B)
+        assert torch.equal(w_s, w_f), (i, B)
+        assert torch.equal(out_s.view(torch.int16), out_f.view(torch.int16)), (i, B)
