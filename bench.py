@@ -456,12 +456,14 @@ def extras(m, cold, stream, args):
 
 
 def nvfp4_configs(m, cold, stream, steps, warmup):
-    """NVFP4 W4A16 layer at batch 1 and 8 (weights packed from each bf16 copy)."""
+    """NVFP4 W4A16 layer at batch 1 and 8, and at 32 and 128 with skewed
+    routing (weights packed from each bf16 copy)."""
     nvs = [fs.nvfp4_layer(W) for W in cold.Ws]
     torch.cuda.synchronize()
     out = {}
-    for B in (1, 8):
+    for B, bias_on in ((1, False), (8, False), (32, True), (128, True)):
         x, res = fs.tokens(TOKEN_SEED + B, B, device=x_device(cold))
+        bias = fs.logit_offsets(OFFSET_SEED, device=x_device(cold)) if bias_on else None
         o = torch.empty_like(res)
         idx = torch.empty((B, 6), dtype=torch.int32, device=x.device)
         ws = m.new_workspace(B, device=x.device)
@@ -469,7 +471,7 @@ def nvfp4_configs(m, cold, stream, steps, warmup):
         with torch.cuda.stream(stream):
             for i, (W, nv) in enumerate(zip(cold.Ws, nvs)):
                 call = (lambda W=W, nv=nv: m.flint_moe_decode_nvfp4_w4a16(
-                    x, res, W["wr"], None, nv, o, ws, idx, None, stream=stream))
+                    x, res, W["wr"], bias, nv, o, ws, idx, None, stream=stream))
                 call()
                 stream.synchronize()
                 g = torch.cuda.CUDAGraph()
@@ -482,7 +484,8 @@ def nvfp4_configs(m, cold, stream, steps, warmup):
                                   stream)
         st = stats_us(times)
         nb = needed_bytes_nvfp4(U)
-        out["nvfp4_b%d" % B] = {"us": round(st["mean"], 3), "p50_us": round(st["p50"], 3),
+        out["nvfp4_b%d%s" % (B, "_skew" if bias_on else "")] = {
+                                "us": round(st["mean"], 3), "p50_us": round(st["p50"], 3),
                                 "unique_experts": U, "needed_bytes": nb,
                                 "gbs": round(nb / (st["mean"] * 1e-6) / 1e9, 1)}
     del nvs
@@ -541,7 +544,9 @@ def stack_configs(m, stream, warmup, steps=20):
         out["stack47_b%d" % B] = {"us_per_step": round(st["mean"], 2), "p50_us": round(st["p50"], 2),
                                   "needed_bytes": nb, "gbs": round(nb / (st["mean"] * 1e-6) / 1e9, 1),
                                   "us_per_layer": round(st["mean"] / STACK_LAYERS, 3),
-                                  "gpu_launches_per_step": 4 * STACK_LAYERS}
+                                  # per layer: the layer's launches + the RMSNorm
+                                  "gpu_launches_per_step":
+                                      ((1 if B <= SMALL_BATCH_MAX else 3) + 1) * STACK_LAYERS}
         del g
     del layers
     torch.cuda.empty_cache()
@@ -575,9 +580,10 @@ def recorded_traffic(kernel: str, batch: int):
 
 
 def run_reference(args, world, rank):
-    """The comparison arm: the fp64 CPU oracle on the host cores, same workload.
-    Each step is a bounded sample: one token of the batch-B layer (its six
-    routed experts, the shared expert and the router)."""
+    """The comparison arm: the fp64 CPU oracle on the host cores, on the same
+    workload as the GPU arm -- each step is the whole batch-B layer (router,
+    selection, the selected and shared experts, combine), the computation the
+    cpu_baseline of the GPU arm times, with OpenMP over the host's threads."""
     if rank != 0:
         return
     import oracle
@@ -585,12 +591,12 @@ def run_reference(args, world, rank):
     W = fs.layer_weights(LAYER_SEED, fs.FULL, device="cpu")
     x, res = fs.tokens(TOKEN_SEED + B, B, device="cpu")
     threads = oracle.max_threads()
+    state = {}
 
     def step(i):
-        t = i % B
-        out, idx, _ = oracle.moe_bf16(fs.FULL, x[t:t + 1], res[t:t + 1], W["wr"], None, W["w13"],
-                                      W["w2"], W["ws13"], W["ws2"], nthreads=1)
-        return idx
+        out, idx, _ = oracle.moe_bf16(fs.FULL, x, res, W["wr"], None, W["w13"], W["w2"],
+                                      W["ws13"], W["ws2"], nthreads=threads)
+        state["idx"] = idx
 
     for i in range(args.warmup):
         step(i)
@@ -599,18 +605,22 @@ def run_reference(args, world, rank):
         step(i)
     wall = time.perf_counter() - t0
     per = wall / args.steps
-    nb = needed_bytes_bf16(6)   # one token: its 6 routed experts + shared + router
+    U = len(set(state["idx"].reshape(-1).tolist()))
+    nb = needed_bytes_bf16(U)
     value = nb / per / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(per * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "one BF16 Flint MoE decode layer, batch %d (one token per step)"
-                               % B, "batch": B},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "one token of the batch-%d layer per step (fp64 C oracle, "
-                                   "selected experts only, single thread; host has %d threads)"
+        "config": {"workload": "one BF16 Flint MoE decode layer, batch %d: hidden 2048, 256 routed "
+                               "experts sigmoid top-6 + 1 shared, intermediate 512, N(0,0.02) "
+                               "weights, unit-RMS N(0,1) tokens" % B,
+                   "batch": B, "unique_experts": U, "needed_bytes": nb},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "the whole batch-%d layer per step (fp64 C oracle, selected "
+                                   "experts only, OpenMP over tokens on %d host threads)"
                                    % (B, threads)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
