@@ -36,6 +36,7 @@ class Dims:
     top_k: int = 6
     inter: int = 512
     n_shared: int = 1
+    offset_mode: int = 0   # 0: logit offsets move ranking and weights; 1: ranking only
 
 
 FULL = Dims()

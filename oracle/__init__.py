@@ -25,7 +25,7 @@ _I = ctypes.c_int
 class _Dims(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32),
-                ("n_shared", ctypes.c_int32)]
+                ("n_shared", ctypes.c_int32), ("offset_mode", ctypes.c_int32)]
 
 
 def load(path: str) -> ctypes.CDLL:
@@ -90,7 +90,8 @@ def _ptr(a):
 
 
 def _dims(d):
-    return _Dims(d.hidden, d.n_experts, d.top_k, d.inter, d.n_shared)
+    return _Dims(d.hidden, d.n_experts, d.top_k, d.inter, d.n_shared,
+                 getattr(d, "offset_mode", 0))
 
 
 def e2m1(code: int) -> float:

@@ -25,16 +25,19 @@ def bf16_to_f64(a) -> np.ndarray:
     return u.view(np.float32).astype(np.float64)
 
 
-def dense_routing(x, wr, bias, top_k):
-    """Returns (logits [B,E], order [B,E] full ranking, dense weights [B,E])."""
+def dense_routing(x, wr, bias, top_k, select_only=False):
+    """Returns (logits [B,E], order [B,E] full ranking, dense weights [B,E]).
+    logits are the ranking keys (router scores plus offsets); with
+    select_only the sigmoid takes the router scores without the offsets."""
     X = bf16_to_f64(x)
     Wr = bf16_to_f64(wr)
-    logits = X @ Wr.T
+    raw = X @ Wr.T
+    logits = raw
     if bias is not None:
-        logits = logits + np.asarray(bias, dtype=np.float32).astype(np.float64)[None, :]
+        logits = raw + np.asarray(bias, dtype=np.float32).astype(np.float64)[None, :]
     order = np.argsort(-logits, axis=1, kind="stable")
     sel = order[:, :top_k]
-    scores = 1.0 / (1.0 + np.exp(-logits))
+    scores = 1.0 / (1.0 + np.exp(-(raw if select_only else logits)))
     dense_w = np.zeros_like(logits)
     rows = np.arange(logits.shape[0])[:, None]
     dense_w[rows, sel] = scores[rows, sel]
@@ -51,12 +54,12 @@ def _ffn_all_tokens(X, w13_e, w2_e, inter):
     return A @ W2.T
 
 
-def dense_moe_bf16(x, residual, wr, bias, w13, w2, ws13, ws2, top_k):
+def dense_moe_bf16(x, residual, wr, bias, w13, w2, ws13, ws2, top_k, select_only=False):
     """Returns (out [B,H], selected idx [B,k], their weights [B,k])."""
     X = bf16_to_f64(x)
     out = bf16_to_f64(residual).copy()
     inter = w13.shape[1] // 2
-    logits, order, dense_w = dense_routing(x, wr, bias, top_k)
+    logits, order, dense_w = dense_routing(x, wr, bias, top_k, select_only)
     for s in range(ws13.shape[0]):
         out += _ffn_all_tokens(X, ws13[s], ws2[s], inter)
     for e in range(w13.shape[0]):

@@ -8,14 +8,16 @@
  * What it computes, written out as the plain definition, only for the experts
  * that routing selects (every bf16 / fp32 input is decoded exactly to fp64 and
  * nothing is rounded afterwards):
- *   1. logits   L[t,e] = sum_h x[t,h] * Wr[e,h] + bias[e]     (bias 0 if absent)
- *      -- the router scores every expert: [vLLM Day-0 Support for Recursive's
- *      Flint, "Flint Model Architecture", "MoE Structure"].
+ *   1. logits   R[t,e] = sum_h x[t,h] * Wr[e,h]; ranking key L = R + bias[e]
+ *      (bias 0 if absent) -- the router scores every expert: [vLLM Day-0
+ *      Support for Recursive's Flint, "Flint Model Architecture", "MoE
+ *      Structure"].
  *   2. selection: rank experts by (L descending, index ascending) and keep the
- *      first top_k; score s = 1 / (1 + exp(-L)); weight w_j = s_j / sum of the
- *      kept s.  "sigmoid top-6 selection": same section; the renormalisation
- *      and the lower-index tie rule are this library's reading (the pages are
- *      silent on both).
+ *      first top_k; score s = 1 / (1 + exp(-L)), or 1 / (1 + exp(-R)) when
+ *      offset_mode is 1 (offsets steer the selection only); weight w_j = s_j /
+ *      sum of the kept s.  "sigmoid top-6 selection": same section; the
+ *      renormalisation, the lower-index tie rule and both offset readings are
+ *      this library's (the pages are silent on all of them).
  *   3. expert FFN (SwiGLU, "Qwen3-MoE-style" and "SiLU-and-mul":
  *      [Flint on Intel Arc Pro B70, "Setup"; "norm.py: Triton kernels that
  *      assumed CUDA"]):  g = Wg v, u = Wu v, a = g / (1 + exp(-g)) * u,
@@ -42,6 +44,7 @@
 
 typedef struct {
   int32_t hidden, n_experts, top_k, inter, n_shared;
+  int32_t offset_mode; /* 0: offsets move ranking and weights; 1: ranking only */
 } ref_dims;
 
 /* ---- exact decoders ------------------------------------------------------ */
@@ -157,11 +160,13 @@ static void expert_ffn(const ref_dims* d, const ref_mat* m13, const ref_mat* m2,
 static void route_token(const ref_dims* d, const uint16_t* x, const uint16_t* wr,
                         const float* bias, double* logits, int32_t* idx, double* w) {
   const int H = d->hidden, E = d->n_experts, k = d->top_k;
+  double* raw = (double*)malloc(sizeof(double) * (size_t)E);
   for (int e = 0; e < E; ++e) {
-    double acc = bias ? (double)bias[e] : 0.0;
+    double acc = 0.0;
     for (int h = 0; h < H; ++h)
       acc += bf16_value(x[h]) * bf16_value(wr[(size_t)e * H + h]);
-    logits[e] = acc;
+    raw[e] = acc;
+    logits[e] = acc + (bias ? (double)bias[e] : 0.0);
   }
   /* Repeated selection of the best remaining expert; scanning indices upward
    * with a strict '>' keeps the lower index on equal logits. */
@@ -173,11 +178,13 @@ static void route_token(const ref_dims* d, const uint16_t* x, const uint16_t* wr
       if (!taken[e] && (best < 0 || logits[e] > logits[best])) best = e;
     taken[best] = 1;
     idx[j] = best;
-    w[j] = 1.0 / (1.0 + exp(-logits[best]));
+    const double score_in = d->offset_mode == 1 ? raw[best] : logits[best];
+    w[j] = 1.0 / (1.0 + exp(-score_in));
     ssum += w[j];
   }
   for (int j = 0; j < k; ++j) w[j] /= ssum;
   free(taken);
+  free(raw);
 }
 
 /* Router only.  logits may be NULL. */

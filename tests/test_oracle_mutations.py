@@ -27,11 +27,16 @@ MUTATIONS = {
     "tie goes to the higher index": (
         "logits[e] > logits[best]", "logits[e] >= logits[best]"),
     "sigmoid sign flipped": (
-        "w[j] = 1.0 / (1.0 + exp(-logits[best]));", "w[j] = 1.0 / (1.0 + exp(logits[best]));"),
+        "w[j] = 1.0 / (1.0 + exp(-score_in));", "w[j] = 1.0 / (1.0 + exp(score_in));"),
     "weights not renormalised": (
         "for (int j = 0; j < k; ++j) w[j] /= ssum;", "for (int j = 0; j < k; ++j) w[j] /= 1.0;"),
     "logit offsets ignored": (
-        "double acc = bias ? (double)bias[e] : 0.0;", "double acc = 0.0;"),
+        "logits[e] = acc + (bias ? (double)bias[e] : 0.0);", "logits[e] = acc;"),
+    "select-only weights take the offsets": (
+        "d->offset_mode == 1 ? raw[best] : logits[best]", "logits[best]"),
+    "select-only offsets ignored in the ranking": (
+        "logits[e] = acc + (bias ? (double)bias[e] : 0.0);",
+        "logits[e] = acc + (bias && d->offset_mode != 1 ? (double)bias[e] : 0.0);"),
     "shared expert dropped": (
         "for (int h = 0; h < H; ++h) o[h] += y[h];",
         "for (int h = 0; h < H; ++h) o[h] += 0.0 * y[h];"),
@@ -53,8 +58,12 @@ MUTATIONS = {
 
 # The pins run against each build: all of test_oracle_pins.py's CPU-quick pins.
 PINS = [
-    ("brute force, tiny, batch 8 with offsets", lambda: pins.test_matches_dense_brute_force_tiny(3, 8, True)),
-    ("brute force, tiny, batch 17", lambda: pins.test_matches_dense_brute_force_tiny(4, 17, False)),
+    ("brute force, tiny, batch 8 with offsets", lambda: pins.test_matches_dense_brute_force_tiny(3, 8, True, False)),
+    ("brute force, tiny, batch 17", lambda: pins.test_matches_dense_brute_force_tiny(4, 17, False, False)),
+    ("brute force, tiny, batch 8, offsets for selection only",
+     lambda: pins.test_matches_dense_brute_force_tiny(6, 8, True, True)),
+    ("x = 0 with offsets for selection only",
+     pins.test_zero_input_select_only_offsets_rank_and_weights_are_equal),
     ("first k of a full sort, weights sum to 1",
      pins.test_selection_is_first_k_of_full_sort_and_weights_sum_to_one),
     ("token permutation", pins.test_token_permutation_permutes_outputs_exactly),

@@ -7,6 +7,7 @@ renormalisation.
 """
 from __future__ import annotations
 
+import dataclasses
 import json
 import math
 import os
@@ -33,17 +34,18 @@ def _f64(t) -> np.ndarray:
 
 # ---------------------------------------------------------------- brute force
 
-@pytest.mark.parametrize("seed,batch,with_bias", [(1, 1, False), (2, 3, False),
-                                                   (3, 8, True), (4, 17, False),
-                                                   (5, 33, True)])
-def test_matches_dense_brute_force_tiny(seed, batch, with_bias):
-    d = fs.TINY
+@pytest.mark.parametrize("seed,batch,with_bias,select_only",
+                         [(1, 1, False, False), (2, 3, False, False), (3, 8, True, False),
+                          (4, 17, False, False), (5, 33, True, False), (6, 8, True, True),
+                          (7, 33, True, True)])
+def test_matches_dense_brute_force_tiny(seed, batch, with_bias, select_only):
+    d = dataclasses.replace(fs.TINY, offset_mode=1 if select_only else 0)
     W = fs.layer_weights(seed, d)
     x, r = fs.tokens(seed + 100, batch, d.hidden)
     bias = fs.logit_offsets(seed + 200, d.n_experts) if with_bias else None
     out, idx, w = oracle.moe_bf16(d, x, r, W["wr"], bias, W["w13"], W["w2"], W["ws13"], W["ws2"])
     o2, i2, w2 = brute.dense_moe_bf16(x, r, W["wr"], bias, W["w13"], W["w2"], W["ws13"],
-                                      W["ws2"], d.top_k)
+                                      W["ws2"], d.top_k, select_only)
     np.testing.assert_array_equal(idx, i2)
     np.testing.assert_allclose(w, w2, rtol=1e-13, atol=0)
     scale = np.abs(o2).max()
@@ -142,6 +144,26 @@ def test_zero_input_with_offsets_ranks_by_offsets():
     expect = np.argsort(-b, kind="stable")[:d.top_k]
     np.testing.assert_array_equal(idx[0], expect)
     np.testing.assert_array_equal(logits[0], b)
+
+
+def test_zero_input_select_only_offsets_rank_and_weights_are_equal():
+    """x = 0 with offsets used for selection only: every router score is 0, so
+    the offsets alone rank the experts and every kept weight is
+    sigmoid(0) / (6 sigmoid(0)) = 1/6 exactly; with the offsets in the logit
+    (mode 0) the weights follow the offsets instead."""
+    d = dataclasses.replace(fs.TINY, offset_mode=1)
+    W = fs.layer_weights(45, d)
+    bias = fs.logit_offsets(46, d.n_experts)
+    x = torch.zeros((2, d.hidden), dtype=torch.bfloat16)
+    idx, w, logits = oracle.route(d, x, W["wr"], bias)
+    b = bias.double().numpy()
+    expect = np.argsort(-b, kind="stable")[:d.top_k]
+    np.testing.assert_array_equal(idx[0], expect)
+    assert np.all(w == 1.0 / d.top_k)
+    idx0, w0, _ = oracle.route(fs.TINY, x, W["wr"], bias)
+    np.testing.assert_array_equal(idx0, idx)
+    s = 1.0 / (1.0 + np.exp(-b[expect]))
+    np.testing.assert_allclose(w0[0], s / s.sum(), rtol=1e-14)
 
 
 def _embedded_layer(d, shared_up=3.0):
