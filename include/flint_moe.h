@@ -54,11 +54,13 @@
  *    for its own asynchronous copies and returns; read the word with
  *    flint_moe_get_device_status.  The outputs of such a call are undefined,
  *    and the workspace must be re-initialised before the next call.
- *  - Routing: logits are computed in fp32 from bf16 inputs.  Experts are
- *    ranked by (logit descending, expert index ascending), the first top_k are
- *    kept, and each kept expert's weight is sigmoid(logit) divided by the sum
- *    of the kept sigmoids (so the weights sum to 1).  topk_idx rows list the
- *    experts in that rank order.
+ *  - Routing: router scores are computed in fp32 from bf16 inputs and the
+ *    logit offsets (if any) are added to them in fp32.  Experts are ranked by
+ *    (score + offset descending, expert index ascending), the first top_k are
+ *    kept, and each kept expert's weight is sigmoid(score + offset) -- or
+ *    sigmoid(score) with FLINT_OFFSET_SELECT -- divided by the sum over the
+ *    kept experts (so the weights sum to 1).  topk_idx rows list the experts
+ *    in that rank order.
  */
 #ifndef FLINT_MOE_H_
 #define FLINT_MOE_H_
@@ -80,14 +82,31 @@ typedef enum {
   FLINT_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait ran out */
 } flint_status;
 
-/* Layer shape.  Supported: hidden 2048, n_experts 256, top_k 6, inter 512,
- * n_shared 1.  Any other value returns FLINT_ERR_UNSUPPORTED. */
+/* What per-expert logit offsets (logit_bias) change.  The pages give only
+ * "sigmoid top-6 selection" ([vLLM Day-0 Support for Recursive's Flint,
+ * "Flint Model Architecture"]) and no offsets; both common conventions are
+ * offered:
+ *   FLINT_OFFSET_LOGIT  (0, default): the offset is added to the router score
+ *     before ranking and before the sigmoid, so it moves both the selection
+ *     and the weights;
+ *   FLINT_OFFSET_SELECT (1): experts are ranked by score + offset, but each
+ *     kept expert's weight is the sigmoid of its score without the offset
+ *     (renormalised over the kept experts), so the offset steers the
+ *     selection only. */
+#define FLINT_OFFSET_LOGIT 0
+#define FLINT_OFFSET_SELECT 1
+
+/* Layer shape and routing convention.  Supported: hidden 2048, n_experts 256,
+ * top_k 6, inter 512, n_shared 1, offset_mode FLINT_OFFSET_LOGIT or
+ * FLINT_OFFSET_SELECT.  Any other value returns FLINT_ERR_UNSUPPORTED.  A
+ * zero-initialised offset_mode is the default convention. */
 typedef struct {
-  int32_t hidden;     /* H */
-  int32_t n_experts;  /* E, routed experts */
-  int32_t top_k;      /* k, experts selected per token */
-  int32_t inter;      /* I, expert intermediate size */
-  int32_t n_shared;   /* S, always-on shared experts (added with weight 1) */
+  int32_t hidden;       /* H */
+  int32_t n_experts;    /* E, routed experts */
+  int32_t top_k;        /* k, experts selected per token */
+  int32_t inter;        /* I, expert intermediate size */
+  int32_t n_shared;     /* S, always-on shared experts (added with weight 1) */
+  int32_t offset_mode;  /* FLINT_OFFSET_LOGIT or FLINT_OFFSET_SELECT */
 } flint_moe_dims;
 
 /* Largest batch (tokens per call) any entry point accepts. */
@@ -119,8 +138,9 @@ flint_status flint_moe_get_device_status(const void* workspace, cudaStream_t str
 /* Router only: logits, sigmoid top-k, renormalised weights.
  *   x_bf16        [batch, H]   token activations (already normalised)
  *   w_router_bf16 [E, H]       router matrix
- *   logit_bias    [E] fp32 or NULL; added to every logit before ranking and
- *                 before the sigmoid (so it moves both selection and weights)
+ *   logit_bias    [E] fp32 or NULL; per-expert logit offsets, applied as
+ *                 dims->offset_mode says (by default added to the logit
+ *                 before ranking and before the sigmoid)
  *   topk_idx      [batch, k]   int32 out, expert ids in rank order
  *   topk_w        [batch, k]   fp32 out, renormalised weights
  * Also leaves the token-to-expert buckets in the workspace for the stage

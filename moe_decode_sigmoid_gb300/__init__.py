@@ -52,13 +52,18 @@ class FlintError(RuntimeError):
         super().__init__("%s: %s" % (where, status_string(status)))
 
 
+FLINT_OFFSET_LOGIT = 0    # offsets move ranking and weights (default)
+FLINT_OFFSET_SELECT = 1   # offsets steer the ranking only
+
+
 class Dims(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32),
-                ("n_shared", ctypes.c_int32)]
+                ("n_shared", ctypes.c_int32), ("offset_mode", ctypes.c_int32)]
 
 
-FULL_DIMS = Dims(HIDDEN, N_EXPERTS, TOP_K, INTER, N_SHARED)
+FULL_DIMS = Dims(HIDDEN, N_EXPERTS, TOP_K, INTER, N_SHARED, FLINT_OFFSET_LOGIT)
+SELECT_DIMS = Dims(HIDDEN, N_EXPERTS, TOP_K, INTER, N_SHARED, FLINT_OFFSET_SELECT)
 
 _lib = None
 _P = ctypes.c_void_p

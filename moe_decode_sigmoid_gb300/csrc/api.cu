@@ -18,7 +18,8 @@ constexpr uint64_t DEFAULT_WAIT_NS = 1000000000ull;  // 1 s
 
 bool dims_supported(const flint_moe_dims* d) {
   return d->hidden == H && d->n_experts == E && d->top_k == TOPK && d->inter == I &&
-         d->n_shared == S;
+         d->n_shared == S &&
+         (d->offset_mode == FLINT_OFFSET_LOGIT || d->offset_mode == FLINT_OFFSET_SELECT);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -157,6 +158,7 @@ flint_status flint_moe_route(const flint_moe_dims* dims, int32_t batch, const vo
   a.x = static_cast<const uint16_t*>(x_bf16);
   a.wr = static_cast<const uint16_t*>(w_router_bf16);
   a.bias = logit_bias;
+  a.bias_select_only = dims->offset_mode == FLINT_OFFSET_SELECT;
   a.B = batch;
   a.ws = ws_view(workspace);
   a.user_idx = topk_idx;
@@ -181,7 +183,8 @@ flint_status flint_moe_bucket(const flint_moe_dims* dims, int32_t batch, const i
   return cuda_status(launch_bucket(w, batch, bo, stream));
 }
 
-static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const void* residual,
+static flint_status run_layer(bool nvfp4, const flint_moe_dims* dims, int32_t batch,
+                              const void* x, const void* residual,
                               const void* wr, const float* bias, const ExpertW& w, void* out,
                               int32_t* idx_out, float* w_out, void* workspace,
                               cudaStream_t stream) {
@@ -191,6 +194,7 @@ static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const vo
   r.x = static_cast<const uint16_t*>(x);
   r.wr = static_cast<const uint16_t*>(wr);
   r.bias = bias;
+  r.bias_select_only = dims->offset_mode == FLINT_OFFSET_SELECT;
   r.B = batch;
   r.ws = ws_view(workspace);
   r.user_idx = idx_out;
@@ -213,6 +217,8 @@ static flint_status run_layer(bool nvfp4, int32_t batch, const void* x, const vo
   // depend on routing, is then computed while the router runs.
   a.early_shared = 1;
   a.local_select = r.logits_only;
+  a.bias = bias;
+  a.bias_select_only = r.bias_select_only;
   a.user_idx = idx_out;
   a.user_w = w_out;
   if (!nvfp4 && batch <= LOCAL_SELECT_MAX_B && small_bf16_supported(sms))
@@ -242,8 +248,8 @@ flint_status flint_moe_decode_bf16(const flint_moe_dims* dims, int32_t batch, co
   w.w2 = static_cast<const uint16_t*>(w2_bf16);
   w.ws13 = static_cast<const uint16_t*>(ws13_bf16);
   w.ws2 = static_cast<const uint16_t*>(ws2_bf16);
-  return run_layer(false, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias, w, out_bf16,
-                   topk_idx_out, topk_w_out, workspace, stream);
+  return run_layer(false, dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias, w,
+                   out_bf16, topk_idx_out, topk_w_out, workspace, stream);
 }
 
 flint_status flint_moe_gateup_bf16(const flint_moe_dims* dims, int32_t batch, const void* x_bf16,
@@ -305,8 +311,8 @@ flint_status flint_moe_decode_nvfp4_w4a16(
   w.w2_q = w2_q; w.w2_sf = w2_sf; w.w2_ts = w2_ts;
   w.ws13_q = ws13_q; w.ws13_sf = ws13_sf; w.ws13_ts = ws13_ts;
   w.ws2_q = ws2_q; w.ws2_sf = ws2_sf; w.ws2_ts = ws2_ts;
-  return run_layer(true, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias, w, out_bf16,
-                   topk_idx_out, topk_w_out, workspace, stream);
+  return run_layer(true, dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias, w,
+                   out_bf16, topk_idx_out, topk_w_out, workspace, stream);
 }
 
 flint_status flint_moe_rmsnorm_bf16(const flint_moe_dims* dims, int32_t batch, const void* in_bf16,

@@ -160,7 +160,7 @@ __device__ __forceinline__ void fill_meta(const ExpertArgs& a, bool local, MetaS
     if (warp < B) {
       int ix;
       float wt;
-      topk_warp<false>(logits_buf + warp * E, ix, wt);
+      topk_warp<false>(logits_buf + warp * E, a.bias, a.bias_select_only != 0, ix, wt);
       if (lane < TOPK) {
         const int p = warp * TOPK + lane;
         ls->idx[p] = ix;

@@ -148,11 +148,11 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
   return acc;
 }
 
-// Logits of experts [e_begin, e_end) for the whole batch (B <= 8), by the 8
-// consumer warps from shared memory (router rows in `rows`, activations in
-// xs): warp w takes expert base + w/4 and the K-quarter w%4.  Published as
-// tagged words.
-__device__ __forceinline__ void router_slice(int B, const float* bias, uint64_t* tlogits,
+// Router scores of experts [e_begin, e_end) for the whole batch (B <= 8), by
+// the 8 consumer warps from shared memory (router rows in `rows`, activations
+// in xs): warp w takes expert base + w/4 and the K-quarter w%4.  Published as
+// tagged words; the logit offsets join at ranking.
+__device__ __forceinline__ void router_slice(int B, uint64_t* tlogits,
                                              const uint16_t* rows, const uint16_t* xs,
                                              int e_begin, int e_end, float (*s_part)[4][8],
                                              uint32_t tag) {
@@ -186,8 +186,7 @@ __device__ __forceinline__ void router_slice(int B, const float* bias, uint64_t*
       const int le = tid >> 3, t = tid & 7, ee = base + le;
       if (ee < e_end && t < B)
         st_tagged(tlogits + (size_t)t * E + ee,
-                  (s_part[le][0][t] + s_part[le][1][t]) + (s_part[le][2][t] + s_part[le][3][t]) +
-                      (bias ? __ldg(bias + ee) : 0.0f),
+                  (s_part[le][0][t] + s_part[le][1][t]) + (s_part[le][2][t] + s_part[le][3][t]),
                   tag);
     }
     named_sync(1, fz::CT);
@@ -862,7 +861,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
     s_abort = 1;
     set_error(hdr, DEV_TIMEOUT);
   }
-  router_slice(B, r.bias, a.ws.tlogits, reinterpret_cast<const uint16_t*>(buf), xs, e_begin,
+  router_slice(B, a.ws.tlogits, reinterpret_cast<const uint16_t*>(buf), xs, e_begin,
                e_end, s_part, tag);
   // 2. every CTA ranks and buckets the batch once all logits are in
   if (tid == 0) {
@@ -896,7 +895,7 @@ __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertAr
   if (warp < B) {
     int ix;
     float wt;
-    topk_warp<false>(buf + warp * E, ix, wt);
+    topk_warp<false>(buf + warp * E, r.bias, r.bias_select_only != 0, ix, wt);
     if (lane < TOPK) {
       const int pp = warp * TOPK + lane;
       s_sel.idx[pp] = ix;

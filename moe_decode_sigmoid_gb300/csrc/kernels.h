@@ -15,7 +15,8 @@ namespace flint {
 struct RouterArgs {
   const uint16_t* x;   // [B,H] bf16
   const uint16_t* wr;  // [E,H] bf16
-  const float* bias;   // [E] or null
+  const float* bias;   // [E] logit offsets or null
+  int bias_select_only;  // the offsets steer the ranking only (not the weights)
   int B;
   Ws ws;
   int* user_idx;       // [B,TOPK] or null
@@ -49,6 +50,8 @@ struct ExpertArgs {
   Ws ws;
   int early_shared;  // gate/up: start the shared expert before the router finishes
   int local_select;  // gate/up: rank and bucket the batch in every CTA (batch <= 8)
+  const float* bias;     // logit offsets (local selection) or null
+  int bias_select_only;  // as RouterArgs
   int* user_idx;     // gate/up with local_select: optional routing copies
   float* user_w;
 };

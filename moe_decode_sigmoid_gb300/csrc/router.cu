@@ -116,9 +116,8 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
     const int le = threadIdx.x >> 3, t = threadIdx.x & 7;
     if (t < nt) {
       const int ee = blockIdx.x * 2 + le;
-      a.ws.logits[(size_t)(t0 + t) * E + ee] =
-          (s_part[le][0][t] + s_part[le][1][t]) + (s_part[le][2][t] + s_part[le][3][t]) +
-          (a.bias ? __ldg(a.bias + ee) : 0.0f);
+      a.ws.logits[(size_t)(t0 + t) * E + ee] =  // the router score; offsets join at ranking
+          (s_part[le][0][t] + s_part[le][1][t]) + (s_part[le][2][t] + s_part[le][3][t]);
     }
   }
   if (a.logits_only) return;
@@ -140,7 +139,7 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
     const int t = t0 + warp;
     int ix;
     float wt;
-    topk_warp<true>(a.ws.logits + (size_t)t * E, ix, wt);
+    topk_warp<true>(a.ws.logits + (size_t)t * E, a.bias, a.bias_select_only != 0, ix, wt);
     if (lane < TOPK) {
       a.ws.topk_idx[t * TOPK + lane] = ix;
       a.ws.topk_w[t * TOPK + lane] = wt;

@@ -30,21 +30,27 @@ __device__ __forceinline__ void topk_cas(uint32_t (&k)[E / 32], uint32_t (&e)[E 
   e[j] = swap ? ei : e[j];
 }
 
-// Top-k of one token's E logits by one warp.  Lane l holds experts l + 32 j
-// and first sorts its 8 (key, expert) pairs -- key descending, expert
-// ascending -- with a 19-comparator sorting network (Batcher's odd-even merge
-// sort).  Each round then takes the largest lane head; among equal logits the
-// lowest expert index wins (a lane's head is its lowest index for that key, and
-// across lanes the minimum index is taken).  Lanes 0..k-1 return slot
-// `lane`'s expert and weight.
+// Top-k of one token's E router scores by one warp.  The ranking key of
+// expert e is its score plus its logit offset (bias, may be null); lane l
+// holds experts l + 32 j and first sorts its 8 (key, expert) pairs -- key
+// descending, expert ascending -- with a 19-comparator sorting network
+// (Batcher's odd-even merge sort).  Each round then takes the largest lane
+// head; among equal keys the lowest expert index wins (a lane's head is its
+// lowest index for that key, and across lanes the minimum index is taken).
+// Each kept expert's weight is the sigmoid of its key -- or, with
+// select_only, of its score without the offset -- divided by the sum over the
+// kept experts.  Lanes 0..k-1 return slot `lane`'s expert and weight.
 template <bool GLOBAL_SRC>
-__device__ __forceinline__ void topk_warp(const float* logits_row, int& idx_out, float& w_out) {
+__device__ __forceinline__ void topk_warp(const float* logits_row, const float* bias,
+                                          bool select_only, int& idx_out, float& w_out) {
   static_assert(E / 32 == 8, "the sorting network is written for 8 values per lane");
   const int lane = threadIdx.x & 31;
   uint32_t k[8], e[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    k[j] = f2key(GLOBAL_SRC ? __ldcg(logits_row + lane + 32 * j) : logits_row[lane + 32 * j]);
+    const float score =
+        GLOBAL_SRC ? __ldcg(logits_row + lane + 32 * j) : logits_row[lane + 32 * j];
+    k[j] = f2key(bias ? score + __ldg(bias + lane + 32 * j) : score);
     e[j] = (uint32_t)(lane + 32 * j);
   }
   topk_cas(k, e, 0, 1); topk_cas(k, e, 2, 3); topk_cas(k, e, 4, 5); topk_cas(k, e, 6, 7);
@@ -86,6 +92,8 @@ __device__ __forceinline__ void topk_warp(const float* logits_row, int& idx_out,
       idx_out = sel_e[r];
     }
   if (lane >= TOPK) idx_out = 0;
+  if (select_only && bias && lane < TOPK)  // the sigmoid of the score itself
+    mine = GLOBAL_SRC ? __ldcg(logits_row + idx_out) : logits_row[idx_out];
   sv = 1.0f / (1.0f + expf(-mine));
   float ssum = 0.f;
 #pragma unroll

@@ -55,6 +55,8 @@ def test_workspace_bytes(L):
     assert m.flint_moe_workspace_bytes(257) == 0
     bad = m.Dims(2048, 256, 6, 256, 1)
     assert m.flint_moe_workspace_bytes(8, bad) == 0
+    assert m.flint_moe_workspace_bytes(8, m.SELECT_DIMS) == m.flint_moe_workspace_bytes(8)
+    assert m.flint_moe_workspace_bytes(8, m.Dims(2048, 256, 6, 512, 1, 2)) == 0  # no such mode
 
 
 # Fake device addresses: validation fails before anything is dereferenced.

@@ -10,6 +10,8 @@ Bar (applied to every case):
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -474,3 +476,48 @@ def test_calls_of_mixed_batches_on_one_workspace_match_fresh_workspaces(m, layer
         assert torch.equal(idx_s, idx_f), (i, B)
         assert torch.equal(w_s, w_f), (i, B)
         assert torch.equal(out_s.view(torch.int16), out_f.view(torch.int16)), (i, B)
+
+
+@pytest.mark.parametrize("B,fmt", [(1, "bf16"), (5, "bf16"), (8, "bf16"), (13, "bf16"),
+                                   (64, "bf16"), (3, "nvfp4"), (40, "nvfp4"), (8, "route"),
+                                   (128, "route")])
+def test_select_only_offsets_match_oracle(m, layer, nv_layer, ws, B, fmt):
+    """Logit offsets used for the selection only (FLINT_OFFSET_SELECT): the
+    ranking uses score + offset, the weights the sigmoid of the score alone."""
+    W, host = layer
+    nv, nv_host = nv_layer
+    Dsel = dataclasses.replace(D, offset_mode=1)
+    x, res = fs.tokens(4900 + B, B, device="cuda")
+    bias = fs.logit_offsets(1003, device="cuda")
+    idx = torch.full((B, K), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((B, K), dtype=torch.float32, device="cuda")
+    out = torch.empty_like(res)
+    if fmt == "route":
+        m.flint_moe_route(x, W["wr"], bias, idx, w, ws, dims=m.SELECT_DIMS)
+    elif fmt == "bf16":
+        m.flint_moe_decode_bf16(x, res, W["wr"], bias, W["w13"], W["w2"], W["ws13"], W["ws2"],
+                                out, ws, idx, w, dims=m.SELECT_DIMS)
+    else:
+        m.flint_moe_decode_nvfp4_w4a16(x, res, W["wr"], bias, nv, out, ws, idx, w,
+                                       dims=m.SELECT_DIMS)
+    torch.cuda.synchronize()
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_OK
+    ref_idx, _, keys = oracle.route(Dsel, x.cpu(), host["wr"], bias.cpu())
+    raw_logits = oracle.route(D, x.cpu(), host["wr"], None)[2]   # scores without offsets
+    gi = idx.cpu().numpy().astype(np.int64)
+    clear = topk_margin(keys, K) >= TAU
+    np.testing.assert_array_equal(gi[clear], ref_idx[clear])
+    s = 1.0 / (1.0 + np.exp(-np.take_along_axis(raw_logits, gi, axis=1)))
+    w_ref = s / s.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=1e-5, atol=0)
+    if fmt == "route":
+        return
+    if fmt == "bf16":
+        ref = oracle.moe_bf16_given_routing(D, x.cpu(), res.cpu(), gi.astype(np.int32), w_ref,
+                                            host["w13"], host["w2"], host["ws13"], host["ws2"])
+    else:
+        ref = oracle.moe_nvfp4_given_routing(D, x.cpu(), res.cpu(), gi.astype(np.int32), w_ref,
+                                             nv_host)
+    got = bf16_bits_to_f64(out)
+    assert rel_err(got, ref) <= REL_TOL
+    assert rel_err_delta(got, ref, bf16_bits_to_f64(res)) <= REL_TOL
