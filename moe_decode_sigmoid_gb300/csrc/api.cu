@@ -221,8 +221,9 @@ static flint_status run_layer(bool nvfp4, const flint_moe_dims* dims, int32_t ba
   a.bias_select_only = r.bias_select_only;
   a.user_idx = idx_out;
   a.user_w = w_out;
-  if (!nvfp4 && batch <= LOCAL_SELECT_MAX_B && small_bf16_supported(sms))
-    return cuda_status(launch_small_bf16(a, r, stream, sms));  // one persistent kernel
+  if (batch <= LOCAL_SELECT_MAX_B && small_supported(sms))  // one persistent kernel
+    return cuda_status(nvfp4 ? launch_small_nvfp4(a, r, stream, sms)
+                             : launch_small_bf16(a, r, stream, sms));
   cudaError_t e = launch_router(r, stream, true);
   if (e != cudaSuccess) return cuda_status(e);
   e = nvfp4 ? launch_gateup_nvfp4(a, stream, sms) : launch_gateup_bf16(a, stream, sms);

@@ -63,11 +63,13 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_bucket(const Ws& ws, int B, const BucketOut& user, cudaStream_t stream);
 cudaError_t launch_gateup_bf16(const ExpertArgs& a, cudaStream_t stream, int num_sms);
 cudaError_t launch_down_bf16(const ExpertArgs& a, cudaStream_t stream);
-// The whole BF16 layer in one persistent cooperative kernel (batch <= 8), for
-// grids of num_sms CTAs where small_bf16_supported(num_sms).
-bool small_bf16_supported(int num_sms);
+// The whole layer in one persistent cooperative kernel (batch <= 8), for
+// grids of num_sms CTAs where small_supported(num_sms): BF16 or NVFP4 weights.
+bool small_supported(int num_sms);
 cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                               int num_sms);
+cudaError_t launch_small_nvfp4(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
+                               int num_sms);
 cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
 cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
 cudaError_t launch_rmsnorm(const uint16_t* in, uint16_t* out, int B, float eps,

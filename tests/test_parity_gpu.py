@@ -442,17 +442,18 @@ def test_large_h_beyond_f16_range_matches_oracle(m, layer, nv_layer, ws, B):
     assert rel_err_delta(got4, ref4, bf16_bits_to_f64(res)) <= REL_TOL
 
 
-def test_nvfp4_reports_activations_beyond_f16(m, layer, nv_layer):
+@pytest.mark.parametrize("B", [5, 13])
+def test_nvfp4_reports_activations_beyond_f16(m, layer, nv_layer, B):
     """The NVFP4 path multiplies f16 activations: a value beyond f16's range
     makes the call report FLINT_ERR_INVALID_ARG on the device instead of
-    returning infinities; after re-initialisation the workspace works again."""
+    returning infinities; after re-initialisation the workspace works again
+    (both the persistent kernel, batch 5, and the three-kernel path)."""
     W, host = layer
     nv, nv_host = nv_layer
-    B = 13
     ws = m.new_workspace(B)
     x, res = fs.tokens(4700, B, device="cuda")
     xb = x.clone()
-    xb[5, 100] = 70000.0
+    xb[B // 2, 100] = 70000.0
     out = torch.empty_like(res)
     m.flint_moe_decode_nvfp4_w4a16(xb, res, W["wr"], None, nv, out, ws)
     assert m.flint_moe_get_device_status(ws) == m.FLINT_ERR_INVALID_ARG
