@@ -35,6 +35,7 @@ constexpr uint32_t DEV_TIMEOUT = 5;
 // [ header | logits fp32 [MAX_B,E] | topk_idx i32 [MAX_B,K] | topk_w f32 [MAX_B,K] |
 //   pair_tok i32 [MAX_B*SLOTS] | pair_w f32 [MAX_B*SLOTS] | groups int4 [MAX_GROUPS] |
 //   tagged logits u64 [SMALL_B,E] | tagged h u64 [SMALL_B*SLOTS, I] |
+//   tagged y u64 [SMALL_B*SLOTS, H] |
 //   h [max_batch*SLOTS, I] x 4 bytes | y fp32 [max_batch*SLOTS, H] ]
 // The tagged regions belong to the persistent small-batch kernels: each 8-byte
 // word holds a 32-bit value and the call's tag (see call_tag), so a reader on
@@ -91,7 +92,8 @@ struct WsLayout {
   static constexpr size_t groups = align256(pair_w + sizeof(float) * (size_t)MAX_B * SLOTS);
   static constexpr size_t tlogits = align256(groups + 16 * (size_t)MAX_GROUPS);
   static constexpr size_t th = align256(tlogits + 8 * (size_t)SMALL_B * E);
-  static constexpr size_t h = align256(th + 8 * (size_t)SMALL_B * SLOTS * I);
+  static constexpr size_t ty = align256(th + 8 * (size_t)SMALL_B * SLOTS * I);
+  static constexpr size_t h = align256(ty + 8 * (size_t)SMALL_B * SLOTS * H);
   static constexpr size_t total(int max_b) {
     return align256(h + sizeof(float) * (size_t)max_b * SLOTS * (I + H));
   }
@@ -103,6 +105,7 @@ struct Ws {
   float* logits;
   uint64_t* tlogits;  // [SMALL_B][E] tagged
   uint64_t* th;       // [SMALL_B * SLOTS][I] tagged
+  uint64_t* ty;       // [SMALL_B * SLOTS][H] tagged per-pair down projections
   int* topk_idx;
   float* topk_w;
   int* pair_tok;
@@ -121,6 +124,7 @@ inline Ws ws_view(void* base) {
   w.logits = reinterpret_cast<float*>(b + WsLayout::logits);
   w.tlogits = reinterpret_cast<uint64_t*>(b + WsLayout::tlogits);
   w.th = reinterpret_cast<uint64_t*>(b + WsLayout::th);
+  w.ty = reinterpret_cast<uint64_t*>(b + WsLayout::ty);
   w.topk_idx = reinterpret_cast<int*>(b + WsLayout::topk_idx);
   w.topk_w = reinterpret_cast<float*>(b + WsLayout::topk_w);
   w.pair_tok = reinterpret_cast<int*>(b + WsLayout::pair_tok);

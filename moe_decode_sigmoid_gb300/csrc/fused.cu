@@ -1,11 +1,11 @@
-// fused.cu — the whole BF16 decode MoE layer in one persistent kernel, for
-// batches of at most SMALL_B (8) tokens: the pages' low-latency path for up to
-// 8 requests, which fuses routing and the expert combine into the neighbouring
-// GEMVs ("Low-Latency Decode Path": vLLM Day-0 Support for Recursive's Flint,
-// "Optimization Strategies").
+// fused.cu — the whole decode MoE layer in one persistent kernel, for batches
+// of at most SMALL_B (8) tokens, with BF16 or NVFP4 expert weights: the pages'
+// low-latency path for up to 8 requests, which fuses routing and the expert
+// combine into the neighbouring GEMVs ("Low-Latency Decode Path": vLLM Day-0
+// Support for Recursive's Flint, "Optimization Strategies").
 //
 // One CTA per SM, all co-resident (cooperative launch), 8 consumer warps + a
-// producer warp + a poll warp.  The producer's lane 0 feeds a ring of 32 KiB
+// producer warp + a poll warp.  The producer's lane 0 feeds a ring of
 // shared-memory slots with cp.async.bulk copies and tags each slot with what
 // it holds; the consumers take the slots in order.
 //
@@ -16,34 +16,34 @@
 //      the producer streams shared-expert gate/up units, which need no routing.
 //   2. Selection: once every CTA has counted its logits in, each CTA reads all
 //      of them, ranks every token (one warp per token) and buckets the pairs --
-//      identical results in every CTA -- and hands the group table to the
-//      producer and the poll warp.
-//   3. Work queue: gate/up units (8 gate + 8 up rows of one group, two slots)
-//      are claimed one at a time from a workspace counter -- the shared
-//      expert's 64 units first, then the routed groups' in group order -- so
-//      CTAs that stream faster take more units and groups finish roughly in
-//      order.  The consumer warps store their h values as tagged words; the
-//      last of them to finish a unit adds one to its group's counter, and 64
-//      marks a group's h complete.
-//   4. Down: CTA b < 128 owns output rows [16b, 16b+16) of every token.  The
-//      poll warp watches the counters of its groups; as soon as one is
-//      complete, the producer posts a DOWN item: the 16 rows of the expert's
-//      Wd (16 KiB) and the group's tagged h rows (4 KiB per token; more than
-//      4 tokens spill into a second slot), and the consumers confirm every h
-//      word's tag and accumulate w(t, g) * (Wd h) per token: groups of <= 4
-//      tokens on CUDA cores into per-lane running sums (reduced once, at the
-//      end), larger ones on tensor cores.  Down items take priority over
-//      gate/up units, so the down projection streams while gate/up is still
-//      running.  Items run in a fixed order (the shared expert, then the
-//      routed groups by expert), so results are reproducible bit for bit.
+//      identical results in every CTA.
+//   3. Work queue: every CTA claims units one at a time from one workspace
+//      counter -- the shared expert's 64 gate/up units, the routed groups'
+//      gate/up units in group order, then the down units of every group (the
+//      shared group first) -- so CTAs that stream faster take more units.
+//      A gate/up unit is 8 gate + 8 up rows of one group (BF16: two 32 KiB
+//      slots; NVFP4: codes and block scales in one 20 KiB slot); the consumer
+//      warps store h as tagged words and the last of them to finish adds one
+//      to the group's completion counter (64 = the group's h is complete).
+//      A down unit is a block of Wd rows of one group's expert (BF16: 32 rows,
+//      one slot; NVFP4: 64 rows, codes and scales in one slot) plus the
+//      group's h rows in one or two more slots: its weights are copied as soon
+//      as it is claimed, its h rows once the poll warp has seen the group
+//      complete.  Every gate/up claim precedes every down claim, so no ring
+//      waits on a unit queued behind it.
+//   4. Each down unit writes y(p, row) = w(p) * (Wd h_p)[row] for its pairs p
+//      as tagged words, each written once per call.  After its ring drains,
+//      each CTA finishes its share of the output rows: out = residual + the
+//      token's SLOTS y values in ascending pair order -- a fixed order, so
+//      results are reproducible bit for bit whichever CTA computed what.
 //
 // No GPU-scope fence is taken on the data path: a fence waits for the SM's
 // outstanding memory traffic, which while weights stream costs 1-3 us per
-// hand-off.  Logits and h cross SMs as tagged words instead (call_tag), and
-// the counters only say when to look.  The counters come in two sets used by
-// alternate calls: a call clears the set of the next call, and CTA 0 advances
-// the workspace's call counter at its end, so nothing is reset at the exit.
-// Every wait is bounded by the workspace's limit.
+// hand-off.  Logits, h and y cross SMs as tagged words instead (call_tag),
+// and the counters only say when to look.  The counters come in two sets used
+// by alternate calls: a call clears the set of the next call, and CTA 0
+// advances the workspace's call counter at its end, so nothing is reset at
+// the exit.  Every wait is bounded by the workspace's limit.
 #include "common.cuh"
 #include "expert_common.cuh"
 #include "gateup_impl.cuh"
@@ -58,69 +58,69 @@ constexpr int POLL = CW + 1;                   // warp index of the poll warp
 constexpr int THREADS = (CW + 2) * 32;
 constexpr int CT = CW * 32;                    // consumer threads
 constexpr int ROWB = H * 2;                    // one gate/up row (bf16), 4 KiB
-constexpr int UNITS = I / 8;                   // gate/up units per group
 constexpr int MAXB = SMALL_B;
 constexpr int MAXG = MAXB * TOPK + S;          // groups at these batches (one shared group)
 constexpr int NPAIR = MAXB * SLOTS;
 constexpr int DONE_SHARED = SYNC_GROUPS - 1;   // counter of the shared group
-constexpr int UCNT = 8;                        // unit-completion counts in flight
-// Ready down items an owner may post between two of its gate/up units.  A
-// claimed unit must not wait behind a long run of down items: its group would
-// complete late for every owner, and their down items with it.
-constexpr int DN_PER_UNIT = 3;
-constexpr uint32_t DONE_TARGET = UNITS;        // unit marks per complete group
-constexpr int RS = 16;                         // output rows per row-slice owner
-constexpr int DOWN_CTAS = H / RS;              // 128 row-slice owners
 constexpr int WROW = I * 2;                    // one Wd row (bf16)
 constexpr int THROW = I * 8;                   // one tagged h row, 4 KiB
-constexpr int CC_MAX = 4;                      // BF16 down items on CUDA cores up to this many tokens
-constexpr int XS_BYTES = MAXB * H * 2;         // bf16 activations of the batch, 32 KiB
+constexpr int XS_BYTES = MAXB * H * 2;         // activations of the batch, 32 KiB
+constexpr int UCNT = 8;                        // unit-completion counts in flight
 constexpr int RED_BYTES = CW * 16 * GROUP_MAX * 4;
 constexpr int LOGIT_BYTES = MAXB * E * 4;
 constexpr int RMAX = 3;                        // router rows per CTA (grids of >= 86 CTAs)
 constexpr int RROW_BYTES = RMAX * H * 2;
+// router rows, then the batch's logits, then the gate/up units' partial tiles
 constexpr int BUF_BYTES = RED_BYTES > LOGIT_BYTES ? (RED_BYTES > RROW_BYTES ? RED_BYTES : RROW_BYTES)
                                                   : (LOGIT_BYTES > RROW_BYTES ? LOGIT_BYTES : RROW_BYTES);
-// Per-lane running sums of the CUDA-core down items: [token * 2 + row][thread],
-// rows padded to 257 floats so that both the updates (one row, consecutive
-// lanes) and the final per-row sums (16 lanes each) are free of bank conflicts.
-constexpr int LACC_STRIDE = CW * 32 + 1;
-constexpr int LACC_BYTES = MAXB * 2 * LACC_STRIDE * 4;
-// Ring and down-slice layout of each weight format.
+// Ring and unit layout of each weight format.
 template <bool NV>
 struct Geo;
 template <>
-struct Geo<false> {  // BF16: a gate/up unit is 2 slots (8 gate rows, 8 up rows)
-  static constexpr int SLOT = 32 * 1024, NS = 5, UNIT_SLOTS = 2;
-  static constexpr int WBYTES = RS * WROW;                  // Wd slice, 16 KiB
-  static constexpr int HROWS_A = (SLOT - WBYTES) / THROW;   // h rows beside it: 4
+struct Geo<false> {  // BF16
+  static constexpr int SLOT = 32 * 1024, NS = 5;
+  static constexpr int GR = 8;                              // gate/up unit: 8 gate + 8 up rows
+  static constexpr int UNIT_SLOTS = 2;                      // gate rows | up rows
+  static constexpr int DR = 64;                             // Wd rows per down unit
+  static constexpr int DN_SLOTS = 2;                        // rows 0-31 | rows 32-63
 };
 template <>
-struct Geo<true> {  // NVFP4: a gate/up unit is 1 slot (codes, then block scales)
-  static constexpr int SLOT = 20 * 1024, NS = 8, UNIT_SLOTS = 1;
+struct Geo<true> {  // NVFP4
+  static constexpr int SLOT = 20 * 1024, NS = 8;
+  static constexpr int GR = 8;                              // gate/up unit: 8 gate + 8 up rows
+  static constexpr int UNIT_SLOTS = 1, DN_SLOTS = 1;
   static constexpr int QROW = H / 2, SFROW = H / 16;        // one gate/up row
   static constexpr int UNIT_BYTES = 16 * QROW + 16 * SFROW; // 18 KiB
   static constexpr int DQROW = I / 2, DSFROW = I / 16;      // one Wd row
-  static constexpr int WQ = RS * DQROW;                     // slice codes, 4 KiB
-  static constexpr int WBYTES = WQ + RS * DSFROW;           // + scales, 4.5 KiB
-  static constexpr int HROWS_A = (SLOT - WBYTES) / THROW;   // h rows beside it: 3
+  static constexpr int DR = 64;                             // Wd rows per down unit
+  static constexpr int WQ = DR * DQROW;                     // codes, 16 KiB
+  static constexpr int WBYTES = WQ + DR * DSFROW;           // + block scales, 18 KiB
 };
 template <bool NV>
+constexpr int UNITS = I / Geo<NV>::GR;         // gate/up units per group
+template <bool NV>
+constexpr int ND = H / Geo<NV>::DR;            // down units per group
+template <bool NV>
 constexpr size_t smem_bytes() {
-  return (size_t)Geo<NV>::NS * Geo<NV>::SLOT + XS_BYTES + BUF_BYTES + LACC_BYTES;
+  return (size_t)Geo<NV>::NS * Geo<NV>::SLOT + XS_BYTES + BUF_BYTES;
 }
+constexpr int NQ = 8;                          // down units posted and not yet released
+// Down units take their h rows from the activations' buffer, which the gate/up
+// units no longer need by then: a ring of HROWS tagged rows.
+constexpr int HROWS = XS_BYTES / THROW;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
 enum : int { IT_GATE = 0, IT_UP = 1, IT_DOWN = 2, IT_DOWN2 = 3, IT_END = 4 };
 static_assert(S == 1 && MAXB <= GROUP_MAX, "one shared group at these batches");
 static_assert(MAXG <= DONE_SHARED, "routed groups and the shared group have distinct counters");
+static_assert(DONE_SHARED < 64, "one bit per counter in a 64-bit mask");
 static_assert(SYNC_LINES <= CT, "one thread clears each counter line");
-static_assert(Geo<false>::HROWS_A == 4 && MAXB - 4 <= Geo<false>::SLOT / THROW,
-              "a BF16 down item fits two slots");
-static_assert(Geo<true>::HROWS_A == 3 && MAXB - 3 <= Geo<true>::SLOT / THROW,
-              "an NVFP4 down item fits two slots");
-static_assert(8 * ROWB == Geo<false>::SLOT, "8 gate (or up) rows fill one BF16 slot");
-static_assert(Geo<true>::UNIT_BYTES <= Geo<true>::SLOT, "an NVFP4 unit fits one slot");
-static_assert(Geo<true>::WBYTES % 16 == 0, "h rows start 16-byte aligned");
+static_assert(Geo<false>::GR * ROWB == Geo<false>::SLOT, "8 gate (or up) rows fill one BF16 slot");
+static_assert(Geo<false>::DR / 2 * WROW == Geo<false>::SLOT, "32 Wd rows fill one BF16 slot");
+static_assert(Geo<true>::UNIT_BYTES <= Geo<true>::SLOT && Geo<true>::WBYTES <= Geo<true>::SLOT,
+              "an NVFP4 unit's weights fit one slot");
+static_assert(HROWS == 8 && MAXB <= HROWS, "a group's h rows fit the h ring");
+static_assert(Geo<false>::NS <= NQ && Geo<true>::NS <= NQ, "every posted down unit has a queue entry");
+static_assert(H % Geo<false>::DR == 0 && H % Geo<true>::DR == 0, "row blocks tile H");
 static_assert((E + RMAX - 1) / RMAX <= 86, "grids of 86 CTAs or more keep <= RMAX router rows");
 static_assert(smem_bytes<false>() + 6 * 1024 <= 232448 && smem_bytes<true>() + 6 * 1024 <= 232448,
               "fits the opt-in shared memory of one SM");
@@ -131,23 +131,15 @@ namespace {
 // What a ring slot holds (written by the producer before it arms the slot).
 struct Item {
   int kind;
-  int blk;       // gate/up: block of 8 intermediate rows
+  int blk;       // gate/up: block of GR intermediate rows; down: block of DR output rows
   int pair0;     // first h row (pair) of the group
   int n;         // tokens in the group
   int tok0;      // gate/up of the shared group: first token (tokens are consecutive), else -1
   int done_idx;  // completion counter of the group
   int expert;    // expert of the group (E + s for shared expert s)
-  int pad;
+  int h0;        // down: the group's first row in the h ring
 };
 
-__device__ __forceinline__ int ld_acquire_cta_shared(const int* p) {
-  int v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_cta_shared(int* p, int v) {
-  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
-}
 // Non-blocking probe of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t done;
@@ -437,281 +429,195 @@ __device__ __forceinline__ void unit_nv(const uint8_t* st, const uint16_t* xh,
   unit_finish<true>(acc, buf, th, d, ok, tag, done, ucnt, ts_g, ts_u);
 }
 
-// Shared context of the down items.
+// Sums of four values over the 32 lanes of a warp in six shuffles: lane l
+// ends with the sum of value ((l >> 4) & 1) * 2 + ((l >> 3) & 1).  Each lane
+// keeps half of its values and adds its partner's copy of them (lanes l and
+// l ^ 16, then l ^ 8), then the last three rounds add plainly.  A fixed
+// pattern, so the sums are reproducible.
+__device__ __forceinline__ float reduce4(float s0, float s1, float s2, float s3) {
+  const int lane = threadIdx.x & 31;
+  const bool up = (lane & 16) != 0, mid = (lane & 8) != 0;
+  float a0 = up ? s2 : s0, a1 = up ? s3 : s1;
+  const float b0 = up ? s0 : s2, b1 = up ? s1 : s3;
+  a0 += __shfl_xor_sync(0xffffffffu, b0, 16);
+  a1 += __shfl_xor_sync(0xffffffffu, b1, 16);
+  float c = mid ? a1 : a0;
+  c += __shfl_xor_sync(0xffffffffu, mid ? a0 : a1, 8);
+  c += __shfl_xor_sync(0xffffffffu, c, 4);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
+
+// Shared context of the down units.
 struct DnCtx {
-  const int* pair_tok;  // shared memory
   const float* pair_w;  // shared memory
-  float* lacc;          // CUDA-core running sums
-  float* acc;           // [MAXB][RS] tensor-core accumulators
-  float* red;           // [CW][RS][GROUP_MAX] partial tiles
   const uint64_t* th;   // tagged h (global), for words whose tag has not landed
+  uint64_t* ty;         // tagged y (global)
   uint32_t tag;
   uint64_t deadline;
   WsHeader* hdr;
   volatile int* abort_flag;
 };
 
-// h value k of a token's row (copy in shared memory at hrow, the tagged row
-// itself at src), confirmed against the call's tag.
-__device__ __forceinline__ float h_settled(const DnCtx& c, const uint8_t* hrow,
-                                           const uint64_t* src, int k) {
-  uint64_t w = *reinterpret_cast<const uint64_t*>(hrow + (size_t)k * 8);
-  if (!settle_tagged(w, src + k, c.tag, c.deadline)) {
-    *c.abort_flag = 1;
-    set_error(c.hdr, DEV_TIMEOUT);
+// Words k of a token's h row (q-th of `cnt`, columns given by col(q)) that do
+// not carry the call's tag yet are confirmed from the row's global copy and
+// written back into the shared copy (rare: the counters run behind the
+// stores).
+template <int CNT, class Col>
+__device__ __forceinline__ void settle_words(const DnCtx& c, const uint8_t* hrow, const uint64_t* src,
+                                             Col col) {
+  uint64_t* sw = reinterpret_cast<uint64_t*>(const_cast<uint8_t*>(hrow));
+#pragma unroll 1
+  for (int q = 0; q < CNT; ++q) {
+    const int k = col(q);
+    uint64_t w = sw[k];
+    if ((uint32_t)(w >> 32) != c.tag) {
+      if (!settle_tagged(w, src + k, c.tag, c.deadline)) {
+        *c.abort_flag = 1;
+        set_error(c.hdr, DEV_TIMEOUT);
+      }
+      sw[k] = w;
+    }
   }
-  return __uint_as_float((uint32_t)w);
 }
 
-// Down item on CUDA cores (<= 4 tokens): warp w owns Wd rows 2w and 2w+1 of
-// the slice; lane l takes columns 2l + 64m (+1), m < 8, which makes every
-// 128-bit load of tagged h words conflict-free.  The lane's 32 weights are
-// unpacked once and reused by every token; each token's two dot products run
-// as four independent chains; each lane adds w(t, g) times its partial sums to
-// its own running sums in shared memory -- the sums across lanes are taken
-// once, when the output is written.  A word whose tag has not landed sends
-// the warp through the same arithmetic with every value confirmed from global
-// memory (rare: the counters run behind the stores).
-__device__ __forceinline__ void down_cc(const DnCtx& c, const uint8_t* st, int pair0, int n,
-                                        bool ok, uint32_t em) {
+// The down units below read token i's h row at ring row (d.h0 + i) mod
+// HROWS of hb, and write y(p, row) = w(p) * (Wd h_p)[row] as tagged words.
+//
+// BF16 down unit on CUDA cores: 64 Wd rows in two slots (rows 0-31 in sa,
+// 32-63 in sb); warp w owns rows 4w .. 4w+3 of each slot; lane l takes
+// columns 2l + 64m (+1), m < 8, which makes every 128-bit load of tagged h
+// words conflict-free, and each h word serves all eight of the warp's rows.
+// Each token's eight row sums run as sixteen chains and meet in two reduce4;
+// lanes 0, 8, 16, 24 store the rows.
+__device__ __forceinline__ void down_cc(const DnCtx& c, const uint8_t* sa, const uint8_t* sb,
+                                        const uint8_t* hb, const Item& d, bool ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int tok[fz::CC_MAX];
-  float wt[fz::CC_MAX];
+  const int n = d.n;
+  if (!ok) return;
+  const uint32_t* wa = reinterpret_cast<const uint32_t*>(sa + (4 * warp) * fz::WROW);
+  const uint32_t* wb = reinterpret_cast<const uint32_t*>(sb + (4 * warp) * fz::WROW);
+  uint32_t va[4][8], vb[4][8];
 #pragma unroll
-  for (int i = 0; i < fz::CC_MAX; ++i) {  // the bookkeeping loads go out first
-    tok[i] = i < n ? c.pair_tok[pair0 + i] : 0;
-    wt[i] = i < n ? c.pair_w[pair0 + i] : 0.f;
-  }
-  float s0[fz::CC_MAX], s1[fz::CC_MAX];
-#pragma unroll
-  for (int i = 0; i < fz::CC_MAX; ++i) s0[i] = s1[i] = 0.f;
-  const uint32_t* w0 = reinterpret_cast<const uint32_t*>(st + (2 * warp) * fz::WROW);
-  const uint32_t* w1 = w0 + fz::WROW / 4;
-  if (ok) {
-    float f0[16], f1[16];
+  for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const uint32_t a0 = w0[lane + 32 * m], a1 = w1[lane + 32 * m];
-      f0[2 * m] = bf_lo(a0);
-      f0[2 * m + 1] = bf_hi(a0);
-      f1[2 * m] = bf_lo(a1);
-      f1[2 * m + 1] = bf_hi(a1);
+      va[r][m] = wa[r * (fz::WROW / 4) + lane + 32 * m];
+      vb[r][m] = wb[r * (fz::WROW / 4) + lane + 32 * m];
     }
-    bool bad = false;
+  const int row = d.blk * fz::Geo<false>::DR + 4 * warp + (lane >> 3);
 #pragma unroll
-    for (int i = 0; i < fz::CC_MAX; ++i) {
-      if (i < n) {
-        const uint4* hr =
-            reinterpret_cast<const uint4*>(st + fz::Geo<false>::WBYTES + i * fz::THROW);
-        float e0 = 0.f, o0 = 0.f, e1 = 0.f, o1 = 0.f;
+  for (int i = 0; i < fz::MAXB; ++i) {
+    if (i < n) {
+      const uint8_t* hrow = hb + ((d.h0 + i) & (fz::HROWS - 1)) * fz::THROW;
+      const uint4* hr = reinterpret_cast<const uint4*>(hrow);
+      float ea[4], oa[4], eb[4], ob[4];
+#pragma unroll 1
+      for (int attempt = 0;; ++attempt) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) ea[r] = oa[r] = eb[r] = ob[r] = 0.f;
+        bool bad = false;
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
           const uint4 hv = hr[lane + 32 * m];
           bad |= (hv.y != c.tag) | (hv.w != c.tag);
           const float h0 = __uint_as_float(hv.x), h1 = __uint_as_float(hv.z);
-          e0 = fmaf(f0[2 * m], h0, e0);
-          o0 = fmaf(f0[2 * m + 1], h1, o0);
-          e1 = fmaf(f1[2 * m], h0, e1);
-          o1 = fmaf(f1[2 * m + 1], h1, o1);
-        }
-        s0[i] = e0 + o0;
-        s1[i] = e1 + o1;
-      }
-    }
-    if (__any_sync(0xffffffffu, bad)) {
-      // Same sums, same order; weights re-read from the slot so that no
-      // register array is indexed at run time.
 #pragma unroll
-      for (int i = 0; i < fz::CC_MAX; ++i) {
-        float e0 = 0.f, o0 = 0.f, e1 = 0.f, o1 = 0.f;
-        if (i < n) {
-          const uint8_t* hrow = st + fz::Geo<false>::WBYTES + i * fz::THROW;
-          const uint64_t* src = c.th + (size_t)(pair0 + i) * I;
-#pragma unroll 1
-          for (int m = 0; m < 8; ++m) {
-            const int k = 2 * lane + 64 * m;
-            const uint32_t u0 = w0[lane + 32 * m], u1 = w1[lane + 32 * m];
-            const float h0 = h_settled(c, hrow, src, k);
-            const float h1 = h_settled(c, hrow, src, k + 1);
-            e0 = fmaf(bf_lo(u0), h0, e0);
-            o0 = fmaf(bf_hi(u0), h1, o0);
-            e1 = fmaf(bf_lo(u1), h0, e1);
-            o1 = fmaf(bf_hi(u1), h1, o1);
+          for (int r = 0; r < 4; ++r) {
+            ea[r] = fmaf(bf_lo(va[r][m]), h0, ea[r]);
+            oa[r] = fmaf(bf_hi(va[r][m]), h1, oa[r]);
+            eb[r] = fmaf(bf_lo(vb[r][m]), h0, eb[r]);
+            ob[r] = fmaf(bf_hi(vb[r][m]), h1, ob[r]);
           }
         }
-        s0[i] = e0 + o0;
-        s1[i] = e1 + o1;
+        if (attempt > 0 || !__any_sync(0xffffffffu, bad)) break;
+        settle_words<16>(c, hrow, c.th + (size_t)(d.pair0 + i) * I,
+                         [lane](int q) { return 2 * lane + 64 * (q >> 1) + (q & 1); });
+        __syncwarp();
       }
-    }
-  }
-  release_slot(em);
-  if (!ok) return;
-#pragma unroll
-  for (int i = 0; i < fz::CC_MAX; ++i) {
-    if (i < n) {
-      float* acc = c.lacc + (2 * tok[i]) * fz::LACC_STRIDE + threadIdx.x;
-      acc[0] = fmaf(wt[i], s0[i], acc[0]);
-      acc[fz::LACC_STRIDE] = fmaf(wt[i], s1[i], acc[fz::LACC_STRIDE]);
+      const float ya = reduce4(ea[0] + oa[0], ea[1] + oa[1], ea[2] + oa[2], ea[3] + oa[3]);
+      const float yb = reduce4(eb[0] + ob[0], eb[1] + ob[1], eb[2] + ob[2], eb[3] + ob[3]);
+      if ((lane & 7) == 0) {
+        const float w = c.pair_w[d.pair0 + i];
+        uint64_t* yp = c.ty + (size_t)(d.pair0 + i) * H + row;
+        st_tagged(yp, w * ya, c.tag);
+        st_tagged(yp + 32, w * yb, c.tag);
+      }
     }
   }
 }
 
-// Down item on tensor cores (5..8 tokens, h rows 0..3 beside the Wd slice in
-// slot A, rows 4.. in slot B): mma.sync m16n8k16 with the 16 Wd rows as M and
-// the tokens as N; the fp32 h is split into two bf16 parts (hi + lo, two
-// MMAs) so the operand keeps ~16 significant bits; warp w owns a 64-column
-// K-slice; the 8 partial tiles are summed through shared memory and weighted
-// into the CTA's accumulators.
-__device__ __forceinline__ void down_mma(const DnCtx& c, const uint8_t* sa, const uint8_t* sb,
-                                         int pair0, int n, bool ok) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, q = lane & 3;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const uint8_t* rlo = sa + g * fz::WROW + (warp * 64 + q * 8) * 2;
-  const uint8_t* rhi = rlo + 8 * fz::WROW;
-  using Gm = fz::Geo<false>;
-  const uint8_t* hrow = g < Gm::HROWS_A ? sa + Gm::WBYTES + g * fz::THROW
-                                        : sb + (g - Gm::HROWS_A) * fz::THROW;
-  if (ok) {
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      const uint4 alo = *reinterpret_cast<const uint4*>(rlo + kb * 64);
-      const uint4 ahi = *reinterpret_cast<const uint4*>(rhi + kb * 64);
-      // h (fp32) = hi + lo with both parts bf16: two MMAs keep ~16 bits of h.
-      uint32_t b[4] = {0u, 0u, 0u, 0u}, l[4] = {0u, 0u, 0u, 0u};
-      if (g < n) {
-        const int k0 = warp * 64 + kb * 32 + q * 8;
-        float hv[8];
-        bool bad = false;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 w = *reinterpret_cast<const uint4*>(hrow + (size_t)(k0 + 2 * j) * 8);
-          bad |= (w.y != c.tag) | (w.w != c.tag);
-          hv[2 * j] = __uint_as_float(w.x);
-          hv[2 * j + 1] = __uint_as_float(w.z);
-        }
-        if (bad) {
-          const uint64_t* src = c.th + (size_t)(pair0 + g) * I;
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            hv[j] = h_settled(c, hrow, src, k0 + j);
-        }
-        split_bf2(hv[0], hv[1], b[0], l[0]);
-        split_bf2(hv[2], hv[3], b[1], l[1]);
-        split_bf2(hv[4], hv[5], b[2], l[2]);
-        split_bf2(hv[6], hv[7], b[3], l[3]);
-      }
-      mma_bf16(acc, alo.x, ahi.x, alo.y, ahi.y, b[0], b[1]);
-      mma_bf16(acc, alo.z, ahi.z, alo.w, ahi.w, b[2], b[3]);
-      mma_bf16(acc, alo.x, ahi.x, alo.y, ahi.y, l[0], l[1]);
-      mma_bf16(acc, alo.z, ahi.z, alo.w, ahi.w, l[2], l[3]);
-    }
-  }
-  float* red = c.red + warp * fz::RS * GROUP_MAX;
-  const int col = 2 * q;
-  red[g * GROUP_MAX + col] = acc[0];
-  red[g * GROUP_MAX + col + 1] = acc[1];
-  red[(g + 8) * GROUP_MAX + col] = acc[2];
-  red[(g + 8) * GROUP_MAX + col + 1] = acc[3];
-  named_sync(1, fz::CT);
-  if (ok) {
-    for (int i = threadIdx.x; i < fz::RS * n; i += fz::CT) {
-      const int r = i & (fz::RS - 1), j = i >> 4;
-      float s = 0.f;
-#pragma unroll
-      for (int w = 0; w < fz::CW; ++w) s += c.red[(w * fz::RS + r) * GROUP_MAX + j];
-      const int t = c.pair_tok[pair0 + j];
-      const float wt = c.pair_w[pair0 + j];
-      c.acc[t * fz::RS + r] += wt * s;
-    }
-  }
-  named_sync(1, fz::CT);
-}
-
-// Down item of NVFP4 weights on CUDA cores (every group size; h rows 0..2
-// beside the slice in slot A, rows 3.. in slot B).  Warp w owns rows 2w and
-// 2w+1 of the 16-row slice; lane l takes columns 256hf + 8l .. +7 of each half
-// hf: one code word and one block scale per row and half, dequantised once
-// (exact in f16, then fp32).  The lane visits its four column pairs starting
-// at pair (l >> 1) & 3 -- which makes every quarter-warp's 128-bit loads of
-// tagged h words hit eight distinct bank groups -- and its code words are
-// rotated by as many bytes to match.  Each token's two dot products run as
-// four chains; the lane adds w(t, g) * ts times its partial sums to its own
-// running sums, as the BF16 items do.
-__device__ __forceinline__ void down_nv(const DnCtx& c, const uint8_t* sa, const uint8_t* sb,
-                                        int pair0, int n, float ts, bool ok) {
+// NVFP4 down unit on CUDA cores: the slot's 64 Wd rows (codes, then block
+// scales).  Warp w owns rows 8w .. 8w+7, four at a time; lane l takes columns
+// 256hf + 8l .. +7 of each half hf: one code word and one block scale per row
+// and half, dequantised once to f16 (exact) and widened to fp32 where used.
+// The lane visits its four column pairs starting at pair (l >> 1) & 3 --
+// which makes every quarter-warp's 128-bit loads of tagged h words hit eight
+// distinct bank groups -- and its code words are rotated by as many bytes to
+// match.  The tensor scale joins the routing weight.
+__device__ __forceinline__ void down_nv(const DnCtx& c, const uint8_t* sw, const uint8_t* hb,
+                                        const Item& d, float ts, bool ok) {
   using Gm = fz::Geo<true>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int tok[fz::MAXB];
-  float wt[fz::MAXB];
-#pragma unroll
-  for (int i = 0; i < fz::MAXB; ++i) {
-    tok[i] = i < n ? c.pair_tok[pair0 + i] : 0;
-    wt[i] = i < n ? c.pair_w[pair0 + i] * ts : 0.f;
-  }
+  const int n = d.n;
   if (!ok) return;
   const int rot = (lane >> 1) & 3;
-  float f[2][2][8];  // [row][half][column pair j (visiting order), even/odd]
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int row0 = 8 * warp + 4 * pass;  // first of this pass's rows within the unit
+    uint32_t wf[4][2][4];  // [row][half][column pair j, visiting order]: f16x2 weights
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int row = 2 * warp + rr;
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      uint32_t wv = *reinterpret_cast<const uint32_t*>(sa + row * Gm::DQROW + hf * 128 + 4 * lane);
-      wv = __funnelshift_r(wv, wv, 8 * rot);
-      const uint32_t sc = nvu::e4m3_bcast_f16x2(sa[Gm::WQ + row * Gm::DSFROW + 16 * hf + (lane >> 1)]);
-      uint32_t pv[4];
-      nvu::e2m1x8_to_f16x2(wv, pv[0], pv[1], pv[2], pv[3]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t v = nvu::hmul2(pv[j], sc);
-        const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&v));
-        f[rr][hf][2 * j] = fv.x;
-        f[rr][hf][2 * j + 1] = fv.y;
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < fz::MAXB; ++i) {
-    if (i < n) {
-      const uint8_t* hrow = i < Gm::HROWS_A ? sa + Gm::WBYTES + i * fz::THROW
-                                            : sb + (i - Gm::HROWS_A) * fz::THROW;
-      const uint4* hr = reinterpret_cast<const uint4*>(hrow);
-      float e0 = 0.f, o0 = 0.f, e1 = 0.f, o1 = 0.f;
-      bool bad = false;
+    for (int rr = 0; rr < 4; ++rr) {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
+        uint32_t wv =
+            *reinterpret_cast<const uint32_t*>(sw + (row0 + rr) * Gm::DQROW + hf * 128 + 4 * lane);
+        wv = __funnelshift_r(wv, wv, 8 * rot);
+        const uint32_t sc =
+            nvu::e4m3_bcast_f16x2(sw[Gm::WQ + (row0 + rr) * Gm::DSFROW + 16 * hf + (lane >> 1)]);
+        uint32_t pv[4];
+        nvu::e2m1x8_to_f16x2(wv, pv[0], pv[1], pv[2], pv[3]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 hv = hr[128 * hf + 4 * lane + ((j + rot) & 3)];
-          bad |= (hv.y != c.tag) | (hv.w != c.tag);
-          const float h0 = __uint_as_float(hv.x), h1 = __uint_as_float(hv.z);
-          e0 = fmaf(f[0][hf][2 * j], h0, e0);
-          o0 = fmaf(f[0][hf][2 * j + 1], h1, o0);
-          e1 = fmaf(f[1][hf][2 * j], h0, e1);
-          o1 = fmaf(f[1][hf][2 * j + 1], h1, o1);
-        }
+        for (int j = 0; j < 4; ++j) wf[rr][hf][j] = nvu::hmul2(pv[j], sc);
       }
-      if (__any_sync(0xffffffffu, bad)) {  // same sums, every value confirmed
-        const uint64_t* src = c.th + (size_t)(pair0 + i) * I;
-        e0 = o0 = e1 = o1 = 0.f;
+    }
+    const int row = d.blk * Gm::DR + row0 + (lane >> 3);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+    for (int i = 0; i < fz::MAXB; ++i) {
+      if (i < n) {
+        const uint8_t* hrow = hb + ((d.h0 + i) & (fz::HROWS - 1)) * fz::THROW;
+        const uint4* hr = reinterpret_cast<const uint4*>(hrow);
+        float e[4], o[4];
+#pragma unroll 1
+        for (int attempt = 0;; ++attempt) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int k = 256 * hf + 8 * lane + 2 * ((j + rot) & 3);
-            const float h0 = h_settled(c, hrow, src, k);
-            const float h1 = h_settled(c, hrow, src, k + 1);
-            e0 = fmaf(f[0][hf][2 * j], h0, e0);
-            o0 = fmaf(f[0][hf][2 * j + 1], h1, o0);
-            e1 = fmaf(f[1][hf][2 * j], h0, e1);
-            o1 = fmaf(f[1][hf][2 * j + 1], h1, o1);
+          for (int r = 0; r < 4; ++r) e[r] = o[r] = 0.f;
+          bool bad = false;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 hv = hr[128 * hf + 4 * lane + ((j + rot) & 3)];
+              bad |= (hv.y != c.tag) | (hv.w != c.tag);
+              const float h0 = __uint_as_float(hv.x), h1 = __uint_as_float(hv.z);
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                const float2 w2 = __half22float2(*reinterpret_cast<const __half2*>(&wf[r][hf][j]));
+                e[r] = fmaf(w2.x, h0, e[r]);
+                o[r] = fmaf(w2.y, h1, o[r]);
+              }
+            }
           }
+          if (attempt > 0 || !__any_sync(0xffffffffu, bad)) break;
+          settle_words<16>(c, hrow, c.th + (size_t)(d.pair0 + i) * I,
+                           [lane](int q) { return 256 * (q >> 3) + 8 * lane + (q & 7); });
+          __syncwarp();
         }
+        const float v = reduce4(e[0] + o[0], e[1] + o[1], e[2] + o[2], e[3] + o[3]);
+        if ((lane & 7) == 0)
+          st_tagged(c.ty + (size_t)(d.pair0 + i) * H + row, (c.pair_w[d.pair0 + i] * ts) * v, c.tag);
       }
-      float* acc = c.lacc + (2 * tok[i]) * fz::LACC_STRIDE + threadIdx.x;
-      acc[0] = fmaf(wt[i], e0 + o0, acc[0]);
-      acc[fz::LACC_STRIDE] = fmaf(wt[i], e1 + o1, acc[fz::LACC_STRIDE]);
     }
   }
 }
@@ -721,36 +627,23 @@ __device__ __forceinline__ void down_nv(const DnCtx& c, const uint8_t* sa, const
 struct Prod {
   uint32_t full0, empty0, stages_addr;
   Item* desc;
-  int it;
-  uint64_t deadline;
-  WsHeader* hdr;
-  volatile int* abort_flag;
+  int it;  // ring iterations issued
 };
 
+// The next ring slot (the caller has seen it free).
 template <bool NV>
-__device__ __forceinline__ bool take_slot(Prod& p, int& slot) {
-  constexpr int NS = fz::Geo<NV>::NS;
-  slot = p.it % NS;
-  if (p.it >= NS &&
-      !mbar_wait(p.empty0 + 8u * slot, (uint32_t)((p.it / NS) - 1) & 1u, p.deadline)) {
-    *p.abort_flag = 1;
-    set_error(p.hdr, DEV_TIMEOUT);
-    return false;
-  }
-  if (*p.abort_flag) return false;
-  ++p.it;
-  return true;
+__device__ __forceinline__ int next_slot(Prod& p) {
+  return p.it++ % fz::Geo<NV>::NS;
 }
 
-// The END slot: armed by a plain arrive (posted even after an abort; waits
-// out the drain bound for its slot).
+// The END slot: armed by a plain arrive; waits out the drain bound for its
+// slot (the consumers release every slot they take, also after an abort).
 template <bool NV>
-__device__ __forceinline__ void post_end(Prod& p) {
+__device__ __forceinline__ void post_end(Prod& p, uint64_t deadline) {
   constexpr int NS = fz::Geo<NV>::NS;
   const int slot = p.it % NS;
   if (p.it >= NS)
-    mbar_wait(p.empty0 + 8u * slot, (uint32_t)((p.it / NS) - 1) & 1u,
-              p.deadline + fz::DRAIN_NS);
+    mbar_wait(p.empty0 + 8u * slot, (uint32_t)((p.it / NS) - 1) & 1u, deadline + fz::DRAIN_NS);
   ++p.it;
   Item d = {};
   d.kind = fz::IT_END;
@@ -761,11 +654,10 @@ __device__ __forceinline__ void post_end(Prod& p) {
 // A gate/up unit (BF16: gate rows g and up rows u, 32 KiB each, in two slots;
 // NVFP4: gate codes g, up codes u, gate scales gs, up scales us in one slot).
 template <bool NV>
-__device__ __forceinline__ bool post_gateup(Prod& p, const uint8_t* g, const uint8_t* u,
+__device__ __forceinline__ void post_gateup(Prod& p, const uint8_t* g, const uint8_t* u,
                                             const uint8_t* gs, const uint8_t* us, const Item& d) {
   using Gm = fz::Geo<NV>;
-  int sa, sb;
-  if (!take_slot<NV>(p, sa)) return false;
+  const int sa = next_slot<NV>(p);
   p.desc[sa] = d;
   const uint32_t bar = p.full0 + 8u * sa, dst = p.stages_addr + sa * Gm::SLOT;
   if constexpr (NV) {
@@ -774,60 +666,63 @@ __device__ __forceinline__ bool post_gateup(Prod& p, const uint8_t* g, const uin
     bulk_g2s_stream(dst + 8 * Gm::QROW, u, 8 * Gm::QROW, bar);
     bulk_g2s_stream(dst + 16 * Gm::QROW, gs, 8 * Gm::SFROW, bar);
     bulk_g2s_stream(dst + 16 * Gm::QROW + 8 * Gm::SFROW, us, 8 * Gm::SFROW, bar);
-    return true;
   } else {
     mbar_expect_tx(bar, Gm::SLOT);
     bulk_g2s_stream(dst, g, Gm::SLOT, bar);
-    if (!take_slot<NV>(p, sb)) return false;  // the END posted next takes the up half's place
+    const int sb = next_slot<NV>(p);
     Item du = d;
     du.kind = fz::IT_UP;
     p.desc[sb] = du;
     mbar_expect_tx(p.full0 + 8u * sb, Gm::SLOT);
     bulk_g2s_stream(p.stages_addr + sb * Gm::SLOT, u, Gm::SLOT, p.full0 + 8u * sb);
-    return true;
   }
 }
 
-// A down item's slots: its Wd slice (issued now) and room for its tagged h
-// rows (counted now, copied once the group is complete).  Returns false on
-// abort; `sl` receives the slots (second -1 for items of <= 4 tokens).
-// (BF16: the 16-row Wd slice wq; NVFP4: its codes wq and block scales wsf.)
+// A down unit's Wd rows (BF16: 64 rows wq, 32 per slot; NVFP4: codes wq and
+// scales wsf in one slot), copied now, and the tx count of its h rows, which
+// post_down_h copies into the h ring once the group is complete.  Returns the
+// slot whose barrier the h rows complete.
 template <bool NV>
-__device__ __forceinline__ bool post_down_w(Prod& p, const Item& d, const uint8_t* wq,
-                                            const uint8_t* wsf, int* sl) {
+__device__ __forceinline__ int post_down_w(Prod& p, const Item& d, const uint8_t* wq,
+                                           const uint8_t* wsf) {
   using Gm = fz::Geo<NV>;
-  sl[1] = -1;
-  if (!take_slot<NV>(p, sl[0])) return false;
-  const int na = d.n < Gm::HROWS_A ? d.n : Gm::HROWS_A;
-  p.desc[sl[0]] = d;
-  const uint32_t bar = p.full0 + 8u * sl[0], dst = p.stages_addr + sl[0] * Gm::SLOT;
-  mbar_expect_tx(bar, Gm::WBYTES + na * fz::THROW);
+  const int sa = next_slot<NV>(p);
+  p.desc[sa] = d;
+  const uint32_t bar = p.full0 + 8u * sa, dst = p.stages_addr + sa * Gm::SLOT;
   if constexpr (NV) {
+    mbar_expect_tx(bar, Gm::WBYTES + d.n * fz::THROW);
     bulk_g2s_stream(dst, wq, Gm::WQ, bar);
     bulk_g2s_stream(dst + Gm::WQ, wsf, Gm::WBYTES - Gm::WQ, bar);
   } else {
-    bulk_g2s_stream(dst, wq, Gm::WBYTES, bar);
-  }
-  if (d.n > Gm::HROWS_A) {
-    if (!take_slot<NV>(p, sl[1])) return false;
+    mbar_expect_tx(bar, Gm::SLOT + d.n * fz::THROW);
+    bulk_g2s_stream(dst, wq, Gm::SLOT, bar);
+    const int sb = next_slot<NV>(p);
     Item d2 = d;
     d2.kind = fz::IT_DOWN2;
-    p.desc[sl[1]] = d2;
-    mbar_expect_tx(p.full0 + 8u * sl[1], (d.n - Gm::HROWS_A) * fz::THROW);
+    p.desc[sb] = d2;
+    mbar_expect_tx(p.full0 + 8u * sb, Gm::SLOT);
+    bulk_g2s_stream(p.stages_addr + sb * Gm::SLOT, wq + Gm::SLOT, Gm::SLOT, p.full0 + 8u * sb);
   }
-  return true;
+  return sa;
 }
 
-template <bool NV>
-__device__ __forceinline__ void post_down_h(Prod& p, const Item& d, const uint64_t* hr,
-                                            const int* sl) {
-  using Gm = fz::Geo<NV>;
-  const int na = d.n < Gm::HROWS_A ? d.n : Gm::HROWS_A;
-  bulk_g2s(p.stages_addr + sl[0] * Gm::SLOT + Gm::WBYTES, hr, na * fz::THROW,
-           p.full0 + 8u * sl[0]);
-  if (sl[1] >= 0)
-    bulk_g2s(p.stages_addr + sl[1] * Gm::SLOT, hr + (size_t)na * I, (d.n - na) * fz::THROW,
-             p.full0 + 8u * sl[1]);
+// The group's h rows hr (tagged, n of them) into ring rows d.h0 .. (mod
+// HROWS) of the h ring at hring, completing the unit's first slot.
+__device__ __forceinline__ void post_down_h(const Prod& p, const Item& d, const uint64_t* hr,
+                                            uint32_t hring, int slot) {
+  const int run = d.n < fz::HROWS - d.h0 ? d.n : fz::HROWS - d.h0;
+  const uint32_t bar = p.full0 + 8u * slot;
+  bulk_g2s(hring + d.h0 * fz::THROW, hr, run * fz::THROW, bar);
+  if (run < d.n) bulk_g2s(hring, hr + (size_t)run * I, (d.n - run) * fz::THROW, bar);
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_cta_shared_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta_shared_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.cta.shared::cta.u64 [%0], %1;" ::"r"(smem_addr(p)), "l"(v) : "memory");
 }
 
 }  // namespace
@@ -835,21 +730,26 @@ __device__ __forceinline__ void post_down_h(Prod& p, const Item& d, const uint64
 template <bool NV>
 __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
   using Gm = fz::Geo<NV>;
+  constexpr int ND = fz::ND<NV>;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ volatile int s_abort;
   __shared__ int s_ngroups;
-  __shared__ int s_ready;  // down items whose groups are complete (poll warp -> producer)
+  __shared__ uint64_t s_gmask;  // groups seen complete, by counter index (poll warp -> producer)
   __shared__ Item s_desc[Gm::NS];
   __shared__ int4 s_groups[fz::MAXG];
   __shared__ int s_pair_tok[fz::NPAIR];
   __shared__ float s_pair_w[fz::NPAIR];
-  __shared__ float s_acc[fz::MAXB * fz::RS];  // this CTA's 16 output rows per token
+  __shared__ int s_tokp[fz::MAXB][SLOTS];  // each token's pairs, ascending
   __shared__ LocalSelectSmem s_sel;
   __shared__ float s_part[2][4][8];
-  __shared__ int s_ucnt[fz::UCNT];  // consumer warps done with recent units
-  __shared__ int s_dslot[Gm::NS][2];  // producer: ring slots of its down items in flight
-  // ring full / empty, router rows, selection done
-  __shared__ __align__(8) uint64_t s_bars[2 * Gm::NS + 2];
+  __shared__ volatile int s_first_dn;  // ring iteration of this CTA's first down unit
+  __shared__ int s_ucnt[fz::UCNT];     // consumer warps done with recent units
+  // producer: down units posted, by post order -- the unit, the slot its h
+  // rows complete, its ring iteration and the h ring's fill after it
+  __shared__ Item s_pq[fz::NQ];
+  __shared__ int s_pq_slot[fz::NQ], s_pq_it[fz::NQ], s_pq_hend[fz::NQ];
+  // ring full / empty, router rows, selection done, activations' buffer free
+  __shared__ __align__(8) uint64_t s_bars[2 * Gm::NS + 3];
   WsHeader* hdr = a.ws.hdr;
   const int G = gridDim.x, cta = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -857,10 +757,9 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
   uint8_t* ring = smem;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + Gm::NS * Gm::SLOT);
   float* buf = reinterpret_cast<float*>(smem + Gm::NS * Gm::SLOT + fz::XS_BYTES);
-  float* lacc = reinterpret_cast<float*>(smem + Gm::NS * Gm::SLOT + fz::XS_BYTES + fz::BUF_BYTES);
   const uint32_t full0 = smem_addr(s_bars), empty0 = smem_addr(s_bars + Gm::NS);
   const uint32_t rrow_bar = smem_addr(s_bars + 2 * Gm::NS);
-  const uint32_t sel_bar = rrow_bar + 8u;
+  const uint32_t sel_bar = rrow_bar + 8u, xs_bar = rrow_bar + 16u;
   const int e_begin = (int)((long long)cta * E / G), e_end = (int)((long long)(cta + 1) * E / G);
 
   if (warp == fz::PRODUCER && lane == 0) {
@@ -870,6 +769,7 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     }
     mbar_init(rrow_bar, 1);
     mbar_init(sel_bar, 1);
+    mbar_init(xs_bar, fz::CW);
     fence_mbar_init();
     // The router rows are weights: nothing the preceding kernel writes.
     const uint32_t rb = (uint32_t)(e_end - e_begin) * (H * 2);
@@ -877,11 +777,10 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     bulk_g2s_stream(smem_addr(buf), r.wr + (size_t)e_begin * H, rb, rrow_bar);
     s_abort = 0;
     s_ngroups = 0;
-    s_ready = 0;
+    s_gmask = 0ull;
+    s_first_dn = 0x7fffffff;
   }
   if (tid < fz::UCNT) s_ucnt[tid] = 0;
-  for (int i = tid; i < fz::MAXB * fz::RS; i += blockDim.x) s_acc[i] = 0.f;
-  for (int i = tid; i < fz::LACC_BYTES / 4; i += blockDim.x) lacc[i] = 0.f;
   __syncthreads();
   // Launched with programmatic serialization: the set-up above overlaps the
   // preceding kernel; x and the workspace are read only after it.
@@ -891,8 +790,6 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
   const uint32_t par = epoch & 1u, tag = call_tag(epoch);
   SyncLine* sync = hdr->sync[par];
   SyncLine* done = sync;  // completion counters: lines 0 .. SYNC_GROUPS-1
-  const bool owner = cta < fz::DOWN_CTAS;
-  const int r0 = cta * fz::RS;
   const int npairs = B * TOPK;
 
   if (warp == fz::PRODUCER) {  // ---------------- producer warp (lane 0 issues)
@@ -903,182 +800,180 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     p.stages_addr = smem_addr(ring);
     p.desc = s_desc;
     p.it = 0;
-    p.deadline = deadline;
-    p.hdr = hdr;
-    p.abort_flag = &s_abort;
     uint32_t* claim = &sync[SYNC_UNIT].v;
-    int u = (int)atomicAdd(claim, 1u);    // unit being issued
+    int u = (int)atomicAdd(claim, 1u);    // unit to post next
     int nxt = (int)atomicAdd(claim, 1u);  // claimed ahead
-    bool meta = false, claims_open = true;
-    int total = 0x7fffffff, ng = 0, ndn = 0;
-    // Down items: the shared group first (its h is ready first), then the
-    // routed groups in table order.  kw: items whose Wd copy is issued, kh:
-    // items whose h copy is issued (kh <= kw; items in between were posted
-    // ahead with only their Wd slice, once this CTA had no gate/up left).
-    int kw = 0, kh = 0;
-    int (*dslot)[2] = s_dslot;  // ring slots of the down items in flight
+    bool meta = false, xs_free = false;
+    constexpr int UNITS = fz::UNITS<NV>;
+    int ng = 0, total_gu = UNITS, total = 0x7fffffff;
+    // Down units: [0, kh) have their h rows posted, [kh, kw) wait for them;
+    // [0, kf) are known released (their h rows free again: hf).  hw: h rows
+    // handed out.  rel: the last ring iteration known released.
+    int kw = 0, kh = 0, kf = 0, hw = 0, hf = 0, rel = -1;
     const uint64_t* const th = a.ws.th;
-    // Down item kk: the group's h rows and this CTA's slice of the expert's
-    // Wd (BF16: wq; NVFP4: codes wq and block scales wsf).
-    auto dn_item = [&](int kk, const uint8_t*& wq, const uint8_t*& wsf, const uint64_t*& hr) {
-      const int4 grp = s_groups[kk == 0 ? ng - 1 : kk - 1];
-      Item d = {};
-      d.kind = fz::IT_DOWN;
-      d.pair0 = grp.y;
-      d.n = grp.z;
-      d.expert = grp.x;
-      const bool routed = grp.x < E;
-      const size_t row0 = (size_t)(routed ? grp.x : grp.x - E) * H + r0;
-      if constexpr (NV) {
-        wq = (routed ? a.w.w2_q : a.w.ws2_q) + row0 * Gm::DQROW;
-        wsf = (routed ? a.w.w2_sf : a.w.ws2_sf) + row0 * Gm::DSFROW;
-      } else {
-        wq = reinterpret_cast<const uint8_t*>((routed ? a.w.w2 : a.w.ws2) + row0 * I);
-        wsf = nullptr;
-      }
-      hr = th + (size_t)grp.y * I;
-      return d;
+    const uint32_t hring = smem_addr(xs);
+    // true if the next `need` slots are free (the consumers release in ring
+    // order: all 8 warps take every item in turn)
+    auto slots_ok = [&](int need) {
+      const int j = p.it + need - 1 - Gm::NS;  // the iteration that must be released
+      if (j <= rel) return true;
+      if (!mbar_test(empty0 + 8u * ((j + Gm::NS) % Gm::NS), (uint32_t)(j / Gm::NS) & 1u)) return false;
+      rel = j;
+      return true;
     };
-    // Gate/up unit d of expert ex (E + s for shared expert s): its 8 gate and
-    // 8 up rows.
-    auto post_unit = [&](int ex, const Item& d) {
-      const bool routed = ex < E;
-      const size_t e = (size_t)(routed ? ex : ex - E);
-      const size_t gr = (size_t)d.blk * 8, ur = (size_t)I + d.blk * 8;
-      if constexpr (NV) {
-        const uint8_t* qb = (routed ? a.w.w13_q : a.w.ws13_q) + e * (2 * I) * Gm::QROW;
-        const uint8_t* sb = (routed ? a.w.w13_sf : a.w.ws13_sf) + e * (2 * I) * Gm::SFROW;
-        return post_gateup<true>(p, qb + gr * Gm::QROW, qb + ur * Gm::QROW, sb + gr * Gm::SFROW,
-                                 sb + ur * Gm::SFROW, d);
-      } else {
-        const uint16_t* base = (routed ? a.w.w13 : a.w.ws13) + e * (2 * I) * H;
-        return post_gateup<false>(p, reinterpret_cast<const uint8_t*>(base + gr * H),
-                                  reinterpret_cast<const uint8_t*>(base + ur * H), nullptr,
-                                  nullptr, d);
+    // retires the posted down units the consumers have released (their queue
+    // entries and h rows are free again); a slot is tested only while it still
+    // holds the iteration (later ones are posted only after rel passed it)
+    auto reap = [&]() {
+      while (kf < kw) {
+        const int j = s_pq_it[kf % fz::NQ];
+        if (j > rel && !mbar_test(empty0 + 8u * (j % Gm::NS), (uint32_t)(j / Gm::NS) & 1u)) break;
+        hf = s_pq_hend[kf % fz::NQ];
+        ++kf;
       }
     };
-    bool ok = true;
-    int dn_budget = 0;  // ready down items still allowed before the claimed unit
-    while (ok && !s_abort) {
-      // Down items whose groups the poll warp has seen complete.
-      const int rdy = meta && kh < ndn ? ld_acquire_cta_shared(&s_ready) : 0;
-      const bool unit_pending = claims_open && (u < fz::UNITS || (meta && u < total));
-      if (rdy > kh && (!unit_pending || dn_budget > 0)) {
-        const uint8_t *wq, *wsf;
-        const uint64_t* hr;
-        const Item d = dn_item(kh, wq, wsf, hr);
-        if (kh >= kw) {
-          if (!(ok = post_down_w<NV>(p, d, wq, wsf, dslot[kh % Gm::NS]))) break;
-          kw = kh + 1;
+    while (!s_abort) {
+      // 1. the oldest down unit waiting for h, once its group is complete and
+      //    the consumers are done with the activations' buffer
+      if (kh < kw) {
+        const Item& pd = s_pq[kh % fz::NQ];
+        if (!xs_free) xs_free = mbar_test(xs_bar, 0u);
+        if (xs_free && ((ld_acquire_cta_shared_u64(&s_gmask) >> pd.done_idx) & 1ull)) {
+          post_down_h(p, pd, th + (size_t)pd.pair0 * I, hring, s_pq_slot[kh % fz::NQ]);
+          ++kh;
+          continue;
         }
-        post_down_h<NV>(p, d, hr, dslot[kh % Gm::NS]);
-        ++kh;
-        --dn_budget;
-        continue;
       }
-      if (claims_open && u < fz::UNITS) {  // shared expert: tokens 0..B-1, pairs after the routed ones
-        Item d = {};
-        d.kind = fz::IT_GATE;
-        d.blk = u;
-        d.pair0 = npairs;
-        d.n = B;
-        d.tok0 = 0;
-        d.done_idx = fz::DONE_SHARED;
-        d.expert = E;
-        ok = post_unit(E, d);
-        u = nxt;
-        nxt = (int)atomicAdd(claim, 1u);
-        dn_budget = fz::DN_PER_UNIT;
-        continue;
-      }
-      if (!meta) {
+      // 2. the next claimed unit, if its slots are free
+      if (!meta && u >= UNITS) {  // beyond the shared expert: needs the routing
         if (!mbar_wait(sel_bar, 0u, deadline)) {
           s_abort = 1;
           set_error(hdr, DEV_TIMEOUT);
           break;
         }
         ng = s_ngroups;
-        total = ng * fz::UNITS;  // the shared group's units and the routed ones
-        ndn = owner ? ng : 0;
+        total_gu = ng * UNITS;  // the shared group's units and the routed ones
+        total = total_gu + ng * ND;
         meta = true;
         continue;
       }
-      if (claims_open && u < total) {
-        const int ru = u - fz::UNITS;
-        const int gi = ru / fz::UNITS;
-        const int4 grp = s_groups[gi];
-        Item d = {};
-        d.kind = fz::IT_GATE;
-        d.blk = ru % fz::UNITS;
-        d.pair0 = grp.y;
-        d.n = grp.z;
-        d.tok0 = -1;
-        d.done_idx = gi;
-        d.expert = grp.x;
-        ok = post_unit(grp.x, d);
+      bool posted = false;
+      if (u < total_gu) {  // gate/up unit
+        if (slots_ok(Gm::UNIT_SLOTS)) {
+          Item d = {};
+          d.kind = fz::IT_GATE;
+          if (u < UNITS) {  // shared expert: tokens 0..B-1, pairs after the routed ones
+            d.blk = u;
+            d.pair0 = npairs;
+            d.n = B;
+            d.tok0 = 0;
+            d.done_idx = fz::DONE_SHARED;
+            d.expert = E;
+          } else {
+            const int ru = u - UNITS, gi = ru / UNITS;
+            const int4 grp = s_groups[gi];
+            d.blk = ru % UNITS;
+            d.pair0 = grp.y;
+            d.n = grp.z;
+            d.tok0 = -1;
+            d.done_idx = gi;
+            d.expert = grp.x;
+          }
+          const bool routed = d.expert < E;
+          const size_t e = (size_t)(routed ? d.expert : d.expert - E);
+          const size_t gr = (size_t)d.blk * Gm::GR, ur = (size_t)I + d.blk * Gm::GR;
+          if constexpr (NV) {
+            const uint8_t* qb = (routed ? a.w.w13_q : a.w.ws13_q) + e * (2 * I) * Gm::QROW;
+            const uint8_t* sb = (routed ? a.w.w13_sf : a.w.ws13_sf) + e * (2 * I) * Gm::SFROW;
+            post_gateup<true>(p, qb + gr * Gm::QROW, qb + ur * Gm::QROW, sb + gr * Gm::SFROW,
+                              sb + ur * Gm::SFROW, d);
+          } else {
+            const uint16_t* base = (routed ? a.w.w13 : a.w.ws13) + e * (2 * I) * H;
+            post_gateup<false>(p, reinterpret_cast<const uint8_t*>(base + gr * H),
+                               reinterpret_cast<const uint8_t*>(base + ur * H), nullptr, nullptr, d);
+          }
+          posted = true;
+        }
+      } else if (u < total) {  // down unit: group k (the shared group first), row block rb
+        const int dc = u - total_gu, k = dc / ND, rb = dc % ND;
+        const int4 grp = s_groups[k == 0 ? ng - 1 : k - 1];
+        reap();
+        if (kw - kf < fz::NQ && hw + grp.z - hf <= fz::HROWS && slots_ok(Gm::DN_SLOTS)) {
+          Item d = {};
+          d.kind = fz::IT_DOWN;
+          d.blk = rb;
+          d.pair0 = grp.y;
+          d.n = grp.z;
+          d.tok0 = -1;
+          d.done_idx = k == 0 ? fz::DONE_SHARED : k - 1;
+          d.expert = grp.x;
+          d.h0 = hw % fz::HROWS;
+          hw += grp.z;
+          const bool routed = grp.x < E;
+          const size_t row0 = (size_t)(routed ? grp.x : grp.x - E) * H + (size_t)rb * Gm::DR;
+          const uint8_t *wq, *wsf;
+          if constexpr (NV) {
+            wq = (routed ? a.w.w2_q : a.w.ws2_q) + row0 * Gm::DQROW;
+            wsf = (routed ? a.w.w2_sf : a.w.ws2_sf) + row0 * Gm::DSFROW;
+          } else {
+            wq = reinterpret_cast<const uint8_t*>((routed ? a.w.w2 : a.w.ws2) + row0 * I);
+            wsf = nullptr;
+          }
+          const int q = kw % fz::NQ;
+          if (kw == 0) s_first_dn = p.it;  // from here on the consumers release xs
+          s_pq[q] = d;
+          s_pq_it[q] = p.it;
+          s_pq_hend[q] = hw;
+          s_pq_slot[q] = post_down_w<NV>(p, d, wq, wsf);
+          ++kw;
+          posted = true;
+        }
+      } else if (kh == kw) {
+        break;  // every claimed unit is posted
+      }
+      if (posted) {
         u = nxt;
         nxt = (int)atomicAdd(claim, 1u);
-        dn_budget = fz::DN_PER_UNIT;
         continue;
       }
-      claims_open = false;
-      if (kh < ndn) {  // nothing left to stream but this CTA's down rows
-        if (kw < ndn && kw - kh < Gm::NS - 1) {
-          // post the next item's Wd slice now; its h follows once complete
-          const uint8_t *wq, *wsf;
-          const uint64_t* hr;
-          const Item d = dn_item(kw, wq, wsf, hr);
-          if (!(ok = post_down_w<NV>(p, d, wq, wsf, dslot[kw % Gm::NS]))) break;
-          ++kw;
-          continue;
-        }
-        if (globaltimer_ns() > deadline) {
-          s_abort = 1;
-          set_error(hdr, DEV_TIMEOUT);
-          break;
-        }
-        __nanosleep(64);
-        continue;  // wait for s_ready (shared memory)
+      if (globaltimer_ns() > deadline) {
+        s_abort = 1;
+        set_error(hdr, DEV_TIMEOUT);
+        break;
       }
-      break;
+      __nanosleep(32);
     }
-    // Items posted with their Wd slice only still wait for h: on an abort,
-    // complete them with the h rows as they are, so no copy stays pending.
-    for (; kh < kw; ++kh) {
-      const uint8_t *wq, *wsf;
-      const uint64_t* hr;
-      const Item d = dn_item(kh, wq, wsf, hr);
-      post_down_h<NV>(p, d, hr, dslot[kh % Gm::NS]);
-    }
-    post_end<NV>(p);
+    // Down units still waiting for h: on an abort, copy their h rows as they
+    // are, so that no slot waits for bytes that never come.
+    for (; kh < kw; ++kh)
+      post_down_h(p, s_pq[kh % fz::NQ], th + (size_t)s_pq[kh % fz::NQ].pair0 * I, hring,
+                  s_pq_slot[kh % fz::NQ]);
+    post_end<NV>(p, deadline);
     return;
   }
 
-  if (warp == fz::POLL) {  // ---------------- poll warp (lane 0, row-slice owners)
-    // Watches the completion counters of this CTA's down items in order (the
-    // shared group first, then the routed groups), eight loads in flight at a
-    // time, and publishes how many are complete.
-    if (lane != 0 || !owner) return;
-    while (!mbar_test(sel_bar, 0u))
-      if (s_abort || globaltimer_ns() > deadline) return;
+  if (warp == fz::POLL) {  // ---------------- poll warp
+    // Watches the completion counters of all groups (lane l: counters l and
+    // l + 32) and publishes the set seen complete.  Every decision is taken
+    // warp-wide (the ballots need all 32 lanes).
+    while (!__any_sync(0xffffffffu, mbar_test(sel_bar, 0u)))
+      if (__any_sync(0xffffffffu, s_abort || globaltimer_ns() > deadline)) return;
     const int ng = s_ngroups;
-    int k = 0;
-    while (k < ng && !s_abort) {
-      uint32_t pw[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        pw[j] = k + j < ng ? ld_relaxed_u32(&done[k + j == 0 ? fz::DONE_SHARED : k + j - 1].v) : 0u;
-      int rdy = 0;
-      bool run = true;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        run = run && k + j < ng && pw[j] >= fz::DONE_TARGET;
-        rdy += run ? 1 : 0;
-      }
-      if (rdy > 0) {
-        k += rdy;
-        st_release_cta_shared(&s_ready, k);
-      } else if (globaltimer_ns() > deadline) {
+    const uint64_t want = ((1ull << (ng - 1)) - 1ull) | (1ull << fz::DONE_SHARED);
+    const bool w_lo = (want >> lane) & 1ull, w_hi = (want >> (lane + 32)) & 1ull;
+    bool d_lo = false, d_hi = false;
+    uint64_t have = 0ull;
+    while (have != want && !__any_sync(0xffffffffu, s_abort)) {
+      const uint32_t c_lo = w_lo && !d_lo ? ld_relaxed_u32(&done[lane].v) : 0u;
+      const uint32_t c_hi = w_hi && !d_hi ? ld_relaxed_u32(&done[lane + 32].v) : 0u;
+      d_lo = d_lo || (w_lo && c_lo >= (uint32_t)fz::UNITS<NV>);
+      d_hi = d_hi || (w_hi && c_hi >= (uint32_t)fz::UNITS<NV>);
+      const uint64_t m = (uint64_t)__ballot_sync(0xffffffffu, d_lo) |
+                         ((uint64_t)__ballot_sync(0xffffffffu, d_hi) << 32);
+      if (m != have) {
+        have = m;
+        if (lane == 0) st_release_cta_shared_u64(&s_gmask, m);
+      } else if (__any_sync(0xffffffffu, globaltimer_ns() > deadline)) {
         break;
       } else {
         __nanosleep(128);
@@ -1118,14 +1013,19 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     for (int t = 0; t < fz::MAXB; ++t)
       if (t < B) reinterpret_cast<uint4*>(xs)[t * (H / 8) + tid] = v[t];
   }
-  // Every word of the tagged regions carries this call's tag or the previous
-  // call's: the rows this call does not use (tokens >= B) are stamped now with
-  // a dead value, so a later call never meets a word older than one call.
+  // Every word of the tagged regions carries a recent call's tag: the rows
+  // this call does not use (tokens >= B) are stamped with a dead value -- h
+  // and logits every call, y one sixteenth of its rows per call -- so a later
+  // call never meets a word old enough for its tag to come round again.
   {
     const int gid = cta * fz::CT + tid, nthr = G * fz::CT;
     const int h_used = B * SLOTS * I, h_all = fz::MAXB * SLOTS * I;
     for (int i = h_used + gid; i < h_all; i += nthr) st_tagged(a.ws.th + i, 0.f, tag);
     for (int i = B * E + gid; i < fz::MAXB * E; i += nthr) st_tagged(a.ws.tlogits + i, 0.f, tag);
+    constexpr int YCH = H / 16;
+    const int y0 = (int)(epoch & 15u) * YCH;
+    for (int i = gid; i < (fz::MAXB - B) * SLOTS * YCH; i += nthr)
+      st_tagged(a.ws.ty + (size_t)(B * SLOTS + i / YCH) * H + y0 + i % YCH, 0.f, tag);
   }
   named_sync(1, fz::CT);
   if (!mbar_wait(rrow_bar, 0u, deadline)) {
@@ -1209,131 +1109,136 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
   }
 
   DnCtx dc;
-  dc.pair_tok = s_pair_tok;
   dc.pair_w = s_pair_w;
-  dc.lacc = lacc;
-  dc.acc = s_acc;
-  dc.red = buf;
   dc.th = a.ws.th;
+  dc.ty = a.ws.ty;
   dc.tag = tag;
   dc.deadline = deadline;
   dc.hdr = hdr;
   dc.abort_flag = &s_abort;
 
-  // 3./4. the ring: gate/up units and this CTA's down items
+  // 3. the ring: every consumer warp takes every item in ring order (gate/up
+  //    units, then down units, then the END)
   int it = 0, useq = 0;
+  bool xs_done = false;  // this warp has handed the activations' buffer over
   const uint64_t drain = deadline + fz::DRAIN_NS;
+  const uint8_t* hb = reinterpret_cast<const uint8_t*>(xs);
+  // Waits (warp-wide decision) for ring iteration j; false: give up the loop.
+  auto wait_it = [&](int j) -> bool {
+    const int slot = j % Gm::NS;
+    const uint32_t ph = (uint32_t)(j / Gm::NS) & 1u;
+    bool got;
+    while (true) {
+      // Every item from the first down unit on is a down unit (or the END):
+      // this warp no longer reads the activations, and their buffer becomes
+      // the h ring once every warp has said so.
+      if (!xs_done && j >= s_first_dn) {
+        xs_done = true;
+        if (lane == 0) mbar_arrive(xs_bar);
+      }
+      if ((got = mbar_try_wait(full0 + 8u * slot, ph))) break;
+      if (globaltimer_ns() > deadline) break;
+    }
+    if (__all_sync(0xffffffffu, got)) return true;
+    s_abort = 1;
+    set_error(hdr, DEV_TIMEOUT);
+    return __all_sync(0xffffffffu, mbar_wait(full0 + 8u * slot, ph, drain));
+  };
   while (true) {
     const int slot = it % Gm::NS;
-    const uint32_t ph = (uint32_t)(it / Gm::NS) & 1u;
-    if (!mbar_wait(full0 + 8u * slot, ph, deadline)) {
-      s_abort = 1;
-      set_error(hdr, DEV_TIMEOUT);
-      if (!mbar_wait(full0 + 8u * slot, ph, drain)) break;
-    }
+    if (!wait_it(it)) break;
     const Item d = s_desc[slot];
     const bool ok = !s_abort;
     if (d.kind == fz::IT_END) break;
-    // both kinds may take a second slot
-    const int slot2 = (it + 1) % Gm::NS;
-    const uint32_t ph2 = (uint32_t)((it + 1) / Gm::NS) & 1u;
-    if constexpr (NV) {
-      const uint8_t* st = ring + slot * Gm::SLOT;
-      const bool routed = d.expert < E;
+    const uint8_t* st = ring + slot * Gm::SLOT;
+    const bool routed = d.expert < E;
+    if constexpr (NV) {  // every NVFP4 unit takes one slot
       if (d.kind == fz::IT_DOWN) {
-        const float ts = __ldg(routed ? a.w.w2_ts + d.expert : a.w.ws2_ts + (d.expert - E));
-        if (d.n <= Gm::HROWS_A) {
-          down_nv(dc, st, nullptr, d.pair0, d.n, ts, ok);
-          release_slot(empty0 + 8u * slot);
-          ++it;
-          continue;
-        }
-        bool ok2 = ok;
-        if (!mbar_wait(full0 + 8u * slot2, ph2, deadline)) {
-          s_abort = 1;
-          set_error(hdr, DEV_TIMEOUT);
-          ok2 = false;
-          if (!mbar_wait(full0 + 8u * slot2, ph2, drain)) break;
-        }
-        if (s_desc[slot2].kind != fz::IT_DOWN2) break;  // the producer gave up mid-item (abort)
-        down_nv(dc, st, ring + slot2 * Gm::SLOT, d.pair0, d.n, ts, ok2);
+        down_nv(dc, st, hb, d, __ldg(routed ? a.w.w2_ts + d.expert : a.w.ws2_ts + (d.expert - E)), ok);
         release_slot(empty0 + 8u * slot);
-        release_slot(empty0 + 8u * slot2);
-        it += 2;
-        continue;
+      } else {
+        const float* ts13 = routed ? a.w.w13_ts + 2 * d.expert : a.w.ws13_ts + 2 * (d.expert - E);
+        unit_nv(st, xs, s_pair_tok, buf, a.ws.th, d, __ldg(ts13), __ldg(ts13 + 1), ok,
+                empty0 + 8u * slot, tag, done, &s_ucnt[useq]);
+        useq = (useq + 1) & (fz::UCNT - 1);
       }
-      const float* ts13 = routed ? a.w.w13_ts + 2 * d.expert : a.w.ws13_ts + 2 * (d.expert - E);
-      unit_nv(st, xs, s_pair_tok, buf, a.ws.th, d, __ldg(ts13), __ldg(ts13 + 1), ok,
-              empty0 + 8u * slot, tag, done, &s_ucnt[useq]);
-      useq = (useq + 1) & (fz::UCNT - 1);
       ++it;
       continue;
-    }
-    if (d.kind == fz::IT_DOWN) {
-      const uint8_t* st = ring + slot * Gm::SLOT;
-      if (d.n <= fz::CC_MAX) {
-        down_cc(dc, st, d.pair0, d.n, ok, empty0 + 8u * slot);
-        ++it;
-        continue;
+    } else {  // every BF16 unit takes two slots
+      const int slot2 = (it + 1) % Gm::NS;
+      if (!wait_it(it + 1)) break;
+      const int k2 = s_desc[slot2].kind;
+      if (k2 != (d.kind == fz::IT_DOWN ? fz::IT_DOWN2 : fz::IT_UP)) break;  // producer gave up (abort)
+      const uint8_t* st2 = ring + slot2 * Gm::SLOT;
+      const bool ok2 = !s_abort;
+      if (d.kind == fz::IT_DOWN) {
+        down_cc(dc, st, st2, hb, d, ok2);
+        release_slot(empty0 + 8u * slot);
+        release_slot(empty0 + 8u * slot2);
+      } else {
+        if (d.n <= gu::CC_MAX) {
+          int tok[2];
+          tok[0] = d.tok0 >= 0 ? d.tok0 : s_pair_tok[d.pair0];
+          tok[1] = d.n > 1 ? (d.tok0 >= 0 ? d.tok0 + 1 : s_pair_tok[d.pair0 + 1]) : tok[0];
+          if (d.n == 1)
+            unit_cc<1>(st, st2, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
+                       empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
+          else
+            unit_cc<2>(st, st2, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
+                       empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
+        } else {
+          unit_mma(st, st2, xs, s_pair_tok, buf, a.ws.th, d, ok2, empty0 + 8u * slot,
+                   empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
+        }
+        useq = (useq + 1) & (fz::UCNT - 1);
       }
-      bool ok2 = ok;
-      if (!mbar_wait(full0 + 8u * slot2, ph2, deadline)) {
-        s_abort = 1;
-        set_error(hdr, DEV_TIMEOUT);
-        ok2 = false;
-        if (!mbar_wait(full0 + 8u * slot2, ph2, drain)) break;
-      }
-      if (s_desc[slot2].kind != fz::IT_DOWN2) break;  // the producer gave up mid-item (abort)
-      down_mma(dc, st, ring + slot2 * Gm::SLOT, d.pair0, d.n, ok2);
-      release_slot(empty0 + 8u * slot);
-      release_slot(empty0 + 8u * slot2);
       it += 2;
-      continue;
     }
-    // gate/up unit: gate rows in this slot, up rows in the next
-    bool ok2 = ok;
-    if (!mbar_wait(full0 + 8u * slot2, ph2, deadline)) {
-      s_abort = 1;
-      set_error(hdr, DEV_TIMEOUT);
-      ok2 = false;
-      if (!mbar_wait(full0 + 8u * slot2, ph2, drain)) break;
-    }
-    if (s_desc[slot2].kind != fz::IT_UP) break;  // the producer gave up mid-unit (abort)
-    const uint8_t* gs = ring + slot * Gm::SLOT;
-    const uint8_t* us = ring + slot2 * Gm::SLOT;
-    if (d.n <= gu::CC_MAX) {
-      int tok[2];
-      tok[0] = d.tok0 >= 0 ? d.tok0 : s_pair_tok[d.pair0];
-      tok[1] = d.n > 1 ? (d.tok0 >= 0 ? d.tok0 + 1 : s_pair_tok[d.pair0 + 1]) : tok[0];
-      if (d.n == 1)
-        unit_cc<1>(gs, us, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
-                   empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
-      else
-        unit_cc<2>(gs, us, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
-                   empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
-    } else {
-      unit_mma(gs, us, xs, s_pair_tok, buf, a.ws.th, d, ok2, empty0 + 8u * slot,
-               empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
-    }
-    useq = (useq + 1) & (fz::UCNT - 1);
-    it += 2;
+    (void)ok;
   }
   named_sync(1, fz::CT);
-  if (owner && !s_abort) {
-    // Thread pair (2s, 2s+1) finishes sum s = (warp w, token t, row r): each
-    // adds 16 lanes' running sums, one shuffle joins the halves; the
-    // tensor-core items' share is in s_acc.  Row 2w + r of the CTA's slice.
-    const int sidx = tid >> 1, half = tid & 1;
-    const int w = sidx >> 4, j = sidx & 15, t = j >> 1, rr = j & 1;
-    const float* src = lacc + j * fz::LACC_STRIDE + w * 32 + half * 16;
-    float v = 0.f;
+  // 4. this CTA's output rows: residual + the token's SLOTS y values in
+  //    ascending pair order.  Warp t lists token t's pairs first (ballots).
+  if (warp < B) {
+    int cnt = 0;
+    for (int base = 0; base < B * SLOTS; base += 32) {
+      const int pr = base + lane;
+      const bool mine = pr < B * SLOTS && s_pair_tok[pr] == warp;
+      const uint32_t m = __ballot_sync(0xffffffffu, mine);
+      const int k = cnt + __popc(m & ((1u << lane) - 1u));
+      if (mine && k < SLOTS) s_tokp[warp][k] = pr;
+      cnt += __popc(m);
+    }
+    if (cnt != SLOTS) {  // every token has SLOTS pairs; without them nothing is combined
+      if (lane == 0) set_error(hdr, DEV_BAD_ROUTING);
+      s_abort = 1;
+    }
+  }
+  named_sync(1, fz::CT);
+  if (!s_abort) {
+    const int row_b = (int)((long long)cta * H / G), nr = (int)((long long)(cta + 1) * H / G) - row_b;
+    for (int i = tid; i < B * nr; i += fz::CT) {
+      const int t = i / nr, row = row_b + i % nr;
+      uint64_t yw[SLOTS];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) v += src[k];
-    v += __shfl_xor_sync(0xffffffffu, v, 1);
-    if (half == 0 && t < B) {
-      const int row = 2 * w + rr;
-      const size_t o = (size_t)t * H + r0 + row;
-      a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + (v + s_acc[t * fz::RS + row]));
+      for (int k = 0; k < SLOTS; ++k) yw[k] = ld_tagged(a.ws.ty + (size_t)s_tokp[t][k] * H + row);
+      float v = 0.f;
+#pragma unroll
+      for (int k = 0; k < SLOTS; ++k) {
+        const uint64_t* src = a.ws.ty + (size_t)s_tokp[t][k] * H + row;
+        while ((uint32_t)(yw[k] >> 32) != tag) {  // not yet written: poll, bounded
+          if (s_abort || globaltimer_ns() > deadline) {
+            s_abort = 1;
+            set_error(hdr, DEV_TIMEOUT);
+            break;
+          }
+          __nanosleep(64);
+          yw[k] = ld_tagged(src);
+        }
+        v += __uint_as_float((uint32_t)yw[k]);
+      }
+      const size_t o = (size_t)t * H + row;
+      if (!s_abort) a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + v);
     }
   }
   // CTA 0 counts the call (also after a timeout, so that words a failed call
