@@ -628,6 +628,35 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(spec: str, calls: int):
+    """A few decode calls of one layer (one weight copy, a couple of GB on the
+    device), for small profiler captures: FMT:B with FMT bf16 or nvfp4.
+    Prints one status line, not a bench line."""
+    from moe_decode_sigmoid_gb300 import build
+    build.build()
+    import moe_decode_sigmoid_gb300 as m
+    fmt, B = spec.split(":")
+    B = int(B)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    W = fs.layer_weights(LAYER_SEED, fs.FULL, device=dev)
+    nv = fs.nvfp4_layer(W) if fmt == "nvfp4" else None
+    x, res = fs.tokens(TOKEN_SEED + B, B, device=dev)
+    out = torch.empty_like(res)
+    ws = m.new_workspace(B, device=dev)
+    for _ in range(calls):
+        if fmt == "nvfp4":
+            m.flint_moe_decode_nvfp4_w4a16(x, res, W["wr"], None, nv, out, ws)
+        else:
+            m.flint_moe_decode_bf16(x, res, W["wr"], None, W["w13"], W["w2"], W["ws13"],
+                                    W["ws2"], out, ws)
+    torch.cuda.synchronize()
+    st = m.flint_moe_get_device_status(ws)
+    print("profile case %s: %d calls, device status %d" % (spec, calls, st), flush=True)
+    if st != m.FLINT_OK:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -643,7 +672,13 @@ def main():
     ap.add_argument("--no-stack", dest="stack", action="store_false")
     ap.add_argument("--l2", choices=("rotate", "flush"), default="rotate",
                     help="cold-L2 method between timed steps")
+    ap.add_argument("--profile-case", default=None, metavar="FMT:B",
+                    help="only run --steps decode calls of one bf16|nvfp4 layer at batch B "
+                         "(for profiler captures) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.steps)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local, barrier = dist_setup()

@@ -221,7 +221,10 @@ static flint_status run_layer(bool nvfp4, const flint_moe_dims* dims, int32_t ba
   a.bias_select_only = r.bias_select_only;
   a.user_idx = idx_out;
   a.user_w = w_out;
-  if (batch <= LOCAL_SELECT_MAX_B && small_supported(sms))  // one persistent kernel
+  // One persistent kernel for small batches.  NVFP4 units are compute-heavy
+  // (dequantisation), and from 4 tokens on the three-kernel path, whose
+  // gate/up and down kernels spread each group's work over all SMs, is faster.
+  if (batch <= (nvfp4 ? NVFP4_FUSED_MAX_B : LOCAL_SELECT_MAX_B) && small_supported(sms))
     return cuda_status(nvfp4 ? launch_small_nvfp4(a, r, stream, sms)
                              : launch_small_bf16(a, r, stream, sms));
   cudaError_t e = launch_router(r, stream, true);

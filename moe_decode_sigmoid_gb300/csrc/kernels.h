@@ -58,6 +58,9 @@ struct ExpertArgs {
 
 // Largest batch whose routing the expert kernels compute themselves.
 constexpr int LOCAL_SELECT_MAX_B = SMALL_B;
+// Largest NVFP4 batch that takes the persistent kernel (measured crossover
+// with the three-kernel path on GB300: between 2 and 4 tokens).
+constexpr int NVFP4_FUSED_MAX_B = 3;
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_bucket(const Ws& ws, int B, const BucketOut& user, cudaStream_t stream);

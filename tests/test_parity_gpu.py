@@ -442,12 +442,12 @@ def test_large_h_beyond_f16_range_matches_oracle(m, layer, nv_layer, ws, B):
     assert rel_err_delta(got4, ref4, bf16_bits_to_f64(res)) <= REL_TOL
 
 
-@pytest.mark.parametrize("B", [5, 13])
+@pytest.mark.parametrize("B", [2, 13])
 def test_nvfp4_reports_activations_beyond_f16(m, layer, nv_layer, B):
     """The NVFP4 path multiplies f16 activations: a value beyond f16's range
     makes the call report FLINT_ERR_INVALID_ARG on the device instead of
     returning infinities; after re-initialisation the workspace works again
-    (both the persistent kernel, batch 5, and the three-kernel path)."""
+    (both the persistent kernel, batch 2, and the three-kernel path)."""
     W, host = layer
     nv, nv_host = nv_layer
     ws = m.new_workspace(B)
