@@ -100,14 +100,23 @@ template <bool NV>
 constexpr int UNITS = I / Geo<NV>::GR;         // gate/up units per group
 template <bool NV>
 constexpr int ND = H / Geo<NV>::DR;            // down units per group
+// Down units take their h rows from the activations' buffer, which the gate/up
+// units no longer need by then, preceded by HDED rows of their own: a ring of
+// HROWS contiguous tagged rows whose first HDED are free from the start (the
+// first down units need not wait for the hand-over).
+constexpr int HDED = 4;
+constexpr int HDED_BYTES = HDED * THROW;
+constexpr int HROWS = HDED + XS_BYTES / THROW;
+// Ring row h0 + i (h0 < HROWS, i < MAXB), wrapped.
+__device__ __forceinline__ int hring_row(int h0, int i) {
+  const int r = h0 + i;
+  return r >= HROWS ? r - HROWS : r;
+}
 template <bool NV>
 constexpr size_t smem_bytes() {
-  return (size_t)Geo<NV>::NS * Geo<NV>::SLOT + XS_BYTES + BUF_BYTES;
+  return (size_t)Geo<NV>::NS * Geo<NV>::SLOT + HDED_BYTES + XS_BYTES + BUF_BYTES;
 }
 constexpr int NQ = 8;                          // down units posted and not yet released
-// Down units take their h rows from the activations' buffer, which the gate/up
-// units no longer need by then: a ring of HROWS tagged rows.
-constexpr int HROWS = XS_BYTES / THROW;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
 enum : int { IT_GATE = 0, IT_UP = 1, IT_DOWN = 2, IT_DOWN2 = 3, IT_END = 4 };
 static_assert(S == 1 && MAXB <= GROUP_MAX, "one shared group at these batches");
@@ -118,7 +127,7 @@ static_assert(Geo<false>::GR * ROWB == Geo<false>::SLOT, "8 gate (or up) rows fi
 static_assert(Geo<false>::DR / 2 * WROW == Geo<false>::SLOT, "32 Wd rows fill one BF16 slot");
 static_assert(Geo<true>::UNIT_BYTES <= Geo<true>::SLOT && Geo<true>::WBYTES <= Geo<true>::SLOT,
               "an NVFP4 unit's weights fit one slot");
-static_assert(HROWS == 8 && MAXB <= HROWS, "a group's h rows fit the h ring");
+static_assert(HROWS == 12 && MAXB <= HROWS, "a group's h rows fit the h ring");
 static_assert(Geo<false>::NS <= NQ && Geo<true>::NS <= NQ, "every posted down unit has a queue entry");
 static_assert(H % Geo<false>::DR == 0 && H % Geo<true>::DR == 0, "row blocks tile H");
 static_assert((E + RMAX - 1) / RMAX <= 86, "grids of 86 CTAs or more keep <= RMAX router rows");
@@ -483,7 +492,8 @@ __device__ __forceinline__ void settle_words(const DnCtx& c, const uint8_t* hrow
 }
 
 // The down units below read token i's h row at ring row (d.h0 + i) mod
-// HROWS of hb, and write y(p, row) = w(p) * (Wd h_p)[row] as tagged words.
+// HROWS of hb (hring_row), and write y(p, row) = w(p) * (Wd h_p)[row] as tagged
+// words.
 //
 // BF16 down unit on CUDA cores: 64 Wd rows in two slots (rows 0-31 in sa,
 // 32-63 in sb); warp w owns rows 4w .. 4w+3 of each slot; lane l takes
@@ -510,7 +520,7 @@ __device__ __forceinline__ void down_cc(const DnCtx& c, const uint8_t* sa, const
 #pragma unroll
   for (int i = 0; i < fz::MAXB; ++i) {
     if (i < n) {
-      const uint8_t* hrow = hb + ((d.h0 + i) & (fz::HROWS - 1)) * fz::THROW;
+      const uint8_t* hrow = hb + fz::hring_row(d.h0, i) * fz::THROW;
       const uint4* hr = reinterpret_cast<const uint4*>(hrow);
       float ea[4], oa[4], eb[4], ob[4];
 #pragma unroll 1
@@ -586,7 +596,7 @@ __device__ __forceinline__ void down_nv(const DnCtx& c, const uint8_t* sw, const
 #pragma unroll
     for (int i = 0; i < fz::MAXB; ++i) {
       if (i < n) {
-        const uint8_t* hrow = hb + ((d.h0 + i) & (fz::HROWS - 1)) * fz::THROW;
+        const uint8_t* hrow = hb + fz::hring_row(d.h0, i) * fz::THROW;
         const uint4* hr = reinterpret_cast<const uint4*>(hrow);
         float e[4], o[4];
 #pragma unroll 1
@@ -707,7 +717,12 @@ __device__ __forceinline__ int post_down_w(Prod& p, const Item& d, const uint8_t
 }
 
 // The group's h rows hr (tagged, n of them) into ring rows d.h0 .. (mod
-// HROWS) of the h ring at hring, completing the unit's first slot.
+// HROWS) of the h ring at hring, completing the unit's first slot.  Rows
+// HDED and up lie in the activations' buffer: the caller has seen it handed
+// over (h_needs_xs).
+__device__ __forceinline__ bool h_needs_xs(const Item& d) {
+  return d.h0 + d.n > fz::HDED;  // some row in [HDED, HROWS) (a wrap passes HDED first)
+}
 __device__ __forceinline__ void post_down_h(const Prod& p, const Item& d, const uint64_t* hr,
                                             uint32_t hring, int slot) {
   const int run = d.n < fz::HROWS - d.h0 ? d.n : fz::HROWS - d.h0;
@@ -755,8 +770,9 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = a.B;
   uint8_t* ring = smem;
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + Gm::NS * Gm::SLOT);
-  float* buf = reinterpret_cast<float*>(smem + Gm::NS * Gm::SLOT + fz::XS_BYTES);
+  uint8_t* hded = smem + Gm::NS * Gm::SLOT;  // h ring rows 0 .. HDED-1, then xs
+  uint16_t* xs = reinterpret_cast<uint16_t*>(hded + fz::HDED_BYTES);
+  float* buf = reinterpret_cast<float*>(hded + fz::HDED_BYTES + fz::XS_BYTES);
   const uint32_t full0 = smem_addr(s_bars), empty0 = smem_addr(s_bars + Gm::NS);
   const uint32_t rrow_bar = smem_addr(s_bars + 2 * Gm::NS);
   const uint32_t sel_bar = rrow_bar + 8u, xs_bar = rrow_bar + 16u;
@@ -811,7 +827,7 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     // handed out.  rel: the last ring iteration known released.
     int kw = 0, kh = 0, kf = 0, hw = 0, hf = 0, rel = -1;
     const uint64_t* const th = a.ws.th;
-    const uint32_t hring = smem_addr(xs);
+    const uint32_t hring = smem_addr(hded);
     // true if the next `need` slots are free (the consumers release in ring
     // order: all 8 warps take every item in turn)
     auto slots_ok = [&](int need) {
@@ -837,8 +853,9 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
       //    the consumers are done with the activations' buffer
       if (kh < kw) {
         const Item& pd = s_pq[kh % fz::NQ];
-        if (!xs_free) xs_free = mbar_test(xs_bar, 0u);
-        if (xs_free && ((ld_acquire_cta_shared_u64(&s_gmask) >> pd.done_idx) & 1ull)) {
+        if (!xs_free && h_needs_xs(pd)) xs_free = mbar_test(xs_bar, 0u);
+        if ((xs_free || !h_needs_xs(pd)) &&
+            ((ld_acquire_cta_shared_u64(&s_gmask) >> pd.done_idx) & 1ull)) {
           post_down_h(p, pd, th + (size_t)pd.pair0 * I, hring, s_pq_slot[kh % fz::NQ]);
           ++kh;
           continue;
@@ -1122,7 +1139,7 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
   int it = 0, useq = 0;
   bool xs_done = false;  // this warp has handed the activations' buffer over
   const uint64_t drain = deadline + fz::DRAIN_NS;
-  const uint8_t* hb = reinterpret_cast<const uint8_t*>(xs);
+  const uint8_t* hb = hded;
   // Waits (warp-wide decision) for ring iteration j; false: give up the loop.
   auto wait_it = [&](int j) -> bool {
     const int slot = j % Gm::NS;
