@@ -163,18 +163,33 @@ template <int MW, bool GLOBAL_SRC, typename Sync>
 __device__ void bucket_cta(int B, const int* src_idx, const float* src_w, BucketDst dst,
                            BucketOut user, BucketScratch<MW>& sc, bool& bad, Sync sync) {
   const int tid = threadIdx.x & 255;
+  // The thread's pairs tid, tid + 256, ...: loaded once, all in flight
+  // together, and kept for both passes.
+  constexpr int PPT = (MW * 32 * TOPK + 255) / 256;
+  const int npairs = B * TOPK;
+  int ev[PPT];
+  float wv[PPT];
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    const int p = tid + 256 * k;
+    ev[k] = p < npairs ? (GLOBAL_SRC ? __ldcg(src_idx + p) : src_idx[p]) : -1;
+    wv[k] = p < npairs && dst.pair_w ? (GLOBAL_SRC ? __ldcg(src_w + p) : src_w[p]) : 0.f;
+  }
   for (int i = tid; i < E * MW; i += 256) (&sc.mask[0][0])[i] = 0u;
   sync();
-  const int npairs = B * TOPK;
-  for (int p = tid; p < npairs; p += 256) {
-    const int e = GLOBAL_SRC ? __ldcg(src_idx + p) : src_idx[p];
-    const int t = p / TOPK;
-    if (e < 0 || e >= E) {
-      bad = true;
-      continue;
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    const int p = tid + 256 * k;
+    if (p < npairs) {
+      const int e = ev[k];
+      const int t = p / TOPK;
+      if (e < 0 || e >= E) {
+        bad = true;
+      } else {
+        const uint32_t bit = 1u << (t & 31);
+        if (atomicOr(&sc.mask[e][t >> 5], bit) & bit) bad = true;
+      }
     }
-    const uint32_t bit = 1u << (t & 31);
-    if (atomicOr(&sc.mask[e][t >> 5], bit) & bit) bad = true;
   }
   sync();
   const int e = tid;
@@ -194,16 +209,18 @@ __device__ void bucket_cta(int B, const int* src_idx, const float* src_w, Bucket
     user.offsets[urank] = off;
   }
   sync();
-  for (int p = tid; p < npairs; p += 256) {
-    const int ex = GLOBAL_SRC ? __ldcg(src_idx + p) : src_idx[p];
-    if (ex < 0 || ex >= E) continue;
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    const int p = tid + 256 * k;
+    const int ex = ev[k];
+    if (p >= npairs || ex < 0 || ex >= E) continue;
     const int t = p / TOPK;
     const int wd = t >> 5;
     int rank = __popc(sc.mask[ex][wd] & ((1u << (t & 31)) - 1u));
     for (int w = 0; w < wd; ++w) rank += __popc(sc.mask[ex][w]);
     const int pos = sc.off[ex] + rank;
     dst.pair_tok[pos] = t;
-    if (dst.pair_w) dst.pair_w[pos] = GLOBAL_SRC ? __ldcg(src_w + p) : src_w[p];
+    if (dst.pair_w) dst.pair_w[pos] = wv[k];
     if (user.pairs) user.pairs[pos] = t * 8 + (p - t * TOPK);
   }
   const int nsg = (B + GROUP_MAX - 1) / GROUP_MAX;
