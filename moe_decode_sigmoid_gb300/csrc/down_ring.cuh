@@ -10,12 +10,13 @@
 //
 // Row-slice-major: CTA b owns output rows [16b, 16b+16) of every token and
 // walks all groups in order, so each weight byte is read by exactly one CTA
-// and the combine needs no atomics.  Per group one producer lane copies the
+// and the combine needs no atomics.  Per group a producer lane copies the
 // CTA's 16-row slice of the group's Wd (the format decides how) and the
 // group's h rows (one bulk copy; the gate/up kernel stores them split into hi
 // + lo parts and already swizzled by row) into a byte ring in shared memory:
 // each group takes only the bytes it needs, so many groups are in flight per
-// SM.
+// SM.  Two producer warps take alternate groups, each into its own half of
+// the ring.
 //
 // Warp pair p (of 4) takes groups p, p + 4, p + 8, ...: mma.sync m16n8k16
 // with the 16 Wd rows as M, the group's tokens as N (8 per tile) and K split
@@ -49,8 +50,9 @@ constexpr int RS = 16;                  // output rows per CTA
 constexpr int HROW = I * 4;             // bytes of one split h row
 constexpr int PAIRS = 4;                // consumer warp pairs; a pair takes one group at a time
 constexpr int CW = 2 * PAIRS;           // consumer warps
-constexpr int PRODUCER = CW;            // warp that fills the ring
-constexpr int THREADS = (CW + 1) * 32;
+constexpr int NPROD = 2;                // producer warps, each filling its own part of the ring
+constexpr int PRODUCER = CW;            // first producer warp
+constexpr int THREADS = (CW + NPROD) * 32;
 constexpr int SMEM_CAP = 232448 - 1024; // opt-in maximum minus static/slack
 constexpr int ALIGN = 1024;             // swizzled tensor copies land on 1 KiB boundaries
 constexpr uint64_t DRAIN_NS = 2000000000ull;
@@ -79,11 +81,14 @@ struct Layout {
   __host__ __device__ static int ring_bytes(int B) {
     return ((SMEM_CAP - ALIGN - fixed_bytes(B)) / ALIGN) * ALIGN;
   }
+  // Each producer's part of the ring.
+  __host__ __device__ static int part_bytes(int B) { return (ring_bytes(B) / NPROD / ALIGN) * ALIGN; }
   __host__ static int smem_bytes(int B) { return ALIGN + ring_bytes(B) + fixed_bytes(B); }
   static_assert(MAX_B * RS * 4 * PAIRS + MAX_GROUPS * 16 + 2 * MAX_B * SLOTS * 4 +
-                        2 * F::NDESC * 8 + ALIGN + F::WBYTES + GROUP_MAX * HROW <=
+                        2 * F::NDESC * 8 + ALIGN + NPROD * (F::WBYTES + GROUP_MAX * HROW + ALIGN) <=
                     SMEM_CAP,
-                "the ring holds the largest group at the largest batch");
+                "each part of the ring holds the largest group at the largest batch");
+  static_assert(F::NDESC % NPROD == 0 && PAIRS % NPROD == 0, "a pair's groups come from one producer");
 };
 
 struct DnMeta {
@@ -134,37 +139,46 @@ struct Ring {
   __device__ static uint32_t parity(int g) { return (uint32_t)(g / NDESC) & 1u; }
 };
 
-// One lane of the producer warp.  Group g is issued once its bytes and its
-// mbarrier pair are free: the producer waits for the oldest unreleased
-// groups, in issue order, until both hold.
+// One lane of producer warp k (of NPROD): groups g = k, k + NPROD, ... into
+// its own part [k * part, (k + 1) * part) of the ring.  Each producer's issue
+// path (bookkeeping, then copy instructions that can stall until the SM's copy
+// unit takes them) then overlaps the other's.  Group g is issued once its
+// bytes and its mbarrier pair are free: the producer waits for its oldest
+// unreleased groups, in issue order, until both hold.  It publishes the
+// group's ring offset in goff[g % NDESC] before the arrival on the group's
+// full barrier, so a consumer that has seen the barrier complete reads it
+// there.
 template <class F>
 __device__ void produce(const Ring<F::NDESC>& R, const DnMeta& meta,
-                        const typename F::Maps& maps, const ExpertArgs& a, int r0,
-                        volatile int* abort_flag, uint64_t deadline) {
+                        const typename F::Maps& maps, const ExpertArgs& a, int r0, int k,
+                        uint32_t part, uint32_t* goff, volatile int* abort_flag,
+                        uint64_t deadline) {
   constexpr int NDESC = F::NDESC;
+  constexpr int WIN = NDESC / NPROD;  // groups of one producer in flight
   using RingT = Ring<NDESC>;
   WsHeader* hdr = a.ws.hdr;
   const int n_groups = meta.n_groups;
-  RingPos pos(R.ring);
-  uint32_t released = 0;  // ring position up to which every byte is free again
-  int rel = 0;            // groups [0, rel) are released
-  // Ring ends of the outstanding groups rel, rel + 1, ... in registers (a
+  const uint32_t base = (uint32_t)k * part;
+  RingPos pos(part);
+  uint32_t released = 0;  // position in the part up to which every byte is free again
+  int rel = k;            // this producer's groups below rel are released
+  // Part ends of the outstanding groups rel, rel + NPROD, ... in registers (a
   // shift register: every access is a static index), so that the wait loop's
   // chain has no shared-memory round trip besides the barrier test.
-  uint32_t ends[NDESC];
+  uint32_t ends[WIN];
 #pragma unroll
-  for (int i = 0; i < NDESC; ++i) ends[i] = 0;
+  for (int i = 0; i < WIN; ++i) ends[i] = 0;
   // The next descriptor is loaded one iteration ahead.
-  int4 grp = n_groups > 0 ? meta.groups[0] : make_int4(0, 0, 0, 0);
-  int g = 0;
-  for (; g < n_groups; ++g) {
+  int4 grp = k < n_groups ? meta.groups[k] : make_int4(0, 0, 0, 0);
+  int g = k;
+  for (; g < n_groups; g += NPROD) {
     const int4 cur = grp;
-    if (g + 1 < n_groups) grp = meta.groups[g + 1];
+    if (g + NPROD < n_groups) grp = meta.groups[g + NPROD];
     const uint32_t need = (uint32_t)Layout<F>::group_bytes(cur.z);
     uint32_t start;
     const uint32_t off = pos.place(need, start);
     bool ok = true;
-    while (rel < g && (g - rel >= NDESC || start + need - released > R.ring)) {
+    while (rel < g && (g - rel >= NDESC || start + need - released > part)) {
       if (!mbar_wait(R.empty(rel), RingT::parity(rel), deadline)) {
         if (!*abort_flag) set_error(hdr, DEV_TIMEOUT);
         *abort_flag = 1;
@@ -173,22 +187,23 @@ __device__ void produce(const Ring<F::NDESC>& R, const DnMeta& meta,
       }
       released = ends[0];
 #pragma unroll
-      for (int i = 0; i + 1 < NDESC; ++i) ends[i] = ends[i + 1];
-      ++rel;
+      for (int i = 0; i + 1 < WIN; ++i) ends[i] = ends[i + 1];
+      rel += NPROD;
     }
-    if (!ok || ((g & 15) == 0 && *abort_flag)) break;
-    const int slot = g - rel;  // < NDESC
+    if (!ok || ((g / NPROD) % 16 == 0 && *abort_flag)) break;
+    const int slot = (g - rel) / NPROD;  // < WIN
 #pragma unroll
-    for (int i = 0; i < NDESC; ++i)
+    for (int i = 0; i < WIN; ++i)
       if (i == slot) ends[i] = start + need;
-    const uint32_t dst = R.base_addr + off;
+    const uint32_t dst = R.base_addr + base + off;
+    goff[g % NDESC] = base + off;
     mbar_expect_tx(R.full(g), (uint32_t)(F::WCOPY + cur.z * HROW));
     F::issue(maps, a, dst, cur, r0, R.full(g));
     bulk_g2s(dst + F::WBYTES, a.ws.h + (size_t)cur.y * I, cur.z * HROW, R.full(g));
   }
   // No copy may still be landing in shared memory when the CTA exits.
   const uint64_t drain = globaltimer_ns() + DRAIN_NS;
-  for (int j = rel; j < g; ++j) mbar_wait(R.full(j), RingT::parity(j), drain);
+  for (int j = rel; j < g; j += NPROD) mbar_wait(R.full(j), RingT::parity(j), drain);
 }
 
 // Barrier over one warp pair (64 threads, barrier id) that also ANDs a flag
@@ -211,18 +226,23 @@ __device__ __forceinline__ bool pair_sync_and(uint32_t id, bool v) {
 // rows sit in shared memory with 16-byte chunks XOR-permuted by the pair
 // index mod 8, so each 8-lane phase of a 128-bit load touches 8 distinct
 // banks.  hi and lo, and the two halves of each step, go to four independent
-// accumulators so the MMA chains overlap.
+// accumulators so the MMA chains overlap; with one token tile, even and odd
+// steps take separate sets as well (eight chains of four MMAs).
 // d element e: (row, token column) = (gq, 2q), (gq, 2q+1), (gq+8, 2q), (gq+8, 2q+1).
 template <class F, int NT>
 __device__ __forceinline__ void group_half(const uint8_t* st, int n, int pair0, int khalf,
                                            float (&d)[NT][4]) {
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, q = lane & 3;
-  float acc[NT][4][4];
+  constexpr int CH = NT == 1 ? 2 : 1;  // accumulator sets, taken by step kk % CH
+  float acc[NT][CH][4][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[nt][c][0] = acc[nt][c][1] = acc[nt][c][2] = acc[nt][c][3] = 0.f;
+    for (int h = 0; h < CH; ++h)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        acc[nt][h][c][0] = acc[nt][h][c][1] = acc[nt][h][c][2] = acc[nt][h][c][3] = 0.f;
   typename F::Frag fr;
   F::load(st, gq, q, khalf, fr);
   // Token columns past n read token 0's row: their results are never used,
@@ -246,17 +266,23 @@ __device__ __forceinline__ void group_half(const uint8_t* st, int n, int pair0, 
       const uint8_t* hl = hrow[nt] + kc * 128;
       const uint4 b = *reinterpret_cast<const uint4*>(hl + (((2 * q) ^ hx[nt]) * 16));
       const uint4 l = *reinterpret_cast<const uint4*>(hl + (((2 * q + 1) ^ hx[nt]) * 16));
-      F::mma(acc[nt][0], alo.x, ahi.x, alo.y, ahi.y, b.x, b.y);
-      F::mma(acc[nt][1], alo.z, ahi.z, alo.w, ahi.w, b.z, b.w);
-      F::mma(acc[nt][2], alo.x, ahi.x, alo.y, ahi.y, l.x, l.y);
-      F::mma(acc[nt][3], alo.z, ahi.z, alo.w, ahi.w, l.z, l.w);
+      float(&ac)[4][4] = acc[nt][kk % CH];
+      F::mma(ac[0], alo.x, ahi.x, alo.y, ahi.y, b.x, b.y);
+      F::mma(ac[1], alo.z, ahi.z, alo.w, ahi.w, b.z, b.w);
+      F::mma(ac[2], alo.x, ahi.x, alo.y, ahi.y, l.x, l.y);
+      F::mma(ac[3], alo.z, ahi.z, alo.w, ahi.w, l.z, l.w);
     }
   }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      d[nt][e] = (acc[nt][0][e] + acc[nt][1][e]) + (acc[nt][2][e] + acc[nt][3][e]);
+    for (int e = 0; e < 4; ++e) {
+      float v = (acc[nt][0][0][e] + acc[nt][0][1][e]) + (acc[nt][0][2][e] + acc[nt][0][3][e]);
+#pragma unroll
+      for (int h = 1; h < CH; ++h)
+        v += (acc[nt][h][0][e] + acc[nt][h][1][e]) + (acc[nt][h][2][e] + acc[nt][h][3][e]);
+      d[nt][e] = v;
+    }
 }
 
 // One group on one warp pair.  The odd warp hands its K-half tiles to the
@@ -313,6 +339,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ int s_abort;
   __shared__ int s_ngroups;
+  __shared__ uint32_t s_goff[NDESC];  // ring offset of group g at g % NDESC
   volatile int* abort_flag = &s_abort;
   const int B = a.B;
   const uint32_t ring = (uint32_t)L::ring_bytes(B);
@@ -348,10 +375,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   meta.groups = groups_s;
   meta.pair_tok = pair_tok_s;
   meta.pair_w = pair_w_s;
-  if (warp == PRODUCER) {
+  if (warp >= PRODUCER) {
     named_sync(2, THREADS);  // routing metadata is in shared memory
     meta.n_groups = s_ngroups;
-    if (lane == 0) produce<F>(R, meta, maps, a, r0, abort_flag, deadline);
+    if (lane == 0)
+      produce<F>(R, meta, maps, a, r0, warp - PRODUCER, (uint32_t)L::part_bytes(B), s_goff,
+                 abort_flag, deadline);
     return;
   }
   // Routing metadata into shared memory: all loads first, then the stores,
@@ -402,19 +431,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int pair = warp >> 1, khalf = warp & 1;
   float* my_acc = accw + pair * B * RS;
   const uint32_t bar_id = 3 + pair;
-  RingPos pos(ring);
-  int placed = 0;  // groups whose ring position `pos` has passed
-  uint32_t off = 0;
   for (int g = pair; g < n_groups; g += PAIRS) {
-    uint32_t start;
-    while (placed <= g) off = pos.place((uint32_t)L::group_bytes(groups_s[placed++].z), start);
     const int4 grp = groups_s[g];
     bool ok = !*abort_flag && mbar_wait(R.full(g), RingT::parity(g), deadline);
     if (!ok && !*abort_flag) {
       set_error(a.ws.hdr, DEV_TIMEOUT);
       *abort_flag = 1;
     }
-    uint8_t* st = smem + off;
+    // Read after the wait: the producer wrote it before its arrival.  (After
+    // a failed wait the slot is not read.)
+    uint8_t* st = smem + (ok ? *static_cast<volatile uint32_t*>(&s_goff[g % NDESC]) : 0u);
     const float sc = F::scale(a, grp.x);
     switch ((grp.z + 7) >> 3) {
       case 1:
