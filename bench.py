@@ -553,14 +553,41 @@ def stack_configs(m, stream, warmup, steps=20):
     return out
 
 
-def sources_sha() -> str:
-    """Hash of the CUDA sources: recorded ncu traffic only counts while it matches."""
+def source_closure(tu: str):
+    """The translation unit `tu` (a file under csrc/) and every header it
+    includes, transitively, from csrc/ and include/ -- the files its kernels
+    are compiled from."""
+    import re
+    dirs = [os.path.join(ROOT, "moe_decode_sigmoid_gb300", "csrc"), os.path.join(ROOT, "include")]
+    seen, todo = {}, [tu]
+    while todo:
+        name = todo.pop()
+        if name in seen:
+            continue
+        for d in dirs:
+            path = os.path.join(d, name)
+            if os.path.exists(path):
+                seen[name] = path
+                with open(path) as f:
+                    todo += re.findall(r'^\s*#\s*include\s+"([^"]+)"', f.read(), re.M)
+                break
+    return [seen[n] for n in sorted(seen)]
+
+
+def sources_sha(tu: str = None) -> str:
+    """Hash of the CUDA sources a kernel is built from (the closure of its
+    translation unit `tu`; every CUDA source when None): recorded ncu traffic
+    only counts while it matches."""
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "moe_decode_sigmoid_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
+    if tu is None:
+        csrc = os.path.join(ROOT, "moe_decode_sigmoid_gb300", "csrc")
+        paths = [os.path.join(csrc, n) for n in sorted(os.listdir(csrc))]
+    else:
+        paths = source_closure(tu)
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -572,7 +599,7 @@ def recorded_traffic(kernel: str, batch: int):
     try:
         with open(path) as f:
             rec = json.load(f).get("%s_b%d" % (kernel, batch))
-        if rec and rec.get("sources_sha") == sources_sha():
+        if rec and rec.get("sources_sha") == sources_sha(rec.get("tu")):
             return rec.get("traffic_bytes")
     except Exception:
         pass

@@ -68,16 +68,36 @@ def test_recorded_traffic_counts_only_for_the_captured_sources(monkeypatch):
     rec = recs[key]
     assert rec["traffic_bytes"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
     assert "--clock-control none" in rec["command"]
-    monkeypatch.setattr(bench, "sources_sha", lambda: rec["sources_sha"])
+    monkeypatch.setattr(bench, "sources_sha", lambda tu=None: rec["sources_sha"])
     assert bench.recorded_traffic(kernel, int(batch)) == rec["traffic_bytes"]
     assert bench.recorded_traffic(kernel, int(batch) + 1) is None
-    monkeypatch.setattr(bench, "sources_sha", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "sources_sha", lambda tu=None: "0" * 16)
     assert bench.recorded_traffic(kernel, int(batch)) is None
 
 
 def test_sources_hash_is_stable_and_short():
     a, b = bench.sources_sha(), bench.sources_sha()
     assert a == b and len(a) == 16 and int(a, 16) >= 0
+    assert bench.sources_sha("fused.cu") == bench.sources_sha("fused.cu")
+
+
+def test_sources_hash_covers_exactly_the_include_closure(tmp_path, monkeypatch):
+    csrc = tmp_path / "moe_decode_sigmoid_gb300" / "csrc"
+    inc = tmp_path / "include"
+    csrc.mkdir(parents=True)
+    inc.mkdir()
+    (csrc / "a.cu").write_text('#include "b.cuh"\n#include <cuda.h>\n')
+    (csrc / "b.cuh").write_text('  #  include "api.h"\n')
+    (csrc / "c.cu").write_text("// another kernel\n")
+    (inc / "api.h").write_text("// the API\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    names = [os.path.basename(p) for p in bench.source_closure("a.cu")]
+    assert names == ["a.cu", "api.h", "b.cuh"]
+    h0 = bench.sources_sha("a.cu")
+    (csrc / "c.cu").write_text("// changed, outside the closure\n")
+    assert bench.sources_sha("a.cu") == h0
+    (inc / "api.h").write_text("// changed, inside the closure\n")
+    assert bench.sources_sha("a.cu") != h0
 
 
 def test_latency_statistics():
