@@ -204,6 +204,57 @@ def timed_steps(fn, steps, warmup, cold, stream, barrier=None, sampler=None):
     return [s.elapsed_time(e) for s, e in ev], wall, clocks
 
 
+class Chain:
+    """CUDA graphs of k consecutive calls call(0), ..., call(k - 1), k = 1..n,
+    where call(i) runs one step on weight copy i: one replay times k steps
+    between one pair of events.  An event pair around a one-launch graph costs
+    ~5.6 us on a GB300 even for an empty kernel, ~1.2 us per launch when eight
+    run back to back; chaining the steps (as a decode step chains its layers)
+    keeps that fixed cost out of the per-step time.  With one weight copy
+    (L2 flush mode) n is 1: every step is its own replay after a flush."""
+
+    def __init__(self, call, n, stream):
+        self.call, self.n, self.stream = call, n, stream
+        self.graphs = {}
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                call(i)
+            stream.synchronize()
+
+    def replay(self, k):
+        if k not in self.graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                with torch.cuda.graph(g, stream=self.stream):
+                    for i in range(k):
+                        self.call(i)
+            self.graphs[k] = g
+        self.graphs[k].replay()
+
+
+def chain_blocks(steps: int, n: int):
+    """Replay sizes for exactly `steps` steps in replays of at most n."""
+    return [n] * (steps // n) + ([steps % n] if steps % n else [])
+
+
+def timed_chain(chain, steps, warmup, cold, stream, barrier=None, sampler=None):
+    """Exactly `steps` timed steps as replays of up to chain.n chained steps
+    (the last replay takes the remainder), after >= warmup untimed steps;
+    cold.before runs before each replay, outside the events.  Returns one
+    per-step time (replay time / its steps) for every step."""
+    blocks = chain_blocks(steps, chain.n)
+    for k in set(blocks):
+        chain.replay(k)  # capture outside the timed region
+    torch.cuda.synchronize()
+    nwarm = -(-max(warmup, 1) // chain.n)
+    times, wall, clocks = timed_steps(lambda j: chain.replay(blocks[j - nwarm] if j >= nwarm else chain.n),
+                                      len(blocks), nwarm, cold, stream, barrier, sampler)
+    per_step = []
+    for k, t in zip(blocks, times):
+        per_step += [t / k] * k
+    return per_step, wall, clocks
+
+
 class BF16Layer:
     def __init__(self, m, cold, B, bias_on, device, seed):
         self.m, self.cold, self.B = m, cold, B
@@ -248,16 +299,25 @@ class BF16Layer:
 def measure_bf16(m, cold, B, bias_on, seed, steps, warmup, stream, barrier=None, sampler=None):
     L = BF16Layer(m, cold, B, bias_on, cold.Ws[0]["wr"].device, seed)
     U = L.unique_experts()
-    L.capture(stream)
-    times, wall, clocks = timed_steps(L.replay, steps, warmup, cold, stream, barrier, sampler)
+    chain = Chain(lambda i: L.call(i, stream), len(cold.Ws), stream)
+    times, wall, clocks = timed_chain(chain, steps, warmup, cold, stream, barrier, sampler)
     st = stats_us(times)
     nb = needed_bytes_bf16(U)
     return L, U, nb, times, st, wall, clocks
 
 
+def single_call_us(L, steps, warmup, stream):
+    """The same layer with an event pair around every one-call replay (the
+    per-step fixed cost of events and graph launch included)."""
+    L.capture(stream)
+    times, _, _ = timed_steps(L.replay, steps, warmup, L.cold, stream)
+    return stats_us(times)["mean"]
+
+
 def stage_times(m, L, steps, warmup, stream):
     """Per-kernel CUDA-event durations of the three kernels, each launched alone
-    on `stream` (route -> gate/up -> down on a routed workspace)."""
+    on `stream` (route -> gate/up -> down on a routed workspace), chained over
+    the weight copies like the layer steps."""
     cold = L.cold
     idx = torch.empty_like(L.idx)
     w = torch.empty_like(L.w)
@@ -280,7 +340,7 @@ def stage_times(m, L, steps, warmup, stream):
         with torch.cuda.stream(stream):
             route(0)
             gate(0)
-        times, _, _ = timed_steps(fn, steps, warmup, cold, stream)
+        times, _, _ = timed_chain(Chain(fn, len(cold.Ws), stream), steps, warmup, cold, stream)
         res[name] = stats_us(times)
     torch.cuda.synchronize()
     return res
@@ -372,9 +432,10 @@ def run_ours(args, world, rank, local, barrier):
 
     roof_steps = min(args.steps, 400)
     kern = stage_times(m, L, roof_steps, max(3, args.warmup // 4), stream)
+    single_us = single_call_us(L, roof_steps, max(3, args.warmup // 4), stream)
     if B <= SMALL_BATCH_MAX:
-        # The whole layer is one launch of the persistent kernel: the per-step
-        # events time exactly that kernel on its stream.
+        # The whole layer is one launch of the persistent kernel: the chained
+        # steps time back-to-back launches of exactly that kernel on its stream.
         roof_kernel = "moe_small_bf16_kernel"
         alg_bytes = nb + 3 * B * 2048 * 2          # weights + x, residual, out
         dur_us = st["mean"]
@@ -408,8 +469,11 @@ def run_ours(args, world, rank, local, barrier):
                         "unit-RMS N(0,1) tokens" % B,
             "batch": B, "unique_experts": U, "needed_bytes": nb,
             "l2": cold.describe(),
-            "timing": "CUDA-graph replay of the layer (%s), CUDA events per step"
-                      % ("one persistent kernel" if B <= SMALL_BATCH_MAX else "3 kernels"),
+            "timing": "CUDA events around CUDA-graph replays of %d consecutive layer steps "
+                      "(one per weight copy, %s per layer); time per step = replay time / %d"
+                      % (len(cold.Ws), "one persistent kernel" if B <= SMALL_BATCH_MAX
+                         else "3 kernels", len(cold.Ws)),
+            "us_single_call": round(single_us, 3),
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "us_per_layer": round(st["mean"], 3),
@@ -467,21 +531,12 @@ def nvfp4_configs(m, cold, stream, steps, warmup):
         o = torch.empty_like(res)
         idx = torch.empty((B, 6), dtype=torch.int32, device=x.device)
         ws = m.new_workspace(B, device=x.device)
-        graphs = []
-        with torch.cuda.stream(stream):
-            for i, (W, nv) in enumerate(zip(cold.Ws, nvs)):
-                call = (lambda W=W, nv=nv: m.flint_moe_decode_nvfp4_w4a16(
-                    x, res, W["wr"], bias, nv, o, ws, idx, None, stream=stream))
-                call()
-                stream.synchronize()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    call()
-                graphs.append(g)
+        chain = Chain(lambda i: m.flint_moe_decode_nvfp4_w4a16(
+            x, res, cold.Ws[i]["wr"], bias, nvs[i], o, ws, idx, None, stream=stream),
+            len(cold.Ws), stream)
         torch.cuda.synchronize()
         U = int(torch.unique(idx).numel())
-        times, _, _ = timed_steps(lambda i: graphs[i % len(graphs)].replay(), steps, warmup, cold,
-                                  stream)
+        times, _, _ = timed_chain(chain, steps, warmup, cold, stream)
         st = stats_us(times)
         nb = needed_bytes_nvfp4(U)
         out["nvfp4_b%d%s" % (B, "_skew" if bias_on else "")] = {

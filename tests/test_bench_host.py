@@ -100,6 +100,17 @@ def test_sources_hash_covers_exactly_the_include_closure(tmp_path, monkeypatch):
     assert bench.sources_sha("a.cu") != h0
 
 
+def test_chained_replays_time_exactly_the_requested_steps():
+    assert bench.chain_blocks(2000, 8) == [8] * 250
+    assert bench.chain_blocks(20, 8) == [8, 8, 4]
+    assert bench.chain_blocks(5, 1) == [1] * 5
+    assert bench.chain_blocks(3, 8) == [3]
+    for steps in range(1, 40):
+        for n in (1, 3, 8):
+            b = bench.chain_blocks(steps, n)
+            assert sum(b) == steps and all(1 <= k <= n for k in b)
+
+
 def test_latency_statistics():
     st = bench.stats_us([0.010, 0.030, 0.020, 0.040, 0.050])   # ms
     assert st["mean"] == pytest.approx(30.0)
