@@ -42,7 +42,7 @@
  *    synchronised (except in the first flint_moe_decode_bf16_noalloc call on
  *    a device): results are visible after the caller's next sync on that
  *    stream.  Launch failures reported by the runtime map to FLINT_ERR_CUDA.
- *  - BF16 decode calls of batch <= 8 and NVFP4 decode calls of batch <= 3
+ *  - BF16 decode calls of batch <= 8 and NVFP4 decode calls of batch <= 2
  *    run one persistent kernel whose CTAs, one per SM, exchange data while
  *    they run.  It is launched as a cooperative
  *    grid, which the runtime starts only when every CTA can be resident at
@@ -235,7 +235,7 @@ flint_status flint_moe_down_bf16(const flint_moe_dims* dims, int32_t batch,
  * the tensor cores, so every activation must satisfy |x| < 65504 (an
  * RMS-normalised x is below sqrt(H) = 45.3): a larger one sets the device
  * status to FLINT_ERR_INVALID_ARG, and the outputs are undefined.  h is kept
- * in fp32 for batches of <= 3 tokens (the persistent kernel) and as a bf16
+ * in fp32 for batches of <= 2 tokens (the persistent kernel) and as a bf16
  * pair hi + lo (about 16 significant bits, the range of fp32) above that.
  *   w13_q [E, 2I, H/2], w13_sf [E, 2I, H/16], w13_ts [E, 2] (gate, up)
  *   w2_q  [E, H, I/2],  w2_sf  [E, H, I/16],  w2_ts  [E]

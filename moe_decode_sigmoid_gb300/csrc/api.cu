@@ -222,8 +222,8 @@ static flint_status run_layer(bool nvfp4, const flint_moe_dims* dims, int32_t ba
   a.user_idx = idx_out;
   a.user_w = w_out;
   // One persistent kernel for small batches.  NVFP4 units are compute-heavy
-  // (dequantisation), and from 4 tokens on the three-kernel path, whose
-  // gate/up and down kernels spread each group's work over all SMs, is faster.
+  // (dequantisation), and from 3 tokens on the chained kernels, whose gate/up
+  // and down kernels spread each group's work over all SMs, are faster.
   if (batch <= (nvfp4 ? NVFP4_FUSED_MAX_B : LOCAL_SELECT_MAX_B) && small_supported(sms))
     return cuda_status(nvfp4 ? launch_small_nvfp4(a, r, stream, sms)
                              : launch_small_bf16(a, r, stream, sms));
@@ -231,8 +231,10 @@ static flint_status run_layer(bool nvfp4, const flint_moe_dims* dims, int32_t ba
   if (e != cudaSuccess) return cuda_status(e);
   e = nvfp4 ? launch_gateup_nvfp4(a, stream, sms) : launch_gateup_bf16(a, stream, sms);
   if (e != cudaSuccess) return cuda_status(e);
-  e = nvfp4 ? launch_down_nvfp4(a, stream, sms) : launch_down_bf16(a, stream);
-  return cuda_status(e);
+  if (!nvfp4) return cuda_status(launch_down_bf16(a, stream));
+  e = launch_down_nvfp4(a, stream, sms);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_combine_y(a, stream));
 }
 
 flint_status flint_moe_decode_bf16(const flint_moe_dims* dims, int32_t batch, const void* x_bf16,

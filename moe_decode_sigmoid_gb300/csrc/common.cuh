@@ -70,7 +70,7 @@ struct WsHeader {
   uint32_t stall_release;    // never written by the library
   uint32_t pad0[23];
   uint32_t tile_ctas_done[MAX_B / 8];  // router: finished CTAs per token tile
-  uint32_t rb_done[16];      // NVFP4 down: finished units per 128-row block
+  uint32_t pad2[16];
   uint32_t pad1[176];
   // small-batch kernels, by epoch parity: completion counters of the groups,
   // the unit queue and the logits arrivals

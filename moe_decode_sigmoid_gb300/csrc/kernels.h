@@ -59,8 +59,9 @@ struct ExpertArgs {
 // Largest batch whose routing the expert kernels compute themselves.
 constexpr int LOCAL_SELECT_MAX_B = SMALL_B;
 // Largest NVFP4 batch that takes the persistent kernel (measured crossover
-// with the three-kernel path on GB300: between 2 and 4 tokens).
-constexpr int NVFP4_FUSED_MAX_B = 3;
+// with the chained kernels on GB300: at 2 tokens 29.4 us against 31.1 us, at 3
+// tokens 36.0 us against 32.5 us).
+constexpr int NVFP4_FUSED_MAX_B = 2;
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_bucket(const Ws& ws, int B, const BucketOut& user, cudaStream_t stream);
@@ -75,6 +76,8 @@ cudaError_t launch_small_nvfp4(const ExpertArgs& a, const RouterArgs& r, cudaStr
                                int num_sms);
 cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
 cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
+// out = residual + each token's SLOTS rows of y (after launch_down_nvfp4).
+cudaError_t launch_combine_y(const ExpertArgs& a, cudaStream_t stream);
 cudaError_t launch_rmsnorm(const uint16_t* in, uint16_t* out, int B, float eps,
                            cudaStream_t stream);
 cudaError_t launch_ws_init(WsHeader* hdr, uint64_t wait_limit_ns, cudaStream_t stream);

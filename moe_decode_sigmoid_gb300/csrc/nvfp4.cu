@@ -147,7 +147,6 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, c
     if (slot < n) {
       const int tok = pair_tok[pair0 + slot];
       const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)tok * H + warp * 256 + q * 32);
-#pragma unroll
       bool big = false;
 #pragma unroll
       for (int m = 0; m < 2; ++m)
@@ -365,10 +364,12 @@ cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int nu
 // 128q + 4s .. +3 of rows g and g + 8, so its 64 code bytes and 8 scale bytes
 // per row are loaded once per unit and dequantised from registers; h follows
 // the same order (h_off_nv).  Each warp writes its rows' partial sums,
-// already weighted by the routing weight and the tensor scale, to y[pair][row];
-// the CTA that finishes the last unit of a row block (an atomic ticket after
-// a fence) adds, for each token, its SLOTS rows of y in ascending pair order to
-// the residual -- a fixed order, so the result is bitwise reproducible.
+// already weighted by the routing weight and the tensor scale, to y[pair][row].
+// A second kernel, chained after this one, adds for each token its SLOTS rows
+// of y in ascending pair order to the residual -- a fixed order, so the result
+// is bitwise reproducible.  The kernel boundary orders every y store before
+// the combine: no fence, ticket or barrier per unit (those cost ~1 us per unit
+// while the copies stream, measured).
 
 namespace f4 {
 constexpr int DN_RB = 128;                      // output rows per unit
@@ -380,37 +381,21 @@ constexpr int DN_SB = DN_RB * DN_SFROW;         // 4 KiB
 constexpr int DN_HROW = I * 4;                  // one h row (bf16 hi + lo pairs)
 constexpr int DN_MAX_STAGES = 4;
 constexpr int SMEM_CAP = 232448 - 1024;
-static_assert(DN_UNITS <= 16, "one ticket per row block in the header");
 __host__ __device__ inline int dn_stage(int B) {
   return DN_QB + DN_SB + (B < GROUP_MAX ? B : GROUP_MAX) * DN_HROW;
 }
-__host__ __device__ inline int dn_fixed() {
-  return (int)sizeof(MetaSmem) + MAX_B * SLOTS * 4 + 2 * DN_MAX_STAGES * 8;
-}
+__host__ __device__ inline int dn_fixed() { return (int)sizeof(MetaSmem) + 2 * DN_MAX_STAGES * 8; }
 __host__ __device__ inline int dn_nstages(int B) {
   const int n = (SMEM_CAP - dn_fixed()) / dn_stage(B);
   return n > DN_MAX_STAGES ? DN_MAX_STAGES : n;
 }
 __host__ __device__ inline int dn_smem(int B) { return dn_nstages(B) * dn_stage(B) + dn_fixed(); }
-static_assert(DN_QB + DN_SB + GROUP_MAX * DN_HROW + (int)sizeof(MetaSmem) + MAX_B * SLOTS * 4 +
-                      2 * DN_MAX_STAGES * 8 <=
+static_assert(DN_QB + DN_SB + GROUP_MAX * DN_HROW + (int)sizeof(MetaSmem) + 2 * DN_MAX_STAGES * 8 <=
                   SMEM_CAP,
               "a stage of the largest group fits");
 }  // namespace f4
 
 namespace {
-
-// Barrier over the consumer warps that also ANDs a flag across them (every
-// consumer thread arrives, so the decision is the same in every warp).
-__device__ __forceinline__ bool consumers_and(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
-      : "=r"(r)
-      : "r"((uint32_t)v), "n"(f4::CWARPS * 32)
-      : "memory");
-  return r != 0;
-}
 
 // One warp, one unit: rows 16w .. 16w + 15 of the block, NT token tiles.
 // Lane (g, q): rows g and g + 8, columns 128q + 4s .. +3 at step s.
@@ -516,36 +501,15 @@ __device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, c
   drain(p, it);
 }
 
-// out rows of block rb for every token: residual + the token's SLOTS y rows,
-// in ascending pair order.
-__device__ __forceinline__ void dn_combine(const ExpertArgs& a, const float* y, const int* tokp,
-                                           int rb) {
-  const int B = a.B;
-  for (int i = threadIdx.x; i < B * f4::DN_RB; i += f4::CWARPS * 32) {
-    const int t = i / f4::DN_RB;
-    const int r = rb * f4::DN_RB + i % f4::DN_RB;
-    float yv[SLOTS];
-#pragma unroll
-    for (int j = 0; j < SLOTS; ++j) yv[j] = __ldcg(y + (size_t)tokp[t * SLOTS + j] * H + r);
-    float v = 0.f;
-#pragma unroll
-    for (int j = 0; j < SLOTS; ++j) v += yv[j];
-    const size_t o = (size_t)t * H + r;
-    a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + v);
-  }
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
-  __shared__ int s_last;
   const int B = a.B;
   const int nstage = f4::dn_nstages(B), stage = f4::dn_stage(B);
   MetaSmem& meta = *reinterpret_cast<MetaSmem*>(smem + nstage * stage);
-  int* tokp = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tokp + MAX_B * SLOTS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
   Pipe p;
   init_pipe(p, smem, stage, nstage, bars, f4::DN_MAX_STAGES, &s_abort, a.ws.hdr);
   __syncthreads();
@@ -562,22 +526,6 @@ __global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a
     return;
   }
   fill_meta(a, false, meta, nullptr, nullptr, nullptr);
-  // Each token's SLOTS pairs in ascending order (warp per token, ballots).
-  for (int t = warp; t < B; t += f4::CWARPS) {
-    int cnt = 0;
-    for (int base = 0; base < B * SLOTS; base += 32) {
-      const int pr = base + lane;
-      const bool mine = pr < B * SLOTS && meta.pair_tok[pr] == t;
-      const uint32_t m = __ballot_sync(0xffffffffu, mine);
-      const int k = cnt + __popc(m & ((1u << lane) - 1u));
-      if (mine && k < SLOTS) tokp[t * SLOTS + k] = pr;
-      cnt += __popc(m);
-    }
-    if (cnt != SLOTS) {  // every token has SLOTS pairs; without them nothing is combined
-      if (lane == 0) set_error(a.ws.hdr, DEV_BAD_ROUTING);
-      *p.abort_flag = 1;
-    }
-  }
   pdl_trigger();
   named_sync(2, ALL_THREADS);
   float* y = ws_y(a.ws, B);
@@ -601,23 +549,47 @@ __global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_bar(p, slot));
-    // Publish this unit: after the consumers' barrier one thread fences (the
-    // barrier orders every warp's y stores before it) and takes a ticket.
-    ok = consumers_and(ok && !*p.abort_flag);
-    if (!ok) break;
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const uint32_t t = atomicAdd(&a.ws.hdr->rb_done[rb], 1u);
-      s_last = t + 1 == (uint32_t)meta.n_groups;
-      if (s_last) a.ws.hdr->rb_done[rb] = 0;  // every unit of the block has counted: reset for the next call
-    }
-    named_sync(1, f4::CWARPS * 32);
-    if (s_last) {
-      __threadfence();
-      dn_combine(a, y, tokp, rb);
-    }
-    named_sync(1, f4::CWARPS * 32);  // s_last is read before it is rewritten
+    if (!ok) break;  // a failed wait set the abort flag: the producer stops too
   }
+}
+
+// out[t][r] = residual[t][r] + the token's SLOTS rows of y at r, added in
+// ascending pair order.  Block (x, t): token t, rows 256x .. 256x + 255; warp 0
+// lists the token's pairs (ballots over pair_tok) before the sums.
+__global__ void __launch_bounds__(256) combine_y_kernel(ExpertArgs a) {
+  __shared__ int s_pairs[SLOTS];
+  __shared__ int s_ok;
+  pdl_wait();  // y and the pair table come from the preceding kernels
+  const int t = blockIdx.y, lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    const int np = a.B * SLOTS;
+    int cnt = 0;
+    for (int base = 0; base < np; base += 32) {
+      const int pr = base + lane;
+      const bool mine = pr < np && __ldcg(a.ws.pair_tok + pr) == t;
+      const uint32_t m = __ballot_sync(0xffffffffu, mine);
+      const int k = cnt + __popc(m & ((1u << lane) - 1u));
+      if (mine && k < SLOTS) s_pairs[k] = pr;
+      cnt += __popc(m);
+    }
+    if (lane == 0) {
+      s_ok = cnt == SLOTS;
+      // every token has SLOTS pairs; without them nothing is combined
+      if (cnt != SLOTS && blockIdx.x == 0) set_error(a.ws.hdr, DEV_BAD_ROUTING);
+    }
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  const float* y = ws_y(a.ws, a.B);
+  const int r = blockIdx.x * 256 + threadIdx.x;
+  float yv[SLOTS];
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) yv[j] = __ldcg(y + (size_t)s_pairs[j] * H + r);
+  float v = 0.f;
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) v += yv[j];
+  const size_t o = (size_t)t * H + r;
+  a.out[o] = f2bf(bf_lo((uint32_t)a.residual[o]) + v);
 }
 
 cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms) {
@@ -635,6 +607,19 @@ cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, down_nvfp4_kernel, a);
+}
+
+cudaError_t launch_combine_y(const ExpertArgs& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(H / 256, a.B, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_y_kernel, a);
 }
 
 }  // namespace flint
