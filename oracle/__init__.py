@@ -50,6 +50,9 @@ def load(path: str) -> ctypes.CDLL:
     L.ref_bucket.argtypes = [_I, _I, _I, _P, _P, _P, _P]
     L.ref_rmsnorm.restype = None
     L.ref_rmsnorm.argtypes = [_I, _I, _P, ctypes.c_double, _P]
+    L.ref_qk_norm_rope.restype = None
+    L.ref_qk_norm_rope.argtypes = [_I, _I, _I, _I, _P, _P, _P, _P, ctypes.c_double,
+                                   ctypes.c_double, _P, _P, _P]
     L.ref_max_threads.restype = _I
     L.ref_max_threads.argtypes = []
     return L
@@ -206,6 +209,24 @@ def rmsnorm(x, eps=1e-6):
     out = np.zeros((B, H), np.float64)
     lib().ref_rmsnorm(B, H, _ptr(x), float(eps), _ptr(out))
     return out
+
+
+def qk_norm_rope(qkv, q_norm, k_norm, positions, n_q_heads, n_kv_heads, theta, eps=1e-6):
+    """Per-head Q/K RMSNorm (learned gain) and RoPE (rotate-half, theta = 0:
+    none) of a decode step's projection rows qkv [B, (nq + 2 nkv) * D] (bf16);
+    returns (q [B, nq, D], k [B, nkv, D], v [B, nkv, D]) in fp64."""
+    qkv = _np(qkv, np.uint16)
+    qn, kn = _np(q_norm, np.uint16), _np(k_norm, np.uint16)
+    pos = _np(positions, np.int32)
+    B = qkv.shape[0]
+    D = qn.shape[0]
+    assert qkv.shape[1] == (n_q_heads + 2 * n_kv_heads) * D and kn.shape[0] == D and pos.shape == (B,)
+    q = np.zeros((B, n_q_heads, D), np.float64)
+    k = np.zeros((B, n_kv_heads, D), np.float64)
+    v = np.zeros((B, n_kv_heads, D), np.float64)
+    lib().ref_qk_norm_rope(B, n_q_heads, n_kv_heads, D, _ptr(qkv), _ptr(qn), _ptr(kn), _ptr(pos),
+                           float(theta), float(eps), _ptr(q), _ptr(k), _ptr(v))
+    return q, k, v
 
 
 def max_threads() -> int:

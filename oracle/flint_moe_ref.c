@@ -349,6 +349,64 @@ void ref_rmsnorm(int B, int H, const uint16_t* in, double eps, double* out) {
   }
 }
 
+/* ---- attention side of a decode step: Q/K norm + RoPE + KV-cache write ----
+ *
+ * The pages fuse "Q/K norm, RoPE, and KV-cache write into a single kernel"
+ * [vLLM Day-0 Support for Recursive's Flint, "Optimization Strategies",
+ * "Fused Kernels"] for attention with "per-head Q/K RMSNorm", GQA with 32
+ * query and 4 KV heads, RoPE on the sliding-window layers and no positional
+ * encoding on the full-attention ones [same page, "Flint Model
+ * Architecture"].  For each token t with position pos[t], its projection row
+ * qkv[t] = [q_0 .. q_{nq-1} | k_0 .. k_{nkv-1} | v_0 .. v_{nkv-1}] (D values
+ * per head) gives:
+ *   q and k heads:  n[i] = x[i] / sqrt(mean_i x[i]^2 + eps) * g[i]
+ *                   (g = q_norm for query heads, k_norm for key heads), then,
+ *                   when theta > 0, for i < D/2 with a_i = pos * theta^(-2i/D):
+ *                   r[i] = n[i] cos a_i - n[i + D/2] sin a_i,
+ *                   r[i + D/2] = n[i + D/2] cos a_i + n[i] sin a_i;
+ *   v heads:        unchanged.
+ * The pairing of element i with i + D/2 (rotate-half) and theta as an input
+ * are this library's readings: the pages name RoPE only.  q_out is
+ * [B][nq][D], k_out and v_out [B][nkv][D]; the cache write is the caller's
+ * placement of k_out and v_out at each token's slot. */
+static void qk_head(int D, const uint16_t* x, const uint16_t* g, int32_t pos, double theta,
+                    double eps, double* out) {
+  double ss = 0.0;
+  for (int i = 0; i < D; ++i) {
+    double v = bf16_value(x[i]);
+    ss += v * v;
+  }
+  double inv = 1.0 / sqrt(ss / D + eps);
+  for (int i = 0; i < D; ++i) out[i] = bf16_value(x[i]) * inv * bf16_value(g[i]);
+  if (theta > 0.0) {
+    int half = D / 2;
+    for (int i = 0; i < half; ++i) {
+      double a = (double)pos * pow(theta, -2.0 * i / D);
+      double c = cos(a), s = sin(a);
+      double lo = out[i], hi = out[i + half];
+      out[i] = lo * c - hi * s;
+      out[i + half] = hi * c + lo * s;
+    }
+  }
+}
+
+void ref_qk_norm_rope(int B, int nq, int nkv, int D, const uint16_t* qkv, const uint16_t* q_norm,
+                      const uint16_t* k_norm, const int32_t* pos, double theta, double eps,
+                      double* q_out, double* k_out, double* v_out) {
+  const size_t row = (size_t)(nq + 2 * nkv) * D;
+  for (int t = 0; t < B; ++t) {
+    const uint16_t* x = qkv + (size_t)t * row;
+    for (int h = 0; h < nq; ++h)
+      qk_head(D, x + (size_t)h * D, q_norm, pos[t], theta, eps, q_out + ((size_t)t * nq + h) * D);
+    for (int h = 0; h < nkv; ++h)
+      qk_head(D, x + (size_t)(nq + h) * D, k_norm, pos[t], theta, eps,
+              k_out + ((size_t)t * nkv + h) * D);
+    for (int h = 0; h < nkv; ++h)
+      for (int i = 0; i < D; ++i)
+        v_out[((size_t)t * nkv + h) * D + i] = bf16_value(x[(size_t)(nq + nkv + h) * D + i]);
+  }
+}
+
 int ref_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

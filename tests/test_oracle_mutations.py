@@ -54,6 +54,20 @@ MUTATIONS = {
     "gate / up tensor scales swapped": (
         "m13->ts_lo = ts13[0];\n    m13->ts_hi = ts13[1];",
         "m13->ts_lo = ts13[1];\n    m13->ts_hi = ts13[0];"),
+    "RoPE rotation sign flipped": ("out[i] = lo * c - hi * s;", "out[i] = lo * c + hi * s;"),
+    "RoPE frequency exponent halved": (
+        "pow(theta, -2.0 * i / D)", "pow(theta, -1.0 * i / D)"),
+    "RoPE position ignored": ("double a = (double)pos * pow(", "double a = pow("),
+    "RoPE pairs element i with i + 1": (
+        "double lo = out[i], hi = out[i + half];\n      out[i] = lo * c - hi * s;\n      out[i + half] = hi * c + lo * s;",
+        "double lo = out[2 * i], hi = out[2 * i + 1];\n      out[2 * i] = lo * c - hi * s;\n      out[2 * i + 1] = hi * c + lo * s;"),
+    "Q/K norm gain ignored": (
+        "out[i] = bf16_value(x[i]) * inv * bf16_value(g[i]);", "out[i] = bf16_value(x[i]) * inv;"),
+    "Q/K norm eps dropped": ("double inv = 1.0 / sqrt(ss / D + eps);", "double inv = 1.0 / sqrt(ss / D);"),
+    "query heads take the key gain": (
+        "qk_head(D, x + (size_t)h * D, q_norm,", "qk_head(D, x + (size_t)h * D, k_norm,"),
+    "value heads read from the key heads": (
+        "bf16_value(x[(size_t)(nq + nkv + h) * D + i]);", "bf16_value(x[(size_t)(nq + h) * D + i]);"),
 }
 
 # The pins run against each build: all of test_oracle_pins.py's CPU-quick pins.
@@ -77,6 +91,10 @@ PINS = [
     ("e2m1 codes", pins.test_e2m1_all_codes_match_spec_table),
     ("e4m3 codes", pins.test_e4m3_all_codes_match_library_decode_and_spec_points),
     ("NVFP4 = BF16 on dequantised weights", pins.test_nvfp4_layer_equals_bf16_layer_on_dequantised_weights),
+    ("Q/K norm + RoPE, hand-computed head", pins.test_qk_norm_rope_hand_computed_head),
+    ("Q/K norm eps under the root", pins.test_qk_norm_eps_sits_under_the_root),
+    ("Q/K norm + RoPE invariants", pins.test_qk_norm_rope_invariants),
+    ("RoPE relative position", pins.test_rope_scores_depend_on_relative_position_only),
 ]
 
 

@@ -412,6 +412,84 @@ def test_rmsnorm_closed_forms():
     np.testing.assert_allclose(y2, y, rtol=1e-14)
 
 
+# ---------------------------------------------------------------- q/k norm + RoPE
+# The attention side of a decode step: per-head Q/K RMSNorm with a learned gain,
+# then RoPE (element i paired with i + D/2, angle pos * theta^(-2i/D); theta = 0
+# on the layers without positional encoding), V unchanged.
+
+def _qkv_rows(seed, B, nq, nkv, D):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((B, (nq + 2 * nkv) * D), generator=g).to(torch.bfloat16)
+
+
+def test_qk_norm_rope_hand_computed_head():
+    # D = 4, one query and one KV head, eps = 0.  q = [1, 0, 0, 0] has RMS 1/2,
+    # so it normalises to [2, 0, 0, 0]; k = [0, 1, 0, 0] to [0, 2, 0, 0], times
+    # its gain 2 at element 1.  theta = 100: frequencies 1 and 100^(-1/2) = 0.1;
+    # at position 3 the pairs (0, 2) and (1, 3) turn by 3 and 0.3 radians.
+    qkv = _bf16([[1, 0, 0, 0, 0, 1, 0, 0, 1.5, -2, 3, 0.25]])
+    q, k, v = oracle.qk_norm_rope(qkv, _bf16([1, 1, 1, 1]), _bf16([0.5, 2, 1, 1]),
+                                  np.array([3], np.int32), 1, 1, 100.0, eps=0.0)
+    np.testing.assert_allclose(q[0, 0], [2 * math.cos(3), 0, 2 * math.sin(3), 0], atol=1e-15)
+    np.testing.assert_allclose(k[0, 0], [0, 4 * math.cos(0.3), 0, 4 * math.sin(0.3)], atol=1e-15)
+    assert v[0, 0].tolist() == [1.5, -2.0, 3.0, 0.25]
+
+
+def test_qk_norm_eps_sits_under_the_root():
+    # every element c = 2^-5 and eps = c^2 = 2^-10: n = c / sqrt(c^2 + eps) = 1/sqrt(2)
+    D = 8
+    qkv = _bf16([[2.0 ** -5] * (3 * D)])
+    q, k, _ = oracle.qk_norm_rope(qkv, _bf16([1] * D), _bf16([1] * D), np.array([0], np.int32),
+                                  1, 1, 0.0, eps=2.0 ** -10)
+    np.testing.assert_allclose(q, 1 / math.sqrt(2), rtol=1e-15)
+    np.testing.assert_allclose(k, 1 / math.sqrt(2), rtol=1e-15)
+
+
+def test_qk_norm_rope_invariants():
+    nq, nkv, D, theta = 32, 4, 128, 1.0e6
+    qkv = _qkv_rows(7, 3, nq, nkv, D)
+    ones = _bf16([1] * D)
+    pos = np.array([0, 5, 200000], np.int32)
+    q0, k0, v0 = oracle.qk_norm_rope(qkv, ones, ones, pos, nq, nkv, 0.0, eps=0.0)
+    q1, k1, v1 = oracle.qk_norm_rope(qkv, ones, ones, pos, nq, nkv, theta, eps=0.0)
+    # unit gain, no eps: every normalised head has RMS 1
+    np.testing.assert_allclose(np.mean(q0 * q0, axis=-1), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(np.mean(k0 * k0, axis=-1), 1.0, rtol=1e-13)
+    # position 0 turns nothing
+    np.testing.assert_allclose(q1[0], q0[0], atol=1e-15)
+    np.testing.assert_allclose(k1[0], k0[0], atol=1e-15)
+    # a rotation keeps the length of every (i, i + D/2) pair
+    h = D // 2
+    for a, b in ((q0, q1), (k0, k1)):
+        np.testing.assert_allclose(a[..., :h] ** 2 + a[..., h:] ** 2,
+                                   b[..., :h] ** 2 + b[..., h:] ** 2, rtol=1e-12, atol=1e-14)
+    # V passes unchanged, bit for bit
+    raw = _f64(qkv).reshape(3, nq + 2 * nkv, D)
+    assert np.array_equal(v0, raw[:, nq + nkv:]) and np.array_equal(v1, v0)
+    # gains scale their own heads only
+    g2 = _bf16([2] * D)
+    q2, k2, _ = oracle.qk_norm_rope(qkv, g2, ones, pos, nq, nkv, theta, eps=0.0)
+    np.testing.assert_allclose(q2, 2 * q1, rtol=1e-15)
+    np.testing.assert_allclose(k2, k1, rtol=0)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    # a query at position m against a key at position n: q.k is the same for
+    # (m, n) and (m + s, n + s), per query head and KV head
+    nq, nkv, D, theta = 4, 2, 128, 1.0e6
+    qkv = _qkv_rows(11, 1, nq, nkv, D).repeat(4, 1)
+    ones = _bf16([1] * D)
+    pos = np.array([10, 3, 1010, 1003], np.int32)
+    q, k, _ = oracle.qk_norm_rope(qkv, ones, ones, pos, nq, nkv, theta, eps=1e-6)
+    s_near = np.einsum("hd,gd->hg", q[0], k[1])
+    s_far = np.einsum("hd,gd->hg", q[2], k[3])
+    np.testing.assert_allclose(s_far, s_near, rtol=1e-9, atol=1e-9)
+    # and it does change with the distance
+    q5, k5, _ = oracle.qk_norm_rope(qkv, ones, ones, np.array([10, 4, 0, 0], np.int32), nq, nkv,
+                                    theta, eps=1e-6)
+    assert np.max(np.abs(np.einsum("hd,gd->hg", q5[0], k5[1]) - s_near)) > 1e-3
+
+
 def test_margin_helper_on_planted_ties():
     L = np.array([[3.0, 1.0, 2.0, 2.0, 0.0]])
     assert topk_margin(L, 2)[0] == 0.0 and topk_margin(L, 1)[0] == 1.0
