@@ -514,6 +514,7 @@ def extras(m, cold, stream, args):
             "needed_bytes": nb, "gbs": round(nb / (st["mean"] * 1e-6) / 1e9, 1)}
         del L
     out.update(nvfp4_configs(m, cold, stream, steps, args.warmup))
+    out.update(attn_configs(m, stream, steps, args.warmup))
     if args.stack:
         out.update(stack_configs(m, stream, args.warmup))
     return out
@@ -544,6 +545,41 @@ def nvfp4_configs(m, cold, stream, steps, warmup):
                                 "unique_experts": U, "needed_bytes": nb,
                                 "gbs": round(nb / (st["mean"] * 1e-6) / 1e9, 1)}
     del nvs
+    return out
+
+
+def attn_configs(m, stream, steps, warmup):
+    """The attention side of a decode step (per-head Q/K RMSNorm + RoPE + bf16
+    KV-cache write, one kernel) at batch 1 / 8 / 32 / 128: 8 distinct input
+    sets (positions up to 2^18, a 4096-row cache each) chained per replay like
+    the layer steps.  Its bytes (~20 KiB per token) stay in L2, so the figure is
+    the kernel's latency, not a bandwidth claim."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = {}
+    for B in (1, 8, 32, 128):
+        sets = []
+        for i in range(8):
+            d = {k: v.to(dev) for k, v in fs.attn_inputs(900 + 16 * B + i, B, 4096).items()}
+            d["q"] = torch.empty((B, m.N_Q_HEADS, m.HEAD_DIM), dtype=torch.bfloat16, device=dev)
+            sets.append(d)
+
+        def call(i, sets=sets):
+            d = sets[i]
+            m.flint_qk_norm_rope_kv_bf16(d["qkv"], d["q_norm"], d["k_norm"], d["positions"],
+                                         d["slot_mapping"], d["q"], d["k_cache"], d["v_cache"],
+                                         1.0e6, 1e-6, stream=stream)
+
+        class _Spacer:
+            def before(self, i):
+                torch.cuda._sleep(SPACER_CYCLES)
+
+        times, _, _ = timed_chain(Chain(call, len(sets), stream), steps, warmup, _Spacer(), stream)
+        st = stats_us(times)
+        row = (m.N_Q_HEADS + 2 * m.N_KV_HEADS) * m.HEAD_DIM
+        nbytes = B * row * 2 + 2 * m.HEAD_DIM * 2 + B * (m.N_Q_HEADS + 2 * m.N_KV_HEADS) * m.HEAD_DIM * 2
+        out["qk_norm_rope_kv_b%d" % B] = {"us": round(st["mean"], 3), "p50_us": round(st["p50"], 3),
+                                          "bytes": nbytes,
+                                          "gbs": round(nbytes / (st["mean"] * 1e-6) / 1e9, 1)}
     return out
 
 

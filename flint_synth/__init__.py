@@ -25,7 +25,7 @@ import torch
 
 __all__ = [
     "Dims", "FULL", "TINY", "layer_weights", "tokens", "logit_offsets",
-    "pack_nvfp4", "nvfp4_layer", "E2M1_VALUES",
+    "pack_nvfp4", "nvfp4_layer", "E2M1_VALUES", "attn_inputs",
 ]
 
 
@@ -101,6 +101,35 @@ def logit_offsets(seed: int, n_experts: int = FULL.n_experts, device="cpu") -> t
     g = _gen(seed, device)
     return torch.randn((n_experts,), generator=g, device=device,
                        dtype=torch.float32) * OFFSET_STD
+
+
+def attn_inputs(seed: int, batch: int, cache_slots: int, n_q: int = 32, n_kv: int = 4,
+                head_dim: int = 128, max_pos: int = 1 << 18, device="cpu") -> dict:
+    """Inputs of a decode step's attention side (per-head Q/K norm + RoPE +
+    KV-cache write; GQA 32 / 4 heads: [vLLM Day-0 Support for Recursive's
+    Flint, "Flint Model Architecture"]):
+      qkv [batch, (n_q + 2 n_kv) * head_dim] bf16 ~ N(0, 1) (projection rows);
+      q_norm, k_norm [head_dim] bf16 ~ N(1, 0.1) (per-element gains);
+      positions [batch] int32 uniform in [0, max_pos) (2^18: the 262k context);
+      slot_mapping [batch] int32: distinct cache rows, every 7th token -1
+      (padding);
+      k_cache, v_cache [cache_slots, n_kv, head_dim] bf16 ~ N(0, 1) (rows the
+      step must leave as they are).
+    The value distributions are this library's choices; the pages give none."""
+    assert cache_slots >= batch
+    g = _gen(seed, device)
+    row = (n_q + 2 * n_kv) * head_dim
+    qkv = torch.randn((batch, row), generator=g, device=device).to(torch.bfloat16)
+    q_norm = (1.0 + 0.1 * torch.randn((head_dim,), generator=g, device=device)).to(torch.bfloat16)
+    k_norm = (1.0 + 0.1 * torch.randn((head_dim,), generator=g, device=device)).to(torch.bfloat16)
+    positions = torch.randint(0, max_pos, (batch,), generator=g, device=device, dtype=torch.int32)
+    slots = torch.randperm(cache_slots, generator=g, device=device)[:batch].to(torch.int32)
+    slots[6::7] = -1
+    cache = (cache_slots, n_kv, head_dim)
+    k_cache = torch.randn(cache, generator=g, device=device).to(torch.bfloat16)
+    v_cache = torch.randn(cache, generator=g, device=device).to(torch.bfloat16)
+    return {"qkv": qkv, "q_norm": q_norm, "k_norm": k_norm, "positions": positions,
+            "slot_mapping": slots, "k_cache": k_cache, "v_cache": v_cache}
 
 
 # --- NVFP4 packing -----------------------------------------------------------

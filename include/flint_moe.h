@@ -262,6 +262,51 @@ flint_status flint_moe_rmsnorm_bf16(const flint_moe_dims* dims, int32_t batch,
                                     const void* in_bf16, void* out_bf16, float eps,
                                     cudaStream_t stream);
 
+/* Shape of the attention side of a decode step: query heads, KV heads, head
+ * size.  Supported: 32, 4, 128 ("Grouped Query Attention (GQA) with 32 query
+ * and 4 KV heads": [vLLM Day-0 Support for Recursive's Flint, "Flint Model
+ * Architecture"]; 128 from the same section's 28 KiB of KV per token over its
+ * 14 full-attention layers: K and V of 4 heads x 128 bf16 values per layer). */
+typedef struct {
+  int32_t n_q_heads, n_kv_heads, head_dim;
+} flint_attn_dims;
+
+/* The attention side of a decode step fused in one kernel: per-head Q/K
+ * RMSNorm, rotary position embedding and the bf16 KV-cache write ("The fusion
+ * of Q/K norm, RoPE, and KV-cache write into a single kernel": [vLLM Day-0
+ * Support for Recursive's Flint, "Optimization Strategies", "Fused Kernels"]).
+ * For each token t (D = head_dim, nq = n_q_heads, nkv = n_kv_heads):
+ *   qkv_bf16      [batch, (nq + 2 nkv) * D]: the token's projection row,
+ *                 query heads, then key heads, then value heads;
+ *   q_norm_bf16, k_norm_bf16 [D]: the learned per-element gains of the
+ *                 query and key head norms ("per-head Q/K RMSNorm");
+ *   positions     [batch] int32 (device): the token's position;
+ *   slot_mapping  [batch] int32 (device): the cache row the token's K and V go
+ *                 to; a slot outside [0, cache_slots) writes nothing (a
+ *                 negative slot marks a padding token);
+ *   q and k heads: n[i] = x[i] / sqrt(mean_i x^2 + eps) * g[i]; then, if
+ *                 rope_theta > 0, elements i and i + D/2 turn by the angle
+ *                 positions[t] * rope_theta^(-2i/D) (rotate-half pairing;
+ *                 rope_theta = 0 for the layers without positional encoding);
+ *   q_out_bf16    [batch, nq, D] <- the query heads;
+ *   k_cache_bf16, v_cache_bf16 [cache_slots, nkv, D]: row slot_mapping[t]
+ *                 <- the key heads, and the value heads unchanged (bit for
+ *                 bit); every other row is left as it was.
+ * fp32 arithmetic (the angles in fp64), one bf16 rounding per output.  The
+ * rotate-half pairing and rope_theta as an argument are this library's
+ * readings: the pages name RoPE only.  Errors (before any launch):
+ * FLINT_ERR_UNSUPPORTED for other dims; FLINT_ERR_INVALID_ARG for a NULL or
+ * misaligned pointer (16 bytes; 4 for positions and slot_mapping), batch
+ * outside [1, FLINT_MOE_MAX_BATCH], cache_slots < 1, a negative or
+ * non-finite rope_theta or eps, or overlapping outputs / inputs.  Needs no
+ * workspace. */
+flint_status flint_qk_norm_rope_kv_bf16(const flint_attn_dims* dims, int32_t batch,
+                                        const void* qkv_bf16, const void* q_norm_bf16,
+                                        const void* k_norm_bf16, const int32_t* positions,
+                                        const int32_t* slot_mapping, float rope_theta, float eps,
+                                        void* q_out_bf16, void* k_cache_bf16, void* v_cache_bf16,
+                                        int64_t cache_slots, cudaStream_t stream);
+
 /* Fault-injection hook for tests: arms a one-shot device-side wait, in the
  * next routing launch on this workspace, on a workspace flag that nothing ever
  * sets.  That wait runs out after the workspace's wait limit and records

@@ -41,7 +41,7 @@ EXPORTS = (
     "flint_moe_get_device_status", "flint_moe_route", "flint_moe_bucket",
     "flint_moe_decode_bf16", "flint_moe_decode_nvfp4_w4a16", "flint_moe_rmsnorm_bf16",
     "flint_moe_debug_arm_stall", "flint_moe_gateup_bf16", "flint_moe_down_bf16",
-    "flint_moe_decode_bf16_noalloc",
+    "flint_moe_decode_bf16_noalloc", "flint_qk_norm_rope_kv_bf16",
 )
 NOALLOC_MAX_BATCH = 8
 
@@ -64,6 +64,17 @@ class Dims(ctypes.Structure):
 
 FULL_DIMS = Dims(HIDDEN, N_EXPERTS, TOP_K, INTER, N_SHARED, FLINT_OFFSET_LOGIT)
 SELECT_DIMS = Dims(HIDDEN, N_EXPERTS, TOP_K, INTER, N_SHARED, FLINT_OFFSET_SELECT)
+
+# The attention side of a decode step (flint_qk_norm_rope_kv_bf16).
+N_Q_HEADS, N_KV_HEADS, HEAD_DIM = 32, 4, 128
+
+
+class AttnDims(ctypes.Structure):
+    _fields_ = [("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32)]
+
+
+ATTN_DIMS = AttnDims(N_Q_HEADS, N_KV_HEADS, HEAD_DIM)
 
 _lib = None
 _P = ctypes.c_void_p
@@ -106,6 +117,9 @@ def lib() -> ctypes.CDLL:
     L.flint_moe_rmsnorm_bf16.argtypes = [_P, _I32, _P, _P, ctypes.c_float, _P]
     L.flint_moe_decode_bf16_noalloc.restype = ctypes.c_int
     L.flint_moe_decode_bf16_noalloc.argtypes = [_P, _I32] + [_P] * 13
+    L.flint_qk_norm_rope_kv_bf16.restype = ctypes.c_int
+    L.flint_qk_norm_rope_kv_bf16.argtypes = ([_P, _I32] + [_P] * 5 + [ctypes.c_float] * 2 +
+                                             [_P] * 3 + [ctypes.c_int64, _P])
     _lib = L
     return L
 
@@ -365,6 +379,31 @@ def flint_moe_rmsnorm_bf16(inp, out, eps: float = 1e-6, stream=None, dims: Dims 
     args = (_arg(f, "inp", inp, _BF16, (B, d.hidden), dev),
             _arg(f, "out", out, _BF16, (B, d.hidden), dev))
     _check(lib().flint_moe_rmsnorm_bf16(_dims(dims), B, *args, float(eps), _stream(stream)), f)
+
+
+def flint_qk_norm_rope_kv_bf16(qkv, q_norm, k_norm, positions, slot_mapping, q_out, k_cache,
+                               v_cache, rope_theta: float, eps: float = 1e-6, stream=None):
+    """Per-head Q/K RMSNorm + RoPE (rope_theta = 0: none) of a decode step's
+    projection rows qkv [B, (32 + 2*4) * 128], writing the query heads to
+    q_out [B, 32, 128] and the key / value heads to row slot_mapping[t] of
+    k_cache / v_cache [slots, 4, 128]; positions and slot_mapping are int32 [B]."""
+    f = "flint_qk_norm_rope_kv_bf16"
+    row = (N_Q_HEADS + 2 * N_KV_HEADS) * HEAD_DIM
+    B, dev = _batch(f, "qkv", qkv, row)
+    if not (isinstance(k_cache, torch.Tensor) and k_cache.dim() == 3):
+        _bad(f, "k_cache", "a [slots, %d, %d] tensor" % (N_KV_HEADS, HEAD_DIM), k_cache)
+    slots = k_cache.shape[0]
+    cache = (slots, N_KV_HEADS, HEAD_DIM)
+    args = (_arg(f, "qkv", qkv, _BF16, (B, row), dev),
+            _arg(f, "q_norm", q_norm, _BF16, (HEAD_DIM,), dev),
+            _arg(f, "k_norm", k_norm, _BF16, (HEAD_DIM,), dev),
+            _arg(f, "positions", positions, _I32T, (B,), dev),
+            _arg(f, "slot_mapping", slot_mapping, _I32T, (B,), dev))
+    outs = (_arg(f, "q_out", q_out, _BF16, (B, N_Q_HEADS, HEAD_DIM), dev),
+            _arg(f, "k_cache", k_cache, _BF16, cache, dev),
+            _arg(f, "v_cache", v_cache, _BF16, cache, dev))
+    _check(lib().flint_qk_norm_rope_kv_bf16(ctypes.byref(ATTN_DIMS), B, *args, float(rope_theta),
+                                            float(eps), *outs, slots, _stream(stream)), f)
 
 
 # ---------------------------------------------------------------- conveniences

@@ -7,8 +7,11 @@
 #include <cstdint>
 #include <cstring>
 
+#include <cmath>
+
 #include "flint_moe.h"
 #include "kernels.h"
+#include "qk_rope.h"
 
 using namespace flint;
 
@@ -319,6 +322,44 @@ flint_status flint_moe_decode_nvfp4_w4a16(
   w.ws2_q = ws2_q; w.ws2_sf = ws2_sf; w.ws2_ts = ws2_ts;
   return run_layer(true, dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias, w,
                    out_bf16, topk_idx_out, topk_w_out, workspace, stream);
+}
+
+flint_status flint_qk_norm_rope_kv_bf16(const flint_attn_dims* dims, int32_t batch,
+                                        const void* qkv_bf16, const void* q_norm_bf16,
+                                        const void* k_norm_bf16, const int32_t* positions,
+                                        const int32_t* slot_mapping, float rope_theta, float eps,
+                                        void* q_out_bf16, void* k_cache_bf16, void* v_cache_bf16,
+                                        int64_t cache_slots, cudaStream_t stream) {
+  if (dims == nullptr) return FLINT_ERR_INVALID_ARG;
+  if (dims->n_q_heads != qk::NQ || dims->n_kv_heads != qk::NKV || dims->head_dim != qk::HD)
+    return FLINT_ERR_UNSUPPORTED;
+  if (batch < 1 || batch > MAX_B || cache_slots < 1 || !req(qkv_bf16) || !req(q_norm_bf16) ||
+      !req(k_norm_bf16) || !req4(positions) || !req4(slot_mapping) || !req(q_out_bf16) ||
+      !req(k_cache_bf16) || !req(v_cache_bf16))
+    return FLINT_ERR_INVALID_ARG;
+  if (!(rope_theta >= 0.0f) || rope_theta > 3.0e38f || !(eps >= 0.0f) || eps > 3.0e38f)
+    return FLINT_ERR_INVALID_ARG;
+  const size_t in_b = (size_t)batch * qk::ROW * 2, q_b = (size_t)batch * qk::NQ * qk::HD * 2;
+  const size_t c_b = (size_t)cache_slots * qk::NKV * qk::HD * 2;
+  if (overlap(q_out_bf16, q_b, qkv_bf16, in_b) || overlap(k_cache_bf16, c_b, qkv_bf16, in_b) ||
+      overlap(v_cache_bf16, c_b, qkv_bf16, in_b) || overlap(k_cache_bf16, c_b, q_out_bf16, q_b) ||
+      overlap(v_cache_bf16, c_b, q_out_bf16, q_b) || overlap(k_cache_bf16, c_b, v_cache_bf16, c_b))
+    return FLINT_ERR_INVALID_ARG;
+  QkArgs a;
+  a.qkv = static_cast<const uint16_t*>(qkv_bf16);
+  a.q_norm = static_cast<const uint16_t*>(q_norm_bf16);
+  a.k_norm = static_cast<const uint16_t*>(k_norm_bf16);
+  a.pos = positions;
+  a.slots = slot_mapping;
+  a.rope = rope_theta > 0.0f;
+  for (int i = 0; i < qk::HD / 2; ++i)
+    a.inv_freq[i] = a.rope ? std::pow((double)rope_theta, -2.0 * i / qk::HD) : 0.0;
+  a.eps = eps;
+  a.q_out = static_cast<uint16_t*>(q_out_bf16);
+  a.k_cache = static_cast<uint16_t*>(k_cache_bf16);
+  a.v_cache = static_cast<uint16_t*>(v_cache_bf16);
+  a.cache_slots = (long long)cache_slots;
+  return cuda_status(launch_qk_norm_rope(a, batch, stream));
 }
 
 flint_status flint_moe_rmsnorm_bf16(const flint_moe_dims* dims, int32_t batch, const void* in_bf16,

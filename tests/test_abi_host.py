@@ -112,6 +112,34 @@ def test_route_bucket_rmsnorm_reject_bad_arguments(L):
     assert L.flint_moe_debug_arm_stall(None, wsb, None) == m.FLINT_ERR_WORKSPACE
 
 
+def test_qk_norm_rope_kv_rejects_bad_arguments(L):
+    f = L.flint_qk_norm_rope_kv_bf16
+    d = ctypes.byref(m.ATTN_DIMS)
+    row = (m.N_Q_HEADS + 2 * m.N_KV_HEADS) * m.HEAD_DIM
+    B, slots = 4, 64
+    qkv, qn, kn, pos, sl = A, A + 0x10000, A + 0x10100, A + 0x10200, A + 0x10300
+    q, kc, vc = A + 0x20000, A + 0x40000, A + 0x60000
+
+    def call(dims=d, batch=B, qkv_=qkv, theta=1.0e6, eps=1e-6, q_=q, kc_=kc, vc_=vc, n=slots,
+             pos_=pos):
+        return f(dims, batch, qkv_, qn, kn, pos_, sl, theta, eps, q_, kc_, vc_, n, None)
+
+    assert call(dims=None) == m.FLINT_ERR_INVALID_ARG
+    assert call(dims=ctypes.byref(m.AttnDims(32, 8, 128))) == m.FLINT_ERR_UNSUPPORTED
+    assert call(dims=ctypes.byref(m.AttnDims(32, 4, 64))) == m.FLINT_ERR_UNSUPPORTED
+    assert call(batch=0) == m.FLINT_ERR_INVALID_ARG
+    assert call(batch=m.MAX_BATCH + 1) == m.FLINT_ERR_INVALID_ARG
+    assert call(qkv_=qkv + 2) == m.FLINT_ERR_INVALID_ARG          # bf16 rows: 16-byte alignment
+    assert call(pos_=pos + 2) == m.FLINT_ERR_INVALID_ARG          # int32 vectors: 4 bytes
+    assert call(qkv_=None) == m.FLINT_ERR_INVALID_ARG
+    assert call(theta=-1.0) == m.FLINT_ERR_INVALID_ARG
+    assert call(theta=float("nan")) == m.FLINT_ERR_INVALID_ARG
+    assert call(eps=float("inf")) == m.FLINT_ERR_INVALID_ARG
+    assert call(n=0) == m.FLINT_ERR_INVALID_ARG
+    assert call(q_=qkv + B * row * 2 - 16) == m.FLINT_ERR_INVALID_ARG       # q_out overlaps qkv
+    assert call(vc_=kc + slots * 4 * 128 * 2 - 16) == m.FLINT_ERR_INVALID_ARG  # caches overlap
+
+
 def test_binding_checks_what_the_c_call_cannot():
     """The C calls take bare pointers: the binding rejects a tensor whose dtype,
     shape, layout or device differs from the header's layout, naming it, before
