@@ -12,9 +12,8 @@
 // so the fragment loads are free of bank conflicts.  The gate/up kernel
 // writes h with the same block order (h_chunk).  The odd warp of a pair hands
 // its tiles over in the half of the slice that only it reads.
-#include <mutex>
-
 #include "down_ring.cuh"
+#include "tmap.h"
 
 namespace flint {
 namespace {
@@ -51,25 +50,6 @@ struct Bf16Wd {
   }
   __device__ static float scale(const ExpertArgs&, int) { return 1.f; }
 };
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
 
 // Map of a Wd stack of `experts` matrices [H][I] (bf16, rows contiguous).
 cudaError_t encode_wd(CUtensorMap* m, const uint16_t* w, int experts) {

@@ -31,6 +31,7 @@
 #include "expert_common.cuh"
 #include "kernels.h"
 #include "nv_util.cuh"
+#include "tmap.h"
 
 namespace flint {
 using namespace nvu;
@@ -38,12 +39,20 @@ namespace f4 {
 constexpr int CWARPS = 8;
 constexpr int THREADS = CWARPS * 32 + 32;
 constexpr uint64_t DRAIN_NS = 2000000000ull;
-// gate/up
+// gate/up.  A stage holds one unit as four tensor-map copies with a 128-byte
+// swizzle (16-byte chunk c of a 128-byte line stored at c ^ (line mod 8)):
+// the 8 gate rows' codes as [column block L of 128 bytes][row r] lines, the 8
+// up rows' codes the same, then the gate and up rows' scales as [row] lines.
 constexpr int GU_QROW = H / 2;                       // 1024 code bytes per row
-constexpr int GU_QSTRIDE = GU_QROW;                  // 8 rows = one contiguous copy
 constexpr int GU_SFROW = H / 16;                     // 128 scale bytes per row
-constexpr int GU_STAGE = 16 * GU_QSTRIDE + 16 * GU_SFROW;  // 18,432
+constexpr int GU_UPQ = 8 * GU_QROW;                  // offsets in a stage
+constexpr int GU_SF = 16 * GU_QROW;
+constexpr int GU_UPSF = GU_SF + 8 * GU_SFROW;
+constexpr int GU_STAGE = 16 * GU_QROW + 16 * GU_SFROW;  // 18,432 (18 x 1 KiB)
 constexpr int GU_NSTAGE = 10;
+constexpr int GU_ALIGN = 1024;                       // swizzled copies land on 1 KiB boundaries
+static_assert(GU_STAGE % GU_ALIGN == 0 && GU_SF % GU_ALIGN == 0 && GU_UPSF % GU_ALIGN == 0,
+              "every copy starts on a 1 KiB boundary");
 // A round takes up to GU_UB(NT) units of one group at once; their partial
 // tiles [unit][warp][16 rows][NT * 8 tokens] share one reduction.
 __host__ __device__ constexpr int gu_ub(int nt) { return nt == 1 ? 4 : nt == 2 ? 2 : 1; }
@@ -52,8 +61,9 @@ static_assert(GU_RED >= 2 * CWARPS * 16 * 16 && GU_RED >= CWARPS * 16 * GROUP_MA
 // The reduction buffer doubles as the logits buffer of the local selection.
 constexpr int GU_BUF = GU_RED * 4 > LOCAL_SELECT_MAX_B * E * 4 ? GU_RED * 4 : LOCAL_SELECT_MAX_B * E * 4;
 constexpr size_t GU_SMEM =
-    (size_t)GU_NSTAGE * GU_STAGE + GU_BUF + sizeof(MetaSmem) + 2 * GU_NSTAGE * 8;
+    GU_ALIGN + (size_t)GU_NSTAGE * GU_STAGE + GU_BUF + sizeof(MetaSmem) + 2 * GU_NSTAGE * 8;
 constexpr int UNITS = I / 8;
+static_assert(GU_SMEM <= 232448, "the gate/up ring fits one CTA's shared memory");
 }  // namespace f4
 
 namespace {
@@ -136,9 +146,11 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   named_sync(1, f4::CWARPS * 32);  // the previous segment is done with `red`
-  // K order inside this warp's 256-column slice: thread q of a quad owns the
-  // 32 consecutive columns [32q + 128m, +32) for m = 0, 1 (16 contiguous code
-  // bytes per row); step (m, i) covers columns 32q + 128m + 8i .. +8.  The
+  // K order inside this warp's 256-column slice (its 128-byte code line):
+  // thread q of a quad owns the 32 consecutive columns [64q + 32m, +32) for
+  // m = 0, 1, i.e. 16-byte chunk 2q + m of the line; step (m, i) covers
+  // columns 64q + 32m + 8i .. +8.  Under the swizzle, rows g and g + 1 of a
+  // quarter-warp then read chunks of opposite parity: no bank conflicts.  The
   // activations follow the same order, so the MMA sums match.
   uint4 bfr[NT][2][4];
 #pragma unroll
@@ -146,13 +158,13 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, c
     const int slot = nt * 8 + g;
     if (slot < n) {
       const int tok = pair_tok[pair0 + slot];
-      const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)tok * H + warp * 256 + q * 32);
+      const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)tok * H + warp * 256 + q * 64);
       bool big = false;
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint4 xv = __ldg(row + m * 16 + i);
+          const uint4 xv = __ldg(row + m * 4 + i);
           big |= bf16x8_beyond_f16(xv);
           bfr[nt][m][i] = bf16x8_to_f16x8(xv);
         }
@@ -181,28 +193,28 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, c
       st[k] = p.stages + slot * p.stage_bytes;
     }
     if (ok) {
-      const bool qh = (q >> 1) != 0;
+      // code line `warp` of row g: [warp][g][128 B], chunk c at c ^ g; scale
+      // line g: the warp's 16 blocks are chunk `warp`, at warp ^ g, of which
+      // this thread's columns use word q
+      const int qoff = (warp * 8 + g) * 128;
+      const int soff = f4::GU_SF + g * f4::GU_SFROW + ((warp ^ g) * 16) + 4 * q;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
 #pragma unroll
         for (int k = 0; k < UB; ++k) {
           if (k >= ub) continue;
-          const uint8_t* qlo = st[k] + g * f4::GU_QSTRIDE + warp * 128 + q * 16;
-          const uint8_t* qhi = qlo + 8 * f4::GU_QSTRIDE;
-          const uint8_t* sfb = st[k] + 16 * f4::GU_QSTRIDE;
-          const uint4 slo = *reinterpret_cast<const uint4*>(sfb + g * f4::GU_SFROW + warp * 16);
-          const uint4 shi = *reinterpret_cast<const uint4*>(sfb + (g + 8) * f4::GU_SFROW + warp * 16);
-          const uint4 clo = *reinterpret_cast<const uint4*>(qlo + m * 64);
-          const uint4 chi = *reinterpret_cast<const uint4*>(qhi + m * 64);
+          const uint8_t* ql = st[k] + qoff + (((2 * q + m) ^ g) * 16);
+          const uint4 clo = *reinterpret_cast<const uint4*>(ql);
+          const uint4 chi = *reinterpret_cast<const uint4*>(ql + f4::GU_UPQ);
+          const uint32_t wl = *reinterpret_cast<const uint32_t*>(st[k] + soff);
+          const uint32_t wh = *reinterpret_cast<const uint32_t*>(st[k] + soff + 8 * f4::GU_SFROW);
           const uint32_t cl[4] = {clo.x, clo.y, clo.z, clo.w};
           const uint32_t ch[4] = {chi.x, chi.y, chi.z, chi.w};
-          // block of step (m, i) = 8m + 2q + i/2 within the warp's 16 blocks:
-          // scale word 2m + q/2
-          const uint32_t wl = m ? (qh ? slo.w : slo.z) : (qh ? slo.y : slo.x);
-          const uint32_t wh = m ? (qh ? shi.w : shi.z) : (qh ? shi.y : shi.x);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int sh_bits = 8 * (2 * (q & 1) + (i >> 1));
+            // block of step (m, i) = 4q + 2m + i/2 of the warp's 16: byte
+            // 2m + i/2 of word q
+            const int sh_bits = 8 * (2 * m + (i >> 1));
             const uint32_t scl = e4m3_bcast_f16x2((wl >> sh_bits) & 0xffu);
             const uint32_t sch = e4m3_bcast_f16x2((wh >> sh_bits) & 0xffu);
             uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
@@ -261,31 +273,47 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, c
   }
 }
 
-__device__ __forceinline__ void gu_produce(const Pipe& p, const ExpertArgs& a, const int4* groups,
-                                           int u_begin,
-                                           int u_end) {
+// Tensor maps of the gate/up codes and scales (routed and shared expert
+// stacks): codes as (128 bytes, row, 8 column blocks) with strides (1 B,
+// 1 KiB, 128 B), scales as (128 bytes, row); boxes of 8 rows; 128-byte swizzle.
+struct GuMaps {
+  CUtensorMap q, sq, sf, ssf;
+};
+
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(0), "r"(c1), "r"(0), "r"(bar), "l"(l2_evict_first())
+      : "memory");
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(0), "r"(c1), "r"(bar), "l"(l2_evict_first())
+      : "memory");
+}
+
+__device__ __forceinline__ void gu_produce(const Pipe& p, const GuMaps& maps, const int4* groups,
+                                           int u_begin, int u_end) {
   int it = 0;
   for (int u = u_begin; u < u_end; ++u) {
     const int4 grp = groups[u / f4::UNITS];
     const int blk = u & (f4::UNITS - 1);
     const bool routed = grp.x < E;
     const int e = routed ? grp.x : grp.x - E;
-    const uint8_t* qb = (routed ? a.w.w13_q : a.w.ws13_q) + (size_t)e * (2 * I) * f4::GU_QROW;
-    const uint8_t* sb = (routed ? a.w.w13_sf : a.w.ws13_sf) + (size_t)e * (2 * I) * f4::GU_SFROW;
+    const CUtensorMap* mq = routed ? &maps.q : &maps.sq;
+    const CUtensorMap* ms = routed ? &maps.sf : &maps.ssf;
+    const int gate_row = e * (2 * I) + blk * 8, up_row = gate_row + I;
     if (!acquire_stage(p, it)) break;
     const int slot = it % p.nstage;
-    mbar_expect_tx(full_bar(p, slot), 16 * f4::GU_QROW + 16 * f4::GU_SFROW);
+    mbar_expect_tx(full_bar(p, slot), f4::GU_STAGE);
     const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
-    bulk_g2s_stream(dst, qb + (size_t)(blk * 8) * f4::GU_QROW, 8 * f4::GU_QROW, full_bar(p, slot));
-    bulk_g2s_stream(dst + 8 * f4::GU_QSTRIDE, qb + (size_t)(I + blk * 8) * f4::GU_QROW,
-                    8 * f4::GU_QROW,
-             full_bar(p, slot));
-    bulk_g2s_stream(dst + 16 * f4::GU_QSTRIDE, sb + (size_t)(blk * 8) * f4::GU_SFROW,
-                    8 * f4::GU_SFROW,
-             full_bar(p, slot));
-    bulk_g2s_stream(dst + 16 * f4::GU_QSTRIDE + 8 * f4::GU_SFROW,
-                    sb + (size_t)(I + blk * 8) * f4::GU_SFROW,
-             8 * f4::GU_SFROW, full_bar(p, slot));
+    tma_3d(dst, mq, gate_row, full_bar(p, slot));
+    tma_3d(dst + f4::GU_UPQ, mq, up_row, full_bar(p, slot));
+    tma_2d(dst + f4::GU_SF, ms, gate_row, full_bar(p, slot));
+    tma_2d(dst + f4::GU_UPSF, ms, up_row, full_bar(p, slot));
     ++it;
   }
   drain(p, it);
@@ -293,8 +321,11 @@ __device__ __forceinline__ void gu_produce(const Pipe& p, const ExpertArgs& a, c
 
 }  // namespace
 
-__global__ void __launch_bounds__(f4::THREADS, 1) gateup_nvfp4_kernel(ExpertArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(f4::THREADS, 1)
+    gateup_nvfp4_kernel(ExpertArgs a, const __grid_constant__ GuMaps maps) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + f4::GU_ALIGN - 1) & ~uint32_t(f4::GU_ALIGN - 1)) - raw_addr);
   __shared__ int s_abort;
   __shared__ LocalSelectSmem s_sel;
   float* red = reinterpret_cast<float*>(smem + f4::GU_NSTAGE * f4::GU_STAGE);
@@ -309,7 +340,7 @@ __global__ void __launch_bounds__(f4::THREADS, 1) gateup_nvfp4_kernel(ExpertArgs
     named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
     if ((threadIdx.x & 31) == 0) {
       const int n_units = meta.n_groups * f4::UNITS;
-      gu_produce(p, a, meta.groups, (int)((long long)blockIdx.x * n_units / gridDim.x),
+      gu_produce(p, maps, meta.groups, (int)((long long)blockIdx.x * n_units / gridDim.x),
                  (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x));
     }
     return;
@@ -336,7 +367,30 @@ __global__ void __launch_bounds__(f4::THREADS, 1) gateup_nvfp4_kernel(ExpertArgs
   }
 }
 
+// Map of `rows` rows of `row_bytes` bytes at `base`, as (128 bytes, row) or,
+// for code rows (1 KiB), as (128 bytes, row, 8 column blocks); boxes of 8 rows.
+static cudaError_t encode_gu(CUtensorMap* m, const uint8_t* base, size_t rows, int row_bytes) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const bool codes = row_bytes == f4::GU_QROW;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)(row_bytes / 128)};
+  const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, 128};  // bytes, for dims 1 and 2
+  const cuuint32_t box[3] = {128, 8, (cuuint32_t)(row_bytes / 128)};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes ? 3 : 2,
+                         const_cast<uint8_t*>(base), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms) {
+  GuMaps maps;
+  cudaError_t em = encode_gu(&maps.q, a.w.w13_q, (size_t)E * 2 * I, f4::GU_QROW);
+  if (em == cudaSuccess) em = encode_gu(&maps.sq, a.w.ws13_q, (size_t)S * 2 * I, f4::GU_QROW);
+  if (em == cudaSuccess) em = encode_gu(&maps.sf, a.w.w13_sf, (size_t)E * 2 * I, f4::GU_SFROW);
+  if (em == cudaSuccess) em = encode_gu(&maps.ssf, a.w.ws13_sf, (size_t)S * 2 * I, f4::GU_SFROW);
+  if (em != cudaSuccess) return em;
   static std::atomic<uint64_t> smem_set{0};
   const cudaError_t es = set_smem_limit_once(gateup_nvfp4_kernel, (int)f4::GU_SMEM, smem_set);
   if (es != cudaSuccess) return es;
@@ -350,7 +404,7 @@ cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int nu
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gateup_nvfp4_kernel, a);
+  return cudaLaunchKernelEx(&cfg, gateup_nvfp4_kernel, a, maps);
 }
 
 // ---------------------------------------------------------------- down
