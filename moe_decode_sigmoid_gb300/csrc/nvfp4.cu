@@ -614,6 +614,7 @@ __global__ void __launch_bounds__(256) combine_y_kernel(ExpertArgs a) {
   __shared__ int s_pairs[SLOTS];
   __shared__ int s_ok;
   pdl_wait();  // y and the pair table come from the preceding kernels
+  pdl_trigger();  // a following router may start loading its rows
   const int t = blockIdx.y, lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
     const int np = a.B * SLOTS;

@@ -121,11 +121,16 @@ __device__ __forceinline__ void route_tail(const RouterArgs& a, int t0, int nt) 
 }  // namespace
 
 __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
-  pdl_wait();     // x may come from the preceding kernel in the stream
-  pdl_trigger();  // the expert kernels may start their prologue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int el = warp >> 2, qk = warp & 3;
   const int e = blockIdx.x * 2 + el;
+  const int c0 = qk * 64 + lane, c1 = c0 + 32;  // 16-byte chunks of the 4 KiB row
+  const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * H);
+  // The router rows are weights, which no kernel writes: their loads start
+  // before the wait, so they overlap the end of the preceding kernel.
+  const uint4 w0 = ldg_stream(wrow + c0), w1 = ldg_stream(wrow + c1);
+  pdl_wait();     // x may come from the preceding kernel in the stream
+  pdl_trigger();  // the expert kernels may start their prologue
   const int t0 = blockIdx.y * 8;
   const int nt = min(8, a.B - t0);
   WsHeader* hdr = a.ws.hdr;
@@ -144,9 +149,6 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
     hdr->stall_armed = 0;
   }
 
-  const int c0 = qk * 64 + lane, c1 = c0 + 32;  // 16-byte chunks of the 4 KiB row
-  const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * H);
-  const uint4 w0 = ldg_stream(wrow + c0), w1 = ldg_stream(wrow + c1);
   uint4 xv[8][2];
 #pragma unroll
   for (int t = 0; t < 8; ++t) {
@@ -201,11 +203,15 @@ __global__ void __launch_bounds__(256) bucket_kernel(Ws ws, int B, BucketOut use
 // ranking / bucketing tail as router_kernel, with 16-token tiles.  Against
 // 8-token tiles of 2 experts, x is re-read 4x less often from L2.
 __global__ void __launch_bounds__(256) router_mma_kernel(RouterArgs a) {
-  pdl_wait();     // x may come from the preceding kernel in the stream
-  pdl_trigger();  // the expert kernels may start their prologue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   const int e0 = blockIdx.x * 8, t0 = blockIdx.y * 16;
+  const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)(e0 + g) * H);
+  uint4 wv[8];
+#pragma unroll
+  for (int b = 0; b < 8; ++b) wv[b] = ldg_stream(wrow + warp * 32 + b * 4 + q);  // before the wait, as above
+  pdl_wait();     // x may come from the preceding kernel in the stream
+  pdl_trigger();  // the expert kernels may start their prologue
   const int nt = min(16, a.B - t0);
   WsHeader* hdr = a.ws.hdr;
   if (a.stall_check && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 &&
@@ -223,15 +229,13 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterArgs a) {
   const bool lo_in = g < nt, hi_in = g + 8 < nt;
   const uint4* xlo = reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + (lo_in ? g : 0)) * H);
   const uint4* xhi = reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + (hi_in ? g + 8 : 0)) * H);
-  const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)(e0 + g) * H);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 xl[8], xh[8], wv[8];
+  uint4 xl[8], xh[8];
 #pragma unroll
   for (int b = 0; b < 8; ++b) {  // all loads of the slice in flight at once
     const int c = warp * 32 + b * 4 + q;  // 16-byte chunk: columns 256w + 32b + 8q
     xl[b] = lo_in ? __ldg(xlo + c) : zero;
     xh[b] = hi_in ? __ldg(xhi + c) : zero;
-    wv[b] = ldg_stream(wrow + c);
   }
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
