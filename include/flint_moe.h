@@ -262,6 +262,34 @@ flint_status flint_moe_rmsnorm_bf16(const flint_moe_dims* dims, int32_t batch,
                                     const void* in_bf16, void* out_bf16, float eps,
                                     cudaStream_t stream);
 
+/* flint_moe_decode_bf16 with the layer's input RMSNorm folded in: the layer
+ * input is x = bf16( residual / sqrt(mean(residual^2) + norm_eps) ) (unit
+ * gain, exactly as flint_moe_rmsnorm_bf16 computes it), so a pre-norm stack
+ * calls this once per layer on the previous layer's output (pre-norm
+ * decoder: [vLLM Day-0 Support for Recursive's Flint, "Flint Model
+ * Architecture"]; the low-latency decode path folds the small ops around the
+ * MoE GEMVs into them: same page, "Optimization Strategies").  For batches of
+ * <= 4 tokens the persistent kernel normalises the rows itself (no extra
+ * launch; measured faster there); above that the norm runs first, into the
+ * workspace.
+ *   residual_bf16 [batch, H]  the pre-norm activations (the residual stream)
+ *   norm_eps      >= 0 (a NaN or negative value is FLINT_ERR_INVALID_ARG)
+ *   out_bf16      [batch, H]  may alias residual_bf16 exactly; no other
+ *                             overlap; residual_bf16 must not overlap the
+ *                             workspace
+ *   the rest as flint_moe_decode_bf16.
+ * Results are bit for bit those of flint_moe_rmsnorm_bf16 into a separate x
+ * followed by flint_moe_decode_bf16. */
+flint_status flint_moe_decode_bf16_prenorm(const flint_moe_dims* dims, int32_t batch,
+                                           const void* residual_bf16, float norm_eps,
+                                           const void* w_router_bf16, const float* logit_bias,
+                                           const void* w13_bf16, const void* w2_bf16,
+                                           const void* ws13_bf16, const void* ws2_bf16,
+                                           void* out_bf16,
+                                           int32_t* topk_idx_out, float* topk_w_out,
+                                           void* workspace, size_t ws_bytes,
+                                           cudaStream_t stream);
+
 /* Shape of the attention side of a decode step: query heads, KV heads, head
  * size.  Supported: 32, 4, 128 ("Grouped Query Attention (GQA) with 32 query
  * and 4 KV heads": [vLLM Day-0 Support for Recursive's Flint, "Flint Model

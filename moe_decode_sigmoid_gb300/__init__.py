@@ -42,8 +42,13 @@ EXPORTS = (
     "flint_moe_decode_bf16", "flint_moe_decode_nvfp4_w4a16", "flint_moe_rmsnorm_bf16",
     "flint_moe_debug_arm_stall", "flint_moe_gateup_bf16", "flint_moe_down_bf16",
     "flint_moe_decode_bf16_noalloc", "flint_qk_norm_rope_kv_bf16",
+    "flint_moe_decode_bf16_prenorm",
 )
 NOALLOC_MAX_BATCH = 8
+# Batches up to which flint_moe_decode_bf16_prenorm is one launch (the
+# persistent kernel normalises its input itself); 5..8 tokens take the RMSNorm
+# kernel + the persistent kernel, larger batches the RMSNorm + three kernels.
+PRENORM_FUSED_MAX_BATCH = 4
 
 
 class FlintError(RuntimeError):
@@ -115,6 +120,9 @@ def lib() -> ctypes.CDLL:
     L.flint_moe_down_bf16.argtypes = [_P, _I32, _P, _P, _P, _P, _P, _SZ, _P]
     L.flint_moe_rmsnorm_bf16.restype = ctypes.c_int
     L.flint_moe_rmsnorm_bf16.argtypes = [_P, _I32, _P, _P, ctypes.c_float, _P]
+    L.flint_moe_decode_bf16_prenorm.restype = ctypes.c_int
+    L.flint_moe_decode_bf16_prenorm.argtypes = ([_P, _I32, _P, ctypes.c_float] + [_P] * 10 +
+                                                [_SZ, _P])
     L.flint_moe_decode_bf16_noalloc.restype = ctypes.c_int
     L.flint_moe_decode_bf16_noalloc.argtypes = [_P, _I32] + [_P] * 13
     L.flint_qk_norm_rope_kv_bf16.restype = ctypes.c_int
@@ -303,6 +311,21 @@ def flint_moe_decode_bf16(x, residual, w_router, logit_bias, w13, w2, ws13, ws2,
                        topk_idx_out, topk_w_out)
     wp, wb = _ws_arg(f, workspace, dev)
     _check(lib().flint_moe_decode_bf16(_dims(dims), B, *args, wp, wb, _stream(stream)), f)
+
+
+def flint_moe_decode_bf16_prenorm(residual, w_router, logit_bias, w13, w2, ws13, ws2, out,
+                                  workspace, norm_eps: float = 1e-6, topk_idx_out=None,
+                                  topk_w_out=None, stream=None, dims: Dims | None = None):
+    """flint_moe_decode_bf16 whose input is RMSNorm(residual) (unit gain,
+    norm_eps), computed inside the call: one launch per layer for batches of
+    at most 8 tokens."""
+    f, d = "flint_moe_decode_bf16_prenorm", _d(dims)
+    B, dev = _batch(f, "residual", residual, d.hidden)
+    args = _layer_args(f, d, B, dev, residual, residual, w_router, logit_bias, w13, w2, ws13, ws2,
+                       out, topk_idx_out, topk_w_out)
+    wp, wb = _ws_arg(f, workspace, dev)
+    _check(lib().flint_moe_decode_bf16_prenorm(_dims(dims), B, args[1], float(norm_eps), *args[2:],
+                                               wp, wb, _stream(stream)), f)
 
 
 def flint_moe_decode_bf16_noalloc(x, residual, w_router, logit_bias, w13, w2, ws13, ws2, out,

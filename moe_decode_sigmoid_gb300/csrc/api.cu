@@ -186,13 +186,32 @@ flint_status flint_moe_bucket(const flint_moe_dims* dims, int32_t batch, const i
   return cuda_status(launch_bucket(w, batch, bo, stream));
 }
 
+// norm_eps >= 0: x is not given; the layer input is RMSNorm(residual), taken
+// by the persistent kernel itself (batch <= PRENORM_FUSED_MAX_B) or written
+// into the workspace first by the RMSNorm kernel (the NVFP4 path's y rows,
+// which the BF16 kernels do not use).
 static flint_status run_layer(bool nvfp4, const flint_moe_dims* dims, int32_t batch,
                               const void* x, const void* residual,
                               const void* wr, const float* bias, const ExpertW& w, void* out,
                               int32_t* idx_out, float* w_out, void* workspace,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, float norm_eps = -1.0f) {
   const int sms = num_sms();
   if (sms <= 0) return FLINT_ERR_CUDA;
+  const bool fused =
+      batch <= (nvfp4 ? NVFP4_FUSED_MAX_B : LOCAL_SELECT_MAX_B) && small_supported(sms);
+  const bool prenorm = norm_eps >= 0.0f;
+  const bool fold = prenorm && fused && batch <= PRENORM_FUSED_MAX_B;
+  if (prenorm) {
+    if (fold) {
+      x = residual;  // the kernel normalises the rows as it stages them
+    } else {
+      uint16_t* xn = reinterpret_cast<uint16_t*>(ws_y(ws_view(workspace), batch));
+      const cudaError_t e = launch_rmsnorm(static_cast<const uint16_t*>(residual), xn, batch,
+                                           norm_eps, stream);
+      if (e != cudaSuccess) return cuda_status(e);
+      x = xn;
+    }
+  }
   RouterArgs r = {};
   r.x = static_cast<const uint16_t*>(x);
   r.wr = static_cast<const uint16_t*>(wr);
@@ -224,10 +243,12 @@ static flint_status run_layer(bool nvfp4, const flint_moe_dims* dims, int32_t ba
   a.bias_select_only = r.bias_select_only;
   a.user_idx = idx_out;
   a.user_w = w_out;
+  a.prenorm = fold;
+  a.norm_eps = norm_eps;
   // One persistent kernel for small batches.  NVFP4 units are compute-heavy
   // (dequantisation), and from 3 tokens on the chained kernels, whose gate/up
   // and down kernels spread each group's work over all SMs, are faster.
-  if (batch <= (nvfp4 ? NVFP4_FUSED_MAX_B : LOCAL_SELECT_MAX_B) && small_supported(sms))
+  if (fused)
     return cuda_status(nvfp4 ? launch_small_nvfp4(a, r, stream, sms)
                              : launch_small_bf16(a, r, stream, sms));
   cudaError_t e = launch_router(r, stream, true);
@@ -259,6 +280,35 @@ flint_status flint_moe_decode_bf16(const flint_moe_dims* dims, int32_t batch, co
   w.ws2 = static_cast<const uint16_t*>(ws2_bf16);
   return run_layer(false, dims, batch, x_bf16, residual_bf16, w_router_bf16, logit_bias, w,
                    out_bf16, topk_idx_out, topk_w_out, workspace, stream);
+}
+
+flint_status flint_moe_decode_bf16_prenorm(const flint_moe_dims* dims, int32_t batch,
+                                           const void* residual_bf16, float norm_eps,
+                                           const void* w_router_bf16, const float* logit_bias,
+                                           const void* w13_bf16, const void* w2_bf16,
+                                           const void* ws13_bf16, const void* ws2_bf16,
+                                           void* out_bf16, int32_t* topk_idx_out,
+                                           float* topk_w_out, void* workspace, size_t ws_bytes,
+                                           cudaStream_t stream) {
+  flint_status st = check_common(dims, batch, workspace, ws_bytes);
+  if (st != FLINT_OK) return st;
+  if (!req(residual_bf16) || !req(w_router_bf16) || !opt4(logit_bias) || !req(w13_bf16) ||
+      !req(w2_bf16) || !req(ws13_bf16) || !req(ws2_bf16) || !req(out_bf16) ||
+      !opt4(topk_idx_out) || !opt4(topk_w_out) || !(norm_eps >= 0.0f))
+    return FLINT_ERR_INVALID_ARG;
+  const size_t act = (size_t)batch * H * 2;
+  if (out_bf16 != residual_bf16 && overlap(out_bf16, act, residual_bf16, act))
+    return FLINT_ERR_INVALID_ARG;
+  if (overlap(out_bf16, act, workspace, ws_bytes) ||
+      overlap(residual_bf16, act, workspace, ws_bytes))
+    return FLINT_ERR_INVALID_ARG;
+  ExpertW w = {};
+  w.w13 = static_cast<const uint16_t*>(w13_bf16);
+  w.w2 = static_cast<const uint16_t*>(w2_bf16);
+  w.ws13 = static_cast<const uint16_t*>(ws13_bf16);
+  w.ws2 = static_cast<const uint16_t*>(ws2_bf16);
+  return run_layer(false, dims, batch, nullptr, residual_bf16, w_router_bf16, logit_bias, w,
+                   out_bf16, topk_idx_out, topk_w_out, workspace, stream, norm_eps);
 }
 
 flint_status flint_moe_gateup_bf16(const flint_moe_dims* dims, int32_t batch, const void* x_bf16,

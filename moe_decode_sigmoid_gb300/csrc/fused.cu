@@ -740,9 +740,54 @@ __device__ __forceinline__ void st_release_cta_shared_u64(uint64_t* p, uint64_t 
   asm volatile("st.release.cta.shared::cta.u64 [%0], %1;" ::"r"(smem_addr(p)), "l"(v) : "memory");
 }
 
+// The layer's input RMSNorm of rows 0 .. NR-1 of a batch staged as in the
+// persistent kernel (consumer thread tid holds elements 8 tid .. 8 tid + 7 of
+// every row; rows at or past the batch are zeros and are never stored), in
+// the same arithmetic as the standalone RMSNorm kernel -- fp32 sum of squares
+// in element order, warp_sum's butterfly, the 8 warp sums added in warp order,
+// rsqrtf -- so x comes out bit for bit as that kernel writes it.  The rows'
+// chains run side by side.
+template <int NR>
+__device__ __forceinline__ void input_rmsnorm(uint4 (&v)[fz::MAXB], float (*s_norm)[fz::CW],
+                                              float eps, int lane, int warp) {
+  float ss[NR];
+#pragma unroll
+  for (int t = 0; t < NR; ++t) {
+    const uint4 u = v[t];
+    const float f[8] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y),
+                        bf_lo(u.z), bf_hi(u.z), bf_lo(u.w), bf_hi(u.w)};
+    ss[t] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss[t] = fmaf(f[i], f[i], ss[t]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int t = 0; t < NR; ++t) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < NR; ++t) s_norm[t][warp] = ss[t];
+  }
+  named_sync(1, fz::CT);
+#pragma unroll
+  for (int t = 0; t < NR; ++t) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < fz::CW; ++w) tot += s_norm[t][w];
+    const float inv = rsqrtf(tot / (float)H + eps);
+    const uint4 u = v[t];
+    v[t] = make_uint4(pack_bf2(bf_lo(u.x) * inv, bf_hi(u.x) * inv),
+                      pack_bf2(bf_lo(u.y) * inv, bf_hi(u.y) * inv),
+                      pack_bf2(bf_lo(u.z) * inv, bf_hi(u.z) * inv),
+                      pack_bf2(bf_lo(u.w) * inv, bf_hi(u.w) * inv));
+  }
+}
+
 }  // namespace
 
-template <bool NV>
+// PRENORM: the rows at a.x are pre-norm activations (input_rmsnorm); a
+// separate instance, so that the plain kernel's code stays as it is.
+template <bool NV, bool PRENORM>
 __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
   using Gm = fz::Geo<NV>;
   constexpr int ND = fz::ND<NV>;
@@ -1031,6 +1076,14 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     for (int t = 0; t < fz::MAXB; ++t)
       v[t] = t < B ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H) + tid)
                    : make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (PRENORM) {
+      __shared__ float s_norm[fz::MAXB][fz::CW];
+      static_assert(PRENORM_FUSED_MAX_B <= fz::MAXB, "rows in registers");
+      if (B == 1)
+        input_rmsnorm<1>(v, s_norm, a.norm_eps, lane, warp);
+      else
+        input_rmsnorm<PRENORM_FUSED_MAX_B>(v, s_norm, a.norm_eps, lane, warp);
+    }
 #pragma unroll
     for (int t = 0; t < fz::MAXB; ++t)
       if (t < B) reinterpret_cast<uint4*>(xs)[t * (H / 8) + tid] = v[t];
@@ -1270,21 +1323,26 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
 }
 
 __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertArgs a, RouterArgs r) {
-  moe_small_body<false>(a, r);
+  moe_small_body<false, false>(a, r);
+}
+__global__ void __launch_bounds__(fz::THREADS, 1)
+    moe_small_bf16_prenorm_kernel(ExpertArgs a, RouterArgs r) {
+  moe_small_body<false, true>(a, r);
 }
 __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_nvfp4_kernel(ExpertArgs a, RouterArgs r) {
-  moe_small_body<true>(a, r);
+  moe_small_body<true, false>(a, r);
 }
 
 bool small_supported(int num_sms) { return num_sms >= 86 && num_sms <= 1024; }
 
 namespace {
-template <bool NV>
+template <bool NV, bool PRENORM>
 cudaError_t launch_small(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                          int num_sms) {
   static std::atomic<uint64_t> smem_set{0};
   constexpr size_t smem = fz::smem_bytes<NV>();
-  void (*const kernel)(ExpertArgs, RouterArgs) = NV ? moe_small_nvfp4_kernel : moe_small_bf16_kernel;
+  void (*const kernel)(ExpertArgs, RouterArgs) =
+      NV ? moe_small_nvfp4_kernel : PRENORM ? moe_small_bf16_prenorm_kernel : moe_small_bf16_kernel;
   const cudaError_t es = set_smem_limit_once(kernel, (int)smem, smem_set);
   if (es != cudaSuccess) return es;
   cudaLaunchConfig_t cfg = {};
@@ -1309,11 +1367,12 @@ cudaError_t launch_small(const ExpertArgs& a, const RouterArgs& r, cudaStream_t 
 
 cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                               int num_sms) {
-  return launch_small<false>(a, r, stream, num_sms);
+  return a.prenorm ? launch_small<false, true>(a, r, stream, num_sms)
+                   : launch_small<false, false>(a, r, stream, num_sms);
 }
 cudaError_t launch_small_nvfp4(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                                int num_sms) {
-  return launch_small<true>(a, r, stream, num_sms);
+  return launch_small<true, false>(a, r, stream, num_sms);
 }
 
 }  // namespace flint

@@ -54,6 +54,11 @@ struct ExpertArgs {
   int bias_select_only;  // as RouterArgs
   int* user_idx;     // gate/up with local_select: optional routing copies
   float* user_w;
+  // Persistent kernel (BF16): the rows at x are the pre-norm activations, and
+  // the kernel (its prenorm instance) takes bf16(x / sqrt(mean(x^2) + norm_eps))
+  // (unit gain) in their place.
+  int prenorm;
+  float norm_eps;
 };
 
 // Largest batch whose routing the expert kernels compute themselves.
@@ -62,6 +67,12 @@ constexpr int LOCAL_SELECT_MAX_B = SMALL_B;
 // with the chained kernels on GB300: at 2 tokens 29.4 us against 31.1 us, at 3
 // tokens 36.0 us against 32.5 us).
 constexpr int NVFP4_FUSED_MAX_B = 2;
+// Largest batch whose input RMSNorm the persistent kernel takes itself (the
+// prenorm call); above it the standalone RMSNorm kernel runs first.  Measured
+// per layer in the 47-layer stack on GB300, folded against RMSNorm kernel +
+// persistent kernel: -1.2, -0.7, -0.6, -0.3 us at 1..4 tokens, +0.3, +0.35,
+// +0.5 us at 5, 6, 8.
+constexpr int PRENORM_FUSED_MAX_B = 4;
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_bucket(const Ws& ws, int B, const BucketOut& user, cudaStream_t stream);

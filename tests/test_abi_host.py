@@ -99,6 +99,36 @@ def test_decode_rejects_bad_arguments_before_launch(L):
                                           None) == m.FLINT_ERR_INVALID_ARG
 
 
+def test_decode_prenorm_rejects_bad_arguments_before_launch(L):
+    f = L.flint_moe_decode_bf16_prenorm
+    res, out = A + 0x10000, A + 0x20000
+
+    def call(dims=m.FULL_DIMS, batch=1, res_=res, eps=1e-6, wr=A, w13=A, out_=out, ws=WS,
+             wsb=None):
+        if wsb is None:
+            wsb = m.flint_moe_workspace_bytes(max(1, min(batch, 256)))
+        return f(ctypes.byref(dims), batch, res_, eps, wr, None, w13, A, A, A, out_, None, None,
+                 ws, wsb, None)
+
+    assert call(dims=m.Dims(2048, 128, 6, 512, 1)) == m.FLINT_ERR_UNSUPPORTED
+    assert call(batch=0) == m.FLINT_ERR_INVALID_ARG
+    assert call(res_=None) == m.FLINT_ERR_INVALID_ARG
+    assert call(res_=res + 2) == m.FLINT_ERR_INVALID_ARG             # misaligned
+    assert call(wr=None) == m.FLINT_ERR_INVALID_ARG
+    assert call(w13=None) == m.FLINT_ERR_INVALID_ARG
+    assert call(eps=-1e-6) == m.FLINT_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == m.FLINT_ERR_INVALID_ARG
+    assert call(ws=None) == m.FLINT_ERR_WORKSPACE
+    assert call(batch=8, wsb=m.flint_moe_workspace_bytes(4)) == m.FLINT_ERR_WORKSPACE
+    # out partially overlapping the residual, or the workspace; the residual
+    # inside the workspace (the norm may be written there)
+    assert call(out_=res + 0x100) == m.FLINT_ERR_INVALID_ARG
+    assert call(out_=WS + 0x100) == m.FLINT_ERR_INVALID_ARG
+    assert call(res_=WS + 0x1000) == m.FLINT_ERR_INVALID_ARG
+    assert f(None, 1, res, 1e-6, A, None, A, A, A, A, out, None, None, WS, 1 << 30,
+             None) == m.FLINT_ERR_INVALID_ARG
+
+
 def test_route_bucket_rmsnorm_reject_bad_arguments(L):
     d = ctypes.byref(m.FULL_DIMS)
     wsb = m.flint_moe_workspace_bytes(4)
