@@ -133,7 +133,8 @@ flint_status flint_moe_workspace_init(void* workspace, size_t ws_bytes,
 /* Synchronises `stream`, then reads and returns the workspace's device error
  * word: FLINT_OK, FLINT_ERR_DEVICE_TIMEOUT, or FLINT_ERR_INVALID_ARG when
  * flint_moe_bucket was given a routing row that is not k distinct experts or
- * an NVFP4 call met an activation beyond f16's range. */
+ * an NVFP4 call met an activation (x, or h above 2 tokens) beyond the range
+ * its f16 operands hold. */
 flint_status flint_moe_get_device_status(const void* workspace, cudaStream_t stream);
 
 /* Router only: logits, sigmoid top-k, renormalised weights.
@@ -235,8 +236,9 @@ flint_status flint_moe_down_bf16(const flint_moe_dims* dims, int32_t batch,
  * the tensor cores, so every activation must satisfy |x| < 65504 (an
  * RMS-normalised x is below sqrt(H) = 45.3): a larger one sets the device
  * status to FLINT_ERR_INVALID_ARG, and the outputs are undefined.  h is kept
- * in fp32 for batches of <= 2 tokens (the persistent kernel) and as a bf16
- * pair hi + lo (about 16 significant bits, the range of fp32) above that.
+ * in fp32 for batches of <= 2 tokens (the persistent kernel) and, above that,
+ * as h / 256 in an f16 pair hi + lo (about 22 significant bits), which holds
+ * |h| < 65520 * 256 (~1.7e7): a larger h also sets FLINT_ERR_INVALID_ARG.
  *   w13_q [E, 2I, H/2], w13_sf [E, 2I, H/16], w13_ts [E, 2] (gate, up)
  *   w2_q  [E, H, I/2],  w2_sf  [E, H, I/16],  w2_ts  [E]
  *   ws13_q/ws13_sf/ws13_ts and ws2_q/ws2_sf/ws2_ts: the shared expert(s),

@@ -28,7 +28,8 @@ constexpr int MAX_GROUPS = TOPK * MAX_B / GROUP_MAX + E + S * (MAX_B / GROUP_MAX
 // Device error codes written to the workspace error word.
 constexpr uint32_t DEV_OK = 0;
 constexpr uint32_t DEV_BAD_ROUTING = 1;  // bucketing got an index outside [0,E) or a repeat
-constexpr uint32_t DEV_BAD_INPUT = 1;    // an NVFP4 activation beyond f16's range (|x| >= 65520)
+constexpr uint32_t DEV_BAD_INPUT = 1;    // an NVFP4 activation beyond its f16 operand's range
+                                         // (|x| >= 65520, or |h| >= 65520 / NV_H_SCALE)
 constexpr uint32_t DEV_TIMEOUT = 5;
 
 // ---- workspace layout ------------------------------------------------------
@@ -40,8 +41,8 @@ constexpr uint32_t DEV_TIMEOUT = 5;
 // The tagged regions belong to the persistent small-batch kernels: each 8-byte
 // word holds a 32-bit value and the call's tag (see call_tag), so a reader on
 // another SM knows from the word itself whether it was written in this call.
-// h holds the three-kernel paths' bf16 hi + lo pairs: the BF16 gate/up
-// kernel's (see h_chunk) or the NVFP4 one's (h_off_nv).
+// h holds the three-kernel paths' hi + lo pairs: the BF16 gate/up kernel's
+// bf16 ones (see h_chunk) or the NVFP4 one's f16 ones (h_off_nv).
 // Every array but the last two is sized for MAX_B (or the small-batch bound),
 // so the offsets do not depend on the batch a workspace was sized for; h and y
 // grow with max_batch, and a call with batch B finds y right after the first
@@ -315,9 +316,12 @@ __device__ __forceinline__ void store_h_block8(float* h, size_t pair, int blk, f
   }
 }
 
-// The NVFP4 path's h: each value as a bf16 pair hi + lo (as the BF16 path,
-// ~16 significant bits and the range of fp32, so no activation overflows),
-// one 2 KiB row per pair (pair p at byte 2048 p of the h region).  The
+// The NVFP4 path's h: each value scaled by NV_H_SCALE (a power of two) as an
+// f16 pair hi + lo -- ~22 significant bits, and the operand type of the down
+// kernel's f16 MMAs, whose dequantised weights are exact in f16 -- for |h| <
+// 65520 / NV_H_SCALE (~1.7e7; beyond that the gate/up kernel reports
+// DEV_BAD_INPUT); one 2 KiB row per pair (pair p at byte 2048 p of the h
+// region).  The
 // 32-byte block b (columns 8b .. 8b + 7: 8 hi values, then 8 lo values) sits
 // in 128-byte line b % 16 at slot b / 16 -- the order in which the NVFP4 down
 // kernel's lanes take K (lane q: columns 128q .. 128q + 127, blocks 16q ..
@@ -326,14 +330,19 @@ __device__ __forceinline__ void store_h_block8(float* h, size_t pair, int blk, f
 __host__ __device__ __forceinline__ int h_off_nv(size_t pair, int blk, int part) {
   return (blk & 15) * 128 + (blk >> 4) * 32 + ((part ^ (int)(pair & 1)) * 16);
 }
+constexpr float NV_H_SCALE = 1.0f / 256.0f;
 
 // One block at once: called by all 32 lanes of a warp, lanes 8m..8m+7
 // holding elements 0..7 of one block (v); the first lane of each 8-lane group
-// stores the block when `store` is true (uniform within the group).
-__device__ __forceinline__ void store_h_block8_nv(float* h, size_t pair, int blk, float v,
+// stores the block when `store` is true (uniform within the group).  Returns
+// true on a lane whose stored value is beyond the f16 range.
+__device__ __forceinline__ bool store_h_block8_nv(float* h, size_t pair, int blk, float v,
                                                   bool store) {
-  const uint32_t hi = f2bf(v);
-  const uint32_t lo = f2bf(v - bf_lo(hi));
+  const float vs = v * NV_H_SCALE;
+  const __half hh = __float2half_rn(vs);
+  const __half hl = __float2half_rn(vs - __half2float(hh));
+  const uint32_t hi = __half_as_ushort(hh);
+  const uint32_t lo = __half_as_ushort(hl);
   const uint32_t hw = hi | (__shfl_down_sync(0xffffffffu, hi, 1) << 16);
   const uint32_t lw = lo | (__shfl_down_sync(0xffffffffu, lo, 1) << 16);
   const uint4 hv = make_uint4(hw, __shfl_down_sync(0xffffffffu, hw, 2),
@@ -347,6 +356,7 @@ __device__ __forceinline__ void store_h_block8_nv(float* h, size_t pair, int blk
     *reinterpret_cast<uint4*>(row + h_off_nv(pair, blk, 0)) = hv;
     *reinterpret_cast<uint4*>(row + h_off_nv(pair, blk, 1)) = lv;
   }
+  return store && !(fabsf(vs) < 65520.0f);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

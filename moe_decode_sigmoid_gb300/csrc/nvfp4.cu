@@ -13,10 +13,11 @@
 // codes with cvt.rn.f16x2.e2m1x2, multiplies by the block scale (f16x2, exact)
 // and feeds mma.sync m16n8k16 f16 x f16 -> fp32.  bf16 activations convert to
 // f16 exactly (8 significant bits; |x| inside f16's normal range); the tensor
-// scale is applied to the fp32 sums.  h is stored as a bf16 pair hi + lo (the
-// range of fp32), so the down kernel converts its dequantised weights to bf16
-// -- still exact, the same value in fewer exponent-limited bits -- and runs
-// bf16 MMAs on both halves.  Dequantisation costs about one instruction per weight, which is
+// scale is applied to the fp32 sums.  h is stored scaled by 2^-8 as an f16
+// pair hi + lo (~22 significant bits; |h| up to ~1.7e7, beyond which the
+// gate/up kernel reports the input), so the down kernel feeds its dequantised
+// f16 weights straight into f16 MMAs on both halves and undoes the scale on
+// the sums.  Dequantisation costs about one instruction per weight, which is
 // why this path uses the tensor cores for every group, including single-token
 // ones: the FMAs then cost nothing on the CUDA cores that do the unpacking.
 //
@@ -266,8 +267,10 @@ __device__ __forceinline__ void gu_segment(const Pipe& p, const ExpertArgs& a, c
         us += red[((kr * f4::CWARPS + w) * 16 + r + 8) * NC + jr];
       }
       const int blk = (u + kr) & (f4::UNITS - 1);
-      store_h_block8_nv(a.ws.h, (size_t)(pair0 + jr), blk, silu_mul(gs * ts_g, us * ts_u),
-                        valid && ok);
+      // h beyond the f16 pair's range would reach the down kernel as infinities
+      if (store_h_block8_nv(a.ws.h, (size_t)(pair0 + jr), blk, silu_mul(gs * ts_g, us * ts_u),
+                            valid && ok))
+        set_error(a.ws.hdr, DEV_BAD_INPUT);
     }
     named_sync(1, f4::CWARPS * 32);
   }
@@ -432,7 +435,7 @@ constexpr int DN_QROW = I / 2;                  // code bytes per row
 constexpr int DN_SFROW = I / 16;                // scale bytes per row
 constexpr int DN_QB = DN_RB * DN_QROW;          // 32 KiB
 constexpr int DN_SB = DN_RB * DN_SFROW;         // 4 KiB
-constexpr int DN_HROW = I * 4;                  // one h row (bf16 hi + lo pairs)
+constexpr int DN_HROW = I * 4;                  // one h row (f16 hi + lo pairs)
 constexpr int DN_MAX_STAGES = 4;
 constexpr int SMEM_CAP = 232448 - 1024;
 __host__ __device__ inline int dn_stage(int B) {
@@ -495,23 +498,23 @@ __device__ __forceinline__ void dn_unit(const ExpertArgs& a, const uint8_t* st, 
     uint32_t l0, l1, l2, l3, u0, u1, u2, u3;
     e2m1x8_to_f16x2(w0, l0, l1, l2, l3);
     e2m1x8_to_f16x2(w1, u0, u1, u2, u3);
-    l0 = bf2_of_h2(hmul2(l0, sc0)); l1 = bf2_of_h2(hmul2(l1, sc0));
-    l2 = bf2_of_h2(hmul2(l2, sc0)); l3 = bf2_of_h2(hmul2(l3, sc0));
-    u0 = bf2_of_h2(hmul2(u0, sc1)); u1 = bf2_of_h2(hmul2(u1, sc1));
-    u2 = bf2_of_h2(hmul2(u2, sc1)); u3 = bf2_of_h2(hmul2(u3, sc1));
+    l0 = hmul2(l0, sc0); l1 = hmul2(l1, sc0); l2 = hmul2(l2, sc0); l3 = hmul2(l3, sc0);
+    u0 = hmul2(u0, sc1); u1 = hmul2(u1, sc1); u2 = hmul2(u2, sc1); u3 = hmul2(u3, sc1);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       // block 16q + j of the token's row (h_off_nv): hi and lo halves
       const uint8_t* hb8 = hrow[nt] + j * 128;
       const uint4 hh = *reinterpret_cast<const uint4*>(hb8 + hx[nt]);
       const uint4 hl = *reinterpret_cast<const uint4*>(hb8 + (16 - hx[nt]));
-      mma_bf16(acc[nt][0], l0, u0, l1, u1, hh.x, hh.y);
-      mma_bf16(acc[nt][1], l2, u2, l3, u3, hh.z, hh.w);
-      mma_bf16(acc[nt][0], l0, u0, l1, u1, hl.x, hl.y);
-      mma_bf16(acc[nt][1], l2, u2, l3, u3, hl.z, hl.w);
+      mma_f16(acc[nt][0], l0, u0, l1, u1, hh.x, hh.y);
+      mma_f16(acc[nt][1], l2, u2, l3, u3, hh.z, hh.w);
+      mma_f16(acc[nt][0], l0, u0, l1, u1, hl.x, hl.y);
+      mma_f16(acc[nt][1], l2, u2, l3, u3, hl.z, hl.w);
     }
   }
-  const float ts = expert < E ? __ldg(a.w.w2_ts + expert) : __ldg(a.w.ws2_ts + (expert - E));
+  // h was stored scaled by NV_H_SCALE (a power of two): undone here, exactly
+  const float ts = (expert < E ? __ldg(a.w.w2_ts + expert) : __ldg(a.w.ws2_ts + (expert - E))) *
+                   (1.0f / NV_H_SCALE);
   const int row = rb * f4::DN_RB + 16 * warp + g;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {

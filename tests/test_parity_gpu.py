@@ -464,6 +464,29 @@ def test_nvfp4_reports_activations_beyond_f16(m, layer, nv_layer, B):
     assert rel_err(bf16_bits_to_f64(out), ref) <= REL_TOL
 
 
+@pytest.mark.parametrize("B", [3, 13])
+def test_nvfp4_reports_h_beyond_its_f16_pair(m, layer, nv_layer, B):
+    """Above 2 tokens the NVFP4 path keeps h / 256 as an f16 pair: gate and up
+    tensor scales times 2^16 put |h| far beyond 65520 * 256, which the call
+    reports as FLINT_ERR_INVALID_ARG on the device instead of returning
+    infinities; after re-initialisation the workspace works again."""
+    W, host = layer
+    nv, nv_host = nv_layer
+    ws = m.new_workspace(B)
+    x, res = fs.tokens(4800 + B, B, device="cuda")
+    nvb = dict(nv)
+    nvb["w13_ts"] = nv["w13_ts"] * 65536.0
+    nvb["ws13_ts"] = nv["ws13_ts"] * 65536.0
+    out = torch.empty_like(res)
+    m.flint_moe_decode_nvfp4_w4a16(x, res, W["wr"], None, nvb, out, ws)
+    assert m.flint_moe_get_device_status(ws) == m.FLINT_ERR_INVALID_ARG
+    m.flint_moe_workspace_init(ws)
+    out, idx, w = run_nvfp4(m, W, nv, x, res, None, ws)
+    gi, w_ref = check_routing(host, x, None, idx, w)
+    ref = oracle.moe_nvfp4_given_routing(D, x.cpu(), res.cpu(), gi, w_ref, nv_host)
+    assert rel_err(bf16_bits_to_f64(out), ref) <= REL_TOL
+
+
 def test_calls_of_mixed_batches_on_one_workspace_match_fresh_workspaces(m, layer):
     """The batch <= 8 kernel tells this call's exchanged data from older data
     by a call tag; calls of different batches (and of the three-kernel path)
