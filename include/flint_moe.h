@@ -236,7 +236,6 @@ flint_status flint_moe_down_bf16(const flint_moe_dims* dims, int32_t batch,
  * the tensor cores, so every activation must satisfy |x| < 65504 (an
  * RMS-normalised x is below sqrt(H) = 45.3): a larger one sets the device
  * status to FLINT_ERR_INVALID_ARG, and the outputs are undefined.  h is kept
- * in fp32 for batches of <= 2 tokens (the persistent kernel) and, above that,
  * as h / 256 in an f16 pair hi + lo (about 22 significant bits), which holds
  * |h| < 65520 * 256 (~1.7e7): a larger h also sets FLINT_ERR_INVALID_ARG.
  *   w13_q [E, 2I, H/2], w13_sf [E, 2I, H/16], w13_ts [E, 2] (gate, up)

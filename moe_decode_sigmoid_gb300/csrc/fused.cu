@@ -1,5 +1,5 @@
-// fused.cu — the whole decode MoE layer in one persistent kernel, for batches
-// of at most SMALL_B (8) tokens, with BF16 or NVFP4 expert weights: the pages'
+// fused.cu — the whole BF16 decode MoE layer in one persistent kernel, for
+// batches of at most SMALL_B (8) tokens: the pages'
 // low-latency path for up to 8 requests, which fuses routing and the expert
 // combine into the neighbouring GEMVs ("Low-Latency Decode Path": vLLM Day-0
 // Support for Recursive's Flint, "Optimization Strategies").
@@ -21,13 +21,11 @@
 //      counter -- the shared expert's 64 gate/up units, the routed groups'
 //      gate/up units in group order, then the down units of every group (the
 //      shared group first) -- so CTAs that stream faster take more units.
-//      A gate/up unit is 8 gate + 8 up rows of one group (BF16: two 32 KiB
-//      slots; NVFP4: codes and block scales in one 20 KiB slot); the consumer
-//      warps store h as tagged words and the last of them to finish adds one
-//      to the group's completion counter (64 = the group's h is complete).
-//      A down unit is a block of Wd rows of one group's expert (BF16: 32 rows,
-//      one slot; NVFP4: 64 rows, codes and scales in one slot) plus the
-//      group's h rows in one or two more slots: its weights are copied as soon
+//      A gate/up unit is 8 gate + 8 up rows of one group (two 32 KiB slots);
+//      the consumer warps store h as tagged words and the last of them to
+//      finish adds one to the group's completion counter (64 = the group's h
+//      is complete).  A down unit is 64 Wd rows of one group's expert (two
+//      slots of 32 rows) plus the group's h rows: its weights are copied as soon
 //      as it is claimed, its h rows once the poll warp has seen the group
 //      complete.  Every gate/up claim precedes every down claim, so no ring
 //      waits on a unit queued behind it.
@@ -48,7 +46,6 @@
 #include "expert_common.cuh"
 #include "gateup_impl.cuh"
 #include "kernels.h"
-#include "nv_util.cuh"
 
 namespace flint {
 namespace fz {
@@ -73,33 +70,16 @@ constexpr int RROW_BYTES = RMAX * H * 2;
 // router rows, then the batch's logits, then the gate/up units' partial tiles
 constexpr int BUF_BYTES = RED_BYTES > LOGIT_BYTES ? (RED_BYTES > RROW_BYTES ? RED_BYTES : RROW_BYTES)
                                                   : (LOGIT_BYTES > RROW_BYTES ? LOGIT_BYTES : RROW_BYTES);
-// Ring and unit layout of each weight format.
-template <bool NV>
-struct Geo;
-template <>
-struct Geo<false> {  // BF16
+// Ring and unit layout.
+struct Geo {
   static constexpr int SLOT = 32 * 1024, NS = 5;
   static constexpr int GR = 8;                              // gate/up unit: 8 gate + 8 up rows
   static constexpr int UNIT_SLOTS = 2;                      // gate rows | up rows
   static constexpr int DR = 64;                             // Wd rows per down unit
   static constexpr int DN_SLOTS = 2;                        // rows 0-31 | rows 32-63
 };
-template <>
-struct Geo<true> {  // NVFP4
-  static constexpr int SLOT = 20 * 1024, NS = 8;
-  static constexpr int GR = 8;                              // gate/up unit: 8 gate + 8 up rows
-  static constexpr int UNIT_SLOTS = 1, DN_SLOTS = 1;
-  static constexpr int QROW = H / 2, SFROW = H / 16;        // one gate/up row
-  static constexpr int UNIT_BYTES = 16 * QROW + 16 * SFROW; // 18 KiB
-  static constexpr int DQROW = I / 2, DSFROW = I / 16;      // one Wd row
-  static constexpr int DR = 64;                             // Wd rows per down unit
-  static constexpr int WQ = DR * DQROW;                     // codes, 16 KiB
-  static constexpr int WBYTES = WQ + DR * DSFROW;           // + block scales, 18 KiB
-};
-template <bool NV>
-constexpr int UNITS = I / Geo<NV>::GR;         // gate/up units per group
-template <bool NV>
-constexpr int ND = H / Geo<NV>::DR;            // down units per group
+constexpr int UNITS = I / Geo::GR;             // gate/up units per group
+constexpr int ND = H / Geo::DR;                // down units per group
 // Down units take their h rows from the activations' buffer, which the gate/up
 // units no longer need by then, preceded by HDED rows of their own: a ring of
 // HROWS contiguous tagged rows whose first HDED are free from the start (the
@@ -112,9 +92,8 @@ __device__ __forceinline__ int hring_row(int h0, int i) {
   const int r = h0 + i;
   return r >= HROWS ? r - HROWS : r;
 }
-template <bool NV>
 constexpr size_t smem_bytes() {
-  return (size_t)Geo<NV>::NS * Geo<NV>::SLOT + HDED_BYTES + XS_BYTES + BUF_BYTES;
+  return (size_t)Geo::NS * Geo::SLOT + HDED_BYTES + XS_BYTES + BUF_BYTES;
 }
 constexpr int NQ = 8;                          // down units posted and not yet released
 constexpr uint64_t DRAIN_NS = 2000000000ull;
@@ -123,16 +102,13 @@ static_assert(S == 1 && MAXB <= GROUP_MAX, "one shared group at these batches");
 static_assert(MAXG <= DONE_SHARED, "routed groups and the shared group have distinct counters");
 static_assert(DONE_SHARED < 64, "one bit per counter in a 64-bit mask");
 static_assert(SYNC_LINES <= CT, "one thread clears each counter line");
-static_assert(Geo<false>::GR * ROWB == Geo<false>::SLOT, "8 gate (or up) rows fill one BF16 slot");
-static_assert(Geo<false>::DR / 2 * WROW == Geo<false>::SLOT, "32 Wd rows fill one BF16 slot");
-static_assert(Geo<true>::UNIT_BYTES <= Geo<true>::SLOT && Geo<true>::WBYTES <= Geo<true>::SLOT,
-              "an NVFP4 unit's weights fit one slot");
+static_assert(Geo::GR * ROWB == Geo::SLOT, "8 gate (or up) rows fill one slot");
+static_assert(Geo::DR / 2 * WROW == Geo::SLOT, "32 Wd rows fill one slot");
 static_assert(HROWS == 12 && MAXB <= HROWS, "a group's h rows fit the h ring");
-static_assert(Geo<false>::NS <= NQ && Geo<true>::NS <= NQ, "every posted down unit has a queue entry");
-static_assert(H % Geo<false>::DR == 0 && H % Geo<true>::DR == 0, "row blocks tile H");
+static_assert(Geo::NS <= NQ, "every posted down unit has a queue entry");
+static_assert(H % Geo::DR == 0, "row blocks tile H");
 static_assert((E + RMAX - 1) / RMAX <= 86, "grids of 86 CTAs or more keep <= RMAX router rows");
-static_assert(smem_bytes<false>() + 6 * 1024 <= 232448 && smem_bytes<true>() + 6 * 1024 <= 232448,
-              "fits the opt-in shared memory of one SM");
+static_assert(smem_bytes() + 6 * 1024 <= 232448, "fits the opt-in shared memory of one SM");
 }  // namespace fz
 
 namespace {
@@ -366,78 +342,6 @@ __device__ __forceinline__ void unit_finish(const float (&acc)[4], float* buf, u
   named_sync(1, fz::CT);  // buf is free again
 }
 
-// Gate/up unit of NVFP4 weights, on tensor cores for every group size (the
-// dequantisation, about one instruction per weight, dominates; the MMA then
-// costs nothing extra).  The slot holds the 8 gate rows' codes, the 8 up
-// rows' codes, then their block scales; the 16 rows are the MMA's M, the
-// tokens its N.  Warp w owns a 256-column K-slice; thread q of a quad takes
-// columns [32q + 128m, +32) for m = 0, 1 (16 contiguous code bytes per row),
-// the f16 activations in shared memory follow the same order.  Each code
-// times its E4M3 block scale is exact in f16.
-__device__ __forceinline__ void unit_nv(const uint8_t* st, const uint16_t* xh,
-                                        const int* pair_tok, float* buf, uint64_t* th,
-                                        const Item& d, float ts_g, float ts_u, bool ok,
-                                        uint32_t em, uint32_t tag, SyncLine* done, int* ucnt) {
-  using Gm = fz::Geo<true>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, q = lane & 3;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  if (ok) {
-    uint4 bfr[2][4];
-    if (g < d.n) {
-      const int tok = d.tok0 >= 0 ? d.tok0 + g : pair_tok[d.pair0 + g];
-      const uint4* row = reinterpret_cast<const uint4*>(xh + (size_t)tok * H + warp * 256 + q * 32);
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) bfr[m][i] = row[m * 16 + i];
-    } else {
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) bfr[m][i] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    const uint8_t* qlo = st + g * Gm::QROW + warp * 128 + q * 16;
-    const uint8_t* qhi = qlo + 8 * Gm::QROW;
-    const uint8_t* sfb = st + 16 * Gm::QROW;
-    const uint4 slo = *reinterpret_cast<const uint4*>(sfb + g * Gm::SFROW + warp * 16);
-    const uint4 shi = *reinterpret_cast<const uint4*>(sfb + (g + 8) * Gm::SFROW + warp * 16);
-    const bool qh = (q >> 1) != 0;
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      const uint4 clo = *reinterpret_cast<const uint4*>(qlo + m * 64);
-      const uint4 chi = *reinterpret_cast<const uint4*>(qhi + m * 64);
-      const uint32_t cl[4] = {clo.x, clo.y, clo.z, clo.w};
-      const uint32_t ch[4] = {chi.x, chi.y, chi.z, chi.w};
-      // columns 32q + 128m + 8i .. +8 are block 8m + 2q + i/2 of the warp's
-      // 16: byte 2(q & 1) + i/2 of scale word 2m + q/2
-      const uint32_t wl = m ? (qh ? slo.w : slo.z) : (qh ? slo.y : slo.x);
-      const uint32_t wh = m ? (qh ? shi.w : shi.z) : (qh ? shi.y : shi.x);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int sh = 8 * (2 * (q & 1) + (i >> 1));
-        const uint32_t scl = nvu::e4m3_bcast_f16x2((wl >> sh) & 0xffu);
-        const uint32_t sch = nvu::e4m3_bcast_f16x2((wh >> sh) & 0xffu);
-        uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
-        nvu::e2m1x8_to_f16x2(cl[i], l0, l1, l2, l3);
-        nvu::e2m1x8_to_f16x2(ch[i], h0, h1, h2, h3);
-        l0 = nvu::hmul2(l0, scl);
-        l1 = nvu::hmul2(l1, scl);
-        l2 = nvu::hmul2(l2, scl);
-        l3 = nvu::hmul2(l3, scl);
-        h0 = nvu::hmul2(h0, sch);
-        h1 = nvu::hmul2(h1, sch);
-        h2 = nvu::hmul2(h2, sch);
-        h3 = nvu::hmul2(h3, sch);
-        nvu::mma_f16(acc, l0, h0, l1, h1, bfr[m][i].x, bfr[m][i].y);
-        nvu::mma_f16(acc, l2, h2, l3, h3, bfr[m][i].z, bfr[m][i].w);
-      }
-    }
-  }
-  release_slot(em);
-  unit_finish<true>(acc, buf, th, d, ok, tag, done, ucnt, ts_g, ts_u);
-}
-
 // Sums of four values over the 32 lanes of a warp in six shuffles: lane l
 // ends with the sum of value ((l >> 4) & 1) * 2 + ((l >> 3) & 1).  Each lane
 // keeps half of its values and adds its partner's copy of them (lanes l and
@@ -516,7 +420,7 @@ __device__ __forceinline__ void down_cc(const DnCtx& c, const uint8_t* sa, const
       va[r][m] = wa[r * (fz::WROW / 4) + lane + 32 * m];
       vb[r][m] = wb[r * (fz::WROW / 4) + lane + 32 * m];
     }
-  const int row = d.blk * fz::Geo<false>::DR + 4 * warp + (lane >> 3);
+  const int row = d.blk * fz::Geo::DR + 4 * warp + (lane >> 3);
 #pragma unroll
   for (int i = 0; i < fz::MAXB; ++i) {
     if (i < n) {
@@ -558,80 +462,6 @@ __device__ __forceinline__ void down_cc(const DnCtx& c, const uint8_t* sa, const
   }
 }
 
-// NVFP4 down unit on CUDA cores: the slot's 64 Wd rows (codes, then block
-// scales).  Warp w owns rows 8w .. 8w+7, four at a time; lane l takes columns
-// 256hf + 8l .. +7 of each half hf: one code word and one block scale per row
-// and half, dequantised once to f16 (exact) and widened to fp32 where used.
-// The lane visits its four column pairs starting at pair (l >> 1) & 3 --
-// which makes every quarter-warp's 128-bit loads of tagged h words hit eight
-// distinct bank groups -- and its code words are rotated by as many bytes to
-// match.  The tensor scale joins the routing weight.
-__device__ __forceinline__ void down_nv(const DnCtx& c, const uint8_t* sw, const uint8_t* hb,
-                                        const Item& d, float ts, bool ok) {
-  using Gm = fz::Geo<true>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = d.n;
-  if (!ok) return;
-  const int rot = (lane >> 1) & 3;
-#pragma unroll 1
-  for (int pass = 0; pass < 2; ++pass) {
-    const int row0 = 8 * warp + 4 * pass;  // first of this pass's rows within the unit
-    uint32_t wf[4][2][4];  // [row][half][column pair j, visiting order]: f16x2 weights
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t wv =
-            *reinterpret_cast<const uint32_t*>(sw + (row0 + rr) * Gm::DQROW + hf * 128 + 4 * lane);
-        wv = __funnelshift_r(wv, wv, 8 * rot);
-        const uint32_t sc =
-            nvu::e4m3_bcast_f16x2(sw[Gm::WQ + (row0 + rr) * Gm::DSFROW + 16 * hf + (lane >> 1)]);
-        uint32_t pv[4];
-        nvu::e2m1x8_to_f16x2(wv, pv[0], pv[1], pv[2], pv[3]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) wf[rr][hf][j] = nvu::hmul2(pv[j], sc);
-      }
-    }
-    const int row = d.blk * Gm::DR + row0 + (lane >> 3);
-#pragma unroll
-    for (int i = 0; i < fz::MAXB; ++i) {
-      if (i < n) {
-        const uint8_t* hrow = hb + fz::hring_row(d.h0, i) * fz::THROW;
-        const uint4* hr = reinterpret_cast<const uint4*>(hrow);
-        float e[4], o[4];
-#pragma unroll 1
-        for (int attempt = 0;; ++attempt) {
-#pragma unroll
-          for (int r = 0; r < 4; ++r) e[r] = o[r] = 0.f;
-          bool bad = false;
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 hv = hr[128 * hf + 4 * lane + ((j + rot) & 3)];
-              bad |= (hv.y != c.tag) | (hv.w != c.tag);
-              const float h0 = __uint_as_float(hv.x), h1 = __uint_as_float(hv.z);
-#pragma unroll
-              for (int r = 0; r < 4; ++r) {
-                const float2 w2 = __half22float2(*reinterpret_cast<const __half2*>(&wf[r][hf][j]));
-                e[r] = fmaf(w2.x, h0, e[r]);
-                o[r] = fmaf(w2.y, h1, o[r]);
-              }
-            }
-          }
-          if (attempt > 0 || !__any_sync(0xffffffffu, bad)) break;
-          settle_words<16>(c, hrow, c.th + (size_t)(d.pair0 + i) * I,
-                           [lane](int q) { return 256 * (q >> 3) + 8 * lane + (q & 7); });
-          __syncwarp();
-        }
-        const float v = reduce4(e[0] + o[0], e[1] + o[1], e[2] + o[2], e[3] + o[3]);
-        if ((lane & 7) == 0)
-          st_tagged(c.ty + (size_t)(d.pair0 + i) * H + row, (c.pair_w[d.pair0 + i] * ts) * v, c.tag);
-      }
-    }
-  }
-}
-
 // ---- producer side (lane 0 of the producer warp) -----------------------------
 
 struct Prod {
@@ -641,16 +471,14 @@ struct Prod {
 };
 
 // The next ring slot (the caller has seen it free).
-template <bool NV>
 __device__ __forceinline__ int next_slot(Prod& p) {
-  return p.it++ % fz::Geo<NV>::NS;
+  return p.it++ % fz::Geo::NS;
 }
 
 // The END slot: armed by a plain arrive; waits out the drain bound for its
 // slot (the consumers release every slot they take, also after an abort).
-template <bool NV>
 __device__ __forceinline__ void post_end(Prod& p, uint64_t deadline) {
-  constexpr int NS = fz::Geo<NV>::NS;
+  constexpr int NS = fz::Geo::NS;
   const int slot = p.it % NS;
   if (p.it >= NS)
     mbar_wait(p.empty0 + 8u * slot, (uint32_t)((p.it / NS) - 1) & 1u, deadline + fz::DRAIN_NS);
@@ -661,58 +489,39 @@ __device__ __forceinline__ void post_end(Prod& p, uint64_t deadline) {
   mbar_arrive(p.full0 + 8u * slot);
 }
 
-// A gate/up unit (BF16: gate rows g and up rows u, 32 KiB each, in two slots;
-// NVFP4: gate codes g, up codes u, gate scales gs, up scales us in one slot).
-template <bool NV>
+// A gate/up unit: gate rows g and up rows u, 32 KiB each, in two slots.
 __device__ __forceinline__ void post_gateup(Prod& p, const uint8_t* g, const uint8_t* u,
-                                            const uint8_t* gs, const uint8_t* us, const Item& d) {
-  using Gm = fz::Geo<NV>;
-  const int sa = next_slot<NV>(p);
+                                            const Item& d) {
+  using Gm = fz::Geo;
+  const int sa = next_slot(p);
   p.desc[sa] = d;
   const uint32_t bar = p.full0 + 8u * sa, dst = p.stages_addr + sa * Gm::SLOT;
-  if constexpr (NV) {
-    mbar_expect_tx(bar, Gm::UNIT_BYTES);
-    bulk_g2s_stream(dst, g, 8 * Gm::QROW, bar);
-    bulk_g2s_stream(dst + 8 * Gm::QROW, u, 8 * Gm::QROW, bar);
-    bulk_g2s_stream(dst + 16 * Gm::QROW, gs, 8 * Gm::SFROW, bar);
-    bulk_g2s_stream(dst + 16 * Gm::QROW + 8 * Gm::SFROW, us, 8 * Gm::SFROW, bar);
-  } else {
-    mbar_expect_tx(bar, Gm::SLOT);
-    bulk_g2s_stream(dst, g, Gm::SLOT, bar);
-    const int sb = next_slot<NV>(p);
-    Item du = d;
-    du.kind = fz::IT_UP;
-    p.desc[sb] = du;
-    mbar_expect_tx(p.full0 + 8u * sb, Gm::SLOT);
-    bulk_g2s_stream(p.stages_addr + sb * Gm::SLOT, u, Gm::SLOT, p.full0 + 8u * sb);
-  }
+  mbar_expect_tx(bar, Gm::SLOT);
+  bulk_g2s_stream(dst, g, Gm::SLOT, bar);
+  const int sb = next_slot(p);
+  Item du = d;
+  du.kind = fz::IT_UP;
+  p.desc[sb] = du;
+  mbar_expect_tx(p.full0 + 8u * sb, Gm::SLOT);
+  bulk_g2s_stream(p.stages_addr + sb * Gm::SLOT, u, Gm::SLOT, p.full0 + 8u * sb);
 }
 
-// A down unit's Wd rows (BF16: 64 rows wq, 32 per slot; NVFP4: codes wq and
-// scales wsf in one slot), copied now, and the tx count of its h rows, which
-// post_down_h copies into the h ring once the group is complete.  Returns the
-// slot whose barrier the h rows complete.
-template <bool NV>
-__device__ __forceinline__ int post_down_w(Prod& p, const Item& d, const uint8_t* wq,
-                                           const uint8_t* wsf) {
-  using Gm = fz::Geo<NV>;
-  const int sa = next_slot<NV>(p);
+// A down unit's 64 Wd rows wq, 32 per slot, copied now, and the tx count of
+// its h rows, which post_down_h copies into the h ring once the group is
+// complete.  Returns the slot whose barrier the h rows complete.
+__device__ __forceinline__ int post_down_w(Prod& p, const Item& d, const uint8_t* wq) {
+  using Gm = fz::Geo;
+  const int sa = next_slot(p);
   p.desc[sa] = d;
   const uint32_t bar = p.full0 + 8u * sa, dst = p.stages_addr + sa * Gm::SLOT;
-  if constexpr (NV) {
-    mbar_expect_tx(bar, Gm::WBYTES + d.n * fz::THROW);
-    bulk_g2s_stream(dst, wq, Gm::WQ, bar);
-    bulk_g2s_stream(dst + Gm::WQ, wsf, Gm::WBYTES - Gm::WQ, bar);
-  } else {
-    mbar_expect_tx(bar, Gm::SLOT + d.n * fz::THROW);
-    bulk_g2s_stream(dst, wq, Gm::SLOT, bar);
-    const int sb = next_slot<NV>(p);
-    Item d2 = d;
-    d2.kind = fz::IT_DOWN2;
-    p.desc[sb] = d2;
-    mbar_expect_tx(p.full0 + 8u * sb, Gm::SLOT);
-    bulk_g2s_stream(p.stages_addr + sb * Gm::SLOT, wq + Gm::SLOT, Gm::SLOT, p.full0 + 8u * sb);
-  }
+  mbar_expect_tx(bar, Gm::SLOT + d.n * fz::THROW);
+  bulk_g2s_stream(dst, wq, Gm::SLOT, bar);
+  const int sb = next_slot(p);
+  Item d2 = d;
+  d2.kind = fz::IT_DOWN2;
+  p.desc[sb] = d2;
+  mbar_expect_tx(p.full0 + 8u * sb, Gm::SLOT);
+  bulk_g2s_stream(p.stages_addr + sb * Gm::SLOT, wq + Gm::SLOT, Gm::SLOT, p.full0 + 8u * sb);
   return sa;
 }
 
@@ -787,10 +596,10 @@ __device__ __forceinline__ void input_rmsnorm(uint4 (&v)[fz::MAXB], float (*s_no
 
 // PRENORM: the rows at a.x are pre-norm activations (input_rmsnorm); a
 // separate instance, so that the plain kernel's code stays as it is.
-template <bool NV, bool PRENORM>
+template <bool PRENORM>
 __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
-  using Gm = fz::Geo<NV>;
-  constexpr int ND = fz::ND<NV>;
+  using Gm = fz::Geo;
+  constexpr int ND = fz::ND;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ volatile int s_abort;
   __shared__ int s_ngroups;
@@ -870,7 +679,7 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     int u = (int)atomicAdd(claim, 1u);    // unit to post next
     int nxt = (int)atomicAdd(claim, 1u);  // claimed ahead
     bool meta = false, xs_free = false;
-    constexpr int UNITS = fz::UNITS<NV>;
+    constexpr int UNITS = fz::UNITS;
     int ng = 0, total_gu = UNITS, total = 0x7fffffff;
     // Down units: [0, kh) have their h rows posted, [kh, kw) wait for them;
     // [0, kf) are known released (their h rows free again: hf).  hw: h rows
@@ -949,16 +758,9 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
           const bool routed = d.expert < E;
           const size_t e = (size_t)(routed ? d.expert : d.expert - E);
           const size_t gr = (size_t)d.blk * Gm::GR, ur = (size_t)I + d.blk * Gm::GR;
-          if constexpr (NV) {
-            const uint8_t* qb = (routed ? a.w.w13_q : a.w.ws13_q) + e * (2 * I) * Gm::QROW;
-            const uint8_t* sb = (routed ? a.w.w13_sf : a.w.ws13_sf) + e * (2 * I) * Gm::SFROW;
-            post_gateup<true>(p, qb + gr * Gm::QROW, qb + ur * Gm::QROW, sb + gr * Gm::SFROW,
-                              sb + ur * Gm::SFROW, d);
-          } else {
-            const uint16_t* base = (routed ? a.w.w13 : a.w.ws13) + e * (2 * I) * H;
-            post_gateup<false>(p, reinterpret_cast<const uint8_t*>(base + gr * H),
-                               reinterpret_cast<const uint8_t*>(base + ur * H), nullptr, nullptr, d);
-          }
+          const uint16_t* base = (routed ? a.w.w13 : a.w.ws13) + e * (2 * I) * H;
+          post_gateup(p, reinterpret_cast<const uint8_t*>(base + gr * H),
+                      reinterpret_cast<const uint8_t*>(base + ur * H), d);
           posted = true;
         }
       } else if (u < total) {  // down unit: group k (the shared group first), row block rb
@@ -978,20 +780,14 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
           hw += grp.z;
           const bool routed = grp.x < E;
           const size_t row0 = (size_t)(routed ? grp.x : grp.x - E) * H + (size_t)rb * Gm::DR;
-          const uint8_t *wq, *wsf;
-          if constexpr (NV) {
-            wq = (routed ? a.w.w2_q : a.w.ws2_q) + row0 * Gm::DQROW;
-            wsf = (routed ? a.w.w2_sf : a.w.ws2_sf) + row0 * Gm::DSFROW;
-          } else {
-            wq = reinterpret_cast<const uint8_t*>((routed ? a.w.w2 : a.w.ws2) + row0 * I);
-            wsf = nullptr;
-          }
+          const uint8_t* wq =
+              reinterpret_cast<const uint8_t*>((routed ? a.w.w2 : a.w.ws2) + row0 * I);
           const int q = kw % fz::NQ;
           if (kw == 0) s_first_dn = p.it;  // from here on the consumers release xs
           s_pq[q] = d;
           s_pq_it[q] = p.it;
           s_pq_hend[q] = hw;
-          s_pq_slot[q] = post_down_w<NV>(p, d, wq, wsf);
+          s_pq_slot[q] = post_down_w(p, d, wq);
           ++kw;
           posted = true;
         }
@@ -1015,7 +811,7 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     for (; kh < kw; ++kh)
       post_down_h(p, s_pq[kh % fz::NQ], th + (size_t)s_pq[kh % fz::NQ].pair0 * I, hring,
                   s_pq_slot[kh % fz::NQ]);
-    post_end<NV>(p, deadline);
+    post_end(p, deadline);
     return;
   }
 
@@ -1033,8 +829,8 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     while (have != want && !__any_sync(0xffffffffu, s_abort)) {
       const uint32_t c_lo = w_lo && !d_lo ? ld_relaxed_u32(&done[lane].v) : 0u;
       const uint32_t c_hi = w_hi && !d_hi ? ld_relaxed_u32(&done[lane + 32].v) : 0u;
-      d_lo = d_lo || (w_lo && c_lo >= (uint32_t)fz::UNITS<NV>);
-      d_hi = d_hi || (w_hi && c_hi >= (uint32_t)fz::UNITS<NV>);
+      d_lo = d_lo || (w_lo && c_lo >= (uint32_t)fz::UNITS);
+      d_hi = d_hi || (w_hi && c_hi >= (uint32_t)fz::UNITS);
       const uint64_t m = (uint64_t)__ballot_sync(0xffffffffu, d_lo) |
                          ((uint64_t)__ballot_sync(0xffffffffu, d_hi) << 32);
       if (m != have) {
@@ -1109,20 +905,6 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
   }
   router_slice(B, a.ws.tlogits, reinterpret_cast<const uint16_t*>(buf), xs, e_begin,
                e_end, s_part, tag);
-  if constexpr (NV) {
-    // The NVFP4 gate/up MMAs take the activations as f16 (exact for bf16
-    // values inside f16's range; larger ones are reported, not clamped).
-    bool big = false;
-#pragma unroll
-    for (int t = 0; t < fz::MAXB; ++t) {
-      if (t < B) {
-        uint4* v = reinterpret_cast<uint4*>(xs) + t * (H / 8) + tid;
-        big |= nvu::bf16x8_beyond_f16(*v);
-        *v = nvu::bf16x8_to_f16x8(*v);
-      }
-    }
-    if (big) set_error(hdr, DEV_BAD_INPUT);
-  }
   // 2. every CTA ranks and buckets the batch once all logits are in
   if (tid == 0) {
     red_add_relaxed(&sync[SYNC_ARRIVE].v, 1u);
@@ -1226,49 +1008,35 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
     const bool ok = !s_abort;
     if (d.kind == fz::IT_END) break;
     const uint8_t* st = ring + slot * Gm::SLOT;
-    const bool routed = d.expert < E;
-    if constexpr (NV) {  // every NVFP4 unit takes one slot
-      if (d.kind == fz::IT_DOWN) {
-        down_nv(dc, st, hb, d, __ldg(routed ? a.w.w2_ts + d.expert : a.w.ws2_ts + (d.expert - E)), ok);
-        release_slot(empty0 + 8u * slot);
+    // every unit takes two slots
+    const int slot2 = (it + 1) % Gm::NS;
+    if (!wait_it(it + 1)) break;
+    const int k2 = s_desc[slot2].kind;
+    if (k2 != (d.kind == fz::IT_DOWN ? fz::IT_DOWN2 : fz::IT_UP)) break;  // producer gave up (abort)
+    const uint8_t* st2 = ring + slot2 * Gm::SLOT;
+    const bool ok2 = !s_abort;
+    if (d.kind == fz::IT_DOWN) {
+      down_cc(dc, st, st2, hb, d, ok2);
+      release_slot(empty0 + 8u * slot);
+      release_slot(empty0 + 8u * slot2);
+    } else {
+      if (d.n <= gu::CC_MAX) {
+        int tok[2];
+        tok[0] = d.tok0 >= 0 ? d.tok0 : s_pair_tok[d.pair0];
+        tok[1] = d.n > 1 ? (d.tok0 >= 0 ? d.tok0 + 1 : s_pair_tok[d.pair0 + 1]) : tok[0];
+        if (d.n == 1)
+          unit_cc<1>(st, st2, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
+                     empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
+        else
+          unit_cc<2>(st, st2, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
+                     empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
       } else {
-        const float* ts13 = routed ? a.w.w13_ts + 2 * d.expert : a.w.ws13_ts + 2 * (d.expert - E);
-        unit_nv(st, xs, s_pair_tok, buf, a.ws.th, d, __ldg(ts13), __ldg(ts13 + 1), ok,
-                empty0 + 8u * slot, tag, done, &s_ucnt[useq]);
-        useq = (useq + 1) & (fz::UCNT - 1);
+        unit_mma(st, st2, xs, s_pair_tok, buf, a.ws.th, d, ok2, empty0 + 8u * slot,
+                 empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
       }
-      ++it;
-      continue;
-    } else {  // every BF16 unit takes two slots
-      const int slot2 = (it + 1) % Gm::NS;
-      if (!wait_it(it + 1)) break;
-      const int k2 = s_desc[slot2].kind;
-      if (k2 != (d.kind == fz::IT_DOWN ? fz::IT_DOWN2 : fz::IT_UP)) break;  // producer gave up (abort)
-      const uint8_t* st2 = ring + slot2 * Gm::SLOT;
-      const bool ok2 = !s_abort;
-      if (d.kind == fz::IT_DOWN) {
-        down_cc(dc, st, st2, hb, d, ok2);
-        release_slot(empty0 + 8u * slot);
-        release_slot(empty0 + 8u * slot2);
-      } else {
-        if (d.n <= gu::CC_MAX) {
-          int tok[2];
-          tok[0] = d.tok0 >= 0 ? d.tok0 : s_pair_tok[d.pair0];
-          tok[1] = d.n > 1 ? (d.tok0 >= 0 ? d.tok0 + 1 : s_pair_tok[d.pair0 + 1]) : tok[0];
-          if (d.n == 1)
-            unit_cc<1>(st, st2, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
-                       empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
-          else
-            unit_cc<2>(st, st2, reinterpret_cast<const uint4*>(xs), tok, a.ws.th, d, ok2,
-                       empty0 + 8u * slot, empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
-        } else {
-          unit_mma(st, st2, xs, s_pair_tok, buf, a.ws.th, d, ok2, empty0 + 8u * slot,
-                   empty0 + 8u * slot2, tag, done, &s_ucnt[useq]);
-        }
-        useq = (useq + 1) & (fz::UCNT - 1);
-      }
-      it += 2;
+      useq = (useq + 1) & (fz::UCNT - 1);
     }
+    it += 2;
     (void)ok;
   }
   named_sync(1, fz::CT);
@@ -1323,26 +1091,23 @@ __device__ __forceinline__ void moe_small_body(ExpertArgs a, RouterArgs r) {
 }
 
 __global__ void __launch_bounds__(fz::THREADS, 1) moe_small_bf16_kernel(ExpertArgs a, RouterArgs r) {
-  moe_small_body<false, false>(a, r);
+  moe_small_body<false>(a, r);
 }
 __global__ void __launch_bounds__(fz::THREADS, 1)
     moe_small_bf16_prenorm_kernel(ExpertArgs a, RouterArgs r) {
-  moe_small_body<false, true>(a, r);
-}
-__global__ void __launch_bounds__(fz::THREADS, 1) moe_small_nvfp4_kernel(ExpertArgs a, RouterArgs r) {
-  moe_small_body<true, false>(a, r);
+  moe_small_body<true>(a, r);
 }
 
 bool small_supported(int num_sms) { return num_sms >= 86 && num_sms <= 1024; }
 
 namespace {
-template <bool NV, bool PRENORM>
+template <bool PRENORM>
 cudaError_t launch_small(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                          int num_sms) {
   static std::atomic<uint64_t> smem_set{0};
-  constexpr size_t smem = fz::smem_bytes<NV>();
+  constexpr size_t smem = fz::smem_bytes();
   void (*const kernel)(ExpertArgs, RouterArgs) =
-      NV ? moe_small_nvfp4_kernel : PRENORM ? moe_small_bf16_prenorm_kernel : moe_small_bf16_kernel;
+      PRENORM ? moe_small_bf16_prenorm_kernel : moe_small_bf16_kernel;
   const cudaError_t es = set_smem_limit_once(kernel, (int)smem, smem_set);
   if (es != cudaSuccess) return es;
   cudaLaunchConfig_t cfg = {};
@@ -1367,12 +1132,8 @@ cudaError_t launch_small(const ExpertArgs& a, const RouterArgs& r, cudaStream_t 
 
 cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                               int num_sms) {
-  return a.prenorm ? launch_small<false, true>(a, r, stream, num_sms)
-                   : launch_small<false, false>(a, r, stream, num_sms);
-}
-cudaError_t launch_small_nvfp4(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
-                               int num_sms) {
-  return launch_small<true, false>(a, r, stream, num_sms);
+  return a.prenorm ? launch_small<true>(a, r, stream, num_sms)
+                   : launch_small<false>(a, r, stream, num_sms);
 }
 
 }  // namespace flint

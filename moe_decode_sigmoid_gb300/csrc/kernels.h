@@ -63,10 +63,6 @@ struct ExpertArgs {
 
 // Largest batch whose routing the expert kernels compute themselves.
 constexpr int LOCAL_SELECT_MAX_B = SMALL_B;
-// Largest NVFP4 batch that takes the persistent kernel (measured crossover
-// with the chained kernels on GB300: at 2 tokens 29.4 us against 31.1 us, at 3
-// tokens 36.0 us against 32.5 us).
-constexpr int NVFP4_FUSED_MAX_B = 2;
 // Largest batch whose input RMSNorm the persistent kernel takes itself (the
 // prenorm call); above it the standalone RMSNorm kernel runs first.  Measured
 // per layer in the 47-layer stack on GB300, folded against RMSNorm kernel +
@@ -78,13 +74,11 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_bucket(const Ws& ws, int B, const BucketOut& user, cudaStream_t stream);
 cudaError_t launch_gateup_bf16(const ExpertArgs& a, cudaStream_t stream, int num_sms);
 cudaError_t launch_down_bf16(const ExpertArgs& a, cudaStream_t stream);
-// The whole layer in one persistent cooperative kernel (batch <= 8), for
-// grids of num_sms CTAs where small_supported(num_sms): BF16 or NVFP4 weights.
+// The whole BF16 layer in one persistent cooperative kernel (batch <= 8), for
+// grids of num_sms CTAs where small_supported(num_sms).
 bool small_supported(int num_sms);
 cudaError_t launch_small_bf16(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
                               int num_sms);
-cudaError_t launch_small_nvfp4(const ExpertArgs& a, const RouterArgs& r, cudaStream_t stream,
-                               int num_sms);
 cudaError_t launch_gateup_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
 cudaError_t launch_down_nvfp4(const ExpertArgs& a, cudaStream_t stream, int num_sms);
 // out = residual + each token's SLOTS rows of y (after launch_down_nvfp4).
