@@ -8,8 +8,12 @@
 // for Recursive's Flint, "Optimization Strategies").
 //
 // Work unit: one group x one block of 8 intermediate rows = the 8 gate rows
-// plus the 8 matching up rows: two contiguous 32 KiB runs of w13.  Each CTA
-// (one per SM) takes an equal share of the units.
+// plus the 8 matching up rows: two contiguous 32 KiB runs of w13.  The units
+// that need the routing are claimed from a workspace counter by the CTAs (one
+// per SM) as they go -- guided self-scheduling: chunks of about remaining /
+// (2 x #SMs) units, at most 8, down to single units at the end -- because SMs
+// stream at different rates: with an equal static share the last CTA ended
+// ~10 us after the median one at batch 128 (skewed routing), 5.5 us at 32.
 //
 // Per CTA: 8 consumer warps + 1 producer warp.  The producer's elected lane
 // streams each unit as one 64 KiB stage -- two cp.async.bulk copies -- through
@@ -37,10 +41,37 @@
 namespace flint {
 using namespace gu_impl;
 
+namespace {
+constexpr int CLAIM_MAX = 8;  // units per claim at most
+
+// Waits (bounded) until ring stage `it` is free again; false on a failed wait
+// or an abort.
+__device__ __forceinline__ bool stage_free(const GuCtx& c, int it) {
+  bool got = true;
+  if (it >= gu::NSTAGE)
+    got = mbar_wait(empty_bar(c, it % gu::NSTAGE), (uint32_t)((it / gu::NSTAGE) - 1) & 1u,
+                    c.deadline);
+  if (!got || *c.abort_flag) {
+    *c.abort_flag = 1;
+    if (!got) set_error(c.hdr, DEV_TIMEOUT);
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ int claim_size(int remaining) {
+  const int s = remaining / (2 * (int)gridDim.x);
+  return s < 1 ? 1 : (s > CLAIM_MAX ? CLAIM_MAX : s);
+}
+}  // namespace
+
 __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
   __shared__ LocalSelectSmem s_sel;
+  // the claimed chunk {first unit, units} that starts at ring stage s (or
+  // {-1, 0}: no more), written before the stage's copies are issued
+  __shared__ int2 s_chunk[gu::NSTAGE];
   GuCtx c;
   c.stages = smem;
   c.buf = reinterpret_cast<float*>(smem + gu::NSTAGE * gu::STAGE_BYTES);
@@ -78,18 +109,48 @@ __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs 
     __syncwarp();
     named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
     if (lane == 0) {
-      plan_post(pl, meta.n_groups, early);
+      // Units [0, n) of the groups after the shared ones handled above (all
+      // groups when none were); one claim is kept in flight ahead.
+      const int n = (meta.n_groups - (early ? S * pl.nsg : 0)) * gu::UNITS;
+      uint32_t* const claim = &a.ws.hdr->gu_claim;
+      int sz = claim_size(n);
+      int c0 = (int)atomicAdd(claim, (uint32_t)sz);
+      int sz_next = claim_size(n - c0 - sz);
+      int c_next = (int)atomicAdd(claim, (uint32_t)sz_next);
       int gi_cached = -1;
       const uint16_t* base = nullptr;
-      for (int u = pl.r_begin; ok && u < pl.r_end; ++u) {
-        const int gi = u / gu::UNITS;
-        if (gi != gi_cached) {
-          const int4 grp = meta.groups[gi];
-          base = grp.x < E ? a.w.w13 + (size_t)grp.x * (2 * I) * H
-                           : a.w.ws13 + (size_t)(grp.x - E) * (2 * I) * H;
-          gi_cached = gi;
+      while (ok && c0 < n) {
+        const int e = min(n, c0 + sz);
+        ok = stage_free(c, it);
+        if (!ok) break;
+        s_chunk[it % gu::NSTAGE] = make_int2(c0, e - c0);
+        for (int u = c0; ok && u < e; ++u) {
+          const int gi = u / gu::UNITS;
+          if (gi != gi_cached) {
+            const int4 grp = meta.groups[gi];
+            base = grp.x < E ? a.w.w13 + (size_t)grp.x * (2 * I) * H
+                             : a.w.ws13 + (size_t)(grp.x - E) * (2 * I) * H;
+            gi_cached = gi;
+          }
+          ok = issue_unit(c, base, u & (gu::UNITS - 1), it);
         }
-        ok = issue_unit(c, base, u & (gu::UNITS - 1), it);
+        c0 = c_next;
+        sz = sz_next;
+        if (c0 < n) {
+          sz_next = claim_size(n - c0 - sz);
+          c_next = (int)atomicAdd(claim, (uint32_t)sz_next);
+        }
+      }
+      if (ok && stage_free(c, it)) {  // no more: the consumers stop at this stage
+        s_chunk[it % gu::NSTAGE] = make_int2(-1, 0);
+        mbar_arrive(full_bar(c, it % gu::NSTAGE));
+        ++it;
+      }
+      // The last CTA done claiming resets the counter for the next call.
+      __threadfence();
+      if (atomicAdd(&a.ws.hdr->gu_done, 1u) == gridDim.x - 1) {
+        atomicExch(claim, 0u);
+        atomicExch(&a.ws.hdr->gu_done, 0u);
       }
       drain(c, it);
     }
@@ -107,14 +168,21 @@ __global__ void __launch_bounds__(gu::THREADS, 1) gateup_bf16_kernel(ExpertArgs 
   fill_meta(a, a.local_select != 0, meta, nullptr, c.buf, &s_sel);
   pdl_trigger();  // the down kernel may start its prologue
   named_sync(2, ALL_THREADS);
-  plan_post(pl, meta.n_groups, early);
-  int u = pl.r_begin;
-  while (u < pl.r_end) {
-    const int gi = u / gu::UNITS;
-    const int4 grp = meta.groups[gi];
-    const int u1 = min(pl.r_end, (gi + 1) * gu::UNITS);
-    segment(c, u, u1, grp.y, grp.z, -1, it, ok);
-    u = u1;
+  // the producer's chunks, in its order
+  while (ok) {
+    const int slot = it % gu::NSTAGE;
+    if (!wait_full(c, slot, (uint32_t)(it / gu::NSTAGE) & 1u)) break;
+    const int2 ch = s_chunk[slot];
+    if (ch.x < 0) break;
+    int u = ch.x;
+    const int u1 = ch.x + ch.y;
+    while (ok && u < u1) {
+      const int gi = u / gu::UNITS;
+      const int4 grp = meta.groups[gi];
+      const int ue = min(u1, (gi + 1) * gu::UNITS);
+      segment(c, u, ue, grp.y, grp.z, -1, it, ok);
+      u = ue;
+    }
   }
 }
 

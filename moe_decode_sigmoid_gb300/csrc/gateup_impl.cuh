@@ -247,45 +247,20 @@ __device__ __forceinline__ void drain(const GuCtx& c, int it) {
     mbar_wait(full_bar(c, j % gu::NSTAGE), (uint32_t)(j / gu::NSTAGE) & 1u, drain);
 }
 
-// Which units a CTA runs.  Shared-expert groups do not depend on routing; in
-// the decode chain ("early") they are dealt round-robin over the CTAs and
-// started before the wait for the router, and the routed units are then split
-// so that every CTA ends up with the same total.  Otherwise every group,
-// shared ones included, is split evenly after the wait.
+// The shared-expert groups do not depend on routing: in the decode chain
+// ("early") their units are dealt round-robin over the CTAs and started
+// before the wait for the router.  Every other unit is claimed after the wait
+// (gateup.cu).
 struct Plan {
   int nsg;        // shared groups per shared expert
   int nsu;        // shared units handled before the wait (early only)
-  int r_begin, r_end;
 };
-
-__device__ __forceinline__ int shared_units_below(int c, int nsu, int G) {
-  return c * (nsu / G) + min(c, nsu % G);
-}
 
 __device__ __forceinline__ Plan plan_pre(int B, bool early) {
   Plan p;
   p.nsg = (B + GROUP_MAX - 1) / GROUP_MAX;
   p.nsu = early ? S * p.nsg * gu::UNITS : 0;
-  p.r_begin = p.r_end = 0;
   return p;
-}
-
-__device__ __forceinline__ void plan_post(Plan& p, int n_groups, bool early) {
-  const int G = gridDim.x, c = blockIdx.x;
-  if (!early) {
-    const int n = n_groups * gu::UNITS;
-    p.r_begin = (int)((long long)c * n / G);
-    p.r_end = (int)((long long)(c + 1) * n / G);
-    return;
-  }
-  const int nru = (n_groups - S * p.nsg) * gu::UNITS;
-  const long long T = (long long)p.nsu + nru;
-  auto R = [&](int cc) {
-    long long r = cc * T / G - shared_units_below(cc, p.nsu, G);
-    return (int)(r < 0 ? 0 : (r > nru ? nru : r));
-  };
-  p.r_begin = R(c);
-  p.r_end = max(p.r_begin, R(c + 1));
 }
 
 // Shared unit j -> (shared expert, group, block) and its pairs / tokens.
