@@ -69,9 +69,11 @@ struct WsHeader {
   uint32_t n_uniq;           // distinct routed experts
   uint32_t stall_armed;      // test hook: one-shot wait on stall_release
   uint32_t stall_release;    // never written by the library
-  uint32_t gu_claim;         // large-batch gate/up: next unit to claim (reset by its last CTA)
-  uint32_t gu_done;          // large-batch gate/up: CTAs done claiming
-  uint32_t pad0[21];
+  uint32_t gu_claim;         // chained gate/up kernels: next unit to claim (reset by the last CTA)
+  uint32_t gu_done;          // chained gate/up kernels: CTAs done claiming
+  uint32_t dn_claim;         // NVFP4 down kernel: next unit to claim (reset by the last CTA)
+  uint32_t dn_done;          // NVFP4 down kernel: CTAs done claiming
+  uint32_t pad0[19];
   uint32_t tile_ctas_done[MAX_B / 8];  // router: finished CTAs per token tile
   uint32_t pad2[16];
   uint32_t pad1[176];

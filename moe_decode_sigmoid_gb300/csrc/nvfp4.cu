@@ -110,6 +110,83 @@ __device__ __forceinline__ void drain(const Pipe& p, int it) {
     mbar_wait(full_bar(p, j % p.nstage), (uint32_t)(j / p.nstage) & 1u, dl);
 }
 
+// Units [0, n) over the CTAs.  With fewer than min_per_cta units per CTA
+// (small batches), CTA c takes the c-th of equal contiguous shares: each CTA's
+// consumers then work through long runs of one group in full reduction rounds.
+// Otherwise each CTA first takes a static chunk of min(8, n / (2 x #SMs))
+// units and then claims the rest as it goes -- guided self-scheduling, as in
+// the BF16 gate/up kernel (SMs stream at different rates, so equal static
+// shares leave a tail): chunks of about remaining / (2 x #SMs) units (1..8)
+// from *claim, the first claim sent while the static chunk streams and the
+// next one claimed ahead while plenty remains.  Each chunk {first unit, units}
+// is published on its first stage in s_chunk, and a stage marked {-1, 0} ends
+// the list; the last CTA done claiming resets the counters for the next call.
+// Measured on GB300 (NVFP4 layer, chained): claimed gate/up units take skewed
+// batch 128 from 183 to 165 us and claimed down units to 168 us (both: 150),
+// but cost 3-7 us at 1-8 tokens, hence the per-kernel minimum.
+__device__ __forceinline__ bool claims_used(int n, int min_per_cta) {
+  return n >= min_per_cta * (int)gridDim.x;
+}
+__device__ __forceinline__ int static_begin(int n, int c) {
+  return (int)((long long)c * n / gridDim.x);
+}
+constexpr int GU_CLAIM_MIN = 32, DN_CLAIM_MIN = 8;  // units per CTA
+
+template <class Issue>
+__device__ __forceinline__ void produce_claimed(const Pipe& p, int n, int min_per_cta,
+                                                uint32_t* claim, uint32_t* done, int2* s_chunk,
+                                                Issue issue) {
+  const int G = (int)gridDim.x, cta = (int)blockIdx.x;
+  int it = 0;
+  bool ok = true;
+  auto run = [&](int c0, int e, bool publish) {  // issue units [c0, e)
+    for (int u = c0; ok && u < e; ++u) {
+      if (!acquire_stage(p, it)) {
+        ok = false;
+        break;
+      }
+      if (publish && u == c0) s_chunk[it % p.nstage] = make_int2(c0, e - c0);
+      issue(u, it % p.nstage);
+      ++it;
+    }
+  };
+  if (!claims_used(n, min_per_cta)) {
+    run(static_begin(n, cta), static_begin(n, cta + 1), false);
+    drain(p, it);
+    return;
+  }
+  auto size_for = [G](int rem) {
+    const int s = rem / (2 * G);
+    return s < 1 ? 1 : (s > 8 ? 8 : s);
+  };
+  const int f = min(8, n / (2 * G));
+  const int base = G * f;  // claimed units start here
+  int sz = size_for(n - base);
+  int c0 = base + (int)atomicAdd(claim, (uint32_t)sz);
+  run(cta * f, cta * f + f, true);
+  while (ok && c0 < n) {
+    const int e = min(n, c0 + sz);
+    const int sz_next = size_for(n - e);
+    const bool ahead = n - e > 2 * G;
+    int c_next = ahead ? base + (int)atomicAdd(claim, (uint32_t)sz_next) : 0;
+    run(c0, e, true);
+    if (!ahead) c_next = base + (int)atomicAdd(claim, (uint32_t)sz_next);
+    c0 = c_next;
+    sz = sz_next;
+  }
+  __threadfence();
+  if (atomicAdd(done, 1u) == (uint32_t)G - 1u) {
+    atomicExch(claim, 0u);
+    atomicExch(done, 0u);
+  }
+  if (ok && acquire_stage(p, it)) {  // no more: the consumers stop at this stage
+    s_chunk[it % p.nstage] = make_int2(-1, 0);
+    mbar_arrive(full_bar(p, it % p.nstage));
+    ++it;
+  }
+  drain(p, it);
+}
+
 __device__ __forceinline__ void init_pipe(Pipe& p, uint8_t* smem, int stage_bytes, int nstage,
                                           uint64_t* bars, int max_stages, volatile int* abort_flag,
                                           WsHeader* hdr) {
@@ -299,9 +376,9 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
 }
 
 __device__ __forceinline__ void gu_produce(const Pipe& p, const GuMaps& maps, const int4* groups,
-                                           int u_begin, int u_end) {
-  int it = 0;
-  for (int u = u_begin; u < u_end; ++u) {
+                                           int n, uint32_t* claim, uint32_t* done,
+                                           int2* s_chunk) {
+  produce_claimed(p, n, GU_CLAIM_MIN, claim, done, s_chunk, [&](int u, int slot) {
     const int4 grp = groups[u / f4::UNITS];
     const int blk = u & (f4::UNITS - 1);
     const bool routed = grp.x < E;
@@ -309,17 +386,13 @@ __device__ __forceinline__ void gu_produce(const Pipe& p, const GuMaps& maps, co
     const CUtensorMap* mq = routed ? &maps.q : &maps.sq;
     const CUtensorMap* ms = routed ? &maps.sf : &maps.ssf;
     const int gate_row = e * (2 * I) + blk * 8, up_row = gate_row + I;
-    if (!acquire_stage(p, it)) break;
-    const int slot = it % p.nstage;
     mbar_expect_tx(full_bar(p, slot), f4::GU_STAGE);
     const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
     tma_3d(dst, mq, gate_row, full_bar(p, slot));
     tma_3d(dst + f4::GU_UPQ, mq, up_row, full_bar(p, slot));
     tma_2d(dst + f4::GU_SF, ms, gate_row, full_bar(p, slot));
     tma_2d(dst + f4::GU_UPSF, ms, up_row, full_bar(p, slot));
-    ++it;
-  }
-  drain(p, it);
+  });
 }
 
 }  // namespace
@@ -331,6 +404,7 @@ __global__ void __launch_bounds__(f4::THREADS, 1)
   uint8_t* smem = smem_raw + (((raw_addr + f4::GU_ALIGN - 1) & ~uint32_t(f4::GU_ALIGN - 1)) - raw_addr);
   __shared__ int s_abort;
   __shared__ LocalSelectSmem s_sel;
+  __shared__ int2 s_chunk[f4::GU_NSTAGE];  // claimed chunk starting at each stage
   float* red = reinterpret_cast<float*>(smem + f4::GU_NSTAGE * f4::GU_STAGE);
   MetaSmem& meta = *reinterpret_cast<MetaSmem*>(reinterpret_cast<uint8_t*>(red) + f4::GU_BUF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(&meta) + sizeof(MetaSmem));
@@ -341,32 +415,41 @@ __global__ void __launch_bounds__(f4::THREADS, 1)
   pdl_wait();     // the router's logits / routing
   if ((threadIdx.x >> 5) == f4::CWARPS) {
     named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
-    if ((threadIdx.x & 31) == 0) {
-      const int n_units = meta.n_groups * f4::UNITS;
-      gu_produce(p, maps, meta.groups, (int)((long long)blockIdx.x * n_units / gridDim.x),
-                 (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x));
-    }
+    if ((threadIdx.x & 31) == 0)
+      gu_produce(p, maps, meta.groups, meta.n_groups * f4::UNITS, &a.ws.hdr->gu_claim,
+                 &a.ws.hdr->gu_done, s_chunk);
     return;
   }
   fill_meta(a, a.local_select != 0, meta, nullptr, red, &s_sel);
   pdl_trigger();
   named_sync(2, ALL_THREADS);
-  const int n_units = meta.n_groups * f4::UNITS;
-  const int u_begin = (int)((long long)blockIdx.x * n_units / gridDim.x);
-  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
   int it = 0;
   bool ok = true;
-  int u = u_begin;
-  while (u < u_end) {
-    const int gi = u / f4::UNITS;
-    const int4 grp = meta.groups[gi];
-    const int u1 = min(u_end, (gi + 1) * f4::UNITS);
-    switch ((grp.z + 7) >> 3) {
-      case 1: gu_segment<1>(p, a, meta.pair_tok, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
-      case 2: gu_segment<2>(p, a, meta.pair_tok, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
-      default: gu_segment<3>(p, a, meta.pair_tok, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+  const int n_units = meta.n_groups * f4::UNITS;
+  const bool claimed = claims_used(n_units, GU_CLAIM_MIN);
+  int2 ch = make_int2(static_begin(n_units, blockIdx.x),
+                      static_begin(n_units, blockIdx.x + 1) - static_begin(n_units, blockIdx.x));
+  while (ok) {  // the CTA's share, or the producer's chunks in its order
+    if (claimed) {
+      const int slot = it % p.nstage;
+      if (!wait_full(p, slot, (uint32_t)(it / p.nstage) & 1u)) break;
+      ch = s_chunk[slot];
+      if (ch.x < 0) break;
     }
-    u = u1;
+    int u = ch.x;
+    const int u_end = ch.x + ch.y;
+    while (ok && u < u_end) {
+      const int gi = u / f4::UNITS;
+      const int4 grp = meta.groups[gi];
+      const int u1 = min(u_end, (gi + 1) * f4::UNITS);
+      switch ((grp.z + 7) >> 3) {
+        case 1: gu_segment<1>(p, a, meta.pair_tok, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+        case 2: gu_segment<2>(p, a, meta.pair_tok, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+        default: gu_segment<3>(p, a, meta.pair_tok, red, u, u1, grp.x, grp.y, grp.z, it, ok); break;
+      }
+      u = u1;
+    }
+    if (!claimed) break;
   }
 }
 
@@ -534,9 +617,9 @@ __device__ __forceinline__ void dn_unit(const ExpertArgs& a, const uint8_t* st, 
 }
 
 __device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, const int4* groups,
-                                           int u_begin, int u_end) {
-  int it = 0;
-  for (int u = u_begin; u < u_end; ++u) {
+                                           int n, int2* s_chunk) {
+  produce_claimed(p, n, DN_CLAIM_MIN, &a.ws.hdr->dn_claim, &a.ws.hdr->dn_done, s_chunk,
+                  [&](int u, int slot) {
     const int4 grp = groups[u / f4::DN_UNITS];
     const int rb = u % f4::DN_UNITS;
     const bool routed = grp.x < E;
@@ -544,8 +627,6 @@ __device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, c
     const size_t row0 = (size_t)e * H + (size_t)rb * f4::DN_RB;
     const uint8_t* qb = (routed ? a.w.w2_q : a.w.ws2_q) + row0 * f4::DN_QROW;
     const uint8_t* sb = (routed ? a.w.w2_sf : a.w.ws2_sf) + row0 * f4::DN_SFROW;
-    if (!acquire_stage(p, it)) break;
-    const int slot = it % p.nstage;
     mbar_expect_tx(full_bar(p, slot), f4::DN_QB + f4::DN_SB + grp.z * f4::DN_HROW);
     const uint32_t dst = p.stages_addr + slot * p.stage_bytes;
     bulk_g2s_stream(dst, qb, f4::DN_QB, full_bar(p, slot));
@@ -553,9 +634,7 @@ __device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, c
     bulk_g2s(dst + f4::DN_QB + f4::DN_SB,
              reinterpret_cast<const uint8_t*>(a.ws.h) + (size_t)grp.y * f4::DN_HROW,
              grp.z * f4::DN_HROW, full_bar(p, slot));
-    ++it;
-  }
-  drain(p, it);
+  });
 }
 
 }  // namespace
@@ -563,6 +642,7 @@ __device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, c
 __global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_abort;
+  __shared__ int2 s_chunk[f4::DN_MAX_STAGES];  // claimed chunk starting at each stage
   const int B = a.B;
   const int nstage = f4::dn_nstages(B), stage = f4::dn_stage(B);
   MetaSmem& meta = *reinterpret_cast<MetaSmem*>(smem + nstage * stage);
@@ -575,38 +655,43 @@ __global__ void __launch_bounds__(f4::THREADS, 1) down_nvfp4_kernel(ExpertArgs a
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == f4::CWARPS) {
     named_sync(2, ALL_THREADS);  // routing metadata is in shared memory
-    if (lane == 0) {
-      const int n_units = meta.n_groups * f4::DN_UNITS;
-      dn_produce(p, a, meta.groups, (int)((long long)blockIdx.x * n_units / gridDim.x),
-                 (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x));
-    }
+    if (lane == 0) dn_produce(p, a, meta.groups, meta.n_groups * f4::DN_UNITS, s_chunk);
     return;
   }
   fill_meta(a, false, meta, nullptr, nullptr, nullptr);
   pdl_trigger();
   named_sync(2, ALL_THREADS);
   float* y = ws_y(a.ws, B);
-  const int n_units = meta.n_groups * f4::DN_UNITS;
-  const int u_begin = (int)((long long)blockIdx.x * n_units / gridDim.x);
-  const int u_end = (int)((long long)(blockIdx.x + 1) * n_units / gridDim.x);
   bool ok = true;
   int it = 0;
-  for (int u = u_begin; u < u_end; ++u, ++it) {
-    const int4 grp = meta.groups[u / f4::DN_UNITS];
-    const int rb = u % f4::DN_UNITS;
-    const int slot = it % p.nstage;
-    if (ok) ok = wait_full(p, slot, (uint32_t)(it / p.nstage) & 1u);
-    if (ok) {
-      const uint8_t* st = p.stages + slot * p.stage_bytes;
-      switch ((grp.z + 7) >> 3) {
-        case 1: dn_unit<1>(a, st, grp.x, grp.y, grp.z, rb, y); break;
-        case 2: dn_unit<2>(a, st, grp.x, grp.y, grp.z, rb, y); break;
-        default: dn_unit<3>(a, st, grp.x, grp.y, grp.z, rb, y); break;
-      }
+  const int n_units = meta.n_groups * f4::DN_UNITS;
+  const bool claimed = claims_used(n_units, DN_CLAIM_MIN);
+  int2 ch = make_int2(static_begin(n_units, blockIdx.x),
+                      static_begin(n_units, blockIdx.x + 1) - static_begin(n_units, blockIdx.x));
+  while (ok) {  // the CTA's share, or the producer's chunks in its order
+    if (claimed) {
+      if (!wait_full(p, it % p.nstage, (uint32_t)(it / p.nstage) & 1u)) break;
+      ch = s_chunk[it % p.nstage];
+      if (ch.x < 0) break;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar(p, slot));
-    if (!ok) break;  // a failed wait set the abort flag: the producer stops too
+    for (int u = ch.x; u < ch.x + ch.y; ++u, ++it) {
+      const int4 grp = meta.groups[u / f4::DN_UNITS];
+      const int rb = u % f4::DN_UNITS;
+      const int slot = it % p.nstage;
+      if (ok) ok = wait_full(p, slot, (uint32_t)(it / p.nstage) & 1u);
+      if (ok) {
+        const uint8_t* st = p.stages + slot * p.stage_bytes;
+        switch ((grp.z + 7) >> 3) {
+          case 1: dn_unit<1>(a, st, grp.x, grp.y, grp.z, rb, y); break;
+          case 2: dn_unit<2>(a, st, grp.x, grp.y, grp.z, rb, y); break;
+          default: dn_unit<3>(a, st, grp.x, grp.y, grp.z, rb, y); break;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(p, slot));
+      if (!ok) break;  // a failed wait set the abort flag: the producer stops too
+    }
+    if (!claimed) break;
   }
 }
 
