@@ -348,19 +348,24 @@ def stage_times(m, L, steps, warmup, stream):
 
 def e2e_measure(m, L, steps, warmup, stream):
     """Same layer through the public call with host buffers: pinned H2D of x and
-    residual, the decode call, D2H of out -- all inside the events."""
-    xh = L.x.cpu().pin_memory()
-    rh = L.res.cpu().pin_memory()
+    residual (kept next to each other, so one copy brings both), the decode
+    call, D2H of out -- all inside the events."""
+    x0, r0 = L.x, L.res
+    xr = torch.stack([x0, r0])          # [2, B, H]: x, then the residual
+    L.x, L.res = xr[0], xr[1]           # contiguous views the call reads
+    xrh = xr.cpu().pin_memory()
     oh = torch.empty_like(L.out, device="cpu").pin_memory()
 
     def step(i):
-        L.x.copy_(xh, non_blocking=True)
-        L.res.copy_(rh, non_blocking=True)
+        xr.copy_(xrh, non_blocking=True)
         L.call(i, stream)
         oh.copy_(L.out, non_blocking=True)
 
-    times, _, _ = timed_steps(step, steps, warmup, L.cold, stream)
-    return times, xh.numel() * 2 + rh.numel() * 2, oh.numel() * 2
+    try:
+        times, _, _ = timed_steps(step, steps, warmup, L.cold, stream)
+    finally:
+        L.x, L.res = x0, r0
+    return times, xrh.numel() * 2, oh.numel() * 2
 
 
 def cpu_baseline(L, W_host, budget_s=10.0):
