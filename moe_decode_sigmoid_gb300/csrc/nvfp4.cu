@@ -116,14 +116,16 @@ __device__ __forceinline__ void drain(const Pipe& p, int it) {
 // Otherwise each CTA first takes a static chunk of min(8, n / (2 x #SMs))
 // units and then claims the rest as it goes -- guided self-scheduling, as in
 // the BF16 gate/up kernel (SMs stream at different rates, so equal static
-// shares leave a tail): chunks of about remaining / (2 x #SMs) units (1..8)
-// from *claim, the first claim sent while the static chunk streams and the
-// next one claimed ahead while plenty remains.  Each chunk {first unit, units}
+// shares leave a tail): chunks of about remaining / (2 x #SMs) units (1..8,
+// in multiples of ALIGN) from *claim, the first claim sent while the static
+// chunk streams and the next one claimed ahead while plenty remains.  Each
+// chunk {first unit, units}
 // is published on its first stage in s_chunk, and a stage marked {-1, 0} ends
 // the list; the last CTA done claiming resets the counters for the next call.
 // Measured on GB300 (NVFP4 layer, chained): claimed gate/up units take skewed
-// batch 128 from 183 to 165 us and claimed down units to 168 us (both: 150),
-// but cost 3-7 us at 1-8 tokens, hence the per-kernel minimum.
+// batch 128 from 183 to 165 us and claimed down units to 168 us (both: 150;
+// 147 with gate/up chunks of whole reduction rounds), but cost 3-7 us at 1-8
+// tokens, hence the per-kernel minimum.
 __device__ __forceinline__ bool claims_used(int n, int min_per_cta) {
   return n >= min_per_cta * (int)gridDim.x;
 }
@@ -131,8 +133,10 @@ __device__ __forceinline__ int static_begin(int n, int c) {
   return (int)((long long)c * n / gridDim.x);
 }
 constexpr int GU_CLAIM_MIN = 32, DN_CLAIM_MIN = 8;  // units per CTA
+// gate/up chunks keep whole reduction rounds (4 units for groups of <= 8 tokens)
+constexpr int GU_CLAIM_ALIGN = 4;
 
-template <class Issue>
+template <int ALIGN, class Issue>
 __device__ __forceinline__ void produce_claimed(const Pipe& p, int n, int min_per_cta,
                                                 uint32_t* claim, uint32_t* done, int2* s_chunk,
                                                 Issue issue) {
@@ -155,11 +159,11 @@ __device__ __forceinline__ void produce_claimed(const Pipe& p, int n, int min_pe
     drain(p, it);
     return;
   }
-  auto size_for = [G](int rem) {
-    const int s = rem / (2 * G);
-    return s < 1 ? 1 : (s > 8 ? 8 : s);
+  auto size_for = [G](int rem) {  // a multiple of ALIGN in [ALIGN, 8]
+    const int s = (rem / (2 * G)) / ALIGN * ALIGN;
+    return s < ALIGN ? ALIGN : (s > 8 ? 8 : s);
   };
-  const int f = min(8, n / (2 * G));
+  const int f = min(8, n / (2 * G)) / ALIGN * ALIGN;
   const int base = G * f;  // claimed units start here
   int sz = size_for(n - base);
   int c0 = base + (int)atomicAdd(claim, (uint32_t)sz);
@@ -378,7 +382,7 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
 __device__ __forceinline__ void gu_produce(const Pipe& p, const GuMaps& maps, const int4* groups,
                                            int n, uint32_t* claim, uint32_t* done,
                                            int2* s_chunk) {
-  produce_claimed(p, n, GU_CLAIM_MIN, claim, done, s_chunk, [&](int u, int slot) {
+  produce_claimed<GU_CLAIM_ALIGN>(p, n, GU_CLAIM_MIN, claim, done, s_chunk, [&](int u, int slot) {
     const int4 grp = groups[u / f4::UNITS];
     const int blk = u & (f4::UNITS - 1);
     const bool routed = grp.x < E;
@@ -618,7 +622,7 @@ __device__ __forceinline__ void dn_unit(const ExpertArgs& a, const uint8_t* st, 
 
 __device__ __forceinline__ void dn_produce(const Pipe& p, const ExpertArgs& a, const int4* groups,
                                            int n, int2* s_chunk) {
-  produce_claimed(p, n, DN_CLAIM_MIN, &a.ws.hdr->dn_claim, &a.ws.hdr->dn_done, s_chunk,
+  produce_claimed<1>(p, n, DN_CLAIM_MIN, &a.ws.hdr->dn_claim, &a.ws.hdr->dn_done, s_chunk,
                   [&](int u, int slot) {
     const int4 grp = groups[u / f4::DN_UNITS];
     const int rb = u % f4::DN_UNITS;
