@@ -502,6 +502,27 @@ def test_calls_of_mixed_batches_on_one_workspace_match_fresh_workspaces(m, layer
         assert torch.equal(out_s.view(torch.int16), out_f.view(torch.int16)), (i, B)
 
 
+def test_claimed_units_reset_between_calls_of_both_formats(m, layer, nv_layer):
+    """The chained gate/up and down kernels hand out units from workspace
+    counters that the last CTA of each call resets: BF16 and NVFP4 calls of
+    claimed (32+ tokens) and equal-share batches in any order on one workspace
+    give exactly what fresh workspaces give."""
+    W, _ = layer
+    nv, _ = nv_layer
+    shared = m.new_workspace(64)
+    seq = [(40, "nvfp4"), (13, "bf16"), (64, "nvfp4"), (40, "bf16"), (8, "nvfp4"),
+           (64, "bf16"), (3, "nvfp4"), (40, "nvfp4")]
+    for i, (B, fmt) in enumerate(seq):
+        x, res = fs.tokens(4900 + i, B, device="cuda")
+        run = (lambda ws: run_decode(m, W, x, res, None, ws)) if fmt == "bf16" else \
+              (lambda ws: run_nvfp4(m, W, nv, x, res, None, ws))
+        out_s, idx_s, w_s = run(shared)
+        out_f, idx_f, w_f = run(m.new_workspace(B))
+        assert torch.equal(idx_s, idx_f), (i, B, fmt)
+        assert torch.equal(w_s, w_f), (i, B, fmt)
+        assert torch.equal(out_s.view(torch.int16), out_f.view(torch.int16)), (i, B, fmt)
+
+
 @pytest.mark.parametrize("B,fmt", [(1, "bf16"), (5, "bf16"), (8, "bf16"), (13, "bf16"),
                                    (64, "bf16"), (3, "nvfp4"), (40, "nvfp4"), (8, "route"),
                                    (128, "route")])
